@@ -1,0 +1,147 @@
+/*
+ * gist_attn.h -- C ABI of the GB300 (sm_103a) library for per-layer GQA
+ * attention of a short block of new tokens against a read-only cached KV
+ * segment.
+ *
+ * Sources, cited by page title and section:
+ *   [Gist page]   "把 item 压成 KV：gist 能不能用在相关性任务上" (liam.page, 2026-10-30)
+ *   [Suffix page] icman.com.cn news 64898 (suffix KV-cache reuse and attention-aware
+ *                 eviction), numbered sections 1-7
+ *   [KV page]     "为什么自回归推理缓存 KV，而不缓存历史 Q？" (mcfzz.com notes)
+ *
+ * The operation ([Gist page, "在线的一次 attention"]; [KV page, "Reusable-state"]):
+ * for every pair p (an (item, query) pair, or a sequence in decode), every
+ * query head h and every new token i,
+ *
+ *     out[p,i,h] = softmax( scale * R(q[p,i,h]) . [K_cached ; R(k_new[p,0..i,g])]^T )
+ *                  . [V_cached ; v_new[p,0..i,g]]
+ *
+ * with g = h / (Hq/Hkv) the KV head of h's group ([Gist page, "收益有多大：存储"]),
+ * R the rotate-half RoPE at position pos_offset[p] + i (new keys at their own
+ * positions), K_cached/V_cached the rows of p's cached blocks in table order,
+ * and nothing written back ([Gist page, "能不能再进一步"]: the cached blocks are
+ * read-only and the new tokens' K/V are not stored).
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller owns every buffer.  No entry point allocates
+ *     memory or keeps state between calls; calls are thread-safe.
+ *   - Asynchrony: work is enqueued on `stream` (0 = legacy default stream);
+ *     no entry point synchronises the host.
+ *   - Pointers are device pointers unless marked "host".  bf16 buffers must be
+ *     16-byte aligned, int32 buffers 4-byte aligned.
+ *   - Return codes are host-detected and mean nothing was launched:
+ *       GIST_ATTN_OK (0), or one of the negative GIST_ATTN_ERR_* codes.
+ *   - Device-detected problems are OR-ed into the optional device status word
+ *     (dims->status) as GIST_ATTN_STATUS_* bits; the kernel never reads out of
+ *     bounds because of them.
+ */
+#ifndef GIST_ATTN_H
+#define GIST_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host return codes. */
+#define GIST_ATTN_OK 0
+#define GIST_ATTN_ERR_NULL (-1)        /* a required pointer is NULL                    */
+#define GIST_ATTN_ERR_DIMS (-2)        /* inconsistent or out-of-range dimensions       */
+#define GIST_ATTN_ERR_UNSUPPORTED (-3) /* head_dim / group / sizes this build can't run */
+#define GIST_ATTN_ERR_ALIGN (-4)       /* a pointer is not aligned as required          */
+#define GIST_ATTN_ERR_LAUNCH (-5)      /* the CUDA launch itself failed                 */
+
+/* Device status bits (OR-ed into *dims->status). */
+#define GIST_ATTN_STATUS_BAD_BLOCK 1 /* a block id was outside [0, num_blocks): that
+                                        pair's output rows were written as zeros     */
+#define GIST_ATTN_STATUS_TIMEOUT 2   /* a bounded wait on an asynchronous copy gave up;
+                                        the affected outputs are unspecified          */
+
+typedef struct {
+  int32_t num_pairs;       /* P >= 0: pairs (or decode sequences) in this call          */
+  int32_t n_new;           /* l >= 1: new tokens per pair, EOS included                 */
+  int32_t num_q_heads;     /* Hq >= 1                                                    */
+  int32_t num_kv_heads;    /* Hkv >= 1, Hq % Hkv == 0; q head h reads KV head h/(Hq/Hkv) */
+  int32_t head_dim;        /* d: 64 or 128                                               */
+  int32_t block_len;       /* cached positions per pool block (k for a gist item,
+                              256 for the paged pool of [Suffix page, §5])               */
+  int32_t blocks_per_pair; /* cached blocks per pair: 1 (item gist), 2 (item + query
+                              gist, [Gist page, "能不能再进一步"]), T/256 (paged)          */
+  int32_t num_blocks;      /* pool extent; every block id must lie in [0, num_blocks)  */
+  int32_t num_layers;      /* L: layers held by the pool                                 */
+  int32_t layer;           /* the layer this call reads, 0 <= layer < L                  */
+  float rope_theta;        /* RoPE base (1e4 in the workloads), > 0                      */
+  float softmax_scale;     /* 0 selects 1/sqrt(d) ([KV page, "Reusable-state"])          */
+  int32_t* status;         /* optional device int32 status word (may be NULL)            */
+} gist_attn_dims;
+
+/*
+ * gist_attn_fwd -- one layer of attention for all pairs, one launch on `stream`.
+ * Defined by [Gist page, "在线的一次 attention"] (cat of cached and new K/V, new
+ * tokens numbered after the cached positions), [Gist page, "能不能再进一步"]
+ * (two read-only cached blocks, l = 1) and [KV page, "Reusable-state"] (the
+ * decode step, l = 1, over a paged cache read through a block table as in
+ * [Suffix page, §6 问题四]).
+ *
+ *   q          bf16 [P][l][Hq][d], pre-RoPE
+ *   k_new      bf16 [P][l][Hkv][d], pre-RoPE
+ *   v_new      bf16 [P][l][Hkv][d]
+ *   kv_pool    bf16 [num_blocks][L][2][Hkv][block_len][d]; index 0 of the "2"
+ *              axis is K (stored already rotated at the positions its producer
+ *              chose), 1 is V.  Read-only.
+ *   item_ids   int32 [P]: the one cached block of each pair (blocks_per_pair == 1),
+ *              or NULL
+ *   block_table int32 [P][blocks_per_pair]: cached blocks in key order, or NULL.
+ *              Exactly one of item_ids / block_table is non-NULL when the cached
+ *              segment is non-empty (blocks_per_pair * block_len > 0).
+ *   pos_offset int32 [P]: position of new token 0, or NULL for
+ *              blocks_per_pair * block_len (the query follows the cached
+ *              segment).  Only pos_offset minus the cached keys' positions
+ *              matters ([Gist page, "在线的一次 attention"], RoPE remark).
+ *   out        bf16 [P][l][Hq][d], written (fp32 accumulation, round to nearest even)
+ *   dims       host pointer to the dimensions above
+ * Returns GIST_ATTN_OK or a negative GIST_ATTN_ERR_* code (nothing launched).
+ * P == 0 launches nothing and returns GIST_ATTN_OK.
+ */
+int gist_attn_fwd(const void* q, const void* k_new, const void* v_new, const void* kv_pool,
+                  const int32_t* item_ids, const int32_t* block_table, const int32_t* pos_offset,
+                  void* out, const gist_attn_dims* dims, cudaStream_t stream);
+
+/*
+ * gist_attn_gather_debug -- copies, bit for bit, the cached rows each pair
+ * reads, through the same device gather routine the attention kernels use
+ * ([Gist page, "在线的一次 attention"]: cache[item].K[layer], .V[layer]).
+ *   dst  bf16 [P][Hkv][2][C][d], C = blocks_per_pair * block_len:
+ *        dst[p][g][kv][c] = kv_pool[block(p, c / block_len)][layer][kv][g][c % block_len]
+ * A pair with an out-of-range block id gets zero rows and sets
+ * GIST_ATTN_STATUS_BAD_BLOCK.  q/k_new/v_new are not read.
+ */
+int gist_attn_gather_debug(const void* kv_pool, const int32_t* item_ids,
+                           const int32_t* block_table, void* dst, const gist_attn_dims* dims,
+                           cudaStream_t stream);
+
+/*
+ * Cache byte counts, host only, no device work.
+ * [Gist page, "先看复用结构" / "收益有多大：存储"]: one position holds
+ * 2 * L * Hkv * d numbers of elem_bytes bytes each; a compressed item holds k
+ * positions ([Gist page, "在线的一次 attention"]).  [KV page, "Memory"]:
+ * M_KV = 2 * B * L * T * Hkv * d * elem_bytes.  Return 0 for a negative argument.
+ */
+size_t gist_kv_bytes_per_position(int L, int Hkv, int d, int elem_bytes);
+size_t gist_kv_bytes_per_item(int L, int Hkv, int d, int k, int elem_bytes);
+size_t gist_kv_bytes_batch(int B, int L, int T, int Hkv, int d, int elem_bytes);
+
+/*
+ * Text for a return code (negative) or a device status word (>= 0, bits OR-ed).
+ * The string is static; the caller must not free it.
+ */
+const char* gist_attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GIST_ATTN_H */
