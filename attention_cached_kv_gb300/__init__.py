@@ -1,0 +1,16 @@
+"""GB300 (sm_103a) library for attention of new tokens against a read-only
+cached KV segment: gist-compressed items gathered by id, or a paged cache read
+through a block table.
+
+The compute lives in ``_lib/libgistattn.so`` (C ABI in include/gist_attn.h);
+``binding`` marshals torch tensors into it; ``workloads`` draws seeded
+synthetic inputs.  The library is loaded on first use and every call fails
+loudly if it has not been built.
+"""
+from .binding import (GistAttnError, STATUS_BAD_BLOCK, STATUS_TIMEOUT, gist_attn_fwd,
+                      gist_attn_gather_debug, kv_bytes_batch, kv_bytes_per_item,
+                      kv_bytes_per_position, load_library, status_string)
+
+__all__ = ["GistAttnError", "STATUS_BAD_BLOCK", "STATUS_TIMEOUT", "gist_attn_fwd",
+           "gist_attn_gather_debug", "kv_bytes_batch", "kv_bytes_per_item",
+           "kv_bytes_per_position", "load_library", "status_string"]

@@ -1,0 +1,171 @@
+"""ctypes binding of libgistattn.so -- argument marshalling only.
+
+Every function here checks dtypes/devices of torch tensors, passes their raw
+pointers to the C ABI (include/gist_attn.h) and turns a negative return code
+into GistAttnError.  All computation runs in the library's CUDA kernels; there
+is no fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libgistattn.so")
+
+OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH = 0, -1, -2, -3, -4, -5
+STATUS_BAD_BLOCK, STATUS_TIMEOUT = 1, 2
+
+EXPORTS = ("gist_attn_fwd", "gist_attn_gather_debug", "gist_kv_bytes_per_position",
+           "gist_kv_bytes_per_item", "gist_kv_bytes_batch", "gist_attn_status_string")
+
+
+class GistAttnError(RuntimeError):
+    def __init__(self, code: int, text: str):
+        super().__init__(f"gist_attn error {code}: {text}")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    """Mirror of gist_attn_dims."""
+    _fields_ = [
+        ("num_pairs", ctypes.c_int32),
+        ("n_new", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("block_len", ctypes.c_int32),
+        ("blocks_per_pair", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("num_layers", ctypes.c_int32),
+        ("layer", ctypes.c_int32),
+        ("rope_theta", ctypes.c_float),
+        ("softmax_scale", ctypes.c_float),
+        ("status", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(p)
+            V = ctypes.c_void_p
+            lib.gist_attn_fwd.restype = ctypes.c_int
+            lib.gist_attn_fwd.argtypes = [V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
+            lib.gist_attn_gather_debug.restype = ctypes.c_int
+            lib.gist_attn_gather_debug.argtypes = [V, V, V, V, ctypes.POINTER(Dims), V]
+            lib.gist_kv_bytes_per_position.restype = ctypes.c_size_t
+            lib.gist_kv_bytes_per_position.argtypes = [ctypes.c_int] * 4
+            lib.gist_kv_bytes_per_item.restype = ctypes.c_size_t
+            lib.gist_kv_bytes_per_item.argtypes = [ctypes.c_int] * 5
+            lib.gist_kv_bytes_batch.restype = ctypes.c_size_t
+            lib.gist_kv_bytes_batch.argtypes = [ctypes.c_int] * 6
+            lib.gist_attn_status_string.restype = ctypes.c_char_p
+            lib.gist_attn_status_string.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load_library().gist_attn_status_string(int(code)).decode()
+
+
+def make_dims(d: dict, status: torch.Tensor | None = None) -> Dims:
+    out = Dims()
+    for name, _ in Dims._fields_:
+        if name == "status":
+            continue
+        setattr(out, name, d[name])
+    if status is not None:
+        _check(status, torch.int32, "status")
+        out.status = status.data_ptr()
+    return out
+
+
+def _check(t, dtype, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise TypeError(f"{name} must be contiguous")
+
+
+def _ptr(t, dtype, name):
+    if t is None:
+        return None
+    _check(t, dtype, name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _raise(rc):
+    if rc != OK:
+        raise GistAttnError(rc, status_string(rc))
+
+
+def gist_attn_fwd(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, pos_offset=None,
+                  out=None, *, dims: dict, status: torch.Tensor | None = None, stream=None):
+    """One layer of cached-KV attention; returns `out` (allocated if None)."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q)
+    bf, i32 = torch.bfloat16, torch.int32
+    D = make_dims(dims, status)
+    rc = lib.gist_attn_fwd(_ptr(q, bf, "q"), _ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"),
+                           _ptr(kv_pool, bf, "kv_pool"), _ptr(item_ids, i32, "item_ids"),
+                           _ptr(block_table, i32, "block_table"),
+                           _ptr(pos_offset, i32, "pos_offset"), _ptr(out, bf, "out"),
+                           ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return out
+
+
+def gist_attn_gather_debug(kv_pool, item_ids=None, block_table=None, dst=None, *, dims: dict,
+                           status: torch.Tensor | None = None, stream=None):
+    """Cached rows per pair, bit for bit: bf16 [P][Hkv][2][C][d]."""
+    lib = load_library()
+    C = dims["block_len"] * dims["blocks_per_pair"]
+    if dst is None:
+        dst = torch.empty((dims["num_pairs"], dims["num_kv_heads"], 2, C, dims["head_dim"]),
+                          dtype=torch.bfloat16, device=kv_pool.device)
+    D = make_dims(dims, status)
+    rc = lib.gist_attn_gather_debug(_ptr(kv_pool, torch.bfloat16, "kv_pool"),
+                                    _ptr(item_ids, torch.int32, "item_ids"),
+                                    _ptr(block_table, torch.int32, "block_table"),
+                                    _ptr(dst, torch.bfloat16, "dst"), ctypes.byref(D),
+                                    _stream(stream))
+    _raise(rc)
+    return dst
+
+
+def kv_bytes_per_position(L, Hkv, d, elem_bytes) -> int:
+    return int(load_library().gist_kv_bytes_per_position(L, Hkv, d, elem_bytes))
+
+
+def kv_bytes_per_item(L, Hkv, d, k, elem_bytes) -> int:
+    return int(load_library().gist_kv_bytes_per_item(L, Hkv, d, k, elem_bytes))
+
+
+def kv_bytes_batch(B, L, T, Hkv, d, elem_bytes) -> int:
+    return int(load_library().gist_kv_bytes_batch(B, L, T, Hkv, d, elem_bytes))

@@ -1,0 +1,172 @@
+// api.cu -- the C ABI declared in include/gist_attn.h: argument checks on the
+// host, kernel selection, and the cache byte-count helpers.
+//
+// Nothing here allocates device memory or keeps state between calls; the only
+// process-wide value is the driver's tensor-map encoder, looked up once.
+//
+// Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上";
+//        [KV page] "为什么自回归推理缓存 KV，而不缓存历史 Q？".
+#include <math.h>
+#include <stdint.h>
+
+#include "gist_attn.h"
+#include "kernels.h"
+
+namespace gattn {
+
+EncodeTiledFn encode_tiled_fn() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+namespace {
+
+constexpr int64_t kMaxKeys = 1 << 24;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Checks the dimensions and fills everything of `pb` except the tensor pointers.
+int check_dims(const gist_attn_dims* dm, Problem* pb) {
+  if (!dm) return GIST_ATTN_ERR_NULL;
+  const gist_attn_dims& d = *dm;
+  if (d.num_pairs < 0 || d.n_new < 1 || d.num_q_heads < 1 || d.num_kv_heads < 1 ||
+      d.num_q_heads % d.num_kv_heads != 0 || d.block_len < 0 || d.blocks_per_pair < 0 ||
+      d.num_layers < 1 || d.layer < 0 || d.layer >= d.num_layers || d.num_blocks < 0)
+    return GIST_ATTN_ERR_DIMS;
+  if (!(d.rope_theta > 0.f) || !isfinite(d.rope_theta) || !(d.softmax_scale >= 0.f) ||
+      !isfinite(d.softmax_scale))
+    return GIST_ATTN_ERR_DIMS;
+  const int64_t C = (int64_t)d.block_len * d.blocks_per_pair;
+  if (C + d.n_new > kMaxKeys) return GIST_ATTN_ERR_DIMS;
+  if (C > 0 && d.num_blocks < 1) return GIST_ATTN_ERR_DIMS;
+  if (d.head_dim != 64 && d.head_dim != 128) return GIST_ATTN_ERR_UNSUPPORTED;
+  if (d.num_q_heads / d.num_kv_heads > 256) return GIST_ATTN_ERR_UNSUPPORTED;
+  // element counts of the largest arrays must fit comfortably in 64 bits
+  const double elems = (double)d.num_pairs * d.n_new * d.num_q_heads * d.head_dim;
+  const double pool = (double)d.num_blocks * d.num_layers * 2 * d.num_kv_heads *
+                      (double)d.block_len * d.head_dim;
+  if (elems > 4e18 || pool > 4e18) return GIST_ATTN_ERR_DIMS;
+
+  pb->status = d.status;
+  pb->P = d.num_pairs;
+  pb->l = d.n_new;
+  pb->Hq = d.num_q_heads;
+  pb->Hkv = d.num_kv_heads;
+  pb->G = d.num_q_heads / d.num_kv_heads;
+  pb->d = d.head_dim;
+  pb->block_len = d.block_len;
+  pb->blocks_per_pair = d.blocks_per_pair;
+  pb->num_blocks = d.num_blocks;
+  pb->L = d.num_layers;
+  pb->layer = d.layer;
+  pb->C = (int)C;
+  const double scale = d.softmax_scale > 0.f ? (double)d.softmax_scale : 1.0 / sqrt((double)d.head_dim);
+  pb->scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
+  for (int j = 0; j < 64; ++j)
+    pb->inv_freq[j] = j < d.head_dim / 2
+                          ? (float)pow((double)d.rope_theta, -2.0 * j / (double)d.head_dim)
+                          : 0.f;
+  return GIST_ATTN_OK;
+}
+
+// The cached-segment arguments: pool and exactly one index array when C > 0.
+int check_cache_args(const Problem& pb, const void* kv_pool, const int32_t* item_ids,
+                     const int32_t* block_table) {
+  if (pb.C == 0) return GIST_ATTN_OK;
+  if (!kv_pool || (!item_ids && !block_table)) return GIST_ATTN_ERR_NULL;
+  if (item_ids && block_table) return GIST_ATTN_ERR_DIMS;
+  if (item_ids && pb.blocks_per_pair != 1) return GIST_ATTN_ERR_DIMS;
+  if (!aligned(kv_pool, 16) || !aligned(item_ids, 4) || !aligned(block_table, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  return GIST_ATTN_OK;
+}
+
+}  // namespace
+}  // namespace gattn
+
+using gattn::Problem;
+
+extern "C" int gist_attn_fwd(const void* q, const void* k_new, const void* v_new,
+                             const void* kv_pool, const int32_t* item_ids,
+                             const int32_t* block_table, const int32_t* pos_offset, void* out,
+                             const gist_attn_dims* dims, cudaStream_t stream) {
+  Problem pb{};
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (pb.P == 0) return GIST_ATTN_OK;
+  if (!q || !k_new || !v_new || !out) return GIST_ATTN_ERR_NULL;
+  rc = gattn::check_cache_args(pb, kv_pool, item_ids, block_table);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (!gattn::aligned(q, 16) || !gattn::aligned(k_new, 16) || !gattn::aligned(v_new, 16) ||
+      !gattn::aligned(out, 16) || !gattn::aligned(pos_offset, 4) ||
+      !gattn::aligned(pb.status, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  pb.q = q;
+  pb.k_new = k_new;
+  pb.v_new = v_new;
+  pb.kv_pool = pb.C > 0 ? kv_pool : nullptr;
+  pb.item_ids = pb.C > 0 ? item_ids : nullptr;
+  pb.block_table = pb.C > 0 ? block_table : nullptr;
+  pb.pos_offset = pos_offset;
+  pb.out = out;
+  if (pb.C == 0) pb.blocks_per_pair = 0;  // nothing cached: no ids to read
+  if (pb.l == 1 && gattn::decode_fits(pb)) return gattn::launch_decode(pb, stream);
+  if (gattn::prefill_fits(pb)) return gattn::launch_prefill(pb, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+extern "C" int gist_attn_gather_debug(const void* kv_pool, const int32_t* item_ids,
+                                      const int32_t* block_table, void* dst,
+                                      const gist_attn_dims* dims, cudaStream_t stream) {
+  Problem pb{};
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (pb.P == 0 || pb.C == 0) return GIST_ATTN_OK;
+  if (!dst) return GIST_ATTN_ERR_NULL;
+  rc = gattn::check_cache_args(pb, kv_pool, item_ids, block_table);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (!gattn::aligned(dst, 16) || !gattn::aligned(pb.status, 4)) return GIST_ATTN_ERR_ALIGN;
+  pb.kv_pool = kv_pool;
+  pb.item_ids = item_ids;
+  pb.block_table = block_table;
+  return gattn::launch_gather(pb, dst, stream);
+}
+
+extern "C" size_t gist_kv_bytes_per_position(int L, int Hkv, int d, int elem_bytes) {
+  if (L < 0 || Hkv < 0 || d < 0 || elem_bytes < 0) return 0;
+  return (size_t)2 * L * Hkv * d * elem_bytes;
+}
+
+extern "C" size_t gist_kv_bytes_per_item(int L, int Hkv, int d, int k, int elem_bytes) {
+  if (k < 0) return 0;
+  return (size_t)k * gist_kv_bytes_per_position(L, Hkv, d, elem_bytes);
+}
+
+extern "C" size_t gist_kv_bytes_batch(int B, int L, int T, int Hkv, int d, int elem_bytes) {
+  if (B < 0 || T < 0) return 0;
+  return (size_t)B * T * gist_kv_bytes_per_position(L, Hkv, d, elem_bytes);
+}
+
+extern "C" const char* gist_attn_status_string(int status) {
+  switch (status) {
+    case GIST_ATTN_OK: return "ok";
+    case GIST_ATTN_ERR_NULL: return "a required pointer is NULL";
+    case GIST_ATTN_ERR_DIMS: return "inconsistent or out-of-range dimensions";
+    case GIST_ATTN_ERR_UNSUPPORTED: return "unsupported head_dim, group size or problem size";
+    case GIST_ATTN_ERR_ALIGN: return "a pointer is not aligned as required";
+    case GIST_ATTN_ERR_LAUNCH: return "the CUDA launch failed";
+    case GIST_ATTN_STATUS_BAD_BLOCK: return "device: a block id was out of range (pair zeroed)";
+    case GIST_ATTN_STATUS_TIMEOUT: return "device: a bounded wait on an asynchronous copy gave up";
+    case GIST_ATTN_STATUS_BAD_BLOCK | GIST_ATTN_STATUS_TIMEOUT:
+      return "device: out-of-range block id and a timed-out wait";
+    default: return status < 0 ? "unknown error" : "unknown device status bits";
+  }
+}

@@ -1,0 +1,46 @@
+// kernels.h -- host-side launch interface between the C-ABI layer and the
+// kernel translation units.  Host code only; no device code here.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gist_attn.h"
+
+namespace gattn {
+
+// Everything a kernel needs, already validated by the C-ABI layer.
+struct Problem {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const void* kv_pool;
+  const int32_t* item_ids;
+  const int32_t* block_table;
+  const int32_t* pos_offset;
+  void* out;
+  int32_t* status;
+  int P, l, Hq, Hkv, G, d, block_len, blocks_per_pair, num_blocks, L, layer;
+  int C;             // cached keys per pair
+  float scale_log2;  // softmax scale * log2(e)
+  float inv_freq[64];  // rope_theta^(-2j/d), j < d/2
+};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// The driver's tensor-map encoder, fetched once through the runtime (no libcuda link).
+EncodeTiledFn encode_tiled_fn();
+
+// Each returns GIST_ATTN_OK or a negative GIST_ATTN_ERR_* code.
+int launch_prefill(const Problem& pb, cudaStream_t stream);
+int launch_decode(const Problem& pb, cudaStream_t stream);
+int launch_gather(const Problem& pb, void* dst, cudaStream_t stream);
+
+// Whether the prefill kernel can hold this problem's tiles in shared memory.
+bool prefill_fits(const Problem& pb);
+bool decode_fits(const Problem& pb);
+
+}  // namespace gattn

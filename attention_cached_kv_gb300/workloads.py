@@ -198,3 +198,37 @@ def make(spec: Spec | str, device="cpu", seed: int = 0, **overrides) -> Workload
     blocks = (block_table if block_table is not None else item_ids).reshape(-1).cpu().numpy()
     meta["unique_blocks"] = int(np.unique(blocks).shape[0])
     return Workload(spec, dims_of(spec), q, k_new, v_new, kv_pool, item_ids, block_table, None, meta)
+
+
+def make_custom(P: int, l: int, Hq: int, Hkv: int, d: int, block_len: int, blocks_per_pair: int,
+                num_blocks: int, num_layers: int = 1, layer: int = 0, device="cpu", seed: int = 0,
+                random_pos: bool = False, use_table: bool | None = None) -> Workload:
+    """Any shape, for edge cases: N(0,1) tensors, uniform block ids (a block
+    table unless there is exactly one block per pair and use_table is not set),
+    and optionally per-pair random positions in [0, 5000)."""
+    spec = Spec(f"custom_P{P}_l{l}_G{Hq // Hkv}_d{d}_C{block_len * blocks_per_pair}", num_layers,
+                Hq, Hkv, d, l, block_len, blocks_per_pair, pool_items=num_blocks,
+                num_pairs_override=P)
+    q = _randn((P, l, Hq, d), device, seed, STREAM_Q)
+    k_new = _randn((P, l, Hkv, d), device, seed, STREAM_K)
+    v_new = _randn((P, l, Hkv, d), device, seed, STREAM_V)
+    kv_pool = _randn((max(num_blocks, 1), num_layers, 2, Hkv, max(block_len, 1), d), device, seed,
+                     STREAM_POOL)
+    rng = np.random.default_rng(16 * seed + STREAM_IDS)
+    ids = rng.integers(0, max(num_blocks, 1), size=(P, blocks_per_pair)).astype(np.int32)
+    if use_table is None:
+        use_table = blocks_per_pair != 1
+    item_ids = block_table = None
+    if blocks_per_pair * block_len > 0:
+        if use_table:
+            block_table = torch.from_numpy(ids).to(device)
+        else:
+            item_ids = torch.from_numpy(ids[:, 0].copy()).to(device)
+    pos = None
+    if random_pos:
+        pos = torch.from_numpy(rng.integers(0, 5000, size=P).astype(np.int32)).to(device)
+    dims = dict(num_pairs=P, n_new=l, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
+                block_len=block_len, blocks_per_pair=blocks_per_pair, num_blocks=num_blocks,
+                num_layers=num_layers, layer=layer, rope_theta=1e4, softmax_scale=0.0)
+    return Workload(spec, dims, q, k_new, v_new, kv_pool, item_ids, block_table, pos,
+                    {"unique_blocks": int(np.unique(ids).shape[0])})

@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Throughput of cached-KV attention: (item, query) pairs per second per
+layer-attention, and the dominant kernel's achieved HBM bandwidth.
+
+A step is one pass of the hot path over one batch: every layer of the
+workload, one library launch per layer, each launch reading its layer's slice
+of the cached-KV pool.  Inputs (Q, K_new, V_new, ids) are resident in HBM
+before timing; they are larger than L2 (3.4 GB per launch for the gist
+workload), so each launch streams from DRAM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gist]
+  python bench.py --impl reference ...   # the fp64 oracle on the host cores
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (weak scaling, no collective on the data path); the
+reported time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "(item,query) pairs/s per layer-attention; achieved HBM GB/s vs GB300 peak"
+UNIT = "pairs/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["api.cu", "prefill.cu", "decode.cu", "common.cuh", "kernels.h"]
+
+DESCR = {
+    "gist": "gist relevance: 24 layers, Hq=14, Hkv=2, d=64, k=8, l=64; 256 queries x 50 "
+            "Zipf(1.1) candidates (12,800 pairs); pool 100k items (9.2 GiB bf16)",
+    "qgist": "query also gisted: 24 layers, Hq=14, Hkv=2, d=64, l=1 against 8 item-gist + 8 "
+             "query-gist positions; 500 queries x 50 Zipf(1.1) candidates (25,000 pairs)",
+    "wide": "wide-KV gist: 28 layers, Hq=32, Hkv=8, d=128, k=8, l=64; 128 queries x 50 uniform "
+            "candidates (6,400 pairs); pool 20k items",
+    "paged": "paged decode: 32 layers, Hq=Hkv=32, d=128, l=1, 4096 cached tokens in 16 blocks "
+             "of 256 behind permuted block tables; batch 32",
+    "tiny": "tiny: 1 layer, Hq=14, Hkv=2, d=64, k=8, l=64, 32 pairs, pool 16 items",
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gist", choices=sorted(DESCR))
+    ap.add_argument("--report", default=None, help="also write a detailed JSON report here")
+    ap.add_argument("--queries", type=int, default=0, help="smaller batch (profiling runs)")
+    ap.add_argument("--pool-items", type=int, default=0, help="smaller pool (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers ---
+
+def algorithmic_bytes_per_launch(wl) -> dict:
+    """Compulsory bytes of one launch: every pair's Q, K_new, V_new, O and ids
+    once, plus every distinct cached block of the layer once."""
+    d = wl.dims
+    P, l, Hq, Hkv, hd = d["num_pairs"], d["n_new"], d["num_q_heads"], d["num_kv_heads"], d["head_dim"]
+    per_pair = 2 * l * Hq * hd * 2 + 2 * l * Hkv * hd * 2 + 4 * d["blocks_per_pair"]
+    block = 2 * Hkv * d["block_len"] * hd * 2
+    uniq = wl.meta["unique_blocks"]
+    return {"per_pair": per_pair, "per_block": block, "unique_blocks": uniq,
+            "total": P * per_pair + uniq * block,
+            "total_per_pair_gather": P * (per_pair + d["blocks_per_pair"] * block)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "attention_cached_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel sources as they are now; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_sources_sha") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) of the SM clock and throttle reasons;
+    only samples stamped inside the timed window are summarised."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.window = [None, None]
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def begin(self):
+        self.window[0] = time.time()
+
+    def end(self):
+        self.window[1] = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        import datetime as _dt
+        rows = []
+        for line in out.strip().splitlines():
+            r = [x.strip() for x in line.split(",")]
+            if len(r) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            rows.append((ts, r))
+        t0, t1 = self.window
+        inside = [r for ts, r in rows if t0 is not None and t0 <= ts <= (t1 or ts)]
+        use = inside if inside else [r for _, r in rows]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[1]) for r in use) if v is not None]
+        mx = [v for v in (num(r[2]) for r in use) if v is not None]
+        reasons = sorted({name for r in use for name, val in zip(self.NAMES, r[5:9])
+                          if val.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside),
+                "note": None if inside else "no sample fell inside the timed window; all samples used"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(value: float, ws: int) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------- CPU baseline ---
+
+def oracle_rate(wl, layer: int, target_s: float) -> dict:
+    import numpy as np
+    import torch
+
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    P = wl.dims["num_pairs"]
+
+    def run(n):
+        sel = np.arange(n) * max(1, P // max(n, 1)) % P
+        idx = torch.from_numpy(sel).to(wl.q.device)
+        q = wl.q.index_select(0, idx).cpu()
+        kn = wl.k_new.index_select(0, idx).cpu()
+        vn = wl.v_new.index_select(0, idx).cpu()
+        dims = dict(wl.dims, num_pairs=n, num_layers=1, layer=0)
+        pool = ids = table = None
+        C = wl.dims["block_len"] * wl.dims["blocks_per_pair"]
+        if C > 0:
+            src = wl.block_table if wl.block_table is not None else wl.item_ids.view(-1, 1)
+            blocks = src.index_select(0, idx).cpu().numpy()
+            uniq, inv = np.unique(blocks, return_inverse=True)
+            inv = inv.reshape(blocks.shape).astype(np.int32)
+            pool = wl.kv_pool[:, layer].index_select(0, torch.from_numpy(uniq).to(wl.q.device).long())
+            pool = pool.unsqueeze(1).contiguous().cpu()
+            dims["num_blocks"] = len(uniq)
+            if wl.block_table is not None:
+                table = inv
+            else:
+                ids = inv[:, 0].copy()
+        t0 = time.perf_counter()
+        oracle.gist_attn(q, kn, vn, pool, item_ids=ids, block_table=table, dims=dims,
+                         num_threads=cores)
+        return time.perf_counter() - t0
+
+    n0 = min(P, max(cores, 8))
+    t0 = run(n0)
+    n = int(min(P, max(n0, n0 * target_s / max(t0, 1e-6))))
+    t = run(n)
+    return {"value": n / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {P} pairs of layer {layer}, all heads and tokens ({t:.1f} s)"}
+
+
+# -------------------------------------------------------------- our arm ---
+
+def run_ours(args) -> dict:
+    import torch
+
+    from attention_cached_kv_gb300 import binding, workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load_library()
+    over = {}
+    if args.queries:
+        over["queries"] = args.queries
+    if args.pool_items:
+        over["pool_items"] = args.pool_items
+    wl = workloads.make(args.workload, device=dev, **over)
+    L, P = wl.dims["num_layers"], wl.dims["num_pairs"]
+    stream = torch.cuda.Stream(device=dev)
+    out = torch.empty_like(wl.q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dims_by_layer = [binding.make_dims(dict(wl.dims, layer=li), status) for li in range(L)]
+    lib = binding.load_library()
+    import ctypes
+    V = ctypes.c_void_p
+    ptrs = [V(t.data_ptr()) if t is not None else None for t in
+            (wl.q, wl.k_new, wl.v_new, wl.kv_pool, wl.item_ids, wl.block_table, wl.pos_offset, out)]
+    sh = V(stream.cuda_stream)
+
+    def launch(li):
+        rc = lib.gist_attn_fwd(*ptrs, ctypes.byref(dims_by_layer[li]), sh)
+        if rc != 0:
+            raise binding.GistAttnError(rc, binding.status_string(rc))
+
+    def step(ev=None):
+        for li in range(L):
+            if ev is not None:
+                ev[li][0].record(stream)
+            launch(li)
+            if ev is not None:
+                ev[li][1].record(stream)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}: {binding.status_string(int(status.item()))}")
+
+    K = args.steps
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid if rank == 0 else None) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.begin()
+    start.record(stream)
+    for k in range(K):
+        step(events[k])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.end()
+    barrier(ws)
+    clk = clocks.stop() if clocks else None
+    elapsed_ms = start.elapsed_time(end)
+    launch_ms = [events[k][li][0].elapsed_time(events[k][li][1]) for k in range(K) for li in range(L)]
+    elapsed_ms = max_over_ranks(elapsed_ms, ws)
+    avg_launch_ms = max_over_ranks(sum(launch_ms) / len(launch_ms), ws)
+
+    bytes_info = algorithmic_bytes_per_launch(wl)
+    peak, peak_src = measured_peaks()
+    achieved = bytes_info["total"] / (avg_launch_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    value = P * L * K * ws / (elapsed_ms * 1e-3)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16; ids per the workload recipe)",
+        "config": {"workload": DESCR[args.workload], "pairs": P, "layers_per_step": L,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (no flush needed)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": bytes_info["total"],
+                     "avg_launch_ms": avg_launch_ms},
+        "gpu_launches": K * L,
+        "clocks": clk,
+        "impl": "ours",
+    }
+
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, wl, lib, ptrs, dims_by_layer, stream, ws)
+    if not args.no_cpu_baseline and rank == 0 and ws == 1:
+        res["cpu_baseline"] = oracle_rate(wl, 0, args.cpu_seconds)
+    return res
+
+
+def run_e2e(args, wl, lib, ptrs, dims_by_layer, stream, ws) -> dict:
+    """Same metric through the C ABI with inputs in pinned host memory: every
+    layer copies that layer's Q/K_new/V_new (and ids) host -> device, runs the
+    kernel, and copies the output back."""
+    import ctypes
+
+    import torch
+
+    L, P = wl.dims["num_layers"], wl.dims["num_pairs"]
+    ids = wl.item_ids if wl.item_ids is not None else wl.block_table
+    host = {n: t.cpu().pin_memory() for n, t in (("q", wl.q), ("k", wl.k_new), ("v", wl.v_new), ("ids", ids))}
+    host_out = torch.empty(wl.q.shape, dtype=wl.q.dtype, pin_memory=True)
+    dev_out = torch.empty_like(wl.q)
+    out_ptr = ctypes.c_void_p(dev_out.data_ptr())
+    p = list(ptrs)
+    p[7] = out_ptr
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def step():
+        with torch.cuda.stream(stream):
+            for li in range(L):
+                wl.q.copy_(host["q"], non_blocking=True)
+                wl.k_new.copy_(host["k"], non_blocking=True)
+                wl.v_new.copy_(host["v"], non_blocking=True)
+                ids.copy_(host["ids"], non_blocking=True)
+                rc = lib.gist_attn_fwd(*p, ctypes.byref(dims_by_layer[li]), sh)
+                if rc != 0:
+                    raise RuntimeError(f"gist_attn_fwd returned {rc}")
+                host_out.copy_(dev_out, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 5))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    start.record(stream)
+    for _ in range(K):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end), ws)
+    return {"value": P * L * K * ws / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d * L,
+            "d2h_bytes_per_step": d2h * L, "steps": K}
+
+
+# -------------------------------------------------------- reference arm ---
+
+def run_reference(args) -> dict | None:
+    """The fp64 oracle on the host cores, each step a bounded sample of the
+    workload (a fresh seeded slice of pairs with its own cached blocks)."""
+    import oracle
+    from attention_cached_kv_gb300 import workloads
+
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    spec = workloads.SPECS[args.workload]
+    cores = len(os.sched_getaffinity(0))
+    # size one step to a few seconds of host time: calibrate on a small slice
+    def slice_of(n, seed):
+        return workloads.make_custom(n, spec.n_new, spec.num_q_heads, spec.num_kv_heads,
+                                     spec.head_dim, spec.block_len, spec.blocks_per_pair, n,
+                                     device="cpu", seed=seed)
+
+    def one(wl):
+        t0 = time.perf_counter()
+        oracle.gist_attn(wl.q, wl.k_new, wl.v_new, wl.kv_pool, item_ids=wl.item_ids,
+                         block_table=wl.block_table, dims=wl.dims, num_threads=cores)
+        return time.perf_counter() - t0
+
+    n0 = max(cores, 4)
+    t0 = one(slice_of(n0, 100))
+    budget_s = 150.0 / max(args.steps + args.warmup, 1)
+    n = int(max(n0, min(spec.num_pairs, n0 * min(budget_s, 5.0) / max(t0, 1e-6))))
+    for w in range(args.warmup):
+        one(slice_of(n, 200 + w))
+    times = [one(slice_of(n, 300 + k)) for k in range(args.steps)]
+    total = sum(times)
+    value = n * args.steps / total
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "pairs_per_step": n, "layers_per_step": 1},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} pairs of one layer per step (of {spec.num_pairs})"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    ws, rank, _ = dist_env()
+    if res is not None and rank == 0:
+        line = json.dumps(res)
+        print(line, flush=True)
+        if args.report:
+            with open(args.report, "a") as f:
+                f.write(line + "\n")
+    if ws > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,108 @@
+"""The C-ABI library without a GPU: it loads, exports every function the header
+declares, rejects bad arguments on the host (nothing reaches CUDA), and its
+byte-count helpers give the figures the pages print."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_cached_kv_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load_library()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "gist_attn.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(gist_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    assert set(binding.EXPORTS) == set(names), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_byte_helpers_match_page_figures(lib, golden):
+    for row in golden["bytes_per_position"]:
+        assert binding.kv_bytes_per_position(row["L"], row["Hkv"], row["d"], row["b"]) == row["bytes"]
+    for row in golden["bytes_per_item"]:
+        assert binding.kv_bytes_per_item(row["L"], row["Hkv"], row["d"], row["k"], row["b"]) == row["bytes"]
+    for row in golden["request_kv"]:
+        got = binding.kv_bytes_batch(row["B"], row["L"], row["S"], 32, row["H"] // 32, row["b"])
+        assert got / 2 ** 30 == row["printed_GB"]
+    assert binding.kv_bytes_per_position(-1, 2, 64, 2) == 0
+
+
+BASE = dict(num_pairs=4, n_new=8, num_q_heads=14, num_kv_heads=2, head_dim=64, block_len=8,
+            blocks_per_pair=1, num_blocks=16, num_layers=2, layer=1, rope_theta=1e4,
+            softmax_scale=0.0)
+P16 = 0x10000  # fake, 16-byte aligned device addresses: never dereferenced on a failing call
+
+
+def call(lib, dims=BASE, q=P16, k=P16, v=P16, pool=P16, ids=P16, table=None, pos=None, out=P16,
+         null_dims=False):
+    D = None if null_dims else ctypes.byref(binding.make_dims(dims))
+    V = ctypes.c_void_p
+    return lib.gist_attn_fwd(V(q) if q else None, V(k) if k else None, V(v) if v else None,
+                             V(pool) if pool else None, V(ids) if ids else None,
+                             V(table) if table else None, V(pos) if pos else None,
+                             V(out) if out else None, D, None)
+
+
+@pytest.mark.parametrize("case,code", [
+    (dict(null_dims=True), binding.ERR_NULL),
+    (dict(q=0), binding.ERR_NULL),
+    (dict(out=0), binding.ERR_NULL),
+    (dict(pool=0), binding.ERR_NULL),
+    (dict(ids=0), binding.ERR_NULL),
+    (dict(table=P16), binding.ERR_DIMS),                       # both index arrays
+    (dict(dims=dict(BASE, blocks_per_pair=2)), binding.ERR_DIMS),  # item ids need one block
+    (dict(dims=dict(BASE, n_new=0)), binding.ERR_DIMS),
+    (dict(dims=dict(BASE, num_kv_heads=3)), binding.ERR_DIMS),
+    (dict(dims=dict(BASE, layer=2)), binding.ERR_DIMS),
+    (dict(dims=dict(BASE, num_pairs=-1)), binding.ERR_DIMS),
+    (dict(dims=dict(BASE, num_blocks=0)), binding.ERR_DIMS),
+    (dict(dims=dict(BASE, rope_theta=0.0)), binding.ERR_DIMS),
+    (dict(dims=dict(BASE, softmax_scale=-1.0)), binding.ERR_DIMS),
+    (dict(dims=dict(BASE, softmax_scale=float("nan"))), binding.ERR_DIMS),
+    (dict(dims=dict(BASE, head_dim=96)), binding.ERR_UNSUPPORTED),
+    (dict(dims=dict(BASE, num_q_heads=600, num_kv_heads=2)), binding.ERR_UNSUPPORTED),
+    (dict(q=P16 + 2), binding.ERR_ALIGN),
+    (dict(out=P16 + 8), binding.ERR_ALIGN),
+    (dict(pool=P16 + 4), binding.ERR_ALIGN),
+    (dict(ids=P16 + 2), binding.ERR_ALIGN),
+    (dict(pos=P16 + 1), binding.ERR_ALIGN),
+])
+def test_host_rejects_bad_arguments(lib, case, code):
+    assert call(lib, **case) == code
+
+
+def test_empty_batch_launches_nothing(lib):
+    assert call(lib, dims=dict(BASE, num_pairs=0), q=0, k=0, v=0, out=0) == binding.OK
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, 1, 2, 3):
+        assert binding.status_string(code)
+    assert "block" in binding.status_string(binding.STATUS_BAD_BLOCK)
+
+
+def test_gather_debug_rejects_bad_arguments(lib):
+    V = ctypes.c_void_p
+    D = ctypes.byref(binding.make_dims(BASE))
+    assert lib.gist_attn_gather_debug(V(P16), V(P16), None, None, D, None) == binding.ERR_NULL
+    assert lib.gist_attn_gather_debug(V(P16), V(P16), None, V(P16 + 2), D, None) == binding.ERR_ALIGN
+    assert lib.gist_attn_gather_debug(V(P16), None, None, V(P16), D, None) == binding.ERR_NULL
