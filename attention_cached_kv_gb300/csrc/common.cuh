@@ -61,10 +61,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(200000u)  // may sleep up to 0.2 ms per try
       : "memory");
   return done != 0;
 }
@@ -76,6 +76,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
   return true;
+}
+
+// Plain arrive (count 1) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Named barrier 1 among the first `n` threads (a warp-multiple) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Same, returning whether any participant passed `pred` = true.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
 }
 
 // ------------------------------------------------------------------ TMA ---
@@ -124,6 +146,11 @@ __device__ __forceinline__ void cp_async_commit() {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// Waits until at most `n` of this thread's most recent cp.async groups are pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
 
 __device__ __forceinline__ uint4 ldg16(const void* p) {
   uint4 v;
@@ -170,6 +197,71 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
 __device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ------------------------------------------------- packed fp32 pairs ---
+// Two fp32 values in one 64-bit register; sm_100+ executes f32x2 add/mul/fma
+// as one instruction.
+__device__ __forceinline__ uint64_t f2_make(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// bf16 pair (low half = first element) -> fp32 pair
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t v) {
+  return f2_make(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+// fp32 pair -> bf16 pair, round to nearest even
+__device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) {
+  float a, b;
+  f2_split(v, a, b);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+// Splits an fp32 pair x into hi + lo with hi = x truncated to bf16 (exact in
+// fp32, returned packed) and lo = bf16(x - hi): hi + lo carries x to ~16 bits.
+__device__ __forceinline__ void f2_split_bf16(uint64_t x, uint32_t& hi_bf, uint32_t& lo_bf) {
+  float a, b;
+  f2_split(x, a, b);
+  const uint32_t ua = __float_as_uint(a) & 0xffff0000u, ub = __float_as_uint(b) & 0xffff0000u;
+  hi_bf = __byte_perm(ua, ub, 0x7632);
+  lo_bf = f2_to_bf16x2(f2_sub(x, f2_make(__uint_as_float(ua), __uint_as_float(ub))));
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
 }
 
 // ----------------------------------------------------------- the gather ---

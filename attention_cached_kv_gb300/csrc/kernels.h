@@ -36,11 +36,13 @@ EncodeTiledFn encode_tiled_fn();
 
 // Each returns GIST_ATTN_OK or a negative GIST_ATTN_ERR_* code.
 int launch_prefill(const Problem& pb, cudaStream_t stream);
+int launch_prefill_tc(const Problem& pb, cudaStream_t stream);
 int launch_decode(const Problem& pb, cudaStream_t stream);
 int launch_gather(const Problem& pb, void* dst, cudaStream_t stream);
 
 // Whether the prefill kernel can hold this problem's tiles in shared memory.
 bool prefill_fits(const Problem& pb);
+bool prefill_tc_fits(const Problem& pb);
 bool decode_fits(const Problem& pb);
 
 }  // namespace gattn

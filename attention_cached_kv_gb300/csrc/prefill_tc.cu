@@ -1,0 +1,645 @@
+// prefill_tc.cu -- attention of l >= 2 new tokens against a short cached
+// segment on the 5th-generation tensor core (tcgen05, TMEM accumulators).
+//
+// [Gist page, "在线的一次 attention"]: per pair and layer, K = cat(G_item, K_new),
+// V = cat(G_item, V_new), queries numbered after the cached positions, causal
+// inside the new block, nothing written back.  [Gist page, "收益有多大：存储"]:
+// the Hq/Hkv query heads of a group share one KV head, so a unit of work is
+// (pair, KV head) and its rows are (token, head-in-group), token-major, which is
+// the memory order of q/out.  [Gist page, "收益有多大：算力"]: only the logits,
+// the softmax and softmax x V depend on the KV length; they are this kernel.
+//
+// Persistent CTAs (two per SM when TMEM and shared memory allow), warp-specialised:
+//   * warp 8 (control): TMA loads of 128-row Q tiles into a 3-stage ring,
+//     tcgen05.mma issue (S = Q K^T, O = P V), TMA stores of O;
+//   * warps 0-7 (compute): two threads per tile row (TMEM lane = row; the
+//     halves split the columns).  They stage each unit's K/V (cached rows
+//     through the pool gather, new rows raw, by 16-byte cp.async two units
+//     ahead), rotate the new keys, rotate q (split into bf16 hi + lo so the
+//     rounding of rotated q does not reach the logits: hi goes to the stage,
+//     lo to TMEM for a second MMA pass), run the softmax out of TMEM (P back
+//     into TMEM as bf16), and normalise O into the stage for the store.
+// Hand-offs use mbarriers; the compute warps are software-pipelined so that the
+// rotation of tile i+1 runs while O(i) = P V is on the tensor core and the
+// normalisation of tile i runs while S(i+1) is.  One pass covers a tile's
+// whole key range (keys <= 128), so the softmax needs no running rescale.
+//
+// Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace gattn {
+namespace {
+
+constexpr int kCompute = 256;            // 8 compute warps
+constexpr int kThreads = kCompute + 32;  // + the control warp
+constexpr int kStages = 3;
+constexpr int kMaxKeys = 128;
+constexpr int kMaxSmem = 227 * 1024;
+constexpr int kMaxBlocksPerPair = 64;
+constexpr uint32_t kBarCompute = 1;  // named barrier of the compute warps
+
+struct TcParams {
+  const bf16* k_new;
+  const bf16* v_new;
+  PoolView pv;
+  const int32_t* pos_offset;
+  int32_t* status;
+  int l, Hkv, G, C;
+  int Tm;         // tokens per M-tile
+  int n_mt;       // M-tiles per unit
+  int num_units;  // P * Hkv
+  int kv_rows;    // rows of one K (or V) panel
+  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_ids, off_red, off_bar;
+  uint32_t p_col, o_col, lo_col, tmem_cols;  // TMEM plan: S at column 0
+  float scale_log2;
+  float inv_freq[64];
+};
+
+struct Layout {
+  int Tm, n_mt, kv_rows;
+  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_ids, off_red, off_bar, bytes;
+  uint32_t p_col, o_col, lo_col, tmem_cols;
+};
+
+Layout plan(const Problem& pb) {
+  Layout L{};
+  const int np = pb.d / 64;
+  L.Tm = 128 / pb.G;
+  L.n_mt = (pb.l + L.Tm - 1) / L.Tm;
+  L.kv_rows = (pb.C + pb.l + 15) / 16 * 16;  // also the widest S of any tile
+  L.stage_bytes = (uint32_t)np * 128 * 128;
+  uint32_t off = kStages * L.stage_bytes;
+  L.off_kv = off;
+  L.kv_buf_bytes = 2u * np * L.kv_rows * 128;  // K panels then V panels
+  off += 2 * L.kv_buf_bytes;
+  L.off_tab = off;
+  // per token: (cos, cos, sin, sin) of frequency pairs, 16 B each, +16 B so that
+  // consecutive tokens start on different banks
+  L.tab_stride = (uint32_t)(pb.d / 4) * 16 + 16;
+  off += (uint32_t)pb.l * L.tab_stride;
+  L.off_ids = off;
+  off += 2u * kMaxBlocksPerPair * 4;
+  L.off_red = off;
+  off += 2u * 2 * 128 * 4;  // partial row max and row sum of each half
+  L.off_bar = off;
+  off += 128;
+  L.bytes = off + 1024;
+  // TMEM: S [0, N) fp32, P [N, 1.5N) bf16 pairs, O [o, o+d), q lo [o+d, o+1.5d)
+  L.p_col = (uint32_t)L.kv_rows;
+  L.o_col = (uint32_t)((L.kv_rows * 3 / 2 + 15) / 16 * 16);
+  L.lo_col = L.o_col + pb.d;
+  const uint32_t need = L.lo_col + pb.d / 2;
+  L.tmem_cols = need <= 256 ? 256 : 512;
+  return L;
+}
+
+// Rotate one 16-byte chunk of x (elements j0..j0+7) against its partner chunk y
+// (elements j0+d/2..): (x, y) <- (x cos - y sin, y cos + x sin), fp32 pairs.
+// The table row holds (cos_j, cos_j+1, sin_j, sin_j+1) per frequency pair.
+__device__ __forceinline__ void rope_chunk(const uint4& x, const uint4& y, const uint8_t* trow,
+                                           int j0, uint64_t (&xr)[4], uint64_t (&yr)[4]) {
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint4 cs = *reinterpret_cast<const uint4*>(trow + ((j0 >> 1) + e) * 16);
+    const uint64_t c = f2_make(__uint_as_float(cs.x), __uint_as_float(cs.y));
+    const uint64_t sn = f2_make(__uint_as_float(cs.z), __uint_as_float(cs.w));
+    const uint64_t xf = bf16x2_to_f2(xw[e]), yf = bf16x2_to_f2(yw[e]);
+    xr[e] = f2_sub(f2_mul(xf, c), f2_mul(yf, sn));
+    yr[e] = f2_fma(yf, c, f2_mul(xf, sn));
+  }
+}
+
+struct Bars {
+  uint64_t qfull[kStages];
+  uint64_t rope_done;  // compute -> control: q tile rotated (hi in the stage, lo in TMEM)
+  uint64_t s_done;     // tensor core -> compute: S ready
+  uint64_t p_done;     // compute -> control: P ready
+  uint64_t o_done;     // tensor core -> compute: O ready
+  uint64_t o_stored;   // compute -> control: O written into the stage
+  uint32_t tmem_slot;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_o,
+                      const __grid_constant__ TcParams prm) {
+  constexpr int NP = D / 64;   // 64-column panels
+  constexpr int CPR = D / 8;   // 16-byte chunks per row
+  constexpr int HALF = D / 2;
+  constexpr float kNegInf = -INFINITY;
+  constexpr uint32_t kPanel = 128 * 128;  // one 128-row Q panel
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  Bars* bars = reinterpret_cast<Bars*>(smem + prm.off_bar);
+  int32_t* ids = reinterpret_cast<int32_t*>(smem + prm.off_ids);
+  float* red_max = reinterpret_cast<float*>(smem + prm.off_red);  // [2][128]
+  float* red_sum = red_max + 256;                                  // [2][128]
+  const uint8_t* tab = smem + prm.off_tab;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = prm.G, C = prm.C, l = prm.l, Tm = prm.Tm, n_mt = prm.n_mt;
+  const uint32_t kv_panel = (uint32_t)prm.kv_rows * 128;
+  const int my_units = blockIdx.x < prm.num_units
+                           ? (prm.num_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
+                           : 0;
+  const int my_tiles = my_units * n_mt;
+  auto unit_of = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
+
+  // ---- set-up (all threads)
+  if (warp == 8) {
+    tc::tmem_alloc(smem_u32(&bars->tmem_slot), prm.tmem_cols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars->qfull[s], 1);
+    mbar_init(&bars->rope_done, kCompute);
+    mbar_init(&bars->s_done, 1);
+    mbar_init(&bars->p_done, kCompute);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_stored, kCompute);
+    fence_mbar_init();
+  }
+  {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    const int pad = prm.kv_rows - (C + l);  // key rows no copy writes
+    for (int idx = tid; idx < 2 * 2 * NP * pad * 8; idx += kThreads) {
+      const int c = idx & 7, rr = (idx >> 3) % pad, rest = (idx >> 3) / pad;  // buf, kv, panel
+      const uint32_t base = sbase + prm.off_kv + (rest / (2 * NP)) * prm.kv_buf_bytes +
+                            ((rest / NP) & 1) * NP * kv_panel + (rest % NP) * kv_panel;
+      sts16(base + swz128(C + l + rr, c), z);
+    }
+    const int qpad = 128 - Tm * G;  // rows of each Q stage that no TMA box reaches
+    for (int idx = tid; idx < kStages * NP * qpad * 8; idx += kThreads) {
+      const int c = idx & 7, rr = (idx >> 3) % qpad, sp = (idx >> 3) / qpad;
+      sts16(sbase + (sp / NP) * prm.stage_bytes + (sp % NP) * kPanel + swz128(Tm * G + rr, c), z);
+    }
+  }
+  auto build_table = [&](int pos_base, int nthreads) {
+    for (int idx = tid; idx < l * (HALF / 2); idx += nthreads) {
+      const int t = idx / (HALF / 2), jp = idx - t * (HALF / 2);
+      float s0, c0, s1, c1;
+      sincosf((float)(pos_base + t) * prm.inv_freq[2 * jp], &s0, &c0);
+      sincosf((float)(pos_base + t) * prm.inv_freq[2 * jp + 1], &s1, &c1);
+      *reinterpret_cast<float4*>(smem + prm.off_tab + t * prm.tab_stride + jp * 16) =
+          make_float4(c0, c1, s0, s1);
+    }
+  };
+  if (!prm.pos_offset) build_table(C, kThreads);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == 8) {
+    // ================================================================ control
+    // All 32 lanes walk the loop (waits are uniform); lane 0 issues.
+    bool failed = false;
+    auto load_tile = [&](int i) {
+      if (i >= my_tiles) return;
+      const int u = unit_of(i / n_mt), mt = i % n_mt, s = i % kStages;
+      const int p = u / prm.Hkv, g = u % prm.Hkv;
+      mbar_arrive_expect_tx(&bars->qfull[s], (uint32_t)NP * Tm * G * 128);
+#pragma unroll
+      for (int pn = 0; pn < NP; ++pn)
+        tma_load_5d(sbase + s * prm.stage_bytes + pn * kPanel, &tm_q, &bars->qfull[s], 0, pn,
+                    g * G, mt * Tm, p);
+    };
+    auto store_tile = [&](int i) {
+      const int u = unit_of(i / n_mt), mt = i % n_mt, s = i % kStages;
+      const int p = u / prm.Hkv, g = u % prm.Hkv;
+#pragma unroll
+      for (int pn = 0; pn < NP; ++pn)
+        tma_store_5d(&tm_o, sbase + s * prm.stage_bytes + pn * kPanel, 0, pn, g * G, mt * Tm, p);
+      bulk_commit();
+    };
+    if (lane == 0 && my_tiles > 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_o);
+      for (int i = 0; i < kStages; ++i) load_tile(i);
+    }
+    for (int i = 0; i < my_tiles; ++i) {
+      const uint32_t par = (uint32_t)i & 1u;
+      const int k = i / n_mt, mt = i % n_mt;
+      const uint32_t stage = sbase + (i % kStages) * prm.stage_bytes;
+      const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
+      const uint32_t vb = kb + NP * kv_panel;
+      const int N = (C + min(l, (mt + 1) * Tm) + 15) & ~15;
+      // ---- S = (q_hi + q_lo) K^T
+      if (__any_sync(0xffffffffu, !mbar_wait(&bars->rope_done, par))) { failed = true; break; }
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t idesc = tc::idesc_bf16_f32(128, N, 0);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (uint32_t)(ks & 3) * 32;  // 16 columns = 32 bytes
+          const uint64_t a = tc::smem_desc_sw128(stage + (ks >> 2) * kPanel + koff, 16, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(kb + (ks >> 2) * kv_panel + koff, 16, 1024);
+          tc::mma_ss(tmem, a, bd, idesc, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (uint32_t)(ks & 3) * 32;
+          const uint64_t bd = tc::smem_desc_sw128(kb + (ks >> 2) * kv_panel + koff, 16, 1024);
+          tc::mma_ts(tmem, tmem + prm.lo_col + ks * 8, bd, idesc, 1);
+        }
+        tc::commit(smem_u32(&bars->s_done));
+      }
+      __syncwarp();
+      // ---- the previous tile's output leaves; its stage is refilled kStages tiles on
+      if (i > 0) {
+        if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored, par ^ 1u))) { failed = true; break; }
+        if (lane == 0) {
+          store_tile(i - 1);
+          bulk_wait_read_all();
+          load_tile(i - 1 + kStages);
+        }
+        __syncwarp();
+      }
+      // ---- O = P V (A = P from TMEM, B = V with d contiguous)
+      if (__any_sync(0xffffffffu, !mbar_wait(&bars->p_done, par))) { failed = true; break; }
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t idesc = tc::idesc_bf16_f32(128, D, 1);
+        for (int ks = 0; ks < N / 16; ++ks) {
+          const uint64_t bd = tc::smem_desc_sw128(vb + ks * 2048, kv_panel, 1024);
+          tc::mma_ts(tmem + prm.o_col, tmem + prm.p_col + ks * 8, bd, idesc, ks > 0);
+        }
+        tc::commit(smem_u32(&bars->o_done));
+      }
+      __syncwarp();
+    }
+    if (!failed && my_tiles > 0) {
+      if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored, (uint32_t)(my_tiles - 1) & 1u)))
+        failed = true;
+      else if (lane == 0)
+        store_tile(my_tiles - 1);
+    }
+    if (lane == 0) {
+      bulk_wait_read_all();
+      if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ compute
+    const int h = warp >> 2;               // which half of the row's columns
+    const int r = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    auto chunk_addr = [](uint32_t base, uint32_t pstride, int row, int J) {
+      return base + (J >> 3) * pstride + swz128(row, J & 7);
+    };
+    // cp.async of unit u's K/V rows (cached, then new ones raw) into buffer b;
+    // true if one of its block ids is out of range (nothing is copied then).
+    auto stage_kv = [&](int u, int b) -> bool {
+      const int p = u / prm.Hkv, g = u % prm.Hkv;
+      int32_t* bid = ids + b * kMaxBlocksPerPair;
+      bool bad = false;
+      for (int i = tid; i < prm.pv.blocks_per_pair; i += kCompute) {
+        const int32_t blk = pool_block_id(prm.pv, p, i);
+        bad |= !pool_block_ok(prm.pv, blk);
+        bid[i] = blk;
+      }
+      bad = named_bar_or(kBarCompute, kCompute, bad);
+      if (!bad) {
+        const uint32_t kb = sbase + prm.off_kv + b * prm.kv_buf_bytes;
+        const uint32_t vb = kb + NP * kv_panel;
+        const int bl = prm.pv.block_len;
+        for (int idx = tid; idx < 2 * C * CPR; idx += kCompute) {
+          const int kv = idx >= C * CPR;
+          const int rr = idx - kv * C * CPR;
+          const int kappa = rr / CPR, c = rr - kappa * CPR;
+          const int bi = kappa / bl;
+          const bf16* src = pool_row(prm.pv, bid[bi], g, kv, kappa - bi * bl) + c * 8;
+          cp_async16((kv ? vb : kb) + (c >> 3) * kv_panel + swz128(kappa, c & 7), src);
+        }
+        for (int idx = tid; idx < 2 * l * CPR; idx += kCompute) {
+          const int kv = idx >= l * CPR;
+          const int rr = idx - kv * l * CPR;
+          const int t = rr / CPR, c = rr - t * CPR;
+          const bf16* src =
+              (kv ? prm.v_new : prm.k_new) + (((int64_t)p * l + t) * prm.Hkv + g) * D + c * 8;
+          cp_async16((kv ? vb : kb) + (c >> 3) * kv_panel + swz128(C + t, c & 7), src);
+        }
+      }
+      cp_async_commit();
+      return bad;
+    };
+    // Unit k's K/V have landed (each thread waited for its own copies): rotate
+    // its new keys in place with the table of its positions.
+    auto prepare_unit = [&](int k, bool bad) {
+      if (prm.pos_offset) {
+        named_bar_sync(kBarCompute, kCompute);  // nobody still reads the previous table
+        build_table(prm.pos_offset[unit_of(k) / prm.Hkv], kCompute);
+      }
+      named_bar_sync(kBarCompute, kCompute);
+      if (!bad) {
+        const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
+        for (int idx = tid; idx < l * (CPR / 2); idx += kCompute) {
+          const int t = idx / (CPR / 2), J = idx - t * (CPR / 2);
+          const uint32_t a0 = chunk_addr(kb, kv_panel, C + t, J);
+          const uint32_t a1 = chunk_addr(kb, kv_panel, C + t, J + CPR / 2);
+          uint64_t xr[4], yr[4];
+          rope_chunk(lds16(a0), lds16(a1), tab + t * prm.tab_stride, 8 * J, xr, yr);
+          sts16(a0, make_uint4(f2_to_bf16x2(xr[0]), f2_to_bf16x2(xr[1]), f2_to_bf16x2(xr[2]),
+                               f2_to_bf16x2(xr[3])));
+          sts16(a1, make_uint4(f2_to_bf16x2(yr[0]), f2_to_bf16x2(yr[1]), f2_to_bf16x2(yr[2]),
+                               f2_to_bf16x2(yr[3])));
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kBarCompute, kCompute);
+    };
+    // Rotate row r of tile i's q (this half's chunk pairs): hi -> stage, lo -> TMEM.
+    auto rope_tile = [&](int i) -> bool {
+      const int s = i % kStages, mt = i % n_mt;
+      const uint32_t stage = sbase + s * prm.stage_bytes;
+      const int t0 = mt * Tm, toks = min(Tm, l - t0);
+      const bool valid = r < toks * G;
+      const int tt = min(r / G, toks - 1);
+      const bool ok = mbar_wait(&bars->qfull[s], (uint32_t)(i / kStages) & 1u);
+      constexpr int JH = CPR / 4;  // chunk pairs per half
+      uint32_t lo_a[JH * 4], lo_b[JH * 4];
+      const uint8_t* trow = tab + (t0 + tt) * prm.tab_stride;
+#pragma unroll
+      for (int jj = 0; jj < JH; ++jj) {
+        const int J = h * JH + jj;
+        const uint32_t a0 = chunk_addr(stage, kPanel, r, J);
+        const uint32_t a1 = chunk_addr(stage, kPanel, r, J + CPR / 2);
+        uint64_t xr[4], yr[4];
+        rope_chunk(lds16(a0), lds16(a1), trow, 8 * J, xr, yr);
+        uint32_t xh[4], yh[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          f2_split_bf16(xr[e], xh[e], lo_a[jj * 4 + e]);
+          f2_split_bf16(yr[e], yh[e], lo_b[jj * 4 + e]);
+        }
+        if (valid) {
+          sts16(a0, make_uint4(xh[0], xh[1], xh[2], xh[3]));
+          sts16(a1, make_uint4(yh[0], yh[1], yh[2], yh[3]));
+        }
+      }
+      // TMEM column c of the lo block holds q elements (2c, 2c+1)
+#pragma unroll
+      for (int q8 = 0; q8 < JH / 2; ++q8) {
+        uint32_t va[8], vb8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          va[e] = valid ? lo_a[q8 * 8 + e] : 0u;
+          vb8[e] = valid ? lo_b[q8 * 8 + e] : 0u;
+        }
+        tc::st8(tmem + lane_base + prm.lo_col + (h * JH + q8 * 2) * 4, va);
+        tc::st8(tmem + lane_base + prm.lo_col + (h * JH + q8 * 2 + CPR / 2) * 4, vb8);
+      }
+      tc::wait_st();
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(&bars->rope_done);
+      return ok;
+    };
+
+    bool bad0 = false, bad1 = false;  // out-of-range block id in the unit of K/V buffer 0 / 1
+    bool failed = false;
+    if (my_units > 0) {
+      bad0 = stage_kv(unit_of(0), 0);
+      if (my_units > 1) {
+        bad1 = stage_kv(unit_of(1), 1);
+        cp_async_wait_group<1>();
+      } else {
+        cp_async_wait_group<0>();
+      }
+      prepare_unit(0, bad0);
+      failed = named_bar_or(kBarCompute, kCompute, !rope_tile(0));
+    }
+    for (int i = 0; i < my_tiles && !failed; ++i) {
+      const uint32_t par = (uint32_t)i & 1u;
+      const int k = i / n_mt, mt = i % n_mt;
+      const bool bad = (k & 1) ? bad1 : bad0;
+      const int t0 = mt * Tm, toks = min(Tm, l - t0);
+      const bool valid = r < toks * G;
+      const int tt = min(r / G, toks - 1);
+      const int N = (C + t0 + toks + 15) & ~15;
+      // ---- softmax of row r over this half's 16-column chunks c = h, h+2, ...
+      bool ok = mbar_wait(&bars->s_done, par);
+      tc::fence_after_sync();
+      const int lim = C + t0 + tt + 1;  // keys row r sees
+      const int lim_all = C + t0 + 1;   // keys every row of the tile sees
+      // chunks below lim_all need no mask (a uniform test across the warp)
+      float mx0 = kNegInf, mx1 = kNegInf;
+#pragma unroll
+      for (int cc = 0; cc < kMaxKeys / 32; ++cc) {
+        const int c = 2 * cc + h;
+        if (c * 16 < N) {
+          uint32_t sv[16];
+          tc::ld16(tmem + lane_base + c * 16, sv);
+          tc::wait_ld();
+          if ((c + 1) * 16 <= lim_all) {
+            const float a = max3f(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+            const float b = max3f(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
+            const float d = max3f(__uint_as_float(sv[6]), __uint_as_float(sv[7]), __uint_as_float(sv[8]));
+            const float e = max3f(__uint_as_float(sv[9]), __uint_as_float(sv[10]), __uint_as_float(sv[11]));
+            const float f = max3f(__uint_as_float(sv[12]), __uint_as_float(sv[13]), __uint_as_float(sv[14]));
+            mx0 = max3f(mx0, a, b);
+            mx1 = max3f(mx1, max3f(d, e, f), __uint_as_float(sv[15]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float a = c * 16 + e < lim ? __uint_as_float(sv[e]) : kNegInf;
+              const float b = c * 16 + e + 1 < lim ? __uint_as_float(sv[e + 1]) : kNegInf;
+              mx0 = max3f(mx0, a, b);
+            }
+          }
+        }
+      }
+      red_max[h * 128 + r] = fmaxf(mx0, mx1);
+      named_bar_sync(kBarCompute, kCompute);
+      const float m = fmaxf(red_max[r], red_max[128 + r]);
+      {
+        const float sc = prm.scale_log2;
+        const uint64_t sc2 = f2_make(sc, sc), nmc2 = f2_make(-m * sc, -m * sc);
+        const uint64_t one2 = f2_make(1.f, 1.f);
+        uint64_t acc[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+#pragma unroll
+        for (int cc = 0; cc < kMaxKeys / 32; ++cc) {
+          const int c = 2 * cc + h;
+          if (c * 16 < N) {
+            uint32_t sv[16];
+            tc::ld16(tmem + lane_base + c * 16, sv);
+            tc::wait_ld();
+            const bool full = (c + 1) * 16 <= lim_all;
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float a = __uint_as_float(sv[2 * e]), bb = __uint_as_float(sv[2 * e + 1]);
+              if (!full) {
+                a = c * 16 + 2 * e < lim ? a : kNegInf;
+                bb = c * 16 + 2 * e + 1 < lim ? bb : kNegInf;
+              }
+              f2_split(f2_fma(f2_make(a, bb), sc2, nmc2), a, bb);
+              const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
+              acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
+              pk[e] = f2_to_bf16x2(pp);
+            }
+            tc::st8(tmem + lane_base + prm.p_col + c * 8, pk);
+          }
+        }
+        float a0, a1, b0, b1;
+        f2_split(acc[0], a0, a1);
+        f2_split(acc[1], b0, b1);
+        red_sum[h * 128 + r] = (a0 + a1) + (b0 + b1);
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(&bars->p_done);
+      // ---- next tile's K/V and q rotation (overlaps O = P V on the tensor core)
+      if (i + 1 < my_tiles) {
+        if ((i + 1) % n_mt == 0) {  // the next tile opens unit k+1
+          cp_async_wait_group<0>();
+          prepare_unit(k + 1, ((k + 1) & 1) ? bad1 : bad0);
+        }
+        if (!rope_tile(i + 1)) ok = false;
+      }
+      // ---- O of row r, this half's columns, normalised into the stage
+      ok = mbar_wait(&bars->o_done, par) && ok;
+      tc::fence_after_sync();
+      if (named_bar_or(kBarCompute, kCompute, !ok)) failed = true;  // also: row sums written
+      {
+        const uint32_t stage = sbase + (i % kStages) * prm.stage_bytes;
+        const float inv = 1.f / (red_sum[r] + red_sum[128 + r]);
+        const uint64_t inv2 = f2_make(inv, inv);
+        constexpr int OC = D / 32;  // 16-column chunks per half
+#pragma unroll
+        for (int c = 0; c < OC; ++c) {
+          uint32_t ov[16];
+          tc::ld16(tmem + lane_base + prm.o_col + (h * OC + c) * 16, ov);
+          tc::wait_ld();
+          if (valid) {  // (one 16-column chunk at a time keeps registers low)
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = bad ? 0u
+                         : f2_to_bf16x2(f2_mul(
+                               f2_make(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])),
+                               inv2));
+            const int J = (h * OC + c) * 2;
+            sts16(chunk_addr(stage, kPanel, r, J), make_uint4(w[0], w[1], w[2], w[3]));
+            sts16(chunk_addr(stage, kPanel, r, J + 1), make_uint4(w[4], w[5], w[6], w[7]));
+          }
+        }
+      }
+      if (bad && mt == 0 && tid == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(&bars->o_stored);
+      // ---- the last tile of unit k: its K/V buffer is free for unit k+2
+      if (mt == n_mt - 1 && k + 2 < my_units) {
+        const bool bk = stage_kv(unit_of(k + 2), k & 1);
+        if (k & 1) bad1 = bk; else bad0 = bk;
+      }
+    }
+    if (failed && tid == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    cp_async_wait_all();
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 8) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, prm.tmem_cols);
+  }
+}
+
+int encode_map(CUtensorMap* m, const void* base, const Problem& pb, int Tm) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return GIST_ATTN_ERR_LAUNCH;
+  const cuuint64_t dims[5] = {64, (cuuint64_t)(pb.d / 64), (cuuint64_t)pb.Hq, (cuuint64_t)pb.l,
+                              (cuuint64_t)pb.P};
+  const cuuint64_t strides[4] = {128, (cuuint64_t)pb.d * 2, (cuuint64_t)pb.Hq * pb.d * 2,
+                                 (cuuint64_t)pb.l * pb.Hq * pb.d * 2};
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)pb.G, (cuuint32_t)Tm, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+template <int D>
+int launch_d(const Problem& pb, cudaStream_t stream) {
+  const Layout L = plan(pb);
+  TcParams prm{};
+  prm.k_new = static_cast<const bf16*>(pb.k_new);
+  prm.v_new = static_cast<const bf16*>(pb.v_new);
+  prm.pv = PoolView{static_cast<const bf16*>(pb.kv_pool), pb.item_ids, pb.block_table,
+                    pb.blocks_per_pair, pb.block_len, pb.num_blocks, pb.L, pb.layer, pb.Hkv, pb.d};
+  prm.pos_offset = pb.pos_offset;
+  prm.status = pb.status;
+  prm.l = pb.l;
+  prm.Hkv = pb.Hkv;
+  prm.G = pb.G;
+  prm.C = pb.C;
+  prm.Tm = L.Tm;
+  prm.n_mt = L.n_mt;
+  prm.num_units = pb.P * pb.Hkv;
+  prm.kv_rows = L.kv_rows;
+  prm.stage_bytes = L.stage_bytes;
+  prm.off_kv = L.off_kv;
+  prm.kv_buf_bytes = L.kv_buf_bytes;
+  prm.off_tab = L.off_tab;
+  prm.tab_stride = L.tab_stride;
+  prm.off_ids = L.off_ids;
+  prm.off_red = L.off_red;
+  prm.off_bar = L.off_bar;
+  prm.p_col = L.p_col;
+  prm.o_col = L.o_col;
+  prm.lo_col = L.lo_col;
+  prm.tmem_cols = L.tmem_cols;
+  prm.scale_log2 = pb.scale_log2;
+  for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+
+  alignas(64) CUtensorMap tm_q, tm_o;
+  int rc = encode_map(&tm_q, pb.q, pb, L.Tm);
+  if (rc != GIST_ATTN_OK) return rc;
+  rc = encode_map(&tm_o, pb.out, pb, L.Tm);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)L.bytes) != cudaSuccess)
+    return GIST_ATTN_ERR_LAUNCH;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GIST_ATTN_ERR_LAUNCH;
+  // Two CTAs per SM only when both fit: two 256-column TMEM allocations and
+  // shared memory for two.  A larger TMEM plan or shared memory means one.
+  const int per_sm = (D == 64 && L.tmem_cols == 256 && L.bytes <= 113 * 1024) ? 2 : 1;
+  const int64_t units = (int64_t)pb.P * pb.Hkv;
+  const int grid = (int)(units < (int64_t)sms * per_sm ? units : (int64_t)sms * per_sm);
+  prefill_tc_kernel<D><<<grid, kThreads, L.bytes, stream>>>(tm_q, tm_o, prm);
+  return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+bool prefill_tc_fits(const Problem& pb) {
+  if (pb.l < 2 || pb.G > 128 || pb.C + pb.l > kMaxKeys) return false;
+  if (pb.blocks_per_pair > kMaxBlocksPerPair) return false;
+  if (pb.d != 64 && pb.d != 128) return false;
+  if ((int64_t)pb.P * pb.Hkv > 0x7fffffff) return false;
+  return plan(pb).bytes <= (uint32_t)kMaxSmem;
+}
+
+int launch_prefill_tc(const Problem& pb, cudaStream_t stream) {
+  if (pb.d == 64) return launch_d<64>(pb, stream);
+  if (pb.d == 128) return launch_d<128>(pb, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace gattn
