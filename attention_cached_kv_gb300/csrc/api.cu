@@ -118,7 +118,11 @@ extern "C" int gist_attn_fwd(const void* q, const void* k_new, const void* v_new
   pb.pos_offset = pos_offset;
   pb.out = out;
   if (pb.C == 0) pb.blocks_per_pair = 0;  // nothing cached: no ids to read
-  if (pb.l == 1 && gattn::decode_fits(pb)) return gattn::launch_decode(pb, stream);
+  if (pb.l == 1) {
+    if (gattn::decode_long_fits(pb)) return gattn::launch_decode_long(pb, stream);
+    if (gattn::decode_short_fits(pb)) return gattn::launch_decode_short(pb, stream);
+    if (gattn::decode_fits(pb)) return gattn::launch_decode(pb, stream);
+  }
   if (gattn::prefill_tc_fits(pb)) return gattn::launch_prefill_tc(pb, stream);
   if (gattn::prefill_fits(pb)) return gattn::launch_prefill(pb, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;

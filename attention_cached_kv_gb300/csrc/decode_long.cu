@@ -1,0 +1,266 @@
+// decode_long.cu -- one new token (l = 1) against a long cached context read
+// through a block table: the paged decode step.
+//
+// [KV page, "Reusable-state"]: o_t = softmax(q_t K_{<=t}^T / sqrt(d_k)) V_{<=t},
+// K_{<=t} = [K_{<t}; k_t]; [Suffix page, §5 第一步 and §6 问题四]: the context
+// lives in fixed-size blocks of a pool, reached through a logical -> physical
+// block table.  The cost is the read of every cached K/V row ([KV page,
+// "Cost"]: O(t d) per step), so the kernel is built to stream.
+//
+// One CTA per (sequence, KV head), four warps, sized so every CTA of a
+// batch-32 x 32-head step is resident at once (no split of the key range, no
+// scratch memory).  A block's rows for one head are contiguous, so the cached
+// keys are streamed 16 rows at a time by 1-D bulk (TMA) copies of K and of V
+// into a 3-stage shared-memory ring.  In a 16-key chunk warp w takes keys
+// 4w..4w+3: eight lanes per key form the dot product with the rotated,
+// pre-scaled query held in registers (fp32), the warp keeps a running max and
+// sum, and each lane accumulates d/32 columns of P V.  The new token's own
+// key/value join at the end; the four warps merge in shared memory.
+//
+// Pages: [Suffix page] icman.com.cn news 64898;
+//        [KV page] "为什么自回归推理缓存 KV，而不缓存历史 Q？".
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gattn {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = 4;
+constexpr int kChunk = 16;  // keys per ring stage
+constexpr int kStages = 3;
+constexpr int kMaxBlocks = 256;
+
+struct LongParams {
+  const bf16* q;
+  const bf16* k_new;
+  const bf16* v_new;
+  bf16* out;
+  PoolView pv;
+  const int32_t* pos_offset;
+  int32_t* status;
+  int Hq, Hkv, C;
+  float scale_log2;
+  float inv_freq[64];
+};
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_constant__ LongParams prm) {
+  constexpr int HALF = D / 2;
+  constexpr int QE = D / 8;        // query elements per lane (8 lanes per key)
+  constexpr int VE = D / 32;       // value columns per lane
+  constexpr uint32_t kRow = D * 2;  // bytes per K or V row
+  constexpr uint32_t kStageBytes = 2 * kChunk * kRow;  // K rows then V rows
+  constexpr float kNegInf = -INFINITY;
+
+  __shared__ __align__(128) uint8_t ring[kStages * kStageBytes];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ int32_t ids[kMaxBlocks];
+  __shared__ float qs[D], kn[D], vn[D];
+  __shared__ float red_m[kWarps], red_l[kWarps];
+  __shared__ float red_o[kWarps][D];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.x % prm.Hkv, p = blockIdx.x / prm.Hkv;
+  const int C = prm.C, bl = prm.pv.block_len;
+  const int n_chunks = C / kChunk;
+
+  bool bad = false;
+  for (int b = tid; b < prm.pv.blocks_per_pair; b += kThreads) {
+    const int32_t blk = pool_block_id(prm.pv, p, b);
+    bad |= !pool_block_ok(prm.pv, blk);
+    ids[b] = blk;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  // rotated query (pre-scaled to log2 units), rotated new key, new value
+  const float pos = (float)(prm.pos_offset ? prm.pos_offset[p] : C);
+  for (int idx = tid; idx < 2 * HALF; idx += kThreads) {
+    const int which = idx / HALF, j = idx - which * HALF;  // 0: q, 1: k_new
+    const bf16* src = which == 0 ? prm.q + ((int64_t)p * prm.Hq + g) * D
+                                 : prm.k_new + ((int64_t)p * prm.Hkv + g) * D;
+    const float x = __bfloat162float(src[j]), y = __bfloat162float(src[j + HALF]);
+    float s, c;
+    sincosf(pos * prm.inv_freq[j], &s, &c);
+    const float sc = which == 0 ? prm.scale_log2 : 1.f;
+    float* dst = which == 0 ? qs : kn;
+    dst[j] = (x * c - y * s) * sc;
+    dst[j + HALF] = (y * c + x * s) * sc;
+  }
+  for (int e = tid; e < D; e += kThreads)
+    vn[e] = __bfloat162float(prm.v_new[((int64_t)p * prm.Hkv + g) * D + e]);
+  bad = __syncthreads_or(bad);
+  bf16* out = prm.out + ((int64_t)p * prm.Hq + g) * D;
+  if (bad) {
+    for (int e = tid; e < D; e += kThreads) out[e] = __float2bfloat16(0.f);
+    if (tid == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
+    return;
+  }
+
+  const uint32_t ring0 = smem_u32(ring);
+  auto issue = [&](int ci) {  // chunk ci -> stage ci % kStages (thread 0)
+    const int s = ci % kStages;
+    const int key = ci * kChunk, b = key / bl, t = key - b * bl;
+    mbar_arrive_expect_tx(&full[s], kStageBytes);
+    bulk_g2s(ring0 + s * kStageBytes, pool_row(prm.pv, ids[b], g, 0, t), kChunk * kRow, &full[s]);
+    bulk_g2s(ring0 + s * kStageBytes + kChunk * kRow, pool_row(prm.pv, ids[b], g, 1, t),
+             kChunk * kRow, &full[s]);
+  };
+  if (tid == 0)
+    for (int ci = 0; ci < kStages && ci < n_chunks; ++ci) issue(ci);
+
+  // this lane's slice of the query: elements (lane % 8) * QE ..
+  const int kg = lane >> 3, sl = lane & 7;
+  float qr[QE];
+#pragma unroll
+  for (int e = 0; e < QE; ++e) qr[e] = qs[sl * QE + e];
+  float m = kNegInf, lsum = 0.f, o[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) o[e] = 0.f;
+
+  // one key per 8-lane group: logit s (all 8 lanes), then the warp's online update
+  auto consume = [&](float s_key, bool valid, const uint8_t* vrows) {
+    float sv = valid ? s_key : kNegInf;
+    float cm = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, 8));
+    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+    const float mn = fmaxf(m, cm);
+    const float al = ex2_approx(m - mn);
+    const float pk = ex2_approx(sv - mn);  // this group's key weight
+    m = mn;
+    float ps = pk + __shfl_xor_sync(0xffffffffu, pk, 8);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+    lsum = lsum * al + ps;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) o[e] *= al;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float pj = __shfl_sync(0xffffffffu, pk, j * 8);
+      if (vrows) {
+        const uint8_t* vr = vrows + j * kRow + lane * VE * 2;
+        if constexpr (VE == 4) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(vr);
+          const float2 a = bf16x2_to_float2(raw.x), b2 = bf16x2_to_float2(raw.y);
+          o[0] += pj * a.x; o[1] += pj * a.y; o[2] += pj * b2.x; o[3] += pj * b2.y;
+        } else {
+          const float2 a = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(vr));
+          o[0] += pj * a.x; o[1] += pj * a.y;
+        }
+      }
+    }
+  };
+
+  bool ok = true;
+  for (int ci = 0; ci < n_chunks; ++ci) {
+    const int s = ci % kStages;
+    ok = mbar_wait(&full[s], (uint32_t)(ci / kStages) & 1u) && ok;
+    const uint8_t* stage = ring + s * kStageBytes;
+    const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE * 2;
+    float acc = 0.f;
+#pragma unroll
+    for (int v = 0; v < QE / 8; ++v) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(krow + v * 16);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 kf = bf16x2_to_float2(w[e]);
+        acc = fmaf(qr[v * 8 + 2 * e], kf.x, acc);
+        acc = fmaf(qr[v * 8 + 2 * e + 1], kf.y, acc);
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    consume(acc, true, stage + kChunk * kRow + warp * 4 * kRow);
+    __syncthreads();  // every warp is done with stage s
+    if (tid == 0 && ci + kStages < n_chunks) issue(ci + kStages);
+  }
+  // the new token's own key and value (warp 0, group 0)
+  if (warp == 0) {
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < QE; ++e) acc = fmaf(qr[e], kn[sl * QE + e], acc);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    // every lane holds the full dot product of q with the new key
+    const float mn = fmaxf(m, acc);
+    const float al = ex2_approx(m - mn);
+    const float pnew = ex2_approx(acc - mn);
+    m = mn;
+    lsum = lsum * al + pnew;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) o[e] = o[e] * al + pnew * vn[lane * VE + e];
+  }
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_l[warp] = lsum;
+  }
+#pragma unroll
+  for (int e = 0; e < VE; ++e) red_o[warp][lane * VE + e] = o[e];
+  __syncthreads();
+  for (int e = tid; e < D; e += kThreads) {
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = ex2_approx(red_m[w] - M);
+      num += red_o[w][e] * f;
+      den += red_l[w] * f;
+    }
+    out[e] = __float2bfloat16(num / den);
+  }
+  if (!ok && tid == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+}
+
+template <int D>
+int launch_d(const Problem& pb, cudaStream_t stream) {
+  LongParams prm{};
+  prm.q = static_cast<const bf16*>(pb.q);
+  prm.k_new = static_cast<const bf16*>(pb.k_new);
+  prm.v_new = static_cast<const bf16*>(pb.v_new);
+  prm.out = static_cast<bf16*>(pb.out);
+  prm.pv = PoolView{static_cast<const bf16*>(pb.kv_pool), pb.item_ids, pb.block_table,
+                    pb.blocks_per_pair, pb.block_len, pb.num_blocks, pb.L, pb.layer, pb.Hkv, pb.d};
+  prm.pos_offset = pb.pos_offset;
+  prm.status = pb.status;
+  prm.Hq = pb.Hq;
+  prm.Hkv = pb.Hkv;
+  prm.C = pb.C;
+  prm.scale_log2 = pb.scale_log2;
+  for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  const int64_t grid = (int64_t)pb.P * pb.Hkv;
+  if (grid > 0x7fffffff) return GIST_ATTN_ERR_UNSUPPORTED;
+  decode_long_kernel<D><<<(unsigned)grid, kThreads, 0, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+// MHA decode over a long cache whose blocks hold whole 16-row chunks.
+bool decode_long_fits(const Problem& pb) {
+  return pb.l == 1 && pb.G == 1 && pb.C >= 64 && pb.block_len % kChunk == 0 &&
+         pb.blocks_per_pair <= kMaxBlocks && (pb.d == 64 || pb.d == 128);
+}
+
+int launch_decode_long(const Problem& pb, cudaStream_t stream) {
+  if (pb.d == 64) return launch_d<64>(pb, stream);
+  if (pb.d == 128) return launch_d<128>(pb, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace gattn

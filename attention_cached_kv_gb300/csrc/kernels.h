@@ -38,11 +38,15 @@ EncodeTiledFn encode_tiled_fn();
 int launch_prefill(const Problem& pb, cudaStream_t stream);
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream);
 int launch_decode(const Problem& pb, cudaStream_t stream);
+int launch_decode_long(const Problem& pb, cudaStream_t stream);
+int launch_decode_short(const Problem& pb, cudaStream_t stream);
 int launch_gather(const Problem& pb, void* dst, cudaStream_t stream);
 
 // Whether the prefill kernel can hold this problem's tiles in shared memory.
 bool prefill_fits(const Problem& pb);
 bool prefill_tc_fits(const Problem& pb);
 bool decode_fits(const Problem& pb);
+bool decode_long_fits(const Problem& pb);
+bool decode_short_fits(const Problem& pb);
 
 }  // namespace gattn

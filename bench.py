@@ -33,7 +33,8 @@ if ROOT not in sys.path:
 METRIC = "(item,query) pairs/s per layer-attention; achieved HBM GB/s vs GB300 peak"
 UNIT = "pairs/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["api.cu", "prefill.cu", "prefill_tc.cu", "decode.cu", "common.cuh", "kernels.h", "tcgen05.cuh"]
+KERNEL_SOURCES = ["api.cu", "prefill.cu", "prefill_tc.cu", "decode.cu", "decode_long.cu",
+                  "decode_short.cu", "common.cuh", "kernels.h", "tcgen05.cuh"]
 
 DESCR = {
     "gist": "gist relevance: 24 layers, Hq=14, Hkv=2, d=64, k=8, l=64; 256 queries x 50 "
