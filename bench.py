@@ -33,8 +33,14 @@ if ROOT not in sys.path:
 METRIC = "(item,query) pairs/s per layer-attention; achieved HBM GB/s vs GB300 peak"
 UNIT = "pairs/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["api.cu", "prefill.cu", "prefill_tc.cu", "decode.cu", "decode_long.cu",
-                  "decode_short.cu", "common.cuh", "kernels.h", "tcgen05.cuh"]
+# the dominant kernel of each workload and the sources it is built from
+KERNEL_OF = {
+    "gist": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh"]),
+    "wide": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh"]),
+    "tiny": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh"]),
+    "qgist": ("decode_short_kernel", ["decode_short.cu", "common.cuh"]),
+    "paged": ("decode_long_kernel", ["decode_long.cu", "common.cuh"]),
+}
 
 DESCR = {
     "gist": "gist relevance: 24 layers, Hq=14, Hkv=2, d=64, k=8, l=64; 256 queries x 50 "
@@ -59,6 +65,7 @@ def parse_args(argv=None):
     ap.add_argument("--report", default=None, help="also write a detailed JSON report here")
     ap.add_argument("--queries", type=int, default=0, help="smaller batch (profiling runs)")
     ap.add_argument("--pool-items", type=int, default=0, help="smaller pool (profiling runs)")
+    ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -81,9 +88,9 @@ def algorithmic_bytes_per_launch(wl) -> dict:
             "total_per_pair_gather": P * (per_pair + d["blocks_per_pair"] * block)}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(workload: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_OF[workload][1]:
         with open(os.path.join(ROOT, "attention_cached_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -107,7 +114,7 @@ def recorded_traffic(workload: str):
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_sources_sha") != kernel_source_hash():
+    if not rec or rec.get("kernel_sources_sha") != kernel_source_hash(workload):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -268,6 +275,8 @@ def run_ours(args) -> dict:
         over["queries"] = args.queries
     if args.pool_items:
         over["pool_items"] = args.pool_items
+    if args.layers:
+        over["num_layers"] = args.layers
     wl = workloads.make(args.workload, device=dev, **over)
     L, P = wl.dims["num_layers"], wl.dims["num_pairs"]
     stream = torch.cuda.Stream(device=dev)
@@ -342,7 +351,8 @@ def run_ours(args) -> dict:
         "config": {"workload": DESCR[args.workload], "pairs": P, "layers_per_step": L,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "inputs larger than L2 (no flush needed)"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"kernel": KERNEL_OF[args.workload][0],
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
