@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libgistattn.so")
 OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH = 0, -1, -2, -3, -4, -5
 STATUS_BAD_BLOCK, STATUS_TIMEOUT = 1, 2
 
-EXPORTS = ("gist_attn_fwd", "gist_attn_gather_debug", "gist_kv_bytes_per_position",
+EXPORTS = ("gist_attn_fwd", "gist_attn_fwd_fp8kv", "gist_attn_gather_debug", "gist_kv_bytes_per_position",
            "gist_kv_bytes_per_item", "gist_kv_bytes_batch", "gist_attn_status_string")
 
 
@@ -65,6 +65,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             V = ctypes.c_void_p
             lib.gist_attn_fwd.restype = ctypes.c_int
             lib.gist_attn_fwd.argtypes = [V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
+            lib.gist_attn_fwd_fp8kv.restype = ctypes.c_int
+            lib.gist_attn_fwd_fp8kv.argtypes = [V, V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_attn_gather_debug.restype = ctypes.c_int
             lib.gist_attn_gather_debug.argtypes = [V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_kv_bytes_per_position.restype = ctypes.c_size_t
@@ -137,6 +139,31 @@ def gist_attn_fwd(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, pos
                            _ptr(block_table, i32, "block_table"),
                            _ptr(pos_offset, i32, "pos_offset"), _ptr(out, bf, "out"),
                            ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return out
+
+
+def gist_attn_fwd_fp8kv(q, k_new, v_new, kv_pool_e4m3, kv_scale, item_ids=None, block_table=None,
+                        pos_offset=None, out=None, *, dims: dict, status: torch.Tensor | None = None,
+                        stream=None):
+    """gist_attn_fwd with an E4M3 pool (torch.float8_e4m3fn or uint8) and fp32 scales
+    [num_blocks][L][2][Hkv]; returns `out` (allocated if None)."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q)
+    bf, i32 = torch.bfloat16, torch.int32
+    if kv_pool_e4m3 is not None and kv_pool_e4m3.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError("kv_pool_e4m3 must be float8_e4m3fn or uint8")
+    pool_ptr = None
+    if kv_pool_e4m3 is not None:
+        _check(kv_pool_e4m3, kv_pool_e4m3.dtype, "kv_pool_e4m3")
+        pool_ptr = ctypes.c_void_p(kv_pool_e4m3.data_ptr())
+    D = make_dims(dims, status)
+    rc = lib.gist_attn_fwd_fp8kv(_ptr(q, bf, "q"), _ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"),
+                                 pool_ptr, _ptr(kv_scale, torch.float32, "kv_scale"),
+                                 _ptr(item_ids, i32, "item_ids"), _ptr(block_table, i32, "block_table"),
+                                 _ptr(pos_offset, i32, "pos_offset"), _ptr(out, bf, "out"),
+                                 ctypes.byref(D), _stream(stream))
     _raise(rc)
     return out
 

@@ -128,6 +128,35 @@ extern "C" int gist_attn_fwd(const void* q, const void* k_new, const void* v_new
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 
+extern "C" int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void* v_new,
+                                   const void* kv_pool_e4m3, const float* kv_scale,
+                                   const int32_t* item_ids, const int32_t* block_table,
+                                   const int32_t* pos_offset, void* out,
+                                   const gist_attn_dims* dims, cudaStream_t stream) {
+  Problem pb{};
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (pb.P == 0) return GIST_ATTN_OK;
+  if (!q || !k_new || !v_new || !out) return GIST_ATTN_ERR_NULL;
+  rc = gattn::check_cache_args(pb, kv_pool_e4m3, item_ids, block_table);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (pb.C > 0 && !kv_scale) return GIST_ATTN_ERR_NULL;
+  if (!gattn::aligned(q, 16) || !gattn::aligned(k_new, 16) || !gattn::aligned(v_new, 16) ||
+      !gattn::aligned(out, 16) || !gattn::aligned(pos_offset, 4) ||
+      !gattn::aligned(pb.status, 4) || !gattn::aligned(kv_scale, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  pb.q = q;
+  pb.k_new = k_new;
+  pb.v_new = v_new;
+  pb.kv_pool = kv_pool_e4m3;
+  pb.item_ids = item_ids;
+  pb.block_table = block_table;
+  pb.pos_offset = pos_offset;
+  pb.out = out;
+  if (pb.C > 0 && gattn::decode_long_fits(pb)) return gattn::launch_decode_long_fp8(pb, kv_scale, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
 extern "C" int gist_attn_gather_debug(const void* kv_pool, const int32_t* item_ids,
                                       const int32_t* block_table, void* dst,
                                       const gist_attn_dims* dims, cudaStream_t stream) {

@@ -17,9 +17,16 @@
 // sum, and each lane accumulates d/32 columns of P V.  The new token's own
 // key/value join at the end; the four warps merge in shared memory.
 //
+// The same kernel reads an FP8 (E4M3) pool ([Suffix page, §2 and the end of §5]:
+// 1-byte KV elements), one fp32 scale per (block, layer, K|V, KV head): the
+// chunks are half as many bytes, widened in registers (e4m3 -> f16x2 -> f32),
+// the K scale multiplies the logit and the V scale the value weight.
+//
 // Pages: [Suffix page] icman.com.cn news 64898;
 //        [KV page] "为什么自回归推理缓存 KV，而不缓存历史 Q？".
 #include <math.h>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -30,10 +37,11 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kWarps = 4;
 constexpr int kChunk = 16;  // keys per ring stage
-constexpr int kStages = 3;
+constexpr int kStagesBf16 = 3;  // ring depth; the fp8 ring has twice the stages (same bytes)
 constexpr int kMaxBlocks = 256;
 
 struct LongParams {
+  const float* kv_scale;  // FP8 pool: [num_blocks][L][2][Hkv], else unused
   const bf16* q;
   const bf16* k_new;
   const bf16* v_new;
@@ -55,13 +63,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-template <int D>
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v16) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)v16));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_constant__ LongParams prm) {
   constexpr int HALF = D / 2;
   constexpr int QE = D / 8;        // query elements per lane (8 lanes per key)
   constexpr int VE = D / 32;       // value columns per lane
-  constexpr uint32_t kRow = D * 2;  // bytes per K or V row
+  constexpr uint32_t kRow = FP8 ? D : D * 2;  // bytes per K or V row
   constexpr uint32_t kStageBytes = 2 * kChunk * kRow;  // K rows then V rows
+  constexpr int kStages = FP8 ? 2 * kStagesBf16 : kStagesBf16;
   constexpr float kNegInf = -INFINITY;
 
   __shared__ __align__(128) uint8_t ring[kStages * kStageBytes];
@@ -70,6 +85,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
   __shared__ float qs[D], kn[D], vn[D];
   __shared__ float red_m[kWarps], red_l[kWarps];
   __shared__ float red_o[kWarps][D];
+  __shared__ float kscale[FP8 ? kMaxBlocks : 1], vscale[FP8 ? kMaxBlocks : 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x % prm.Hkv, p = blockIdx.x / prm.Hkv;
@@ -79,8 +95,15 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
   bool bad = false;
   for (int b = tid; b < prm.pv.blocks_per_pair; b += kThreads) {
     const int32_t blk = pool_block_id(prm.pv, p, b);
-    bad |= !pool_block_ok(prm.pv, blk);
+    const bool okb = pool_block_ok(prm.pv, blk);
+    bad |= !okb;
     ids[b] = blk;
+    if constexpr (FP8) {
+      const int64_t si = (((int64_t)(okb ? blk : 0) * prm.pv.num_layers + prm.pv.layer) * 2) *
+                             prm.Hkv + g;
+      kscale[b] = prm.kv_scale[si];
+      vscale[b] = prm.kv_scale[si + prm.Hkv];
+    }
   }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
@@ -115,9 +138,15 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
     const int s = ci % kStages;
     const int key = ci * kChunk, b = key / bl, t = key - b * bl;
     mbar_arrive_expect_tx(&full[s], kStageBytes);
-    bulk_g2s(ring0 + s * kStageBytes, pool_row(prm.pv, ids[b], g, 0, t), kChunk * kRow, &full[s]);
-    bulk_g2s(ring0 + s * kStageBytes + kChunk * kRow, pool_row(prm.pv, ids[b], g, 1, t),
-             kChunk * kRow, &full[s]);
+    const bf16* krow = pool_row(prm.pv, ids[b], g, 0, t);
+    const bf16* vrow = pool_row(prm.pv, ids[b], g, 1, t);
+    if constexpr (FP8) {  // the same element offsets, one byte per element
+      const uint8_t* p8 = reinterpret_cast<const uint8_t*>(prm.pv.pool);
+      krow = reinterpret_cast<const bf16*>(p8 + (krow - prm.pv.pool));
+      vrow = reinterpret_cast<const bf16*>(p8 + (vrow - prm.pv.pool));
+    }
+    bulk_g2s(ring0 + s * kStageBytes, krow, kChunk * kRow, &full[s]);
+    bulk_g2s(ring0 + s * kStageBytes + kChunk * kRow, vrow, kChunk * kRow, &full[s]);
   };
   if (tid == 0)
     for (int ci = 0; ci < kStages && ci < n_chunks; ++ci) issue(ci);
@@ -132,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
   for (int e = 0; e < VE; ++e) o[e] = 0.f;
 
   // one key per 8-lane group: logit s (all 8 lanes), then the warp's online update
-  auto consume = [&](float s_key, bool valid, const uint8_t* vrows) {
+  auto consume = [&](float s_key, bool valid, const uint8_t* vrows, float vsc) {
     float sv = valid ? s_key : kNegInf;
     float cm = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, 8));
     cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
@@ -147,8 +176,18 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
     for (int e = 0; e < VE; ++e) o[e] *= al;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float pj = __shfl_sync(0xffffffffu, pk, j * 8);
-      if (vrows) {
+      const float pj = __shfl_sync(0xffffffffu, pk, j * 8) * vsc;
+      if constexpr (FP8) {
+        const uint8_t* vr = vrows + j * kRow + lane * VE;
+        if constexpr (VE == 4) {
+          const uint32_t raw = *reinterpret_cast<const uint32_t*>(vr);
+          const float2 a = e4m3x2_to_float2(raw & 0xffffu), b2 = e4m3x2_to_float2(raw >> 16);
+          o[0] += pj * a.x; o[1] += pj * a.y; o[2] += pj * b2.x; o[3] += pj * b2.y;
+        } else {
+          const float2 a = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vr));
+          o[0] += pj * a.x; o[1] += pj * a.y;
+        }
+      } else {
         const uint8_t* vr = vrows + j * kRow + lane * VE * 2;
         if constexpr (VE == 4) {
           const uint2 raw = *reinterpret_cast<const uint2*>(vr);
@@ -167,23 +206,49 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
     const int s = ci % kStages;
     ok = mbar_wait(&full[s], (uint32_t)(ci / kStages) & 1u) && ok;
     const uint8_t* stage = ring + s * kStageBytes;
-    const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE * 2;
     float acc = 0.f;
+    if constexpr (FP8) {
+      const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE;
+      uint32_t w[QE / 4];
+      if constexpr (QE == 16) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(krow);
+        w[0] = raw.x; w[1] = raw.y; w[2] = raw.z; w[3] = raw.w;
+      } else {
+        const uint2 raw = *reinterpret_cast<const uint2*>(krow);
+        w[0] = raw.x; w[1] = raw.y;
+      }
 #pragma unroll
-    for (int v = 0; v < QE / 8; ++v) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(krow + v * 16);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      for (int e = 0; e < QE / 4; ++e) {
+        const float2 k0 = e4m3x2_to_float2(w[e] & 0xffffu), k1 = e4m3x2_to_float2(w[e] >> 16);
+        acc = fmaf(qr[4 * e], k0.x, acc);
+        acc = fmaf(qr[4 * e + 1], k0.y, acc);
+        acc = fmaf(qr[4 * e + 2], k1.x, acc);
+        acc = fmaf(qr[4 * e + 3], k1.y, acc);
+      }
+    } else {
+      const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE * 2;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 kf = bf16x2_to_float2(w[e]);
-        acc = fmaf(qr[v * 8 + 2 * e], kf.x, acc);
-        acc = fmaf(qr[v * 8 + 2 * e + 1], kf.y, acc);
+      for (int v = 0; v < QE / 8; ++v) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(krow + v * 16);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 kf = bf16x2_to_float2(w[e]);
+          acc = fmaf(qr[v * 8 + 2 * e], kf.x, acc);
+          acc = fmaf(qr[v * 8 + 2 * e + 1], kf.y, acc);
+        }
       }
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    consume(acc, true, stage + kChunk * kRow + warp * 4 * kRow);
+    float vsc = 1.f;
+    if constexpr (FP8) {
+      const int b = (ci * kChunk) / bl;
+      acc *= kscale[b];
+      vsc = vscale[b];
+    }
+    consume(acc, true, stage + kChunk * kRow + warp * 4 * kRow, vsc);
     __syncthreads();  // every warp is done with stage s
     if (tid == 0 && ci + kStages < n_chunks) issue(ci + kStages);
   }
@@ -227,9 +292,10 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
   if (!ok && tid == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
 }
 
-template <int D>
-int launch_d(const Problem& pb, cudaStream_t stream) {
+template <int D, bool FP8>
+int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
   LongParams prm{};
+  prm.kv_scale = kv_scale;
   prm.q = static_cast<const bf16*>(pb.q);
   prm.k_new = static_cast<const bf16*>(pb.k_new);
   prm.v_new = static_cast<const bf16*>(pb.v_new);
@@ -245,7 +311,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
   const int64_t grid = (int64_t)pb.P * pb.Hkv;
   if (grid > 0x7fffffff) return GIST_ATTN_ERR_UNSUPPORTED;
-  decode_long_kernel<D><<<(unsigned)grid, kThreads, 0, stream>>>(prm);
+  decode_long_kernel<D, FP8><<<(unsigned)grid, kThreads, 0, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
@@ -258,8 +324,14 @@ bool decode_long_fits(const Problem& pb) {
 }
 
 int launch_decode_long(const Problem& pb, cudaStream_t stream) {
-  if (pb.d == 64) return launch_d<64>(pb, stream);
-  if (pb.d == 128) return launch_d<128>(pb, stream);
+  if (pb.d == 64) return launch_d<64, false>(pb, nullptr, stream);
+  if (pb.d == 128) return launch_d<128, false>(pb, nullptr, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+int launch_decode_long_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
+  if (pb.d == 64) return launch_d<64, true>(pb, kv_scale, stream);
+  if (pb.d == 128) return launch_d<128, true>(pb, kv_scale, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 

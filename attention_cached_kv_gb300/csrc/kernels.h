@@ -39,6 +39,7 @@ int launch_prefill(const Problem& pb, cudaStream_t stream);
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream);
 int launch_decode(const Problem& pb, cudaStream_t stream);
 int launch_decode_long(const Problem& pb, cudaStream_t stream);
+int launch_decode_long_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
 int launch_decode_short(const Problem& pb, cudaStream_t stream);
 int launch_gather(const Problem& pb, void* dst, cudaStream_t stream);
 

@@ -34,7 +34,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-STREAM_Q, STREAM_K, STREAM_V, STREAM_POOL, STREAM_IDS = 0, 1, 2, 3, 4
+STREAM_Q, STREAM_K, STREAM_V, STREAM_POOL, STREAM_IDS, STREAM_SCALE = 0, 1, 2, 3, 4, 5
 
 
 @dataclass
@@ -232,3 +232,23 @@ def make_custom(P: int, l: int, Hq: int, Hkv: int, d: int, block_len: int, block
                 num_layers=num_layers, layer=layer, rope_theta=1e4, softmax_scale=0.0)
     return Workload(spec, dims, q, k_new, v_new, kv_pool, item_ids, block_table, pos,
                     {"unique_blocks": int(np.unique(ids).shape[0])})
+
+
+def make_fp8_pool(wl: Workload, seed: int = 0, chunk_blocks: int = 64):
+    """An E4M3 pool of the workload's shape (float8_e4m3fn, N(0,1) draws cast to
+    E4M3, generated a few blocks at a time) and fp32 scales uniform in
+    [0.25, 1.75) per (block, layer, K|V, KV head).  Replaces wl.kv_pool; returns
+    (pool8, scales)."""
+    shape = wl.kv_pool.shape
+    dev = wl.kv_pool.device
+    wl.kv_pool = None
+    pool8 = torch.empty(shape, dtype=torch.float8_e4m3fn, device=dev)
+    g = _gen(dev, seed, STREAM_POOL)
+    for b0 in range(0, shape[0], chunk_blocks):
+        b1 = min(shape[0], b0 + chunk_blocks)
+        part = torch.randn((b1 - b0,) + tuple(shape[1:]), generator=g, device=dev, dtype=torch.bfloat16)
+        pool8[b0:b1] = part.to(torch.float8_e4m3fn)
+        del part
+    scale = torch.rand(tuple(shape[:4]), generator=_gen(dev, seed, STREAM_SCALE), device=dev,
+                       dtype=torch.float32) * 1.5 + 0.25
+    return pool8, scale

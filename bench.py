@@ -66,6 +66,8 @@ def parse_args(argv=None):
     ap.add_argument("--queries", type=int, default=0, help="smaller batch (profiling runs)")
     ap.add_argument("--pool-items", type=int, default=0, help="smaller pool (profiling runs)")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs)")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="cached-KV element type (fp8: E4M3 pool with per-block scales)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -75,13 +77,14 @@ def parse_args(argv=None):
 
 # ----------------------------------------------------------------- helpers ---
 
-def algorithmic_bytes_per_launch(wl) -> dict:
+def algorithmic_bytes_per_launch(wl, kv_elem_bytes: int = 2) -> dict:
     """Compulsory bytes of one launch: every pair's Q, K_new, V_new, O and ids
-    once, plus every distinct cached block of the layer once."""
+    once, plus every distinct cached block of the layer once (with its scales
+    for an fp8 pool)."""
     d = wl.dims
     P, l, Hq, Hkv, hd = d["num_pairs"], d["n_new"], d["num_q_heads"], d["num_kv_heads"], d["head_dim"]
     per_pair = 2 * l * Hq * hd * 2 + 2 * l * Hkv * hd * 2 + 4 * d["blocks_per_pair"]
-    block = 2 * Hkv * d["block_len"] * hd * 2
+    block = 2 * Hkv * d["block_len"] * hd * kv_elem_bytes + (2 * Hkv * 4 if kv_elem_bytes == 1 else 0)
     uniq = wl.meta["unique_blocks"]
     return {"per_pair": per_pair, "per_block": block, "unique_blocks": uniq,
             "total": P * per_pair + uniq * block,
@@ -279,6 +282,9 @@ def run_ours(args) -> dict:
         over["num_layers"] = args.layers
     wl = workloads.make(args.workload, device=dev, **over)
     L, P = wl.dims["num_layers"], wl.dims["num_pairs"]
+    kv_scale = None
+    if args.kv == "fp8":
+        wl.kv_pool, kv_scale = workloads.make_fp8_pool(wl)
     stream = torch.cuda.Stream(device=dev)
     out = torch.empty_like(wl.q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -289,9 +295,14 @@ def run_ours(args) -> dict:
     ptrs = [V(t.data_ptr()) if t is not None else None for t in
             (wl.q, wl.k_new, wl.v_new, wl.kv_pool, wl.item_ids, wl.block_table, wl.pos_offset, out)]
     sh = V(stream.cuda_stream)
+    if kv_scale is not None:  # fp8 entry point: the scales follow the pool pointer
+        fwd = lib.gist_attn_fwd_fp8kv
+        ptrs = ptrs[:4] + [V(kv_scale.data_ptr())] + ptrs[4:]
+    else:
+        fwd = lib.gist_attn_fwd
 
     def launch(li):
-        rc = lib.gist_attn_fwd(*ptrs, ctypes.byref(dims_by_layer[li]), sh)
+        rc = fwd(*ptrs, ctypes.byref(dims_by_layer[li]), sh)
         if rc != 0:
             raise binding.GistAttnError(rc, binding.status_string(rc))
 
@@ -338,7 +349,7 @@ def run_ours(args) -> dict:
     elapsed_ms = max_over_ranks(elapsed_ms, ws)
     avg_launch_ms = max_over_ranks(sum(launch_ms) / len(launch_ms), ws)
 
-    bytes_info = algorithmic_bytes_per_launch(wl)
+    bytes_info = algorithmic_bytes_per_launch(wl, 1 if kv_scale is not None else 2)
     peak, peak_src = measured_peaks()
     achieved = bytes_info["total"] / (avg_launch_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
@@ -348,7 +359,9 @@ def run_ours(args) -> dict:
         "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16; ids per the workload recipe)",
-        "config": {"workload": DESCR[args.workload], "pairs": P, "layers_per_step": L,
+        "config": {"workload": DESCR[args.workload] + ("; E4M3 KV pool, fp32 scale per block-head"
+                                                       if kv_scale is not None else ""),
+                   "pairs": P, "layers_per_step": L,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "inputs larger than L2 (no flush needed)"},
         "roofline": {"kernel": KERNEL_OF[args.workload][0],
@@ -363,7 +376,7 @@ def run_ours(args) -> dict:
         "impl": "ours",
     }
 
-    if not args.no_e2e:
+    if not args.no_e2e and kv_scale is None:
         res["e2e"] = run_e2e(args, wl, lib, ptrs, dims_by_layer, stream, ws)
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
         res["cpu_baseline"] = oracle_rate(wl, 0, args.cpu_seconds)

@@ -111,6 +111,25 @@ int gist_attn_fwd(const void* q, const void* k_new, const void* v_new, const voi
                   void* out, const gist_attn_dims* dims, cudaStream_t stream);
 
 /*
+ * gist_attn_fwd_fp8kv -- gist_attn_fwd with the cached segment stored as FP8
+ * E4M3 bytes ([Suffix page, §2 and the end of §5]: a 1-byte-per-element KV
+ * cache).  The pages give no scale convention; here each (block, layer, K|V,
+ * KV head) has one fp32 scale and a cached value is e4m3 * scale.
+ *   kv_pool_e4m3 uint8 [num_blocks][L][2][Hkv][block_len][d] (same layout as the
+ *                bf16 pool, one byte per element), 16-byte aligned
+ *   kv_scale     float [num_blocks][L][2][Hkv], 4-byte aligned
+ * Other arguments as gist_attn_fwd.  This build runs the decode step (l = 1) with
+ * equal query and KV head counts, a cache of at least 64 rows and blocks of a
+ * multiple of 16 rows (the paged layout); other shapes return
+ * GIST_ATTN_ERR_UNSUPPORTED.
+ */
+int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void* v_new,
+                        const void* kv_pool_e4m3, const float* kv_scale,
+                        const int32_t* item_ids, const int32_t* block_table,
+                        const int32_t* pos_offset, void* out, const gist_attn_dims* dims,
+                        cudaStream_t stream);
+
+/*
  * gist_attn_gather_debug -- copies, bit for bit, the cached rows each pair
  * reads, through the same device gather routine the attention kernels use
  * ([Gist page, "在线的一次 attention"]: cache[item].K[layer], .V[layer]).

@@ -73,6 +73,11 @@ def _load(plant: int = 0):
                 fn.restype = ctypes.c_int
                 fn.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int32, P, P,
                                ctypes.POINTER(OraDims), ctypes.c_int32]
+            lib.ora_gist_attn_fp8kv.restype = ctypes.c_int
+            lib.ora_gist_attn_fp8kv.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_int32, P, P,
+                                                ctypes.POINTER(OraDims), ctypes.c_int32]
+            lib.ora_e4m3_to_f64.restype = ctypes.c_double
+            lib.ora_e4m3_to_f64.argtypes = [ctypes.c_uint8]
             lib.ora_gather.restype = ctypes.c_int
             lib.ora_gather.argtypes = [P, P, P, P, ctypes.POINTER(OraDims)]
             lib.ora_rope.restype = None
@@ -165,6 +170,43 @@ def gist_attn(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, pos_off
     if rc != 0:
         raise ValueError(f"oracle rejected the inputs (code {rc})")
     return (out, w) if want_weights else out
+
+
+def u8(x) -> np.ndarray:
+    """E4M3 bytes as a contiguous uint8 array (torch float8/uint8 tensor or numpy)."""
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.uint8)
+    import torch
+    return np.ascontiguousarray(x.detach().contiguous().cpu().view(torch.uint8).numpy())
+
+
+def gist_attn_fp8kv(q, k_new, v_new, kv_pool_e4m3, kv_scale, item_ids=None, block_table=None,
+                    pos_offset=None, *, dims: dict, pairs=None, num_threads: int | None = None):
+    """Attention with the cached segment stored as E4M3 bytes times one fp32 scale per
+    (block, layer, K|V, KV head); float64 output [n][l][Hq][d]."""
+    lib = _load()
+    D = make_dims(**dims)
+    qb, kb, vb = bf16_bits(q), bf16_bits(k_new), bf16_bits(v_new)
+    pb = u8(kv_pool_e4m3) if kv_pool_e4m3 is not None else None
+    sc = None
+    if kv_scale is not None:
+        sc = kv_scale if isinstance(kv_scale, np.ndarray) else kv_scale.detach().cpu().numpy()
+        sc = np.ascontiguousarray(sc, dtype=np.float32)
+    ids, tab, pos, sel = _i32(item_ids), _i32(block_table), _i32(pos_offset), _i32(pairs)
+    n = D.num_pairs if sel is None else int(sel.shape[0])
+    out = np.zeros((n, D.n_new, D.num_q_heads, D.head_dim), dtype=np.float64)
+    if num_threads is None:
+        num_threads = len(os.sched_getaffinity(0))
+    rc = lib.ora_gist_attn_fp8kv(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pb), _ptr(sc), _ptr(ids),
+                                 _ptr(tab), _ptr(pos), _ptr(sel), n, _ptr(out), None,
+                                 ctypes.byref(D), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the inputs (code {rc})")
+    return out
+
+
+def e4m3_to_f64(byte: int) -> float:
+    return float(_load().ora_e4m3_to_f64(int(byte)))
 
 
 def gather(kv_pool, item_ids=None, block_table=None, *, dims: dict):

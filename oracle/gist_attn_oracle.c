@@ -74,6 +74,19 @@ double ora_bf16_to_f64(uint16_t b) {
   return (double)f;
 }
 
+/* FP8 E4M3 (the "fn" variant: no infinities) widened exactly to double:
+ * sign s, 4-bit exponent e (bias 7), 3-bit mantissa m.  e = 0 is subnormal,
+ * (m / 8) * 2^-6; e = 15 with m = 7 is NaN; otherwise (1 + m / 8) * 2^(e - 7).
+ * [Suffix page, §2 and the end of §5]: a KV cache of 1-byte elements. */
+double ora_e4m3_to_f64(uint8_t v) {
+  const int sgn = v >> 7, e = (v >> 3) & 15, m = v & 7;
+  double x;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) x = ldexp((double)m / 8.0, -6);
+  else x = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sgn ? -x : x;
+}
+
 /* RoPE, rotate-half form: for j < d/2 the pair (x[j], x[j+d/2]) is turned by
  * the angle pos * theta^(-2j/d).  Only position differences survive in the
  * dot product q.k ([Gist page, "在线的一次 attention"], second remark). */
@@ -135,6 +148,8 @@ typedef struct {
   const ora_dims* D;
   int f64_inputs;        /* 0: q/k_new/v_new/pool are bf16 bit patterns; 1: doubles */
   const void *q, *k_new, *v_new, *pool;
+  const float* kv_scale; /* non-NULL: pool holds E4M3 bytes, one scale per
+                            (block, layer, K|V, KV head); value = e4m3 * scale */
   const int32_t *item_ids, *block_table, *pos_offset;
   const int32_t* pairs; /* which pairs to compute; NULL = all */
   int32_t n_pairs_out;
@@ -148,6 +163,17 @@ typedef struct {
 static double elem(const ora_job* J, const void* a, size_t idx) {
   if (J->f64_inputs) return ((const double*)a)[idx];
   return ora_bf16_to_f64(((const uint16_t*)a)[idx]);
+}
+
+/* Cached element e of row t of (block, layer, kv, KV head g). */
+static double pool_elem(const ora_job* J, int blk, int kv, int g, int t, int e) {
+  const ora_dims* D = J->D;
+  size_t idx = off_pool(D, blk, kv, g, t) + e;
+  if (J->kv_scale) {
+    size_t sidx = (((size_t)blk * D->num_layers + D->layer) * 2 + kv) * D->num_kv_heads + g;
+    return ora_e4m3_to_f64(((const uint8_t*)J->pool)[idx]) * (double)J->kv_scale[sidx];
+  }
+  return elem(J, J->pool, idx);
 }
 
 static int32_t block_of(const ora_job* J, int p, int b) {
@@ -190,8 +216,8 @@ static int attend_pair(const ora_job* J, int p, double* out_p, double* w_p) {
       for (int t = 0; t < D->block_len; ++t) {
         int kappa = b * D->block_len + t;
         for (int e = 0; e < d; ++e) {
-          keys[(size_t)kappa * d + e] = elem(J, J->pool, off_pool(D, blk, 0, g, t) + e);
-          vals[(size_t)kappa * d + e] = elem(J, J->pool, off_pool(D, blk, 1, g, t) + e);
+          keys[(size_t)kappa * d + e] = pool_elem(J, blk, 0, g, t, e);
+          vals[(size_t)kappa * d + e] = pool_elem(J, blk, 1, g, t, e);
         }
       }
     }
@@ -287,7 +313,8 @@ static int dims_ok(const ora_dims* D) {
  * Returns 0, or a negative code (bad argument, block id out of range, no memory).
  */
 static int run_attn(int f64_inputs, const void* q, const void* k_new, const void* v_new,
-                    const void* pool, const int32_t* item_ids, const int32_t* block_table,
+                    const void* pool, const float* kv_scale, const int32_t* item_ids,
+                    const int32_t* block_table,
                     const int32_t* pos_offset, const int32_t* pairs, int32_t n_pairs_out,
                     double* out, double* weights, const ora_dims* D, int32_t num_threads) {
   if (!dims_ok(D) || !out) return ORA_BAD_ARG;
@@ -305,7 +332,7 @@ static int run_attn(int f64_inputs, const void* q, const void* k_new, const void
   if (!jobs || !th) { free(jobs); free(th); return ORA_NO_MEM; }
   for (int t = 0; t < num_threads; ++t) {
     ora_job* J = &jobs[t];
-    J->D = D; J->f64_inputs = f64_inputs; J->q = q; J->k_new = k_new; J->v_new = v_new; J->pool = pool;
+    J->D = D; J->f64_inputs = f64_inputs; J->kv_scale = kv_scale; J->q = q; J->k_new = k_new; J->v_new = v_new; J->pool = pool;
     J->item_ids = item_ids; J->block_table = block_table; J->pos_offset = pos_offset;
     J->pairs = pairs; J->n_pairs_out = n_pairs_out; J->out = out; J->weights = weights;
     J->first = (int32_t)((int64_t)n_pairs_out * t / num_threads);
@@ -333,7 +360,20 @@ int ora_gist_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_ne
                   const uint16_t* pool, const int32_t* item_ids, const int32_t* block_table,
                   const int32_t* pos_offset, const int32_t* pairs, int32_t n_pairs_out,
                   double* out, double* weights, const ora_dims* D, int32_t num_threads) {
-  return run_attn(0, q, k_new, v_new, pool, item_ids, block_table, pos_offset, pairs,
+  return run_attn(0, q, k_new, v_new, pool, NULL, item_ids, block_table, pos_offset, pairs,
+                  n_pairs_out, out, weights, D, num_threads);
+}
+
+/* The same computation with the cached segment stored as E4M3 bytes and one
+ * fp32 scale per (block, layer, K|V, KV head), kv_scale[num_blocks][L][2][Hkv];
+ * q, k_new, v_new stay bf16. */
+int ora_gist_attn_fp8kv(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                        const uint8_t* pool, const float* kv_scale, const int32_t* item_ids,
+                        const int32_t* block_table, const int32_t* pos_offset,
+                        const int32_t* pairs, int32_t n_pairs_out, double* out, double* weights,
+                        const ora_dims* D, int32_t num_threads) {
+  if (!kv_scale && D && D->blocks_per_pair * D->block_len > 0) return ORA_BAD_ARG;
+  return run_attn(0, q, k_new, v_new, pool, kv_scale, item_ids, block_table, pos_offset, pairs,
                   n_pairs_out, out, weights, D, num_threads);
 }
 
@@ -343,7 +383,7 @@ int ora_gist_attn_f64(const double* q, const double* k_new, const double* v_new,
                       const double* pool, const int32_t* item_ids, const int32_t* block_table,
                       const int32_t* pos_offset, const int32_t* pairs, int32_t n_pairs_out,
                       double* out, double* weights, const ora_dims* D, int32_t num_threads) {
-  return run_attn(1, q, k_new, v_new, pool, item_ids, block_table, pos_offset, pairs,
+  return run_attn(1, q, k_new, v_new, pool, NULL, item_ids, block_table, pos_offset, pairs,
                   n_pairs_out, out, weights, D, num_threads);
 }
 

@@ -63,3 +63,24 @@ def compare(got: torch.Tensor, ref: np.ndarray, what: str = ""):
         raise AssertionError(f"{what}: |d|={err[i]:.3e} > bound {bound[i]:.3e} at {i} "
                              f"(got {g[i]:.5f}, ref {ref[i]:.5f}); max|d|={err.max():.3e}")
     return worst
+
+
+def oracle_ref_fp8(wl, pool8, scale, layer=0, pairs=None):
+    """Oracle output for an E4M3 pool, copying only the selected pairs' blocks."""
+    P = wl.dims["num_pairs"]
+    sel = np.arange(P) if pairs is None else np.asarray(pairs)
+    idx = torch.from_numpy(sel).to(wl.q.device)
+    src = wl.block_table if wl.block_table is not None else wl.item_ids.view(-1, 1)
+    blocks = src.index_select(0, idx).cpu().numpy()
+    uniq, inv = np.unique(blocks, return_inverse=True)
+    inv = inv.reshape(blocks.shape).astype(np.int32)
+    u = torch.from_numpy(uniq).to(wl.q.device).long()
+    p8 = pool8.view(torch.uint8)[:, layer].index_select(0, u).unsqueeze(1).contiguous()
+    sc = scale[:, layer].index_select(0, u).unsqueeze(1).contiguous()
+    dims = dict(wl.dims, num_pairs=len(sel), num_layers=1, layer=0, num_blocks=len(uniq))
+    table = inv if wl.block_table is not None else None
+    ids = None if wl.block_table is not None else inv[:, 0].copy()
+    pos = None if wl.pos_offset is None else wl.pos_offset.index_select(0, idx)
+    return oracle.gist_attn_fp8kv(wl.q.index_select(0, idx), wl.k_new.index_select(0, idx),
+                                  wl.v_new.index_select(0, idx), p8, sc, item_ids=ids,
+                                  block_table=table, pos_offset=pos, dims=dims)

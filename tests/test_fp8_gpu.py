@@ -1,0 +1,69 @@
+"""GPU parity of the E4M3 (fp8) KV pool path against the fp64 oracle, which
+dequantises every cached element exactly (e4m3 value times its block's scale)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from attention_cached_kv_gb300 import binding, workloads
+from parity_utils import compare, oracle_ref_fp8
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load_library()
+    yield
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("d,bl,bpp,random_pos", [(128, 256, 2, False), (64, 16, 5, True),
+                                                 (128, 32, 3, True), (64, 64, 1, False)])
+def test_fp8_decode_every_sequence(d, bl, bpp, random_pos):
+    wl = workloads.make_custom(6, 1, 8, 8, d, bl, bpp, 9, num_layers=3, layer=2, device=DEV,
+                               seed=bl + bpp, random_pos=random_pos, use_table=True)
+    pool8, scale = workloads.make_fp8_pool(wl, seed=bl)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, None, wl.block_table,
+                                      wl.pos_offset, dims=dict(wl.dims, layer=2), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(got, oracle_ref_fp8(wl, pool8, scale, layer=2), f"fp8 d={d} bl={bl}")
+
+
+def test_fp8_paged_workload_sampled():
+    wl = workloads.make("paged", device=DEV, num_layers=4)
+    pool8, scale = workloads.make_fp8_pool(wl)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, None, wl.block_table,
+                                      None, dims=dict(wl.dims, layer=3))
+    sel = np.arange(0, 32, 3)
+    compare(got[torch.from_numpy(sel).to(DEV)], oracle_ref_fp8(wl, pool8, scale, layer=3, pairs=sel),
+            "fp8 paged")
+
+
+def test_fp8_unsupported_shapes_are_refused():
+    wl = workloads.make_custom(2, 4, 8, 2, 64, 8, 1, 3, device=DEV)
+    pool8, scale = workloads.make_fp8_pool(wl)
+    with pytest.raises(binding.GistAttnError) as e:
+        binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, wl.item_ids, None, None,
+                                    dims=wl.dims)
+    assert e.value.code == binding.ERR_UNSUPPORTED
+
+
+def test_fp8_bad_block_zeroes_and_flags():
+    wl = workloads.make_custom(4, 1, 8, 8, 128, 32, 3, 6, device=DEV, seed=2, use_table=True)
+    pool8, scale = workloads.make_fp8_pool(wl)
+    wl.block_table[1, 2] = 99
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, None, wl.block_table,
+                                      None, dims=wl.dims, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & binding.STATUS_BAD_BLOCK
+    assert not got[1].float().abs().any()
+    ok = np.array([0, 2, 3])
+    compare(got[torch.from_numpy(ok).to(DEV)], oracle_ref_fp8(wl, pool8, scale, pairs=ok), "fp8 good")

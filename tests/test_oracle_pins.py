@@ -523,3 +523,50 @@ def test_flop_share_and_traffic_figures(golden):
 def test_planted_mistake_is_caught(plant):
     failures = [c.__name__ for c in ALL_CHECKS if c(plant=plant) is not None]
     assert failures, f"planted mistake {plant} slipped through every pin"
+
+
+# ------------------------------------------------- the fp8 (E4M3) KV pool ---
+
+def test_e4m3_decoder_all_256_patterns():
+    """Suffix page §2 / end of §5 (1-byte KV elements): the oracle's E4M3 decoder
+    against torch's float8_e4m3fn conversion, every bit pattern."""
+    pats = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = pats.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(b) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert oracle.e4m3_to_f64(0x38) == 1.0 and oracle.e4m3_to_f64(0x7E) == 448.0
+    assert oracle.e4m3_to_f64(0x01) == 2.0 ** -9
+
+
+def _fp8_case(seed, P=3, l=1, Hq=4, Hkv=4, d=32, bl=16, bpp=3, nb=7, L=2, layer=1, pow2=False):
+    g = torch.Generator().manual_seed(seed)
+    pool8 = torch.randn((nb, L, 2, Hkv, bl, d), generator=g).to(torch.float8_e4m3fn)
+    if pow2:
+        scale = 2.0 ** torch.randint(-3, 4, (nb, L, 2, Hkv), generator=g).to(torch.float32)
+    else:
+        scale = torch.rand((nb, L, 2, Hkv), generator=g, dtype=torch.float32) * 1.5 + 0.25
+    q, kn, vn = bf16((P, l, Hq, d), seed + 1), bf16((P, l, Hkv, d), seed + 2), bf16((P, l, Hkv, d), seed + 3)
+    table = np.random.default_rng(seed).integers(0, nb, size=(P, bpp)).astype(np.int32)
+    D = dims(P, l, Hq, Hkv, d, bl, bpp, nb, L, layer)
+    deq = pool8.to(torch.float64) * scale.to(torch.float64)[..., None, None]
+    return q, kn, vn, pool8, scale, deq, table, D
+
+
+def test_fp8_pool_equals_f64_oracle_on_dequantised_pool():
+    q, kn, vn, pool8, scale, deq, table, D = _fp8_case(40)
+    got = oracle.gist_attn_fp8kv(q, kn, vn, pool8, scale, block_table=table, dims=D)
+    ref = oracle.gist_attn(f64(q), f64(kn), f64(vn), deq.numpy(), block_table=table, dims=D,
+                           f64_inputs=True)
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_pool_with_power_of_two_scales_equals_bf16_path():
+    """E4M3 values times powers of two are exact bf16 values: both paths agree."""
+    q, kn, vn, pool8, scale, deq, table, D = _fp8_case(41, l=3, Hq=6, Hkv=2, pow2=True)
+    got = oracle.gist_attn_fp8kv(q, kn, vn, pool8, scale, block_table=table, dims=D)
+    pool_bf16 = deq.to(torch.bfloat16)
+    assert torch.equal(pool_bf16.to(torch.float64), deq)
+    ref = oracle.gist_attn(q, kn, vn, pool_bf16, block_table=table, dims=D)
+    assert np.array_equal(got, ref)
