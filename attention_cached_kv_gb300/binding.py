@@ -19,8 +19,9 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libgistattn.so")
 OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH = 0, -1, -2, -3, -4, -5
 STATUS_BAD_BLOCK, STATUS_TIMEOUT = 1, 2
 
-EXPORTS = ("gist_attn_fwd", "gist_attn_fwd_fp8kv", "gist_attn_gather_debug", "gist_kv_bytes_per_position",
-           "gist_kv_bytes_per_item", "gist_kv_bytes_batch", "gist_attn_status_string")
+EXPORTS = ("gist_attn_fwd", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
+           "gist_attn_gather_debug", "gist_kv_bytes_per_position", "gist_kv_bytes_per_item",
+           "gist_kv_bytes_batch", "gist_attn_status_string")
 
 
 class GistAttnError(RuntimeError):
@@ -67,6 +68,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.gist_attn_fwd.argtypes = [V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_attn_fwd_fp8kv.restype = ctypes.c_int
             lib.gist_attn_fwd_fp8kv.argtypes = [V, V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
+            lib.gist_attn_fwd_block_mass.restype = ctypes.c_int
+            lib.gist_attn_fwd_block_mass.argtypes = [V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
+            lib.gist_kv_append.restype = ctypes.c_int
+            lib.gist_kv_append.argtypes = [V, V, V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_attn_gather_debug.restype = ctypes.c_int
             lib.gist_attn_gather_debug.argtypes = [V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_kv_bytes_per_position.restype = ctypes.c_size_t
@@ -166,6 +171,39 @@ def gist_attn_fwd_fp8kv(q, k_new, v_new, kv_pool_e4m3, kv_scale, item_ids=None, 
                                  ctypes.byref(D), _stream(stream))
     _raise(rc)
     return out
+
+
+def gist_attn_fwd_block_mass(q, k_new, v_new, kv_pool, block_table, pos_offset=None, out=None,
+                             block_mass=None, *, dims: dict, status=None, stream=None):
+    """Decode step plus per-block attention mass [P][Hq][blocks_per_pair]; returns (out, mass)."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q)
+    if block_mass is None:
+        block_mass = torch.empty((dims["num_pairs"], dims["num_q_heads"], dims["blocks_per_pair"]),
+                                 dtype=torch.float32, device=q.device)
+    bf, i32 = torch.bfloat16, torch.int32
+    D = make_dims(dims, status)
+    rc = lib.gist_attn_fwd_block_mass(_ptr(q, bf, "q"), _ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"),
+                                      _ptr(kv_pool, bf, "kv_pool"), _ptr(block_table, i32, "block_table"),
+                                      _ptr(pos_offset, i32, "pos_offset"), _ptr(out, bf, "out"),
+                                      _ptr(block_mass, torch.float32, "block_mass"), ctypes.byref(D),
+                                      _stream(stream))
+    _raise(rc)
+    return out, block_mass
+
+
+def gist_kv_append(k_new, v_new, kv_pool, block_table, slot, pos_offset=None, *, dims: dict,
+                   status=None, stream=None):
+    """Writes the new token's rotated K and its V into kv_pool (in place)."""
+    lib = load_library()
+    bf, i32 = torch.bfloat16, torch.int32
+    D = make_dims(dims, status)
+    rc = lib.gist_kv_append(_ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"), _ptr(kv_pool, bf, "kv_pool"),
+                            _ptr(block_table, i32, "block_table"), _ptr(slot, i32, "slot"),
+                            _ptr(pos_offset, i32, "pos_offset"), ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return kv_pool
 
 
 def gist_attn_gather_debug(kv_pool, item_ids=None, block_table=None, dst=None, *, dims: dict,

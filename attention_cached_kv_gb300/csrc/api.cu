@@ -157,6 +157,55 @@ extern "C" int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void*
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 
+extern "C" int gist_attn_fwd_block_mass(const void* q, const void* k_new, const void* v_new,
+                                        const void* kv_pool, const int32_t* block_table,
+                                        const int32_t* pos_offset, void* out, float* block_mass,
+                                        const gist_attn_dims* dims, cudaStream_t stream) {
+  Problem pb{};
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (pb.P == 0) return GIST_ATTN_OK;
+  if (!q || !k_new || !v_new || !out || !block_mass || !kv_pool || !block_table)
+    return GIST_ATTN_ERR_NULL;
+  rc = gattn::check_cache_args(pb, kv_pool, nullptr, block_table);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (!gattn::aligned(q, 16) || !gattn::aligned(k_new, 16) || !gattn::aligned(v_new, 16) ||
+      !gattn::aligned(out, 16) || !gattn::aligned(pos_offset, 4) ||
+      !gattn::aligned(pb.status, 4) || !gattn::aligned(block_mass, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  pb.q = q;
+  pb.k_new = k_new;
+  pb.v_new = v_new;
+  pb.kv_pool = kv_pool;
+  pb.block_table = block_table;
+  pb.pos_offset = pos_offset;
+  pb.out = out;
+  if (pb.C > 0 && gattn::decode_long_stats_fits(pb))
+    return gattn::launch_decode_long_stats(pb, block_mass, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+extern "C" int gist_kv_append(const void* k_new, const void* v_new, void* kv_pool,
+                              const int32_t* block_table, const int32_t* slot,
+                              const int32_t* pos_offset, const gist_attn_dims* dims,
+                              cudaStream_t stream) {
+  Problem pb{};
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (pb.P == 0) return GIST_ATTN_OK;
+  if (pb.l != 1 || pb.C == 0) return GIST_ATTN_ERR_DIMS;
+  if (!k_new || !v_new || !kv_pool || !block_table || !slot) return GIST_ATTN_ERR_NULL;
+  if (!gattn::aligned(k_new, 16) || !gattn::aligned(v_new, 16) || !gattn::aligned(kv_pool, 16) ||
+      !gattn::aligned(block_table, 4) || !gattn::aligned(slot, 4) ||
+      !gattn::aligned(pos_offset, 4) || !gattn::aligned(pb.status, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  pb.k_new = k_new;
+  pb.v_new = v_new;
+  pb.block_table = block_table;
+  pb.pos_offset = pos_offset;
+  return gattn::launch_append(pb, kv_pool, slot, stream);
+}
+
 extern "C" int gist_attn_gather_debug(const void* kv_pool, const int32_t* item_ids,
                                       const int32_t* block_table, void* dst,
                                       const gist_attn_dims* dims, cudaStream_t stream) {

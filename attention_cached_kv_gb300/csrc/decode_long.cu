@@ -22,6 +22,12 @@
 // chunks are half as many bytes, widened in registers (e4m3 -> f16x2 -> f32),
 // the K scale multiplies the logit and the V scale the value weight.
 //
+// With STATS it also writes, per (sequence, head, cached block), the block's
+// attention mass -- the sum of the softmax weights of its rows -- the statistic
+// the eviction of [Suffix page, §5 第三步] aggregates every 64 generated tokens.
+// Each warp records log2 of its share of every chunk against its running max;
+// the shares are brought to the final max and normaliser at the end.
+//
 // Pages: [Suffix page] icman.com.cn news 64898;
 //        [KV page] "为什么自回归推理缓存 KV，而不缓存历史 Q？".
 #include <math.h>
@@ -39,9 +45,11 @@ constexpr int kWarps = 4;
 constexpr int kChunk = 16;  // keys per ring stage
 constexpr int kStagesBf16 = 3;  // ring depth; the fp8 ring has twice the stages (same bytes)
 constexpr int kMaxBlocks = 256;
+constexpr int kMaxStatChunks = 512;  // cached rows / 16 when block masses are requested
 
 struct LongParams {
   const float* kv_scale;  // FP8 pool: [num_blocks][L][2][Hkv], else unused
+  float* block_mass;      // STATS: [P][Hq][blocks_per_pair]
   const bf16* q;
   const bf16* k_new;
   const bf16* v_new;
@@ -69,8 +77,9 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v16) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_constant__ LongParams prm) {
+template <int D, bool FP8, bool STATS>
+__global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
+    decode_long_kernel(const __grid_constant__ LongParams prm) {
   constexpr int HALF = D / 2;
   constexpr int QE = D / 8;        // query elements per lane (8 lanes per key)
   constexpr int VE = D / 32;       // value columns per lane
@@ -86,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
   __shared__ float red_m[kWarps], red_l[kWarps];
   __shared__ float red_o[kWarps][D];
   __shared__ float kscale[FP8 ? kMaxBlocks : 1], vscale[FP8 ? kMaxBlocks : 1];
+  __shared__ float chunk_lg[STATS ? kMaxStatChunks : 1][kWarps];  // log2 of a warp's chunk share
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x % prm.Hkv, p = blockIdx.x / prm.Hkv;
@@ -129,6 +139,10 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
   bf16* out = prm.out + ((int64_t)p * prm.Hq + g) * D;
   if (bad) {
     for (int e = tid; e < D; e += kThreads) out[e] = __float2bfloat16(0.f);
+    if constexpr (STATS) {
+      float* mass = prm.block_mass + ((int64_t)p * prm.Hq + g) * prm.pv.blocks_per_pair;
+      for (int b = tid; b < prm.pv.blocks_per_pair; b += kThreads) mass[b] = 0.f;
+    }
     if (tid == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
     return;
   }
@@ -156,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
   float qr[QE];
 #pragma unroll
   for (int e = 0; e < QE; ++e) qr[e] = qs[sl * QE + e];
-  float m = kNegInf, lsum = 0.f, o[VE];
+  float m = kNegInf, lsum = 0.f, o[VE], last_share = kNegInf;
 #pragma unroll
   for (int e = 0; e < VE; ++e) o[e] = 0.f;
 
@@ -172,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
     float ps = pk + __shfl_xor_sync(0xffffffffu, pk, 8);
     ps += __shfl_xor_sync(0xffffffffu, ps, 16);
     lsum = lsum * al + ps;
+    last_share = ps > 0.f ? __log2f(ps) + mn : kNegInf;
 #pragma unroll
     for (int e = 0; e < VE; ++e) o[e] *= al;
 #pragma unroll
@@ -249,6 +264,9 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
       vsc = vscale[b];
     }
     consume(acc, true, stage + kChunk * kRow + warp * 4 * kRow, vsc);
+    if constexpr (STATS) {
+      if (lane == 0) chunk_lg[ci][warp] = last_share;
+    }
     __syncthreads();  // every warp is done with stage s
     if (tid == 0 && ci + kStages < n_chunks) issue(ci + kStages);
   }
@@ -289,13 +307,33 @@ __global__ void __launch_bounds__(kThreads, 7) decode_long_kernel(const __grid_c
     }
     out[e] = __float2bfloat16(num / den);
   }
+  if constexpr (STATS) {
+    // chunk share at the final max M, over the final normaliser L
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w]);
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) L += red_l[w] * ex2_approx(red_m[w] - M);
+    const float invL = 1.f / L;
+    const int cpb = bl / kChunk;  // chunks per block
+    float* mass = prm.block_mass + ((int64_t)p * prm.Hq + g) * prm.pv.blocks_per_pair;
+    for (int b = tid; b < prm.pv.blocks_per_pair; b += kThreads) {
+      float acc = 0.f;
+      for (int c = b * cpb; c < (b + 1) * cpb; ++c)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) acc += ex2_approx(chunk_lg[c][w] - M);
+      mass[b] = acc * invL;
+    }
+  }
   if (!ok && tid == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
 }
 
-template <int D, bool FP8>
-int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
+template <int D, bool FP8, bool STATS>
+int launch_d(const Problem& pb, const float* kv_scale, float* block_mass, cudaStream_t stream) {
   LongParams prm{};
   prm.kv_scale = kv_scale;
+  prm.block_mass = block_mass;
   prm.q = static_cast<const bf16*>(pb.q);
   prm.k_new = static_cast<const bf16*>(pb.k_new);
   prm.v_new = static_cast<const bf16*>(pb.v_new);
@@ -311,7 +349,7 @@ int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
   const int64_t grid = (int64_t)pb.P * pb.Hkv;
   if (grid > 0x7fffffff) return GIST_ATTN_ERR_UNSUPPORTED;
-  decode_long_kernel<D, FP8><<<(unsigned)grid, kThreads, 0, stream>>>(prm);
+  decode_long_kernel<D, FP8, STATS><<<(unsigned)grid, kThreads, 0, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
@@ -324,14 +362,24 @@ bool decode_long_fits(const Problem& pb) {
 }
 
 int launch_decode_long(const Problem& pb, cudaStream_t stream) {
-  if (pb.d == 64) return launch_d<64, false>(pb, nullptr, stream);
-  if (pb.d == 128) return launch_d<128, false>(pb, nullptr, stream);
+  if (pb.d == 64) return launch_d<64, false, false>(pb, nullptr, nullptr, stream);
+  if (pb.d == 128) return launch_d<128, false, false>(pb, nullptr, nullptr, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 
 int launch_decode_long_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
-  if (pb.d == 64) return launch_d<64, true>(pb, kv_scale, stream);
-  if (pb.d == 128) return launch_d<128, true>(pb, kv_scale, stream);
+  if (pb.d == 64) return launch_d<64, true, false>(pb, kv_scale, nullptr, stream);
+  if (pb.d == 128) return launch_d<128, true, false>(pb, kv_scale, nullptr, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+bool decode_long_stats_fits(const Problem& pb) {
+  return decode_long_fits(pb) && pb.C / kChunk <= kMaxStatChunks;
+}
+
+int launch_decode_long_stats(const Problem& pb, float* block_mass, cudaStream_t stream) {
+  if (pb.d == 64) return launch_d<64, false, true>(pb, nullptr, block_mass, stream);
+  if (pb.d == 128) return launch_d<128, false, true>(pb, nullptr, block_mass, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 

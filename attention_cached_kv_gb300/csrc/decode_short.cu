@@ -61,7 +61,6 @@ struct WarpRegion {  // per-warp shared memory, 128-byte swizzled rows
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_constant__ ShortParams prm) {
   using R = WarpRegion<D>;
-  constexpr int NP = D / 64;
   constexpr int CPR = D / 8;
   constexpr int HALF = D / 2;
   constexpr float kNegInf = -INFINITY;

@@ -42,6 +42,8 @@ int launch_decode_long(const Problem& pb, cudaStream_t stream);
 int launch_decode_long_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
 int launch_decode_short(const Problem& pb, cudaStream_t stream);
 int launch_gather(const Problem& pb, void* dst, cudaStream_t stream);
+int launch_decode_long_stats(const Problem& pb, float* block_mass, cudaStream_t stream);
+int launch_append(const Problem& pb, void* pool, const int32_t* slot, cudaStream_t stream);
 
 // Whether the prefill kernel can hold this problem's tiles in shared memory.
 bool prefill_fits(const Problem& pb);
@@ -49,5 +51,6 @@ bool prefill_tc_fits(const Problem& pb);
 bool decode_fits(const Problem& pb);
 bool decode_long_fits(const Problem& pb);
 bool decode_short_fits(const Problem& pb);
+bool decode_long_stats_fits(const Problem& pb);
 
 }  // namespace gattn

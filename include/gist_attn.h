@@ -130,6 +130,41 @@ int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void* v_new,
                         cudaStream_t stream);
 
 /*
+ * gist_attn_fwd_block_mass -- the decode step (l = 1) of gist_attn_fwd over a
+ * paged cache, also writing each cached block's attention mass, the statistic
+ * of the attention-aware eviction in [Suffix page, §4 and §5 第三步] (every 64
+ * generated tokens the caller averages the weights per history token and marks
+ * blocks below 0.3 x the mean; the policy itself is the caller's):
+ *   block_mass  float [P][Hq][blocks_per_pair]: the sum of head h's softmax
+ *               weights over the rows of the b-th block of p's table.  The new
+ *               token's own weight is 1 - sum_b block_mass[p][h][b].
+ * Other arguments as gist_attn_fwd (block_table required).  This build runs
+ * equal query and KV head counts, at least 64 cached rows, at most 8192, in
+ * blocks of a multiple of 16 rows; other shapes return GIST_ATTN_ERR_UNSUPPORTED.
+ */
+int gist_attn_fwd_block_mass(const void* q, const void* k_new, const void* v_new,
+                             const void* kv_pool, const int32_t* block_table,
+                             const int32_t* pos_offset, void* out, float* block_mass,
+                             const gist_attn_dims* dims, cudaStream_t stream);
+
+/*
+ * gist_kv_append -- writes one new token per sequence into the paged cache at
+ * `layer` ([KV page, "Reusable-state"]: K_{<=t} = [K_{<t}; k_t], the new K/V
+ * are appended to every layer's cache).  For sequence p and KV head g:
+ *   kv_pool[block_table[p][slot[p] / block_len]][layer][0][g][slot[p] % block_len]
+ *       = bf16(R(k_new[p][0][g]))  (RoPE at pos_offset[p], or at slot[p] when NULL;
+ *                                   rounded to nearest even)
+ *   ... [1][g][same row] = v_new[p][0][g]
+ *   k_new, v_new bf16 [P][1][Hkv][d]; slot int32 [P]; kv_pool is written.
+ * dims: n_new must be 1 and the table non-empty (GIST_ATTN_ERR_DIMS otherwise).
+ * A slot outside [0, blocks_per_pair * block_len) or an out-of-range block id
+ * skips that sequence and sets GIST_ATTN_STATUS_BAD_BLOCK.
+ */
+int gist_kv_append(const void* k_new, const void* v_new, void* kv_pool,
+                   const int32_t* block_table, const int32_t* slot, const int32_t* pos_offset,
+                   const gist_attn_dims* dims, cudaStream_t stream);
+
+/*
  * gist_attn_gather_debug -- copies, bit for bit, the cached rows each pair
  * reads, through the same device gather routine the attention kernels use
  * ([Gist page, "在线的一次 attention"]: cache[item].K[layer], .V[layer]).

@@ -78,6 +78,8 @@ def _load(plant: int = 0):
                                                 ctypes.POINTER(OraDims), ctypes.c_int32]
             lib.ora_e4m3_to_f64.restype = ctypes.c_double
             lib.ora_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.ora_kv_append.restype = ctypes.c_int
+            lib.ora_kv_append.argtypes = [P, P, P, P, P, P, ctypes.POINTER(OraDims)]
             lib.ora_gather.restype = ctypes.c_int
             lib.ora_gather.argtypes = [P, P, P, P, ctypes.POINTER(OraDims)]
             lib.ora_rope.restype = None
@@ -244,3 +246,25 @@ def kv_bytes_per_item(L, Hkv, d, k, b) -> int:
 
 def kv_bytes_batch(B, L, T, Hkv, d, b) -> int:
     return int(_load().ora_kv_bytes_batch(B, L, T, Hkv, d, b))
+
+
+def block_mass(weights: np.ndarray, blocks_per_pair: int, block_len: int) -> np.ndarray:
+    """Per-block attention mass of decode weights [n][1][Hq][C+1] -> [n][Hq][blocks]:
+    the sum of the softmax weights over each cached block's rows (the new token's
+    own key belongs to no block)."""
+    C = blocks_per_pair * block_len
+    w = weights[:, 0, :, :C].reshape(weights.shape[0], weights.shape[2], blocks_per_pair, block_len)
+    return w.sum(axis=-1)
+
+
+def kv_append(k_new, v_new, kv_pool, block_table, slot, pos_offset=None, *, dims: dict):
+    """A copy of the pool (uint16 bf16 bits) with each sequence's new K (rotated,
+    rounded to bf16) and V written at its slot; also the return code."""
+    lib = _load()
+    D = make_dims(**dims)
+    pool = bf16_bits(kv_pool).copy()
+    kb, vb = bf16_bits(k_new), bf16_bits(v_new)
+    tab, sl, pos = _i32(block_table), _i32(slot), _i32(pos_offset)
+    rc = lib.ora_kv_append(_ptr(kb), _ptr(vb), _ptr(pool), _ptr(tab), _ptr(sl), _ptr(pos),
+                           ctypes.byref(D))
+    return pool, rc

@@ -419,3 +419,65 @@ int ora_gather(const uint16_t* pool, const int32_t* item_ids, const int32_t* blo
   }
   return rc;
 }
+
+/*
+ * The decode step's append ([KV page, "Reusable-state"]: K_{<=t} = [K_{<t}; k_t],
+ * the new K/V are appended to every layer's cache): for each sequence p and KV
+ * head g, row slot[p] of the sequence's cache -- block block_table[p][slot /
+ * block_len], row slot % block_len, at `layer` -- receives k_new rotated at
+ * position pos_offset[p] (NULL: slot[p]) and rounded to bf16 (nearest even),
+ * and v_new unchanged.  The pool is bf16 bits [num_blocks][L][2][Hkv][block_len][d].
+ * Returns ORA_BAD_BLOCK (writing nothing for that sequence) on an out-of-range
+ * block id or slot.
+ */
+static uint16_t f64_to_bf16_rne(double v) {
+  float f = (float)v; /* exact enough: the bf16 rounding below decides */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)(u >> 16); /* inf / nan */
+  /* round the double directly: the nearest bf16 to v, ties to even */
+  double a = fabs(v);
+  if (a == 0.0) return (uint16_t)(signbit(v) ? 0x8000u : 0u);
+  int e;
+  frexp(a, &e);                    /* a = m * 2^e, m in [0.5, 1) */
+  int q = e - 8;                   /* bf16 keeps 8 significant bits */
+  if (q < -133) q = -133;          /* subnormal spacing 2^-133 */
+  double ulp = ldexp(1.0, q);
+  double n = a / ulp, fl = floor(n), r = n - fl;
+  if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+  float rf = (float)(fl * ulp);
+  memcpy(&u, &rf, sizeof u);
+  u >>= 16;
+  return (uint16_t)(signbit(v) ? (u | 0x8000u) : u);
+}
+
+int ora_kv_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* pool,
+                  const int32_t* block_table, const int32_t* slot, const int32_t* pos_offset,
+                  const ora_dims* D) {
+  if (!dims_ok(D) || !k_new || !v_new || !pool || !block_table || !slot) return ORA_BAD_ARG;
+  const int d = D->head_dim, Hkv = D->num_kv_heads;
+  double* x = malloc(sizeof(double) * (size_t)d);
+  double* y = malloc(sizeof(double) * (size_t)d);
+  if (!x || !y) { free(x); free(y); return ORA_NO_MEM; }
+  int rc = ORA_OK;
+  for (int p = 0; p < D->num_pairs; ++p) {
+    int s = slot[p];
+    if (s < 0 || s >= D->blocks_per_pair * D->block_len) { rc = ORA_BAD_BLOCK; continue; }
+    int32_t blk = block_table[(size_t)p * D->blocks_per_pair + s / D->block_len];
+    if (blk < 0 || blk >= D->num_blocks) { rc = ORA_BAD_BLOCK; continue; }
+    double pos = pos_offset ? (double)pos_offset[p] : (double)s;
+    for (int g = 0; g < Hkv; ++g) {
+      size_t src = ((size_t)p * Hkv + g) * d; /* one new token: [P][1][Hkv][d] */
+      for (int e = 0; e < d; ++e) x[e] = ora_bf16_to_f64(k_new[src + e]);
+      ora_rope(x, d, pos, D->rope_theta, y);
+      uint16_t* krow = pool + off_pool(D, blk, 0, g, s % D->block_len);
+      uint16_t* vrow = pool + off_pool(D, blk, 1, g, s % D->block_len);
+      for (int e = 0; e < d; ++e) {
+        krow[e] = f64_to_bf16_rne(y[e]);
+        vrow[e] = v_new[src + e];
+      }
+    }
+  }
+  free(x); free(y);
+  return rc;
+}

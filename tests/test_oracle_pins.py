@@ -570,3 +570,51 @@ def test_fp8_pool_with_power_of_two_scales_equals_bf16_path():
     assert torch.equal(pool_bf16.to(torch.float64), deq)
     ref = oracle.gist_attn(q, kn, vn, pool_bf16, block_table=table, dims=D)
     assert np.array_equal(got, ref)
+
+
+# ---------------------------------- block attention mass and the KV append ---
+
+def test_block_mass_closed_form_and_total():
+    """Suffix page §5 第三步 (attention per history block): with q = 0 every key
+    weighs 1/(C+1), so a block of bl rows weighs bl/(C+1); the masses plus the new
+    token's own weight sum to 1."""
+    P, Hq, d, bl, bpp, nb = 2, 3, 16, 4, 3, 5
+    kn, vn = bf16((P, 1, Hq, d), 50), bf16((P, 1, Hq, d), 51)
+    pool = bf16((nb, 1, 2, Hq, bl, d), 52)
+    table = np.array([[0, 3, 1], [4, 2, 2]], dtype=np.int32)
+    D = dims(P, 1, Hq, Hq, d, bl, bpp, nb)
+    _, w = oracle.gist_attn(torch.zeros((P, 1, Hq, d), dtype=torch.bfloat16), kn, vn, pool,
+                            block_table=table, dims=D, want_weights=True)
+    mass = oracle.block_mass(w, bpp, bl)
+    assert np.allclose(mass, bl / (bpp * bl + 1), rtol=0, atol=1e-15)
+    q = bf16((P, 1, Hq, d), 53)
+    _, w = oracle.gist_attn(q, kn, vn, pool, block_table=table, dims=D, want_weights=True)
+    mass = oracle.block_mass(w, bpp, bl)
+    assert np.allclose(mass.sum(-1) + w[:, 0, :, -1], 1.0, rtol=0, atol=1e-12)
+
+
+def test_kv_append_writes_rotated_key_and_value():
+    """KV page, Reusable-state: the new k_t (rotated at its position) and v_t join
+    the cache.  The key is checked against the complex-rotation RoPE rounded by
+    torch to bf16; the value bit for bit; nothing else changes."""
+    P, Hkv, d, bl, bpp, nb, L = 3, 2, 32, 8, 2, 6, 2
+    kn, vn = bf16((P, 1, Hkv, d), 60), bf16((P, 1, Hkv, d), 61)
+    pool = bf16((nb, L, 2, Hkv, bl, d), 62)
+    table = np.array([[1, 4], [0, 5], [3, 2]], dtype=np.int32)
+    slot = np.array([3, 8, 15], dtype=np.int32)
+    D = dims(P, 1, Hkv, Hkv, d, bl, bpp, nb, L=L, layer=1)
+    new, rc = oracle.kv_append(kn, vn, pool, table, slot, dims=D)
+    assert rc == 0
+    old = oracle.bf16_bits(pool)
+    changed = np.argwhere(np.any(new != old, axis=-1))
+    for p in range(P):
+        blk, t = table[p, slot[p] // bl], slot[p] % bl
+        for g in range(Hkv):
+            want_k = torch.from_numpy(rope_complex(f64(kn[p, 0, g]), slot[p])).to(torch.bfloat16)
+            assert np.array_equal(new[blk, 1, 0, g, t], oracle.bf16_bits(want_k))
+            assert np.array_equal(new[blk, 1, 1, g, t], oracle.bf16_bits(vn[p, 0, g]))
+    assert len({tuple(c[:3]) + (c[4],) for c in changed}) <= P * 2  # only the written rows
+    bad = slot.copy()
+    bad[1] = bpp * bl
+    _, rc = oracle.kv_append(kn, vn, pool, table, bad, dims=D)
+    assert rc == -2
