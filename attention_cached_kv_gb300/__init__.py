@@ -8,11 +8,12 @@ synthetic inputs.  The library is loaded on first use and every call fails
 loudly if it has not been built.
 """
 from .binding import (GistAttnError, STATUS_BAD_BLOCK, STATUS_TIMEOUT, gist_attn_fwd,
-                      gist_attn_fwd_block_mass, gist_attn_fwd_fp8kv, gist_kv_append,
+                      gist_attn_fwd_block_mass, gist_attn_fwd_fp8kv, gist_attn_fwd_gist_mask,
+                      gist_kv_append, gist_kv_store,
                       gist_attn_gather_debug, kv_bytes_batch, kv_bytes_per_item,
                       kv_bytes_per_position, load_library, status_string)
 
 __all__ = ["GistAttnError", "STATUS_BAD_BLOCK", "STATUS_TIMEOUT", "gist_attn_fwd", "gist_attn_fwd_fp8kv",
-           "gist_attn_fwd_block_mass", "gist_kv_append",
+           "gist_attn_fwd_block_mass", "gist_attn_fwd_gist_mask", "gist_kv_append", "gist_kv_store",
            "gist_attn_gather_debug", "kv_bytes_batch", "kv_bytes_per_item",
            "kv_bytes_per_position", "load_library", "status_string"]

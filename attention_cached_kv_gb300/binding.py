@@ -20,7 +20,7 @@ OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH = 0, -1, -2, -3, 
 STATUS_BAD_BLOCK, STATUS_TIMEOUT = 1, 2
 
 EXPORTS = ("gist_attn_fwd", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
-           "gist_attn_gather_debug", "gist_kv_bytes_per_position", "gist_kv_bytes_per_item",
+           "gist_attn_fwd_gist_mask", "gist_kv_store", "gist_attn_gather_debug", "gist_kv_bytes_per_position", "gist_kv_bytes_per_item",
            "gist_kv_bytes_batch", "gist_attn_status_string")
 
 
@@ -72,6 +72,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.gist_attn_fwd_block_mass.argtypes = [V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_kv_append.restype = ctypes.c_int
             lib.gist_kv_append.argtypes = [V, V, V, V, V, V, ctypes.POINTER(Dims), V]
+            lib.gist_attn_fwd_gist_mask.restype = ctypes.c_int
+            lib.gist_attn_fwd_gist_mask.argtypes = [V, V, V, V, V, V, V, V, ctypes.c_int, V,
+                                                    ctypes.POINTER(Dims), V]
+            lib.gist_kv_store.restype = ctypes.c_int
+            lib.gist_kv_store.argtypes = [V, V, V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_attn_gather_debug.restype = ctypes.c_int
             lib.gist_attn_gather_debug.argtypes = [V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_kv_bytes_per_position.restype = ctypes.c_size_t
@@ -202,6 +207,38 @@ def gist_kv_append(k_new, v_new, kv_pool, block_table, slot, pos_offset=None, *,
     rc = lib.gist_kv_append(_ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"), _ptr(kv_pool, bf, "kv_pool"),
                             _ptr(block_table, i32, "block_table"), _ptr(slot, i32, "slot"),
                             _ptr(pos_offset, i32, "pos_offset"), ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return kv_pool
+
+
+def gist_attn_fwd_gist_mask(q, k_new, v_new, kv_pool=None, item_ids=None, block_table=None,
+                            pos_offset=None, gist_start=None, gist_len: int = 0, out=None, *,
+                            dims: dict, status=None, stream=None):
+    """gist_attn_fwd under the gist mask (gist_start int32 [P] required); returns `out`."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q)
+    bf, i32 = torch.bfloat16, torch.int32
+    D = make_dims(dims, status)
+    rc = lib.gist_attn_fwd_gist_mask(_ptr(q, bf, "q"), _ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"),
+                                     _ptr(kv_pool, bf, "kv_pool"), _ptr(item_ids, i32, "item_ids"),
+                                     _ptr(block_table, i32, "block_table"),
+                                     _ptr(pos_offset, i32, "pos_offset"),
+                                     _ptr(gist_start, i32, "gist_start"), int(gist_len),
+                                     _ptr(out, bf, "out"), ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return out
+
+
+def gist_kv_store(k_new, v_new, kv_pool, item_ids, first_row, store_pos=None, *, dims: dict,
+                  status=None, stream=None):
+    """Writes each pair's k gist rows (K rotated, V copied) into kv_pool (in place)."""
+    lib = load_library()
+    bf, i32 = torch.bfloat16, torch.int32
+    D = make_dims(dims, status)
+    rc = lib.gist_kv_store(_ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"), _ptr(kv_pool, bf, "kv_pool"),
+                           _ptr(item_ids, i32, "item_ids"), _ptr(first_row, i32, "first_row"),
+                           _ptr(store_pos, i32, "store_pos"), ctypes.byref(D), _stream(stream))
     _raise(rc)
     return kv_pool
 

@@ -70,10 +70,11 @@ int check_dims(const gist_attn_dims* dm, Problem* pb) {
   pb->C = (int)C;
   const double scale = d.softmax_scale > 0.f ? (double)d.softmax_scale : 1.0 / sqrt((double)d.head_dim);
   pb->scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
-  for (int j = 0; j < 64; ++j)
-    pb->inv_freq[j] = j < d.head_dim / 2
-                          ? (float)pow((double)d.rope_theta, -2.0 * j / (double)d.head_dim)
-                          : 0.f;
+  for (int j = 0; j < 64; ++j) {
+    pb->inv_freq_d[j] =
+        j < d.head_dim / 2 ? pow((double)d.rope_theta, -2.0 * j / (double)d.head_dim) : 0.0;
+    pb->inv_freq[j] = (float)pb->inv_freq_d[j];
+  }
   return GIST_ATTN_OK;
 }
 
@@ -204,6 +205,59 @@ extern "C" int gist_kv_append(const void* k_new, const void* v_new, void* kv_poo
   pb.block_table = block_table;
   pb.pos_offset = pos_offset;
   return gattn::launch_append(pb, kv_pool, slot, stream);
+}
+
+extern "C" int gist_attn_fwd_gist_mask(const void* q, const void* k_new, const void* v_new,
+                                       const void* kv_pool, const int32_t* item_ids,
+                                       const int32_t* block_table, const int32_t* pos_offset,
+                                       const int32_t* gist_start, int gist_len, void* out,
+                                       const gist_attn_dims* dims, cudaStream_t stream) {
+  Problem pb{};
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (gist_len < 0) return GIST_ATTN_ERR_DIMS;
+  if (pb.P == 0) return GIST_ATTN_OK;
+  if (!q || !k_new || !v_new || !out || !gist_start) return GIST_ATTN_ERR_NULL;
+  rc = gattn::check_cache_args(pb, kv_pool, item_ids, block_table);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (!gattn::aligned(q, 16) || !gattn::aligned(k_new, 16) || !gattn::aligned(v_new, 16) ||
+      !gattn::aligned(out, 16) || !gattn::aligned(pos_offset, 4) ||
+      !gattn::aligned(gist_start, 4) || !gattn::aligned(pb.status, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  pb.q = q;
+  pb.k_new = k_new;
+  pb.v_new = v_new;
+  pb.kv_pool = pb.C > 0 ? kv_pool : nullptr;
+  pb.item_ids = pb.C > 0 ? item_ids : nullptr;
+  pb.block_table = pb.C > 0 ? block_table : nullptr;
+  pb.pos_offset = pos_offset;
+  pb.out = out;
+  pb.gist_start = gist_start;
+  pb.gist_len = gist_len;
+  if (pb.C == 0) pb.blocks_per_pair = 0;
+  if (!gattn::prefill_fits(pb)) return GIST_ATTN_ERR_UNSUPPORTED;
+  return gattn::launch_prefill(pb, stream);
+}
+
+extern "C" int gist_kv_store(const void* k_new, const void* v_new, void* kv_pool,
+                             const int32_t* item_ids, const int32_t* first_row,
+                             const int32_t* store_pos, const gist_attn_dims* dims,
+                             cudaStream_t stream) {
+  Problem pb{};
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (pb.P == 0) return GIST_ATTN_OK;
+  if (pb.blocks_per_pair != 1 || pb.block_len < 1 || pb.block_len > pb.l)
+    return GIST_ATTN_ERR_DIMS;
+  if (!k_new || !v_new || !kv_pool || !item_ids || !first_row) return GIST_ATTN_ERR_NULL;
+  if (!gattn::aligned(k_new, 16) || !gattn::aligned(v_new, 16) || !gattn::aligned(kv_pool, 16) ||
+      !gattn::aligned(item_ids, 4) || !gattn::aligned(first_row, 4) ||
+      !gattn::aligned(store_pos, 4) || !gattn::aligned(pb.status, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  pb.k_new = k_new;
+  pb.v_new = v_new;
+  pb.item_ids = item_ids;
+  return gattn::launch_store(pb, kv_pool, first_row, store_pos, stream);
 }
 
 extern "C" int gist_attn_gather_debug(const void* kv_pool, const int32_t* item_ids,

@@ -23,8 +23,11 @@ struct Problem {
   int32_t* status;
   int P, l, Hq, Hkv, G, d, block_len, blocks_per_pair, num_blocks, L, layer;
   int C;             // cached keys per pair
+  const int32_t* gist_start;  // [P] or nullptr: the gist mask (streaming prefill only)
+  int gist_len;
   float scale_log2;  // softmax scale * log2(e)
   float inv_freq[64];  // rope_theta^(-2j/d), j < d/2
+  double inv_freq_d[64];  // the same in double (the pool writers rotate in double)
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -44,6 +47,8 @@ int launch_decode_short(const Problem& pb, cudaStream_t stream);
 int launch_gather(const Problem& pb, void* dst, cudaStream_t stream);
 int launch_decode_long_stats(const Problem& pb, float* block_mass, cudaStream_t stream);
 int launch_append(const Problem& pb, void* pool, const int32_t* slot, cudaStream_t stream);
+int launch_store(const Problem& pb, void* pool, const int32_t* first_row, const int32_t* store_pos,
+                 cudaStream_t stream);
 
 // Whether the prefill kernel can hold this problem's tiles in shared memory.
 bool prefill_fits(const Problem& pb);

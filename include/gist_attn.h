@@ -165,6 +165,51 @@ int gist_kv_append(const void* k_new, const void* v_new, void* kv_pool,
                    const gist_attn_dims* dims, cudaStream_t stream);
 
 /*
+ * gist_attn_fwd_gist_mask -- gist_attn_fwd under the gist mask of
+ * [Gist page, "论文做了什么"] (the ordinary causal mask with the block
+ * (tokens after the gist) x (tokens before it) removed).  Keys of pair p are
+ * numbered kappa = 0 .. C + l - 1 over [cached; new]; the prompt is
+ * kappa < gist_start[p], the gist the next gist_len keys.  A token whose own
+ * index C + i is at least gist_start[p] + gist_len sees only the keys
+ * gist_start[p] <= kappa <= C + i; every other token sees kappa <= C + i.
+ * With an empty cache and the new tokens [prompt; gist; rest] this is the
+ * training-layout forward of whole sequences (sequences of different lengths
+ * right-padded to l, their own gist_start each); over [prompt; gist] alone it is
+ * the plain causal pass of the offline compression ([Gist page, "在线的一次
+ * attention"]: the item is forwarded once, offline).
+ *   gist_start int32 [P], device, required; a negative value is taken as 0
+ *   gist_len   host int >= 0 (GIST_ATTN_ERR_DIMS otherwise)
+ * Other arguments as gist_attn_fwd.  Runs on the streaming kernel: any cache
+ * length and l; groups of at most 64 query heads per KV head, and at most 4096
+ * cached blocks per pair (GIST_ATTN_ERR_UNSUPPORTED otherwise).
+ */
+int gist_attn_fwd_gist_mask(const void* q, const void* k_new, const void* v_new,
+                            const void* kv_pool, const int32_t* item_ids,
+                            const int32_t* block_table, const int32_t* pos_offset,
+                            const int32_t* gist_start, int gist_len, void* out,
+                            const gist_attn_dims* dims, cudaStream_t stream);
+
+/*
+ * gist_kv_store -- writes compressed items into the pool ([Gist page,
+ * "论文做了什么"]: after the offline pass over [prompt; gist], each layer keeps
+ * the K/V at the k gist positions as the item's cache entry).  dims: n_new = l,
+ * the sequence length; block_len = k, the gist length (1 <= k <= l);
+ * blocks_per_pair = 1; num_blocks, num_layers, layer as usual (GIST_ATTN_ERR_DIMS
+ * otherwise).  For pair p, KV head g and t < k:
+ *   kv_pool[item_ids[p]][layer][0][g][t] = bf16(R(k_new[p][first_row[p] + t][g]))
+ *       (RoPE at store_pos[p] + t, or at t when store_pos is NULL, i.e. the
+ *        online layout where the query follows the gist; rounded to nearest even)
+ *   kv_pool[item_ids[p]][layer][1][g][t] = v_new[p][first_row[p] + t][g]
+ *   k_new, v_new bf16 [P][l][Hkv][d] (pre-RoPE keys, as gist_attn_fwd takes them)
+ *   item_ids, first_row int32 [P]; store_pos int32 [P] or NULL; kv_pool is written.
+ * A pair whose rows leave [0, l) or whose block id is out of range is skipped and
+ * sets GIST_ATTN_STATUS_BAD_BLOCK.  Two pairs naming the same block race.
+ */
+int gist_kv_store(const void* k_new, const void* v_new, void* kv_pool, const int32_t* item_ids,
+                  const int32_t* first_row, const int32_t* store_pos, const gist_attn_dims* dims,
+                  cudaStream_t stream);
+
+/*
  * gist_attn_gather_debug -- copies, bit for bit, the cached rows each pair
  * reads, through the same device gather routine the attention kernels use
  * ([Gist page, "在线的一次 attention"]: cache[item].K[layer], .V[layer]).

@@ -78,6 +78,12 @@ def _load(plant: int = 0):
                                                 ctypes.POINTER(OraDims), ctypes.c_int32]
             lib.ora_e4m3_to_f64.restype = ctypes.c_double
             lib.ora_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.ora_gist_attn_masked.restype = ctypes.c_int
+            lib.ora_gist_attn_masked.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int32, P,
+                                                 ctypes.c_int32, P, P, ctypes.POINTER(OraDims),
+                                                 ctypes.c_int32]
+            lib.ora_kv_store.restype = ctypes.c_int
+            lib.ora_kv_store.argtypes = [P, P, P, P, P, P, ctypes.POINTER(OraDims)]
             lib.ora_kv_append.restype = ctypes.c_int
             lib.ora_kv_append.argtypes = [P, P, P, P, P, P, ctypes.POINTER(OraDims)]
             lib.ora_gather.restype = ctypes.c_int
@@ -145,13 +151,15 @@ def _f64(x):
 
 def gist_attn(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, pos_offset=None, *,
               dims: dict, pairs=None, want_weights: bool = False, num_threads: int | None = None,
-              f64_inputs: bool = False, plant: int = 0):
+              f64_inputs: bool = False, plant: int = 0, gist_start=None, gist_len: int = 0):
     """Attention output in float64, shape [n][l][Hq][d] (n = len(pairs) or P).
 
     Inputs are bf16 (torch tensors or uint16 bit arrays) in the library's
     layouts; see gist_attn_oracle.c.  With ``f64_inputs`` they are float64
     arrays in the same layouts instead.  With want_weights the softmax weights
-    [n][l][Hq][C+l] (zeros where masked) are returned too.
+    [n][l][Hq][C+l] (zeros where masked) are returned too.  With ``gist_start``
+    ([P] ints) the gist mask applies: a token after keys
+    [gist_start, gist_start + gist_len) no longer sees the keys before them.
     """
     lib = _load(plant)
     D = make_dims(**dims)
@@ -166,9 +174,17 @@ def gist_attn(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, pos_off
          if want_weights else None)
     if num_threads is None:
         num_threads = len(os.sched_getaffinity(0))
-    fn = lib.ora_gist_attn_f64 if f64_inputs else lib.ora_gist_attn
-    rc = fn(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pb), _ptr(ids), _ptr(tab), _ptr(pos), _ptr(sel),
-            n, _ptr(out), _ptr(w), ctypes.byref(D), int(num_threads))
+    if gist_start is not None:
+        if f64_inputs:
+            raise ValueError("the gist mask takes bf16 inputs")
+        gs = _i32(gist_start)
+        rc = lib.ora_gist_attn_masked(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pb), _ptr(ids), _ptr(tab),
+                                      _ptr(pos), _ptr(gs), int(gist_len), _ptr(sel), n, _ptr(out),
+                                      _ptr(w), ctypes.byref(D), int(num_threads))
+    else:
+        fn = lib.ora_gist_attn_f64 if f64_inputs else lib.ora_gist_attn
+        rc = fn(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pb), _ptr(ids), _ptr(tab), _ptr(pos), _ptr(sel),
+                n, _ptr(out), _ptr(w), ctypes.byref(D), int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle rejected the inputs (code {rc})")
     return (out, w) if want_weights else out
@@ -267,4 +283,19 @@ def kv_append(k_new, v_new, kv_pool, block_table, slot, pos_offset=None, *, dims
     tab, sl, pos = _i32(block_table), _i32(slot), _i32(pos_offset)
     rc = lib.ora_kv_append(_ptr(kb), _ptr(vb), _ptr(pool), _ptr(tab), _ptr(sl), _ptr(pos),
                            ctypes.byref(D))
+    return pool, rc
+
+
+def kv_store(k_new, v_new, kv_pool, item_ids, first_row, store_pos=None, *, dims: dict):
+    """A copy of the pool (uint16 bf16 bits) with each pair's rows
+    first_row .. first_row + block_len - 1 stored as its item's cache entry at
+    dims["layer"] (K rotated at store_pos + t, default t, rounded to bf16; V
+    copied); also the return code."""
+    lib = _load()
+    D = make_dims(**dims)
+    pool = bf16_bits(kv_pool).copy()
+    kb, vb = bf16_bits(k_new), bf16_bits(v_new)
+    ids, fr, sp = _i32(item_ids), _i32(first_row), _i32(store_pos)
+    rc = lib.ora_kv_store(_ptr(kb), _ptr(vb), _ptr(pool), _ptr(ids), _ptr(fr), _ptr(sp),
+                          ctypes.byref(D))
     return pool, rc

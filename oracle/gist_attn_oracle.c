@@ -151,6 +151,8 @@ typedef struct {
   const float* kv_scale; /* non-NULL: pool holds E4M3 bytes, one scale per
                             (block, layer, K|V, KV head); value = e4m3 * scale */
   const int32_t *item_ids, *block_table, *pos_offset;
+  const int32_t* gist_start; /* NULL, or [P]: first prompt-free key of the gist mask */
+  int32_t gist_len;          /* k, the gist length of the gist mask              */
   const int32_t* pairs; /* which pairs to compute; NULL = all */
   int32_t n_pairs_out;
   double* out;          /* [n_pairs_out][l][Hq][d]                         */
@@ -244,28 +246,34 @@ static int attend_pair(const ora_job* J, int p, double* out_p, double* w_p) {
 #else
         int n = C + i + 1; /* every cached key, then new keys 0..i */
 #endif
+        /* [Gist page, "论文做了什么"]: under the gist mask a token after the
+         * gist (index C + i >= start + k) no longer sees the prompt before it. */
+        int lo = 0;
+#if ORA_PLANT != 9 /* gist mask ignored: post-gist tokens still see the prompt */
+        if (J->gist_start && C + i >= J->gist_start[p] + J->gist_len) lo = J->gist_start[p];
+#endif
         double m = -INFINITY;
-        for (int j = 0; j < n; ++j) {
+        for (int j = lo; j < n; ++j) {
           double acc = 0.0;
           for (int e = 0; e < d; ++e) acc += qr[e] * keys[(size_t)j * d + e];
           s[j] = scale * acc;
           if (s[j] > m) m = s[j];
         }
         double denom = 0.0;
-        for (int j = 0; j < n; ++j) { s[j] = exp(s[j] - m); denom += s[j]; }
+        for (int j = lo; j < n; ++j) { s[j] = exp(s[j] - m); denom += s[j]; }
         double* o = out_p + ((size_t)i * Hq + h) * d;
         for (int e = 0; e < d; ++e) {
           double acc = 0.0;
 #if ORA_PLANT == 8 /* keys used as values */
-          for (int j = 0; j < n; ++j) acc += s[j] * keys[(size_t)j * d + e];
+          for (int j = lo; j < n; ++j) acc += s[j] * keys[(size_t)j * d + e];
 #else
-          for (int j = 0; j < n; ++j) acc += s[j] * vals[(size_t)j * d + e];
+          for (int j = lo; j < n; ++j) acc += s[j] * vals[(size_t)j * d + e];
 #endif
           o[e] = acc / denom;
         }
         if (w_p) {
           double* w = w_p + ((size_t)i * Hq + h) * nk;
-          for (int j = 0; j < nk; ++j) w[j] = j < n ? s[j] / denom : 0.0;
+          for (int j = 0; j < nk; ++j) w[j] = (j >= lo && j < n) ? s[j] / denom : 0.0;
         }
       }
     }
@@ -315,9 +323,15 @@ static int dims_ok(const ora_dims* D) {
 static int run_attn(int f64_inputs, const void* q, const void* k_new, const void* v_new,
                     const void* pool, const float* kv_scale, const int32_t* item_ids,
                     const int32_t* block_table,
-                    const int32_t* pos_offset, const int32_t* pairs, int32_t n_pairs_out,
+                    const int32_t* pos_offset, const int32_t* gist_start, int32_t gist_len,
+                    const int32_t* pairs, int32_t n_pairs_out,
                     double* out, double* weights, const ora_dims* D, int32_t num_threads) {
   if (!dims_ok(D) || !out) return ORA_BAD_ARG;
+  if (gist_start) {
+    if (gist_len < 0) return ORA_BAD_ARG;
+    for (int p = 0; p < D->num_pairs; ++p)
+      if (gist_start[p] < 0) return ORA_BAD_ARG;
+  }
   int C = D->blocks_per_pair * D->block_len;
   if (C > 0 && (!pool || (!item_ids && !block_table))) return ORA_BAD_ARG;
   if (C > 0 && !block_table && D->blocks_per_pair != 1) return ORA_BAD_ARG;
@@ -334,6 +348,7 @@ static int run_attn(int f64_inputs, const void* q, const void* k_new, const void
     ora_job* J = &jobs[t];
     J->D = D; J->f64_inputs = f64_inputs; J->kv_scale = kv_scale; J->q = q; J->k_new = k_new; J->v_new = v_new; J->pool = pool;
     J->item_ids = item_ids; J->block_table = block_table; J->pos_offset = pos_offset;
+    J->gist_start = gist_start; J->gist_len = gist_len;
     J->pairs = pairs; J->n_pairs_out = n_pairs_out; J->out = out; J->weights = weights;
     J->first = (int32_t)((int64_t)n_pairs_out * t / num_threads);
     J->last = (int32_t)((int64_t)n_pairs_out * (t + 1) / num_threads);
@@ -360,8 +375,8 @@ int ora_gist_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_ne
                   const uint16_t* pool, const int32_t* item_ids, const int32_t* block_table,
                   const int32_t* pos_offset, const int32_t* pairs, int32_t n_pairs_out,
                   double* out, double* weights, const ora_dims* D, int32_t num_threads) {
-  return run_attn(0, q, k_new, v_new, pool, NULL, item_ids, block_table, pos_offset, pairs,
-                  n_pairs_out, out, weights, D, num_threads);
+  return run_attn(0, q, k_new, v_new, pool, NULL, item_ids, block_table, pos_offset, NULL, 0,
+                  pairs, n_pairs_out, out, weights, D, num_threads);
 }
 
 /* The same computation with the cached segment stored as E4M3 bytes and one
@@ -373,8 +388,8 @@ int ora_gist_attn_fp8kv(const uint16_t* q, const uint16_t* k_new, const uint16_t
                         const int32_t* pairs, int32_t n_pairs_out, double* out, double* weights,
                         const ora_dims* D, int32_t num_threads) {
   if (!kv_scale && D && D->blocks_per_pair * D->block_len > 0) return ORA_BAD_ARG;
-  return run_attn(0, q, k_new, v_new, pool, kv_scale, item_ids, block_table, pos_offset, pairs,
-                  n_pairs_out, out, weights, D, num_threads);
+  return run_attn(0, q, k_new, v_new, pool, kv_scale, item_ids, block_table, pos_offset, NULL, 0,
+                  pairs, n_pairs_out, out, weights, D, num_threads);
 }
 
 /* The same computation on double inputs (same layouts), for multi-layer pins
@@ -383,8 +398,29 @@ int ora_gist_attn_f64(const double* q, const double* k_new, const double* v_new,
                       const double* pool, const int32_t* item_ids, const int32_t* block_table,
                       const int32_t* pos_offset, const int32_t* pairs, int32_t n_pairs_out,
                       double* out, double* weights, const ora_dims* D, int32_t num_threads) {
-  return run_attn(1, q, k_new, v_new, pool, NULL, item_ids, block_table, pos_offset, pairs,
-                  n_pairs_out, out, weights, D, num_threads);
+  return run_attn(1, q, k_new, v_new, pool, NULL, item_ids, block_table, pos_offset, NULL, 0,
+                  pairs, n_pairs_out, out, weights, D, num_threads);
+}
+
+/*
+ * The same computation under the gist mask ([Gist page, "论文做了什么"]): the
+ * keys of pair p are numbered kappa = 0 .. C + l - 1 over [cached; new]; the
+ * prompt is kappa < gist_start[p] and the gist the next gist_len keys; a token
+ * whose own index C + i lies after the gist sees only keys kappa >= gist_start[p]
+ * (and, as always, kappa <= C + i).  With C = 0 and new tokens
+ * [prompt; gist; rest] this is the training forward of one whole sequence;
+ * over [prompt; gist] alone it is the plain causal mask (the offline
+ * compression pass).  gist_start[p] >= 0, gist_len >= 0.
+ */
+int ora_gist_attn_masked(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                         const uint16_t* pool, const int32_t* item_ids,
+                         const int32_t* block_table, const int32_t* pos_offset,
+                         const int32_t* gist_start, int32_t gist_len, const int32_t* pairs,
+                         int32_t n_pairs_out, double* out, double* weights, const ora_dims* D,
+                         int32_t num_threads) {
+  if (!gist_start) return ORA_BAD_ARG;
+  return run_attn(0, q, k_new, v_new, pool, NULL, item_ids, block_table, pos_offset, gist_start,
+                  gist_len, pairs, n_pairs_out, out, weights, D, num_threads);
 }
 
 /*
@@ -475,6 +511,50 @@ int ora_kv_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* pool,
       for (int e = 0; e < d; ++e) {
         krow[e] = f64_to_bf16_rne(y[e]);
         vrow[e] = v_new[src + e];
+      }
+    }
+  }
+  free(x); free(y);
+  return rc;
+}
+
+/*
+ * Stores a compressed item ([Gist page, "论文做了什么" and "在线的一次 attention"]:
+ * after the offline pass over [prompt; gist] each layer keeps the K/V at the
+ * k gist positions as the item's cache entry).  For pair p (one sequence of
+ * n_new tokens) and KV head g, rows first_row[p] + t, t < block_len (= k), of
+ * k_new / v_new go to block item_ids[p] at `layer`:
+ *   pool[blk][layer][0][g][t] = bf16_rne(R(k_new[p][first_row[p] + t][g]) at
+ *                               position (store_pos ? store_pos[p] : 0) + t)
+ *   pool[blk][layer][1][g][t] = v_new[p][first_row[p] + t][g]
+ * A pair whose rows fall outside [0, n_new) or whose block id is out of range
+ * writes nothing and the call returns ORA_BAD_BLOCK.
+ */
+int ora_kv_store(const uint16_t* k_new, const uint16_t* v_new, uint16_t* pool,
+                 const int32_t* item_ids, const int32_t* first_row, const int32_t* store_pos,
+                 const ora_dims* D) {
+  if (!dims_ok(D) || !k_new || !v_new || !pool || !item_ids || !first_row) return ORA_BAD_ARG;
+  const int d = D->head_dim, Hkv = D->num_kv_heads, k = D->block_len, l = D->n_new;
+  double* x = malloc(sizeof(double) * (size_t)d);
+  double* y = malloc(sizeof(double) * (size_t)d);
+  if (!x || !y) { free(x); free(y); return ORA_NO_MEM; }
+  int rc = ORA_OK;
+  for (int p = 0; p < D->num_pairs; ++p) {
+    int r0 = first_row[p];
+    int32_t blk = item_ids[p];
+    if (r0 < 0 || r0 > l - k || blk < 0 || blk >= D->num_blocks) { rc = ORA_BAD_BLOCK; continue; }
+    double pos0 = store_pos ? (double)store_pos[p] : 0.0;
+    for (int g = 0; g < Hkv; ++g) {
+      for (int t = 0; t < k; ++t) {
+        size_t src = (((size_t)p * l + r0 + t) * Hkv + g) * d;
+        for (int e = 0; e < d; ++e) x[e] = ora_bf16_to_f64(k_new[src + e]);
+        ora_rope(x, d, pos0 + t, D->rope_theta, y);
+        uint16_t* krow = pool + off_pool(D, blk, 0, g, t);
+        uint16_t* vrow = pool + off_pool(D, blk, 1, g, t);
+        for (int e = 0; e < d; ++e) {
+          krow[e] = f64_to_bf16_rne(y[e]);
+          vrow[e] = v_new[src + e];
+        }
       }
     }
   }

@@ -106,3 +106,31 @@ def test_gather_debug_rejects_bad_arguments(lib):
     assert lib.gist_attn_gather_debug(V(P16), V(P16), None, None, D, None) == binding.ERR_NULL
     assert lib.gist_attn_gather_debug(V(P16), V(P16), None, V(P16 + 2), D, None) == binding.ERR_ALIGN
     assert lib.gist_attn_gather_debug(V(P16), None, None, V(P16), D, None) == binding.ERR_NULL
+
+
+def test_gist_mask_rejects_bad_arguments(lib):
+    V = ctypes.c_void_p
+    D0 = dict(BASE, block_len=0, blocks_per_pair=0, num_blocks=0)
+    D = ctypes.byref(binding.make_dims(D0))
+    f = lib.gist_attn_fwd_gist_mask
+    # gist_start is required; gist_len must not be negative; alignment of gist_start
+    assert f(V(P16), V(P16), V(P16), None, None, None, None, None, 4, V(P16), D, None) == binding.ERR_NULL
+    assert f(V(P16), V(P16), V(P16), None, None, None, None, V(P16), -1, V(P16), D, None) == binding.ERR_DIMS
+    assert f(V(P16), V(P16), V(P16), None, None, None, None, V(P16 + 2), 4, V(P16), D, None) == binding.ERR_ALIGN
+    Dg = ctypes.byref(binding.make_dims(dict(D0, num_q_heads=130, num_kv_heads=1)))
+    assert f(V(P16), V(P16), V(P16), None, None, None, None, V(P16), 4, V(P16), Dg, None) == binding.ERR_UNSUPPORTED
+
+
+def test_kv_store_rejects_bad_arguments(lib):
+    V = ctypes.c_void_p
+    f = lib.gist_kv_store
+    ok = dict(BASE, n_new=12, block_len=8, blocks_per_pair=1)
+    D = ctypes.byref(binding.make_dims(ok))
+    assert f(V(P16), V(P16), V(P16), V(P16), None, None, D, None) == binding.ERR_NULL
+    assert f(V(P16), V(P16), None, V(P16), V(P16), None, D, None) == binding.ERR_NULL
+    assert f(V(P16), V(P16), V(P16), V(P16), V(P16 + 1), None, D, None) == binding.ERR_ALIGN
+    for bad in (dict(ok, blocks_per_pair=2), dict(ok, block_len=13), dict(ok, block_len=0)):
+        Db = ctypes.byref(binding.make_dims(bad))
+        assert f(V(P16), V(P16), V(P16), V(P16), V(P16), None, Db, None) == binding.ERR_DIMS
+    Dz = ctypes.byref(binding.make_dims(dict(ok, num_pairs=0)))
+    assert f(None, None, None, None, None, None, Dz, None) == binding.OK

@@ -190,8 +190,35 @@ def check_rows_sum(plant=0):
     return None
 
 
+def check_gist_mask_brute_force(plant=0):
+    """gist page, 论文做了什么: the oracle's gist-masked attention over whole
+    sequences [prompt j_p; gist k; rest] (right-padded to one length, a
+    different j_p per pair) against the brute-force mask, the loop-per-row
+    masked attention and the loop-per-element RoPE of oracle/gist_mask.py."""
+    P, n, Hq, Hkv, d, k = 3, 13, 4, 2, 8, 3
+    G = Hq // Hkv
+    q, kn, vn = bf16((P, n, Hq, d), 70), bf16((P, n, Hkv, d), 71), bf16((P, n, Hkv, d), 72)
+    starts = np.array([2, 5, 0], dtype=np.int32)
+    pos0 = np.array([0, 17, 300], dtype=np.int32)
+    got = oracle.gist_attn(q, kn, vn, None, pos_offset=pos0, dims=dims(P, n, Hq, Hkv, d, 0, 0, 0),
+                           gist_start=starts, gist_len=k, plant=plant)
+    for p in range(P):
+        j = int(starts[p])
+        allowed = gm.gist_mask(j, k, n - j - k)
+        pos = pos0[p] + np.arange(n)
+        for h in range(Hq):
+            qr = gm.rope_rotate_half(f64(q[p, :, h]), pos)
+            kr = gm.rope_rotate_half(f64(kn[p, :, h // G]), pos)
+            want = gm.masked_attention(qr, kr, f64(vn[p, :, h // G]), allowed, 1 / math.sqrt(d))
+            err = np.abs(got[p, :, h] - want).max()
+            if err > 1e-12:
+                return f"gist mask pair {p} head {h}: {err:.3e}"
+    return None
+
+
 ALL_CHECKS = [check_rope_complex, check_sdpa_general, check_gqa_equals_repeated_mha,
-              check_layer_selection, check_closed_forms, check_rows_sum]
+              check_layer_selection, check_closed_forms, check_rows_sum,
+              check_gist_mask_brute_force]
 
 
 # ------------------------------------------------------------------ tests ---
@@ -519,7 +546,7 @@ def test_flop_share_and_traffic_figures(golden):
 
 # ------------------------------------------- each planted mistake is caught ---
 
-@pytest.mark.parametrize("plant", range(1, 9))
+@pytest.mark.parametrize("plant", range(1, 10))
 def test_planted_mistake_is_caught(plant):
     failures = [c.__name__ for c in ALL_CHECKS if c(plant=plant) is not None]
     assert failures, f"planted mistake {plant} slipped through every pin"
@@ -618,3 +645,68 @@ def test_kv_append_writes_rotated_key_and_value():
     bad[1] = bpp * bl
     _, rc = oracle.kv_append(kn, vn, pool, table, bad, dims=D)
     assert rc == -2
+
+
+# ------------------------------------------- offline compression: the store ---
+
+def test_kv_store_writes_rotated_gist_rows():
+    """gist page, 论文做了什么 / 在线的一次 attention: the item's cache entry is
+    each layer's K/V at the k gist positions.  Keys against the complex-rotation
+    RoPE rounded by torch to bf16, values bit for bit, other rows untouched."""
+    P, n, Hkv, d, k, nb, L = 3, 11, 2, 32, 4, 5, 2
+    kn, vn = bf16((P, n, Hkv, d), 80), bf16((P, n, Hkv, d), 81)
+    pool = bf16((nb, L, 2, Hkv, k, d), 82)
+    ids = np.array([4, 0, 2], dtype=np.int32)
+    first = np.array([7, 0, 3], dtype=np.int32)
+    spos = np.array([7, 0, 1000], dtype=np.int32)
+    D = dims(P, n, Hkv, Hkv, d, k, 1, nb, L=L, layer=1)
+    new, rc = oracle.kv_store(kn, vn, pool, ids, first, spos, dims=D)
+    assert rc == 0
+    old = oracle.bf16_bits(pool)
+    for p in range(P):
+        for g in range(Hkv):
+            for t in range(k):
+                r = first[p] + t
+                want_k = torch.from_numpy(rope_complex(f64(kn[p, r, g]), spos[p] + t)).to(torch.bfloat16)
+                assert np.array_equal(new[ids[p], 1, 0, g, t], oracle.bf16_bits(want_k))
+                assert np.array_equal(new[ids[p], 1, 1, g, t], oracle.bf16_bits(vn[p, r, g]))
+    untouched = np.ones(nb, dtype=bool)
+    untouched[ids] = False
+    assert np.array_equal(new[untouched], old[untouched])
+    assert np.array_equal(new[:, 0], old[:, 0])  # other layer
+    # default positions 0..k-1
+    new0, _ = oracle.kv_store(kn, vn, pool, ids, first, None, dims=D)
+    want = torch.from_numpy(rope_complex(f64(kn[0, 7 + 2, 1]), 2)).to(torch.bfloat16)
+    assert np.array_equal(new0[4, 1, 0, 1, 2], oracle.bf16_bits(want))
+    # rows past the sequence end, or a bad id: rejected
+    _, rc = oracle.kv_store(kn, vn, pool, ids, np.array([8, 0, 3], np.int32), dims=D)
+    assert rc == -2
+    _, rc = oracle.kv_store(kn, vn, pool, np.array([4, 5, 2], np.int32), first, dims=D)
+    assert rc == -2
+
+
+def test_offline_pass_store_then_online_equals_masked_forward():
+    """gist page, 论文做了什么 + 在线的一次 attention, one layer: the gist-masked
+    forward over [prompt; gist; query] gives, on the query rows, what the query
+    gets against the stored gist entry (gist rotated at j..j+k-1, query from
+    j+k).  Equal up to the bf16 rounding of the stored keys."""
+    j, k, l, Hq, Hkv, d = 9, 4, 6, 6, 2, 16
+    n = j + k + l
+    q, kn, vn = bf16((1, n, Hq, d), 90), bf16((1, n, Hkv, d), 91), bf16((1, n, Hkv, d), 92)
+    full = oracle.gist_attn(q, kn, vn, None, dims=dims(1, n, Hq, Hkv, d, 0, 0, 0),
+                            gist_start=np.array([j], np.int32), gist_len=k)
+    pool0 = torch.zeros((1, 1, 2, Hkv, k, d), dtype=torch.bfloat16)
+    store_dims = dims(1, n, Hkv, Hkv, d, k, 1, 1)
+    entry, rc = oracle.kv_store(kn, vn, pool0, np.zeros(1, np.int32), np.array([j], np.int32),
+                                np.array([j], np.int32), dims=store_dims)
+    assert rc == 0
+    online = oracle.gist_attn(q[:, j + k:].contiguous(), kn[:, j + k:].contiguous(),
+                              vn[:, j + k:].contiguous(), entry, item_ids=np.zeros(1, np.int32),
+                              pos_offset=np.array([j + k], np.int32),
+                              dims=dims(1, l, Hq, Hkv, d, k, 1, 1))
+    assert np.abs(online - full[:, j + k:]).max() < 1e-2
+    # the unmasked (plain causal) forward differs on the query rows
+    plain = oracle.gist_attn(q, kn, vn, None, dims=dims(1, n, Hq, Hkv, d, 0, 0, 0))
+    assert np.abs(plain[:, j + k:] - full[:, j + k:]).max() > 5e-2
+    # and the rows before the gist's end are plain causal attention
+    assert np.array_equal(plain[:, : j + k], full[:, : j + k])
