@@ -53,7 +53,7 @@ struct TcParams {
   int n_mt;       // M-tiles per unit
   int num_units;  // P * Hkv
   int kv_rows;    // rows of one K (or V) panel
-  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_ids, off_red, off_bar;
+  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_ids, off_red, off_bias, off_bar;
   uint32_t p_col, o_col, lo_col, tmem_cols;  // TMEM plan: S at column 0
   float scale_log2;
   float inv_freq[64];
@@ -61,7 +61,8 @@ struct TcParams {
 
 struct Layout {
   int Tm, n_mt, kv_rows;
-  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_ids, off_red, off_bar, bytes;
+  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_ids, off_red, off_bias, off_bar,
+      bytes;
   uint32_t p_col, o_col, lo_col, tmem_cols;
 };
 
@@ -85,6 +86,8 @@ Layout plan(const Problem& pb) {
   off += 2u * kMaxBlocksPerPair * 4;
   L.off_red = off;
   off += 2u * 2 * 128 * 4;  // partial row max and row sum of each half
+  L.off_bias = off;
+  off += 17u * 16 * 4;  // mask rows: bias[v][e] = 0 for e < v, else -inf
   L.off_bar = off;
   off += 128;
   L.bytes = off + 1024;
@@ -124,8 +127,11 @@ struct Bars {
   uint32_t tmem_slot;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
+// NCH: S chunks of 16 columns per thread (the tile's keys / 32, rounded up).
+// Registers: each of the 4 SM sub-partitions holds 16 K; two CTAs of 9 warps
+// put 5 warps on one of them (96 registers a thread), one CTA puts 3 (168).
+template <int D, int NCH>
+__global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_o,
                       const __grid_constant__ TcParams prm) {
@@ -144,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
   float* red_max = reinterpret_cast<float*>(smem + prm.off_red);  // [2][128]
   float* red_sum = red_max + 256;                                  // [2][128]
   const uint8_t* tab = smem + prm.off_tab;
+  float* bias = reinterpret_cast<float*>(smem + prm.off_bias);  // [17][16]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = prm.G, C = prm.C, l = prm.l, Tm = prm.Tm, n_mt = prm.n_mt;
@@ -177,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
                             ((rest / NP) & 1) * NP * kv_panel + (rest % NP) * kv_panel;
       sts16(base + swz128(C + l + rr, c), z);
     }
+    for (int idx = tid; idx < 17 * 16; idx += kThreads) bias[idx] = (idx & 15) < (idx >> 4) ? 0.f : kNegInf;
     const int qpad = 128 - Tm * G;  // rows of each Q stage that no TMA box reaches
     for (int idx = tid; idx < kStages * NP * qpad * 8; idx += kThreads) {
       const int c = idx & 7, rr = (idx >> 3) % qpad, sp = (idx >> 3) / qpad;
@@ -357,14 +365,23 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       fence_proxy_async_smem();
       named_bar_sync(kBarCompute, kCompute);
     };
+    // A wait that has timed out once turns every later wait of this thread
+    // into a no-op, so a stuck pipeline ends in bounded time (the status word
+    // says so); the loop structure and every barrier stay uniform.
+    bool failed = false;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      if (!failed && !mbar_wait(bar, parity)) failed = true;
+    };
+    const uint32_t pair_bar = 2 + (warp & 3);  // this row's two threads (warps w, w + 4)
     // Rotate row r of tile i's q (this half's chunk pairs): hi -> stage, lo -> TMEM.
-    auto rope_tile = [&](int i) -> bool {
+    // Rows past the tile's tokens hold zeros (TMA fill, or set-up for rows no
+    // box reaches), so their hi and lo come out zero without a select.
+    auto rope_tile = [&](int i) {
       const int s = i % kStages, mt = i % n_mt;
       const uint32_t stage = sbase + s * prm.stage_bytes;
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
-      const bool valid = r < toks * G;
       const int tt = min(r / G, toks - 1);
-      const bool ok = mbar_wait(&bars->qfull[s], (uint32_t)(i / kStages) & 1u);
+      wait(&bars->qfull[s], (uint32_t)(i / kStages) & 1u);
       constexpr int JH = CPR / 4;  // chunk pairs per half
       uint32_t lo_a[JH * 4], lo_b[JH * 4];
       const uint8_t* trow = tab + (t0 + tt) * prm.tab_stride;
@@ -381,10 +398,8 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
           f2_split_bf16(xr[e], xh[e], lo_a[jj * 4 + e]);
           f2_split_bf16(yr[e], yh[e], lo_b[jj * 4 + e]);
         }
-        if (valid) {
-          sts16(a0, make_uint4(xh[0], xh[1], xh[2], xh[3]));
-          sts16(a1, make_uint4(yh[0], yh[1], yh[2], yh[3]));
-        }
+        sts16(a0, make_uint4(xh[0], xh[1], xh[2], xh[3]));
+        sts16(a1, make_uint4(yh[0], yh[1], yh[2], yh[3]));
       }
       // TMEM column c of the lo block holds q elements (2c, 2c+1)
 #pragma unroll
@@ -392,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         uint32_t va[8], vb8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          va[e] = valid ? lo_a[q8 * 8 + e] : 0u;
-          vb8[e] = valid ? lo_b[q8 * 8 + e] : 0u;
+          va[e] = lo_a[q8 * 8 + e];
+          vb8[e] = lo_b[q8 * 8 + e];
         }
         tc::st8(tmem + lane_base + prm.lo_col + (h * JH + q8 * 2) * 4, va);
         tc::st8(tmem + lane_base + prm.lo_col + (h * JH + q8 * 2 + CPR / 2) * 4, vb8);
@@ -402,11 +417,9 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       fence_proxy_async_smem();
       tc::fence_before_sync();
       mbar_arrive(&bars->rope_done);
-      return ok;
     };
 
     bool bad0 = false, bad1 = false;  // out-of-range block id in the unit of K/V buffer 0 / 1
-    bool failed = false;
     if (my_units > 0) {
       bad0 = stage_kv(unit_of(0), 0);
       if (my_units > 1) {
@@ -416,9 +429,9 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         cp_async_wait_group<0>();
       }
       prepare_unit(0, bad0);
-      failed = named_bar_or(kBarCompute, kCompute, !rope_tile(0));
+      rope_tile(0);
     }
-    for (int i = 0; i < my_tiles && !failed; ++i) {
+    for (int i = 0; i < my_tiles; ++i) {
       const uint32_t par = (uint32_t)i & 1u;
       const int k = i / n_mt, mt = i % n_mt;
       const bool bad = (k & 1) ? bad1 : bad0;
@@ -427,39 +440,48 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       const int tt = min(r / G, toks - 1);
       const int N = (C + t0 + toks + 15) & ~15;
       // ---- softmax of row r over this half's 16-column chunks c = h, h+2, ...
-      bool ok = mbar_wait(&bars->s_done, par);
+      // (read from TMEM twice: for the max, then for the exponentials; holding
+      // the chunks in registers between the two costs more in spills)
+      wait(&bars->s_done, par);
       tc::fence_after_sync();
       const int lim = C + t0 + tt + 1;  // keys row r sees
       const int lim_all = C + t0 + 1;   // keys every row of the tile sees
-      // chunks below lim_all need no mask (a uniform test across the warp)
+      // chunk c of this row's logits, with 0 added to the visible keys and -inf
+      // to the rest when the chunk reaches the causal diagonal (a tile-uniform test)
+      auto load_chunk = [&](int c, uint32_t (&sv)[16]) {
+        tc::ld16(tmem + lane_base + c * 16, sv);
+        tc::wait_ld();
+        if ((c + 1) * 16 > lim_all) {
+          const int v = min(max(lim - c * 16, 0), 16);
+          const float4* bt = reinterpret_cast<const float4*>(bias + v * 16);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float4 b = bt[q4];
+            sv[4 * q4 + 0] = __float_as_uint(__uint_as_float(sv[4 * q4 + 0]) + b.x);
+            sv[4 * q4 + 1] = __float_as_uint(__uint_as_float(sv[4 * q4 + 1]) + b.y);
+            sv[4 * q4 + 2] = __float_as_uint(__uint_as_float(sv[4 * q4 + 2]) + b.z);
+            sv[4 * q4 + 3] = __float_as_uint(__uint_as_float(sv[4 * q4 + 3]) + b.w);
+          }
+        }
+      };
       float mx0 = kNegInf, mx1 = kNegInf;
 #pragma unroll
-      for (int cc = 0; cc < kMaxKeys / 32; ++cc) {
+      for (int cc = 0; cc < NCH; ++cc) {
         const int c = 2 * cc + h;
         if (c * 16 < N) {
-          uint32_t sv[16];
-          tc::ld16(tmem + lane_base + c * 16, sv);
-          tc::wait_ld();
-          if ((c + 1) * 16 <= lim_all) {
-            const float a = max3f(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
-            const float b = max3f(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
-            const float d = max3f(__uint_as_float(sv[6]), __uint_as_float(sv[7]), __uint_as_float(sv[8]));
-            const float e = max3f(__uint_as_float(sv[9]), __uint_as_float(sv[10]), __uint_as_float(sv[11]));
-            const float f = max3f(__uint_as_float(sv[12]), __uint_as_float(sv[13]), __uint_as_float(sv[14]));
-            mx0 = max3f(mx0, a, b);
-            mx1 = max3f(mx1, max3f(d, e, f), __uint_as_float(sv[15]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              const float a = c * 16 + e < lim ? __uint_as_float(sv[e]) : kNegInf;
-              const float b = c * 16 + e + 1 < lim ? __uint_as_float(sv[e + 1]) : kNegInf;
-              mx0 = max3f(mx0, a, b);
-            }
-          }
+          uint32_t v[16];
+          load_chunk(c, v);
+          const float a = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+          const float b = max3f(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
+          const float d = max3f(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
+          const float e = max3f(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
+          const float f = max3f(__uint_as_float(v[12]), __uint_as_float(v[13]), __uint_as_float(v[14]));
+          mx0 = max3f(mx0, a, b);
+          mx1 = max3f(mx1, max3f(d, e, f), __uint_as_float(v[15]));
         }
       }
       red_max[h * 128 + r] = fmaxf(mx0, mx1);
-      named_bar_sync(kBarCompute, kCompute);
+      named_bar_sync(pair_bar, 64);
       const float m = fmaxf(red_max[r], red_max[128 + r]);
       {
         const float sc = prm.scale_log2;
@@ -467,22 +489,17 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         const uint64_t one2 = f2_make(1.f, 1.f);
         uint64_t acc[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
-        for (int cc = 0; cc < kMaxKeys / 32; ++cc) {
+        for (int cc = 0; cc < NCH; ++cc) {
           const int c = 2 * cc + h;
           if (c * 16 < N) {
-            uint32_t sv[16];
-            tc::ld16(tmem + lane_base + c * 16, sv);
-            tc::wait_ld();
-            const bool full = (c + 1) * 16 <= lim_all;
+            uint32_t v[16];
+            load_chunk(c, v);
             uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              float a = __uint_as_float(sv[2 * e]), bb = __uint_as_float(sv[2 * e + 1]);
-              if (!full) {
-                a = c * 16 + 2 * e < lim ? a : kNegInf;
-                bb = c * 16 + 2 * e + 1 < lim ? bb : kNegInf;
-              }
-              f2_split(f2_fma(f2_make(a, bb), sc2, nmc2), a, bb);
+              float a, bb;
+              f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, nmc2),
+                       a, bb);
               const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
               acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
               pk[e] = f2_to_bf16x2(pp);
@@ -504,33 +521,39 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
           cp_async_wait_group<0>();
           prepare_unit(k + 1, ((k + 1) & 1) ? bad1 : bad0);
         }
-        if (!rope_tile(i + 1)) ok = false;
+        rope_tile(i + 1);
       }
       // ---- O of row r, this half's columns, normalised into the stage
-      ok = mbar_wait(&bars->o_done, par) && ok;
+      wait(&bars->o_done, par);
       tc::fence_after_sync();
-      if (named_bar_or(kBarCompute, kCompute, !ok)) failed = true;  // also: row sums written
+      named_bar_sync(pair_bar, 64);  // the partner's row sum is written
       {
         const uint32_t stage = sbase + (i % kStages) * prm.stage_bytes;
-        const float inv = 1.f / (red_sum[r] + red_sum[128 + r]);
-        const uint64_t inv2 = f2_make(inv, inv);
         constexpr int OC = D / 32;  // 16-column chunks per half
+        if (bad) {
+          if (valid) {
 #pragma unroll
-        for (int c = 0; c < OC; ++c) {
-          uint32_t ov[16];
-          tc::ld16(tmem + lane_base + prm.o_col + (h * OC + c) * 16, ov);
-          tc::wait_ld();
-          if (valid) {  // (one 16-column chunk at a time keeps registers low)
-            uint32_t w[8];
+            for (int J = 0; J < 2 * OC; ++J)
+              sts16(chunk_addr(stage, kPanel, r, h * 2 * OC + J), make_uint4(0, 0, 0, 0));
+          }
+        } else {
+          const float inv = 1.f / (red_sum[r] + red_sum[128 + r]);
+          const uint64_t inv2 = f2_make(inv, inv);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              w[e] = bad ? 0u
-                         : f2_to_bf16x2(f2_mul(
-                               f2_make(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])),
-                               inv2));
-            const int J = (h * OC + c) * 2;
-            sts16(chunk_addr(stage, kPanel, r, J), make_uint4(w[0], w[1], w[2], w[3]));
-            sts16(chunk_addr(stage, kPanel, r, J + 1), make_uint4(w[4], w[5], w[6], w[7]));
+          for (int c = 0; c < OC; ++c) {
+            uint32_t ov[16];
+            tc::ld16(tmem + lane_base + prm.o_col + (h * OC + c) * 16, ov);
+            tc::wait_ld();
+            if (valid) {  // (one 16-column chunk at a time keeps registers low)
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                w[e] = f2_to_bf16x2(
+                    f2_mul(f2_make(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), inv2));
+              const int J = (h * OC + c) * 2;
+              sts16(chunk_addr(stage, kPanel, r, J), make_uint4(w[0], w[1], w[2], w[3]));
+              sts16(chunk_addr(stage, kPanel, r, J + 1), make_uint4(w[4], w[5], w[6], w[7]));
+            }
           }
         }
       }
@@ -544,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         if (k & 1) bad1 = bk; else bad0 = bk;
       }
     }
-    if (failed && tid == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     cp_async_wait_all();
   }
 
@@ -572,7 +595,7 @@ int encode_map(CUtensorMap* m, const void* base, const Problem& pb, int Tm) {
   return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
 }
 
-template <int D>
+template <int D, int NCH>
 int launch_d(const Problem& pb, cudaStream_t stream) {
   const Layout L = plan(pb);
   TcParams prm{};
@@ -597,6 +620,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.tab_stride = L.tab_stride;
   prm.off_ids = L.off_ids;
   prm.off_red = L.off_red;
+  prm.off_bias = L.off_bias;
   prm.off_bar = L.off_bar;
   prm.p_col = L.p_col;
   prm.o_col = L.o_col;
@@ -610,7 +634,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   if (rc != GIST_ATTN_OK) return rc;
   rc = encode_map(&tm_o, pb.out, pb, L.Tm);
   if (rc != GIST_ATTN_OK) return rc;
-  if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(prefill_tc_kernel<D, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)L.bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   int dev = 0, sms = 0;
@@ -622,7 +646,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   const int per_sm = (D == 64 && L.tmem_cols == 256 && L.bytes <= 113 * 1024) ? 2 : 1;
   const int64_t units = (int64_t)pb.P * pb.Hkv;
   const int grid = (int)(units < (int64_t)sms * per_sm ? units : (int64_t)sms * per_sm);
-  prefill_tc_kernel<D><<<grid, kThreads, L.bytes, stream>>>(tm_q, tm_o, prm);
+  prefill_tc_kernel<D, NCH><<<grid, kThreads, L.bytes, stream>>>(tm_q, tm_o, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
@@ -637,8 +661,17 @@ bool prefill_tc_fits(const Problem& pb) {
 }
 
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream) {
-  if (pb.d == 64) return launch_d<64>(pb, stream);
-  if (pb.d == 128) return launch_d<128>(pb, stream);
+  const int chunks = (plan(pb).kv_rows / 16 + 1) / 2;  // per thread: chunks h, h+2, ...
+  if (pb.d == 64) {
+    if (chunks <= 2) return launch_d<64, 2>(pb, stream);
+    if (chunks <= 3) return launch_d<64, 3>(pb, stream);
+    return launch_d<64, 4>(pb, stream);
+  }
+  if (pb.d == 128) {
+    if (chunks <= 2) return launch_d<128, 2>(pb, stream);
+    if (chunks <= 3) return launch_d<128, 3>(pb, stream);
+    return launch_d<128, 4>(pb, stream);
+  }
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 

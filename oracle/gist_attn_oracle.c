@@ -21,6 +21,12 @@
  *   back.  [KV page, "Reusable-state"]: o_t = softmax(q_t K^T / sqrt(d_k)) V.
  *   [Gist page, "收益有多大：存储"]: G is stored per KV head; with GQA each KV
  *   head serves a contiguous group of Hq/Hkv query heads.
+ *   [Gist page, "论文做了什么"]: optionally the gist mask (tokens after the gist
+ *   no longer see the prompt), and the store of each layer's K/V at the gist
+ *   positions as an item's cache entry.
+ *   [Suffix page, §2 and the end of §5]: optionally an fp8 (E4M3) cached
+ *   segment with one scale per (block, layer, K|V, KV head).
+ *   [KV page, "Reusable-state"]: the append of the decode step's k_t, v_t.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - RoPE is the rotate-half form on pairs (j, j + d/2) with
