@@ -386,34 +386,61 @@ def run_ours(args) -> dict:
 def run_e2e(args, wl, lib, ptrs, dims_by_layer, stream, ws) -> dict:
     """Same metric through the C ABI with inputs in pinned host memory: every
     layer copies that layer's Q/K_new/V_new (and ids) host -> device, runs the
-    kernel, and copies the output back."""
+    kernel, and copies the output back.  Two device buffer sets and three
+    streams (host->device, compute, device->host) let layer i's copies overlap
+    layer i-1's kernel and read-back, as a serving loop would run them."""
     import ctypes
 
     import torch
 
     L, P = wl.dims["num_layers"], wl.dims["num_pairs"]
     ids = wl.item_ids if wl.item_ids is not None else wl.block_table
+    use_ids = wl.item_ids is not None
     host = {n: t.cpu().pin_memory() for n, t in (("q", wl.q), ("k", wl.k_new), ("v", wl.v_new), ("ids", ids))}
-    host_out = torch.empty(wl.q.shape, dtype=wl.q.dtype, pin_memory=True)
-    dev_out = torch.empty_like(wl.q)
-    out_ptr = ctypes.c_void_p(dev_out.data_ptr())
-    p = list(ptrs)
-    p[7] = out_ptr
+    host_out = [torch.empty(wl.q.shape, dtype=wl.q.dtype, pin_memory=True) for _ in range(2)]
+    sets = []
+    for b in range(2):
+        d = {"q": wl.q if b == 0 else torch.empty_like(wl.q),
+             "k": wl.k_new if b == 0 else torch.empty_like(wl.k_new),
+             "v": wl.v_new if b == 0 else torch.empty_like(wl.v_new),
+             "ids": ids if b == 0 else torch.empty_like(ids),
+             "out": torch.empty_like(wl.q)}
+        p = list(ptrs)
+        V = ctypes.c_void_p
+        p[0], p[1], p[2], p[7] = V(d["q"].data_ptr()), V(d["k"].data_ptr()), V(d["v"].data_ptr()), V(d["out"].data_ptr())
+        if use_ids:
+            p[4] = V(d["ids"].data_ptr())
+        else:
+            p[5] = V(d["ids"].data_ptr())
+        d["ptrs"] = p
+        sets.append(d)
+    h2d_s, d2h_s = torch.cuda.Stream(device=wl.q.device), torch.cuda.Stream(device=wl.q.device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "done", "back")}
 
     def step():
-        with torch.cuda.stream(stream):
-            for li in range(L):
-                wl.q.copy_(host["q"], non_blocking=True)
-                wl.k_new.copy_(host["k"], non_blocking=True)
-                wl.v_new.copy_(host["v"], non_blocking=True)
-                ids.copy_(host["ids"], non_blocking=True)
-                rc = lib.gist_attn_fwd(*p, ctypes.byref(dims_by_layer[li]), sh)
-                if rc != 0:
-                    raise RuntimeError(f"gist_attn_fwd returned {rc}")
-                host_out.copy_(dev_out, non_blocking=True)
+        for li in range(L):
+            b = li & 1
+            d = sets[b]
+            with torch.cuda.stream(h2d_s):
+                h2d_s.wait_event(ev["done"][b])  # the kernel two layers back read this set
+                d["q"].copy_(host["q"], non_blocking=True)
+                d["k"].copy_(host["k"], non_blocking=True)
+                d["v"].copy_(host["v"], non_blocking=True)
+                d["ids"].copy_(host["ids"], non_blocking=True)
+                ev["in"][b].record(h2d_s)
+            stream.wait_event(ev["in"][b])
+            stream.wait_event(ev["back"][b])  # this set's previous output has left
+            rc = lib.gist_attn_fwd(*d["ptrs"], ctypes.byref(dims_by_layer[li]), sh)
+            if rc != 0:
+                raise RuntimeError(f"gist_attn_fwd returned {rc}")
+            ev["done"][b].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev["done"][b])
+                host_out[b].copy_(d["out"], non_blocking=True)
+                ev["back"][b].record(d2h_s)
 
     step()
     torch.cuda.synchronize()
@@ -421,13 +448,18 @@ def run_e2e(args, wl, lib, ptrs, dims_by_layer, stream, ws) -> dict:
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     start.record(stream)
+    h2d_s.wait_event(start)
+    d2h_s.wait_event(start)
     for _ in range(K):
         step()
+    stream.wait_event(ev["back"][0])
+    stream.wait_event(ev["back"][1])
     end.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(start.elapsed_time(end), ws)
     return {"value": P * L * K * ws / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d * L,
-            "d2h_bytes_per_step": d2h * L, "steps": K}
+            "d2h_bytes_per_step": d2h * L, "steps": K,
+            "overlap": "two buffer sets; host->device, compute and device->host streams"}
 
 
 # -------------------------------------------------------- reference arm ---
