@@ -10,8 +10,9 @@
 // the softmax and softmax x V depend on the KV length; they are this kernel.
 //
 // Persistent CTAs (two per SM when TMEM and shared memory allow), warp-specialised:
-//   * warp 8 (control): TMA loads of 128-row Q tiles into a 3-stage ring,
-//     tcgen05.mma issue (S = Q K^T, O = P V), TMA stores of O;
+//   * warp 8 (MMA): tcgen05.mma issue (S = Q K^T, O = P V);
+//   * warp 9 (TMA): TMA loads of 128-row Q tiles into a 3-stage ring and TMA
+//     stores of O, so that waiting for a store never delays the tensor core;
 //   * warps 0-7 (compute): two threads per tile row (TMEM lane = row; the
 //     halves split the columns).  They stage each unit's K/V (cached rows
 //     through the pool gather, new rows raw, by 16-byte cp.async two units
@@ -35,7 +36,7 @@ namespace gattn {
 namespace {
 
 constexpr int kCompute = 256;            // 8 compute warps
-constexpr int kThreads = kCompute + 32;  // + the control warp
+constexpr int kThreads = kCompute + 64;  // + the MMA warp and the TMA warp
 constexpr int kStages = 3;
 constexpr int kMaxKeys = 128;
 constexpr int kMaxSmem = 227 * 1024;
@@ -119,11 +120,13 @@ __device__ __forceinline__ void rope_chunk(const uint4& x, const uint4& y, const
 
 struct Bars {
   uint64_t qfull[kStages];
-  uint64_t rope_done;  // compute -> control: q tile rotated (hi in the stage, lo in TMEM)
+  uint64_t rope_done;  // compute -> MMA warp: q tile rotated (hi in the stage, lo in TMEM)
   uint64_t s_done;     // tensor core -> compute: S ready
-  uint64_t p_done;     // compute -> control: P ready
+  uint64_t p_done;     // compute -> MMA warp: P ready
   uint64_t o_done;     // tensor core -> compute: O ready
-  uint64_t o_stored;   // compute -> control: O written into the stage
+  uint64_t o_stored[2];  // compute -> TMA warp: O of tile i written into its stage
+                         // (two, alternating: the compute warps can finish tile i+1
+                         // before the TMA warp has waited on tile i)
   uint32_t tmem_slot;
 };
 
@@ -172,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     mbar_init(&bars->s_done, 1);
     mbar_init(&bars->p_done, kCompute);
     mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->o_stored, kCompute);
+    mbar_init(&bars->o_stored[0], kCompute);
+    mbar_init(&bars->o_stored[1], kCompute);
     fence_mbar_init();
   }
   {
@@ -208,32 +212,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
   const uint32_t tmem = bars->tmem_slot;
 
   if (warp == 8) {
-    // ================================================================ control
+    // ================================================================ MMA issue
     // All 32 lanes walk the loop (waits are uniform); lane 0 issues.
     bool failed = false;
-    auto load_tile = [&](int i) {
-      if (i >= my_tiles) return;
-      const int u = unit_of(i / n_mt), mt = i % n_mt, s = i % kStages;
-      const int p = u / prm.Hkv, g = u % prm.Hkv;
-      mbar_arrive_expect_tx(&bars->qfull[s], (uint32_t)NP * Tm * G * 128);
-#pragma unroll
-      for (int pn = 0; pn < NP; ++pn)
-        tma_load_5d(sbase + s * prm.stage_bytes + pn * kPanel, &tm_q, &bars->qfull[s], 0, pn,
-                    g * G, mt * Tm, p);
-    };
-    auto store_tile = [&](int i) {
-      const int u = unit_of(i / n_mt), mt = i % n_mt, s = i % kStages;
-      const int p = u / prm.Hkv, g = u % prm.Hkv;
-#pragma unroll
-      for (int pn = 0; pn < NP; ++pn)
-        tma_store_5d(&tm_o, sbase + s * prm.stage_bytes + pn * kPanel, 0, pn, g * G, mt * Tm, p);
-      bulk_commit();
-    };
-    if (lane == 0 && my_tiles > 0) {
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_o);
-      for (int i = 0; i < kStages; ++i) load_tile(i);
-    }
     for (int i = 0; i < my_tiles; ++i) {
       const uint32_t par = (uint32_t)i & 1u;
       const int k = i / n_mt, mt = i % n_mt;
@@ -262,17 +243,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
         tc::commit(smem_u32(&bars->s_done));
       }
       __syncwarp();
-      // ---- the previous tile's output leaves; its stage is refilled kStages tiles on
-      if (i > 0) {
-        if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored, par ^ 1u))) { failed = true; break; }
-        if (lane == 0) {
-          store_tile(i - 1);
-          bulk_wait_read_all();
-          load_tile(i - 1 + kStages);
-        }
-        __syncwarp();
-      }
-      // ---- O = P V (A = P from TMEM, B = V with d contiguous)
+      // ---- O = P V (A = P from TMEM, B = V with d contiguous).  Every compute
+      // thread arrives on p_done(i) after reading O(i-1), so O may be overwritten.
       if (__any_sync(0xffffffffu, !mbar_wait(&bars->p_done, par))) { failed = true; break; }
       tc::fence_after_sync();
       if (lane == 0) {
@@ -285,14 +257,47 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       }
       __syncwarp();
     }
-    if (!failed && my_tiles > 0) {
-      if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored, (uint32_t)(my_tiles - 1) & 1u)))
+    if (lane == 0 && failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    __syncwarp();
+  } else if (warp == 9) {
+    // ================================================================ TMA
+    // Q tiles in, O tiles out; a stage is refilled kStages tiles on as soon as
+    // the store of its output has read it.
+    bool failed = false;
+    auto load_tile = [&](int i) {
+      if (i >= my_tiles) return;
+      const int u = unit_of(i / n_mt), mt = i % n_mt, s = i % kStages;
+      const int p = u / prm.Hkv, g = u % prm.Hkv;
+      mbar_arrive_expect_tx(&bars->qfull[s], (uint32_t)NP * Tm * G * 128);
+#pragma unroll
+      for (int pn = 0; pn < NP; ++pn)
+        tma_load_5d(sbase + s * prm.stage_bytes + pn * kPanel, &tm_q, &bars->qfull[s], 0, pn,
+                    g * G, mt * Tm, p);
+    };
+    if (lane == 0 && my_tiles > 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_o);
+      for (int i = 0; i < kStages; ++i) load_tile(i);
+    }
+    for (int i = 0; i < my_tiles; ++i) {
+      if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored[i & 1], (uint32_t)(i >> 1) & 1u))) {
         failed = true;
-      else if (lane == 0)
-        store_tile(my_tiles - 1);
+        break;
+      }
+      if (lane == 0) {
+        const int u = unit_of(i / n_mt), mt = i % n_mt, s = i % kStages;
+        const int p = u / prm.Hkv, g = u % prm.Hkv;
+#pragma unroll
+        for (int pn = 0; pn < NP; ++pn)
+          tma_store_5d(&tm_o, sbase + s * prm.stage_bytes + pn * kPanel, 0, pn, g * G, mt * Tm, p);
+        bulk_commit();
+        bulk_wait_read_all();
+        load_tile(i + kStages);
+      }
+      __syncwarp();
     }
     if (lane == 0) {
-      bulk_wait_read_all();
+      bulk_wait_all();
       if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     }
     __syncwarp();
@@ -560,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       if (bad && mt == 0 && tid == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
       fence_proxy_async_smem();
       tc::fence_before_sync();
-      mbar_arrive(&bars->o_stored);
+      mbar_arrive(&bars->o_stored[i & 1]);
       // ---- the last tile of unit k: its K/V buffer is free for unit k+2
       if (mt == n_mt - 1 && k + 2 < my_units) {
         const bool bk = stage_kv(unit_of(k + 2), k & 1);
