@@ -54,7 +54,7 @@ struct TcParams {
   int n_mt;       // M-tiles per unit
   int num_units;  // P * Hkv
   int kv_rows;    // rows of one K (or V) panel
-  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_ids, off_red, off_bias, off_bar;
+  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_bar;
   uint32_t p_col, o_col, lo_col, tmem_cols;  // TMEM plan: S at column 0
   float scale_log2;
   float inv_freq[64];
@@ -62,7 +62,7 @@ struct TcParams {
 
 struct Layout {
   int Tm, n_mt, kv_rows;
-  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_ids, off_red, off_bias, off_bar,
+  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_bar,
       bytes;
   uint32_t p_col, o_col, lo_col, tmem_cols;
 };
@@ -83,8 +83,6 @@ Layout plan(const Problem& pb) {
   // consecutive tokens start on different banks
   L.tab_stride = (uint32_t)(pb.d / 4) * 16 + 16;
   off += (uint32_t)pb.l * L.tab_stride;
-  L.off_ids = off;
-  off += 2u * kMaxBlocksPerPair * 4;
   L.off_red = off;
   off += 2u * 2 * 128 * 4;  // partial row max and row sum of each half
   L.off_bias = off;
@@ -149,7 +147,6 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   Bars* bars = reinterpret_cast<Bars*>(smem + prm.off_bar);
-  int32_t* ids = reinterpret_cast<int32_t*>(smem + prm.off_ids);
   float* red_max = reinterpret_cast<float*>(smem + prm.off_red);  // [2][128]
   float* red_sum = red_max + 256;                                  // [2][128]
   const uint8_t* tab = smem + prm.off_tab;
@@ -309,50 +306,53 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     auto chunk_addr = [](uint32_t base, uint32_t pstride, int row, int J) {
       return base + (J >> 3) * pstride + swz128(row, J & 7);
     };
-    // cp.async of unit u's K/V rows (cached, then new ones raw) into buffer b;
-    // true if one of its block ids is out of range (nothing is copied then).
+    // cp.async of unit u's K/V rows (cached, then new ones raw) into buffer b.
     auto stage_kv = [&](int u, int b) -> bool {
+      // Each thread copies one 16-byte chunk column (c) of every kRowStep-th
+      // row, so no per-row index arithmetic is needed; block ids are read by
+      // every thread (a broadcast load) instead of being shared through a
+      // barrier.  Returns true if one of this unit's block ids is out of range
+      // (its rows are then not copied).
+      constexpr int kRowStep = kCompute / CPR;
       const int p = u / prm.Hkv, g = u % prm.Hkv;
-      int32_t* bid = ids + b * kMaxBlocksPerPair;
+      const int c = tid % CPR, r0 = tid / CPR;
+      const uint32_t kb = sbase + prm.off_kv + b * prm.kv_buf_bytes;
+      const uint32_t vb = kb + NP * kv_panel;
+      const int bl = prm.pv.block_len;
       bool bad = false;
-      for (int i = tid; i < prm.pv.blocks_per_pair; i += kCompute) {
-        const int32_t blk = pool_block_id(prm.pv, p, i);
-        bad |= !pool_block_ok(prm.pv, blk);
-        bid[i] = blk;
+      for (int bi = 0; bi < prm.pv.blocks_per_pair; ++bi) {
+        const int32_t blk = pool_block_id(prm.pv, p, bi);
+        if (!pool_block_ok(prm.pv, blk)) {
+          bad = true;
+          continue;
+        }
+        const bf16* ks = pool_row(prm.pv, blk, g, 0, 0) + c * 8;
+        const bf16* vs = pool_row(prm.pv, blk, g, 1, 0) + c * 8;
+        for (int t = r0; t < bl; t += kRowStep) {
+          const uint32_t o = (c >> 3) * kv_panel + swz128(bi * bl + t, c & 7);
+          cp_async16(kb + o, ks + (size_t)t * D);
+          cp_async16(vb + o, vs + (size_t)t * D);
+        }
       }
-      bad = named_bar_or(kBarCompute, kCompute, bad);
-      if (!bad) {
-        const uint32_t kb = sbase + prm.off_kv + b * prm.kv_buf_bytes;
-        const uint32_t vb = kb + NP * kv_panel;
-        const int bl = prm.pv.block_len;
-        for (int idx = tid; idx < 2 * C * CPR; idx += kCompute) {
-          const int kv = idx >= C * CPR;
-          const int rr = idx - kv * C * CPR;
-          const int kappa = rr / CPR, c = rr - kappa * CPR;
-          const int bi = kappa / bl;
-          const bf16* src = pool_row(prm.pv, bid[bi], g, kv, kappa - bi * bl) + c * 8;
-          cp_async16((kv ? vb : kb) + (c >> 3) * kv_panel + swz128(kappa, c & 7), src);
-        }
-        for (int idx = tid; idx < 2 * l * CPR; idx += kCompute) {
-          const int kv = idx >= l * CPR;
-          const int rr = idx - kv * l * CPR;
-          const int t = rr / CPR, c = rr - t * CPR;
-          const bf16* src =
-              (kv ? prm.v_new : prm.k_new) + (((int64_t)p * l + t) * prm.Hkv + g) * D + c * 8;
-          cp_async16((kv ? vb : kb) + (c >> 3) * kv_panel + swz128(C + t, c & 7), src);
-        }
+      const size_t row_stride = (size_t)prm.Hkv * D;  // between consecutive new tokens
+      const size_t first = ((size_t)p * l * prm.Hkv + g) * D + c * 8;
+      for (int t = r0; t < l; t += kRowStep) {
+        const uint32_t o = (c >> 3) * kv_panel + swz128(C + t, c & 7);
+        cp_async16(kb + o, prm.k_new + first + t * row_stride);
+        cp_async16(vb + o, prm.v_new + first + t * row_stride);
       }
       cp_async_commit();
       return bad;
     };
-    // Unit k's K/V have landed (each thread waited for its own copies): rotate
-    // its new keys in place with the table of its positions.
-    auto prepare_unit = [&](int k, bool bad) {
+    // Unit k's K/V have landed (each thread waited for its own copies): share
+    // the unit's block-id status (bad: in, this thread's; out, the unit's) and
+    // rotate its new keys in place with the table of its positions.
+    auto prepare_unit = [&](int k, bool& bad) {
       if (prm.pos_offset) {
         named_bar_sync(kBarCompute, kCompute);  // nobody still reads the previous table
         build_table(prm.pos_offset[unit_of(k) / prm.Hkv], kCompute);
       }
-      named_bar_sync(kBarCompute, kCompute);
+      bad = named_bar_or(kBarCompute, kCompute, bad);
       if (!bad) {
         const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
         for (int idx = tid; idx < l * (CPR / 2); idx += kCompute) {
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       const int tt = min(r / G, toks - 1);
       wait(&bars->qfull[s], (uint32_t)(i / kStages) & 1u);
       constexpr int JH = CPR / 4;  // chunk pairs per half
-      uint32_t lo_a[JH * 4], lo_b[JH * 4];
+      uint32_t lo_a[4], lo_b[4];
       const uint8_t* trow = tab + (t0 + tt) * prm.tab_stride;
 #pragma unroll
       for (int jj = 0; jj < JH; ++jj) {
@@ -400,23 +400,14 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
         uint32_t xh[4], yh[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          f2_split_bf16(xr[e], xh[e], lo_a[jj * 4 + e]);
-          f2_split_bf16(yr[e], yh[e], lo_b[jj * 4 + e]);
+          f2_split_bf16(xr[e], xh[e], lo_a[e]);
+          f2_split_bf16(yr[e], yh[e], lo_b[e]);
         }
         sts16(a0, make_uint4(xh[0], xh[1], xh[2], xh[3]));
         sts16(a1, make_uint4(yh[0], yh[1], yh[2], yh[3]));
-      }
-      // TMEM column c of the lo block holds q elements (2c, 2c+1)
-#pragma unroll
-      for (int q8 = 0; q8 < JH / 2; ++q8) {
-        uint32_t va[8], vb8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          va[e] = lo_a[q8 * 8 + e];
-          vb8[e] = lo_b[q8 * 8 + e];
-        }
-        tc::st8(tmem + lane_base + prm.lo_col + (h * JH + q8 * 2) * 4, va);
-        tc::st8(tmem + lane_base + prm.lo_col + (h * JH + q8 * 2 + CPR / 2) * 4, vb8);
+        // TMEM column c of the lo block holds q elements (2c, 2c+1)
+        tc::st4(tmem + lane_base + prm.lo_col + J * 4, lo_a[0], lo_a[1], lo_a[2], lo_a[3]);
+        tc::st4(tmem + lane_base + prm.lo_col + (J + CPR / 2) * 4, lo_b[0], lo_b[1], lo_b[2], lo_b[3]);
       }
       tc::wait_st();
       fence_proxy_async_smem();
@@ -424,7 +415,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       mbar_arrive(&bars->rope_done);
     };
 
-    bool bad0 = false, bad1 = false;  // out-of-range block id in the unit of K/V buffer 0 / 1
+    // out-of-range block id in the unit of K/V buffer 0 / 1 (this thread's view
+    // until prepare_unit makes it the unit's)
+    bool bad0 = false, bad1 = false;
     if (my_units > 0) {
       bad0 = stage_kv(unit_of(0), 0);
       if (my_units > 1) {
@@ -524,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       if (i + 1 < my_tiles) {
         if ((i + 1) % n_mt == 0) {  // the next tile opens unit k+1
           cp_async_wait_group<0>();
-          prepare_unit(k + 1, ((k + 1) & 1) ? bad1 : bad0);
+          prepare_unit(k + 1, ((k + 1) & 1) ? bad1 : bad0);  // (a reference)
         }
         rope_tile(i + 1);
       }
@@ -623,7 +616,6 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.kv_buf_bytes = L.kv_buf_bytes;
   prm.off_tab = L.off_tab;
   prm.tab_stride = L.tab_stride;
-  prm.off_ids = L.off_ids;
   prm.off_red = L.off_red;
   prm.off_bias = L.off_bias;
   prm.off_bar = L.off_bar;
