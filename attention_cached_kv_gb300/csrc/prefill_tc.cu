@@ -212,9 +212,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     // ================================================================ MMA issue
     // All 32 lanes walk the loop (waits are uniform); lane 0 issues.
     bool failed = false;
-    for (int i = 0; i < my_tiles; ++i) {
+    // tile i is the mt-th tile of this CTA's k-th unit (kept incrementally:
+    // no integer division on the per-tile path)
+    for (int i = 0, k = 0, mt = 0; i < my_tiles; ++i, mt = (mt + 1 == n_mt) ? (++k, 0) : mt + 1) {
       const uint32_t par = (uint32_t)i & 1u;
-      const int k = i / n_mt, mt = i % n_mt;
       const uint32_t stage = sbase + (i % kStages) * prm.stage_bytes;
       const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
       const uint32_t vb = kb + NP * kv_panel;
@@ -261,9 +262,15 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     // Q tiles in, O tiles out; a stage is refilled kStages tiles on as soon as
     // the store of its output has read it.
     bool failed = false;
-    auto load_tile = [&](int i) {
+    // loads and stores each walk the tiles in order: (unit, tile-in-unit) cursors
+    int lk = 0, lmt = 0, sk = 0, smt = 0;
+    auto load_tile = [&](int i) {  // i = the next tile to load
       if (i >= my_tiles) return;
-      const int u = unit_of(i / n_mt), mt = i % n_mt, s = i % kStages;
+      const int u = unit_of(lk), mt = lmt, s = i % kStages;
+      if (++lmt == n_mt) {
+        lmt = 0;
+        ++lk;
+      }
       const int p = u / prm.Hkv, g = u % prm.Hkv;
       mbar_arrive_expect_tx(&bars->qfull[s], (uint32_t)NP * Tm * G * 128);
 #pragma unroll
@@ -282,7 +289,11 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
         break;
       }
       if (lane == 0) {
-        const int u = unit_of(i / n_mt), mt = i % n_mt, s = i % kStages;
+        const int u = unit_of(sk), mt = smt, s = i % kStages;
+        if (++smt == n_mt) {
+          smt = 0;
+          ++sk;
+        }
         const int p = u / prm.Hkv, g = u % prm.Hkv;
 #pragma unroll
         for (int pn = 0; pn < NP; ++pn)
@@ -378,14 +389,15 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       if (!failed && !mbar_wait(bar, parity)) failed = true;
     };
     const uint32_t pair_bar = 2 + (warp & 3);  // this row's two threads (warps w, w + 4)
+    const int row_tok = r / G;                  // token of row r within its tile
     // Rotate row r of tile i's q (this half's chunk pairs): hi -> stage, lo -> TMEM.
     // Rows past the tile's tokens hold zeros (TMA fill, or set-up for rows no
     // box reaches), so their hi and lo come out zero without a select.
-    auto rope_tile = [&](int i) {
-      const int s = i % kStages, mt = i % n_mt;
+    auto rope_tile = [&](int i, int mt) {
+      const int s = i % kStages;
       const uint32_t stage = sbase + s * prm.stage_bytes;
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
-      const int tt = min(r / G, toks - 1);
+      const int tt = min(row_tok, toks - 1);
       wait(&bars->qfull[s], (uint32_t)(i / kStages) & 1u);
       constexpr int JH = CPR / 4;  // chunk pairs per half
       uint32_t lo_a[4], lo_b[4];
@@ -427,15 +439,14 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
         cp_async_wait_group<0>();
       }
       prepare_unit(0, bad0);
-      rope_tile(0);
+      rope_tile(0, 0);
     }
-    for (int i = 0; i < my_tiles; ++i) {
+    for (int i = 0, k = 0, mt = 0; i < my_tiles; ++i, mt = (mt + 1 == n_mt) ? (++k, 0) : mt + 1) {
       const uint32_t par = (uint32_t)i & 1u;
-      const int k = i / n_mt, mt = i % n_mt;
       const bool bad = (k & 1) ? bad1 : bad0;
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
-      const bool valid = r < toks * G;
-      const int tt = min(r / G, toks - 1);
+      const bool valid = row_tok < toks;
+      const int tt = min(row_tok, toks - 1);
       const int N = (C + t0 + toks + 15) & ~15;
       // ---- softmax of row r over this half's 16-column chunks c = h, h+2, ...
       // (read from TMEM twice: for the max, then for the exponentials; holding
@@ -515,11 +526,11 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       mbar_arrive(&bars->p_done);
       // ---- next tile's K/V and q rotation (overlaps O = P V on the tensor core)
       if (i + 1 < my_tiles) {
-        if ((i + 1) % n_mt == 0) {  // the next tile opens unit k+1
+        if (mt + 1 == n_mt) {  // the next tile opens unit k+1
           cp_async_wait_group<0>();
           prepare_unit(k + 1, ((k + 1) & 1) ? bad1 : bad0);  // (a reference)
         }
-        rope_tile(i + 1);
+        rope_tile(i + 1, mt + 1 == n_mt ? 0 : mt + 1);
       }
       // ---- O of row r, this half's columns, normalised into the stage
       wait(&bars->o_done, par);
@@ -535,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
               sts16(chunk_addr(stage, kPanel, r, h * 2 * OC + J), make_uint4(0, 0, 0, 0));
           }
         } else {
-          const float inv = 1.f / (red_sum[r] + red_sum[128 + r]);
+          const float inv = rcp_approx(red_sum[r] + red_sum[128 + r]);
           const uint64_t inv2 = f2_make(inv, inv);
 #pragma unroll
           for (int c = 0; c < OC; ++c) {
