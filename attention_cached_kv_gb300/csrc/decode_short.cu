@@ -6,16 +6,18 @@
 // read-only blocks) and to its own key, and its K/V are never stored.
 // [KV page, "Reusable-state"]: o_t = softmax(q_t K_{<=t}^T / sqrt(d_k)) V_{<=t}.
 //
-// One warp per (pair, KV head).  The warp copies the group's G query rows, the
-// cached K/V rows (through the pool gather) and the new value row into its own
-// shared-memory region with 16-byte cp.async, rotates the new key in
-// registers, and runs the whole (G <= 16) x (C + 1 <= 32) x d problem as
-// tensor-core tiles: the query fragments are rotated in registers and split
-// into bf16 hi + lo (two MMA passes, so the rounding of rotated q stays out of
-// the logits), S = q K^T and O = P V on mma.sync m16n8k16 with fp32
-// accumulation, the softmax on the S fragments with quad shuffles.  Rows are
-// written straight from the accumulator fragments.  (The problem is 7 x 17 x
-// 64 here; the 5th-generation MMA needs at least 64 rows.)
+// Persistent warps, one (pair, KV head) unit at a time, two units in flight per
+// warp: while a warp computes unit n from one shared-memory buffer, the 16-byte
+// cp.async copies of unit n+1 (its cached K/V rows through the pool gather, its
+// new key and value rows) fill the other buffer, its query rows travel straight
+// into registers in the mma fragment layout, and the block ids of unit n+2 are
+// on their way.  A unit is (G <= 16) x (C + 1 <= 32) x d: the query fragments
+// are rotated in registers and split into bf16 hi + lo (two MMA passes, so the
+// rounding of rotated q stays out of the logits), S = q K^T and O = P V run on
+// mma.sync (m16n8k16, and m16n8k8 for a last 8-key step) with fp32
+// accumulation, the softmax on the S fragments with quad shuffles; rows are
+// written straight from the accumulator fragments.  (The problem is 7 x 17 x 64
+// here; the 5th-generation MMA needs at least 64 rows.)
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上";
 //        [KV page] "为什么自回归推理缓存 KV，而不缓存历史 Q？".
@@ -41,216 +43,307 @@ struct ShortParams {
   const int32_t* pos_offset;
   int32_t* status;
   int Hq, Hkv, G, C;
+  int kvr;          // key rows per buffer: C + 1 rounded up to 8
+  uint32_t region;  // bytes of one warp's shared memory
   int64_t units;
   float scale_log2;
   float inv_freq[64];
 };
 
+// One warp's shared memory: two buffers, each with the K panels then the V
+// panels (kvr rows of 128 bytes, 128-byte swizzle), then the (cos, sin) table of
+// the new token's position.
 template <int D>
-struct WarpRegion {  // per-warp shared memory, 128-byte swizzled rows
-  static constexpr uint32_t kPanelQ = 16 * 128;         // one 64-column panel of 16 q rows
-  static constexpr uint32_t kPanelKV = kMaxKeys * 128;  // one panel of 32 key rows
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + (D / 64) * kPanelQ;
-  static constexpr uint32_t kV = kK + (D / 64) * kPanelKV;
-  static constexpr uint32_t kTab = kV + (D / 64) * kPanelKV;  // (cos, sin) per frequency
-  static constexpr uint32_t kIds = kTab + (D / 2) * 8;         // the pair's block ids
-  static constexpr uint32_t kBytes = kIds + kMaxBlocks * 4;
+struct Region {
+  static constexpr int NP = D / 64;
+  __host__ __device__ static uint32_t panel(int kvr) { return (uint32_t)kvr * 128; }
+  __host__ __device__ static uint32_t buf(int kvr) { return 2u * NP * panel(kvr); }
+  __host__ __device__ static uint32_t tab(int kvr) { return 2 * buf(kvr); }
+  __host__ __device__ static uint32_t bytes(int kvr) { return (tab(kvr) + (D / 2) * 8 + 127) & ~127u; }
 };
+
+// D(16x8) += A(16x8, bf16, row) * B(8x8, bf16, col)
+__device__ __forceinline__ void mma_1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6},"
+      " {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+__device__ __forceinline__ uint32_t ldg32(const bf16* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_constant__ ShortParams prm) {
-  using R = WarpRegion<D>;
+  using R = Region<D>;
+  constexpr int NP = D / 64;
   constexpr int CPR = D / 8;
   constexpr int HALF = D / 2;
+  constexpr int KS = D / 16;  // k-steps of the q fragments
   constexpr float kNegInf = -INFINITY;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t unit = (int64_t)blockIdx.x * kWarps + warp;
-  if (unit >= prm.units) return;
-  const int g = (int)(unit % prm.Hkv);
-  const int64_t p = unit / prm.Hkv;
-  const int G = prm.G, C = prm.C, NK = C + 1;
-  const int bl = prm.pv.block_len;
-  uint8_t* reg = smem + warp * ((R::kBytes + 1023) & ~1023u);
+  const int64_t W = (int64_t)gridDim.x * kWarps;
+  int64_t u = (int64_t)blockIdx.x * kWarps + warp;
+  if (u >= prm.units) return;  // warp-uniform; nothing below synchronises the CTA
+  const int G = prm.G, C = prm.C, NK = C + 1, kvr = prm.kvr;
+  const int bpp = prm.pv.blocks_per_pair, bl = prm.pv.block_len;
+  uint8_t* reg = smem + warp * prm.region;
   const uint32_t base = smem_u32(reg);
-  const uint32_t sQ = base + R::kQ, sK = base + R::kK, sV = base + R::kV;
-  auto addr = [](uint32_t b, uint32_t pstride, int row, int chunk) {
-    return b + (chunk >> 3) * pstride + swz128(row, chunk & 7);
+  const uint32_t pnl = R::panel(kvr), bufb = R::buf(kvr);
+  float2* tab = reinterpret_cast<float2*>(reg + R::tab(kvr));
+  auto kaddr = [&](int b, int row, int c) {
+    return base + b * bufb + (c >> 3) * pnl + swz128(row, c & 7);
+  };
+  auto vaddr = [&](int b, int row, int c) {
+    return base + b * bufb + (NP + (c >> 3)) * pnl + swz128(row, c & 7);
   };
 
-  // block ids of this pair (lanes < blocks_per_pair), kept in the warp's region
-  int32_t* ids = reinterpret_cast<int32_t*>(reg + R::kIds);
-  bool bad = false;
-  if (lane < prm.pv.blocks_per_pair) {
-    const int32_t blk = pool_block_id(prm.pv, (int)p, lane);
-    bad = !pool_block_ok(prm.pv, blk);
-    ids[lane] = blk;
-  }
-  bad = __any_sync(0xffffffffu, bad);
-  __syncwarp();  // the ids are visible to every lane
-  bf16* out = prm.out + (p * prm.Hq + (int64_t)g * G) * D;
-  if (bad) {
-    for (int idx = lane; idx < G * D / 8; idx += 32)
-      *reinterpret_cast<uint4*>(out + idx * 8) = make_uint4(0, 0, 0, 0);
-    if (lane == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
-    return;
-  }
-
-  // ---- copies: q rows, cached K/V rows, the new V row; zero the rest
-  const bf16* qsrc = prm.q + (p * prm.Hq + (int64_t)g * G) * D;
-  for (int idx = lane; idx < G * CPR; idx += 32) {
-    const int row = idx / CPR, c = idx - row * CPR;
-    cp_async16(addr(sQ, R::kPanelQ, row, c), qsrc + row * D + c * 8);
-  }
-  for (int idx = lane; idx < 2 * C * CPR; idx += 32) {
-    const int kv = idx >= C * CPR;
-    const int rr = idx - kv * C * CPR;
-    const int kappa = rr / CPR, c = rr - kappa * CPR;
-    const int bi = kappa / bl;
-    cp_async16(addr(kv ? sV : sK, R::kPanelKV, kappa, c),
-               pool_row(prm.pv, ids[bi], g, kv, kappa - bi * bl) + c * 8);
-  }
-  const bf16* vsrc = prm.v_new + (p * prm.Hkv + g) * D;
-  for (int c = lane; c < CPR; c += 32) cp_async16(addr(sV, R::kPanelKV, C, c), vsrc + c * 8);
-  cp_async_commit();
-  const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int idx = lane; idx < (16 - G) * CPR; idx += 32) {
-    const int row = G + idx / CPR, c = idx % CPR;
-    sts16(addr(sQ, R::kPanelQ, row, c), z);
-  }
-  for (int idx = lane; idx < 2 * (kMaxKeys - NK) * CPR; idx += 32) {
-    const int kv = idx >= (kMaxKeys - NK) * CPR;
-    const int rr = idx - kv * (kMaxKeys - NK) * CPR;
-    const int row = NK + rr / CPR, c = rr % CPR;
-    sts16(addr(kv ? sV : sK, R::kPanelKV, row, c), z);
-  }
-  // cos/sin of the new token's position, and its rotated key (row C)
-  const float pos = (float)(prm.pos_offset ? prm.pos_offset[p] : C);
-  float2* tab = reinterpret_cast<float2*>(reg + R::kTab);
-  for (int j = lane; j < HALF; j += 32) {
-    float s, c;
-    sincosf(pos * prm.inv_freq[j], &s, &c);
-    tab[j] = make_float2(c, s);
-  }
-  __syncwarp();
-  {
-    const bf16* ksrc = prm.k_new + (p * prm.Hkv + g) * D;
-    for (int c = lane; c < CPR / 2; c += 32) {
-      uint4 lo = ldg16(ksrc + c * 8), hi = ldg16(ksrc + HALF + c * 8);
-      uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w}, hw[4] = {hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 c0 = tab[c * 8 + 2 * e], c1 = tab[c * 8 + 2 * e + 1];
-        const float2 x = bf16x2_to_float2(lw[e]), y = bf16x2_to_float2(hw[e]);
-        lw[e] = float2_to_bf16x2(x.x * c0.x - y.x * c0.y, x.y * c1.x - y.y * c1.y);
-        hw[e] = float2_to_bf16x2(y.x * c0.x + x.x * c0.y, y.y * c1.x + x.y * c1.y);
-      }
-      sts16(addr(sK, R::kPanelKV, C, c), make_uint4(lw[0], lw[1], lw[2], lw[3]));
-      sts16(addr(sK, R::kPanelKV, C, c + CPR / 2), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+  // rows past the keys stay zero in both buffers (no copy writes them)
+  if (kvr > NK) {
+    const int pad = kvr - NK;
+    for (int idx = lane; idx < 2 * 2 * pad * CPR; idx += 32) {
+      const int c = idx % CPR, rest = idx / CPR;
+      const int row = NK + rest % pad, kv = (rest / pad) & 1, b = rest / (2 * pad);
+      sts16(kv ? vaddr(b, row, c) : kaddr(b, row, c), make_uint4(0, 0, 0, 0));
     }
   }
-  cp_async_wait_all();
-  __syncwarp();
+  auto build_tab = [&](int pos) {
+    for (int j = lane; j < HALF; j += 32) {
+      float s, c;
+      sincosf((float)pos * prm.inv_freq[j], &s, &c);
+      tab[j] = make_float2(c, s);
+    }
+    __syncwarp();
+  };
+  const bool fixed_pos = prm.pos_offset == nullptr;
+  if (fixed_pos) build_tab(C);
 
-  // ---- q fragments (rows 0..15 = heads), rotated, scaled, split into hi + lo
-  uint32_t qh[D / 16][4], ql[D / 16][4];
-  {
-    const int row = lane & 15;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) ldsm_x4(addr(sQ, R::kPanelQ, row, ks * 2 + (lane >> 4)), qh[ks]);
-    const float sc = prm.scale_log2;
-#pragma unroll
-    for (int ks = 0; ks < D / 32; ++ks) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int j = ks * 16 + 2 * (lane & 3) + ((r & 2) ? 8 : 0);
-        const float2 c0 = tab[j], c1 = tab[j + 1];
-        const float2 x = bf16x2_to_float2(qh[ks][r]), y = bf16x2_to_float2(qh[ks + D / 32][r]);
-        const uint64_t xr = f2_make((x.x * c0.x - y.x * c0.y) * sc, (x.y * c1.x - y.y * c1.y) * sc);
-        const uint64_t yr = f2_make((y.x * c0.x + x.x * c0.y) * sc, (y.y * c1.x + x.y * c1.y) * sc);
-        f2_split_bf16(xr, qh[ks][r], ql[ks][r]);
-        f2_split_bf16(yr, qh[ks + D / 32][r], ql[ks + D / 32][r]);
+  // block id of the unit's lane-th block (lanes < blocks_per_pair)
+  auto load_id = [&](int64_t v) -> int32_t {
+    return (v < prm.units && lane < bpp) ? pool_block_id(prm.pv, (int)(v / prm.Hkv), lane) : 0;
+  };
+  // cp.async of unit v's rows into buffer b; true (warp-uniform) if one of its
+  // block ids is out of range (its cached rows are then not copied)
+  auto issue = [&](int64_t v, int b, int32_t id) -> bool {
+    const int g = (int)(v % prm.Hkv);
+    const int64_t p = v / prm.Hkv;
+    const bool bad = __any_sync(0xffffffffu, lane < bpp && !pool_block_ok(prm.pv, id));
+    constexpr int kStep = 32 / CPR;  // rows per pass of the warp
+    const int c = lane % CPR, r0 = lane / CPR;
+    if (!bad) {
+      for (int bi = 0; bi < bpp; ++bi) {  // uniform loop: the shuffle is safe
+        const int32_t blk = __shfl_sync(0xffffffffu, id, bi);
+        const bf16* ks = pool_row(prm.pv, blk, g, 0, 0) + c * 8;
+        const bf16* vs = pool_row(prm.pv, blk, g, 1, 0) + c * 8;
+        for (int t = r0; t < bl; t += kStep) {
+          cp_async16(kaddr(b, bi * bl + t, c), ks + (size_t)t * D);
+          cp_async16(vaddr(b, bi * bl + t, c), vs + (size_t)t * D);
+        }
       }
     }
-  }
-  // ---- S = q K^T over 32 keys (4 n-tiles)
-  float s[4][4];
-#pragma unroll
-  for (int n = 0; n < 4; ++n) {
-    s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-    const int krow = n * 8 + (lane & 7);
-#pragma unroll
-    for (int k2 = 0; k2 < D / 32; ++k2) {
-      uint32_t b[4];
-      ldsm_x4(addr(sK, R::kPanelKV, krow, k2 * 4 + (lane >> 3)), b);
-      mma_16816(s[n], qh[2 * k2], b[0], b[1]);
-      mma_16816(s[n], qh[2 * k2 + 1], b[2], b[3]);
-      mma_16816(s[n], ql[2 * k2], b[0], b[1]);
-      mma_16816(s[n], ql[2 * k2 + 1], b[2], b[3]);
+    // the new token's raw key (rotated later) and its value: row C
+    const size_t nrow = ((size_t)p * prm.Hkv + g) * D;
+    for (int c2 = lane; c2 < 2 * CPR; c2 += 32) {
+      if (c2 < CPR)
+        cp_async16(kaddr(b, C, c2), prm.k_new + nrow + c2 * 8);
+      else
+        cp_async16(vaddr(b, C, c2 - CPR), prm.v_new + nrow + (c2 - CPR) * 8);
     }
-  }
-  // ---- softmax over the NK valid keys (rows: lane/4 and lane/4 + 8)
-  float ma = kNegInf, mb = kNegInf;
+    cp_async_commit();
+    return bad;
+  };
+  // unit v's query rows (heads) lane/4 and lane/4 + 8 of its group in the mma
+  // A-fragment layout: columns ks*16 + 2(lane%4) + {0, 1} and + 8
+  auto load_q = [&](int64_t v, uint32_t (&a)[KS][4]) {
+    const int g = (int)(v % prm.Hkv);
+    const int64_t p = v / prm.Hkv;
+    const bf16* q0 = prm.q + (p * prm.Hq + (int64_t)g * G) * D + 2 * (lane & 3);
+    const int ra = lane >> 2, rb = ra + 8;
 #pragma unroll
-  for (int n = 0; n < 4; ++n) {
-    const int key = n * 8 + 2 * (lane & 3);
-    s[n][0] = key < NK ? s[n][0] : kNegInf;
-    s[n][1] = key + 1 < NK ? s[n][1] : kNegInf;
-    s[n][2] = key < NK ? s[n][2] : kNegInf;
-    s[n][3] = key + 1 < NK ? s[n][3] : kNegInf;
-    ma = max3f(ma, s[n][0], s[n][1]);
-    mb = max3f(mb, s[n][2], s[n][3]);
-  }
-  ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
-  ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
-  mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-  mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-  float la = 0.f, lb = 0.f;
-#pragma unroll
-  for (int n = 0; n < 4; ++n) {
-    s[n][0] = ex2_approx(s[n][0] - ma);
-    s[n][1] = ex2_approx(s[n][1] - ma);
-    s[n][2] = ex2_approx(s[n][2] - mb);
-    s[n][3] = ex2_approx(s[n][3] - mb);
-    la += s[n][0] + s[n][1];
-    lb += s[n][2] + s[n][3];
-  }
-  la += __shfl_xor_sync(0xffffffffu, la, 1);
-  la += __shfl_xor_sync(0xffffffffu, la, 2);
-  lb += __shfl_xor_sync(0xffffffffu, lb, 1);
-  lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-  // ---- O = P V (2 key steps of 16)
-  float o[D / 8][4];
-#pragma unroll
-  for (int dn = 0; dn < D / 8; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
-    uint32_t pa[4];
-    pa[0] = float2_to_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-    pa[1] = float2_to_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-    pa[2] = float2_to_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-    pa[3] = float2_to_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-    const int vrow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int dq = 0; dq < D / 16; ++dq) {
-      uint32_t b[4];
-      ldsm_x4_trans(addr(sV, R::kPanelKV, vrow, dq * 2 + (lane >> 4)), b);
-      mma_16816(o[2 * dq], pa, b[0], b[1]);
-      mma_16816(o[2 * dq + 1], pa, b[2], b[3]);
+    for (int ks = 0; ks < KS; ++ks) {
+      a[ks][0] = ra < G ? ldg32(q0 + (size_t)ra * D + ks * 16) : 0u;
+      a[ks][2] = ra < G ? ldg32(q0 + (size_t)ra * D + ks * 16 + 8) : 0u;
+      a[ks][1] = rb < G ? ldg32(q0 + (size_t)rb * D + ks * 16) : 0u;
+      a[ks][3] = rb < G ? ldg32(q0 + (size_t)rb * D + ks * 16 + 8) : 0u;
     }
-  }
-  // ---- rows 0..G-1 straight to global (row lane/4; rows lane/4 + 8 when G > 8)
-  const int ra = lane >> 2, rb = ra + 8;
-  const float ia = 1.f / la, ib = 1.f / lb;
+  };
+
+  // ---- prologue: unit u's copies and query; the next unit's block ids
+  uint32_t qcur[KS][4];
+  bool bad_cur = issue(u, 0, load_id(u));
+  load_q(u, qcur);
+  int64_t un = u + W;
+  int32_t id_next = load_id(un);
+
+  for (int n = 0;; ++n) {
+    const int b = n & 1;
+    // ---- unit un's copies into the other buffer (free since the last unit),
+    // its query into registers, and the block ids of the unit after it
+    uint32_t qnext[KS][4];
+    bool bad_next = false;
+    const bool more = un < prm.units;
+    if (more) {
+      bad_next = issue(un, b ^ 1, id_next);
+      load_q(un, qnext);
+      id_next = load_id(un + W);
+      cp_async_wait_group<1>();
+    } else {
+      cp_async_wait_group<0>();
+    }
+    __syncwarp();  // every lane's copies of unit u have landed
+
+    // ---- unit u
+    const int g = (int)(u % prm.Hkv);
+    const int64_t p = u / prm.Hkv;
+    bf16* out = prm.out + (p * prm.Hq + (int64_t)g * G) * D;
+    if (bad_cur) {
+      for (int idx = lane; idx < G * CPR; idx += 32)
+        *reinterpret_cast<uint4*>(out + idx * 8) = make_uint4(0, 0, 0, 0);
+      if (lane == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
+    } else {
+      if (!fixed_pos) build_tab(prm.pos_offset[p]);
+      // the new key (row C), rotated in place: lane j takes frequencies j, j + 32
+      for (int j = lane; j < HALF; j += 32) {
+        const float2 cs = tab[j];
+        const uint32_t ax = kaddr(b, C, j >> 3) + (j & 7) * 2;
+        const uint32_t ay = kaddr(b, C, (j + HALF) >> 3) + (j & 7) * 2;
+        uint16_t xb, yb;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(xb) : "r"(ax));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(yb) : "r"(ay));
+        const float x = __uint_as_float((uint32_t)xb << 16), y = __uint_as_float((uint32_t)yb << 16);
+        const bf16 xr = __float2bfloat16_rn(x * cs.x - y * cs.y);
+        const bf16 yr = __float2bfloat16_rn(y * cs.x + x * cs.y);
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(ax), "h"(*reinterpret_cast<const uint16_t*>(&xr)));
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(ay), "h"(*reinterpret_cast<const uint16_t*>(&yr)));
+      }
+      __syncwarp();
+
+      // ---- q fragments: rotated, scaled, split into hi + lo
+      uint32_t qh[KS][4], ql[KS][4];
+      {
+        const float sc = prm.scale_log2;
 #pragma unroll
-  for (int dn = 0; dn < D / 8; ++dn) {
-    const int col = dn * 8 + 2 * (lane & 3);
-    if (ra < G)
-      *reinterpret_cast<uint32_t*>(out + (int64_t)ra * D + col) = float2_to_bf16x2(o[dn][0] * ia, o[dn][1] * ia);
-    if (rb < G)
-      *reinterpret_cast<uint32_t*>(out + (int64_t)rb * D + col) = float2_to_bf16x2(o[dn][2] * ib, o[dn][3] * ib);
+        for (int ks = 0; ks < KS / 2; ++ks) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = ks * 16 + 2 * (lane & 3) + ((r & 2) ? 8 : 0);
+            const float2 c0 = tab[j], c1 = tab[j + 1];
+            const float2 x = bf16x2_to_float2(qcur[ks][r]), y = bf16x2_to_float2(qcur[ks + KS / 2][r]);
+            const uint64_t xr = f2_make((x.x * c0.x - y.x * c0.y) * sc, (x.y * c1.x - y.y * c1.y) * sc);
+            const uint64_t yr = f2_make((y.x * c0.x + x.x * c0.y) * sc, (y.y * c1.x + x.y * c1.y) * sc);
+            f2_split_bf16(xr, qh[ks][r], ql[ks][r]);
+            f2_split_bf16(yr, qh[ks + KS / 2][r], ql[ks + KS / 2][r]);
+          }
+        }
+      }
+      // ---- S = q K^T over kvr keys (n-tiles of 8)
+      float s[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        if (nt * 8 < kvr) {
+          const int krow = nt * 8 + (lane & 7);
+#pragma unroll
+          for (int k2 = 0; k2 < D / 32; ++k2) {
+            uint32_t bb[4];
+            ldsm_x4(kaddr(b, krow, k2 * 4 + (lane >> 3)), bb);
+            mma_16816(s[nt], qh[2 * k2], bb[0], bb[1]);
+            mma_16816(s[nt], qh[2 * k2 + 1], bb[2], bb[3]);
+            mma_16816(s[nt], ql[2 * k2], bb[0], bb[1]);
+            mma_16816(s[nt], ql[2 * k2 + 1], bb[2], bb[3]);
+          }
+        }
+      }
+      // ---- softmax over the NK valid keys (rows: lane/4 and lane/4 + 8)
+      float ma = kNegInf, mb = kNegInf;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int key = nt * 8 + 2 * (lane & 3);
+        s[nt][0] = key < NK ? s[nt][0] : kNegInf;
+        s[nt][1] = key + 1 < NK ? s[nt][1] : kNegInf;
+        s[nt][2] = key < NK ? s[nt][2] : kNegInf;
+        s[nt][3] = key + 1 < NK ? s[nt][3] : kNegInf;
+        ma = max3f(ma, s[nt][0], s[nt][1]);
+        mb = max3f(mb, s[nt][2], s[nt][3]);
+      }
+      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      float la = 0.f, lb = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        s[nt][0] = ex2_approx(s[nt][0] - ma);
+        s[nt][1] = ex2_approx(s[nt][1] - ma);
+        s[nt][2] = ex2_approx(s[nt][2] - mb);
+        s[nt][3] = ex2_approx(s[nt][3] - mb);
+        la += s[nt][0] + s[nt][1];
+        lb += s[nt][2] + s[nt][3];
+      }
+      la += __shfl_xor_sync(0xffffffffu, la, 1);
+      la += __shfl_xor_sync(0xffffffffu, la, 2);
+      lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+      lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+      // ---- O = P V: key steps of 16, then one of 8 when kvr is an odd multiple of 8
+      float o[D / 8][4];
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        if (kk * 16 + 16 <= kvr) {
+          uint32_t pa[4];
+          pa[0] = float2_to_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+          pa[1] = float2_to_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+          pa[2] = float2_to_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+          pa[3] = float2_to_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+          const int vrow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int dq = 0; dq < D / 16; ++dq) {
+            uint32_t bb[4];
+            ldsm_x4_trans(vaddr(b, vrow, dq * 2 + (lane >> 4)), bb);
+            mma_16816(o[2 * dq], pa, bb[0], bb[1]);
+            mma_16816(o[2 * dq + 1], pa, bb[2], bb[3]);
+          }
+        } else if (kk * 16 + 8 == kvr) {
+          const uint32_t a0 = float2_to_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+          const uint32_t a1 = float2_to_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+          const int vrow = kk * 16 + (lane & 7);
+#pragma unroll
+          for (int cq = 0; cq < D / 32; ++cq) {  // four 8-column n-tiles per load
+            uint32_t bb[4];
+            ldsm_x4_trans(vaddr(b, vrow, cq * 4 + (lane >> 3)), bb);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) mma_1688(o[4 * cq + m], a0, a1, bb[m]);
+          }
+        }
+      }
+      // ---- rows 0..G-1 straight to global (row lane/4; rows lane/4 + 8 when G > 8)
+      const int ra = lane >> 2, rb = ra + 8;
+      const float ia = rcp_approx(la), ib = rcp_approx(lb);
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) {
+        const int col = dn * 8 + 2 * (lane & 3);
+        if (ra < G)
+          *reinterpret_cast<uint32_t*>(out + (int64_t)ra * D + col) = float2_to_bf16x2(o[dn][0] * ia, o[dn][1] * ia);
+        if (rb < G)
+          *reinterpret_cast<uint32_t*>(out + (int64_t)rb * D + col) = float2_to_bf16x2(o[dn][2] * ib, o[dn][3] * ib);
+      }
+    }
+    __syncwarp();  // buffer b is free for the unit after next
+    if (!more) break;
+    u = un;
+    un += W;
+    bad_cur = bad_next;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) qcur[ks][r] = qnext[ks][r];
   }
 }
 
@@ -269,17 +362,25 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.Hkv = pb.Hkv;
   prm.G = pb.G;
   prm.C = pb.C;
+  prm.kvr = (pb.C + 1 + 7) / 8 * 8;
+  prm.region = Region<D>::bytes(prm.kvr);
   prm.units = (int64_t)pb.P * pb.Hkv;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
-  const uint32_t per_warp = (WarpRegion<D>::kBytes + 1023) & ~1023u;
-  const uint32_t bytes = kWarps * per_warp;
-  if (bytes > 48 * 1024 &&
-      cudaFuncSetAttribute(decode_short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const uint32_t bytes = kWarps * prm.region;
+  if (cudaFuncSetAttribute(decode_short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
-  const int64_t grid = (prm.units + kWarps - 1) / kWarps;
-  if (grid > 0x7fffffff) return GIST_ATTN_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_short_kernel<D>, kThreads,
+                                                    bytes) != cudaSuccess ||
+      per_sm < 1)
+    return GIST_ATTN_ERR_LAUNCH;
+  // persistent: one wave of resident CTAs walks all units
+  const int64_t need = (prm.units + kWarps - 1) / kWarps;
+  const int64_t grid = need < (int64_t)sms * per_sm ? need : (int64_t)sms * per_sm;
   decode_short_kernel<D><<<(unsigned)grid, kThreads, bytes, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
