@@ -45,7 +45,7 @@ struct ShortParams {
   int Hq, Hkv, G, C;
   int kvr;          // key rows per buffer: C + 1 rounded up to 8
   uint32_t region;  // bytes of one warp's shared memory
-  int64_t units;
+  int units;        // P * Hkv (below 2^31)
   float scale_log2;
   float inv_freq[64];
 };
@@ -77,7 +77,9 @@ __device__ __forceinline__ uint32_t ldg32(const bf16* p) {
   return v;
 }
 
-template <int D>
+// G8: the group has at most 8 query heads, so rows 8..15 of every 16-row
+// fragment are zero and their work is left out at compile time.
+template <int D, bool G8>
 __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_constant__ ShortParams prm) {
   using R = Region<D>;
   constexpr int NP = D / 64;
@@ -88,8 +90,8 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t W = (int64_t)gridDim.x * kWarps;
-  int64_t u = (int64_t)blockIdx.x * kWarps + warp;
+  const int W = gridDim.x * kWarps;
+  int u = blockIdx.x * kWarps + warp;
   if (u >= prm.units) return;  // warp-uniform; nothing below synchronises the CTA
   const int G = prm.G, C = prm.C, NK = C + 1, kvr = prm.kvr;
   const int bpp = prm.pv.blocks_per_pair, bl = prm.pv.block_len;
@@ -113,11 +115,16 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       sts16(kv ? vaddr(b, row, c) : kaddr(b, row, c), make_uint4(0, 0, 0, 0));
     }
   }
+  // (cos, sin) of the new token's position: lane j keeps frequencies j (and
+  // j + 32) in registers for the key; the table holds them times the softmax
+  // scale for the query fragments
+  float kcos[HALF / 32], ksin[HALF / 32];
   auto build_tab = [&](int pos) {
-    for (int j = lane; j < HALF; j += 32) {
-      float s, c;
-      sincosf((float)pos * prm.inv_freq[j], &s, &c);
-      tab[j] = make_float2(c, s);
+#pragma unroll
+    for (int e = 0; e < HALF / 32; ++e) {
+      const int j = lane + 32 * e;
+      sincosf((float)pos * prm.inv_freq[j], &ksin[e], &kcos[e]);
+      tab[j] = make_float2(kcos[e] * prm.scale_log2, ksin[e] * prm.scale_log2);
     }
     __syncwarp();
   };
@@ -125,14 +132,12 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   if (fixed_pos) build_tab(C);
 
   // block id of the unit's lane-th block (lanes < blocks_per_pair)
-  auto load_id = [&](int64_t v) -> int32_t {
-    return (v < prm.units && lane < bpp) ? pool_block_id(prm.pv, (int)(v / prm.Hkv), lane) : 0;
+  auto load_id = [&](int v) -> int32_t {
+    return (v < prm.units && lane < bpp) ? pool_block_id(prm.pv, v / prm.Hkv, lane) : 0;
   };
   // cp.async of unit v's rows into buffer b; true (warp-uniform) if one of its
   // block ids is out of range (its cached rows are then not copied)
-  auto issue = [&](int64_t v, int b, int32_t id) -> bool {
-    const int g = (int)(v % prm.Hkv);
-    const int64_t p = v / prm.Hkv;
+  auto issue = [&](int p, int g, int b, int32_t id) -> bool {
     const bool bad = __any_sync(0xffffffffu, lane < bpp && !pool_block_ok(prm.pv, id));
     constexpr int kStep = 32 / CPR;  // rows per pass of the warp
     const int c = lane % CPR, r0 = lane / CPR;
@@ -160,25 +165,25 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   };
   // unit v's query rows (heads) lane/4 and lane/4 + 8 of its group in the mma
   // A-fragment layout: columns ks*16 + 2(lane%4) + {0, 1} and + 8
-  auto load_q = [&](int64_t v, uint32_t (&a)[KS][4]) {
-    const int g = (int)(v % prm.Hkv);
-    const int64_t p = v / prm.Hkv;
-    const bf16* q0 = prm.q + (p * prm.Hq + (int64_t)g * G) * D + 2 * (lane & 3);
+  auto load_q = [&](int p, int g, uint32_t (&a)[KS][4]) {
+    const bf16* q0 = prm.q + ((size_t)p * prm.Hq + (size_t)g * G) * D + 2 * (lane & 3);
     const int ra = lane >> 2, rb = ra + 8;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       a[ks][0] = ra < G ? ldg32(q0 + (size_t)ra * D + ks * 16) : 0u;
       a[ks][2] = ra < G ? ldg32(q0 + (size_t)ra * D + ks * 16 + 8) : 0u;
-      a[ks][1] = rb < G ? ldg32(q0 + (size_t)rb * D + ks * 16) : 0u;
-      a[ks][3] = rb < G ? ldg32(q0 + (size_t)rb * D + ks * 16 + 8) : 0u;
+      a[ks][1] = (!G8 && rb < G) ? ldg32(q0 + (size_t)rb * D + ks * 16) : 0u;
+      a[ks][3] = (!G8 && rb < G) ? ldg32(q0 + (size_t)rb * D + ks * 16 + 8) : 0u;
     }
   };
 
   // ---- prologue: unit u's copies and query; the next unit's block ids
   uint32_t qcur[KS][4];
-  bool bad_cur = issue(u, 0, load_id(u));
-  load_q(u, qcur);
-  int64_t un = u + W;
+  int p = u / prm.Hkv, g = u - p * prm.Hkv;
+  bool bad_cur = issue(p, g, 0, load_id(u));
+  load_q(p, g, qcur);
+  int un = u + W;
+  int pn = un / prm.Hkv, gn = un - pn * prm.Hkv;
   int32_t id_next = load_id(un);
 
   for (int n = 0;; ++n) {
@@ -189,8 +194,8 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     bool bad_next = false;
     const bool more = un < prm.units;
     if (more) {
-      bad_next = issue(un, b ^ 1, id_next);
-      load_q(un, qnext);
+      bad_next = issue(pn, gn, b ^ 1, id_next);
+      load_q(pn, gn, qnext);
       id_next = load_id(un + W);
       cp_async_wait_group<1>();
     } else {
@@ -198,10 +203,8 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     }
     __syncwarp();  // every lane's copies of unit u have landed
 
-    // ---- unit u
-    const int g = (int)(u % prm.Hkv);
-    const int64_t p = u / prm.Hkv;
-    bf16* out = prm.out + (p * prm.Hq + (int64_t)g * G) * D;
+    // ---- unit u = (pair p, KV head g)
+    bf16* out = prm.out + ((size_t)p * prm.Hq + (size_t)g * G) * D;
     if (bad_cur) {
       for (int idx = lane; idx < G * CPR; idx += 32)
         *reinterpret_cast<uint4*>(out + idx * 8) = make_uint4(0, 0, 0, 0);
@@ -209,8 +212,10 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     } else {
       if (!fixed_pos) build_tab(prm.pos_offset[p]);
       // the new key (row C), rotated in place: lane j takes frequencies j, j + 32
-      for (int j = lane; j < HALF; j += 32) {
-        const float2 cs = tab[j];
+#pragma unroll
+      for (int e = 0; e < HALF / 32; ++e) {
+        const int j = lane + 32 * e;
+        const float2 cs = make_float2(kcos[e], ksin[e]);
         const uint32_t ax = kaddr(b, C, j >> 3) + (j & 7) * 2;
         const uint32_t ay = kaddr(b, C, (j + HALF) >> 3) + (j & 7) * 2;
         uint16_t xb, yb;
@@ -226,20 +231,20 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
 
       // ---- q fragments: rotated, scaled, split into hi + lo
       uint32_t qh[KS][4], ql[KS][4];
-      {
-        const float sc = prm.scale_log2;
 #pragma unroll
-        for (int ks = 0; ks < KS / 2; ++ks) {
+      for (int ks = 0; ks < KS / 2; ++ks) {
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int j = ks * 16 + 2 * (lane & 3) + ((r & 2) ? 8 : 0);
-            const float2 c0 = tab[j], c1 = tab[j + 1];
-            const float2 x = bf16x2_to_float2(qcur[ks][r]), y = bf16x2_to_float2(qcur[ks + KS / 2][r]);
-            const uint64_t xr = f2_make((x.x * c0.x - y.x * c0.y) * sc, (x.y * c1.x - y.y * c1.y) * sc);
-            const uint64_t yr = f2_make((y.x * c0.x + x.x * c0.y) * sc, (y.y * c1.x + x.y * c1.y) * sc);
-            f2_split_bf16(xr, qh[ks][r], ql[ks][r]);
-            f2_split_bf16(yr, qh[ks + KS / 2][r], ql[ks + KS / 2][r]);
+        for (int r = 0; r < 4; ++r) {
+          if (G8 && (r & 1)) {  // rows 8..15
+            qh[ks][r] = ql[ks][r] = qh[ks + KS / 2][r] = ql[ks + KS / 2][r] = 0u;
+            continue;
           }
+          const int j = ks * 16 + 2 * (lane & 3) + ((r & 2) ? 8 : 0);
+          const float4 cs = *reinterpret_cast<const float4*>(&tab[j]);  // (c_j, s_j, c_j+1, s_j+1)
+          const uint64_t c = f2_make(cs.x, cs.z), sn = f2_make(cs.y, cs.w);
+          const uint64_t x = bf16x2_to_f2(qcur[ks][r]), y = bf16x2_to_f2(qcur[ks + KS / 2][r]);
+          f2_split_bf16(f2_sub(f2_mul(x, c), f2_mul(y, sn)), qh[ks][r], ql[ks][r]);
+          f2_split_bf16(f2_fma(y, c, f2_mul(x, sn)), qh[ks + KS / 2][r], ql[ks + KS / 2][r]);
         }
       }
       // ---- S = q K^T over kvr keys (n-tiles of 8)
@@ -264,11 +269,13 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       float ma = kNegInf, mb = kNegInf;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-        const int key = nt * 8 + 2 * (lane & 3);
-        s[nt][0] = key < NK ? s[nt][0] : kNegInf;
-        s[nt][1] = key + 1 < NK ? s[nt][1] : kNegInf;
-        s[nt][2] = key < NK ? s[nt][2] : kNegInf;
-        s[nt][3] = key + 1 < NK ? s[nt][3] : kNegInf;
+        if (nt * 8 + 8 > NK) {  // the n-tile holding the last key, or past it (uniform)
+          const int key = nt * 8 + 2 * (lane & 3);
+          s[nt][0] = key < NK ? s[nt][0] : kNegInf;
+          s[nt][1] = key + 1 < NK ? s[nt][1] : kNegInf;
+          s[nt][2] = key < NK ? s[nt][2] : kNegInf;
+          s[nt][3] = key + 1 < NK ? s[nt][3] : kNegInf;
+        }
         ma = max3f(ma, s[nt][0], s[nt][1]);
         mb = max3f(mb, s[nt][2], s[nt][3]);
       }
@@ -279,12 +286,18 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       float la = 0.f, lb = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-        s[nt][0] = ex2_approx(s[nt][0] - ma);
-        s[nt][1] = ex2_approx(s[nt][1] - ma);
-        s[nt][2] = ex2_approx(s[nt][2] - mb);
-        s[nt][3] = ex2_approx(s[nt][3] - mb);
-        la += s[nt][0] + s[nt][1];
-        lb += s[nt][2] + s[nt][3];
+        if (nt * 8 < kvr) {
+          s[nt][0] = ex2_approx(s[nt][0] - ma);
+          s[nt][1] = ex2_approx(s[nt][1] - ma);
+          la += s[nt][0] + s[nt][1];
+          if (G8) {
+            s[nt][2] = s[nt][3] = 0.f;
+          } else {
+            s[nt][2] = ex2_approx(s[nt][2] - mb);
+            s[nt][3] = ex2_approx(s[nt][3] - mb);
+            lb += s[nt][2] + s[nt][3];
+          }
+        }
       }
       la += __shfl_xor_sync(0xffffffffu, la, 1);
       la += __shfl_xor_sync(0xffffffffu, la, 2);
@@ -331,14 +344,18 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         const int col = dn * 8 + 2 * (lane & 3);
         if (ra < G)
           *reinterpret_cast<uint32_t*>(out + (int64_t)ra * D + col) = float2_to_bf16x2(o[dn][0] * ia, o[dn][1] * ia);
-        if (rb < G)
+        if (!G8 && rb < G)
           *reinterpret_cast<uint32_t*>(out + (int64_t)rb * D + col) = float2_to_bf16x2(o[dn][2] * ib, o[dn][3] * ib);
       }
     }
     __syncwarp();  // buffer b is free for the unit after next
     if (!more) break;
     u = un;
+    p = pn;
+    g = gn;
     un += W;
+    pn = un / prm.Hkv;
+    gn = un - pn * prm.Hkv;
     bad_cur = bad_next;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
@@ -347,7 +364,7 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   }
 }
 
-template <int D>
+template <int D, bool G8>
 int launch_d(const Problem& pb, cudaStream_t stream) {
   ShortParams prm{};
   prm.q = static_cast<const bf16*>(pb.q);
@@ -364,24 +381,24 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.C = pb.C;
   prm.kvr = (pb.C + 1 + 7) / 8 * 8;
   prm.region = Region<D>::bytes(prm.kvr);
-  prm.units = (int64_t)pb.P * pb.Hkv;
+  prm.units = pb.P * pb.Hkv;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
   const uint32_t bytes = kWarps * prm.region;
-  if (cudaFuncSetAttribute(decode_short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_short_kernel<D, G8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_short_kernel<D>, kThreads,
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_short_kernel<D, G8>, kThreads,
                                                     bytes) != cudaSuccess ||
       per_sm < 1)
     return GIST_ATTN_ERR_LAUNCH;
   // persistent: one wave of resident CTAs walks all units
   const int64_t need = (prm.units + kWarps - 1) / kWarps;
   const int64_t grid = need < (int64_t)sms * per_sm ? need : (int64_t)sms * per_sm;
-  decode_short_kernel<D><<<(unsigned)grid, kThreads, bytes, stream>>>(prm);
+  decode_short_kernel<D, G8><<<(unsigned)grid, kThreads, bytes, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
@@ -389,12 +406,13 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
 
 bool decode_short_fits(const Problem& pb) {
   return pb.l == 1 && pb.G <= 16 && pb.C + 1 <= kMaxKeys && pb.blocks_per_pair <= kMaxBlocks &&
-         (pb.d == 64 || pb.d == 128);
+         (pb.d == 64 || pb.d == 128) && (int64_t)pb.P * pb.Hkv <= (1 << 30);  // int unit indices
 }
 
 int launch_decode_short(const Problem& pb, cudaStream_t stream) {
-  if (pb.d == 64) return launch_d<64>(pb, stream);
-  if (pb.d == 128) return launch_d<128>(pb, stream);
+  const bool g8 = pb.G <= 8;
+  if (pb.d == 64) return g8 ? launch_d<64, true>(pb, stream) : launch_d<64, false>(pb, stream);
+  if (pb.d == 128) return g8 ? launch_d<128, true>(pb, stream) : launch_d<128, false>(pb, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 
