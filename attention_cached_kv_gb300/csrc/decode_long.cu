@@ -19,8 +19,10 @@
 //
 // The same kernel reads an FP8 (E4M3) pool ([Suffix page, §2 and the end of §5]:
 // 1-byte KV elements), one fp32 scale per (block, layer, K|V, KV head): the
-// chunks are half as many bytes, widened in registers (e4m3 -> f16x2 -> f32),
-// the K scale multiplies the logit and the V scale the value weight.
+// chunks are half as many bytes, widened in registers only to f16 pairs
+// (cvt e4m3x2 -> f16x2) and multiplied against the f16 query slice and the
+// f16 value weight with fp32 accumulation (mixed-precision FMA); the K scale
+// multiplies the logit and the V scale the value weight.
 //
 // With STATS it also writes, per (sequence, head, cached block), the block's
 // attention mass -- the sum of the softmax weights of its rows -- the statistic
@@ -71,10 +73,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v16) {
+// acc + a * b with a, b f16 (the low halves of the two registers) and fp32 acc
+__device__ __forceinline__ float fma_f16f32(uint32_t a, uint32_t b, float acc) {
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"((unsigned short)a), "h"((unsigned short)b));
+  return acc;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
   uint32_t h;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)v16));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return h;
 }
 
 template <int D, bool FP8, bool STATS>
@@ -170,6 +177,16 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
   float qr[QE];
 #pragma unroll
   for (int e = 0; e < QE; ++e) qr[e] = qs[sl * QE + e];
+  // FP8: the query slice as f16 (low half of each register), for the mixed
+  // f16 x f16 + fp32 products against keys widened only to f16
+  uint32_t qh[FP8 ? QE : 1];
+  if constexpr (FP8) {
+#pragma unroll
+    for (int e = 0; e < QE; ++e) {
+      const __half hq = __float2half_rn(qr[e]);
+      qh[e] = *reinterpret_cast<const unsigned short*>(&hq);
+    }
+  }
   float m = kNegInf, lsum = 0.f, o[VE], last_share = kNegInf;
 #pragma unroll
   for (int e = 0; e < VE; ++e) o[e] = 0.f;
@@ -194,13 +211,19 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
       const float pj = __shfl_sync(0xffffffffu, pk, j * 8) * vsc;
       if constexpr (FP8) {
         const uint8_t* vr = vrows + j * kRow + lane * VE;
+        const __half ph = __float2half_rn(pj);
+        const uint32_t p16 = *reinterpret_cast<const unsigned short*>(&ph);
         if constexpr (VE == 4) {
           const uint32_t raw = *reinterpret_cast<const uint32_t*>(vr);
-          const float2 a = e4m3x2_to_float2(raw & 0xffffu), b2 = e4m3x2_to_float2(raw >> 16);
-          o[0] += pj * a.x; o[1] += pj * a.y; o[2] += pj * b2.x; o[3] += pj * b2.y;
+          const uint32_t a = e4m3x2_to_f16x2(raw & 0xffffu), b2 = e4m3x2_to_f16x2(raw >> 16);
+          o[0] = fma_f16f32(p16, a, o[0]);
+          o[1] = fma_f16f32(p16, a >> 16, o[1]);
+          o[2] = fma_f16f32(p16, b2, o[2]);
+          o[3] = fma_f16f32(p16, b2 >> 16, o[3]);
         } else {
-          const float2 a = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vr));
-          o[0] += pj * a.x; o[1] += pj * a.y;
+          const uint32_t a = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(vr));
+          o[0] = fma_f16f32(p16, a, o[0]);
+          o[1] = fma_f16f32(p16, a >> 16, o[1]);
         }
       } else {
         const uint8_t* vr = vrows + j * kRow + lane * VE * 2;
@@ -234,11 +257,11 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
       }
 #pragma unroll
       for (int e = 0; e < QE / 4; ++e) {
-        const float2 k0 = e4m3x2_to_float2(w[e] & 0xffffu), k1 = e4m3x2_to_float2(w[e] >> 16);
-        acc = fmaf(qr[4 * e], k0.x, acc);
-        acc = fmaf(qr[4 * e + 1], k0.y, acc);
-        acc = fmaf(qr[4 * e + 2], k1.x, acc);
-        acc = fmaf(qr[4 * e + 3], k1.y, acc);
+        const uint32_t k0 = e4m3x2_to_f16x2(w[e] & 0xffffu), k1 = e4m3x2_to_f16x2(w[e] >> 16);
+        acc = fma_f16f32(qh[4 * e], k0, acc);
+        acc = fma_f16f32(qh[4 * e + 1], k0 >> 16, acc);
+        acc = fma_f16f32(qh[4 * e + 2], k1, acc);
+        acc = fma_f16f32(qh[4 * e + 3], k1 >> 16, acc);
       }
     } else {
       const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE * 2;
