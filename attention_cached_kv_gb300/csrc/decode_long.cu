@@ -240,12 +240,10 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
   };
 
   bool ok = true;
-  for (int ci = 0; ci < n_chunks; ++ci) {
-    const int s = ci % kStages;
-    ok = mbar_wait(&full[s], (uint32_t)(ci / kStages) & 1u) && ok;
-    const uint8_t* stage = ring + s * kStageBytes;
-    float acc = 0.f;
-    if constexpr (FP8) {
+  if constexpr (FP8) {
+    // Two 16-key chunks per step (an fp8 chunk is half the bytes of a bf16 one):
+    // one online-softmax update and one barrier per 8 keys of a warp.
+    auto kdot = [&](const uint8_t* stage) {
       const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE;
       uint32_t w[QE / 4];
       if constexpr (QE == 16) {
@@ -255,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
         const uint2 raw = *reinterpret_cast<const uint2*>(krow);
         w[0] = raw.x; w[1] = raw.y;
       }
+      float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < QE / 4; ++e) {
         const uint32_t k0 = e4m3x2_to_f16x2(w[e] & 0xffffu), k1 = e4m3x2_to_f16x2(w[e] >> 16);
@@ -263,35 +262,124 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
         acc = fma_f16f32(qh[4 * e + 2], k1, acc);
         acc = fma_f16f32(qh[4 * e + 3], k1 >> 16, acc);
       }
-    } else {
-      const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE * 2;
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      return acc;
+    };
+    auto vacc = [&](const uint8_t* stage, float pk, float vsc) {
+      const uint8_t* vrows = stage + kChunk * kRow + warp * 4 * kRow;
 #pragma unroll
-      for (int v = 0; v < QE / 8; ++v) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(krow + v * 16);
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 kf = bf16x2_to_float2(w[e]);
-          acc = fmaf(qr[v * 8 + 2 * e], kf.x, acc);
-          acc = fmaf(qr[v * 8 + 2 * e + 1], kf.y, acc);
+      for (int j = 0; j < 4; ++j) {
+        const __half ph = __float2half_rn(__shfl_sync(0xffffffffu, pk, j * 8) * vsc);
+        const uint32_t p16 = *reinterpret_cast<const unsigned short*>(&ph);
+        const uint8_t* vr = vrows + j * kRow + lane * VE;
+        if constexpr (VE == 4) {
+          const uint32_t raw = *reinterpret_cast<const uint32_t*>(vr);
+          const uint32_t a = e4m3x2_to_f16x2(raw & 0xffffu), b2 = e4m3x2_to_f16x2(raw >> 16);
+          o[0] = fma_f16f32(p16, a, o[0]);
+          o[1] = fma_f16f32(p16, a >> 16, o[1]);
+          o[2] = fma_f16f32(p16, b2, o[2]);
+          o[3] = fma_f16f32(p16, b2 >> 16, o[3]);
+        } else {
+          const uint32_t a = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(vr));
+          o[0] = fma_f16f32(p16, a, o[0]);
+          o[1] = fma_f16f32(p16, a >> 16, o[1]);
         }
       }
+    };
+    for (int ci = 0; ci < n_chunks; ci += 2) {
+      const bool two = ci + 1 < n_chunks;  // uniform
+      const int s0 = ci % kStages, s1 = (ci + 1) % kStages;
+      ok = mbar_wait(&full[s0], (uint32_t)(ci / kStages) & 1u) && ok;
+      if (two) ok = mbar_wait(&full[s1], (uint32_t)((ci + 1) / kStages) & 1u) && ok;
+      const uint8_t* st0 = ring + s0 * kStageBytes;
+      const uint8_t* st1 = ring + s1 * kStageBytes;
+      const int b0 = (ci * kChunk) / bl, b1 = ((ci + 1) * kChunk) / bl;
+      const float x0 = kdot(st0) * kscale[b0];
+      const float x1 = two ? kdot(st1) * kscale[b1] : kNegInf;
+      float cm = fmaxf(x0, x1);
+      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
+      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+      const float mn = fmaxf(m, cm);
+      const float al = ex2_approx(m - mn);
+      const float p0 = ex2_approx(x0 - mn), p1 = ex2_approx(x1 - mn);
+      m = mn;
+      float ps0 = p0 + __shfl_xor_sync(0xffffffffu, p0, 8);
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 16);
+      float ps1 = p1 + __shfl_xor_sync(0xffffffffu, p1, 8);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 16);
+      lsum = lsum * al + ps0 + ps1;
+#pragma unroll
+      for (int e = 0; e < VE; ++e) o[e] *= al;
+      vacc(st0, p0, vscale[b0]);
+      if (two) vacc(st1, p1, vscale[b1]);
+      if constexpr (STATS) {
+        if (lane == 0) {
+          chunk_lg[ci][warp] = ps0 > 0.f ? __log2f(ps0) + mn : kNegInf;
+          if (two) chunk_lg[ci + 1][warp] = ps1 > 0.f ? __log2f(ps1) + mn : kNegInf;
+        }
+      }
+      __syncthreads();  // every warp is done with both stages
+      if (tid == 0) {
+        if (ci + kStages < n_chunks) issue(ci + kStages);
+        if (ci + 1 + kStages < n_chunks) issue(ci + 1 + kStages);
+      }
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    float vsc = 1.f;
-    if constexpr (FP8) {
-      const int b = (ci * kChunk) / bl;
-      acc *= kscale[b];
-      vsc = vscale[b];
+  } else {
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int s = ci % kStages;
+      ok = mbar_wait(&full[s], (uint32_t)(ci / kStages) & 1u) && ok;
+      const uint8_t* stage = ring + s * kStageBytes;
+      float acc = 0.f;
+      if constexpr (FP8) {
+        const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE;
+        uint32_t w[QE / 4];
+        if constexpr (QE == 16) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(krow);
+          w[0] = raw.x; w[1] = raw.y; w[2] = raw.z; w[3] = raw.w;
+        } else {
+          const uint2 raw = *reinterpret_cast<const uint2*>(krow);
+          w[0] = raw.x; w[1] = raw.y;
+        }
+  #pragma unroll
+        for (int e = 0; e < QE / 4; ++e) {
+          const uint32_t k0 = e4m3x2_to_f16x2(w[e] & 0xffffu), k1 = e4m3x2_to_f16x2(w[e] >> 16);
+          acc = fma_f16f32(qh[4 * e], k0, acc);
+          acc = fma_f16f32(qh[4 * e + 1], k0 >> 16, acc);
+          acc = fma_f16f32(qh[4 * e + 2], k1, acc);
+          acc = fma_f16f32(qh[4 * e + 3], k1 >> 16, acc);
+        }
+      } else {
+        const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE * 2;
+  #pragma unroll
+        for (int v = 0; v < QE / 8; ++v) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(krow + v * 16);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 kf = bf16x2_to_float2(w[e]);
+            acc = fmaf(qr[v * 8 + 2 * e], kf.x, acc);
+            acc = fmaf(qr[v * 8 + 2 * e + 1], kf.y, acc);
+          }
+        }
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      float vsc = 1.f;
+      if constexpr (FP8) {
+        const int b = (ci * kChunk) / bl;
+        acc *= kscale[b];
+        vsc = vscale[b];
+      }
+      consume(acc, true, stage + kChunk * kRow + warp * 4 * kRow, vsc);
+      if constexpr (STATS) {
+        if (lane == 0) chunk_lg[ci][warp] = last_share;
+      }
+      __syncthreads();  // every warp is done with stage s
+      if (tid == 0 && ci + kStages < n_chunks) issue(ci + kStages);
     }
-    consume(acc, true, stage + kChunk * kRow + warp * 4 * kRow, vsc);
-    if constexpr (STATS) {
-      if (lane == 0) chunk_lg[ci][warp] = last_share;
-    }
-    __syncthreads();  // every warp is done with stage s
-    if (tid == 0 && ci + kStages < n_chunks) issue(ci + kStages);
   }
   // the new token's own key and value (warp 0, group 0)
   if (warp == 0) {
