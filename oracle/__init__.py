@@ -6,7 +6,8 @@ nothing from it.
 
 The arithmetic lives in ``gist_attn_oracle.c`` (plain C, double precision);
 this module compiles it with gcc on first use and exposes it through ctypes.
-``gist_mask`` holds the training-side gist mask used by the brute-force pins.
+``gist_mask`` holds the training-side gist mask used by the brute-force pins;
+``projections`` the linear layers on either side of the attention.
 
 Sources are cited by page title and section:
   [Gist page]  "把 item 压成 KV：gist 能不能用在相关性任务上" (liam.page, 2026-10-30)
@@ -42,6 +43,7 @@ class OraDims(ctypes.Structure):
         ("layer", ctypes.c_int32),
         ("rope_theta", ctypes.c_double),
         ("softmax_scale", ctypes.c_double),
+        ("prerotated", ctypes.c_int32),
     ]
 
 
@@ -134,10 +136,14 @@ def make_dims(**kw) -> OraDims:
     d = OraDims()
     d.rope_theta = 1e4
     d.softmax_scale = 0.0
+    d.prerotated = 0
     d.num_layers = 1
     d.layer = 0
     for k, v in kw.items():
-        setattr(d, k, v)
+        if k == "flags":  # the library's flag word: bit 0 = q and k_new arrive rotated
+            d.prerotated = int(v) & 1
+        else:
+            setattr(d, k, v)
     return d
 
 

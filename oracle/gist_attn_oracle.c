@@ -67,6 +67,8 @@ typedef struct {
   int32_t layer;           /* layer this call reads                         */
   double rope_theta;       /* RoPE base                                     */
   double softmax_scale;    /* 0 -> 1/sqrt(d)                                */
+  int32_t prerotated;      /* 1: q and k_new arrive rotated at their positions
+                              (by the projection that made them): no RoPE here */
 } ora_dims;
 
 enum { ORA_OK = 0, ORA_BAD_ARG = -1, ORA_BAD_BLOCK = -2, ORA_NO_MEM = -3 };
@@ -232,7 +234,10 @@ static int attend_pair(const ora_job* J, int p, double* out_p, double* w_p) {
     /* New rows: K rotated at its own position, V as given. */
     for (int i = 0; i < l; ++i) {
       for (int e = 0; e < d; ++e) x[e] = elem(J, J->k_new, off_kvnew(D, p, i, g) + e);
-      ora_rope(x, d, pos0 + i, D->rope_theta, &keys[(size_t)(C + i) * d]);
+      if (D->prerotated)
+        memcpy(&keys[(size_t)(C + i) * d], x, sizeof(double) * (size_t)d);
+      else
+        ora_rope(x, d, pos0 + i, D->rope_theta, &keys[(size_t)(C + i) * d]);
       for (int e = 0; e < d; ++e)
         vals[(size_t)(C + i) * d + e] = elem(J, J->v_new, off_kvnew(D, p, i, g) + e);
     }
@@ -244,7 +249,10 @@ static int attend_pair(const ora_job* J, int p, double* out_p, double* w_p) {
         int hq = h;
 #endif
         for (int e = 0; e < d; ++e) x[e] = elem(J, J->q, off_q(D, p, i, hq) + e);
-        ora_rope(x, d, pos0 + i, D->rope_theta, qr);
+        if (D->prerotated)
+          memcpy(qr, x, sizeof(double) * (size_t)d);
+        else
+          ora_rope(x, d, pos0 + i, D->rope_theta, qr);
 #if ORA_PLANT == 2 /* not causal inside the new block */
         int n = C + l;
 #elif ORA_PLANT == 6 /* a token does not see its own key */

@@ -710,3 +710,71 @@ def test_offline_pass_store_then_online_equals_masked_forward():
     assert np.abs(plain[:, j + k:] - full[:, j + k:]).max() > 5e-2
     # and the rows before the gist's end are plain causal attention
     assert np.array_equal(plain[:, : j + k], full[:, : j + k])
+
+
+# ------------------------------- the projections either side of attention ---
+
+from oracle import projections as proj  # noqa: E402
+
+
+def test_qkv_rope_selects_and_rotates():
+    """gist page, 在线的一次 attention (per layer: project, then attend): with a
+    one-hot W_qkv the projected heads are chosen coordinates of x; Q and K are
+    then rotated at cached + t (complex-rotation RoPE, written independently)."""
+    P, l, Dm, Hq, Hkv, d, C = 2, 5, 24, 2, 1, 8, 7
+    rng = np.random.default_rng(3)
+    x = bf16((P, l, Dm), 100)
+    sel = rng.integers(0, Dm, size=(Hq + 2 * Hkv) * d)
+    w = torch.zeros(((Hq + 2 * Hkv) * d, Dm), dtype=torch.float32)
+    w[np.arange(len(sel)), torch.from_numpy(sel)] = 1.0
+    w = w.to(torch.bfloat16)
+    q, k, v = proj.qkv_rope(x, w, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, cached=C)
+    xf = f64(x)
+    picked = xf[:, :, sel]  # [P][l][(Hq + 2Hkv) d]
+    for p in range(P):
+        pos = C + np.arange(l)
+        for h in range(Hq):
+            want = rope_complex(picked[p, :, h * d:(h + 1) * d], pos)
+            assert np.abs(q[p, :, h] - want).max() < 1e-12
+        want_k = rope_complex(picked[p, :, Hq * d:(Hq + 1) * d], pos)
+        assert np.abs(k[p, :, 0] - want_k).max() < 1e-12
+        assert np.array_equal(v[p, :, 0], picked[p, :, (Hq + Hkv) * d:])
+    # given positions move the rotation
+    pos_off = np.array([100, 0])
+    q2, _, _ = proj.qkv_rope(x, w, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, cached=C,
+                             pos_offset=pos_off)
+    assert np.abs(q2[0, :, 0] - rope_complex(picked[0, :, :d], 100 + np.arange(l))).max() < 1e-12
+
+
+def test_prerotated_attention_equals_in_attention_rope():
+    """The attention given Q and K_new already rotated at their positions equals
+    the attention that rotates them itself."""
+    q, kn, vn, pool, table, pos0, D = small_case(17)
+    P, l = D["num_pairs"], D["n_new"]
+    qr = np.stack([np.stack([rope_complex(f64(q[p, :, h]), pos0[p] + np.arange(l))
+                             for h in range(q.shape[2])], axis=1) for p in range(P)])
+    kr = np.stack([np.stack([rope_complex(f64(kn[p, :, g]), pos0[p] + np.arange(l))
+                             for g in range(kn.shape[2])], axis=1) for p in range(P)])
+    a = oracle.gist_attn(f64(q), f64(kn), f64(vn), f64(pool), block_table=table, pos_offset=pos0,
+                         dims=D, f64_inputs=True)
+    b = oracle.gist_attn(qr, kr, f64(vn), f64(pool), block_table=table, pos_offset=pos0,
+                         dims=dict(D, flags=1), f64_inputs=True)
+    assert np.abs(a - b).max() < 1e-12
+    # without the flag the rotation would be applied twice
+    c = oracle.gist_attn(qr, kr, f64(vn), f64(pool), block_table=table, pos_offset=pos0, dims=D,
+                         f64_inputs=True)
+    assert np.abs(a - c).max() > 1e-3
+
+
+def test_out_proj_closed_form():
+    """A one-hot W_o picks attention columns; the projection is linear."""
+    M, K, N = 6, 32, 5
+    a = bf16((M, K), 110)
+    cols = np.array([3, 0, 31, 7, 7])
+    w = torch.zeros((N, K), dtype=torch.float32)
+    w[np.arange(N), torch.from_numpy(cols)] = 1.0
+    y = proj.out_proj(a, w.to(torch.bfloat16))
+    assert np.array_equal(y, f64(a)[:, cols])
+    w2 = bf16((N, K), 111)
+    y1, y2 = proj.out_proj(a, w2), proj.out_proj(f64(a) * 2.0, w2)
+    assert np.abs(y2 - 2.0 * y1).max() < 1e-12
