@@ -18,9 +18,11 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libgistattn.so")
 
 OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH = 0, -1, -2, -3, -4, -5
 STATUS_BAD_BLOCK, STATUS_TIMEOUT = 1, 2
+FLAG_PREROTATED = 1
 
 EXPORTS = ("gist_attn_fwd", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
-           "gist_attn_fwd_gist_mask", "gist_kv_store", "gist_attn_gather_debug", "gist_kv_bytes_per_position", "gist_kv_bytes_per_item",
+           "gist_attn_fwd_gist_mask", "gist_kv_store", "gist_qkv_rope", "gist_out_proj",
+           "gist_attn_gather_debug", "gist_kv_bytes_per_position", "gist_kv_bytes_per_item",
            "gist_kv_bytes_batch", "gist_attn_status_string")
 
 
@@ -46,6 +48,7 @@ class Dims(ctypes.Structure):
         ("rope_theta", ctypes.c_float),
         ("softmax_scale", ctypes.c_float),
         ("status", ctypes.c_void_p),
+        ("flags", ctypes.c_int32),
     ]
 
 
@@ -77,6 +80,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                     ctypes.POINTER(Dims), V]
             lib.gist_kv_store.restype = ctypes.c_int
             lib.gist_kv_store.argtypes = [V, V, V, V, V, V, ctypes.POINTER(Dims), V]
+            lib.gist_qkv_rope.restype = ctypes.c_int
+            lib.gist_qkv_rope.argtypes = [V, V, V, V, V, V, ctypes.c_int, ctypes.POINTER(Dims), V]
+            lib.gist_out_proj.restype = ctypes.c_int
+            lib.gist_out_proj.argtypes = [V, V, V, ctypes.c_int, ctypes.POINTER(Dims), V]
             lib.gist_attn_gather_debug.restype = ctypes.c_int
             lib.gist_attn_gather_debug.argtypes = [V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_kv_bytes_per_position.restype = ctypes.c_size_t
@@ -100,7 +107,7 @@ def make_dims(d: dict, status: torch.Tensor | None = None) -> Dims:
     for name, _ in Dims._fields_:
         if name == "status":
             continue
-        setattr(out, name, d[name])
+        setattr(out, name, d.get(name, 0) if name == "flags" else d[name])
     if status is not None:
         _check(status, torch.int32, "status")
         out.status = status.data_ptr()
@@ -241,6 +248,43 @@ def gist_kv_store(k_new, v_new, kv_pool, item_ids, first_row, store_pos=None, *,
                            _ptr(store_pos, i32, "store_pos"), ctypes.byref(D), _stream(stream))
     _raise(rc)
     return kv_pool
+
+
+def gist_qkv_rope(x, w_qkv, pos_offset=None, q=None, k_new=None, v_new=None, *, dims: dict,
+                  status=None, stream=None):
+    """QKV projection of x [P][l][d_model] with q and k rotated in the epilogue;
+    returns (q, k_new, v_new) for gist_attn_fwd with flags=FLAG_PREROTATED."""
+    lib = load_library()
+    P, l, Hq, Hkv, d = (dims["num_pairs"], dims["n_new"], dims["num_q_heads"], dims["num_kv_heads"],
+                        dims["head_dim"])
+    dev = x.device
+    if q is None:
+        q = torch.empty((P, l, Hq, d), dtype=torch.bfloat16, device=dev)
+    if k_new is None:
+        k_new = torch.empty((P, l, Hkv, d), dtype=torch.bfloat16, device=dev)
+    if v_new is None:
+        v_new = torch.empty((P, l, Hkv, d), dtype=torch.bfloat16, device=dev)
+    bf, i32 = torch.bfloat16, torch.int32
+    D = make_dims(dims, status)
+    rc = lib.gist_qkv_rope(_ptr(x, bf, "x"), _ptr(w_qkv, bf, "w_qkv"), _ptr(pos_offset, i32, "pos_offset"),
+                           _ptr(q, bf, "q"), _ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"),
+                           int(x.shape[-1]), ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return q, k_new, v_new
+
+
+def gist_out_proj(attn_out, w_o, y=None, *, dims: dict, status=None, stream=None):
+    """y [P][l][d_model] = attn_out [P][l][Hq][d] . w_o^T (w_o [d_model][Hq d])."""
+    lib = load_library()
+    d_model = int(w_o.shape[0])
+    if y is None:
+        y = torch.empty((dims["num_pairs"], dims["n_new"], d_model), dtype=torch.bfloat16,
+                        device=attn_out.device)
+    D = make_dims(dims, status)
+    rc = lib.gist_out_proj(_ptr(attn_out, torch.bfloat16, "attn_out"), _ptr(w_o, torch.bfloat16, "w_o"),
+                           _ptr(y, torch.bfloat16, "y"), d_model, ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return y
 
 
 def gist_attn_gather_debug(kv_pool, item_ids=None, block_table=None, dst=None, *, dims: dict,

@@ -70,11 +70,16 @@ int check_dims(const gist_attn_dims* dm, Problem* pb) {
   pb->C = (int)C;
   const double scale = d.softmax_scale > 0.f ? (double)d.softmax_scale : 1.0 / sqrt((double)d.head_dim);
   pb->scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
+  if (d.flags & ~GIST_ATTN_FLAG_PREROTATED) return GIST_ATTN_ERR_DIMS;
+  // pre-rotated inputs: every rotation angle is 0 (cos 1, sin 0), the identity
+  const bool rotate = !(d.flags & GIST_ATTN_FLAG_PREROTATED);
   for (int j = 0; j < 64; ++j) {
-    pb->inv_freq_d[j] =
-        j < d.head_dim / 2 ? pow((double)d.rope_theta, -2.0 * j / (double)d.head_dim) : 0.0;
+    pb->inv_freq_d[j] = rotate && j < d.head_dim / 2
+                            ? pow((double)d.rope_theta, -2.0 * j / (double)d.head_dim)
+                            : 0.0;
     pb->inv_freq[j] = (float)pb->inv_freq_d[j];
   }
+  pb->flags = d.flags;
   return GIST_ATTN_OK;
 }
 
@@ -258,6 +263,38 @@ extern "C" int gist_kv_store(const void* k_new, const void* v_new, void* kv_pool
   pb.v_new = v_new;
   pb.item_ids = item_ids;
   return gattn::launch_store(pb, kv_pool, first_row, store_pos, stream);
+}
+
+extern "C" int gist_qkv_rope(const void* x, const void* w_qkv, const int32_t* pos_offset, void* q,
+                             void* k_new, void* v_new, int d_model, const gist_attn_dims* dims,
+                             cudaStream_t stream) {
+  Problem pb{};
+  if (dims && (dims->flags & GIST_ATTN_FLAG_PREROTATED)) return GIST_ATTN_ERR_DIMS;
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (d_model < 1) return GIST_ATTN_ERR_DIMS;
+  if (pb.P == 0) return GIST_ATTN_OK;
+  if (!x || !w_qkv || !q || !k_new || !v_new) return GIST_ATTN_ERR_NULL;
+  if (!gattn::aligned(x, 16) || !gattn::aligned(w_qkv, 16) || !gattn::aligned(q, 16) ||
+      !gattn::aligned(k_new, 16) || !gattn::aligned(v_new, 16) || !gattn::aligned(pos_offset, 4) ||
+      !gattn::aligned(pb.status, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  pb.pos_offset = pos_offset;
+  return gattn::launch_qkv_rope(pb, x, w_qkv, d_model, q, k_new, v_new, stream);
+}
+
+extern "C" int gist_out_proj(const void* attn_out, const void* w_o, void* y, int d_model,
+                             const gist_attn_dims* dims, cudaStream_t stream) {
+  Problem pb{};
+  int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (d_model < 1) return GIST_ATTN_ERR_DIMS;
+  if (pb.P == 0) return GIST_ATTN_OK;
+  if (!attn_out || !w_o || !y) return GIST_ATTN_ERR_NULL;
+  if (!gattn::aligned(attn_out, 16) || !gattn::aligned(w_o, 16) || !gattn::aligned(y, 16) ||
+      !gattn::aligned(pb.status, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  return gattn::launch_out_proj(pb, attn_out, w_o, d_model, y, stream);
 }
 
 extern "C" int gist_attn_gather_debug(const void* kv_pool, const int32_t* item_ids,

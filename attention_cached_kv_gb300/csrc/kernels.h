@@ -25,6 +25,7 @@ struct Problem {
   int C;             // cached keys per pair
   const int32_t* gist_start;  // [P] or nullptr: the gist mask (streaming prefill only)
   int gist_len;
+  int flags;                  // GIST_ATTN_FLAG_* (pre-rotated inputs: inv_freq is all 0)
   float scale_log2;  // softmax scale * log2(e)
   float inv_freq[64];  // rope_theta^(-2j/d), j < d/2
   double inv_freq_d[64];  // the same in double (the pool writers rotate in double)
@@ -49,6 +50,11 @@ int launch_decode_long_stats(const Problem& pb, float* block_mass, cudaStream_t 
 int launch_append(const Problem& pb, void* pool, const int32_t* slot, cudaStream_t stream);
 int launch_store(const Problem& pb, void* pool, const int32_t* first_row, const int32_t* store_pos,
                  cudaStream_t stream);
+// The projections either side of the attention (gemm.cu).
+int launch_qkv_rope(const Problem& pb, const void* x, const void* w, int d_model, void* q,
+                    void* kn, void* vn, cudaStream_t stream);
+int launch_out_proj(const Problem& pb, const void* attn, const void* w, int d_model, void* y,
+                    cudaStream_t stream);
 
 // Whether the prefill kernel can hold this problem's tiles in shared memory.
 bool prefill_fits(const Problem& pb);

@@ -76,7 +76,12 @@ typedef struct {
   float rope_theta;        /* RoPE base (1e4 in the workloads), > 0                      */
   float softmax_scale;     /* 0 selects 1/sqrt(d) ([KV page, "Reusable-state"])          */
   int32_t* status;         /* optional device int32 status word (may be NULL)            */
+  int32_t flags;           /* GIST_ATTN_FLAG_* bits; 0 for the plain operation           */
 } gist_attn_dims;
+
+/* dims->flags: q and k_new arrive already rotated at their positions (for example
+ * by gist_qkv_rope), so the attention and the pool writers apply no RoPE. */
+#define GIST_ATTN_FLAG_PREROTATED 1
 
 /*
  * gist_attn_fwd -- one layer of attention for all pairs, one launch on `stream`.
@@ -208,6 +213,34 @@ int gist_attn_fwd_gist_mask(const void* q, const void* k_new, const void* v_new,
 int gist_kv_store(const void* k_new, const void* v_new, void* kv_pool, const int32_t* item_ids,
                   const int32_t* first_row, const int32_t* store_pos, const gist_attn_dims* dims,
                   cudaStream_t stream);
+
+/*
+ * gist_qkv_rope -- the QKV projection of the new tokens with RoPE in its
+ * epilogue, the fusion before the attention ([Gist page, "在线的一次 attention"]:
+ * per layer X is projected to Q, K, V, then attends).  For every new token row
+ * m = p*l + i:
+ *   [q | k | v][m] = x[m] . w_qkv^T   (fp32 accumulation), then q and k heads are
+ *   rotated at position pos_offset[p] + i (NULL: blocks_per_pair*block_len + i)
+ *   from the fp32 values and rounded once to bf16 (nearest even).
+ *   x      bf16 [P][l][d_model], 16-byte aligned, d_model a multiple of 8
+ *   w_qkv  bf16 [(Hq + 2 Hkv) d][d_model]: rows are q heads, then k heads, then v heads
+ *   q      bf16 [P][l][Hq][d];  k_new, v_new bf16 [P][l][Hkv][d]  (written)
+ * Feed the results to gist_attn_fwd with GIST_ATTN_FLAG_PREROTATED.  This build
+ * needs Hq*d and Hkv*d multiples of 128 and l >= 22 (a 128-row tile spans at most
+ * 8 pairs), else GIST_ATTN_ERR_UNSUPPORTED.
+ */
+int gist_qkv_rope(const void* x, const void* w_qkv, const int32_t* pos_offset, void* q,
+                  void* k_new, void* v_new, int d_model, const gist_attn_dims* dims,
+                  cudaStream_t stream);
+
+/*
+ * gist_out_proj -- the output projection after the attention: for every row
+ * m < P*l, y[m] = attn_out[m] . w_o^T (fp32 accumulation, bf16 out).
+ *   attn_out bf16 [P][l][Hq][d] (gist_attn_fwd's out), w_o bf16 [d_model][Hq d],
+ *   y bf16 [P][l][d_model] (written).  d_model must be a multiple of 128 and Hq*d of 8.
+ */
+int gist_out_proj(const void* attn_out, const void* w_o, void* y, int d_model,
+                  const gist_attn_dims* dims, cudaStream_t stream);
 
 /*
  * gist_attn_gather_debug -- copies, bit for bit, the cached rows each pair

@@ -134,3 +134,24 @@ def test_kv_store_rejects_bad_arguments(lib):
         assert f(V(P16), V(P16), V(P16), V(P16), V(P16), None, Db, None) == binding.ERR_DIMS
     Dz = ctypes.byref(binding.make_dims(dict(ok, num_pairs=0)))
     assert f(None, None, None, None, None, None, Dz, None) == binding.OK
+
+
+def test_projections_reject_bad_arguments(lib):
+    V = ctypes.c_void_p
+    D = ctypes.byref(binding.make_dims(dict(BASE, n_new=64)))
+    q = lib.gist_qkv_rope
+    assert q(None, V(P16), None, V(P16), V(P16), V(P16), 256, D, None) == binding.ERR_NULL
+    assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 0, D, None) == binding.ERR_DIMS
+    assert q(V(P16 + 2), V(P16), None, V(P16), V(P16), V(P16), 256, D, None) == binding.ERR_ALIGN
+    pre = ctypes.byref(binding.make_dims(dict(BASE, n_new=64, flags=binding.FLAG_PREROTATED)))
+    assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, pre, None) == binding.ERR_DIMS
+    odd = ctypes.byref(binding.make_dims(dict(BASE, n_new=64, num_q_heads=3, num_kv_heads=1)))
+    assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, odd, None) == binding.ERR_UNSUPPORTED
+    short = ctypes.byref(binding.make_dims(dict(BASE, n_new=4)))
+    assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, short, None) == binding.ERR_UNSUPPORTED
+    o = lib.gist_out_proj
+    assert o(V(P16), None, V(P16), 256, D, None) == binding.ERR_NULL
+    assert o(V(P16), V(P16), V(P16), 200, D, None) == binding.ERR_UNSUPPORTED  # not a multiple of 128
+    bad_flags = ctypes.byref(binding.make_dims(dict(BASE, flags=4)))
+    assert lib.gist_attn_fwd(V(P16), V(P16), V(P16), V(P16), V(P16), None, None, V(P16), bad_flags,
+                             None) == binding.ERR_DIMS
