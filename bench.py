@@ -68,6 +68,8 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="cached-KV element type (fp8: E4M3 pool with per-block scales)")
+    ap.add_argument("--fused", action="store_true",
+                    help="also time the projections either side (QKV + RoPE, output projection)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -376,11 +378,76 @@ def run_ours(args) -> dict:
         "impl": "ours",
     }
 
+    if args.fused and kv_scale is None and wl.dims["n_new"] > 1:
+        res["fused_layer"] = run_fused(args, wl, stream, ws)
     if not args.no_e2e and kv_scale is None:
         res["e2e"] = run_e2e(args, wl, lib, ptrs, dims_by_layer, stream, ws)
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
         res["cpu_baseline"] = oracle_rate(wl, 0, args.cpu_seconds)
     return res
+
+
+def run_fused(args, wl, stream, ws) -> dict:
+    """One layer's projections around the attention, each timed on its own:
+    QKV projection with RoPE in the epilogue, the attention on its pre-rotated
+    output, the output projection (d_model = Hq * d, synthetic weights)."""
+    import torch
+
+    from attention_cached_kv_gb300 import binding
+
+    d = wl.dims
+    P, l, Hq, Hkv, hd, L = (d["num_pairs"], d["n_new"], d["num_q_heads"], d["num_kv_heads"],
+                            d["head_dim"], d["num_layers"])
+    dm = Hq * hd
+    dev = wl.q.device
+    g = torch.Generator(device=dev).manual_seed(11)
+    x = torch.randn((P, l, dm), generator=g, device=dev).to(torch.bfloat16)
+    wqkv = (torch.randn(((Hq + 2 * Hkv) * hd, dm), generator=g, device=dev) / dm ** 0.5).to(torch.bfloat16)
+    wo = (torch.randn((dm, Hq * hd), generator=g, device=dev) / dm ** 0.5).to(torch.bfloat16)
+    q, kn, vn = torch.empty_like(wl.q), torch.empty_like(wl.k_new), torch.empty_like(wl.v_new)
+    attn, y = torch.empty_like(wl.q), torch.empty((P, l, dm), dtype=torch.bfloat16, device=dev)
+    pre = dict(d, flags=binding.FLAG_PREROTATED)
+    steps = max(1, min(args.steps, 5))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps * L)]
+
+    def layer(li, e=None):
+        dl = dict(d, layer=li)
+        with torch.cuda.stream(stream):
+            if e: e[0].record(stream)
+            binding.gist_qkv_rope(x, wqkv, wl.pos_offset, q, kn, vn, dims=dl, stream=stream)
+            if e: e[1].record(stream)
+            binding.gist_attn_fwd(q, kn, vn, wl.kv_pool, wl.item_ids, wl.block_table, wl.pos_offset,
+                                  attn, dims=dict(pre, layer=li), stream=stream)
+            if e: e[2].record(stream)
+            binding.gist_out_proj(attn, wo, y, dims=dl, stream=stream)
+            if e: e[3].record(stream)
+
+    for li in range(min(L, 3)):
+        layer(li)
+    torch.cuda.synchronize()
+    n = 0
+    for _ in range(steps):
+        for li in range(L):
+            layer(li, ev[n])
+            n += 1
+    torch.cuda.synchronize()
+    t = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(n)) / n for j in range(3)]
+    t = [max_over_ranks(v, ws) for v in t]
+    M = P * l
+    fl_qkv = 2.0 * M * dm * (Hq + 2 * Hkv) * hd
+    fl_o = 2.0 * M * (Hq * hd) * dm
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        peak = 1900.0
+    tq, to = fl_qkv / (t[0] * 1e-3) / 1e12, fl_o / (t[2] * 1e-3) / 1e12
+    return {"d_model": dm, "qkv_rope_ms": t[0], "attention_ms": t[1], "out_proj_ms": t[2],
+            "qkv_rope_tflops": tq, "out_proj_tflops": to, "peak_tflops": peak,
+            "qkv_rope_frac": tq / peak, "out_proj_frac": to / peak,
+            "peak_source": "MEASURED_PEAKS bf16_tflops (burst, cuBLAS)",
+            "note": "synthetic weights; per-layer launches timed one by one on the launching stream"}
 
 
 def run_e2e(args, wl, lib, ptrs, dims_by_layer, stream, ws) -> dict:
