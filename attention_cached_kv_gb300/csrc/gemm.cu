@@ -10,12 +10,13 @@
 // fp32 accumulator (rotate-half RoPE) before the one rounding to bf16, so the
 // attention can take them as they are.
 //
-// Persistent CTAs, one per SM, warp-specialised: warp 4 streams 128 x 64 tiles
-// of A and B by TMA (128-byte swizzle) through a 4-stage ring, warp 5 issues
-// tcgen05.mma into one of two 128-column TMEM accumulators, and warps 0-3 (one
-// thread per output row) drain the other accumulator: RoPE, bf16, 16-byte
-// stores.  Output tiles run along N first, so the 128-row strip of A a CTA
-// reads stays in L2 for the next tiles.
+// Persistent CTAs, one per SM, warp-specialised: warp 4 streams 128 x 64
+// tiles of A and 256 x 64 tiles of B by TMA (128-byte swizzle) through a
+// 3-stage ring, warp 5 issues tcgen05.mma (128 x 256 x 16) into one of two
+// 256-column TMEM accumulators, and warps 0-3 (one thread per output row) drain
+// the other: RoPE, bf16, then 32-row x 64-column boxes written to shared memory
+// and stored by TMA while the next columns are computed.  Output tiles run
+// along N first, so the 128-row strip of A a CTA reads stays in L2.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
 #include <math.h>
@@ -29,24 +30,23 @@ namespace {
 
 constexpr int kEpi = 128;            // epilogue threads: one per tile row
 constexpr int kThreads = kEpi + 64;  // + the TMA warp and the MMA warp
-constexpr int kStages = 4;
-constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr uint32_t kTile = kBM * kBK * 2;  // bytes of one A (or B) k-block tile
-constexpr int kMaxSlots = 8;               // pairs one 128-row tile can touch (QKV mode)
+constexpr int kStages = 3;
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr uint32_t kTileA = kBM * kBK * 2;    // bytes of one A k-block tile
+constexpr uint32_t kTileB = kBN * kBK * 2;    // bytes of one B k-block tile
+constexpr uint32_t kStage = kTileA + kTileB;
+constexpr uint32_t kSlot = 32 * 128;          // one warp's 32 rows x 64 columns of bf16
+constexpr int kMaxSlots = 8;                  // pairs one 128-row tile can touch (QKV mode)
 constexpr int kMaxSmem = 227 * 1024;
 
 struct GemmParams {
   int M, N, K;
-  int qkv;        // 0: y[M][N]; 1: split into q / k_new / v_new, rotating q and k
-  bf16* y;
-  bf16* q;
-  bf16* kn;
-  bf16* vn;
-  int l, Hq, Hkv, d, C;
+  int qkv;  // 0: y[M][N]; 1: split into q / k_new / v_new, rotating q and k
+  int l, Hq, Hkv, C;
   const int32_t* pos_offset;
   int32_t* status;
   int ntn, num_tiles;
-  uint32_t off_tab, off_base, off_bar;
+  uint32_t off_out, off_tab, tab_stride, off_base, off_bar;
   float inv_freq[64];
 };
 
@@ -56,11 +56,15 @@ struct GBars {
   uint32_t tmem_slot;
 };
 
+// tm_o0 / tm_o1 / tm_o2: q / k_new / v_new (QKV mode) or y (tm_o0 only), each
+// [rows][columns] bf16 with 64 x 32 boxes.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                const __grid_constant__ GemmParams prm) {
+                const __grid_constant__ CUtensorMap tm_o0, const __grid_constant__ CUtensorMap tm_o1,
+                const __grid_constant__ CUtensorMap tm_o2, const __grid_constant__ GemmParams prm) {
   constexpr int HALF = D / 2;
+  constexpr int PC = D / 32;  // 16-column chunks from a rotated column to its partner
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float s0, c0, s1, c1;
       sincosf((float)t * prm.inv_freq[2 * jp], &s0, &c0);
       sincosf((float)t * prm.inv_freq[2 * jp + 1], &s1, &c1);
-      *reinterpret_cast<float4*>(smem + prm.off_tab + (t * (HALF / 2) + jp) * 16) =
+      *reinterpret_cast<float4*>(smem + prm.off_tab + t * prm.tab_stride + jp * 16) =
           make_float4(c0, c1, s0, s1);
     }
   }
@@ -105,6 +109,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4) {
     // ================================================================ TMA
     bool failed = false;
+    if (lane == 0) {
+      tma_prefetch_map(&tm_a);
+      tma_prefetch_map(&tm_b);
+    }
     int it = 0;  // k-blocks issued so far: ring slot it % kStages
     for (int tl = 0; tl < my_tiles && !failed; ++tl) {
       const int tile = (int)blockIdx.x + tl * (int)gridDim.x;
@@ -119,9 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->full[s], 2 * kTile);
-          tma_load_2d(sbase + s * 2 * kTile, &tm_a, &bars->full[s], kb * kBK, m0);
-          tma_load_2d(sbase + s * 2 * kTile + kTile, &tm_b, &bars->full[s], kb * kBK, n0);
+          // rows of B past N (a narrower last tile) are zero-filled and counted
+          mbar_arrive_expect_tx(&bars->full[s], kStage);
+          tma_load_2d(sbase + s * kStage, &tm_a, &bars->full[s], kb * kBK, m0);
+          tma_load_2d(sbase + s * kStage + kTileA, &tm_b, &bars->full[s], kb * kBK, n0);
         }
         __syncwarp();
       }
@@ -131,9 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ MMA
     bool failed = false;
     int it = 0;
-    const uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN, 0);
     for (int tl = 0; tl < my_tiles && !failed; ++tl) {
       const int b = tl & 1;
+      const int tile = (int)blockIdx.x + tl * (int)gridDim.x;
+      const int width = min(kBN, prm.N - (tile % prm.ntn) * kBN);
+      const uint32_t idesc = tc::idesc_bf16_f32(kBM, (uint32_t)width, 0);
       if (__any_sync(0xffffffffu,
                      !mbar_wait(&bars->acc_empty[b], ((uint32_t)(tl >> 1) & 1u) ^ 1u))) {
         failed = true;
@@ -148,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
         if (lane == 0) {
-          const uint32_t a0 = sbase + s * 2 * kTile, b0 = a0 + kTile;
+          const uint32_t a0 = sbase + s * kStage, b0 = a0 + kTileA;
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks) {
             const uint64_t ad = tc::smem_desc_sw128(a0 + ks * 32, 16, 1024);
@@ -165,32 +176,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================================================ epilogue
     const int r = tid;  // tile row == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t out = sbase + prm.off_out + warp * 2 * kSlot;  // this warp's two 64-column boxes
     const uint8_t* tab = smem + prm.off_tab;
     uint8_t* base = smem + prm.off_base;  // [kMaxSlots][HALF / 2] of (cos, cos, sin, sin)
+    const int rot_end = prm.qkv ? (prm.Hq + prm.Hkv) * D : 0;  // columns before it are rotated
     bool failed = false;
+    if (lane == 0) {
+      tma_prefetch_map(&tm_o0);
+      if (prm.qkv) {
+        tma_prefetch_map(&tm_o1);
+        tma_prefetch_map(&tm_o2);
+      }
+    }
     for (int tl = 0; tl < my_tiles; ++tl) {
       const int b = tl & 1;
       const int tile = (int)blockIdx.x + tl * (int)gridDim.x;
       const int m0 = (tile / prm.ntn) * kBM, n0 = (tile % prm.ntn) * kBN;
-      const int m = m0 + r;
-      // what the tile's columns are: y, or q / k heads (rotated) / v heads
-      int sect = 0;  // 0: y or v, 1: q or k (rotated)
-      bf16* dst = nullptr;
-      if (!prm.qkv) {
-        dst = prm.y + (size_t)m * prm.N + n0;
-      } else if (n0 < prm.Hq * D) {
-        sect = 1;
-        dst = prm.q + ((size_t)m * prm.Hq) * D + n0;
-      } else if (n0 < (prm.Hq + prm.Hkv) * D) {
-        sect = 1;
-        dst = prm.kn + ((size_t)m * prm.Hkv) * D + (n0 - prm.Hq * D);
-      } else {
-        dst = prm.vn + ((size_t)m * prm.Hkv) * D + (n0 - (prm.Hq + prm.Hkv) * D);
-      }
+      const int width = min(kBN, prm.N - n0);
       // the first position of each pair the tile touches (uniform branch)
-      int slot = 0, t = 0;
-      if (sect) {
+      const uint8_t* trow = tab;
+      const uint8_t* brow = base;
+      if (n0 < rot_end) {
         const int p_first = m0 / prm.l;
         named_bar_sync(1, kEpi);  // every thread is done with the previous tile's slots
         for (int idx = r; idx < kMaxSlots * (HALF / 2); idx += kEpi) {
@@ -205,69 +212,102 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         named_bar_sync(1, kEpi);
+        const int m = m0 + r;
         const int p = m / prm.l;
-        slot = p - p_first;
-        t = m - p * prm.l;
+        trow = tab + (m - p * prm.l) * prm.tab_stride;
+        brow = base + (p - p_first) * (HALF / 2) * 16;
       }
       if (!failed && !mbar_wait(&bars->acc_full[b], (uint32_t)(tl >> 1) & 1u)) failed = true;
       tc::fence_after_sync();
-      const uint32_t acc = tmem + lane_base + b * kBN;
-      if (sect) {
-        // heads of D columns: chunk c (16 columns) pairs with chunk c + D/32
-        const uint8_t* trow = tab + t * (HALF / 2) * 16;
-        const uint8_t* brow = base + slot * (HALF / 2) * 16;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 16; ++c) {
-          if ((c % (D / 16)) >= D / 32) continue;  // the second half of a head
-          uint32_t xv[16], yv[16];
-          tc::ld16(acc + c * 16, xv);
-          tc::ld16(acc + (c + D / 32) * 16, yv);
-          tc::wait_ld();
-          const int j0 = (c % (D / 16)) * 16;  // first frequency of the chunk
-          uint32_t xw[8], yw[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int jp = (j0 >> 1) + e;
-            const uint4 cs = *reinterpret_cast<const uint4*>(trow + jp * 16);
-            const uint4 bs = *reinterpret_cast<const uint4*>(brow + jp * 16);
-            const uint64_t tc2 = f2_make(__uint_as_float(cs.x), __uint_as_float(cs.y));
-            const uint64_t ts2 = f2_make(__uint_as_float(cs.z), __uint_as_float(cs.w));
-            const uint64_t bc2 = f2_make(__uint_as_float(bs.x), __uint_as_float(bs.y));
-            const uint64_t bs2 = f2_make(__uint_as_float(bs.z), __uint_as_float(bs.w));
-            // angle of position pos0 + t = angle(pos0) + angle(t)
-            const uint64_t cc = f2_sub(f2_mul(bc2, tc2), f2_mul(bs2, ts2));
-            const uint64_t ss = f2_fma(bs2, tc2, f2_mul(bc2, ts2));
-            const uint64_t x = f2_make(__uint_as_float(xv[2 * e]), __uint_as_float(xv[2 * e + 1]));
-            const uint64_t y = f2_make(__uint_as_float(yv[2 * e]), __uint_as_float(yv[2 * e + 1]));
-            xw[e] = f2_to_bf16x2(f2_sub(f2_mul(x, cc), f2_mul(y, ss)));
-            yw[e] = f2_to_bf16x2(f2_fma(y, cc, f2_mul(x, ss)));
-          }
-          if (m < prm.M) {
-            stg16(dst + c * 16, make_uint4(xw[0], xw[1], xw[2], xw[3]));
-            stg16(dst + c * 16 + 8, make_uint4(xw[4], xw[5], xw[6], xw[7]));
-            stg16(dst + (c + D / 32) * 16, make_uint4(yw[0], yw[1], yw[2], yw[3]));
-            stg16(dst + (c + D / 32) * 16 + 8, make_uint4(yw[4], yw[5], yw[6], yw[7]));
+      for (int u = 0; u < width / 128; ++u) {
+        const int nu = n0 + u * 128;  // first column of this 128-column unit
+        const CUtensorMap* map = &tm_o0;
+        int col = nu;
+        if (prm.qkv && nu >= prm.Hq * D) {
+          if (nu < rot_end) {
+            map = &tm_o1;
+            col = nu - prm.Hq * D;
+          } else {
+            map = &tm_o2;
+            col = nu - rot_end;
           }
         }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < kBN / 16; ++c) {
-          uint32_t v[16];
-          tc::ld16(acc + c * 16, v);
-          tc::wait_ld();
-          if (m < prm.M) {
-            uint32_t w[8];
+        const bool rot = nu < rot_end;
+        const uint32_t acc = tmem + lane_base + b * kBN + u * 128;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              w[e] = f2_to_bf16x2(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])));
-            stg16(dst + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
-            stg16(dst + c * 16 + 8, make_uint4(w[4], w[5], w[6], w[7]));
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[4][16], w[4][8];
+          int oc[4];  // 16-column chunk (0..7) of the unit each w[] goes to
+          if (rot) {
+            // x chunks x0, x0+1 pair with x0+PC, x0+1+PC (rotate-half inside a head)
+            const int x0 = D == 64 ? hf * 4 : hf * 2;
+            oc[0] = x0;
+            oc[1] = x0 + 1;
+            oc[2] = x0 + PC;
+            oc[3] = x0 + 1 + PC;
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) oc[q] = hf * 4 + q;
           }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tc::ld16(acc + oc[q] * 16, v[q]);
+          tc::wait_ld();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tc::pin(v[q]);
+          if (rot) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int j0 = (oc[q] % (D / 16)) * 16;  // first frequency of the chunk
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int jp = (j0 >> 1) + e;
+                const uint4 cs = *reinterpret_cast<const uint4*>(trow + jp * 16);
+                const uint4 bs = *reinterpret_cast<const uint4*>(brow + jp * 16);
+                const uint64_t tc2 = f2_make(__uint_as_float(cs.x), __uint_as_float(cs.y));
+                const uint64_t ts2 = f2_make(__uint_as_float(cs.z), __uint_as_float(cs.w));
+                const uint64_t bc2 = f2_make(__uint_as_float(bs.x), __uint_as_float(bs.y));
+                const uint64_t bs2 = f2_make(__uint_as_float(bs.z), __uint_as_float(bs.w));
+                // angle of position pos0 + t = angle(pos0) + angle(t)
+                const uint64_t cc = f2_sub(f2_mul(bc2, tc2), f2_mul(bs2, ts2));
+                const uint64_t ss = f2_fma(bs2, tc2, f2_mul(bc2, ts2));
+                const uint64_t x = f2_make(__uint_as_float(v[q][2 * e]), __uint_as_float(v[q][2 * e + 1]));
+                const uint64_t y =
+                    f2_make(__uint_as_float(v[q + 2][2 * e]), __uint_as_float(v[q + 2][2 * e + 1]));
+                w[q][e] = f2_to_bf16x2(f2_sub(f2_mul(x, cc), f2_mul(y, ss)));
+                w[q + 2][e] = f2_to_bf16x2(f2_fma(y, cc, f2_mul(x, ss)));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                w[q][e] = f2_to_bf16x2(f2_make(__uint_as_float(v[q][2 * e]), __uint_as_float(v[q][2 * e + 1])));
+          }
+          if (hf == 0) {  // the boxes of the previous unit have been read out
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+          // chunk k of the unit: box k / 4, 16-byte chunks 2 (k % 4) and 2 (k % 4) + 1 of row `lane`
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t box = out + (oc[q] >> 2) * kSlot;
+            sts16(box + swz128(lane, 2 * (oc[q] & 3)), make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]));
+            sts16(box + swz128(lane, 2 * (oc[q] & 3) + 1), make_uint4(w[q][4], w[q][5], w[q][6], w[q][7]));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {  // rows past M are dropped by the store
+          tma_store_2d(map, out, col, m0 + warp * 32);
+          tma_store_2d(map, out + kSlot, col + 64, m0 + warp * 32);
+          bulk_commit();
         }
       }
       tc::fence_before_sync();
       mbar_arrive(&bars->acc_empty[b]);
     }
+    if (lane == 0) bulk_wait_all();
     if (failed && r == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
   }
 
@@ -279,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Row-major [rows][cols] bf16, tiles of kBK columns x 128 rows, 128-byte swizzle.
-int encode_2d(CUtensorMap* m, const void* base, int rows, int cols) {
+// Row-major [rows][cols] bf16, boxes of box_cols x box_rows, 128-byte swizzle.
+int encode_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_cols, int box_rows) {
   const EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return GIST_ATTN_ERR_LAUNCH;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {kBK, kBM};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -294,22 +334,41 @@ int encode_2d(CUtensorMap* m, const void* base, int rows, int cols) {
   return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
 }
 
-template <int D>
-int launch_gemm_d(GemmParams prm, const void* a, const void* b, cudaStream_t stream) {
-  alignas(64) CUtensorMap tm_a, tm_b;
-  int rc = encode_2d(&tm_a, a, prm.M, prm.K);
-  if (rc != GIST_ATTN_OK) return rc;
-  rc = encode_2d(&tm_b, b, prm.N, prm.K);
-  if (rc != GIST_ATTN_OK) return rc;
-  uint32_t off = kStages * 2 * kTile;
+// Shared memory: the ring, the output boxes, the RoPE table of l rows and the
+// per-tile base slots; 0 if it does not fit.
+uint32_t smem_plan(GemmParams& prm, int d) {
+  uint32_t off = kStages * kStage;
+  prm.off_out = off;
+  off += 4 * 2 * kSlot;
   prm.off_tab = off;
-  off += prm.qkv ? (uint32_t)prm.l * (D / 4) * 16 : 0;
+  prm.tab_stride = (uint32_t)(d / 4) * 16 + 16;  // +16 B: consecutive tokens on different banks
+  off += prm.qkv ? (uint32_t)prm.l * prm.tab_stride : 0;
   prm.off_base = off;
-  off += prm.qkv ? (uint32_t)kMaxSlots * (D / 4) * 16 : 0;
+  off += prm.qkv ? (uint32_t)kMaxSlots * (d / 4) * 16 : 0;
   prm.off_bar = off;
   off += 128;
   const uint32_t bytes = off + 1024;
-  if (bytes > (uint32_t)kMaxSmem) return GIST_ATTN_ERR_UNSUPPORTED;
+  return bytes <= (uint32_t)kMaxSmem ? bytes : 0;
+}
+
+template <int D>
+int launch_gemm_d(GemmParams prm, const void* a, const void* b, void* o0, void* o1, void* o2,
+                  cudaStream_t stream) {
+  const uint32_t bytes = smem_plan(prm, D);
+  if (bytes == 0) return GIST_ATTN_ERR_UNSUPPORTED;
+  alignas(64) CUtensorMap tm_a, tm_b, tm_o0, tm_o1, tm_o2;
+  int rc = encode_2d(&tm_a, a, prm.M, prm.K, kBK, kBM);
+  if (rc == GIST_ATTN_OK) rc = encode_2d(&tm_b, b, prm.N, prm.K, kBK, kBN);
+  if (prm.qkv) {
+    if (rc == GIST_ATTN_OK) rc = encode_2d(&tm_o0, o0, prm.M, prm.Hq * D, 64, 32);
+    if (rc == GIST_ATTN_OK) rc = encode_2d(&tm_o1, o1, prm.M, prm.Hkv * D, 64, 32);
+    if (rc == GIST_ATTN_OK) rc = encode_2d(&tm_o2, o2, prm.M, prm.Hkv * D, 64, 32);
+  } else {
+    if (rc == GIST_ATTN_OK) rc = encode_2d(&tm_o0, o0, prm.M, prm.N, 64, 32);
+    tm_o1 = tm_o0;
+    tm_o2 = tm_o0;
+  }
+  if (rc != GIST_ATTN_OK) return rc;
   if (cudaFuncSetAttribute(gemm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
@@ -318,26 +377,28 @@ int launch_gemm_d(GemmParams prm, const void* a, const void* b, cudaStream_t str
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   const int grid = prm.num_tiles < sms ? prm.num_tiles : sms;
-  gemm_kernel<D><<<grid, kThreads, bytes, stream>>>(tm_a, tm_b, prm);
+  gemm_kernel<D><<<grid, kThreads, bytes, stream>>>(tm_a, tm_b, tm_o0, tm_o1, tm_o2, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
-int launch_common(GemmParams& prm, const void* a, const void* b, int d, cudaStream_t stream) {
+int launch_common(GemmParams& prm, const void* a, const void* b, int d, void* o0, void* o1,
+                  void* o2, cudaStream_t stream) {
   const int64_t mt = ((int64_t)prm.M + kBM - 1) / kBM;
-  prm.ntn = prm.N / kBN;
+  prm.ntn = (prm.N + kBN - 1) / kBN;
   if (mt * prm.ntn > 0x7fffffff) return GIST_ATTN_ERR_UNSUPPORTED;
   prm.num_tiles = (int)(mt * prm.ntn);
   if (prm.num_tiles == 0) return GIST_ATTN_OK;
-  if (d == 64) return launch_gemm_d<64>(prm, a, b, stream);
-  return launch_gemm_d<128>(prm, a, b, stream);
+  if (d == 64) return launch_gemm_d<64>(prm, a, b, o0, o1, o2, stream);
+  return launch_gemm_d<128>(prm, a, b, o0, o1, o2, stream);
 }
 
 }  // namespace
 
-// Sizes this build runs: N a multiple of 128, K a multiple of 8 (16-byte rows
-// for TMA), M below 2^31; for the QKV split also head groups that tile N.
+// Sizes this build runs: N a multiple of 128 (whole 128-column units), K a
+// multiple of 8 (16-byte rows for TMA), M below 2^31; for the QKV split also
+// q and k/v sections made of whole units.
 bool gemm_fits(int64_t M, int N, int K) {
-  return M >= 0 && M < 0x7fffffff && N > 0 && N % kBN == 0 && K > 0 && K % 8 == 0;
+  return M >= 0 && M < 0x7fffffff && N > 0 && N % 128 == 0 && K > 0 && K % 8 == 0;
 }
 
 int launch_qkv_rope(const Problem& pb, const void* x, const void* w, int d_model, void* q,
@@ -347,23 +408,20 @@ int launch_qkv_rope(const Problem& pb, const void* x, const void* w, int d_model
   prm.N = (pb.Hq + 2 * pb.Hkv) * pb.d;
   prm.K = d_model;
   if (!gemm_fits((int64_t)pb.P * pb.l, prm.N, prm.K)) return GIST_ATTN_ERR_UNSUPPORTED;
-  // every 128-column tile must lie inside one of the q / k / v sections
-  if ((pb.Hq * pb.d) % kBN != 0 || (pb.Hkv * pb.d) % kBN != 0) return GIST_ATTN_ERR_UNSUPPORTED;
-  // a 128-row tile must touch at most kMaxSlots pairs, and the table hold l rows
-  if ((kBM - 1) / pb.l + 2 > kMaxSlots || pb.l > 1024) return GIST_ATTN_ERR_UNSUPPORTED;
+  // every 128-column unit must lie inside one of the q / k / v sections
+  if ((pb.Hq * pb.d) % 128 != 0 || (pb.Hkv * pb.d) % 128 != 0) return GIST_ATTN_ERR_UNSUPPORTED;
+  // a 128-row tile must touch at most kMaxSlots pairs (the table's size is checked with
+  // the shared-memory plan)
+  if ((kBM - 1) / pb.l + 2 > kMaxSlots) return GIST_ATTN_ERR_UNSUPPORTED;
   prm.qkv = 1;
-  prm.q = static_cast<bf16*>(q);
-  prm.kn = static_cast<bf16*>(kn);
-  prm.vn = static_cast<bf16*>(vn);
   prm.l = pb.l;
   prm.Hq = pb.Hq;
   prm.Hkv = pb.Hkv;
-  prm.d = pb.d;
   prm.C = pb.C;
   prm.pos_offset = pb.pos_offset;
   prm.status = pb.status;
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
-  return launch_common(prm, x, w, pb.d, stream);
+  return launch_common(prm, x, w, pb.d, q, kn, vn, stream);
 }
 
 int launch_out_proj(const Problem& pb, const void* attn, const void* w, int d_model, void* y,
@@ -374,10 +432,9 @@ int launch_out_proj(const Problem& pb, const void* attn, const void* w, int d_mo
   prm.K = pb.Hq * pb.d;
   if (!gemm_fits((int64_t)pb.P * pb.l, prm.N, prm.K)) return GIST_ATTN_ERR_UNSUPPORTED;
   prm.qkv = 0;
-  prm.y = static_cast<bf16*>(y);
   prm.status = pb.status;
   prm.l = pb.l;
-  return launch_common(prm, attn, w, 64, stream);
+  return launch_common(prm, attn, w, 64, y, nullptr, nullptr, stream);
 }
 
 }  // namespace gattn

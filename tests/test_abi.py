@@ -149,6 +149,10 @@ def test_projections_reject_bad_arguments(lib):
     assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, odd, None) == binding.ERR_UNSUPPORTED
     short = ctypes.byref(binding.make_dims(dict(BASE, n_new=4)))
     assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, short, None) == binding.ERR_UNSUPPORTED
+    # the table of l token angles must fit shared memory: l <= 180 (d = 64), l <= 88 (d = 128)
+    for dd in (dict(BASE, n_new=181), dict(BASE, n_new=89, head_dim=128, num_q_heads=8)):
+        long_ = ctypes.byref(binding.make_dims(dd))
+        assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, long_, None) == binding.ERR_UNSUPPORTED
     o = lib.gist_out_proj
     assert o(V(P16), None, V(P16), 256, D, None) == binding.ERR_NULL
     assert o(V(P16), V(P16), V(P16), 200, D, None) == binding.ERR_UNSUPPORTED  # not a multiple of 128
