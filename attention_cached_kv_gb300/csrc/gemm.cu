@@ -39,6 +39,23 @@ constexpr uint32_t kSlot = 32 * 128;          // one warp's 32 rows x 64 columns
 constexpr int kMaxSlots = 8;                  // pairs one 128-row tile can touch (QKV mode)
 constexpr int kMaxSmem = 227 * 1024;
 
+// 2-D tiled store from shared memory (elements outside the tensor are dropped).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// After tcgen05.wait::ld: makes every use of the loaded registers depend on
+// the wait, so several TMEM loads can be in flight before one wait.
+__device__ __forceinline__ void tmem_pin(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                 "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
 struct GemmParams {
   int M, N, K;
   int qkv;  // 0: y[M][N]; 1: split into q / k_new / v_new, rotating q and k
@@ -253,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 4; ++q) tc::ld16(acc + oc[q] * 16, v[q]);
           tc::wait_ld();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) tc::pin(v[q]);
+          for (int q = 0; q < 4; ++q) tmem_pin(v[q]);
           if (rot) {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {

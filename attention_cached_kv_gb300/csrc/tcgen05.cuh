@@ -89,9 +89,6 @@ __device__ __forceinline__ void commit(uint32_t mbar_smem_addr) {
 }
 
 // ---- TMEM <-> registers: each thread its own lane (warp w: lanes 32(w%4)..) ----
-// ld16 is volatile so that it keeps its place before the wait::ld that
-// follows it; pin() after the wait makes every use of the loaded registers
-// depend on the wait (several loads may then be in flight at once).
 __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -103,12 +100,6 @@ __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void pin(uint32_t (&r)[16]) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
-                 "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 __device__ __forceinline__ void st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a),

@@ -110,13 +110,14 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, variant: str = ""):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the kernel sources as they are now; else None."""
+    the kernel sources as they are now; else None.  `variant` names a second
+    record of the same workload (e.g. "fp8" for the E4M3 pool)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(workload)
+            rec = json.load(f).get(workload + ("_" + variant if variant else ""))
     except (OSError, ValueError):
         return None
     if not rec or rec.get("kernel_sources_sha") != kernel_source_hash(workload):
@@ -354,7 +355,7 @@ def run_ours(args) -> dict:
     bytes_info = algorithmic_bytes_per_launch(wl, 1 if kv_scale is not None else 2)
     peak, peak_src = measured_peaks()
     achieved = bytes_info["total"] / (avg_launch_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload, "fp8" if kv_scale is not None else "")
     value = P * L * K * ws / (elapsed_ms * 1e-3)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
