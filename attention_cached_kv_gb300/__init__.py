@@ -7,13 +7,13 @@ The compute lives in ``_lib/libgistattn.so`` (C ABI in include/gist_attn.h);
 synthetic inputs.  The library is loaded on first use and every call fails
 loudly if it has not been built.
 """
-from .binding import (FLAG_PREROTATED, GistAttnError, STATUS_BAD_BLOCK, STATUS_TIMEOUT, gist_attn_fwd,
+from .binding import (FLAG_PREROTATED, GistAttnError, STATUS_BAD_BLOCK, STATUS_RANGE, STATUS_TIMEOUT, gist_attn_fwd,
                       gist_attn_fwd_block_mass, gist_attn_fwd_fp8kv, gist_attn_fwd_gist_mask,
                       gist_kv_append, gist_kv_store, gist_out_proj, gist_qkv_rope,
                       gist_attn_gather_debug, kv_bytes_batch, kv_bytes_per_item,
                       kv_bytes_per_position, load_library, status_string)
 
-__all__ = ["FLAG_PREROTATED", "GistAttnError", "STATUS_BAD_BLOCK", "STATUS_TIMEOUT", "gist_attn_fwd", "gist_attn_fwd_fp8kv",
+__all__ = ["FLAG_PREROTATED", "GistAttnError", "STATUS_BAD_BLOCK", "STATUS_RANGE", "STATUS_TIMEOUT", "gist_attn_fwd", "gist_attn_fwd_fp8kv",
            "gist_attn_fwd_block_mass", "gist_attn_fwd_gist_mask", "gist_kv_append", "gist_kv_store",
            "gist_qkv_rope", "gist_out_proj",
            "gist_attn_gather_debug", "kv_bytes_batch", "kv_bytes_per_item",

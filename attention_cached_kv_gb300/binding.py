@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libgistattn.so")
 
 OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH = 0, -1, -2, -3, -4, -5
-STATUS_BAD_BLOCK, STATUS_TIMEOUT = 1, 2
+STATUS_BAD_BLOCK, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4
 FLAG_PREROTATED = 1
 
 EXPORTS = ("gist_attn_fwd", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",

@@ -16,10 +16,13 @@
 //   * warps 0-7 (compute): two threads per tile row (TMEM lane = row; the
 //     halves split the columns).  They stage each unit's K/V (cached rows
 //     through the pool gather, new rows raw, by 16-byte cp.async two units
-//     ahead), rotate the new keys, rotate q (split into bf16 hi + lo so the
-//     rounding of rotated q does not reach the logits: hi goes to the stage,
-//     lo to TMEM for a second MMA pass), run the softmax out of TMEM (P back
-//     into TMEM as bf16), and normalise O into the stage for the store.
+//     ahead), rotate the new keys, rotate q, run the softmax out of TMEM (P
+//     back into TMEM as bf16), and normalise O into the stage for the store.
+//   S = q K^T takes q and K in f16: rotated q and the rotated new keys are
+//   rounded once to f16 (11 significant bits, where bf16 has 8), and the cached
+//   bf16 keys convert to f16 exactly (magnitudes in [2^-17, 65504]).  A value
+//   past the f16 range makes its rows' softmax sums non-finite, which the
+//   status word reports.  P V stays bf16 x bf16.
 // Hand-offs use mbarriers; the compute warps are software-pipelined so that the
 // rotation of tile i+1 runs while O(i) = P V is on the tensor core and the
 // normalisation of tile i runs while S(i+1) is.  One pass covers a tile's
@@ -55,7 +58,7 @@ struct TcParams {
   int num_units;  // P * Hkv
   int kv_rows;    // rows of one K (or V) panel
   uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_bar;
-  uint32_t p_col, o_col, lo_col, tmem_cols;  // TMEM plan: S at column 0
+  uint32_t p_col, o_col, tmem_cols;  // TMEM plan: S at column 0
   float scale_log2;
   float inv_freq[64];
 };
@@ -64,7 +67,7 @@ struct Layout {
   int Tm, n_mt, kv_rows;
   uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_bar,
       bytes;
-  uint32_t p_col, o_col, lo_col, tmem_cols;
+  uint32_t p_col, o_col, tmem_cols;
 };
 
 Layout plan(const Problem& pb) {
@@ -90,11 +93,10 @@ Layout plan(const Problem& pb) {
   L.off_bar = off;
   off += 128;
   L.bytes = off + 1024;
-  // TMEM: S [0, N) fp32, P [N, 1.5N) bf16 pairs, O [o, o+d), q lo [o+d, o+1.5d)
+  // TMEM: S [0, N) fp32, P [N, 1.5N) bf16 pairs, O [o, o+d)
   L.p_col = (uint32_t)L.kv_rows;
   L.o_col = (uint32_t)((L.kv_rows * 3 / 2 + 15) / 16 * 16);
-  L.lo_col = L.o_col + pb.d;
-  const uint32_t need = L.lo_col + pb.d / 2;
+  const uint32_t need = L.o_col + pb.d;
   L.tmem_cols = need <= 256 ? 256 : 512;
   return L;
 }
@@ -220,23 +222,17 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
       const uint32_t vb = kb + NP * kv_panel;
       const int N = (C + min(l, (mt + 1) * Tm) + 15) & ~15;
-      // ---- S = (q_hi + q_lo) K^T
+      // ---- S = q K^T (f16 x f16)
       if (__any_sync(0xffffffffu, !mbar_wait(&bars->rope_done, par))) { failed = true; break; }
       tc::fence_after_sync();
       if (lane == 0) {
-        const uint32_t idesc = tc::idesc_bf16_f32(128, N, 0);
+        const uint32_t idesc = tc::idesc_f16_f32(128, N, 0);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = (uint32_t)(ks & 3) * 32;  // 16 columns = 32 bytes
           const uint64_t a = tc::smem_desc_sw128(stage + (ks >> 2) * kPanel + koff, 16, 1024);
           const uint64_t bd = tc::smem_desc_sw128(kb + (ks >> 2) * kv_panel + koff, 16, 1024);
           tc::mma_ss(tmem, a, bd, idesc, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (uint32_t)(ks & 3) * 32;
-          const uint64_t bd = tc::smem_desc_sw128(kb + (ks >> 2) * kv_panel + koff, 16, 1024);
-          tc::mma_ts(tmem, tmem + prm.lo_col + ks * 8, bd, idesc, 1);
         }
         tc::commit(smem_u32(&bars->s_done));
       }
@@ -366,16 +362,25 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       bad = named_bar_or(kBarCompute, kCompute, bad);
       if (!bad) {
         const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
+        // cached keys: bf16 -> f16 in place
+        for (int idx = tid; idx < C * CPR; idx += kCompute) {
+          const int t = idx / CPR, J = idx - t * CPR;
+          const uint32_t a = chunk_addr(kb, kv_panel, t, J);
+          const uint4 v = lds16(a);
+          sts16(a, make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                              bf16x2_to_f16x2(v.w)));
+        }
+        // new keys: rotated, rounded once to f16
         for (int idx = tid; idx < l * (CPR / 2); idx += kCompute) {
           const int t = idx / (CPR / 2), J = idx - t * (CPR / 2);
           const uint32_t a0 = chunk_addr(kb, kv_panel, C + t, J);
           const uint32_t a1 = chunk_addr(kb, kv_panel, C + t, J + CPR / 2);
           uint64_t xr[4], yr[4];
           rope_chunk(lds16(a0), lds16(a1), tab + t * prm.tab_stride, 8 * J, xr, yr);
-          sts16(a0, make_uint4(f2_to_bf16x2(xr[0]), f2_to_bf16x2(xr[1]), f2_to_bf16x2(xr[2]),
-                               f2_to_bf16x2(xr[3])));
-          sts16(a1, make_uint4(f2_to_bf16x2(yr[0]), f2_to_bf16x2(yr[1]), f2_to_bf16x2(yr[2]),
-                               f2_to_bf16x2(yr[3])));
+          sts16(a0, make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]), f2_to_f16x2(xr[2]),
+                               f2_to_f16x2(xr[3])));
+          sts16(a1, make_uint4(f2_to_f16x2(yr[0]), f2_to_f16x2(yr[1]), f2_to_f16x2(yr[2]),
+                               f2_to_f16x2(yr[3])));
         }
       }
       fence_proxy_async_smem();
@@ -390,17 +395,23 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     };
     const uint32_t pair_bar = 2 + (warp & 3);  // this row's two threads (warps w, w + 4)
     const int row_tok = r / G;                  // token of row r within its tile
-    // Rotate row r of tile i's q (this half's chunk pairs): hi -> stage, lo -> TMEM.
+    // Rotate row r of tile i's q (this half's chunk pairs) into the stage as f16.
     // Rows past the tile's tokens hold zeros (TMA fill, or set-up for rows no
-    // box reaches), so their hi and lo come out zero without a select.
+    // box reaches), so they come out zero without a select.
     auto rope_tile = [&](int i, int mt) {
       const int s = i % kStages;
       const uint32_t stage = sbase + s * prm.stage_bytes;
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
       const int tt = min(row_tok, toks - 1);
       wait(&bars->qfull[s], (uint32_t)(i / kStages) & 1u);
+      // a warp whose 32 rows are all past the tile's tokens skips the work:
+      // rows are independent in both products, and such rows are never stored
+      if ((warp & 3) * 32 >= toks * G) {
+        tc::fence_before_sync();
+        mbar_arrive(&bars->rope_done);
+        return;
+      }
       constexpr int JH = CPR / 4;  // chunk pairs per half
-      uint32_t lo_a[4], lo_b[4];
       const uint8_t* trow = tab + (t0 + tt) * prm.tab_stride;
 #pragma unroll
       for (int jj = 0; jj < JH; ++jj) {
@@ -409,19 +420,11 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
         const uint32_t a1 = chunk_addr(stage, kPanel, r, J + CPR / 2);
         uint64_t xr[4], yr[4];
         rope_chunk(lds16(a0), lds16(a1), trow, 8 * J, xr, yr);
-        uint32_t xh[4], yh[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          f2_split_bf16(xr[e], xh[e], lo_a[e]);
-          f2_split_bf16(yr[e], yh[e], lo_b[e]);
-        }
-        sts16(a0, make_uint4(xh[0], xh[1], xh[2], xh[3]));
-        sts16(a1, make_uint4(yh[0], yh[1], yh[2], yh[3]));
-        // TMEM column c of the lo block holds q elements (2c, 2c+1)
-        tc::st4(tmem + lane_base + prm.lo_col + J * 4, lo_a[0], lo_a[1], lo_a[2], lo_a[3]);
-        tc::st4(tmem + lane_base + prm.lo_col + (J + CPR / 2) * 4, lo_b[0], lo_b[1], lo_b[2], lo_b[3]);
+        sts16(a0, make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]), f2_to_f16x2(xr[2]),
+                             f2_to_f16x2(xr[3])));
+        sts16(a1, make_uint4(f2_to_f16x2(yr[0]), f2_to_f16x2(yr[1]), f2_to_f16x2(yr[2]),
+                             f2_to_f16x2(yr[3])));
       }
-      tc::wait_st();
       fence_proxy_async_smem();
       tc::fence_before_sync();
       mbar_arrive(&bars->rope_done);
@@ -446,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       const bool bad = (k & 1) ? bad1 : bad0;
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
       const bool valid = row_tok < toks;
+      const bool wlive = (warp & 3) * 32 < toks * G;  // warp-uniform, same for the row's partner
       const int tt = min(row_tok, toks - 1);
       const int N = (C + t0 + toks + 15) & ~15;
       // ---- softmax of row r over this half's 16-column chunks c = h, h+2, ...
@@ -473,53 +477,55 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           }
         }
       };
-      float mx0 = kNegInf, mx1 = kNegInf;
-#pragma unroll
-      for (int cc = 0; cc < NCH; ++cc) {
-        const int c = 2 * cc + h;
-        if (c * 16 < N) {
-          uint32_t v[16];
-          load_chunk(c, v);
-          const float a = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-          const float b = max3f(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
-          const float d = max3f(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
-          const float e = max3f(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
-          const float f = max3f(__uint_as_float(v[12]), __uint_as_float(v[13]), __uint_as_float(v[14]));
-          mx0 = max3f(mx0, a, b);
-          mx1 = max3f(mx1, max3f(d, e, f), __uint_as_float(v[15]));
-        }
-      }
-      red_max[h * 128 + r] = fmaxf(mx0, mx1);
-      named_bar_sync(pair_bar, 64);
-      const float m = fmaxf(red_max[r], red_max[128 + r]);
-      {
-        const float sc = prm.scale_log2;
-        const uint64_t sc2 = f2_make(sc, sc), nmc2 = f2_make(-m * sc, -m * sc);
-        const uint64_t one2 = f2_make(1.f, 1.f);
-        uint64_t acc[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
-#pragma unroll
+      if (wlive) {
+        float mx0 = kNegInf, mx1 = kNegInf;
+  #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
           const int c = 2 * cc + h;
           if (c * 16 < N) {
             uint32_t v[16];
             load_chunk(c, v);
-            uint32_t pk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float a, bb;
-              f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, nmc2),
-                       a, bb);
-              const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
-              acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
-              pk[e] = f2_to_bf16x2(pp);
-            }
-            tc::st8(tmem + lane_base + prm.p_col + c * 8, pk);
+            const float a = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+            const float b = max3f(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
+            const float d = max3f(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
+            const float e = max3f(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
+            const float f = max3f(__uint_as_float(v[12]), __uint_as_float(v[13]), __uint_as_float(v[14]));
+            mx0 = max3f(mx0, a, b);
+            mx1 = max3f(mx1, max3f(d, e, f), __uint_as_float(v[15]));
           }
         }
-        float a0, a1, b0, b1;
-        f2_split(acc[0], a0, a1);
-        f2_split(acc[1], b0, b1);
-        red_sum[h * 128 + r] = (a0 + a1) + (b0 + b1);
+        red_max[h * 128 + r] = fmaxf(mx0, mx1);
+        named_bar_sync(pair_bar, 64);
+        const float m = fmaxf(red_max[r], red_max[128 + r]);
+        {
+          const float sc = prm.scale_log2;
+          const uint64_t sc2 = f2_make(sc, sc), nmc2 = f2_make(-m * sc, -m * sc);
+          const uint64_t one2 = f2_make(1.f, 1.f);
+          uint64_t acc[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+  #pragma unroll
+          for (int cc = 0; cc < NCH; ++cc) {
+            const int c = 2 * cc + h;
+            if (c * 16 < N) {
+              uint32_t v[16];
+              load_chunk(c, v);
+              uint32_t pk[8];
+  #pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                float a, bb;
+                f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, nmc2),
+                         a, bb);
+                const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
+                acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
+                pk[e] = f2_to_bf16x2(pp);
+              }
+              tc::st8(tmem + lane_base + prm.p_col + c * 8, pk);
+            }
+          }
+          float a0, a1, b0, b1;
+          f2_split(acc[0], a0, a1);
+          f2_split(acc[1], b0, b1);
+          red_sum[h * 128 + r] = (a0 + a1) + (b0 + b1);
+        }
       }
       tc::wait_st();
       tc::fence_before_sync();
@@ -535,8 +541,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       // ---- O of row r, this half's columns, normalised into the stage
       wait(&bars->o_done, par);
       tc::fence_after_sync();
-      named_bar_sync(pair_bar, 64);  // the partner's row sum is written
-      {
+      if (wlive) {
+        named_bar_sync(pair_bar, 64);  // the partner's row sum is written
         const uint32_t stage = sbase + (i % kStages) * prm.stage_bytes;
         constexpr int OC = D / 32;  // 16-column chunks per half
         if (bad) {
@@ -546,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
               sts16(chunk_addr(stage, kPanel, r, h * 2 * OC + J), make_uint4(0, 0, 0, 0));
           }
         } else {
-          const float inv = rcp_approx(red_sum[r] + red_sum[128 + r]);
+          const float sum = red_sum[r] + red_sum[128 + r];
+          if (valid && !(sum <= 3.0e38f)) report(prm.status, GIST_ATTN_STATUS_RANGE);
+          const float inv = rcp_approx(sum);
           const uint64_t inv2 = f2_make(inv, inv);
 #pragma unroll
           for (int c = 0; c < OC; ++c) {
@@ -632,7 +640,6 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.off_bar = L.off_bar;
   prm.p_col = L.p_col;
   prm.o_col = L.o_col;
-  prm.lo_col = L.lo_col;
   prm.tmem_cols = L.tmem_cols;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];

@@ -60,6 +60,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
          | ((M >> 4) << 24);       // M / 16
 }
 
+// Instruction descriptor for kind::f16 with f16 A and B, fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uint32_t b_mn_major) {
+  return (1u << 4)                 // D format: f32 (A and B format 0: f16)
+         | (b_mn_major << 16)      // B major-ness
+         | ((N >> 3) << 17)        // N / 8
+         | ((M >> 4) << 24);       // M / 16
+}
+
 // ---- MMA: D(tmem) (+)= A * B ----
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
