@@ -118,6 +118,27 @@ __device__ __forceinline__ void rope_chunk(const uint4& x, const uint4& y, const
   }
 }
 
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// TMEM load of 16 columns of this thread's lane that also returns their maximum.
+__device__ __forceinline__ float ld16_max(uint32_t taddr) {
+  uint32_t r[16];
+  float m;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, %16, [%17];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=f"(m)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+f"(m)::"memory");
+  return m;
+}
+
 struct Bars {
   uint64_t qfull[kStages];
   uint64_t rope_done;  // compute -> MMA warp: q tile rotated (hi in the stage, lo in TMEM)
@@ -315,14 +336,14 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     };
     // cp.async of unit u's K/V rows (cached, then new ones raw) into buffer b.
     auto stage_kv = [&](int u, int b) -> bool {
-      // Each thread copies one 16-byte chunk column (c) of every kRowStep-th
-      // row, so no per-row index arithmetic is needed; block ids are read by
-      // every thread (a broadcast load) instead of being shared through a
-      // barrier.  Returns true if one of this unit's block ids is out of range
-      // (its rows are then not copied).
-      constexpr int kRowStep = kCompute / CPR;
+      // Each thread copies fixed 16-byte chunks of the unit's rows, and later
+      // converts or rotates exactly the chunks it copied, so waiting for its
+      // own copies is enough (no barrier): a new key row's chunk pair (J,
+      // J + d/16) goes to one thread.  Block ids are read by every thread (a
+      // broadcast load), so `bad` comes out the same in all of them.  Returns
+      // true if one of this unit's block ids is out of range (its rows are then
+      // not copied).
       const int p = u / prm.Hkv, g = u % prm.Hkv;
-      const int c = tid % CPR, r0 = tid / CPR;
       const uint32_t kb = sbase + prm.off_kv + b * prm.kv_buf_bytes;
       const uint32_t vb = kb + NP * kv_panel;
       const int bl = prm.pv.block_len;
@@ -333,46 +354,54 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           bad = true;
           continue;
         }
-        const bf16* ks = pool_row(prm.pv, blk, g, 0, 0) + c * 8;
-        const bf16* vs = pool_row(prm.pv, blk, g, 1, 0) + c * 8;
-        for (int t = r0; t < bl; t += kRowStep) {
+        const bf16* ks = pool_row(prm.pv, blk, g, 0, 0);
+        const bf16* vs = pool_row(prm.pv, blk, g, 1, 0);
+        for (int w = tid; w < bl * CPR; w += kCompute) {
+          const int t = w / CPR, c = w % CPR;
           const uint32_t o = (c >> 3) * kv_panel + swz128(bi * bl + t, c & 7);
-          cp_async16(kb + o, ks + (size_t)t * D);
-          cp_async16(vb + o, vs + (size_t)t * D);
+          cp_async16(kb + o, ks + t * D + c * 8);
+          cp_async16(vb + o, vs + t * D + c * 8);
         }
       }
       const size_t row_stride = (size_t)prm.Hkv * D;  // between consecutive new tokens
-      const size_t first = ((size_t)p * l * prm.Hkv + g) * D + c * 8;
-      for (int t = r0; t < l; t += kRowStep) {
-        const uint32_t o = (c >> 3) * kv_panel + swz128(C + t, c & 7);
-        cp_async16(kb + o, prm.k_new + first + t * row_stride);
-        cp_async16(vb + o, prm.v_new + first + t * row_stride);
+      const bf16* kn = prm.k_new + ((size_t)p * l * prm.Hkv + g) * D;
+      const bf16* vn = prm.v_new + ((size_t)p * l * prm.Hkv + g) * D;
+      for (int w = tid; w < l * (CPR / 2); w += kCompute) {
+        const int t = w / (CPR / 2), J = w % (CPR / 2);
+        const bf16* src = kn + t * row_stride + J * 8;
+        cp_async16(chunk_addr(kb, kv_panel, C + t, J), src);
+        cp_async16(chunk_addr(kb, kv_panel, C + t, J + CPR / 2), src + HALF);
+      }
+      for (int w = tid; w < l * CPR; w += kCompute) {
+        const int t = w / CPR, c = w % CPR;
+        cp_async16(chunk_addr(vb, kv_panel, C + t, c), vn + t * row_stride + c * 8);
       }
       cp_async_commit();
       return bad;
     };
-    // Unit k's K/V have landed (each thread waited for its own copies): share
-    // the unit's block-id status (bad: in, this thread's; out, the unit's) and
-    // rotate its new keys in place with the table of its positions.
-    auto prepare_unit = [&](int k, bool& bad) {
+    // Unit k's K/V have landed (each thread waited for its own copies): convert
+    // this thread's cached key chunks to f16 and rotate its new key chunk
+    // pairs with the table of the unit's positions, in place.
+    auto prepare_unit = [&](int k, bool bad) {
       if (prm.pos_offset) {
         named_bar_sync(kBarCompute, kCompute);  // nobody still reads the previous table
         build_table(prm.pos_offset[unit_of(k) / prm.Hkv], kCompute);
+        named_bar_sync(kBarCompute, kCompute);
       }
-      bad = named_bar_or(kBarCompute, kCompute, bad);
       if (!bad) {
         const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
-        // cached keys: bf16 -> f16 in place
-        for (int idx = tid; idx < C * CPR; idx += kCompute) {
-          const int t = idx / CPR, J = idx - t * CPR;
-          const uint32_t a = chunk_addr(kb, kv_panel, t, J);
-          const uint4 v = lds16(a);
-          sts16(a, make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                              bf16x2_to_f16x2(v.w)));
+        const int bl = prm.pv.block_len;
+        for (int bi = 0; bi < prm.pv.blocks_per_pair; ++bi) {
+          for (int w = tid; w < bl * CPR; w += kCompute) {
+            const int t = w / CPR, c = w % CPR;
+            const uint32_t a = chunk_addr(kb, kv_panel, bi * bl + t, c);
+            const uint4 v = lds16(a);
+            sts16(a, make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                                bf16x2_to_f16x2(v.w)));
+          }
         }
-        // new keys: rotated, rounded once to f16
-        for (int idx = tid; idx < l * (CPR / 2); idx += kCompute) {
-          const int t = idx / (CPR / 2), J = idx - t * (CPR / 2);
+        for (int w = tid; w < l * (CPR / 2); w += kCompute) {
+          const int t = w / (CPR / 2), J = w % (CPR / 2);
           const uint32_t a0 = chunk_addr(kb, kv_panel, C + t, J);
           const uint32_t a1 = chunk_addr(kb, kv_panel, C + t, J + CPR / 2);
           uint64_t xr[4], yr[4];
@@ -383,8 +412,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
                                f2_to_f16x2(yr[3])));
         }
       }
-      fence_proxy_async_smem();
-      named_bar_sync(kBarCompute, kCompute);
+      fence_proxy_async_smem();  // before the rope_done arrival that hands K to the MMA
     };
     // A wait that has timed out once turns every later wait of this thread
     // into a no-op, so a stuck pipeline ends in bounded time (the status word
@@ -459,40 +487,55 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       tc::fence_after_sync();
       const int lim = C + t0 + tt + 1;  // keys row r sees
       const int lim_all = C + t0 + 1;   // keys every row of the tile sees
-      // chunk c of this row's logits, with 0 added to the visible keys and -inf
-      // to the rest when the chunk reaches the causal diagonal (a tile-uniform test)
-      auto load_chunk = [&](int c, uint32_t (&sv)[16]) {
-        tc::ld16(tmem + lane_base + c * 16, sv);
-        tc::wait_ld();
-        if ((c + 1) * 16 > lim_all) {
-          const int v = min(max(lim - c * 16, 0), 16);
-          const float4* bt = reinterpret_cast<const float4*>(bias + v * 16);
+      // Chunks c < cd lie below the causal diagonal for every row of the tile;
+      // chunks from cd on reach it and take an additive 0 / -inf row from the
+      // bias table.  Those run in a separate (not unrolled) loop, so the mask
+      // code is not predicated onto the other chunks.
+      const int cd = lim_all >> 4;
+      const int c_diag = cd + ((cd ^ h) & 1);  // this half's first chunk at the diagonal
+      // the row of the bias table for chunk c: 0 for the keys row r sees, -inf after
+      auto bias_row = [&](int c) {
+        return reinterpret_cast<const float4*>(bias + min(max(lim - c * 16, 0), 16) * 16);
+      };
+      auto mask16 = [&](int c, uint32_t (&sv)[16]) {
+        const float4* bt = bias_row(c);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const float4 b = bt[q4];
-            sv[4 * q4 + 0] = __float_as_uint(__uint_as_float(sv[4 * q4 + 0]) + b.x);
-            sv[4 * q4 + 1] = __float_as_uint(__uint_as_float(sv[4 * q4 + 1]) + b.y);
-            sv[4 * q4 + 2] = __float_as_uint(__uint_as_float(sv[4 * q4 + 2]) + b.z);
-            sv[4 * q4 + 3] = __float_as_uint(__uint_as_float(sv[4 * q4 + 3]) + b.w);
-          }
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 bq = bt[q4];
+          float a, b;
+          f2_split(f2_add(f2_make(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1])),
+                          f2_make(bq.x, bq.y)), a, b);
+          sv[4 * q4] = __float_as_uint(a);
+          sv[4 * q4 + 1] = __float_as_uint(b);
+          f2_split(f2_add(f2_make(__uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3])),
+                          f2_make(bq.z, bq.w)), a, b);
+          sv[4 * q4 + 2] = __float_as_uint(a);
+          sv[4 * q4 + 3] = __float_as_uint(b);
         }
+      };
+      auto max16 = [&](const uint32_t (&v)[16], float& mx0, float& mx1) {
+        const float a = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+        const float b = max3f(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
+        const float d = max3f(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
+        const float e = max3f(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
+        const float f = max3f(__uint_as_float(v[12]), __uint_as_float(v[13]), __uint_as_float(v[14]));
+        mx0 = max3f(mx0, a, b);
+        mx1 = max3f(mx1, max3f(d, e, f), __uint_as_float(v[15]));
       };
       if (wlive) {
         float mx0 = kNegInf, mx1 = kNegInf;
-  #pragma unroll
+#pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
           const int c = 2 * cc + h;
-          if (c * 16 < N) {
-            uint32_t v[16];
-            load_chunk(c, v);
-            const float a = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-            const float b = max3f(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
-            const float d = max3f(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
-            const float e = max3f(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
-            const float f = max3f(__uint_as_float(v[12]), __uint_as_float(v[13]), __uint_as_float(v[14]));
-            mx0 = max3f(mx0, a, b);
-            mx1 = max3f(mx1, max3f(d, e, f), __uint_as_float(v[15]));
-          }
+          if (c < cd && c * 16 < N) mx0 = fmaxf(mx0, ld16_max(tmem + lane_base + c * 16));
+        }
+#pragma unroll 1
+        for (int c = c_diag; c * 16 < N; c += 2) {
+          uint32_t v[16];
+          tc::ld16(tmem + lane_base + c * 16, v);
+          tc::wait_ld();
+          mask16(c, v);
+          max16(v, mx0, mx1);
         }
         red_max[h * 128 + r] = fmaxf(mx0, mx1);
         named_bar_sync(pair_bar, 64);
@@ -502,24 +545,41 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           const uint64_t sc2 = f2_make(sc, sc), nmc2 = f2_make(-m * sc, -m * sc);
           const uint64_t one2 = f2_make(1.f, 1.f);
           uint64_t acc[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
-  #pragma unroll
+          // exponentials of chunk c; at the diagonal the bias row joins the offset
+          auto exp16 = [&](int c, const uint32_t (&v)[16], const float4* bt) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              uint64_t off = nmc2;
+              if (bt) {
+                const float4 bq = bt[e >> 1];
+                off = f2_add(nmc2, (e & 1) ? f2_make(bq.z, bq.w) : f2_make(bq.x, bq.y));
+              }
+              float a, bb;
+              f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, off),
+                       a, bb);
+              const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
+              acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
+              pk[e] = f2_to_bf16x2(pp);
+            }
+            tc::st8(tmem + lane_base + prm.p_col + c * 8, pk);
+          };
+#pragma unroll
           for (int cc = 0; cc < NCH; ++cc) {
             const int c = 2 * cc + h;
-            if (c * 16 < N) {
+            if (c < cd && c * 16 < N) {
               uint32_t v[16];
-              load_chunk(c, v);
-              uint32_t pk[8];
-  #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                float a, bb;
-                f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, nmc2),
-                         a, bb);
-                const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
-                acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
-                pk[e] = f2_to_bf16x2(pp);
-              }
-              tc::st8(tmem + lane_base + prm.p_col + c * 8, pk);
+              tc::ld16(tmem + lane_base + c * 16, v);
+              tc::wait_ld();
+              exp16(c, v, nullptr);
             }
+          }
+#pragma unroll 1
+          for (int c = c_diag; c * 16 < N; c += 2) {
+            uint32_t v[16];
+            tc::ld16(tmem + lane_base + c * 16, v);
+            tc::wait_ld();
+            exp16(c, v, bias_row(c));
           }
           float a0, a1, b0, b1;
           f2_split(acc[0], a0, a1);
@@ -534,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       if (i + 1 < my_tiles) {
         if (mt + 1 == n_mt) {  // the next tile opens unit k+1
           cp_async_wait_group<0>();
-          prepare_unit(k + 1, ((k + 1) & 1) ? bad1 : bad0);  // (a reference)
+          prepare_unit(k + 1, ((k + 1) & 1) ? bad1 : bad0);
         }
         rope_tile(i + 1, mt + 1 == n_mt ? 0 : mt + 1);
       }
