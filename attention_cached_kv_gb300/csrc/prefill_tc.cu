@@ -22,7 +22,9 @@
 //   rounded once to f16 (11 significant bits, where bf16 has 8), and the cached
 //   bf16 keys convert to f16 exactly (magnitudes in [2^-17, 65504]).  A value
 //   past the f16 range makes its rows' softmax sums non-finite, which the
-//   status word reports.  P V stays bf16 x bf16.
+//   status word reports.  P V stays bf16 x bf16.  Inputs that arrive rotated
+//   (the QKV projection's epilogue rotated and rounded them once) skip the
+//   rotation and the conversion: S = q K^T runs on the bf16 values as stored.
 // Hand-offs use mbarriers; the compute warps are software-pipelined so that the
 // rotation of tile i+1 runs while O(i) = P V is on the tensor core and the
 // normalisation of tile i runs while S(i+1) is.  One pass covers a tile's
@@ -57,6 +59,7 @@ struct TcParams {
   int n_mt;       // M-tiles per unit
   int num_units;  // P * Hkv
   int kv_rows;    // rows of one K (or V) panel
+  int rotated;    // q and k_new arrive rotated: no RoPE, S = q K^T in bf16 as stored
   uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_bar;
   uint32_t p_col, o_col, tmem_cols;  // TMEM plan: S at column 0
   float scale_log2;
@@ -243,11 +246,12 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
       const uint32_t vb = kb + NP * kv_panel;
       const int N = (C + min(l, (mt + 1) * Tm) + 15) & ~15;
-      // ---- S = q K^T (f16 x f16)
+      // ---- S = q K^T (f16 x f16, or bf16 x bf16 for inputs that arrive rotated)
       if (__any_sync(0xffffffffu, !mbar_wait(&bars->rope_done, par))) { failed = true; break; }
       tc::fence_after_sync();
       if (lane == 0) {
-        const uint32_t idesc = tc::idesc_f16_f32(128, N, 0);
+        const uint32_t idesc =
+            prm.rotated ? tc::idesc_bf16_f32(128, N, 0) : tc::idesc_f16_f32(128, N, 0);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = (uint32_t)(ks & 3) * 32;  // 16 columns = 32 bytes
@@ -383,12 +387,12 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     // this thread's cached key chunks to f16 and rotate its new key chunk
     // pairs with the table of the unit's positions, in place.
     auto prepare_unit = [&](int k, bool bad) {
-      if (prm.pos_offset) {
+      if (prm.pos_offset && !prm.rotated) {
         named_bar_sync(kBarCompute, kCompute);  // nobody still reads the previous table
         build_table(prm.pos_offset[unit_of(k) / prm.Hkv], kCompute);
         named_bar_sync(kBarCompute, kCompute);
       }
-      if (!bad) {
+      if (!bad && !prm.rotated) {
         const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
         const int bl = prm.pv.block_len;
         for (int bi = 0; bi < prm.pv.blocks_per_pair; ++bi) {
@@ -432,9 +436,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
       const int tt = min(row_tok, toks - 1);
       wait(&bars->qfull[s], (uint32_t)(i / kStages) & 1u);
-      // a warp whose 32 rows are all past the tile's tokens skips the work:
-      // rows are independent in both products, and such rows are never stored
-      if ((warp & 3) * 32 >= toks * G) {
+      // q that arrives rotated stays in the stage as loaded (bf16).  A warp whose
+      // 32 rows are all past the tile's tokens skips the work: rows are
+      // independent in both products, and such rows are never stored.
+      if (prm.rotated || (warp & 3) * 32 >= toks * G) {
         tc::fence_before_sync();
         mbar_arrive(&bars->rope_done);
         return;
@@ -690,6 +695,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.n_mt = L.n_mt;
   prm.num_units = pb.P * pb.Hkv;
   prm.kv_rows = L.kv_rows;
+  prm.rotated = (pb.flags & GIST_ATTN_FLAG_PREROTATED) ? 1 : 0;
   prm.stage_bytes = L.stage_bytes;
   prm.off_kv = L.off_kv;
   prm.kv_buf_bytes = L.kv_buf_bytes;
