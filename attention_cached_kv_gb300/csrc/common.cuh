@@ -255,18 +255,6 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
   return r;
 }
-// fp32 pair -> f16 pair, round to nearest even (|x| >= 65520 gives inf)
-__device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t v) {
-  float a, b;
-  f2_split(v, a, b);
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
-  return r;
-}
-// bf16 pair -> f16 pair (exact for magnitudes in [2^-17, 65504])
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-  return f2_to_f16x2(bf16x2_to_f2(v));
-}
 // Splits an fp32 pair x into hi + lo with hi = x truncated to bf16 (exact in
 // fp32, returned packed) and lo = bf16(x - hi): hi + lo carries x to ~16 bits.
 __device__ __forceinline__ void f2_split_bf16(uint64_t x, uint32_t& hi_bf, uint32_t& lo_bf) {

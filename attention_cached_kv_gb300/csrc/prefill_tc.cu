@@ -121,6 +121,18 @@ __device__ __forceinline__ void rope_chunk(const uint4& x, const uint4& y, const
   }
 }
 
+// fp32 pair -> f16 pair, round to nearest even (|x| >= 65520 gives inf)
+__device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t v) {
+  float a, b;
+  f2_split(v, a, b);
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+// bf16 pair -> f16 pair (exact for magnitudes in [2^-17, 65504])
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  return f2_to_f16x2(bf16x2_to_f2(v));
+}
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
