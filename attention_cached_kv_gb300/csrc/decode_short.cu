@@ -142,13 +142,18 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     constexpr int kStep = 32 / CPR;  // rows per pass of the warp
     const int c = lane % CPR, r0 = lane / CPR;
     if (!bad) {
+      // this lane's chunk column c of rows r0, r0 + kStep, ... of every block;
+      // a block's V rows sit Hkv * block_len rows after its K rows
+      const uint32_t col = base + b * bufb + (c >> 3) * pnl;
+      const uint32_t v_off = NP * pnl;
+      const int64_t v_gap = (int64_t)prm.Hkv * bl * D;
       for (int bi = 0; bi < bpp; ++bi) {  // uniform loop: the shuffle is safe
         const int32_t blk = __shfl_sync(0xffffffffu, id, bi);
-        const bf16* ks = pool_row(prm.pv, blk, g, 0, 0) + c * 8;
-        const bf16* vs = pool_row(prm.pv, blk, g, 1, 0) + c * 8;
-        for (int t = r0; t < bl; t += kStep) {
-          cp_async16(kaddr(b, bi * bl + t, c), ks + (size_t)t * D);
-          cp_async16(vaddr(b, bi * bl + t, c), vs + (size_t)t * D);
+        const bf16* src = pool_row(prm.pv, blk, g, 0, r0) + c * 8;
+        for (int row = bi * bl + r0; row < (bi + 1) * bl; row += kStep, src += kStep * D) {
+          const uint32_t dst = col + swz128(row, c & 7);
+          cp_async16(dst, src);
+          cp_async16(dst + v_off, src + v_gap);
         }
       }
     }
