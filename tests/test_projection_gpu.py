@@ -49,6 +49,7 @@ def _dims(P, l, Hq, Hkv, d, bl=8, bpp=1, nb=1, flags=0):
     (3, 64, 14, 2, 64, 256, None),       # the gist model's heads, a narrow model width
     (2, 37, 14, 2, 64, 896, "random"),   # ragged rows, the gist model width
     (2, 64, 8, 2, 128, 512, "random"),   # d = 128
+    (3, 40, 14, 2, 64, 200, "random"),   # d_model not a multiple of the 64-wide k-block
 ])
 def test_qkv_rope_matches_oracle(P, l, Hq, Hkv, d, dm, pos):
     x, w = _x(P, l, dm, 1), _weights((Hq + 2 * Hkv) * d, dm, 2)
@@ -67,7 +68,8 @@ def test_qkv_rope_matches_oracle(P, l, Hq, Hkv, d, dm, pos):
     compare(v, rv, "v_new")
 
 
-@pytest.mark.parametrize("P,l,Hq,d,dm", [(3, 50, 14, 64, 256), (2, 64, 14, 64, 896), (1, 200, 8, 128, 384)])
+@pytest.mark.parametrize("P,l,Hq,d,dm", [(3, 50, 14, 64, 256), (2, 64, 14, 64, 896), (1, 200, 8, 128, 384),
+                                          (5, 77, 14, 64, 1152)])
 def test_out_proj_matches_oracle(P, l, Hq, d, dm):
     a = _x(P, l * Hq, d, 4).reshape(P, l, Hq, d).contiguous()
     w = _weights(dm, Hq * d, 5)
