@@ -101,6 +101,9 @@ def kernel_source_hash(workload: str) -> str:
     return h.hexdigest()[:16]
 
 
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (~8 TB/s): context beside the measured copy peak
+
+
 def measured_peaks() -> tuple[float, str]:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -370,6 +373,7 @@ def run_ours(args) -> dict:
         "roofline": {"kernel": KERNEL_OF[args.workload][0],
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": bytes_info["total"],
