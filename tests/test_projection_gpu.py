@@ -107,11 +107,16 @@ def test_one_layer_projections_around_attention():
     assert (err <= 5e-2 + 5e-2 * np.abs(ry)).all(), err.max()
 
 
-def test_prerotated_flag_skips_rope_in_the_attention():
+@pytest.mark.parametrize("P,l,Hq,Hkv,d,nb", [
+    (3, 12, 14, 2, 64, 5),     # tensor-core prefill, two CTAs per SM
+    (2, 64, 32, 8, 128, 4),    # tensor-core prefill, d = 128
+    (4, 1, 14, 2, 64, 6),      # decode (short cache)
+    (3, 200, 14, 2, 64, 4),    # streaming prefill (cache + l > 128 keys)
+])
+def test_prerotated_flag_skips_rope_in_the_attention(P, l, Hq, Hkv, d, nb):
     """Rotating q and k_new outside (the oracle's rotation, rounded to bf16) and
     passing the flag gives the attention of the unrotated inputs."""
-    wl = workloads.make_custom(3, 12, 14, 2, 64, 8, 1, 5, device=DEV, seed=10)
-    P, l = 3, 12
+    wl = workloads.make_custom(P, l, Hq, Hkv, d, 8, 1, nb, device=DEV, seed=10)
     pos = 8 + np.arange(l)
     qr = np.stack([proj.rope_rows(oracle_f64(wl.q[p]).transpose(1, 0, 2), pos).transpose(1, 0, 2)
                    for p in range(P)])
