@@ -12,11 +12,12 @@
 //
 // Persistent CTAs, one per SM, warp-specialised: warp 4 streams 128 x 64
 // tiles of A and 256 x 64 tiles of B by TMA (128-byte swizzle) through a
-// 3-stage ring, warp 5 issues tcgen05.mma (128 x 256 x 16) into one of two
-// 256-column TMEM accumulators, and warps 0-3 (one thread per output row) drain
-// the other: RoPE, bf16, then 32-row x 64-column boxes written to shared memory
-// and stored by TMA while the next columns are computed.  Output tiles run
-// along N first, so the 128-row strip of A a CTA reads stays in L2.
+// 4-stage ring (3 where the RoPE table leaves no room for a fourth), warp 5
+// issues tcgen05.mma (128 x 256 x 16) into one of two 256-column TMEM
+// accumulators, and warps 0-3 (one thread per output row) drain the other:
+// RoPE, bf16, then one 32-row x 64-column box per warp in shared memory, stored
+// by TMA while the next box is computed.  Output tiles run along N first, so
+// the 128-row strip of A a CTA reads stays in L2.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
 #include <math.h>
@@ -30,13 +31,13 @@ namespace {
 
 constexpr int kEpi = 128;            // epilogue threads: one per tile row
 constexpr int kThreads = kEpi + 64;  // + the TMA warp and the MMA warp
-constexpr int kStages = 3;
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr uint32_t kTileA = kBM * kBK * 2;    // bytes of one A k-block tile
 constexpr uint32_t kTileB = kBN * kBK * 2;    // bytes of one B k-block tile
 constexpr uint32_t kStage = kTileA + kTileB;
 constexpr uint32_t kSlot = 32 * 128;          // one warp's 32 rows x 64 columns of bf16
 constexpr int kMaxSlots = 8;                  // pairs one 128-row tile can touch (QKV mode)
+constexpr int kMaxStages = 4;
 constexpr int kMaxSmem = 227 * 1024;
 
 // 2-D tiled store from shared memory (elements outside the tensor are dropped).
@@ -63,25 +64,27 @@ struct GemmParams {
   const int32_t* pos_offset;
   int32_t* status;
   int ntn, num_tiles;
+  int slots;     // pairs one 128-row tile can touch: (127 / l) + 2, at most kMaxSlots
+  int tab_rows;  // 8 + ceil(l / 8): the two levels of the token-angle table
   uint32_t off_out, off_tab, tab_stride, off_base, off_bar;
   float inv_freq[64];
 };
 
 struct GBars {
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_slot;
 };
 
 // tm_o0 / tm_o1 / tm_o2: q / k_new / v_new (QKV mode) or y (tm_o0 only), each
 // [rows][columns] bf16 with 64 x 32 boxes.
-template <int D>
+// S: stages of the operand ring (4 where shared memory allows, else 3).
+template <int D, int S>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_o0, const __grid_constant__ CUtensorMap tm_o1,
                 const __grid_constant__ CUtensorMap tm_o2, const __grid_constant__ GemmParams prm) {
   constexpr int HALF = D / 2;
-  constexpr int PC = D / 32;  // 16-column chunks from a rotated column to its partner
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -98,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
@@ -108,13 +111,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
-  if (prm.qkv) {  // (cos, cos, sin, sin) of t theta for frequency pairs, t < l
-    for (int idx = tid; idx < prm.l * (HALF / 2); idx += kThreads) {
-      const int t = idx / (HALF / 2), jp = idx - t * (HALF / 2);
+  if (prm.qkv) {
+    // (cos, cos, sin, sin) of t theta for frequency pairs, in two levels: rows
+    // 0..7 hold t = b < 8, rows 8.. hold t = 8a (a token's angle is the sum)
+    for (int idx = tid; idx < prm.tab_rows * (HALF / 2); idx += kThreads) {
+      const int row = idx / (HALF / 2), jp = idx - row * (HALF / 2);
+      const int t = row < 8 ? row : 8 * (row - 8);
       float s0, c0, s1, c1;
       sincosf((float)t * prm.inv_freq[2 * jp], &s0, &c0);
       sincosf((float)t * prm.inv_freq[2 * jp + 1], &s1, &c1);
-      *reinterpret_cast<float4*>(smem + prm.off_tab + t * prm.tab_stride + jp * 16) =
+      *reinterpret_cast<float4*>(smem + prm.off_tab + row * prm.tab_stride + jp * 16) =
           make_float4(c0, c1, s0, s1);
     }
   }
@@ -130,16 +136,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_a);
       tma_prefetch_map(&tm_b);
     }
-    int it = 0;  // k-blocks issued so far: ring slot it % kStages
+    int it = 0;  // k-blocks issued so far: ring slot it % S
     for (int tl = 0; tl < my_tiles && !failed; ++tl) {
       const int tile = (int)blockIdx.x + tl * (int)gridDim.x;
       const int m0 = (tile / prm.ntn) * kBM, n0 = (tile % prm.ntn) * kBN;
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int s = it % kStages;
+        const int s = it % S;
         // the slot is free once the MMAs that read it are done (a fresh
         // barrier passes the first wait)
         if (__any_sync(0xffffffffu,
-                       !mbar_wait(&bars->empty[s], ((uint32_t)(it / kStages) & 1u) ^ 1u))) {
+                       !mbar_wait(&bars->empty[s], ((uint32_t)(it / S) & 1u) ^ 1u))) {
           failed = true;
           break;
         }
@@ -169,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int s = it % kStages;
-        if (__any_sync(0xffffffffu, !mbar_wait(&bars->full[s], (uint32_t)(it / kStages) & 1u))) {
+        const int s = it % S;
+        if (__any_sync(0xffffffffu, !mbar_wait(&bars->full[s], (uint32_t)(it / S) & 1u))) {
           failed = true;
           break;
         }
@@ -194,9 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ epilogue
     const int r = tid;  // tile row == TMEM lane
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t out = sbase + prm.off_out + warp * 2 * kSlot;  // this warp's two 64-column boxes
+    const uint32_t out = sbase + prm.off_out + warp * kSlot;  // this warp's 32 x 64 output box
     const uint8_t* tab = smem + prm.off_tab;
-    uint8_t* base = smem + prm.off_base;  // [kMaxSlots][HALF / 2] of (cos, cos, sin, sin)
+    uint8_t* base = smem + prm.off_base;  // [slots][HALF / 2] of (cos, cos, sin, sin)
     const int rot_end = prm.qkv ? (prm.Hq + prm.Hkv) * D : 0;  // columns before it are rotated
     bool failed = false;
     if (lane == 0) {
@@ -212,12 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = (tile / prm.ntn) * kBM, n0 = (tile % prm.ntn) * kBN;
       const int width = min(kBN, prm.N - n0);
       // the first position of each pair the tile touches (uniform branch)
-      const uint8_t* trow = tab;
+      const uint8_t* tlo = tab;  // angle of t mod 8
+      const uint8_t* thi = tab;  // angle of 8 (t / 8)
       const uint8_t* brow = base;
       if (n0 < rot_end) {
         const int p_first = m0 / prm.l;
         named_bar_sync(1, kEpi);  // every thread is done with the previous tile's slots
-        for (int idx = r; idx < kMaxSlots * (HALF / 2); idx += kEpi) {
+        for (int idx = r; idx < prm.slots * (HALF / 2); idx += kEpi) {
           const int sl = idx / (HALF / 2), jp = idx - sl * (HALF / 2);
           const int p = p_first + sl;
           if (p * prm.l < prm.M) {
@@ -231,93 +238,115 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, kEpi);
         const int m = m0 + r;
         const int p = m / prm.l;
-        trow = tab + (m - p * prm.l) * prm.tab_stride;
+        const int t = m - p * prm.l;
+        tlo = tab + (t & 7) * prm.tab_stride;
+        thi = tab + (8 + (t >> 3)) * prm.tab_stride;
         brow = base + (p - p_first) * (HALF / 2) * 16;
       }
       if (!failed && !mbar_wait(&bars->acc_full[b], (uint32_t)(tl >> 1) & 1u)) failed = true;
       tc::fence_after_sync();
-      for (int u = 0; u < width / 128; ++u) {
-        const int nu = n0 + u * 128;  // first column of this 128-column unit
+      const uint32_t acc = tmem + lane_base + b * kBN;
+      // x' = x cos - y sin or y' = y cos + x sin for 16 columns, frequencies j0..j0+15
+      auto rotate16 = [&](const uint32_t (&xv)[16], const uint32_t (&yv)[16], int j0, bool second,
+                          uint32_t (&w)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int jp = (j0 >> 1) + e;
+          const uint4 ls = *reinterpret_cast<const uint4*>(tlo + jp * 16);
+          const uint4 hs = *reinterpret_cast<const uint4*>(thi + jp * 16);
+          const uint4 bs = *reinterpret_cast<const uint4*>(brow + jp * 16);
+          const uint64_t lc2 = f2_make(__uint_as_float(ls.x), __uint_as_float(ls.y));
+          const uint64_t ls2 = f2_make(__uint_as_float(ls.z), __uint_as_float(ls.w));
+          const uint64_t hc2 = f2_make(__uint_as_float(hs.x), __uint_as_float(hs.y));
+          const uint64_t hs2 = f2_make(__uint_as_float(hs.z), __uint_as_float(hs.w));
+          // angle of t = angle(8 (t / 8)) + angle(t mod 8)
+          const uint64_t tc2 = f2_sub(f2_mul(hc2, lc2), f2_mul(hs2, ls2));
+          const uint64_t ts2 = f2_fma(hs2, lc2, f2_mul(hc2, ls2));
+          const uint64_t bc2 = f2_make(__uint_as_float(bs.x), __uint_as_float(bs.y));
+          const uint64_t bs2 = f2_make(__uint_as_float(bs.z), __uint_as_float(bs.w));
+          // angle of position pos0 + t = angle(pos0) + angle(t)
+          const uint64_t cc = f2_sub(f2_mul(bc2, tc2), f2_mul(bs2, ts2));
+          const uint64_t ss = f2_fma(bs2, tc2, f2_mul(bc2, ts2));
+          const uint64_t x = f2_make(__uint_as_float(xv[2 * e]), __uint_as_float(xv[2 * e + 1]));
+          const uint64_t y = f2_make(__uint_as_float(yv[2 * e]), __uint_as_float(yv[2 * e + 1]));
+          w[e] = second ? f2_to_bf16x2(f2_fma(y, cc, f2_mul(x, ss)))
+                        : f2_to_bf16x2(f2_sub(f2_mul(x, cc), f2_mul(y, ss)));
+        }
+      };
+      // one 64-column box at a time: computed, written to the warp's box once the
+      // previous box's store has read it, and stored by TMA
+      for (int j = 0; j < width / 64; ++j) {
+        const int nb = n0 + 64 * j;  // first column of the box
         const CUtensorMap* map = &tm_o0;
-        int col = nu;
-        if (prm.qkv && nu >= prm.Hq * D) {
-          if (nu < rot_end) {
+        int col = nb;
+        if (prm.qkv && nb >= prm.Hq * D) {
+          if (nb < rot_end) {
             map = &tm_o1;
-            col = nu - prm.Hq * D;
+            col = nb - prm.Hq * D;
           } else {
             map = &tm_o2;
-            col = nu - rot_end;
+            col = nb - rot_end;
           }
         }
-        const bool rot = nu < rot_end;
-        const uint32_t acc = tmem + lane_base + b * kBN + u * 128;
+        const uint32_t a0 = acc + 64 * j;
+        uint32_t w[4][8];
+        if (nb >= rot_end) {
+          uint32_t v[4][16];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t v[4][16], w[4][8];
-          int oc[4];  // 16-column chunk (0..7) of the unit each w[] goes to
-          if (rot) {
-            // x chunks x0, x0+1 pair with x0+PC, x0+1+PC (rotate-half inside a head)
-            const int x0 = D == 64 ? hf * 4 : hf * 2;
-            oc[0] = x0;
-            oc[1] = x0 + 1;
-            oc[2] = x0 + PC;
-            oc[3] = x0 + 1 + PC;
-          } else {
+          for (int q = 0; q < 4; ++q) tc::ld16(a0 + 16 * q, v[q]);
+          tc::wait_ld();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) oc[q] = hf * 4 + q;
+          for (int q = 0; q < 4; ++q) {
+            tmem_pin(v[q]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[q][e] = f2_to_bf16x2(f2_make(__uint_as_float(v[q][2 * e]), __uint_as_float(v[q][2 * e + 1])));
           }
+        } else if (D == 64) {
+          // the box is one head: x = columns 0..31, y = 32..63
+          uint32_t v[4][16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) tc::ld16(acc + oc[q] * 16, v[q]);
+          for (int q = 0; q < 4; ++q) tc::ld16(a0 + 16 * q, v[q]);
           tc::wait_ld();
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_pin(v[q]);
-          if (rot) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            rotate16(v[q], v[q + 2], 16 * q, false, w[q]);
+            rotate16(v[q], v[q + 2], 16 * q, true, w[q + 2]);
+          }
+        } else {
+          // half of a 128-column head: x' from the first box (j even), y' from the second
+          const bool second = (j & 1) != 0;
+          const uint32_t hx = second ? a0 - 64 : a0;  // the head's x columns
+#pragma unroll
+          for (int q2 = 0; q2 < 4; q2 += 2) {
+            uint32_t xv[2][16], yv[2][16];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-              const int j0 = (oc[q] % (D / 16)) * 16;  // first frequency of the chunk
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int jp = (j0 >> 1) + e;
-                const uint4 cs = *reinterpret_cast<const uint4*>(trow + jp * 16);
-                const uint4 bs = *reinterpret_cast<const uint4*>(brow + jp * 16);
-                const uint64_t tc2 = f2_make(__uint_as_float(cs.x), __uint_as_float(cs.y));
-                const uint64_t ts2 = f2_make(__uint_as_float(cs.z), __uint_as_float(cs.w));
-                const uint64_t bc2 = f2_make(__uint_as_float(bs.x), __uint_as_float(bs.y));
-                const uint64_t bs2 = f2_make(__uint_as_float(bs.z), __uint_as_float(bs.w));
-                // angle of position pos0 + t = angle(pos0) + angle(t)
-                const uint64_t cc = f2_sub(f2_mul(bc2, tc2), f2_mul(bs2, ts2));
-                const uint64_t ss = f2_fma(bs2, tc2, f2_mul(bc2, ts2));
-                const uint64_t x = f2_make(__uint_as_float(v[q][2 * e]), __uint_as_float(v[q][2 * e + 1]));
-                const uint64_t y =
-                    f2_make(__uint_as_float(v[q + 2][2 * e]), __uint_as_float(v[q + 2][2 * e + 1]));
-                w[q][e] = f2_to_bf16x2(f2_sub(f2_mul(x, cc), f2_mul(y, ss)));
-                w[q + 2][e] = f2_to_bf16x2(f2_fma(y, cc, f2_mul(x, ss)));
-              }
+              tc::ld16(hx + 16 * (q2 + q), xv[q]);
+              tc::ld16(hx + 64 + 16 * (q2 + q), yv[q]);
             }
-          } else {
+            tc::wait_ld();
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 2; ++q) {
+              tmem_pin(xv[q]);
+              tmem_pin(yv[q]);
+              rotate16(xv[q], yv[q], 16 * (q2 + q), second, w[q2 + q]);
+            }
+          }
+        }
+        if (lane == 0) bulk_wait_read_all();  // the previous box has been read out
+        __syncwarp();
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                w[q][e] = f2_to_bf16x2(f2_make(__uint_as_float(v[q][2 * e]), __uint_as_float(v[q][2 * e + 1])));
-          }
-          if (hf == 0) {  // the boxes of the previous unit have been read out
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-          }
-          // chunk k of the unit: box k / 4, 16-byte chunks 2 (k % 4) and 2 (k % 4) + 1 of row `lane`
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t box = out + (oc[q] >> 2) * kSlot;
-            sts16(box + swz128(lane, 2 * (oc[q] & 3)), make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]));
-            sts16(box + swz128(lane, 2 * (oc[q] & 3) + 1), make_uint4(w[q][4], w[q][5], w[q][6], w[q][7]));
-          }
+        for (int q = 0; q < 4; ++q) {
+          sts16(out + swz128(lane, 2 * q), make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]));
+          sts16(out + swz128(lane, 2 * q + 1), make_uint4(w[q][4], w[q][5], w[q][6], w[q][7]));
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {  // rows past M are dropped by the store
           tma_store_2d(map, out, col, m0 + warp * 32);
-          tma_store_2d(map, out + kSlot, col + 64, m0 + warp * 32);
           bulk_commit();
         }
       }
@@ -351,27 +380,27 @@ int encode_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_
   return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
 }
 
-// Shared memory: the ring, the output boxes, the RoPE table of l rows and the
-// per-tile base slots; 0 if it does not fit.
-uint32_t smem_plan(GemmParams& prm, int d) {
-  uint32_t off = kStages * kStage;
+// Shared memory: the ring of S stages, the output boxes, the RoPE table of l rows
+// and the per-tile base slots; 0 if it does not fit.
+uint32_t smem_plan(GemmParams& prm, int d, int stages) {
+  uint32_t off = (uint32_t)stages * kStage;
   prm.off_out = off;
-  off += 4 * 2 * kSlot;
+  off += 4 * kSlot;
   prm.off_tab = off;
   prm.tab_stride = (uint32_t)(d / 4) * 16 + 16;  // +16 B: consecutive tokens on different banks
-  off += prm.qkv ? (uint32_t)prm.l * prm.tab_stride : 0;
+  off += prm.qkv ? (uint32_t)prm.tab_rows * prm.tab_stride : 0;
   prm.off_base = off;
-  off += prm.qkv ? (uint32_t)kMaxSlots * (d / 4) * 16 : 0;
+  off += prm.qkv ? (uint32_t)prm.slots * (d / 4) * 16 : 0;
   prm.off_bar = off;
   off += 128;
   const uint32_t bytes = off + 1024;
   return bytes <= (uint32_t)kMaxSmem ? bytes : 0;
 }
 
-template <int D>
+template <int D, int S>
 int launch_gemm_d(GemmParams prm, const void* a, const void* b, void* o0, void* o1, void* o2,
                   cudaStream_t stream) {
-  const uint32_t bytes = smem_plan(prm, D);
+  const uint32_t bytes = smem_plan(prm, D, S);
   if (bytes == 0) return GIST_ATTN_ERR_UNSUPPORTED;
   alignas(64) CUtensorMap tm_a, tm_b, tm_o0, tm_o1, tm_o2;
   int rc = encode_2d(&tm_a, a, prm.M, prm.K, kBK, kBM);
@@ -386,7 +415,7 @@ int launch_gemm_d(GemmParams prm, const void* a, const void* b, void* o0, void* 
     tm_o2 = tm_o0;
   }
   if (rc != GIST_ATTN_OK) return rc;
-  if (cudaFuncSetAttribute(gemm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_kernel<D, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   int dev = 0, sms = 0;
@@ -394,8 +423,17 @@ int launch_gemm_d(GemmParams prm, const void* a, const void* b, void* o0, void* 
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   const int grid = prm.num_tiles < sms ? prm.num_tiles : sms;
-  gemm_kernel<D><<<grid, kThreads, bytes, stream>>>(tm_a, tm_b, tm_o0, tm_o1, tm_o2, prm);
+  gemm_kernel<D, S><<<grid, kThreads, bytes, stream>>>(tm_a, tm_b, tm_o0, tm_o1, tm_o2, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
+}
+
+// Four stages where they fit beside the output boxes and the RoPE table, else three.
+template <int D>
+int launch_gemm_stages(GemmParams prm, const void* a, const void* b, void* o0, void* o1,
+                       void* o2, cudaStream_t stream) {
+  GemmParams probe = prm;
+  if (smem_plan(probe, D, 4) != 0) return launch_gemm_d<D, 4>(prm, a, b, o0, o1, o2, stream);
+  return launch_gemm_d<D, 3>(prm, a, b, o0, o1, o2, stream);
 }
 
 int launch_common(GemmParams& prm, const void* a, const void* b, int d, void* o0, void* o1,
@@ -405,8 +443,8 @@ int launch_common(GemmParams& prm, const void* a, const void* b, int d, void* o0
   if (mt * prm.ntn > 0x7fffffff) return GIST_ATTN_ERR_UNSUPPORTED;
   prm.num_tiles = (int)(mt * prm.ntn);
   if (prm.num_tiles == 0) return GIST_ATTN_OK;
-  if (d == 64) return launch_gemm_d<64>(prm, a, b, o0, o1, o2, stream);
-  return launch_gemm_d<128>(prm, a, b, o0, o1, o2, stream);
+  if (d == 64) return launch_gemm_stages<64>(prm, a, b, o0, o1, o2, stream);
+  return launch_gemm_stages<128>(prm, a, b, o0, o1, o2, stream);
 }
 
 }  // namespace
@@ -431,6 +469,8 @@ int launch_qkv_rope(const Problem& pb, const void* x, const void* w, int d_model
   // the shared-memory plan)
   if ((kBM - 1) / pb.l + 2 > kMaxSlots) return GIST_ATTN_ERR_UNSUPPORTED;
   prm.qkv = 1;
+  prm.slots = (kBM - 1) / pb.l + 2;
+  prm.tab_rows = 8 + (pb.l + 7) / 8;
   prm.l = pb.l;
   prm.Hq = pb.Hq;
   prm.Hkv = pb.Hkv;

@@ -231,8 +231,8 @@ int gist_kv_store(const void* k_new, const void* v_new, void* kv_pool, const int
  *   q      bf16 [P][l][Hq][d];  k_new, v_new bf16 [P][l][Hkv][d]  (written)
  * Feed the results to gist_attn_fwd with GIST_ATTN_FLAG_PREROTATED.  This build
  * needs Hq*d and Hkv*d multiples of 128, l >= 22 (a 128-row tile spans at most
- * 8 pairs) and l <= 180 for d = 64, l <= 88 for d = 128 (the table of the l
- * token angles sits in shared memory), else GIST_ATTN_ERR_UNSUPPORTED.
+ * 8 pairs) and l <= 1904 for d = 64, l <= 936 for d = 128 (the table of token
+ * angles sits in shared memory), else GIST_ATTN_ERR_UNSUPPORTED.
  */
 int gist_qkv_rope(const void* x, const void* w_qkv, const int32_t* pos_offset, void* q,
                   void* k_new, void* v_new, int d_model, const gist_attn_dims* dims,

@@ -20,6 +20,21 @@ def lib():
     return binding.load_library()
 
 
+@pytest.fixture
+def fake_ptrs(lib):
+    """The rejection tests pass fake device addresses that only a call failing on
+    the host never touches.  Where a GPU is visible a call that unexpectedly
+    passed every check would launch on them, so these tests run without one."""
+    try:
+        import torch
+        visible = torch.cuda.is_available()
+    except Exception:  # pragma: no cover - torch is part of the environment
+        visible = False
+    if visible:
+        pytest.skip("fake device addresses: host-only test")
+    return lib
+
+
 def header_functions():
     text = open(os.path.join(ROOT, "include", "gist_attn.h")).read()
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(gist_\w+)\s*\(", text, re.M)))
@@ -86,11 +101,13 @@ def call(lib, dims=BASE, q=P16, k=P16, v=P16, pool=P16, ids=P16, table=None, pos
     (dict(ids=P16 + 2), binding.ERR_ALIGN),
     (dict(pos=P16 + 1), binding.ERR_ALIGN),
 ])
-def test_host_rejects_bad_arguments(lib, case, code):
+def test_host_rejects_bad_arguments(fake_ptrs, case, code):
+    lib = fake_ptrs
     assert call(lib, **case) == code
 
 
-def test_empty_batch_launches_nothing(lib):
+def test_empty_batch_launches_nothing(fake_ptrs):
+    lib = fake_ptrs
     assert call(lib, dims=dict(BASE, num_pairs=0), q=0, k=0, v=0, out=0) == binding.OK
 
 
@@ -101,7 +118,8 @@ def test_status_strings(lib):
     assert "f16" in binding.status_string(binding.STATUS_RANGE)
 
 
-def test_gather_debug_rejects_bad_arguments(lib):
+def test_gather_debug_rejects_bad_arguments(fake_ptrs):
+    lib = fake_ptrs
     V = ctypes.c_void_p
     D = ctypes.byref(binding.make_dims(BASE))
     assert lib.gist_attn_gather_debug(V(P16), V(P16), None, None, D, None) == binding.ERR_NULL
@@ -109,7 +127,8 @@ def test_gather_debug_rejects_bad_arguments(lib):
     assert lib.gist_attn_gather_debug(V(P16), None, None, V(P16), D, None) == binding.ERR_NULL
 
 
-def test_gist_mask_rejects_bad_arguments(lib):
+def test_gist_mask_rejects_bad_arguments(fake_ptrs):
+    lib = fake_ptrs
     V = ctypes.c_void_p
     D0 = dict(BASE, block_len=0, blocks_per_pair=0, num_blocks=0)
     D = ctypes.byref(binding.make_dims(D0))
@@ -122,7 +141,8 @@ def test_gist_mask_rejects_bad_arguments(lib):
     assert f(V(P16), V(P16), V(P16), None, None, None, None, V(P16), 4, V(P16), Dg, None) == binding.ERR_UNSUPPORTED
 
 
-def test_kv_store_rejects_bad_arguments(lib):
+def test_kv_store_rejects_bad_arguments(fake_ptrs):
+    lib = fake_ptrs
     V = ctypes.c_void_p
     f = lib.gist_kv_store
     ok = dict(BASE, n_new=12, block_len=8, blocks_per_pair=1)
@@ -137,7 +157,8 @@ def test_kv_store_rejects_bad_arguments(lib):
     assert f(None, None, None, None, None, None, Dz, None) == binding.OK
 
 
-def test_projections_reject_bad_arguments(lib):
+def test_projections_reject_bad_arguments(fake_ptrs):
+    lib = fake_ptrs
     V = ctypes.c_void_p
     D = ctypes.byref(binding.make_dims(dict(BASE, n_new=64)))
     q = lib.gist_qkv_rope
@@ -150,8 +171,8 @@ def test_projections_reject_bad_arguments(lib):
     assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, odd, None) == binding.ERR_UNSUPPORTED
     short = ctypes.byref(binding.make_dims(dict(BASE, n_new=4)))
     assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, short, None) == binding.ERR_UNSUPPORTED
-    # the table of l token angles must fit shared memory: l <= 180 (d = 64), l <= 88 (d = 128)
-    for dd in (dict(BASE, n_new=181), dict(BASE, n_new=89, head_dim=128, num_q_heads=8)):
+    # the table of token angles must fit shared memory: l <= 1904 (d = 64), l <= 936 (d = 128)
+    for dd in (dict(BASE, n_new=1905), dict(BASE, n_new=937, head_dim=128, num_q_heads=8)):
         long_ = ctypes.byref(binding.make_dims(dd))
         assert q(V(P16), V(P16), None, V(P16), V(P16), V(P16), 256, long_, None) == binding.ERR_UNSUPPORTED
     o = lib.gist_out_proj
