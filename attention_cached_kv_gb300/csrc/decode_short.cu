@@ -59,7 +59,9 @@ struct Region {
   __host__ __device__ static uint32_t panel(int kvr) { return (uint32_t)kvr * 128; }
   __host__ __device__ static uint32_t buf(int kvr) { return 2u * NP * panel(kvr); }
   __host__ __device__ static uint32_t tab(int kvr) { return 2 * buf(kvr); }
-  __host__ __device__ static uint32_t bytes(int kvr) { return (tab(kvr) + (D / 2) * 8 + 127) & ~127u; }
+  __host__ __device__ static uint32_t bars(int kvr) { return tab(kvr) + (D / 2) * 8; }  // 2 mbarriers
+  // rounded to 1 KiB so that every buffer of every warp starts on a swizzle atom
+  __host__ __device__ static uint32_t bytes(int kvr) { return (bars(kvr) + 16 + 1023) & ~1023u; }
 };
 
 // D(16x8) += A(16x8, bf16, row) * B(8x8, bf16, col)
@@ -79,8 +81,15 @@ __device__ __forceinline__ uint32_t ldg32(const bf16* p) {
 
 // G8: the group has at most 8 query heads, so rows 8..15 of every 16-row
 // fragment are zero and their work is left out at compile time.
-template <int D, bool G8>
-__global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_constant__ ShortParams prm) {
+// TMA: a unit's rows arrive by tensor copies issued by one lane (cached blocks of
+// a multiple of 8 rows, each (block, K|V) a {64, block_len} box, the new key and
+// value {64, 1} boxes), completing on the buffer's mbarrier; otherwise every lane
+// issues 16-byte cp.async copies.
+template <int D, bool G8, bool TMA>
+__global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_constant__ ShortParams prm,
+                                                                const __grid_constant__ CUtensorMap tm_pool,
+                                                                const __grid_constant__ CUtensorMap tm_kn,
+                                                                const __grid_constant__ CUtensorMap tm_vn) {
   using R = Region<D>;
   constexpr int NP = D / 64;
   constexpr int CPR = D / 8;
@@ -99,6 +108,19 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   const uint32_t base = smem_u32(reg);
   const uint32_t pnl = R::panel(kvr), bufb = R::buf(kvr);
   float2* tab = reinterpret_cast<float2*>(reg + R::tab(kvr));
+  uint64_t* kvbar = reinterpret_cast<uint64_t*>(reg + R::bars(kvr));  // one per buffer (TMA)
+  if (TMA) {
+    if ((base & 1023u) != 0) {  // the swizzle atoms need 1 KiB alignment: never expected
+      if (lane == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+      return;
+    }
+    if (lane == 0) {
+      mbar_init(&kvbar[0], 1);
+      mbar_init(&kvbar[1], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+  }
   auto kaddr = [&](int b, int row, int c) {
     return base + b * bufb + (c >> 3) * pnl + swz128(row, c & 7);
   };
@@ -139,6 +161,31 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   // block ids is out of range (its cached rows are then not copied)
   auto issue = [&](int p, int g, int b, int32_t id) -> bool {
     const bool bad = __any_sync(0xffffffffu, lane < bpp && !pool_block_ok(prm.pv, id));
+    if (TMA) {
+      const uint32_t buf = base + b * bufb;
+      if (lane == 0)
+        mbar_arrive_expect_tx(&kvbar[b], (bad ? 0u : (uint32_t)bpp * 2 * bl * 128 * NP) + 2u * 128 * NP);
+      for (int bi = 0; bi < bpp; ++bi) {  // uniform loop: the shuffle is safe
+        const int32_t blk = __shfl_sync(0xffffffffu, id, bi);
+        if (lane == 0 && !bad) {
+          const int row_k = (int)((((int64_t)blk * prm.pv.num_layers + prm.pv.layer) * 2 * prm.Hkv + g) * bl);
+          const int row_v = row_k + prm.Hkv * bl;
+#pragma unroll
+          for (int x = 0; x < NP; ++x) {
+            tma_load_2d(buf + x * pnl + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x, row_k);
+            tma_load_2d(buf + (NP + x) * pnl + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x, row_v);
+          }
+        }
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int x = 0; x < NP; ++x) {
+          tma_load_2d(buf + x * pnl + C * 128, &tm_kn, &kvbar[b], 64 * x, p * prm.Hkv + g);
+          tma_load_2d(buf + (NP + x) * pnl + C * 128, &tm_vn, &kvbar[b], 64 * x, p * prm.Hkv + g);
+        }
+      }
+      return bad;
+    }
     constexpr int kStep = 32 / CPR;  // rows per pass of the warp
     const int c = lane % CPR, r0 = lane / CPR;
     if (!bad) {
@@ -202,9 +249,13 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       bad_next = issue(pn, gn, b ^ 1, id_next);
       load_q(pn, gn, qnext);
       id_next = load_id(un + W);
-      cp_async_wait_group<1>();
-    } else {
+      if (!TMA) cp_async_wait_group<1>();
+    } else if (!TMA) {
       cp_async_wait_group<0>();
+    }
+    if (TMA) {  // unit u's copies are the ((n / 2) + 1)-th phase of its buffer's barrier
+      if (!mbar_wait(&kvbar[b], (uint32_t)(n >> 1) & 1u) && lane == 0)
+        report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     }
     __syncwarp();  // every lane's copies of unit u have landed
 
@@ -353,7 +404,10 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
           *reinterpret_cast<uint32_t*>(out + (int64_t)rb * D + col) = float2_to_bf16x2(o[dn][2] * ib, o[dn][3] * ib);
       }
     }
-    __syncwarp();  // buffer b is free for the unit after next
+    // buffer b is free for the unit after next; its shared-memory reads and the
+    // key rotation's writes come before the tensor copies that refill it
+    fence_proxy_async_smem();
+    __syncwarp();
     if (!more) break;
     u = un;
     p = pn;
@@ -369,7 +423,30 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   }
 }
 
-template <int D, bool G8>
+// [rows][d] bf16 viewed as 64-column boxes of box_rows rows, 128-byte swizzle.
+int encode_rows(CUtensorMap* m, const void* base, int64_t rows, int d, int box_rows) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return GIST_ATTN_ERR_LAUNCH;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+// Tensor copies need whole swizzle atoms per cached block (a multiple of 8 rows),
+// boxes of at most 256 rows and row coordinates below 2^31.
+bool tma_path(const Problem& pb) {
+  const int64_t pool_rows = (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len;
+  return pb.blocks_per_pair > 0 && pb.block_len % 8 == 0 && pb.block_len <= 256 &&
+         pool_rows < 0x7fffffff && (int64_t)pb.P * pb.Hkv < 0x7fffffff;
+}
+
+template <int D, bool G8, bool TMA>
 int launch_d(const Problem& pb, cudaStream_t stream) {
   ShortParams prm{};
   prm.q = static_cast<const bf16*>(pb.q);
@@ -389,22 +466,35 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.units = pb.P * pb.Hkv;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  alignas(64) CUtensorMap tm_pool{}, tm_kn{}, tm_vn{};
+  if (TMA) {
+    int rc = encode_rows(&tm_pool, pb.kv_pool, (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len,
+                         D, pb.block_len);
+    if (rc == GIST_ATTN_OK) rc = encode_rows(&tm_kn, pb.k_new, (int64_t)pb.P * pb.Hkv, D, 1);
+    if (rc == GIST_ATTN_OK) rc = encode_rows(&tm_vn, pb.v_new, (int64_t)pb.P * pb.Hkv, D, 1);
+    if (rc != GIST_ATTN_OK) return rc;
+  }
   const uint32_t bytes = kWarps * prm.region;
-  if (cudaFuncSetAttribute(decode_short_kernel<D, G8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_short_kernel<D, G8, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_short_kernel<D, G8>, kThreads,
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_short_kernel<D, G8, TMA>, kThreads,
                                                     bytes) != cudaSuccess ||
       per_sm < 1)
     return GIST_ATTN_ERR_LAUNCH;
   // persistent: one wave of resident CTAs walks all units
   const int64_t need = (prm.units + kWarps - 1) / kWarps;
   const int64_t grid = need < (int64_t)sms * per_sm ? need : (int64_t)sms * per_sm;
-  decode_short_kernel<D, G8><<<(unsigned)grid, kThreads, bytes, stream>>>(prm);
+  decode_short_kernel<D, G8, TMA><<<(unsigned)grid, kThreads, bytes, stream>>>(prm, tm_pool, tm_kn, tm_vn);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
+}
+
+template <int D, bool G8>
+int launch_path(const Problem& pb, cudaStream_t stream) {
+  return tma_path(pb) ? launch_d<D, G8, true>(pb, stream) : launch_d<D, G8, false>(pb, stream);
 }
 
 }  // namespace
@@ -416,8 +506,8 @@ bool decode_short_fits(const Problem& pb) {
 
 int launch_decode_short(const Problem& pb, cudaStream_t stream) {
   const bool g8 = pb.G <= 8;
-  if (pb.d == 64) return g8 ? launch_d<64, true>(pb, stream) : launch_d<64, false>(pb, stream);
-  if (pb.d == 128) return g8 ? launch_d<128, true>(pb, stream) : launch_d<128, false>(pb, stream);
+  if (pb.d == 64) return g8 ? launch_path<64, true>(pb, stream) : launch_path<64, false>(pb, stream);
+  if (pb.d == 128) return g8 ? launch_path<128, true>(pb, stream) : launch_path<128, false>(pb, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 
