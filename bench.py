@@ -70,6 +70,9 @@ def parse_args(argv=None):
                     help="cached-KV element type (fp8: E4M3 pool with per-block scales)")
     ap.add_argument("--fused", action="store_true",
                     help="also time the projections either side (QKV + RoPE, output projection)")
+    ap.add_argument("--row", choices=["offline", "block-mass"], default=None,
+                    help="measure a widening row instead of the hot path: the offline gist "
+                         "compression pass, or the paged decode with per-block attention mass + append")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -580,9 +583,158 @@ def run_reference(args) -> dict | None:
     }
 
 
+def _timed_layers(args, L, launch, stream, ws):
+    """W warm-up steps, then K steps of L layers; returns (total ms, per-layer
+    ms of each phase) with CUDA events on the launching stream, max over ranks."""
+    import torch
+
+    for _ in range(max(args.warmup, 0)):
+        for li in range(L):
+            launch(li, None)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    start.record(stream)
+    for k in range(K):
+        for li in range(L):
+            launch(li, ev[k][li])
+    end.record(stream)
+    torch.cuda.synchronize()
+    total = max_over_ranks(start.elapsed_time(end), ws)
+    ph = [max_over_ranks(sum(e[li][j].elapsed_time(e[li][j + 1]) for e in ev for li in range(L)) / (K * L), ws)
+          for j in range(2)]
+    return total, ph
+
+
+def run_row(args) -> dict:
+    """The widening rows, each through its C-ABI entry points on synthetic data.
+
+    offline: the gist compression pass of Gist page "论文做了什么" / "在线的一次
+      attention": B items of j = 1000 prompt tokens + k = 8 gist tokens (an item
+      runs to about a thousand tokens on that page), the gist model (Hq 14, Hkv 2,
+      d 64), per layer the causal pass over [prompt; gist] through
+      gist_attn_fwd_gist_mask, then gist_kv_store of the k gist rows.
+    block-mass: the paged decode workload through gist_attn_fwd_block_mass
+      (Suffix page §4, §5 第三步) followed by gist_kv_append of the new token
+      (KV page "Reusable-state"); the append writes the sequence's last cached
+      slot, a stand-in for the next block's first one (the pool has no spare
+      block), so the cache the next step reads keeps its size."""
+    import torch
+
+    from attention_cached_kv_gb300 import binding, workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load_library()
+    stream = torch.cuda.Stream(device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    peak, peak_src = measured_peaks()
+    if args.row == "offline":
+        B, j, k = args.queries or 128, 1000, 8
+        L = args.layers or 24
+        l, Hq, Hkv, d = j + k, 14, 2, 64
+        g = torch.Generator(device=dev).manual_seed(21)
+        q = torch.randn((B, l, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+        kn = torch.randn((B, l, Hkv, d), generator=g, device=dev).to(torch.bfloat16)
+        vn = torch.randn((B, l, Hkv, d), generator=g, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        pool = torch.zeros((B, L, 2, Hkv, k, d), dtype=torch.bfloat16, device=dev)
+        ids = torch.arange(B, dtype=torch.int32, device=dev)
+        gstart = torch.full((B,), j, dtype=torch.int32, device=dev)
+        base = dict(num_pairs=B, n_new=l, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_len=k,
+                    num_blocks=B, num_layers=L, rope_theta=1e4, softmax_scale=0.0)
+
+        def launch(li, e):
+            attn_dims = dict(base, blocks_per_pair=0, layer=li)
+            store_dims = dict(base, blocks_per_pair=1, layer=li)
+            if e: e[0].record(stream)
+            binding.gist_attn_fwd_gist_mask(q, kn, vn, pool, None, None, None, gstart, k, out,
+                                            dims=attn_dims, status=status, stream=stream)
+            if e: e[1].record(stream)
+            binding.gist_kv_store(kn, vn, pool, ids, gstart, None, dims=store_dims, status=status,
+                                  stream=stream)
+            if e: e[2].record(stream)
+
+        total, (t_attn, t_store) = _timed_layers(args, L, launch, stream, ws)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())}")
+        flops = 4.0 * d * Hq * (l * (l + 1) / 2)      # useful: causal scores + PV per item-layer
+        nbytes = 2 * (2 * l * Hq * d) + 2 * (2 * l * Hkv * d)  # q, out, k_new, v_new
+        tfl = B * flops / (t_attn * 1e-3) / 1e12
+        bf16_peak = 1890.5
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                bf16_peak = float(json.load(f)["bf16_tflops"])
+        except (OSError, KeyError, ValueError):
+            pass
+        return {"metric": "items compressed per second per layer (offline gist pass + store)",
+                "value": B * L * args.steps * ws / (total * 1e-3), "unit": "items/s",
+                "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": total / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+                "config": {"workload": f"offline gist compression: {B} items x ({j} prompt + {k} gist) "
+                                       f"tokens, {L} layers, Hq={Hq}, Hkv={Hkv}, d={d}; causal pass + store",
+                           "items": B, "layers_per_step": L},
+                "roofline": {"kernel": "prefill_stream_kernel", "bound": "tensor",
+                             "achieved": tfl, "peak": bf16_peak, "unit": "TFLOP/s",
+                             "frac": tfl / bf16_peak, "traffic": None,
+                             "peak_source": "MEASURED_PEAKS bf16_tflops (cuBLAS burst)",
+                             "useful_flops_per_item_layer": flops,
+                             "hbm_bytes_per_item_layer": nbytes,
+                             "achieved_gbs": B * nbytes / (t_attn * 1e-3) / 1e9,
+                             "attention_ms": t_attn, "store_ms": t_store},
+                "gpu_launches": 2 * L * args.steps, "impl": "ours"}
+    # block-mass
+    wl = workloads.make("paged", device=dev, **({"num_layers": args.layers} if args.layers else {}))
+    L, P = wl.dims["num_layers"], wl.dims["num_pairs"]
+    dd = wl.dims
+    C = dd["block_len"] * dd["blocks_per_pair"]
+    out = torch.empty_like(wl.q)
+    mass = torch.empty((P, dd["num_q_heads"], dd["blocks_per_pair"]), dtype=torch.float32, device=dev)
+    slot = torch.full((P,), C - 1, dtype=torch.int32, device=dev)
+
+    def launch(li, e):
+        dl = dict(dd, layer=li)
+        if e: e[0].record(stream)
+        binding.gist_attn_fwd_block_mass(wl.q, wl.k_new, wl.v_new, wl.kv_pool, wl.block_table, wl.pos_offset,
+                                         out, mass, dims=dl, status=status, stream=stream)
+        if e: e[1].record(stream)
+        binding.gist_kv_append(wl.k_new, wl.v_new, wl.kv_pool, wl.block_table, slot, wl.pos_offset,
+                               dims=dl, status=status, stream=stream)
+        if e: e[2].record(stream)
+
+    total, (t_dec, t_app) = _timed_layers(args, L, launch, stream, ws)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    bytes_info = algorithmic_bytes_per_launch(wl)
+    nbytes = bytes_info["total"] + mass.numel() * 4
+    achieved = nbytes / (t_dec * 1e-3) / 1e9
+    return {"metric": "(sequence, step) pairs/s per layer: decode with per-block attention mass + KV append",
+            "value": P * L * args.steps * ws / (total * 1e-3), "unit": "pairs/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16; permuted block tables)",
+            "config": {"workload": DESCR["paged"] + "; per-block attention mass, then the new token appended",
+                       "pairs": P, "layers_per_step": L},
+            "roofline": {"kernel": "decode_long_kernel (block mass)", "bound": "hbm", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peak_src} copy bandwidth",
+                         "algorithmic_bytes_per_launch": nbytes, "decode_ms": t_dec, "append_ms": t_app},
+            "gpu_launches": 2 * L * args.steps, "impl": "ours"}
+
+
 def main(argv=None):
     args = parse_args(argv)
-    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.row and args.impl == "ours":
+        res = run_row(args)
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_ours(args)
     ws, rank, _ = dist_env()
     if res is not None and rank == 0:
         line = json.dumps(res)
