@@ -10,18 +10,21 @@
 // optional per-pair gist start the kernel also applies the full gist mask (a
 // token after the gist no longer sees the prompt), the training-layout forward.
 //
-// One CTA (4 warps) per (pair, KV head, group of whole tokens with at most 64
+// One CTA (8 warps) per (pair, KV head, group of whole tokens with at most 128
 // rows); rows are (token, head-in-group), token-major -- the memory order of
 // q/out, so the group's q rows arrive by one TMA tensor copy per 64-column
 // panel (128-byte swizzle) and leave the same way.  Keys stream through a
 // double-buffered shared-memory ring in tiles of 64: cached rows by 16-byte
-// cp.async through the pool gather, new values by cp.async, new keys rotated
-// in registers on the way in.  Rotations use angle addition: one table of
-// (cos, sin)(r theta) for r < 64 per CTA and a per-tile base angle, so no
-// angle grows with the position.  Each warp keeps its 16-row tile's q
-// fragments (rotated, split into bf16 hi + lo so the rounding of rotated q
-// stays out of the logits), S = q K^T and O += P V on mma.sync m16n8k16 with
-// fp32 accumulation, and a running max / sum softmax across key tiles.
+// cp.async through the pool gather (then converted to f16 in place), new values
+// by cp.async, new keys rotated in registers on the way in and rounded once to
+// f16.  Rotations use angle addition: one table of (cos, sin)(r theta) for
+// r < 64 per CTA and a per-tile base angle, so no angle grows with the
+// position.  Each warp keeps its 16-row tile's q fragments (rotated, scaled,
+// rounded once to f16: 11 significant bits, so the rounding of rotated q stays
+// small against the bf16 output), S = q K^T (f16 x f16) and O += P V (bf16 x
+// bf16) on mma.sync m16n8k16 with fp32 accumulation, and a running max / sum
+// softmax across key tiles.  A value past the f16 range makes its rows' sums
+// non-finite, which the status word reports.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
 #include <math.h>
@@ -32,9 +35,10 @@
 namespace gattn {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kKT = 64;        // keys per streamed tile
-constexpr int kRowsMax = 64;   // rows per CTA (4 warps x 16)
+constexpr int kRowsMax = 128;  // rows per CTA (8 warps x 16)
+constexpr int kRT = kRowsMax > kKT ? kRowsMax : kKT;  // rows of the (cos, sin)(r theta) table
 constexpr int kMaxSmem = 227 * 1024;
 
 struct StreamParams {
@@ -68,7 +72,9 @@ Layout plan(const Problem& pb) {
   L.ring_buf = 2u * np * kKT * 128;  // K tile then V tile
   off += 2 * L.ring_buf;
   L.off_rt = off;
-  off += (uint32_t)kKT * (pb.d / 2) * 8;  // (cos, sin)(r theta_j), r < 64
+  // (cos, sin)(r theta_j) for r < kRT: a key's offset in its tile (< kKT) and a
+  // token's offset in its group (< Tg <= kRowsMax)
+  off += (uint32_t)kRT * (pb.d / 2) * 8;
   L.off_bq = off;
   off += (uint32_t)(pb.d / 2) * 8;
   L.off_bk = off;
@@ -81,13 +87,33 @@ Layout plan(const Problem& pb) {
   return L;
 }
 
+// fp32 pair -> f16 pair, round to nearest even (|x| >= 65520 gives inf)
+__device__ __forceinline__ uint32_t f16pair(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// bf16 pair -> f16 pair (exact for magnitudes in [2^-17, 65504])
+__device__ __forceinline__ uint32_t bf16x2_to_f16pair(uint32_t v) {
+  return f16pair(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+// D(16x8) += A(16x16, f16, row) * B(16x8, f16, col)
+__device__ __forceinline__ void mma_16816_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // (cos, sin) of (base + r) theta from cos/sin of base theta and of r theta.
 __device__ __forceinline__ float2 add_angle(float2 b, float2 r) {
   return make_float2(b.x * r.x - b.y * r.y, b.y * r.x + b.x * r.y);
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     prefill_stream_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_o,
                           const __grid_constant__ StreamParams prm) {
@@ -101,7 +127,7 @@ __global__ void __launch_bounds__(kThreads)
                                              ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sRing = sQ + prm.off_ring;
-  const float2* rt = reinterpret_cast<const float2*>(smem + prm.off_rt);  // [64][HALF]
+  const float2* rt = reinterpret_cast<const float2*>(smem + prm.off_rt);  // [kRT][HALF]
   float2* bq = reinterpret_cast<float2*>(smem + prm.off_bq);
   float2* bk = reinterpret_cast<float2*>(smem + prm.off_bk);            // [2][HALF]
   int32_t* ids = reinterpret_cast<int32_t*>(smem + prm.off_ids);
@@ -137,7 +163,7 @@ __global__ void __launch_bounds__(kThreads)
     bad |= !pool_block_ok(prm.pv, blk);
     ids[b] = blk;
   }
-  for (int idx = tid; idx < kKT * HALF; idx += kThreads) {
+  for (int idx = tid; idx < kRT * HALF; idx += kThreads) {
     const int r = idx / HALF, j = idx - r * HALF;
     float s, c;
     sincosf((float)r * prm.inv_freq[j], &s, &c);
@@ -188,8 +214,8 @@ __global__ void __launch_bounds__(kThreads)
             const float2 c0 = add_angle(base[j], rt[rr * HALF + j]);
             const float2 c1 = add_angle(base[j + 1], rt[rr * HALF + j + 1]);
             const float2 x = bf16x2_to_float2(lw[e]), y = bf16x2_to_float2(hw[e]);
-            ol[e] = float2_to_bf16x2(x.x * c0.x - y.x * c0.y, x.y * c1.x - y.y * c1.y);
-            oh[e] = float2_to_bf16x2(y.x * c0.x + x.x * c0.y, y.y * c1.x + x.y * c1.y);
+            ol[e] = f16pair(x.x * c0.x - y.x * c0.y, x.y * c1.x - y.y * c1.y);
+            oh[e] = f16pair(y.x * c0.x + x.x * c0.y, y.y * c1.x + x.y * c1.y);
           }
           sts16(kb + ko, make_uint4(ol[0], ol[1], ol[2], ol[3]));
           const int ch = c + CPR / 2;
@@ -198,6 +224,24 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     cp_async_commit();
+  };
+
+  // the cached keys of tile kt (landed, copied by this same thread): bf16 -> f16
+  // in place; returns whether the tile had any (then a barrier must follow)
+  auto convert_cached = [&](int kt) -> bool {
+    const int k0 = kt * kKT;
+    if (k0 >= C) return false;
+    const uint32_t kb = sRing + (kt & 1) * prm.ring_buf;
+    for (int idx = tid; idx < kKT * CPR; idx += kThreads) {
+      const int r = idx / CPR, c = idx - r * CPR;
+      if (k0 + r < C && k0 + r < kmax) {
+        const uint32_t a = kb + (c >> 3) * kv_panel + swz128(r, c & 7);
+        const uint4 v = lds16(a);
+        sts16(a, make_uint4(bf16x2_to_f16pair(v.x), bf16x2_to_f16pair(v.y), bf16x2_to_f16pair(v.z),
+                            bf16x2_to_f16pair(v.w)));
+      }
+    }
+    return true;
   };
 
   bool timed_out = !mbar_wait(bar, 0);
@@ -211,11 +255,12 @@ __global__ void __launch_bounds__(kThreads)
   if (!bad) {
     stage(0);
     cp_async_wait_all();
+    if (convert_cached(0)) __syncthreads();
     __syncthreads();
-    // ---- this warp's 16-row tile: q fragments rotated, scaled, split hi + lo
+    // ---- this warp's 16-row tile: q fragments rotated, scaled, rounded to f16
     const int r0 = warp * 16;
     const bool active = r0 < rows;
-    uint32_t qh[D / 16][4], ql[D / 16][4];
+    uint32_t qh[D / 16][4];
     const int ra = r0 + (lane >> 2), rb = ra + 8;
     const int tta = min(ra / G, Tc - 1), ttb = min(rb / G, Tc - 1);
     if (active) {
@@ -235,10 +280,8 @@ __global__ void __launch_bounds__(kThreads)
           const float2 c1 = add_angle(bq[j + 1], rt[tt * HALF + j + 1]);
           const float2 x = bf16x2_to_float2(qh[ks][r]), y = bf16x2_to_float2(qh[ks + D / 32][r]);
           const float sc = prm.scale_log2;
-          f2_split_bf16(f2_make((x.x * c0.x - y.x * c0.y) * sc, (x.y * c1.x - y.y * c1.y) * sc),
-                        qh[ks][r], ql[ks][r]);
-          f2_split_bf16(f2_make((y.x * c0.x + x.x * c0.y) * sc, (y.y * c1.x + x.y * c1.y) * sc),
-                        qh[ks + D / 32][r], ql[ks + D / 32][r]);
+          qh[ks][r] = f16pair((x.x * c0.x - y.x * c0.y) * sc, (x.y * c1.x - y.y * c1.y) * sc);
+          qh[ks + D / 32][r] = f16pair((y.x * c0.x + x.x * c0.y) * sc, (y.y * c1.x + x.y * c1.y) * sc);
         }
       }
     }
@@ -271,10 +314,8 @@ __global__ void __launch_bounds__(kThreads)
             uint32_t b[4];
             const int c8 = k2 * 4 + (lane >> 3);
             ldsm_x4(kb + (c8 >> 3) * kv_panel + swz128(krow, c8 & 7), b);
-            mma_16816(s[n], qh[2 * k2], b[0], b[1]);
-            mma_16816(s[n], qh[2 * k2 + 1], b[2], b[3]);
-            mma_16816(s[n], ql[2 * k2], b[0], b[1]);
-            mma_16816(s[n], ql[2 * k2 + 1], b[2], b[3]);
+            mma_16816_f16(s[n], qh[2 * k2], b[0], b[1]);
+            mma_16816_f16(s[n], qh[2 * k2 + 1], b[2], b[3]);
           }
         }
         float mx_a = kNegInf, mx_b = kNegInf;
@@ -336,6 +377,7 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
       cp_async_wait_all();
+      if (kt + 1 < nkt && convert_cached(kt + 1)) __syncthreads();
       __syncthreads();  // tile kt+1 landed; every warp is done with tile kt's buffer
     }
     if (active) {
@@ -343,6 +385,9 @@ __global__ void __launch_bounds__(kThreads)
       l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
       l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
       l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+      // a non-finite sum: a query or key value past the f16 range
+      if ((ra < rows && !(l_a <= 3.0e38f)) || (rb < rows && !(l_b <= 3.0e38f)))
+        report(prm.status, GIST_ATTN_STATUS_RANGE);
       const float inv_a = 1.f / l_a, inv_b = 1.f / l_b;
 #pragma unroll
       for (int dn = 0; dn < D / 8; ++dn) {
