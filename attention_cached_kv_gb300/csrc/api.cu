@@ -130,6 +130,7 @@ extern "C" int gist_attn_fwd(const void* q, const void* k_new, const void* v_new
     if (gattn::decode_fits(pb)) return gattn::launch_decode(pb, stream);
   }
   if (gattn::prefill_tc_fits(pb)) return gattn::launch_prefill_tc(pb, stream);
+  if (gattn::prefill_long_fits(pb)) return gattn::launch_prefill_long(pb, stream);
   if (gattn::prefill_fits(pb)) return gattn::launch_prefill(pb, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }

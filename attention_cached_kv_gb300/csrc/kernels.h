@@ -41,6 +41,7 @@ EncodeTiledFn encode_tiled_fn();
 // Each returns GIST_ATTN_OK or a negative GIST_ATTN_ERR_* code.
 int launch_prefill(const Problem& pb, cudaStream_t stream);
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream);
+int launch_prefill_long(const Problem& pb, cudaStream_t stream);
 int launch_decode(const Problem& pb, cudaStream_t stream);
 int launch_decode_long(const Problem& pb, cudaStream_t stream);
 int launch_decode_long_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
@@ -59,6 +60,7 @@ int launch_out_proj(const Problem& pb, const void* attn, const void* w, int d_mo
 // Whether the prefill kernel can hold this problem's tiles in shared memory.
 bool prefill_fits(const Problem& pb);
 bool prefill_tc_fits(const Problem& pb);
+bool prefill_long_fits(const Problem& pb);
 bool decode_fits(const Problem& pb);
 bool decode_long_fits(const Problem& pb);
 bool decode_short_fits(const Problem& pb);

@@ -1,0 +1,527 @@
+// prefill_long.cu -- causal attention over whole pre-rotated sequences (no
+// cached segment, l up to thousands of tokens) on the 5th-generation tensor
+// core: the offline gist compression pass in the fused pipeline.
+//
+// [Gist page, "论文做了什么" and "在线的一次 attention"]: the item is forwarded
+// once, offline: [prompt; gist] through every layer, plain causal attention
+// over the whole sequence (the gist mask only hides the prompt from tokens
+// after the gist, and there are none in this pass); each layer's K/V at the
+// gist positions is then stored (gist_kv_store).  Here q and k_new arrive
+// rotated by the QKV projection's epilogue (GIST_ATTN_FLAG_PREROTATED), so the
+// kernel streams them as stored.
+//
+// A work item is a 128-row tile of one (pair, KV head): floor(128 / G) whole
+// tokens x G heads, token-major (the memory order of q/out).  Its keys are the
+// tokens before its last one, in blocks of 128.  Two passes over the blocks
+// keep the softmax exact without rescaling O: pass 1 takes each row's maximum
+// (S = q K^T recomputed in pass 2 is cheap on the tensor core), pass 2 forms
+// P = exp2((S - m) scale) in TMEM as bf16, sums it, and accumulates O += P V.
+// Persistent CTAs, two per SM, warp-specialised:
+//   * warp 8: streams the K and V blocks by TMA (two slots each) and issues
+//     tcgen05.mma (S into TMEM, then O from P in TMEM);
+//   * warp 9: TMA loads of the q tiles (two stages) and TMA stores of O;
+//   * warps 0-7: two threads per row (TMEM lane = row), the softmax passes
+//     (block maxima by tcgen05.ld.red.max below the causal diagonal, a 0/-inf
+//     bias row at it) and the normalisation of O into the stage.
+//
+// Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace gattn {
+namespace {
+
+constexpr int kCompute = 256;            // 8 compute warps
+constexpr int kThreads = kCompute + 64;  // + the MMA/K-V warp and the Q/O warp
+constexpr int kKB = 128;                 // keys per block
+constexpr uint32_t kTile = 128 * 128;    // bytes of a 128-row x 64-column bf16 tile
+constexpr int kMaxSmem = 227 * 1024;
+
+struct LongParams {
+  int32_t* status;
+  int l, Hkv, G, Tm, n_mt, num_tiles;
+  float scale_log2;
+};
+
+// shared memory: q/O stages [2], K slots [2], V slots [2], then the small parts
+constexpr uint32_t kOffQ = 0, kOffK = 2 * kTile, kOffV = 4 * kTile, kOffRed = 6 * kTile;
+constexpr uint32_t kOffBias = kOffRed + 2 * 2 * 128 * 4;
+constexpr uint32_t kOffBar = kOffBias + 17 * 16 * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+// TMEM: S [0, 128) fp32, P [128, 192) bf16 pairs, O [192, 256)
+constexpr uint32_t kPCol = 128, kOCol = 192, kTmemCols = 256;
+
+struct LBars {
+  uint64_t qfull[2], kfull[2], kfree[2], vfull[2], vfree[2];
+  uint64_t s_done, s_free, p_done, o_done, o_stored[2];
+  uint32_t tmem_slot;
+};
+
+// 4-D tiled load into shared memory, completing bytes on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// TMEM load of 16 columns of this thread's lane that also returns their maximum.
+__device__ __forceinline__ float ld16_max(uint32_t taddr) {
+  uint32_t r[16];
+  float m;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, %16, [%17];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=f"(m)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+f"(m)::"memory");
+  return m;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_long_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_o,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ LongParams prm) {
+  constexpr float kNegInf = -INFINITY;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  LBars* bars = reinterpret_cast<LBars*>(smem + kOffBar);
+  float* red_max = reinterpret_cast<float*>(smem + kOffRed);  // [2][128]
+  float* red_sum = red_max + 256;                              // [2][128]
+  float* bias = reinterpret_cast<float*>(smem + kOffBias);     // [17][16]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = prm.G, l = prm.l, Tm = prm.Tm, n_mt = prm.n_mt;
+  const int my_tiles = (int)blockIdx.x < prm.num_tiles
+                           ? (prm.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
+                           : 0;
+  // tile i of this CTA: (unit, row tile) and its number of key blocks
+  auto tile_of = [&](int i, int& p, int& g, int& mt) {
+    const int t = (int)blockIdx.x + i * (int)gridDim.x;
+    mt = t % n_mt;
+    const int u = t / n_mt;
+    g = u % prm.Hkv;
+    p = u / prm.Hkv;
+  };
+  auto blocks_of = [&](int mt) { return (min(l, (mt + 1) * Tm) + kKB - 1) / kKB; };
+
+  if (warp == 8) {
+    tc::tmem_alloc(smem_u32(&bars->tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->qfull[s], 1);
+      mbar_init(&bars->kfull[s], 1);
+      mbar_init(&bars->kfree[s], 1);
+      mbar_init(&bars->vfull[s], 1);
+      mbar_init(&bars->vfree[s], 1);
+      mbar_init(&bars->o_stored[s], kCompute);
+    }
+    mbar_init(&bars->s_done, 1);
+    mbar_init(&bars->s_free, kCompute);
+    mbar_init(&bars->p_done, kCompute);
+    mbar_init(&bars->o_done, 1);
+    fence_mbar_init();
+  }
+  for (int idx = tid; idx < 17 * 16; idx += kThreads) bias[idx] = (idx & 15) < (idx >> 4) ? 0.f : kNegInf;
+  {  // rows of each q stage that no TMA box reaches stay zero
+    const int qpad = 128 - Tm * G;
+    for (int idx = tid; idx < 2 * qpad * 8; idx += kThreads) {
+      const int c = idx & 7, rr = (idx >> 3) % qpad, s = (idx >> 3) / qpad;
+      sts16(sbase + kOffQ + s * kTile + swz128(Tm * G + rr, c), make_uint4(0, 0, 0, 0));
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == 8) {
+    // ============================================ K/V blocks by TMA, tcgen05.mma
+    // The K loads follow the S products one to one: for each tile, pass 1 then
+    // pass 2, blocks 0 .. nb-1; the V loads follow the P V products (pass 2).
+    // Each load is issued one step ahead of its product.
+    bool failed = false;
+    int kc = 0, vc = 0;  // loads issued
+    // cursors of the next K and V loads: (tile, pass, block) / (tile, block)
+    int kl_i = 0, kl_pass = 0, kl_b = 0, vl_i = 0, vl_b = 0;
+    auto load_next_k = [&]() {
+      if (kl_i >= my_tiles) return;
+      int p, g, mt;
+      tile_of(kl_i, p, g, mt);
+      const int s = kc & 1;
+      if (!mbar_wait(&bars->kfree[s], ((uint32_t)(kc >> 1) & 1u) ^ 1u)) failed = true;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->kfull[s], kTile);
+        tma_load_4d(sbase + kOffK + s * kTile, &tm_k, &bars->kfull[s], 0, g, kl_b * kKB, p);
+      }
+      ++kc;
+      if (++kl_b == blocks_of(mt)) {
+        kl_b = 0;
+        if (++kl_pass == 2) {
+          kl_pass = 0;
+          ++kl_i;
+        }
+      }
+    };
+    auto load_next_v = [&]() {
+      if (vl_i >= my_tiles) return;
+      int p, g, mt;
+      tile_of(vl_i, p, g, mt);
+      const int s = vc & 1;
+      if (!mbar_wait(&bars->vfree[s], ((uint32_t)(vc >> 1) & 1u) ^ 1u)) failed = true;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->vfull[s], kTile);
+        tma_load_4d(sbase + kOffV + s * kTile, &tm_v, &bars->vfull[s], 0, g, vl_b * kKB, p);
+      }
+      ++vc;
+      if (++vl_b == blocks_of(mt)) {
+        vl_b = 0;
+        ++vl_i;
+      }
+    };
+    if (lane == 0) {
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+    }
+    load_next_k();
+    load_next_v();
+    int sx = 0, kx = 0, vx = 0, px = 0;  // products issued: S, K consumed, V consumed, P V
+    for (int i = 0; i < my_tiles && !failed; ++i) {
+      int p, g, mt;
+      tile_of(i, p, g, mt);
+      const int nb = blocks_of(mt);
+      const int kend = min(l, (mt + 1) * Tm);  // keys of the tile's last token
+      const uint32_t stage = sbase + kOffQ + (i & 1) * kTile;
+      if (__any_sync(0xffffffffu, !mbar_wait(&bars->qfull[i & 1], (uint32_t)(i >> 1) & 1u))) {
+        failed = true;
+        break;
+      }
+      for (int pass = 0; pass < 2 && !failed; ++pass) {
+        for (int b = 0; b < nb; ++b) {
+          const int N = (min(kKB, kend - b * kKB) + 15) & ~15;
+          load_next_k();  // one step ahead
+          const int ks = kx & 1;
+          // S may be overwritten once the compute warps have read the last one
+          if (__any_sync(0xffffffffu, !mbar_wait(&bars->kfull[ks], (uint32_t)(kx >> 1) & 1u) ||
+                                          !mbar_wait(&bars->s_free, ((uint32_t)sx & 1u) ^ 1u))) {
+            failed = true;
+            break;
+          }
+          tc::fence_after_sync();
+          if (lane == 0) {
+            const uint32_t idesc = tc::idesc_bf16_f32(128, N, 0);
+            const uint32_t kb = sbase + kOffK + ks * kTile;
+#pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16) {
+              const uint64_t a = tc::smem_desc_sw128(stage + k16 * 32, 16, 1024);
+              const uint64_t bd = tc::smem_desc_sw128(kb + k16 * 32, 16, 1024);
+              tc::mma_ss(tmem, a, bd, idesc, k16 > 0);
+            }
+            tc::commit(smem_u32(&bars->s_done));
+            tc::commit(smem_u32(&bars->kfree[ks]));
+          }
+          __syncwarp();
+          ++kx;
+          ++sx;
+          if (pass == 1) {
+            // O (+)= P V once P is in TMEM and V has landed
+            load_next_v();
+            const int vs = vx & 1;
+            if (__any_sync(0xffffffffu, !mbar_wait(&bars->vfull[vs], (uint32_t)(vx >> 1) & 1u) ||
+                                            !mbar_wait(&bars->p_done, (uint32_t)px & 1u))) {
+              failed = true;
+              break;
+            }
+            tc::fence_after_sync();
+            if (lane == 0) {
+              const uint32_t idesc = tc::idesc_bf16_f32(128, 64, 1);
+              const uint32_t vb = sbase + kOffV + vs * kTile;
+              for (int k16 = 0; k16 < N / 16; ++k16) {
+                const uint64_t bd = tc::smem_desc_sw128(vb + k16 * 2048, kTile, 1024);
+                tc::mma_ts(tmem + kOCol, tmem + kPCol + k16 * 8, bd, idesc, (b > 0 || k16 > 0) ? 1u : 0u);
+              }
+              tc::commit(smem_u32(&bars->vfree[vs]));
+              if (b == nb - 1) tc::commit(smem_u32(&bars->o_done));
+            }
+            __syncwarp();
+            ++vx;
+            ++px;
+          }
+        }
+      }
+    }
+    if (lane == 0 && failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    __syncwarp();
+  } else if (warp == 9) {
+    // ============================================ q tiles in, O tiles out
+    bool failed = false;
+    auto load_q = [&](int i) {
+      if (i >= my_tiles) return;
+      int p, g, mt;
+      tile_of(i, p, g, mt);
+      mbar_arrive_expect_tx(&bars->qfull[i & 1], (uint32_t)Tm * G * 128);
+      tma_load_5d(sbase + kOffQ + (i & 1) * kTile, &tm_q, &bars->qfull[i & 1], 0, 0, g * G, mt * Tm, p);
+    };
+    if (lane == 0 && my_tiles > 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_o);
+      load_q(0);
+      load_q(1);
+    }
+    for (int i = 0; i < my_tiles; ++i) {
+      if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored[i & 1], (uint32_t)(i >> 1) & 1u))) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        int p, g, mt;
+        tile_of(i, p, g, mt);
+        tma_store_5d(&tm_o, sbase + kOffQ + (i & 1) * kTile, 0, 0, g * G, mt * Tm, p);
+        bulk_commit();
+        bulk_wait_read_all();
+        load_q(i + 2);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      bulk_wait_all();
+      if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ============================================ softmax passes, normalisation
+    const int h = warp >> 2;               // which half of the row's columns
+    const int r = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t pair_bar = 2 + (warp & 3);
+    const int row_tok = r / G;
+    bool failed = false;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      if (!failed && !mbar_wait(bar, parity)) failed = true;
+    };
+    const float sc = prm.scale_log2;
+    int sx = 0, px = 0;
+    for (int i = 0; i < my_tiles; ++i) {
+      int p, g, mt;
+      tile_of(i, p, g, mt);
+      const int nb = blocks_of(mt);
+      const int t0 = mt * Tm, toks = min(Tm, l - t0);
+      const bool valid = row_tok < toks;
+      const bool wlive = (warp & 3) * 32 < toks * G;  // warp-uniform, same for the row's partner
+      const int kend = t0 + toks;
+      const int lim = t0 + min(row_tok, toks - 1) + 1;  // keys row r sees
+      const int lim_all = t0 + 1;                          // keys every row of the tile sees
+      // chunk c (16 keys) of block b: below the diagonal for every row, or at it
+      auto bias_row = [&](int key0) {
+        return reinterpret_cast<const float4*>(bias + min(max(lim - key0, 0), 16) * 16);
+      };
+      // ---- pass 1: the row maximum over all blocks
+      float mx = kNegInf;
+      for (int b = 0; b < nb; ++b) {
+        const int N = (min(kKB, kend - b * kKB) + 15) & ~15;
+        wait(&bars->s_done, (uint32_t)sx & 1u);
+        tc::fence_after_sync();
+        if (wlive) {
+          for (int c = h; c * 16 < N; c += 2) {
+            const int key0 = b * kKB + c * 16;
+            if (key0 + 16 <= lim_all) {
+              mx = fmaxf(mx, ld16_max(tmem + lane_base + c * 16));
+            } else {
+              uint32_t v[16];
+              tc::ld16(tmem + lane_base + c * 16, v);
+              tc::wait_ld();
+              const float4* bt = bias_row(key0);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 bq = bt[q4];
+                mx = max3f(mx, __uint_as_float(v[4 * q4]) + bq.x, __uint_as_float(v[4 * q4 + 1]) + bq.y);
+                mx = max3f(mx, __uint_as_float(v[4 * q4 + 2]) + bq.z, __uint_as_float(v[4 * q4 + 3]) + bq.w);
+              }
+            }
+          }
+        }
+        tc::fence_before_sync();
+        mbar_arrive(&bars->s_free);
+        ++sx;
+      }
+      float m = 0.f;
+      if (wlive) {
+        red_max[h * 128 + r] = mx;
+        named_bar_sync(pair_bar, 64);
+        m = fmaxf(red_max[r], red_max[128 + r]);
+      }
+      // ---- pass 2: P = exp2((S - m) scale) into TMEM, row sums, O += P V
+      const uint64_t sc2 = f2_make(sc, sc), nmc2 = f2_make(-m * sc, -m * sc);
+      const uint64_t one2 = f2_make(1.f, 1.f);
+      uint64_t acc[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+      for (int b = 0; b < nb; ++b) {
+        const int N = (min(kKB, kend - b * kKB) + 15) & ~15;
+        // S(b) done also means the P V of block b - 1 is done: P may be rewritten
+        wait(&bars->s_done, (uint32_t)sx & 1u);
+        tc::fence_after_sync();
+        if (wlive) {
+          for (int c = h; c * 16 < N; c += 2) {
+            const int key0 = b * kKB + c * 16;
+            uint32_t v[16];
+            tc::ld16(tmem + lane_base + c * 16, v);
+            tc::wait_ld();
+            const float4* bt = key0 + 16 <= lim_all ? nullptr : bias_row(key0);
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              uint64_t off = nmc2;
+              if (bt) {
+                const float4 bq = bt[e >> 1];
+                off = f2_add(nmc2, (e & 1) ? f2_make(bq.z, bq.w) : f2_make(bq.x, bq.y));
+              }
+              float a, bb;
+              f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, off),
+                       a, bb);
+              const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
+              acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
+              pk[e] = f2_to_bf16x2(pp);
+            }
+            tc::st8(tmem + lane_base + kPCol + c * 8, pk);
+          }
+        }
+        tc::wait_st();
+        tc::fence_before_sync();
+        mbar_arrive(&bars->p_done);
+        mbar_arrive(&bars->s_free);
+        ++sx;
+        ++px;
+      }
+      // ---- O of row r, this half's 32 columns, normalised into the stage
+      wait(&bars->o_done, (uint32_t)i & 1u);
+      tc::fence_after_sync();
+      if (wlive) {
+        float a0, a1, b0, b1;
+        f2_split(acc[0], a0, a1);
+        f2_split(acc[1], b0, b1);
+        red_sum[h * 128 + r] = (a0 + a1) + (b0 + b1);
+        named_bar_sync(pair_bar, 64);
+        const float sum = red_sum[r] + red_sum[128 + r];
+        const float inv = rcp_approx(sum);
+        const uint32_t stage = sbase + kOffQ + (i & 1) * kTile;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ov[16];
+          tc::ld16(tmem + lane_base + kOCol + (h * 2 + c) * 16, ov);
+          tc::wait_ld();
+          if (valid) {
+            const uint64_t inv2 = f2_make(inv, inv);
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = f2_to_bf16x2(f2_mul(f2_make(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), inv2));
+            const int J = (h * 2 + c) * 2;
+            sts16(stage + swz128(r, J), make_uint4(w[0], w[1], w[2], w[3]));
+            sts16(stage + swz128(r, J + 1), make_uint4(w[4], w[5], w[6], w[7]));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(&bars->o_stored[i & 1]);
+    }
+    if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 8) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// q / out: [P][l][Hq][64] as {64, 1, Hq, l, P}, boxes of G heads x Tm tokens.
+int encode_qo(CUtensorMap* m, const void* base, const Problem& pb, int Tm) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return GIST_ATTN_ERR_LAUNCH;
+  const cuuint64_t dims[5] = {64, 1, (cuuint64_t)pb.Hq, (cuuint64_t)pb.l, (cuuint64_t)pb.P};
+  const cuuint64_t strides[4] = {128, (cuuint64_t)pb.d * 2, (cuuint64_t)pb.Hq * pb.d * 2,
+                                 (cuuint64_t)pb.l * pb.Hq * pb.d * 2};
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)pb.G, (cuuint32_t)Tm, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+// k_new / v_new: [P][l][Hkv][64] as {64, Hkv, l, P}, boxes of 128 tokens of one head.
+int encode_kv(CUtensorMap* m, const void* base, const Problem& pb) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return GIST_ATTN_ERR_LAUNCH;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)pb.Hkv, (cuuint64_t)pb.l, (cuuint64_t)pb.P};
+  const cuuint64_t strides[3] = {(cuuint64_t)pb.d * 2, (cuuint64_t)pb.Hkv * pb.d * 2,
+                                 (cuuint64_t)pb.l * pb.Hkv * pb.d * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kKB, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+// Pre-rotated inputs, no cached segment, d = 64, groups of at most 128 heads,
+// sequences longer than the single-pass kernel's 128 keys.
+bool prefill_long_fits(const Problem& pb) {
+  return (pb.flags & GIST_ATTN_FLAG_PREROTATED) && pb.C == 0 && pb.d == 64 && pb.l > 128 &&
+         pb.G <= 128 && (int64_t)pb.P * pb.Hkv * ((pb.l + 128 / pb.G - 1) / (128 / pb.G)) < 0x7fffffff &&
+         kSmemBytes <= (uint32_t)kMaxSmem;
+}
+
+int launch_prefill_long(const Problem& pb, cudaStream_t stream) {
+  LongParams prm{};
+  prm.status = pb.status;
+  prm.l = pb.l;
+  prm.Hkv = pb.Hkv;
+  prm.G = pb.G;
+  prm.Tm = 128 / pb.G;
+  prm.n_mt = (pb.l + prm.Tm - 1) / prm.Tm;
+  prm.num_tiles = (int)((int64_t)pb.P * pb.Hkv * prm.n_mt);
+  prm.scale_log2 = pb.scale_log2;
+  alignas(64) CUtensorMap tm_q, tm_o, tm_k, tm_v;
+  int rc = encode_qo(&tm_q, pb.q, pb, prm.Tm);
+  if (rc == GIST_ATTN_OK) rc = encode_qo(&tm_o, pb.out, pb, prm.Tm);
+  if (rc == GIST_ATTN_OK) rc = encode_kv(&tm_k, pb.k_new, pb);
+  if (rc == GIST_ATTN_OK) rc = encode_kv(&tm_v, pb.v_new, pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (cudaFuncSetAttribute(prefill_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes) != cudaSuccess)
+    return GIST_ATTN_ERR_LAUNCH;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GIST_ATTN_ERR_LAUNCH;
+  const int grid = prm.num_tiles < 2 * sms ? prm.num_tiles : 2 * sms;
+  prefill_long_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_o, tm_k, tm_v, prm);
+  return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
+}
+
+}  // namespace gattn
