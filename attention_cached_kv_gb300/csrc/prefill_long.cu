@@ -12,17 +12,20 @@
 //
 // A work item is a 128-row tile of one (pair, KV head): floor(128 / G) whole
 // tokens x G heads, token-major (the memory order of q/out).  Its keys are the
-// tokens before its last one, in blocks of 128.  Two passes over the blocks
-// keep the softmax exact without rescaling O: pass 1 takes each row's maximum
-// (S = q K^T recomputed in pass 2 is cheap on the tensor core), pass 2 forms
-// P = exp2((S - m) scale) in TMEM as bf16, sums it, and accumulates O += P V.
+// tokens before its last one, in blocks of 128, one pass: per block S = q K^T
+// into TMEM, the block's row maxima, P = exp2((S - m) scale) as bf16 into TMEM
+// with m the running maximum, O += P V.  m moves only when a block's maximum
+// exceeds it by more than 8 (log2 units); then the row's O and sum are scaled
+// down first.  P stays below 2^8, the result is exact softmax either way, and O
+// is touched in between only for those rare rows: S(b) done means the tensor
+// core has finished P V of block b - 1, and P V of block b waits for P.
 // Persistent CTAs, two per SM, warp-specialised:
 //   * warp 8: streams the K and V blocks by TMA (two slots each) and issues
 //     tcgen05.mma (S into TMEM, then O from P in TMEM);
 //   * warp 9: TMA loads of the q tiles (two stages) and TMA stores of O;
-//   * warps 0-7: two threads per row (TMEM lane = row), the softmax passes
-//     (block maxima by tcgen05.ld.red.max below the causal diagonal, a 0/-inf
-//     bias row at it) and the normalisation of O into the stage.
+//   * warps 0-7: two threads per row (TMEM lane = row), the softmax (block
+//     maxima by tcgen05.ld.red.max below the causal diagonal, a 0/-inf bias row
+//     at it) and the normalisation of O into the stage.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
 #include <math.h>
@@ -48,7 +51,7 @@ struct LongParams {
 
 // shared memory: q/O stages [2], K slots [2], V slots [2], then the small parts
 constexpr uint32_t kOffQ = 0, kOffK = 2 * kTile, kOffV = 4 * kTile, kOffRed = 6 * kTile;
-constexpr uint32_t kOffBias = kOffRed + 2 * 2 * 128 * 4;
+constexpr uint32_t kOffBias = kOffRed + 3 * 2 * 128 * 4;  // block maxima [2 blocks][2], sums [2]
 constexpr uint32_t kOffBar = kOffBias + 17 * 16 * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 // TMEM: S [0, 128) fp32, P [128, 192) bf16 pairs, O [192, 256)
@@ -85,6 +88,16 @@ __device__ __forceinline__ float ld16_max(uint32_t taddr) {
   return m;
 }
 
+// 16 columns of this thread's lane into TMEM.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -103,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   LBars* bars = reinterpret_cast<LBars*>(smem + kOffBar);
-  float* red_max = reinterpret_cast<float*>(smem + kOffRed);  // [2][128]
-  float* red_sum = red_max + 256;                              // [2][128]
+  float* red_max = reinterpret_cast<float*>(smem + kOffRed);  // [2 blocks][2][128]
+  float* red_sum = red_max + 512;                              // [2][128]
   float* bias = reinterpret_cast<float*>(smem + kOffBias);     // [17][16]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -156,13 +169,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == 8) {
     // ============================================ K/V blocks by TMA, tcgen05.mma
-    // The K loads follow the S products one to one: for each tile, pass 1 then
-    // pass 2, blocks 0 .. nb-1; the V loads follow the P V products (pass 2).
-    // Each load is issued one step ahead of its product.
+    // The K and V loads follow the products one to one: for each tile, blocks
+    // 0 .. nb-1.  Each load is issued one step ahead of its product.
     bool failed = false;
     int kc = 0, vc = 0;  // loads issued
-    // cursors of the next K and V loads: (tile, pass, block) / (tile, block)
-    int kl_i = 0, kl_pass = 0, kl_b = 0, vl_i = 0, vl_b = 0;
+    // cursors of the next K and V loads: (tile, block)
+    int kl_i = 0, kl_b = 0, vl_i = 0, vl_b = 0;
     auto load_next_k = [&]() {
       if (kl_i >= my_tiles) return;
       int p, g, mt;
@@ -176,10 +188,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       ++kc;
       if (++kl_b == blocks_of(mt)) {
         kl_b = 0;
-        if (++kl_pass == 2) {
-          kl_pass = 0;
-          ++kl_i;
-        }
+        ++kl_i;
       }
     };
     auto load_next_v = [&]() {
@@ -215,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         failed = true;
         break;
       }
-      for (int pass = 0; pass < 2 && !failed; ++pass) {
+      {
         for (int b = 0; b < nb; ++b) {
           const int N = (min(kKB, kend - b * kKB) + 15) & ~15;
           load_next_k();  // one step ahead
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           __syncwarp();
           ++kx;
           ++sx;
-          if (pass == 1) {
+          {
             // O (+)= P V once P is in TMEM and V has landed
             load_next_v();
             const int vs = vx & 1;
@@ -334,13 +343,19 @@ __global__ void __launch_bounds__(kThreads, 2)
       auto bias_row = [&](int key0) {
         return reinterpret_cast<const float4*>(bias + min(max(lim - key0, 0), 16) * 16);
       };
-      // ---- pass 1: the row maximum over all blocks
-      float mx = kNegInf;
+      constexpr float kSlack = 8.f;  // log2 units the running maximum may trail a block's
+      const uint64_t sc2 = f2_make(sc, sc);
+      const uint64_t one2 = f2_make(1.f, 1.f);
+      uint64_t acc[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+      float m = kNegInf;  // running maximum of row r (the same in both threads)
       for (int b = 0; b < nb; ++b) {
         const int N = (min(kKB, kend - b * kKB) + 15) & ~15;
+        // S(b) done also means the P V of block b - 1 is done: P and O are quiet
         wait(&bars->s_done, (uint32_t)sx & 1u);
         tc::fence_after_sync();
         if (wlive) {
+          // the block's maximum over this half's chunks, then over the row
+          float mx = kNegInf;
           for (int c = h; c * 16 < N; c += 2) {
             const int key0 = b * kKB + c * 16;
             if (key0 + 16 <= lim_all) {
@@ -358,27 +373,38 @@ __global__ void __launch_bounds__(kThreads, 2)
               }
             }
           }
-        }
-        tc::fence_before_sync();
-        mbar_arrive(&bars->s_free);
-        ++sx;
-      }
-      float m = 0.f;
-      if (wlive) {
-        red_max[h * 128 + r] = mx;
-        named_bar_sync(pair_bar, 64);
-        m = fmaxf(red_max[r], red_max[128 + r]);
-      }
-      // ---- pass 2: P = exp2((S - m) scale) into TMEM, row sums, O += P V
-      const uint64_t sc2 = f2_make(sc, sc), nmc2 = f2_make(-m * sc, -m * sc);
-      const uint64_t one2 = f2_make(1.f, 1.f);
-      uint64_t acc[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
-      for (int b = 0; b < nb; ++b) {
-        const int N = (min(kKB, kend - b * kKB) + 15) & ~15;
-        // S(b) done also means the P V of block b - 1 is done: P may be rewritten
-        wait(&bars->s_done, (uint32_t)sx & 1u);
-        tc::fence_after_sync();
-        if (wlive) {
+          float* slot = red_max + (b & 1) * 256;  // two slots: a partner may still read the last
+          slot[h * 128 + r] = mx;
+          named_bar_sync(pair_bar, 64);
+          const float mb = fmaxf(slot[r], slot[128 + r]);
+          // (S - m) scale is in log2 units; the first block always moves m
+          if ((mb - m) * sc > kSlack) {  // the first block, or a jump: move m, scale O and the sum down
+            if (m != kNegInf) {
+              const float f = ex2_approx((m - mb) * sc);
+              const uint64_t f2 = f2_make(f, f);
+              acc[0] = f2_mul(acc[0], f2);
+              acc[1] = f2_mul(acc[1], f2);
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                uint32_t ov[16];
+                const uint32_t oa = tmem + lane_base + kOCol + (h * 2 + c) * 16;
+                tc::ld16(oa, ov);
+                tc::wait_ld();
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  float x, y;
+                  f2_split(f2_mul(f2_make(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), f2), x, y);
+                  w[2 * e] = __float_as_uint(x);
+                  w[2 * e + 1] = __float_as_uint(y);
+                }
+                tmem_st16(oa, w);
+              }
+            }
+            m = mb;
+          }
+          // P = exp2((S - m) scale) into TMEM as bf16, summed
+          const uint64_t nmc2 = f2_make(-m * sc, -m * sc);
           for (int c = h; c * 16 < N; c += 2) {
             const int key0 = b * kKB + c * 16;
             uint32_t v[16];
