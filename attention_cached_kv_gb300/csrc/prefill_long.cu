@@ -49,6 +49,60 @@ struct LongParams {
   float scale_log2;
 };
 
+// A CTA's tiles are blockIdx.x, blockIdx.x + gridDim.x, ... of the row-major
+// (pair, KV head, row tile) order; the walk steps (mt, g, p) by carries, with
+// the division done once.
+struct TileWalk {
+  int dmt, dg, dp;  // gridDim.x split over (row tile, KV head, pair)
+  int mt, g, p;     // current tile
+  __device__ void init(const LongParams& prm) {
+    const int x = (int)blockIdx.x, du = (int)gridDim.x / prm.n_mt;
+    dmt = (int)gridDim.x % prm.n_mt;
+    dg = du % prm.Hkv;
+    dp = du / prm.Hkv;
+    mt = x % prm.n_mt;
+    const int u = x / prm.n_mt;
+    g = u % prm.Hkv;
+    p = u / prm.Hkv;
+  }
+  __device__ void next(const LongParams& prm) {
+    mt += dmt;
+    int c = 0;
+    if (mt >= prm.n_mt) {
+      mt -= prm.n_mt;
+      c = 1;
+    }
+    g += dg + c;  // < 2 Hkv
+    p += dp;
+    if (g >= prm.Hkv) {
+      g -= prm.Hkv;
+      ++p;
+    }
+  }
+};
+
+// A position in the stream of (tile, key block) steps of one CTA.
+struct StepWalk {
+  TileWalk t;
+  int i, b, nb;  // tile index, block, blocks of the tile
+  __device__ static int blocks(const LongParams& prm, int mt) {
+    return (min(prm.l, (mt + 1) * prm.Tm) + kKB - 1) / kKB;
+  }
+  __device__ void init(const LongParams& prm) {
+    t.init(prm);
+    i = b = 0;
+    nb = blocks(prm, t.mt);
+  }
+  __device__ void next(const LongParams& prm) {
+    if (++b == nb) {
+      b = 0;
+      ++i;
+      t.next(prm);
+      nb = blocks(prm, t.mt);
+    }
+  }
+};
+
 // shared memory: q/O stages [2], K slots [2], V slots [2], then the small parts
 constexpr uint32_t kOffQ = 0, kOffK = 2 * kTile, kOffV = 4 * kTile, kOffRed = 6 * kTile;
 constexpr uint32_t kOffBias = kOffRed + 3 * 2 * 128 * 4;  // block maxima [2 blocks][2], sums [2]
@@ -59,7 +113,7 @@ constexpr uint32_t kPCol = 128, kOCol = 192, kTmemCols = 256;
 
 struct LBars {
   uint64_t qfull[2], kfull[2], kfree[2], vfull[2], vfree[2];
-  uint64_t s_done, s_free, p_done, o_done, o_stored[2];
+  uint64_t s_done, p_done, o_done, o_stored[2];
   uint32_t tmem_slot;
 };
 
@@ -121,19 +175,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* bias = reinterpret_cast<float*>(smem + kOffBias);     // [17][16]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = prm.G, l = prm.l, Tm = prm.Tm, n_mt = prm.n_mt;
+  const int G = prm.G, l = prm.l, Tm = prm.Tm;
   const int my_tiles = (int)blockIdx.x < prm.num_tiles
                            ? (prm.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
                            : 0;
-  // tile i of this CTA: (unit, row tile) and its number of key blocks
-  auto tile_of = [&](int i, int& p, int& g, int& mt) {
-    const int t = (int)blockIdx.x + i * (int)gridDim.x;
-    mt = t % n_mt;
-    const int u = t / n_mt;
-    g = u % prm.Hkv;
-    p = u / prm.Hkv;
-  };
-  auto blocks_of = [&](int mt) { return (min(l, (mt + 1) * Tm) + kKB - 1) / kKB; };
 
   if (warp == 8) {
     tc::tmem_alloc(smem_u32(&bars->tmem_slot), kTmemCols);
@@ -149,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&bars->o_stored[s], kCompute);
     }
     mbar_init(&bars->s_done, 1);
-    mbar_init(&bars->s_free, kCompute);
     mbar_init(&bars->p_done, kCompute);
     mbar_init(&bars->o_done, 1);
     fence_mbar_init();
@@ -169,147 +213,145 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == 8) {
     // ============================================ K/V blocks by TMA, tcgen05.mma
-    // The K and V loads follow the products one to one: for each tile, blocks
-    // 0 .. nb-1.  Each load is issued one step ahead of its product.
+    // Steps run over this CTA's tiles and their key blocks.  Per step: P V once
+    // P is in TMEM, then at once S of the next step (so S done also means the
+    // P V before it is done), then the K and V loads two steps ahead, whose
+    // slots the S and the P V just issued free.
     bool failed = false;
-    int kc = 0, vc = 0;  // loads issued
-    // cursors of the next K and V loads: (tile, block)
-    int kl_i = 0, kl_b = 0, vl_i = 0, vl_b = 0;
-    auto load_next_k = [&]() {
-      if (kl_i >= my_tiles) return;
-      int p, g, mt;
-      tile_of(kl_i, p, g, mt);
+    int kc = 0, vc = 0, sx = 0, px = 0;  // K, V loads issued; S, P V products issued
+    StepWalk kw, vw, sw, pw;             // next K load, V load, S, P V
+    kw.init(prm);
+    vw.init(prm);
+    sw.init(prm);
+    pw.init(prm);
+    auto load_k = [&]() {
+      if (kw.i >= my_tiles) return;
       const int s = kc & 1;
       if (!mbar_wait(&bars->kfree[s], ((uint32_t)(kc >> 1) & 1u) ^ 1u)) failed = true;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->kfull[s], kTile);
-        tma_load_4d(sbase + kOffK + s * kTile, &tm_k, &bars->kfull[s], 0, g, kl_b * kKB, p);
+        tma_load_4d(sbase + kOffK + s * kTile, &tm_k, &bars->kfull[s], 0, kw.t.g, kw.b * kKB, kw.t.p);
       }
       ++kc;
-      if (++kl_b == blocks_of(mt)) {
-        kl_b = 0;
-        ++kl_i;
-      }
+      kw.next(prm);
     };
-    auto load_next_v = [&]() {
-      if (vl_i >= my_tiles) return;
-      int p, g, mt;
-      tile_of(vl_i, p, g, mt);
+    auto load_v = [&]() {
+      if (vw.i >= my_tiles) return;
       const int s = vc & 1;
       if (!mbar_wait(&bars->vfree[s], ((uint32_t)(vc >> 1) & 1u) ^ 1u)) failed = true;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->vfull[s], kTile);
-        tma_load_4d(sbase + kOffV + s * kTile, &tm_v, &bars->vfull[s], 0, g, vl_b * kKB, p);
+        tma_load_4d(sbase + kOffV + s * kTile, &tm_v, &bars->vfull[s], 0, vw.t.g, vw.b * kKB, vw.t.p);
       }
       ++vc;
-      if (++vl_b == blocks_of(mt)) {
-        vl_b = 0;
-        ++vl_i;
+      vw.next(prm);
+    };
+    // S = q K^T of the next step into TMEM [0, 128); the compute warps have
+    // finished reading the last S (P of its step is done)
+    auto issue_s = [&]() {
+      if (sw.i >= my_tiles || failed) return;
+      const int ks = sx & 1;
+      if (__any_sync(0xffffffffu,
+                     (sw.b == 0 && !mbar_wait(&bars->qfull[sw.i & 1], (uint32_t)(sw.i >> 1) & 1u)) ||
+                         !mbar_wait(&bars->kfull[ks], (uint32_t)(sx >> 1) & 1u))) {
+        failed = true;
+        return;
       }
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const int kend = min(l, (sw.t.mt + 1) * Tm);
+        const int N = (min(kKB, kend - sw.b * kKB) + 15) & ~15;
+        const uint32_t idesc = tc::idesc_bf16_f32(128, N, 0);
+        const uint32_t stage = sbase + kOffQ + (sw.i & 1) * kTile;
+        const uint32_t kb = sbase + kOffK + ks * kTile;
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16) {
+          const uint64_t a = tc::smem_desc_sw128(stage + k16 * 32, 16, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(kb + k16 * 32, 16, 1024);
+          tc::mma_ss(tmem, a, bd, idesc, k16 > 0);
+        }
+        tc::commit(smem_u32(&bars->s_done));
+        tc::commit(smem_u32(&bars->kfree[ks]));
+      }
+      __syncwarp();
+      ++sx;
+      sw.next(prm);
     };
     if (lane == 0) {
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
     }
-    load_next_k();
-    load_next_v();
-    int sx = 0, kx = 0, vx = 0, px = 0;  // products issued: S, K consumed, V consumed, P V
-    for (int i = 0; i < my_tiles && !failed; ++i) {
-      int p, g, mt;
-      tile_of(i, p, g, mt);
-      const int nb = blocks_of(mt);
-      const int kend = min(l, (mt + 1) * Tm);  // keys of the tile's last token
-      const uint32_t stage = sbase + kOffQ + (i & 1) * kTile;
-      if (__any_sync(0xffffffffu, !mbar_wait(&bars->qfull[i & 1], (uint32_t)(i >> 1) & 1u))) {
+    load_k();
+    load_k();
+    load_v();
+    load_v();
+    issue_s();
+    while (pw.i < my_tiles && !failed) {
+      // O (+)= P V once P is in TMEM and V has landed
+      const int vs = px & 1;
+      if (__any_sync(0xffffffffu, !mbar_wait(&bars->vfull[vs], (uint32_t)(px >> 1) & 1u) ||
+                                      !mbar_wait(&bars->p_done, (uint32_t)px & 1u))) {
         failed = true;
         break;
       }
-      {
-        for (int b = 0; b < nb; ++b) {
-          const int N = (min(kKB, kend - b * kKB) + 15) & ~15;
-          load_next_k();  // one step ahead
-          const int ks = kx & 1;
-          // S may be overwritten once the compute warps have read the last one
-          if (__any_sync(0xffffffffu, !mbar_wait(&bars->kfull[ks], (uint32_t)(kx >> 1) & 1u) ||
-                                          !mbar_wait(&bars->s_free, ((uint32_t)sx & 1u) ^ 1u))) {
-            failed = true;
-            break;
-          }
-          tc::fence_after_sync();
-          if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16_f32(128, N, 0);
-            const uint32_t kb = sbase + kOffK + ks * kTile;
-#pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16) {
-              const uint64_t a = tc::smem_desc_sw128(stage + k16 * 32, 16, 1024);
-              const uint64_t bd = tc::smem_desc_sw128(kb + k16 * 32, 16, 1024);
-              tc::mma_ss(tmem, a, bd, idesc, k16 > 0);
-            }
-            tc::commit(smem_u32(&bars->s_done));
-            tc::commit(smem_u32(&bars->kfree[ks]));
-          }
-          __syncwarp();
-          ++kx;
-          ++sx;
-          {
-            // O (+)= P V once P is in TMEM and V has landed
-            load_next_v();
-            const int vs = vx & 1;
-            if (__any_sync(0xffffffffu, !mbar_wait(&bars->vfull[vs], (uint32_t)(vx >> 1) & 1u) ||
-                                            !mbar_wait(&bars->p_done, (uint32_t)px & 1u))) {
-              failed = true;
-              break;
-            }
-            tc::fence_after_sync();
-            if (lane == 0) {
-              const uint32_t idesc = tc::idesc_bf16_f32(128, 64, 1);
-              const uint32_t vb = sbase + kOffV + vs * kTile;
-              for (int k16 = 0; k16 < N / 16; ++k16) {
-                const uint64_t bd = tc::smem_desc_sw128(vb + k16 * 2048, kTile, 1024);
-                tc::mma_ts(tmem + kOCol, tmem + kPCol + k16 * 8, bd, idesc, (b > 0 || k16 > 0) ? 1u : 0u);
-              }
-              tc::commit(smem_u32(&bars->vfree[vs]));
-              if (b == nb - 1) tc::commit(smem_u32(&bars->o_done));
-            }
-            __syncwarp();
-            ++vx;
-            ++px;
-          }
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const int kend = min(l, (pw.t.mt + 1) * Tm);
+        const int N = (min(kKB, kend - pw.b * kKB) + 15) & ~15;
+        const uint32_t idesc = tc::idesc_bf16_f32(128, 64, 1);
+        const uint32_t vb = sbase + kOffV + vs * kTile;
+        for (int k16 = 0; k16 < N / 16; ++k16) {
+          const uint64_t bd = tc::smem_desc_sw128(vb + k16 * 2048, kTile, 1024);
+          tc::mma_ts(tmem + kOCol, tmem + kPCol + k16 * 8, bd, idesc, (pw.b > 0 || k16 > 0) ? 1u : 0u);
         }
+        tc::commit(smem_u32(&bars->vfree[vs]));
+        if (pw.b == pw.nb - 1) tc::commit(smem_u32(&bars->o_done));
       }
+      __syncwarp();
+      ++px;
+      pw.next(prm);
+      issue_s();
+      load_k();
+      load_v();
     }
     if (lane == 0 && failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     __syncwarp();
   } else if (warp == 9) {
     // ============================================ q tiles in, O tiles out
     bool failed = false;
-    auto load_q = [&](int i) {
-      if (i >= my_tiles) return;
-      int p, g, mt;
-      tile_of(i, p, g, mt);
-      mbar_arrive_expect_tx(&bars->qfull[i & 1], (uint32_t)Tm * G * 128);
-      tma_load_5d(sbase + kOffQ + (i & 1) * kTile, &tm_q, &bars->qfull[i & 1], 0, 0, g * G, mt * Tm, p);
+    TileWalk qw, ow;  // next q load, next O store
+    qw.init(prm);
+    ow.init(prm);
+    int qi = 0;
+    auto load_q = [&]() {
+      if (qi >= my_tiles) return;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->qfull[qi & 1], (uint32_t)Tm * G * 128);
+        tma_load_5d(sbase + kOffQ + (qi & 1) * kTile, &tm_q, &bars->qfull[qi & 1], 0, 0, qw.g * G,
+                    qw.mt * Tm, qw.p);
+      }
+      ++qi;
+      qw.next(prm);
     };
     if (lane == 0 && my_tiles > 0) {
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_o);
-      load_q(0);
-      load_q(1);
     }
+    load_q();
+    load_q();
     for (int i = 0; i < my_tiles; ++i) {
       if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored[i & 1], (uint32_t)(i >> 1) & 1u))) {
         failed = true;
         break;
       }
       if (lane == 0) {
-        int p, g, mt;
-        tile_of(i, p, g, mt);
-        tma_store_5d(&tm_o, sbase + kOffQ + (i & 1) * kTile, 0, 0, g * G, mt * Tm, p);
+        tma_store_5d(&tm_o, sbase + kOffQ + (i & 1) * kTile, 0, 0, ow.g * G, ow.mt * Tm, ow.p);
         bulk_commit();
         bulk_wait_read_all();
-        load_q(i + 2);
       }
       __syncwarp();
+      ow.next(prm);
+      load_q();
     }
     if (lane == 0) {
       bulk_wait_all();
@@ -328,11 +370,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!failed && !mbar_wait(bar, parity)) failed = true;
     };
     const float sc = prm.scale_log2;
-    int sx = 0, px = 0;
-    for (int i = 0; i < my_tiles; ++i) {
-      int p, g, mt;
-      tile_of(i, p, g, mt);
-      const int nb = blocks_of(mt);
+    int sx = 0;
+    TileWalk tw;
+    tw.init(prm);
+    for (int i = 0; i < my_tiles; ++i, tw.next(prm)) {
+      const int mt = tw.mt;
+      const int nb = StepWalk::blocks(prm, mt);
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
       const bool valid = row_tok < toks;
       const bool wlive = (warp & 3) * 32 < toks * G;  // warp-uniform, same for the row's partner
@@ -431,10 +474,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         tc::wait_st();
         tc::fence_before_sync();
-        mbar_arrive(&bars->p_done);
-        mbar_arrive(&bars->s_free);
+        mbar_arrive(&bars->p_done);  // P in TMEM, and S read: the next S may go
         ++sx;
-        ++px;
       }
       // ---- O of row r, this half's 32 columns, normalised into the stage
       wait(&bars->o_done, (uint32_t)i & 1u);
