@@ -127,16 +127,21 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// TMEM load of 16 columns of this thread's lane that also returns their maximum.
-__device__ __forceinline__ float ld16_max(uint32_t taddr) {
-  uint32_t r[16];
+// 32 columns of this thread's lane out of TMEM (completes at tc::wait_ld).
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+// TMEM load of 32 columns of this thread's lane that also returns their maximum.
+__device__ __forceinline__ float ld32_max(uint32_t taddr) {
+  uint32_t r[32];
   float m;
   asm volatile(
-      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, %16, [%17];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=f"(m)
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=f"(m)
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" : "+f"(m)::"memory");
   return m;
@@ -397,22 +402,31 @@ __global__ void __launch_bounds__(kThreads, 2)
         wait(&bars->s_done, (uint32_t)sx & 1u);
         tc::fence_after_sync();
         if (wlive) {
-          // the block's maximum over this half's chunks, then over the row
+          // the block's maximum over this half's 32-column groups q = h, h + 2
+          // (the second 16 columns of a group may lie past the block's keys)
           float mx = kNegInf;
-          for (int c = h; c * 16 < N; c += 2) {
-            const int key0 = b * kKB + c * 16;
-            if (key0 + 16 <= lim_all) {
-              mx = fmaxf(mx, ld16_max(tmem + lane_base + c * 16));
+          for (int q = h; q * 32 < N; q += 2) {
+            const int key0 = b * kKB + q * 32;
+            const uint32_t ta = tmem + lane_base + q * 32;
+            if (key0 + 32 <= lim_all) {
+              mx = fmaxf(mx, ld32_max(ta));
             } else {
-              uint32_t v[16];
-              tc::ld16(tmem + lane_base + c * 16, v);
+              uint32_t v[32];
+              ld32(ta, v);
               tc::wait_ld();
-              const float4* bt = bias_row(key0);
+              const int nh = q * 32 + 16 < N ? 2 : 1;
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const float4 bq = bt[q4];
-                mx = max3f(mx, __uint_as_float(v[4 * q4]) + bq.x, __uint_as_float(v[4 * q4 + 1]) + bq.y);
-                mx = max3f(mx, __uint_as_float(v[4 * q4 + 2]) + bq.z, __uint_as_float(v[4 * q4 + 3]) + bq.w);
+              for (int hh = 0; hh < 2; ++hh) {
+                if (hh < nh) {
+                  const float4* bt = bias_row(key0 + hh * 16);
+#pragma unroll
+                  for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 bq = bt[q4];
+                    const int o = hh * 16 + 4 * q4;
+                    mx = max3f(mx, __uint_as_float(v[o]) + bq.x, __uint_as_float(v[o + 1]) + bq.y);
+                    mx = max3f(mx, __uint_as_float(v[o + 2]) + bq.z, __uint_as_float(v[o + 3]) + bq.w);
+                  }
+                }
               }
             }
           }
@@ -446,30 +460,47 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             m = mb;
           }
-          // P = exp2((S - m) scale) into TMEM as bf16, summed
+          // P = exp2((S - m) scale) into TMEM as bf16 pairs (group q -> P
+          // columns [16 q, 16 q + 16)), summed
           const uint64_t nmc2 = f2_make(-m * sc, -m * sc);
-          for (int c = h; c * 16 < N; c += 2) {
-            const int key0 = b * kKB + c * 16;
-            uint32_t v[16];
-            tc::ld16(tmem + lane_base + c * 16, v);
+          for (int q = h; q * 32 < N; q += 2) {
+            const int key0 = b * kKB + q * 32;
+            uint32_t v[32];
+            ld32(tmem + lane_base + q * 32, v);
             tc::wait_ld();
-            const float4* bt = key0 + 16 <= lim_all ? nullptr : bias_row(key0);
-            uint32_t pk[8];
+            const bool two = q * 32 + 16 < N;
+            uint32_t pk[16];
+            if (key0 + 32 <= lim_all) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              uint64_t off = nmc2;
-              if (bt) {
-                const float4 bq = bt[e >> 1];
-                off = f2_add(nmc2, (e & 1) ? f2_make(bq.z, bq.w) : f2_make(bq.x, bq.y));
+              for (int e = 0; e < 16; ++e) {
+                float a, bb;
+                f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, nmc2),
+                         a, bb);
+                const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
+                acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
+                pk[e] = f2_to_bf16x2(pp);
               }
-              float a, bb;
-              f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, off),
-                       a, bb);
-              const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
-              acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
-              pk[e] = f2_to_bf16x2(pp);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                if (e < 8 || two) {
+                  const float4 bq = bias_row(key0 + (e >> 3) * 16)[(e >> 1) & 3];
+                  const uint64_t off = f2_add(nmc2, (e & 1) ? f2_make(bq.z, bq.w) : f2_make(bq.x, bq.y));
+                  float a, bb;
+                  f2_split(f2_fma(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, off),
+                           a, bb);
+                  const uint64_t pp = f2_make(ex2_approx(a), ex2_approx(bb));
+                  acc[e & 1] = f2_fma(pp, one2, acc[e & 1]);
+                  pk[e] = f2_to_bf16x2(pp);
+                }
+              }
             }
-            tc::st8(tmem + lane_base + kPCol + c * 8, pk);
+            const uint32_t pa = tmem + lane_base + kPCol + q * 16;
+            if (two) {
+              tmem_st16(pa, pk);
+            } else {
+              tc::st8(pa, *reinterpret_cast<const uint32_t(*)[8]>(pk));
+            }
           }
         }
         tc::wait_st();
