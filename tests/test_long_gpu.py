@@ -5,6 +5,7 @@ epilogue has already rotated q and k_new), against the float64 oracle, on
 sequences longer than the 128 keys of the single-pass kernel."""
 from __future__ import annotations
 
+import numpy as np
 import pytest
 import torch
 
@@ -52,3 +53,40 @@ def test_long_kernel_is_deterministic_and_layer_independent():
     b = binding.gist_attn_fwd(wl.q, wl.k_new, wl.v_new, wl.kv_pool, None, None, None, dims=dims)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("P,l,Hq,Hkv", [
+    (64, 200, 14, 2),   # 1,536 row tiles: several per persistent CTA
+    (40, 300, 4, 4),    # G = 1: 480 tiles, the last CTAs take two
+    (40, 140, 128, 1),  # G = 128: 5,600 one-token tiles, ~18 per CTA
+])
+def test_long_many_tiles_per_cta_every_pair(P, l, Hq, Hkv):
+    """Grids where each persistent CTA walks several row tiles (the tile walk,
+    the two q stages and the K/V streams across tile boundaries)."""
+    wl = workloads.make_custom(P, l, Hq, Hkv, 64, 0, 0, 0, device=DEV, seed=P + l)
+    dims = dict(wl.dims, flags=binding.FLAG_PREROTATED)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd(wl.q, wl.k_new, wl.v_new, wl.kv_pool, None, None, None, dims=dims,
+                                status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.gist_attn(wl.q, wl.k_new, wl.v_new, wl.kv_pool, dims=dims)
+    compare(got, ref, f"P={P} l={l} G={Hq // Hkv}")
+
+
+def test_long_offline_pass_full_size_sampled():
+    """The offline pass as the benchmark times it (128 items of 1000 prompt +
+    8 gist tokens, the gist model's heads); the oracle checks a sample of items
+    spread over the grid."""
+    P, l, Hq, Hkv = 128, 1008, 14, 2
+    wl = workloads.make_custom(P, l, Hq, Hkv, 64, 0, 0, 0, device=DEV, seed=21)
+    dims = dict(wl.dims, flags=binding.FLAG_PREROTATED)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd(wl.q, wl.k_new, wl.v_new, wl.kv_pool, None, None, None, dims=dims,
+                                status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel = np.array([0, 1, 37, 64, 101, 127], dtype=np.int32)
+    ref = oracle.gist_attn(wl.q, wl.k_new, wl.v_new, wl.kv_pool, dims=dims, pairs=sel)
+    compare(got[torch.from_numpy(sel).long().to(DEV)], ref, "offline pass, sampled items")
+    assert torch.isfinite(got.float()).all()
