@@ -68,6 +68,28 @@ def test_qkv_rope_matches_oracle(P, l, Hq, Hkv, d, dm, pos):
     compare(v, rv, "v_new")
 
 
+def test_projections_with_several_tiles_per_cta():
+    """Both GEMMs at a size where each persistent CTA takes two or three output
+    tiles (the k-block ring and the two TMEM accumulators carried across
+    tiles): 128 pairs x 64 tokens of the gist model (8,192 rows)."""
+    P, l, Hq, Hkv, d, dm = 128, 64, 14, 2, 64, 1152
+    x, w = _x(P, l, dm, 11), _weights((Hq + 2 * Hkv) * d, dm, 12)
+    pos_t = torch.from_numpy(np.random.default_rng(13).integers(0, 4000, P).astype(np.int32)).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q, k, v = binding.gist_qkv_rope(x, w, pos_t, dims=_dims(P, l, Hq, Hkv, d), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rq, rk, rv = proj.qkv_rope(x, w, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, cached=8,
+                               pos_offset=pos_t.cpu().numpy())
+    compare(q, rq, "q")
+    compare(k, rk, "k_new")
+    compare(v, rv, "v_new")
+    wo = _weights(dm, Hq * d, 14)
+    y = binding.gist_out_proj(q, wo, dims=_dims(P, l, Hq, Hkv, d))
+    torch.cuda.synchronize()
+    compare(y, proj.out_proj(q.reshape(P, l, Hq * d), wo), "y")
+
+
 @pytest.mark.parametrize("P,l,Hq,d,dm", [(3, 50, 14, 64, 256), (2, 64, 14, 64, 896), (1, 200, 8, 128, 384),
                                           (5, 77, 14, 64, 1152)])
 def test_out_proj_matches_oracle(P, l, Hq, d, dm):
