@@ -42,7 +42,7 @@ namespace {
 
 constexpr int kCompute = 256;            // 8 compute warps
 constexpr int kThreads = kCompute + 64;  // + the MMA warp and the TMA warp
-constexpr int kStages = 3;
+constexpr int kMaxStages = 3;  // q/O stages: 3, or 2 where that lets two CTAs share an SM
 constexpr int kMaxKeys = 128;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxBlocksPerPair = 64;
@@ -67,20 +67,21 @@ struct TcParams {
 };
 
 struct Layout {
-  int Tm, n_mt, kv_rows;
+  int Tm, n_mt, kv_rows, stages;
   uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_bar,
       bytes;
   uint32_t p_col, o_col, tmem_cols;
 };
 
-Layout plan(const Problem& pb) {
+Layout plan_stages(const Problem& pb, int stages) {
   Layout L{};
+  L.stages = stages;
   const int np = pb.d / 64;
   L.Tm = 128 / pb.G;
   L.n_mt = (pb.l + L.Tm - 1) / L.Tm;
   L.kv_rows = (pb.C + pb.l + 15) / 16 * 16;  // also the widest S of any tile
   L.stage_bytes = (uint32_t)np * 128 * 128;
-  uint32_t off = kStages * L.stage_bytes;
+  uint32_t off = (uint32_t)stages * L.stage_bytes;
   L.off_kv = off;
   L.kv_buf_bytes = 2u * np * L.kv_rows * 128;  // K panels then V panels
   off += 2 * L.kv_buf_bytes;
@@ -102,6 +103,20 @@ Layout plan(const Problem& pb) {
   const uint32_t need = L.o_col + pb.d;
   L.tmem_cols = need <= 256 ? 256 : 512;
   return L;
+}
+
+// Two CTAs share an SM when d = 64, the TMEM plan is 256 columns and shared
+// memory holds two; where three q/O stages miss that by the shared memory, two
+// stages take their place.
+constexpr uint32_t kTwoPerSmBytes = 113 * 1024;
+Layout plan(const Problem& pb) {
+  const Layout L3 = plan_stages(pb, kMaxStages);
+  // (wider key sets than 96 run one CTA per SM for their registers anyway)
+  if (pb.d == 64 && L3.kv_rows <= 96 && L3.tmem_cols == 256 && L3.bytes > kTwoPerSmBytes) {
+    const Layout L2 = plan_stages(pb, 2);
+    if (L2.bytes <= kTwoPerSmBytes) return L2;
+  }
+  return L3;
 }
 
 // Rotate one 16-byte chunk of x (elements j0..j0+7) against its partner chunk y
@@ -155,7 +170,7 @@ __device__ __forceinline__ float ld16_max(uint32_t taddr) {
 }
 
 struct Bars {
-  uint64_t qfull[kStages];
+  uint64_t qfull[kMaxStages];
   uint64_t rope_done;  // compute -> MMA warp: q tile rotated (hi in the stage, lo in TMEM)
   uint64_t s_done;     // tensor core -> compute: S ready
   uint64_t p_done;     // compute -> MMA warp: P ready
@@ -169,7 +184,7 @@ struct Bars {
 // NCH: S chunks of 16 columns per thread (the tile's keys / 32, rounded up).
 // Registers: each of the 4 SM sub-partitions holds 16 K; two CTAs of 9 warps
 // put 5 warps on one of them (96 registers a thread), one CTA puts 3 (168).
-template <int D, int NCH>
+template <int D, int NCH, int NS>
 __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_o,
@@ -198,6 +213,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
                            : 0;
   const int my_tiles = my_units * n_mt;
   auto unit_of = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
+  // tile i uses q/O stage i mod stages, in its (i / stages)-th round
+  auto stage_of = [](int i) { return i % NS; };
+  auto stage_round = [](int i) { return (uint32_t)(i / NS) & 1u; };
 
   // ---- set-up (all threads)
   if (warp == 8) {
@@ -205,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars->qfull[s], 1);
+    for (int s = 0; s < kMaxStages; ++s) mbar_init(&bars->qfull[s], 1);
     mbar_init(&bars->rope_done, kCompute);
     mbar_init(&bars->s_done, 1);
     mbar_init(&bars->p_done, kCompute);
@@ -225,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     }
     for (int idx = tid; idx < 17 * 16; idx += kThreads) bias[idx] = (idx & 15) < (idx >> 4) ? 0.f : kNegInf;
     const int qpad = 128 - Tm * G;  // rows of each Q stage that no TMA box reaches
-    for (int idx = tid; idx < kStages * NP * qpad * 8; idx += kThreads) {
+    for (int idx = tid; idx < NS * NP * qpad * 8; idx += kThreads) {
       const int c = idx & 7, rr = (idx >> 3) % qpad, sp = (idx >> 3) / qpad;
       sts16(sbase + (sp / NP) * prm.stage_bytes + (sp % NP) * kPanel + swz128(Tm * G + rr, c), z);
     }
@@ -254,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     // no integer division on the per-tile path)
     for (int i = 0, k = 0, mt = 0; i < my_tiles; ++i, mt = (mt + 1 == n_mt) ? (++k, 0) : mt + 1) {
       const uint32_t par = (uint32_t)i & 1u;
-      const uint32_t stage = sbase + (i % kStages) * prm.stage_bytes;
+      const uint32_t stage = sbase + stage_of(i) * prm.stage_bytes;
       const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
       const uint32_t vb = kb + NP * kv_panel;
       const int N = (C + min(l, (mt + 1) * Tm) + 15) & ~15;
@@ -292,14 +310,14 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     __syncwarp();
   } else if (warp == 9) {
     // ================================================================ TMA
-    // Q tiles in, O tiles out; a stage is refilled kStages tiles on as soon as
+    // Q tiles in, O tiles out; a stage is refilled NS tiles on as soon as
     // the store of its output has read it.
     bool failed = false;
     // loads and stores each walk the tiles in order: (unit, tile-in-unit) cursors
     int lk = 0, lmt = 0, sk = 0, smt = 0;
     auto load_tile = [&](int i) {  // i = the next tile to load
       if (i >= my_tiles) return;
-      const int u = unit_of(lk), mt = lmt, s = i % kStages;
+      const int u = unit_of(lk), mt = lmt, s = stage_of(i);
       if (++lmt == n_mt) {
         lmt = 0;
         ++lk;
@@ -314,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     if (lane == 0 && my_tiles > 0) {
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_o);
-      for (int i = 0; i < kStages; ++i) load_tile(i);
+      for (int i = 0; i < NS; ++i) load_tile(i);
     }
     for (int i = 0; i < my_tiles; ++i) {
       if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored[i & 1], (uint32_t)(i >> 1) & 1u))) {
@@ -322,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
         break;
       }
       if (lane == 0) {
-        const int u = unit_of(sk), mt = smt, s = i % kStages;
+        const int u = unit_of(sk), mt = smt, s = stage_of(i);
         if (++smt == n_mt) {
           smt = 0;
           ++sk;
@@ -333,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           tma_store_5d(&tm_o, sbase + s * prm.stage_bytes + pn * kPanel, 0, pn, g * G, mt * Tm, p);
         bulk_commit();
         bulk_wait_read_all();
-        load_tile(i + kStages);
+        load_tile(i + NS);
       }
       __syncwarp();
     }
@@ -443,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     // Rows past the tile's tokens hold zeros (TMA fill, or set-up for rows no
     // box reaches), so they come out zero without a select.
     auto rope_tile = [&](int i, int mt) {
-      const int s = i % kStages;
+      const int s = stage_of(i);
       const uint32_t stage = sbase + s * prm.stage_bytes;
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
       const int tt = min(row_tok, toks - 1);
-      wait(&bars->qfull[s], (uint32_t)(i / kStages) & 1u);
+      wait(&bars->qfull[s], stage_round(i));
       // q that arrives rotated stays in the stage as loaded (bf16).  A warp whose
       // 32 rows are all past the tile's tokens skips the work: rows are
       // independent in both products, and such rows are never stored.
@@ -620,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       tc::fence_after_sync();
       if (wlive) {
         named_bar_sync(pair_bar, 64);  // the partner's row sum is written
-        const uint32_t stage = sbase + (i % kStages) * prm.stage_bytes;
+        const uint32_t stage = sbase + stage_of(i) * prm.stage_bytes;
         constexpr int OC = D / 32;  // 16-column chunks per half
         if (bad) {
           if (valid) {
@@ -689,9 +707,10 @@ int encode_map(CUtensorMap* m, const void* base, const Problem& pb, int Tm) {
   return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
 }
 
-template <int D, int NCH>
+template <int D, int NCH, int NS>
 int launch_d(const Problem& pb, cudaStream_t stream) {
   const Layout L = plan(pb);
+  if (L.stages != NS) return GIST_ATTN_ERR_UNSUPPORTED;  // shared memory is sized for L.stages
   TcParams prm{};
   prm.k_new = static_cast<const bf16*>(pb.k_new);
   prm.v_new = static_cast<const bf16*>(pb.v_new);
@@ -727,7 +746,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   if (rc != GIST_ATTN_OK) return rc;
   rc = encode_map(&tm_o, pb.out, pb, L.Tm);
   if (rc != GIST_ATTN_OK) return rc;
-  if (cudaFuncSetAttribute(prefill_tc_kernel<D, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(prefill_tc_kernel<D, NCH, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)L.bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   int dev = 0, sms = 0;
@@ -736,10 +755,10 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
     return GIST_ATTN_ERR_LAUNCH;
   // Two CTAs per SM only when both fit: two 256-column TMEM allocations and
   // shared memory for two.  A larger TMEM plan or shared memory means one.
-  const int per_sm = (D == 64 && L.tmem_cols == 256 && L.bytes <= 113 * 1024) ? 2 : 1;
+  const int per_sm = (D == 64 && L.tmem_cols == 256 && L.bytes <= kTwoPerSmBytes) ? 2 : 1;
   const int64_t units = (int64_t)pb.P * pb.Hkv;
   const int grid = (int)(units < (int64_t)sms * per_sm ? units : (int64_t)sms * per_sm);
-  prefill_tc_kernel<D, NCH><<<grid, kThreads, L.bytes, stream>>>(tm_q, tm_o, prm);
+  prefill_tc_kernel<D, NCH, NS><<<grid, kThreads, L.bytes, stream>>>(tm_q, tm_o, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
@@ -756,14 +775,15 @@ bool prefill_tc_fits(const Problem& pb) {
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream) {
   const int chunks = (plan(pb).kv_rows / 16 + 1) / 2;  // per thread: chunks h, h+2, ...
   if (pb.d == 64) {
-    if (chunks <= 2) return launch_d<64, 2>(pb, stream);
-    if (chunks <= 3) return launch_d<64, 3>(pb, stream);
-    return launch_d<64, 4>(pb, stream);
+    if (chunks <= 2) return launch_d<64, 2, 3>(pb, stream);
+    if (chunks <= 3)
+      return plan(pb).stages == 2 ? launch_d<64, 3, 2>(pb, stream) : launch_d<64, 3, 3>(pb, stream);
+    return launch_d<64, 4, 3>(pb, stream);
   }
   if (pb.d == 128) {
-    if (chunks <= 2) return launch_d<128, 2>(pb, stream);
-    if (chunks <= 3) return launch_d<128, 3>(pb, stream);
-    return launch_d<128, 4>(pb, stream);
+    if (chunks <= 2) return launch_d<128, 2, 3>(pb, stream);
+    if (chunks <= 3) return launch_d<128, 3, 3>(pb, stream);
+    return launch_d<128, 4, 3>(pb, stream);
   }
   return GIST_ATTN_ERR_UNSUPPORTED;
 }

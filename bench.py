@@ -71,9 +71,10 @@ def parse_args(argv=None):
                     help="cached-KV element type (fp8: E4M3 pool with per-block scales)")
     ap.add_argument("--fused", action="store_true",
                     help="also time the projections either side (QKV + RoPE, output projection)")
-    ap.add_argument("--row", choices=["offline", "block-mass"], default=None,
+    ap.add_argument("--row", choices=["offline", "block-mass", "sweep"], default=None,
                     help="measure a widening row instead of the hot path: the offline gist "
-                         "compression pass, or the paged decode with per-block attention mass + append")
+                         "compression pass, the paged decode with per-block attention mass + append, "
+                         "or the gist workload over k x l (one JSON line per point)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -609,6 +610,58 @@ def _timed_layers(args, L, launch, stream, ws):
     return total, ph
 
 
+def run_sweep(args, dev, stream, status, ws, rank, peak, peak_src):
+    """The gist workload (12,800 Zipf pairs, the gist model's heads) with k in
+    {1, 4, 8, 16, 32, 64} cached gist positions and l in {16, 64, 256} new
+    tokens, each point through gist_attn_fwd on layers 0 and 1 of a two-layer
+    pool.  Prints one JSON line per point; returns None."""
+    import torch
+
+    from attention_cached_kv_gb300 import binding, workloads
+
+    for l_new in (16, 64, 256):
+        for k in (1, 4, 8, 16, 32, 64):
+            over = {"num_layers": 2}
+            if args.queries:
+                over["queries"] = args.queries
+            wl = workloads.make(workloads.sweep_spec(k, l_new), device=dev, **over)
+            d = wl.dims
+            P, Hq, hd = d["num_pairs"], d["num_q_heads"], d["head_dim"]
+            out = torch.empty_like(wl.q)
+
+            def launch(li, e, wl=wl, out=out):
+                if e: e[0].record(stream)
+                binding.gist_attn_fwd(wl.q, wl.k_new, wl.v_new, wl.kv_pool, wl.item_ids, None, None, out,
+                                      dims=dict(wl.dims, layer=li), status=status, stream=stream)
+                if e:
+                    e[1].record(stream)
+                    e[2].record(stream)
+
+            _, (t_attn, _) = _timed_layers(args, 2, launch, stream, ws)
+            if int(status.item()) != 0:
+                raise RuntimeError(f"device status {int(status.item())} at k={k} l={l_new}")
+            nbytes = algorithmic_bytes_per_launch(wl)["total"]
+            flops = 4.0 * hd * Hq * (l_new * k + l_new * (l_new + 1) / 2) * P  # useful: scores + PV
+            gbs = nbytes / (t_attn * 1e-3) / 1e9
+            # the library's dispatch: the single-pass tensor-core kernel while the
+            # keys fit 128, else the streaming kernel
+            kernel = "prefill_tc_kernel" if k + l_new <= 128 else "prefill_stream_kernel"
+            if rank == 0:
+                print(json.dumps({
+                    "metric": "(item,query) pairs/s per layer-attention", "row": "sweep", "k": k, "l": l_new,
+                    "value": P * ws / (t_attn * 1e-3), "unit": "pairs/s", "n_gpus": ws,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_launch": t_attn,
+                    "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+                    "config": {"workload": f"gist model, {P} Zipf(1.1) pairs, k={k} cached, l={l_new} new",
+                               "pairs": P, "layers_timed": 2},
+                    "kernel": kernel, "algorithmic_bytes_per_launch": nbytes, "achieved_gbs": gbs,
+                    "frac_of_hbm": gbs / peak, "peak_source": peak_src,
+                    "tflops": flops / (t_attn * 1e-3) / 1e12}), flush=True)
+            del wl, out
+            torch.cuda.empty_cache()
+    return None
+
+
 def run_row(args) -> dict:
     """The widening rows, each through its C-ABI entry points on synthetic data.
 
@@ -636,6 +689,8 @@ def run_row(args) -> dict:
     stream = torch.cuda.Stream(device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     peak, peak_src = measured_peaks()
+    if args.row == "sweep":
+        return run_sweep(args, dev, stream, status, ws, rank, peak, peak_src)
     if args.row == "offline":
         B, j, k = args.queries or 128, 1000, 8
         L = args.layers or 24

@@ -100,6 +100,22 @@ def test_full_size_workloads_sampled(name, n_sample, layer):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("k,l", [(32, 64), (64, 16)])
+def test_sweep_points_full_size_sampled(k, l):
+    """Sweep points of the gist workload at full size (12,800 Zipf pairs): k = 32
+    runs with two q stages so that two CTAs share an SM; k = 64, l = 16 is the
+    widest cache of the sweep's single-pass shapes."""
+    wl = workloads.make(workloads.sweep_spec(k, l), device=DEV, num_layers=2)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = run_gpu(wl, layer=1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel = sample(wl.dims["num_pairs"], 120, seed=k + l)
+    compare(got[torch.from_numpy(sel).to(DEV)], oracle_ref(wl, layer=1, pairs=sel), f"k={k} l={l}")
+    del wl, got
+    torch.cuda.empty_cache()
+
+
 def test_shift_invariance_on_gpu():
     """Gist page, 在线的一次 attention: the same relative distances give the same
     output, whether the gist sits at 0..k-1 (query from k) or at j..j+k-1 (query
