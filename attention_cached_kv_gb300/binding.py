@@ -20,7 +20,7 @@ OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH = 0, -1, -2, -3, 
 STATUS_BAD_BLOCK, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4
 FLAG_PREROTATED = 1
 
-EXPORTS = ("gist_attn_fwd", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
+EXPORTS = ("gist_attn_fwd", "gist_attn_workspace_bytes", "gist_attn_fwd_ws", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
            "gist_attn_fwd_gist_mask", "gist_kv_store", "gist_qkv_rope", "gist_out_proj",
            "gist_attn_gather_debug", "gist_kv_bytes_per_position", "gist_kv_bytes_per_item",
            "gist_kv_bytes_batch", "gist_attn_status_string")
@@ -69,6 +69,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             V = ctypes.c_void_p
             lib.gist_attn_fwd.restype = ctypes.c_int
             lib.gist_attn_fwd.argtypes = [V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
+            lib.gist_attn_workspace_bytes.restype = ctypes.c_size_t
+            lib.gist_attn_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+            lib.gist_attn_fwd_ws.restype = ctypes.c_int
+            lib.gist_attn_fwd_ws.argtypes = [V, V, V, V, V, V, V, V, V, ctypes.c_size_t,
+                                             ctypes.POINTER(Dims), V]
             lib.gist_attn_fwd_fp8kv.restype = ctypes.c_int
             lib.gist_attn_fwd_fp8kv.argtypes = [V, V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_attn_fwd_block_mass.restype = ctypes.c_int
@@ -156,6 +161,35 @@ def gist_attn_fwd(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, pos
                            _ptr(block_table, i32, "block_table"),
                            _ptr(pos_offset, i32, "pos_offset"), _ptr(out, bf, "out"),
                            ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return out
+
+
+def workspace_bytes(dims: dict) -> int:
+    """Device bytes gist_attn_fwd_ws wants for these dimensions (0: none)."""
+    D = make_dims(dims)
+    return int(load_library().gist_attn_workspace_bytes(ctypes.byref(D)))
+
+
+def gist_attn_fwd_ws(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, pos_offset=None,
+                     out=None, workspace=None, *, dims: dict, status: torch.Tensor | None = None,
+                     stream=None):
+    """gist_attn_fwd with a caller-owned device workspace (a uint8 tensor of at
+    least workspace_bytes(dims) bytes, or None); returns `out`."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q)
+    bf, i32 = torch.bfloat16, torch.int32
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _check(workspace, torch.uint8, "workspace")
+        ws_ptr, ws_bytes = ctypes.c_void_p(workspace.data_ptr()), workspace.numel()
+    D = make_dims(dims, status)
+    rc = lib.gist_attn_fwd_ws(_ptr(q, bf, "q"), _ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"),
+                              _ptr(kv_pool, bf, "kv_pool"), _ptr(item_ids, i32, "item_ids"),
+                              _ptr(block_table, i32, "block_table"),
+                              _ptr(pos_offset, i32, "pos_offset"), _ptr(out, bf, "out"), ws_ptr,
+                              ws_bytes, ctypes.byref(D), _stream(stream))
     _raise(rc)
     return out
 

@@ -100,39 +100,87 @@ int check_cache_args(const Problem& pb, const void* kv_pool, const int32_t* item
 
 using gattn::Problem;
 
+namespace gattn {
+namespace {
+
+// Checks and fills `pb` for gist_attn_fwd / gist_attn_fwd_ws; returns
+// GIST_ATTN_OK, or a code to return as is (P == 0 also comes back OK with
+// pb->P == 0).
+int prepare_fwd(const void* q, const void* k_new, const void* v_new, const void* kv_pool,
+                const int32_t* item_ids, const int32_t* block_table, const int32_t* pos_offset,
+                void* out, const gist_attn_dims* dims, Problem* pb) {
+  int rc = check_dims(dims, pb);
+  if (rc != GIST_ATTN_OK || pb->P == 0) return rc;
+  if (!q || !k_new || !v_new || !out) return GIST_ATTN_ERR_NULL;
+  rc = check_cache_args(*pb, kv_pool, item_ids, block_table);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
+      !aligned(pos_offset, 4) || !aligned(pb->status, 4))
+    return GIST_ATTN_ERR_ALIGN;
+  pb->q = q;
+  pb->k_new = k_new;
+  pb->v_new = v_new;
+  pb->kv_pool = pb->C > 0 ? kv_pool : nullptr;
+  pb->item_ids = pb->C > 0 ? item_ids : nullptr;
+  pb->block_table = pb->C > 0 ? block_table : nullptr;
+  pb->pos_offset = pos_offset;
+  pb->out = out;
+  if (pb->C == 0) pb->blocks_per_pair = 0;  // nothing cached: no ids to read
+  return GIST_ATTN_OK;
+}
+
+// The staged path applies: more than 128 keys on d = 64 where neither
+// single-kernel tensor-core path runs.
+bool wants_stage(const Problem& pb) {
+  return pb.l >= 2 && !prefill_tc_fits(pb) && !prefill_long_fits(pb) && staged_fits(pb);
+}
+
+int dispatch_fwd(const Problem& pb, cudaStream_t stream) {
+  if (pb.l == 1) {
+    if (decode_long_fits(pb)) return launch_decode_long(pb, stream);
+    if (decode_short_fits(pb)) return launch_decode_short(pb, stream);
+    if (decode_fits(pb)) return launch_decode(pb, stream);
+  }
+  if (prefill_tc_fits(pb)) return launch_prefill_tc(pb, stream);
+  if (prefill_long_fits(pb)) return launch_prefill_long(pb, stream);
+  if (prefill_fits(pb)) return launch_prefill(pb, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace gattn
+
 extern "C" int gist_attn_fwd(const void* q, const void* k_new, const void* v_new,
                              const void* kv_pool, const int32_t* item_ids,
                              const int32_t* block_table, const int32_t* pos_offset, void* out,
                              const gist_attn_dims* dims, cudaStream_t stream) {
   Problem pb{};
-  int rc = gattn::check_dims(dims, &pb);
-  if (rc != GIST_ATTN_OK) return rc;
-  if (pb.P == 0) return GIST_ATTN_OK;
-  if (!q || !k_new || !v_new || !out) return GIST_ATTN_ERR_NULL;
-  rc = gattn::check_cache_args(pb, kv_pool, item_ids, block_table);
-  if (rc != GIST_ATTN_OK) return rc;
-  if (!gattn::aligned(q, 16) || !gattn::aligned(k_new, 16) || !gattn::aligned(v_new, 16) ||
-      !gattn::aligned(out, 16) || !gattn::aligned(pos_offset, 4) ||
-      !gattn::aligned(pb.status, 4))
-    return GIST_ATTN_ERR_ALIGN;
-  pb.q = q;
-  pb.k_new = k_new;
-  pb.v_new = v_new;
-  pb.kv_pool = pb.C > 0 ? kv_pool : nullptr;
-  pb.item_ids = pb.C > 0 ? item_ids : nullptr;
-  pb.block_table = pb.C > 0 ? block_table : nullptr;
-  pb.pos_offset = pos_offset;
-  pb.out = out;
-  if (pb.C == 0) pb.blocks_per_pair = 0;  // nothing cached: no ids to read
-  if (pb.l == 1) {
-    if (gattn::decode_long_fits(pb)) return gattn::launch_decode_long(pb, stream);
-    if (gattn::decode_short_fits(pb)) return gattn::launch_decode_short(pb, stream);
-    if (gattn::decode_fits(pb)) return gattn::launch_decode(pb, stream);
-  }
-  if (gattn::prefill_tc_fits(pb)) return gattn::launch_prefill_tc(pb, stream);
-  if (gattn::prefill_long_fits(pb)) return gattn::launch_prefill_long(pb, stream);
-  if (gattn::prefill_fits(pb)) return gattn::launch_prefill(pb, stream);
-  return GIST_ATTN_ERR_UNSUPPORTED;
+  const int rc = gattn::prepare_fwd(q, k_new, v_new, kv_pool, item_ids, block_table, pos_offset, out,
+                                    dims, &pb);
+  if (rc != GIST_ATTN_OK || pb.P == 0) return rc;
+  return gattn::dispatch_fwd(pb, stream);
+}
+
+extern "C" size_t gist_attn_workspace_bytes(const gist_attn_dims* dims) {
+  Problem pb{};
+  if (gattn::check_dims(dims, &pb) != GIST_ATTN_OK || pb.P == 0) return 0;
+  if (pb.C == 0) pb.blocks_per_pair = 0;
+  return gattn::wants_stage(pb) ? gattn::stage_layout(pb).bytes : 0;
+}
+
+extern "C" int gist_attn_fwd_ws(const void* q, const void* k_new, const void* v_new,
+                                const void* kv_pool, const int32_t* item_ids,
+                                const int32_t* block_table, const int32_t* pos_offset, void* out,
+                                void* workspace, size_t workspace_bytes,
+                                const gist_attn_dims* dims, cudaStream_t stream) {
+  Problem pb{};
+  const int rc = gattn::prepare_fwd(q, k_new, v_new, kv_pool, item_ids, block_table, pos_offset, out,
+                                    dims, &pb);
+  if (rc != GIST_ATTN_OK || pb.P == 0) return rc;
+  if (workspace && gattn::aligned(workspace, 256) && gattn::wants_stage(pb) &&
+      workspace_bytes >= gattn::stage_layout(pb).bytes)
+    return gattn::launch_staged(pb, workspace, stream);
+  return gattn::dispatch_fwd(pb, stream);
 }
 
 extern "C" int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void* v_new,

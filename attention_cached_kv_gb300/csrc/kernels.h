@@ -42,6 +42,14 @@ EncodeTiledFn encode_tiled_fn();
 int launch_prefill(const Problem& pb, cudaStream_t stream);
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream);
 int launch_prefill_long(const Problem& pb, cudaStream_t stream);
+int launch_prefill_long_on(const Problem& pb, const void* q, const void* k, const void* v, int C,
+                           bool f16, cudaStream_t stream);
+// The staged path (stage.cu): workspace layout, fit and launch (pre-pass + long kernel).
+struct StageLayout {
+  size_t q_off, k_off, v_off, bytes;
+};
+StageLayout stage_layout(const Problem& pb);
+int launch_staged(const Problem& pb, void* workspace, cudaStream_t stream);
 int launch_decode(const Problem& pb, cudaStream_t stream);
 int launch_decode_long(const Problem& pb, cudaStream_t stream);
 int launch_decode_long_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
@@ -61,6 +69,8 @@ int launch_out_proj(const Problem& pb, const void* attn, const void* w, int d_mo
 bool prefill_fits(const Problem& pb);
 bool prefill_tc_fits(const Problem& pb);
 bool prefill_long_fits(const Problem& pb);
+bool prefill_long_grid_ok(const Problem& pb, int rows);
+bool staged_fits(const Problem& pb);
 bool decode_fits(const Problem& pb);
 bool decode_long_fits(const Problem& pb);
 bool decode_short_fits(const Problem& pb);

@@ -46,6 +46,8 @@ constexpr int kMaxSmem = 227 * 1024;
 struct LongParams {
   int32_t* status;
   int l, Hkv, G, Tm, n_mt, num_tiles;
+  int C;    // keys before new token 0 (the staged cache), 0 for whole sequences
+  int f16;  // q and keys are f16 (staged), else bf16 as stored
   float scale_log2;
 };
 
@@ -86,7 +88,7 @@ struct StepWalk {
   TileWalk t;
   int i, b, nb;  // tile index, block, blocks of the tile
   __device__ static int blocks(const LongParams& prm, int mt) {
-    return (min(prm.l, (mt + 1) * prm.Tm) + kKB - 1) / kKB;
+    return (prm.C + min(prm.l, (mt + 1) * prm.Tm) + kKB - 1) / kKB;
   }
   __device__ void init(const LongParams& prm) {
     t.init(prm);
@@ -264,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc::fence_after_sync();
       if (lane == 0) {
-        const int kend = min(l, (sw.t.mt + 1) * Tm);
+        const int kend = prm.C + min(l, (sw.t.mt + 1) * Tm);
         const int N = (min(kKB, kend - sw.b * kKB) + 15) & ~15;
-        const uint32_t idesc = tc::idesc_bf16_f32(128, N, 0);
+        const uint32_t idesc = prm.f16 ? tc::idesc_f16_f32(128, N, 0) : tc::idesc_bf16_f32(128, N, 0);
         const uint32_t stage = sbase + kOffQ + (sw.i & 1) * kTile;
         const uint32_t kb = sbase + kOffK + ks * kTile;
 #pragma unroll
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc::fence_after_sync();
       if (lane == 0) {
-        const int kend = min(l, (pw.t.mt + 1) * Tm);
+        const int kend = prm.C + min(l, (pw.t.mt + 1) * Tm);
         const int N = (min(kKB, kend - pw.b * kKB) + 15) & ~15;
         const uint32_t idesc = tc::idesc_bf16_f32(128, 64, 1);
         const uint32_t vb = sbase + kOffV + vs * kTile;
@@ -384,9 +386,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
       const bool valid = row_tok < toks;
       const bool wlive = (warp & 3) * 32 < toks * G;  // warp-uniform, same for the row's partner
-      const int kend = t0 + toks;
-      const int lim = t0 + min(row_tok, toks - 1) + 1;  // keys row r sees
-      const int lim_all = t0 + 1;                          // keys every row of the tile sees
+      const int kend = prm.C + t0 + toks;
+      const int lim = prm.C + t0 + min(row_tok, toks - 1) + 1;  // keys row r sees
+      const int lim_all = prm.C + t0 + 1;                          // keys every row of the tile sees
       // chunk c (16 keys) of block b: below the diagonal for every row, or at it
       auto bias_row = [&](int key0) {
         return reinterpret_cast<const float4*>(bias + min(max(lim - key0, 0), 16) * 16);
@@ -518,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         red_sum[h * 128 + r] = (a0 + a1) + (b0 + b1);
         named_bar_sync(pair_bar, 64);
         const float sum = red_sum[r] + red_sum[128 + r];
+        if (valid && !(sum <= 3.0e38f)) report(prm.status, GIST_ATTN_STATUS_RANGE);
         const float inv = rcp_approx(sum);
         const uint32_t stage = sbase + kOffQ + (i & 1) * kTile;
 #pragma unroll
@@ -552,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// q / out: [P][l][Hq][64] as {64, 1, Hq, l, P}, boxes of G heads x Tm tokens.
+// q / out: [P][l][Hq][64] as {64, 1, Hq, l, P}, boxes of G heads x Tm tokens
+// (2-byte elements, copied as they are).
 int encode_qo(CUtensorMap* m, const void* base, const Problem& pb, int Tm) {
   const EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return GIST_ATTN_ERR_LAUNCH;
@@ -568,13 +572,13 @@ int encode_qo(CUtensorMap* m, const void* base, const Problem& pb, int Tm) {
   return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
 }
 
-// k_new / v_new: [P][l][Hkv][64] as {64, Hkv, l, P}, boxes of 128 tokens of one head.
-int encode_kv(CUtensorMap* m, const void* base, const Problem& pb) {
+// keys / values: [P][rows][Hkv][64] as {64, Hkv, rows, P}, boxes of 128 tokens of one head.
+int encode_kv(CUtensorMap* m, const void* base, const Problem& pb, int rows) {
   const EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return GIST_ATTN_ERR_LAUNCH;
-  const cuuint64_t dims[4] = {64, (cuuint64_t)pb.Hkv, (cuuint64_t)pb.l, (cuuint64_t)pb.P};
+  const cuuint64_t dims[4] = {64, (cuuint64_t)pb.Hkv, (cuuint64_t)rows, (cuuint64_t)pb.P};
   const cuuint64_t strides[3] = {(cuuint64_t)pb.d * 2, (cuuint64_t)pb.Hkv * pb.d * 2,
-                                 (cuuint64_t)pb.l * pb.Hkv * pb.d * 2};
+                                 (cuuint64_t)rows * pb.Hkv * pb.d * 2};
   const cuuint32_t box[4] = {64, 1, (cuuint32_t)kKB, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
@@ -586,15 +590,24 @@ int encode_kv(CUtensorMap* m, const void* base, const Problem& pb) {
 
 }  // namespace
 
-// Pre-rotated inputs, no cached segment, d = 64, groups of at most 128 heads,
-// sequences longer than the single-pass kernel's 128 keys.
-bool prefill_long_fits(const Problem& pb) {
-  return (pb.flags & GIST_ATTN_FLAG_PREROTATED) && pb.C == 0 && pb.d == 64 && pb.l > 128 &&
-         pb.G <= 128 && (int64_t)pb.P * pb.Hkv * ((pb.l + 128 / pb.G - 1) / (128 / pb.G)) < 0x7fffffff &&
+// The grid of row tiles fits the kernel's int counters, and its shared memory
+// fits a CTA.
+bool prefill_long_grid_ok(const Problem& pb, int rows) {
+  return pb.d == 64 && pb.G <= 128 && rows > 0 &&
+         (int64_t)pb.P * pb.Hkv * ((pb.l + 128 / pb.G - 1) / (128 / pb.G)) < 0x7fffffff &&
          kSmemBytes <= (uint32_t)kMaxSmem;
 }
 
-int launch_prefill_long(const Problem& pb, cudaStream_t stream) {
+// Pre-rotated inputs, no cached segment, d = 64, groups of at most 128 heads,
+// sequences longer than the single-pass kernel's 128 keys.
+bool prefill_long_fits(const Problem& pb) {
+  return (pb.flags & GIST_ATTN_FLAG_PREROTATED) && pb.C == 0 && pb.l > 128 && prefill_long_grid_ok(pb, pb.l);
+}
+
+// q [P][l][Hq][64], keys and values [P][C + l][Hkv][64]: new token i sees keys
+// [0, C + i]; q and keys f16 (f16 = true) or bf16.
+int launch_prefill_long_on(const Problem& pb, const void* q, const void* k, const void* v, int C,
+                           bool f16, cudaStream_t stream) {
   LongParams prm{};
   prm.status = pb.status;
   prm.l = pb.l;
@@ -603,12 +616,14 @@ int launch_prefill_long(const Problem& pb, cudaStream_t stream) {
   prm.Tm = 128 / pb.G;
   prm.n_mt = (pb.l + prm.Tm - 1) / prm.Tm;
   prm.num_tiles = (int)((int64_t)pb.P * pb.Hkv * prm.n_mt);
+  prm.C = C;
+  prm.f16 = f16 ? 1 : 0;
   prm.scale_log2 = pb.scale_log2;
   alignas(64) CUtensorMap tm_q, tm_o, tm_k, tm_v;
-  int rc = encode_qo(&tm_q, pb.q, pb, prm.Tm);
+  int rc = encode_qo(&tm_q, q, pb, prm.Tm);
   if (rc == GIST_ATTN_OK) rc = encode_qo(&tm_o, pb.out, pb, prm.Tm);
-  if (rc == GIST_ATTN_OK) rc = encode_kv(&tm_k, pb.k_new, pb);
-  if (rc == GIST_ATTN_OK) rc = encode_kv(&tm_v, pb.v_new, pb);
+  if (rc == GIST_ATTN_OK) rc = encode_kv(&tm_k, k, pb, C + pb.l);
+  if (rc == GIST_ATTN_OK) rc = encode_kv(&tm_v, v, pb, C + pb.l);
   if (rc != GIST_ATTN_OK) return rc;
   if (cudaFuncSetAttribute(prefill_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes) != cudaSuccess)
@@ -620,6 +635,10 @@ int launch_prefill_long(const Problem& pb, cudaStream_t stream) {
   const int grid = prm.num_tiles < 2 * sms ? prm.num_tiles : 2 * sms;
   prefill_long_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_o, tm_k, tm_v, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
+}
+
+int launch_prefill_long(const Problem& pb, cudaStream_t stream) {
+  return launch_prefill_long_on(pb, pb.q, pb.k_new, pb.v_new, 0, false, stream);
 }
 
 }  // namespace gattn

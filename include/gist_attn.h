@@ -120,6 +120,40 @@ int gist_attn_fwd(const void* q, const void* k_new, const void* v_new, const voi
                   void* out, const gist_attn_dims* dims, cudaStream_t stream);
 
 /*
+ * gist_attn_workspace_bytes -- device bytes of the workspace gist_attn_fwd_ws
+ * uses for these dimensions, or 0 when they run without one.  Host only.
+ * Non-zero for d = 64, n_new >= 2, cached + new keys above 128 and groups of
+ * at most 128 heads (cached blocks per pair <= 64), where the staged path
+ * applies: 2 * P * 64 * (n_new * Hq + 2 * (cached + n_new) * Hkv) bytes, each
+ * part rounded up to 256.  Invalid dims return 0.
+ */
+size_t gist_attn_workspace_bytes(const gist_attn_dims* dims);
+
+/*
+ * gist_attn_fwd_ws -- gist_attn_fwd with a caller-provided device workspace
+ * (the same definition: [Gist page, "在线的一次 attention"], K = cat(cached K,
+ * new K) with the new tokens numbered after the cached positions, causal
+ * inside the new block).  Arguments as gist_attn_fwd, plus:
+ *   workspace       device pointer, 256-byte aligned, at least
+ *                   gist_attn_workspace_bytes(dims) bytes, or NULL
+ *   workspace_bytes its size in bytes
+ * Where the workspace applies and is large enough, a pre-pass writes each
+ * pair's rotated q and its key sequence [cached; new] into it (keys and q
+ * rounded once to f16, values bf16), and the long-sequence tensor-core kernel
+ * runs on that: two launches on `stream`.  The caller owns the workspace; its
+ * contents are scratch, overwritten by every call, and must not be touched
+ * until the work on `stream` has finished.  Otherwise (no workspace, too small,
+ * misaligned, or shapes without a staged path) the call does exactly what
+ * gist_attn_fwd does.  Errors as gist_attn_fwd; a block id outside the pool
+ * zeroes that pair's rows and sets GIST_ATTN_STATUS_BAD_BLOCK, a value past the
+ * f16 range sets GIST_ATTN_STATUS_RANGE.
+ */
+int gist_attn_fwd_ws(const void* q, const void* k_new, const void* v_new, const void* kv_pool,
+                     const int32_t* item_ids, const int32_t* block_table,
+                     const int32_t* pos_offset, void* out, void* workspace, size_t workspace_bytes,
+                     const gist_attn_dims* dims, cudaStream_t stream);
+
+/*
  * gist_attn_fwd_fp8kv -- gist_attn_fwd with the cached segment stored as FP8
  * E4M3 bytes ([Suffix page, §2 and the end of §5]: a 1-byte-per-element KV
  * cache).  The pages give no scale convention; here each (block, layer, K|V,

@@ -181,3 +181,31 @@ def test_projections_reject_bad_arguments(fake_ptrs):
     bad_flags = ctypes.byref(binding.make_dims(dict(BASE, flags=4)))
     assert lib.gist_attn_fwd(V(P16), V(P16), V(P16), V(P16), V(P16), None, None, V(P16), bad_flags,
                              None) == binding.ERR_DIMS
+
+
+def _dims(**kw):
+    d = dict(num_pairs=12800, n_new=256, num_q_heads=14, num_kv_heads=2, head_dim=64, block_len=8,
+             blocks_per_pair=1, num_blocks=100000, num_layers=2, layer=0, rope_theta=1e4,
+             softmax_scale=0.0)
+    d.update(kw)
+    return d
+
+
+def test_workspace_bytes(lib):
+    """The staged path's workspace: rotated q (f16) plus the [cached; new] key and
+    value sequences of every pair, each part rounded up to 256 bytes; 0 where a
+    shape runs without one, and for invalid dimensions."""
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    for P, l, Hq, Hkv, C in [(12800, 256, 14, 2, 8), (3, 129, 7, 1, 64), (5, 200, 16, 2, 1)]:
+        d = _dims(num_pairs=P, n_new=l, num_q_heads=Hq, num_kv_heads=Hkv, block_len=C)
+        want = up(P * l * Hq * 64 * 2) + 2 * up(P * (C + l) * Hkv * 64 * 2)
+        assert binding.workspace_bytes(d) == want, (P, l, C)
+    assert binding.workspace_bytes(_dims(n_new=64)) == 0            # 72 keys: single-pass kernel
+    assert binding.workspace_bytes(_dims(n_new=1)) == 0             # decode
+    assert binding.workspace_bytes(_dims(head_dim=128)) == 0        # d = 128: streaming kernel
+    assert binding.workspace_bytes(_dims(num_pairs=0)) == 0
+    assert binding.workspace_bytes(_dims(num_kv_heads=3)) == 0      # invalid: 14 % 3
+    assert binding.workspace_bytes(_dims(block_len=0, blocks_per_pair=0, flags=1)) == 0  # pre-rotated, no cache
+    assert binding.workspace_bytes(_dims(block_len=0, blocks_per_pair=0)) > 0  # raw inputs, no cache
