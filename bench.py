@@ -75,6 +75,8 @@ def parse_args(argv=None):
                     help="measure a widening row instead of the hot path: the offline gist "
                          "compression pass, the paged decode with per-block attention mass + append, "
                          "or the gist workload over k x l (one JSON line per point)")
+    ap.add_argument("--sweep-point", default=None,
+                    help="with --row sweep: only this k:l point (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -619,8 +621,12 @@ def run_sweep(args, dev, stream, status, ws, rank, peak, peak_src):
 
     from attention_cached_kv_gb300 import binding, workloads
 
-    for l_new in (16, 64, 256):
-        for k in (1, 4, 8, 16, 32, 64):
+    points = [(k, l_new) for l_new in (16, 64, 256) for k in (1, 4, 8, 16, 32, 64)]
+    if args.sweep_point:
+        k_, l_ = (int(x) for x in args.sweep_point.split(":"))
+        points = [(k_, l_)]
+    for k, l_new in points:
+        if True:
             over = {"num_layers": 2}
             if args.queries:
                 over["queries"] = args.queries
