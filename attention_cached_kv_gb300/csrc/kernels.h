@@ -43,10 +43,10 @@ int launch_prefill(const Problem& pb, cudaStream_t stream);
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream);
 int launch_prefill_long(const Problem& pb, cudaStream_t stream);
 int launch_prefill_long_on(const Problem& pb, const void* q, const void* k, const void* v, int C,
-                           bool f16, cudaStream_t stream);
+                           bool f16, const float2* q_base, const float2* q_rel, cudaStream_t stream);
 // The staged path (stage.cu): workspace layout, fit and launch (pre-pass + long kernel).
 struct StageLayout {
-  size_t q_off, k_off, v_off, bytes;
+  size_t base_off, rel_off, k_off, v_off, bytes;
 };
 StageLayout stage_layout(const Problem& pb);
 int launch_staged(const Problem& pb, void* workspace, cudaStream_t stream);

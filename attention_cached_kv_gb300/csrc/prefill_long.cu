@@ -48,6 +48,10 @@ struct LongParams {
   int l, Hkv, G, Tm, n_mt, num_tiles;
   int C;    // keys before new token 0 (the staged cache), 0 for whole sequences
   int f16;  // q and keys are f16 (staged), else bf16 as stored
+  // q to rotate in the kernel (else null: q arrives rotated): (cos, sin) of
+  // pos_offset[p] theta_j [P][32] and of i theta_j [l][32], added per token
+  const float2* q_base;
+  const float2* q_rel;
   float scale_log2;
 };
 
@@ -116,6 +120,7 @@ constexpr uint32_t kPCol = 128, kOCol = 192, kTmemCols = 256;
 struct LBars {
   uint64_t qfull[2], kfull[2], kfree[2], vfull[2], vfree[2];
   uint64_t s_done, p_done, o_done, o_stored[2];
+  uint64_t q_ready[2];  // q rotated in its stage (when it arrives unrotated)
   uint32_t tmem_slot;
 };
 
@@ -159,6 +164,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// fp32 pair -> f16 pair (round to nearest even), first element in the low half.
+__device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t v) {
+  float a, b;
+  f2_split(v, a, b);
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -199,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&bars->vfull[s], 1);
       mbar_init(&bars->vfree[s], 1);
       mbar_init(&bars->o_stored[s], kCompute);
+      mbar_init(&bars->q_ready[s], kCompute);
     }
     mbar_init(&bars->s_done, 1);
     mbar_init(&bars->p_done, kCompute);
@@ -259,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (sw.i >= my_tiles || failed) return;
       const int ks = sx & 1;
       if (__any_sync(0xffffffffu,
-                     (sw.b == 0 && !mbar_wait(&bars->qfull[sw.i & 1], (uint32_t)(sw.i >> 1) & 1u)) ||
+                     (sw.b == 0 && !mbar_wait(prm.q_base ? &bars->q_ready[sw.i & 1] : &bars->qfull[sw.i & 1],
+                                              (uint32_t)(sw.i >> 1) & 1u)) ||
                          !mbar_wait(&bars->kfull[ks], (uint32_t)(sx >> 1) & 1u))) {
         failed = true;
         return;
@@ -377,9 +392,45 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!failed && !mbar_wait(bar, parity)) failed = true;
     };
     const float sc = prm.scale_log2;
+    // q that arrives unrotated: each thread rotates frequencies [16 h, 16 h + 16)
+    // of its row (elements j and j + 32) in the stage and rounds once to f16; the
+    // angle is the pair's base plus the token's index angle.  Tile i + 1's q is
+    // rotated once tile i's last P is in TMEM, while its P V runs.
+    auto rotate_q = [&](int qi, const TileWalk& qt) {
+      if (!prm.q_base || qi >= my_tiles) return;
+      wait(&bars->qfull[qi & 1], (uint32_t)(qi >> 1) & 1u);
+      const int tq = qt.mt * Tm + row_tok;
+      if (row_tok < min(Tm, l - qt.mt * Tm) && !failed) {
+        const uint32_t stage = sbase + kOffQ + (qi & 1) * kTile;
+        const float4* bs = reinterpret_cast<const float4*>(prm.q_base + (size_t)qt.p * 32 + 16 * h);
+        const float4* rl = reinterpret_cast<const float4*>(prm.q_rel + (size_t)tq * 32 + 16 * h);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t ax = stage + swz128(r, 2 * h + cc), ay = stage + swz128(r, 4 + 2 * h + cc);
+          const uint4 xv = lds16(ax), yv = lds16(ay);
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, yw[4] = {yv.x, yv.y, yv.z, yv.w};
+          uint32_t ox[4], oy[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {  // frequencies 16 h + 8 cc + 2 e, + 1
+            const float4 b4 = __ldg(bs + 4 * cc + e), r4 = __ldg(rl + 4 * cc + e);
+            const float c0 = b4.x * r4.x - b4.y * r4.y, s0 = b4.y * r4.x + b4.x * r4.y;
+            const float c1 = b4.z * r4.z - b4.w * r4.w, s1 = b4.w * r4.z + b4.z * r4.w;
+            const float x0 = __uint_as_float(xw[e] << 16), x1 = __uint_as_float(xw[e] & 0xffff0000u);
+            const float y0 = __uint_as_float(yw[e] << 16), y1 = __uint_as_float(yw[e] & 0xffff0000u);
+            ox[e] = f2_to_f16x2(f2_make(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1));
+            oy[e] = f2_to_f16x2(f2_make(y0 * c0 + x0 * s0, y1 * c1 + x1 * s1));
+          }
+          sts16(ax, make_uint4(ox[0], ox[1], ox[2], ox[3]));
+          sts16(ay, make_uint4(oy[0], oy[1], oy[2], oy[3]));
+        }
+      }
+      fence_proxy_async_smem();  // the tensor core reads the stage next
+      mbar_arrive(&bars->q_ready[qi & 1]);
+    };
     int sx = 0;
     TileWalk tw;
     tw.init(prm);
+    rotate_q(0, tw);
     for (int i = 0; i < my_tiles; ++i, tw.next(prm)) {
       const int mt = tw.mt;
       const int nb = StepWalk::blocks(prm, mt);
@@ -510,6 +561,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_arrive(&bars->p_done);  // P in TMEM, and S read: the next S may go
         ++sx;
       }
+      if (prm.q_base) {  // tile i + 1's q, while this tile's last P V runs
+        TileWalk nt = tw;
+        nt.next(prm);
+        rotate_q(i + 1, nt);
+      }
       // ---- O of row r, this half's 32 columns, normalised into the stage
       wait(&bars->o_done, (uint32_t)i & 1u);
       tc::fence_after_sync();
@@ -607,7 +663,7 @@ bool prefill_long_fits(const Problem& pb) {
 // q [P][l][Hq][64], keys and values [P][C + l][Hkv][64]: new token i sees keys
 // [0, C + i]; q and keys f16 (f16 = true) or bf16.
 int launch_prefill_long_on(const Problem& pb, const void* q, const void* k, const void* v, int C,
-                           bool f16, cudaStream_t stream) {
+                           bool f16, const float2* q_base, const float2* q_rel, cudaStream_t stream) {
   LongParams prm{};
   prm.status = pb.status;
   prm.l = pb.l;
@@ -618,6 +674,8 @@ int launch_prefill_long_on(const Problem& pb, const void* q, const void* k, cons
   prm.num_tiles = (int)((int64_t)pb.P * pb.Hkv * prm.n_mt);
   prm.C = C;
   prm.f16 = f16 ? 1 : 0;
+  prm.q_base = q_base;
+  prm.q_rel = q_rel;
   prm.scale_log2 = pb.scale_log2;
   alignas(64) CUtensorMap tm_q, tm_o, tm_k, tm_v;
   int rc = encode_qo(&tm_q, q, pb, prm.Tm);
@@ -638,7 +696,7 @@ int launch_prefill_long_on(const Problem& pb, const void* q, const void* k, cons
 }
 
 int launch_prefill_long(const Problem& pb, cudaStream_t stream) {
-  return launch_prefill_long_on(pb, pb.q, pb.k_new, pb.v_new, 0, false, stream);
+  return launch_prefill_long_on(pb, pb.q, pb.k_new, pb.v_new, 0, false, nullptr, nullptr, stream);
 }
 
 }  // namespace gattn

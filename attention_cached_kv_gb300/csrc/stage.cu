@@ -1,18 +1,19 @@
 // stage.cu -- the staged path for long new blocks behind a cached segment
-// (more than 128 keys, d = 64): a pre-pass writes each pair's rotated q and its
-// whole key sequence [cached; new] into a caller-provided workspace, then the
-// long-sequence tensor-core kernel runs on it.
+// (more than 128 keys, d = 64): a pre-pass writes each pair's whole key sequence
+// [cached; new] and the rotation angles of q into a caller-provided workspace,
+// then the long-sequence tensor-core kernel runs on it, rotating q as it loads.
 //
 // [Gist page, "在线的一次 attention"]: K = cat(cache[item].K[layer], K_new),
 // V likewise, the new tokens numbered after the cached positions, causal inside
 // the new block.  The pre-pass writes exactly that concatenation, per pair:
-//   qw [P][l][Hq][64]        f16, q rotated at pos_offset + i
 //   kw [P][C + l][Hkv][64]   f16, the cached keys as stored (already rotated by
 //                            their producer), then the new keys rotated
 //   vw [P][C + l][Hkv][64]   bf16, the cached values, then v_new
 // so that every key block of the attention is one TMA box and each key is
-// rotated once per call, not once per row tile that reads it.  Rotated q and
-// keys are rounded once to f16 (cached bf16 keys convert exactly), as in the
+// rotated once per call, not once per row tile that reads it; and the angles
+// of q: (cos, sin)(pos_offset[p] theta_j) per pair and (cos, sin)(i theta_j)
+// per new-token index, which the attention kernel adds.  Rotated q and keys are
+// rounded once to f16 (cached bf16 keys convert exactly), as in the
 // single-pass tensor-core kernel.  A pair with a block id outside the pool gets
 // zero values, so its output rows come out exactly 0, and the status word says
 // so.
@@ -42,7 +43,8 @@ struct StageParams {
   PoolView pv;
   const int32_t* pos_offset;
   int32_t* status;
-  uint16_t* qw;  // f16 bits
+  float2* base;  // [P][32]: (cos, sin) of pos_offset[p] theta_j
+  float2* rel;   // [l][32]: (cos, sin) of i theta_j
   uint16_t* kw;  // f16 bits
   bf16* vw;
   int l, Hq, Hkv, C;
@@ -121,8 +123,23 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(const __grid_constant__
     stg16(prm.vw + o, v);
   }
 
-  // new tokens, kTabRows at a time
+  // the angles of q: this pair's base, and the rows i = p, p + P, ... of the
+  // per-index table
   const int pos0 = prm.pos_offset ? prm.pos_offset[p] : C;
+  if (tid < 32) {
+    float s, c;
+    sincosf((float)pos0 * prm.inv_freq[tid], &s, &c);
+    prm.base[(size_t)p * 32 + tid] = make_float2(c, s);
+  }
+  if (tid < 32) {
+    for (int t = (int)blockIdx.x; t < l; t += (int)gridDim.x) {
+      float s, c;
+      sincosf((float)t * prm.inv_freq[tid], &s, &c);
+      prm.rel[(size_t)t * 32 + tid] = make_float2(c, s);
+    }
+  }
+
+  // new keys, kTabRows at a time
   for (int t0 = 0; t0 < l; t0 += kTabRows) {
     const int nt = min(kTabRows, l - t0);
     __syncthreads();  // the previous table is no longer read
@@ -134,11 +151,6 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(const __grid_constant__
       tab[idx] = make_float4(c0, c1, s0, s1);
     }
     __syncthreads();
-    for (int idx = tid; idx < nt * Hq * 4; idx += kThreads) {
-      const int c = idx & 3, h = (idx >> 2) % Hq, t = (idx >> 2) / Hq;
-      const size_t row = ((size_t)p * l + t0 + t) * Hq + h;
-      rotate_store(prm.q + row * kD, prm.qw + row * kD, tab + t * 16, c);
-    }
     for (int idx = tid; idx < nt * Hkv * 4; idx += kThreads) {
       const int c = idx & 3, g = (idx >> 2) % Hkv, t = (idx >> 2) / Hkv;
       const size_t src = ((size_t)p * l + t0 + t) * Hkv + g;
@@ -163,10 +175,10 @@ StageLayout stage_layout(const Problem& pb) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   StageLayout L{};
   const size_t rows = (size_t)pb.C + pb.l;
-  const size_t q_bytes = (size_t)pb.P * pb.l * pb.Hq * 64 * 2;
   const size_t kv_bytes = (size_t)pb.P * rows * pb.Hkv * 64 * 2;
-  L.q_off = 0;
-  L.k_off = up(q_bytes);
+  L.base_off = 0;
+  L.rel_off = up((size_t)pb.P * 32 * 8);
+  L.k_off = L.rel_off + up((size_t)pb.l * 32 * 8);
   L.v_off = L.k_off + up(kv_bytes);
   L.bytes = L.v_off + up(kv_bytes);
   return L;
@@ -189,7 +201,8 @@ int launch_staged(const Problem& pb, void* workspace, cudaStream_t stream) {
                     pb.blocks_per_pair, pb.block_len, pb.num_blocks, pb.L, pb.layer, pb.Hkv, 64};
   prm.pos_offset = pb.pos_offset;
   prm.status = pb.status;
-  prm.qw = reinterpret_cast<uint16_t*>(ws + L.q_off);
+  prm.base = reinterpret_cast<float2*>(ws + L.base_off);
+  prm.rel = reinterpret_cast<float2*>(ws + L.rel_off);
   prm.kw = reinterpret_cast<uint16_t*>(ws + L.k_off);
   prm.vw = reinterpret_cast<bf16*>(ws + L.v_off);
   prm.l = pb.l;
@@ -199,7 +212,9 @@ int launch_staged(const Problem& pb, void* workspace, cudaStream_t stream) {
   for (int j = 0; j < 32; ++j) prm.inv_freq[j] = pb.inv_freq[j];
   stage_kernel<<<pb.P, kThreads, 0, stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return GIST_ATTN_ERR_LAUNCH;
-  return launch_prefill_long_on(pb, ws + L.q_off, ws + L.k_off, ws + L.v_off, pb.C, true, stream);
+  return launch_prefill_long_on(pb, pb.q, ws + L.k_off, ws + L.v_off, pb.C, true,
+                                reinterpret_cast<const float2*>(ws + L.base_off),
+                                reinterpret_cast<const float2*>(ws + L.rel_off), stream);
 }
 
 }  // namespace gattn

@@ -124,8 +124,8 @@ int gist_attn_fwd(const void* q, const void* k_new, const void* v_new, const voi
  * uses for these dimensions, or 0 when they run without one.  Host only.
  * Non-zero for d = 64, n_new >= 2, cached + new keys above 128 and groups of
  * at most 128 heads (cached blocks per pair <= 64), where the staged path
- * applies: 2 * P * 64 * (n_new * Hq + 2 * (cached + n_new) * Hkv) bytes, each
- * part rounded up to 256.  Invalid dims return 0.
+ * applies: 256 * P + 256 * n_new + 2 * (2 * P * (cached + n_new) * Hkv * 64)
+ * bytes, each of the four parts rounded up to 256.  Invalid dims return 0.
  */
 size_t gist_attn_workspace_bytes(const gist_attn_dims* dims);
 
@@ -138,9 +138,10 @@ size_t gist_attn_workspace_bytes(const gist_attn_dims* dims);
  *                   gist_attn_workspace_bytes(dims) bytes, or NULL
  *   workspace_bytes its size in bytes
  * Where the workspace applies and is large enough, a pre-pass writes each
- * pair's rotated q and its key sequence [cached; new] into it (keys and q
- * rounded once to f16, values bf16), and the long-sequence tensor-core kernel
- * runs on that: two launches on `stream`.  The caller owns the workspace; its
+ * pair's key sequence [cached; new] into it (keys rotated and rounded once to
+ * f16, values bf16) with the rotation angles of q, and the long-sequence
+ * tensor-core kernel runs on that, rotating q (rounded once to f16) as it
+ * loads each tile: two launches on `stream`.  The caller owns the workspace; its
  * contents are scratch, overwritten by every call, and must not be touched
  * until the work on `stream` has finished.  Otherwise (no workspace, too small,
  * misaligned, or shapes without a staged path) the call does exactly what

@@ -192,15 +192,16 @@ def _dims(**kw):
 
 
 def test_workspace_bytes(lib):
-    """The staged path's workspace: rotated q (f16) plus the [cached; new] key and
-    value sequences of every pair, each part rounded up to 256 bytes; 0 where a
-    shape runs without one, and for invalid dimensions."""
+    """The staged path's workspace: the angles of q (a (cos, sin) pair per
+    frequency for every pair and every new-token index) plus the [cached; new]
+    key and value sequences of every pair, each part rounded up to 256 bytes; 0
+    where a shape runs without one, and for invalid dimensions."""
     def up(x):
         return (x + 255) // 256 * 256
 
     for P, l, Hq, Hkv, C in [(12800, 256, 14, 2, 8), (3, 129, 7, 1, 64), (5, 200, 16, 2, 1)]:
         d = _dims(num_pairs=P, n_new=l, num_q_heads=Hq, num_kv_heads=Hkv, block_len=C)
-        want = up(P * l * Hq * 64 * 2) + 2 * up(P * (C + l) * Hkv * 64 * 2)
+        want = up(P * 32 * 8) + up(l * 32 * 8) + 2 * up(P * (C + l) * Hkv * 64 * 2)
         assert binding.workspace_bytes(d) == want, (P, l, C)
     assert binding.workspace_bytes(_dims(n_new=64)) == 0            # 72 keys: single-pass kernel
     assert binding.workspace_bytes(_dims(n_new=1)) == 0             # decode
