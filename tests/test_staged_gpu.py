@@ -1,9 +1,10 @@
 """GPU parity of the staged path (gist_attn_fwd_ws): more than 128 keys on
 d = 64 with a cached segment in front, or a whole sequence on pre-RoPE inputs.
-A pre-pass writes each pair's rotated q and its [cached; new] key sequence into
-the caller's workspace, then the long-sequence tensor-core kernel runs on it
-([Gist page, "在线的一次 attention"]: K = cat(cache[item].K[layer], K_new), the
-new tokens numbered after the cached positions, causal inside the new block).
+A pre-pass writes each pair's [cached; new] key sequence (keys rotated) and the
+angles of q into the caller's workspace, then the long-sequence tensor-core
+kernel runs on it and rotates q itself ([Gist page, "在线的一次 attention"]:
+K = cat(cache[item].K[layer], K_new), the new tokens numbered after the cached
+positions, causal inside the new block).
 Every case is checked element by element against the float64 oracle."""
 from __future__ import annotations
 
@@ -118,3 +119,21 @@ def test_sweep_point_l256_full_size_sampled():
     assert torch.isfinite(got.float()).all()
     del wl, got
     torch.cuda.empty_cache()
+
+
+def test_staged_prerotated_inputs_with_a_cache():
+    """Pre-rotated q and k_new (GIST_ATTN_FLAG_PREROTATED) behind a cache: the
+    pre-pass only converts (every angle is 0) and the result is the oracle's
+    prerotated attention."""
+    wl = workloads.make_custom(3, 210, 14, 2, 64, 16, 1, 5, device=DEV, seed=12, random_pos=True)
+    dims = dict(wl.dims, flags=binding.FLAG_PREROTATED)
+    n = binding.workspace_bytes(dims)
+    assert n > 0
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_ws(wl.q, wl.k_new, wl.v_new, wl.kv_pool, wl.item_ids, None, wl.pos_offset,
+                                   None, ws, dims=dims, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    wl.dims = dims
+    compare(got, oracle_ref(wl), "staged, pre-rotated inputs")
