@@ -18,9 +18,9 @@
 // zero values, so its output rows come out exactly 0, and the status word says
 // so.
 //
-// One CTA per pair.  Angles: fp32 sincos of (position x frequency) for up to
-// 128 tokens at a time into shared memory, (cos_j, cos_j+1, sin_j, sin_j+1) per
-// frequency pair.
+// One CTA per pair.  Angles: fp32 sincos of (position x frequency); those of
+// the new keys for up to 128 tokens at a time in shared memory, (cos_j,
+// cos_j+1, sin_j, sin_j+1) per frequency pair.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
 #include <math.h>
@@ -37,7 +37,6 @@ constexpr int kMaxStageBlocks = 64;  // cached blocks per pair
 constexpr int kD = 64;
 
 struct StageParams {
-  const bf16* q;
   const bf16* k_new;
   const bf16* v_new;
   PoolView pv;
@@ -47,7 +46,7 @@ struct StageParams {
   float2* rel;   // [l][32]: (cos, sin) of i theta_j
   uint16_t* kw;  // f16 bits
   bf16* vw;
-  int l, Hq, Hkv, C;
+  int l, Hkv, C;
   float inv_freq[32];
 };
 
@@ -87,7 +86,7 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(const __grid_constant__
   __shared__ float4 tab[kTabRows * 16];
   __shared__ int32_t ids[kMaxStageBlocks];
   const int tid = threadIdx.x, p = blockIdx.x;
-  const int l = prm.l, Hq = prm.Hq, Hkv = prm.Hkv, C = prm.C, rows = C + l;
+  const int l = prm.l, Hkv = prm.Hkv, C = prm.C, rows = C + l;
   const int bpp = prm.pv.blocks_per_pair;
 
   bool bad = false;
@@ -194,7 +193,6 @@ int launch_staged(const Problem& pb, void* workspace, cudaStream_t stream) {
   const StageLayout L = stage_layout(pb);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   StageParams prm{};
-  prm.q = static_cast<const bf16*>(pb.q);
   prm.k_new = static_cast<const bf16*>(pb.k_new);
   prm.v_new = static_cast<const bf16*>(pb.v_new);
   prm.pv = PoolView{static_cast<const bf16*>(pb.kv_pool), pb.item_ids, pb.block_table,
@@ -206,7 +204,6 @@ int launch_staged(const Problem& pb, void* workspace, cudaStream_t stream) {
   prm.kw = reinterpret_cast<uint16_t*>(ws + L.k_off);
   prm.vw = reinterpret_cast<bf16*>(ws + L.v_off);
   prm.l = pb.l;
-  prm.Hq = pb.Hq;
   prm.Hkv = pb.Hkv;
   prm.C = pb.C;
   for (int j = 0; j < 32; ++j) prm.inv_freq[j] = pb.inv_freq[j];
