@@ -1,18 +1,21 @@
-// prefill_long.cu -- causal attention over whole pre-rotated sequences (no
-// cached segment, l up to thousands of tokens) on the 5th-generation tensor
-// core: the offline gist compression pass in the fused pipeline.
+// prefill_long.cu -- causal attention of long new blocks (l up to thousands of
+// tokens) over key sequences streamed by TMA, on the 5th-generation tensor core.
 //
 // [Gist page, "论文做了什么" and "在线的一次 attention"]: the item is forwarded
 // once, offline: [prompt; gist] through every layer, plain causal attention
 // over the whole sequence (the gist mask only hides the prompt from tokens
 // after the gist, and there are none in this pass); each layer's K/V at the
-// gist positions is then stored (gist_kv_store).  Here q and k_new arrive
-// rotated by the QKV projection's epilogue (GIST_ATTN_FLAG_PREROTATED), so the
-// kernel streams them as stored.
+// gist positions is then stored (gist_kv_store).  Two modes:
+//   * q and k_new arrive rotated by the QKV projection's epilogue
+//     (GIST_ATTN_FLAG_PREROTATED), no cache: the kernel streams them as stored
+//     (bf16 scores);
+//   * the staged path (stage.cu): keys and values are a pair's [cached; new]
+//     sequence prepared in a workspace, token i sees keys [0, C + i], and the
+//     softmax warps rotate q in its stage as it arrives (f16 scores).
 //
 // A work item is a 128-row tile of one (pair, KV head): floor(128 / G) whole
 // tokens x G heads, token-major (the memory order of q/out).  Its keys are the
-// tokens before its last one, in blocks of 128, one pass: per block S = q K^T
+// keys up to its last token's, in blocks of 128, one pass: per block S = q K^T
 // into TMEM, the block's row maxima, P = exp2((S - m) scale) as bf16 into TMEM
 // with m the running maximum, O += P V.  m moves only when a block's maximum
 // exceeds it by more than 8 (log2 units); then the row's O and sum are scaled
