@@ -136,6 +136,14 @@ __device__ __forceinline__ void rope_chunk(const uint4& x, const uint4& y, const
   }
 }
 
+// A shared store ordered only against the other volatile shared accesses
+// (lds16 / sts16 / barriers), not against plain C++ loads: for stores whose
+// target no plain load in the same stretch of code reads.
+__device__ __forceinline__ void sts16_ordered(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w));
+}
+
 // fp32 pair -> f16 pair, round to nearest even (|x| >= 65520 gives inf)
 __device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t v) {
   float a, b;
@@ -476,17 +484,26 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       }
       constexpr int JH = CPR / 4;  // chunk pairs per half
       const uint8_t* trow = tab + (t0 + tt) * prm.tab_stride;
+      // All of this thread's chunks are read before the first store, and the
+      // stores leave the table reads free to move, so one shared-memory round
+      // trip covers the whole row half.
+      uint4 xs[JH], ys[JH];
+#pragma unroll
+      for (int jj = 0; jj < JH; ++jj) {
+        xs[jj] = lds16(chunk_addr(stage, kPanel, r, h * JH + jj));
+        ys[jj] = lds16(chunk_addr(stage, kPanel, r, h * JH + jj + CPR / 2));
+      }
 #pragma unroll
       for (int jj = 0; jj < JH; ++jj) {
         const int J = h * JH + jj;
-        const uint32_t a0 = chunk_addr(stage, kPanel, r, J);
-        const uint32_t a1 = chunk_addr(stage, kPanel, r, J + CPR / 2);
         uint64_t xr[4], yr[4];
-        rope_chunk(lds16(a0), lds16(a1), trow, 8 * J, xr, yr);
-        sts16(a0, make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]), f2_to_f16x2(xr[2]),
-                             f2_to_f16x2(xr[3])));
-        sts16(a1, make_uint4(f2_to_f16x2(yr[0]), f2_to_f16x2(yr[1]), f2_to_f16x2(yr[2]),
-                             f2_to_f16x2(yr[3])));
+        rope_chunk(xs[jj], ys[jj], trow, 8 * J, xr, yr);
+        sts16_ordered(chunk_addr(stage, kPanel, r, J),
+                      make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]), f2_to_f16x2(xr[2]),
+                                 f2_to_f16x2(xr[3])));
+        sts16_ordered(chunk_addr(stage, kPanel, r, J + CPR / 2),
+                      make_uint4(f2_to_f16x2(yr[0]), f2_to_f16x2(yr[1]), f2_to_f16x2(yr[2]),
+                                 f2_to_f16x2(yr[3])));
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
