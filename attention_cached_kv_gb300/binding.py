@@ -16,11 +16,12 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libgistattn.so")
 
-OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH = 0, -1, -2, -3, -4, -5
+OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH, ERR_SCRATCH = 0, -1, -2, -3, -4, -5, -6
+NOALLOC_SCRATCH_BYTES = 64 << 20  # GIST_ATTN_NOALLOC_SCRATCH_BYTES
 STATUS_BAD_BLOCK, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4
 FLAG_PREROTATED = 1
 
-EXPORTS = ("gist_attn_fwd", "gist_attn_workspace_bytes", "gist_attn_fwd_ws", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
+EXPORTS = ("gist_attn_fwd", "gist_attn_workspace_bytes", "gist_attn_fwd_ws", "gist_attn_fwd_noalloc", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
            "gist_attn_fwd_gist_mask", "gist_kv_store", "gist_qkv_rope", "gist_out_proj",
            "gist_attn_gather_debug", "gist_kv_bytes_per_position", "gist_kv_bytes_per_item",
            "gist_kv_bytes_batch", "gist_attn_status_string")
@@ -74,6 +75,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.gist_attn_fwd_ws.restype = ctypes.c_int
             lib.gist_attn_fwd_ws.argtypes = [V, V, V, V, V, V, V, V, V, ctypes.c_size_t,
                                              ctypes.POINTER(Dims), V]
+            lib.gist_attn_fwd_noalloc.restype = ctypes.c_int
+            lib.gist_attn_fwd_noalloc.argtypes = [V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_attn_fwd_fp8kv.restype = ctypes.c_int
             lib.gist_attn_fwd_fp8kv.argtypes = [V, V, V, V, V, V, V, V, V, ctypes.POINTER(Dims), V]
             lib.gist_attn_fwd_block_mass.restype = ctypes.c_int
@@ -190,6 +193,28 @@ def gist_attn_fwd_ws(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, 
                               _ptr(block_table, i32, "block_table"),
                               _ptr(pos_offset, i32, "pos_offset"), _ptr(out, bf, "out"), ws_ptr,
                               ws_bytes, ctypes.byref(D), _stream(stream))
+    _raise(rc)
+    return out
+
+
+def gist_attn_fwd_noalloc(q, k_new, v_new, kv_pool, item_ids=None, block_table=None,
+                          pos_offset=None, out=None, *, dims: dict,
+                          status: torch.Tensor | None = None, stream=None):
+    """gist_attn_fwd_ws for callers that cannot allocate: the scratch is the
+    library's fixed device array (NOALLOC_SCRATCH_BYTES), so no workspace is
+    passed.  `out` must be given by such a caller (None allocates it here, for
+    convenience only).  Returns `out`."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(q)
+    bf, i32 = torch.bfloat16, torch.int32
+    D = make_dims(dims, status)
+    rc = lib.gist_attn_fwd_noalloc(_ptr(q, bf, "q"), _ptr(k_new, bf, "k_new"),
+                                   _ptr(v_new, bf, "v_new"), _ptr(kv_pool, bf, "kv_pool"),
+                                   _ptr(item_ids, i32, "item_ids"),
+                                   _ptr(block_table, i32, "block_table"),
+                                   _ptr(pos_offset, i32, "pos_offset"), _ptr(out, bf, "out"),
+                                   ctypes.byref(D), _stream(stream))
     _raise(rc)
     return out
 

@@ -386,6 +386,8 @@ extern "C" const char* gist_attn_status_string(int status) {
     case GIST_ATTN_ERR_UNSUPPORTED: return "unsupported head_dim, group size or problem size";
     case GIST_ATTN_ERR_ALIGN: return "a pointer is not aligned as required";
     case GIST_ATTN_ERR_LAUNCH: return "the CUDA launch failed";
+    case GIST_ATTN_ERR_SCRATCH:
+      return "the call needs more scratch than the library's fixed no-allocation array holds";
     case GIST_ATTN_STATUS_BAD_BLOCK: return "device: a block id was out of range (pair zeroed)";
     case GIST_ATTN_STATUS_TIMEOUT: return "device: a bounded wait on an asynchronous copy gave up";
     case GIST_ATTN_STATUS_BAD_BLOCK | GIST_ATTN_STATUS_TIMEOUT:

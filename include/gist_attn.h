@@ -24,7 +24,8 @@
  *
  * Conventions for every entry point:
  *   - Ownership: the caller owns every buffer.  No entry point allocates
- *     memory or keeps state between calls; calls are thread-safe.
+ *     memory or keeps state between calls; calls are thread-safe.  (The one
+ *     exception, gist_attn_fwd_noalloc, keeps a fixed scratch array of its own.)
  *   - Asynchrony: work is enqueued on `stream` (0 = legacy default stream);
  *     no entry point synchronises the host.
  *   - Pointers are device pointers unless marked "host".  bf16 buffers must be
@@ -53,6 +54,8 @@ extern "C" {
 #define GIST_ATTN_ERR_UNSUPPORTED (-3) /* head_dim / group / sizes this build can't run */
 #define GIST_ATTN_ERR_ALIGN (-4)       /* a pointer is not aligned as required          */
 #define GIST_ATTN_ERR_LAUNCH (-5)      /* the CUDA launch itself failed                 */
+#define GIST_ATTN_ERR_SCRATCH (-6)     /* gist_attn_fwd_noalloc: the call needs more
+                                          scratch than the library's fixed array holds */
 
 /* Device status bits (OR-ed into *dims->status). */
 #define GIST_ATTN_STATUS_BAD_BLOCK 1 /* a block id was outside [0, num_blocks): that
@@ -153,6 +156,36 @@ int gist_attn_fwd_ws(const void* q, const void* k_new, const void* v_new, const 
                      const int32_t* item_ids, const int32_t* block_table,
                      const int32_t* pos_offset, void* out, void* workspace, size_t workspace_bytes,
                      const gist_attn_dims* dims, cudaStream_t stream);
+
+/*
+ * gist_attn_fwd_noalloc -- gist_attn_fwd_ws without a caller workspace and
+ * without any allocation.  The paper has no counterpart: this entry point is
+ * for callers that cannot allocate device memory where they call the
+ * attention -- a plugin inside a host program that owns all device memory and
+ * gives its kernels no workspace, or a latency-critical loop that must not pay
+ * the implicit device synchronisation of cudaMalloc / cudaFree.
+ *
+ * Arguments, result and errors as gist_attn_fwd.  Where gist_attn_fwd_ws would
+ * take its staged path, the scratch it needs lives in a fixed device array of
+ * GIST_ATTN_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, reserved on every
+ * device that loads the library's device code until the process exits; calls
+ * whose gist_attn_workspace_bytes(dims) exceeds it return GIST_ATTN_ERR_SCRATCH
+ * and launch nothing.  Shapes without a staged path need no scratch and run
+ * exactly as gist_attn_fwd.  No call allocates or frees memory.
+ *   - Set-up: the first call on a device that needs scratch looks up the
+ *     array's device address (cudaGetSymbolAddress, with the caller's current
+ *     device, which must be the device of `stream`); GIST_ATTN_ERR_LAUNCH if
+ *     that fails.  Make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, and it keeps the
+ *     previous call's contents; each call writes every scratch byte it reads,
+ *     so nothing has to start at zero.  Calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race on the array: order them.
+ */
+#define GIST_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int gist_attn_fwd_noalloc(const void* q, const void* k_new, const void* v_new,
+                          const void* kv_pool, const int32_t* item_ids,
+                          const int32_t* block_table, const int32_t* pos_offset, void* out,
+                          const gist_attn_dims* dims, cudaStream_t stream);
 
 /*
  * gist_attn_fwd_fp8kv -- gist_attn_fwd with the cached segment stored as FP8
