@@ -393,7 +393,7 @@ extern "C" const char* gist_attn_status_string(int status) {
     case GIST_ATTN_STATUS_BAD_BLOCK | GIST_ATTN_STATUS_TIMEOUT:
       return "device: out-of-range block id and a timed-out wait";
     case GIST_ATTN_STATUS_RANGE:
-      return "device: a query or key value beyond the f16 range made a softmax row non-finite";
+      return "device: a softmax row was not finite in fp32 (a NaN input or values near the fp32 limit)";
     default: return status < 0 ? "unknown error" : "unknown device status bits";
   }
 }

@@ -314,6 +314,19 @@ __device__ __forceinline__ const bf16* pool_row(const PoolView& v, int32_t blk, 
   return v.pool + r * v.head_dim;
 }
 
+// ------------------------------------------------------------ RoPE angle ---
+// pos * theta reduced to [-pi, pi]: the product is formed in double (one
+// rounding, at most 2^-53 |pos theta| off) and 2 pi is subtracted in two parts
+// (the double nearest 2 pi and the remainder), so the angle stays accurate for
+// every int32 position; an fp32 product drifts by about |pos theta| 2^-24.
+__device__ __forceinline__ float rope_reduce(long long pos, double theta) {
+  const double a = (double)pos * theta;
+  const double k = rint(a * 0.15915494309189535);  // 1 / (2 pi)
+  double r = fma(-k, 6.283185307179586, a);         // 2 pi rounded to double
+  r = fma(-k, 2.4492935982947064e-16, r);           // 2 pi minus that
+  return (float)r;
+}
+
 __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -40,7 +40,7 @@ struct DecodeParams {
   int32_t* status;
   int Hq, Hkv, G, C;
   float scale_log2;
-  float inv_freq[64];
+  double theta[64];  // RoPE frequencies (angles reduced in double)
 };
 
 // shared memory: ids[bpp] | q_s[G][D] | kn_s[D] | vn_s[D] | red_m[W][G] | red_l[W][G] | red_o[W][G][D]
@@ -81,14 +81,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     ids[b] = blk;
   }
   // rotated, pre-scaled queries of the group; rotated new key; new value
-  const float pos = (float)(prm.pos_offset ? prm.pos_offset[p] : C);
+  const long long pos = prm.pos_offset ? prm.pos_offset[p] : C;
   for (int idx = tid; idx < (G + 1) * HALF; idx += kThreads) {
     const int h = idx / HALF, j = idx - h * HALF;  // h == G: the new key
     const bf16* src = h < G ? prm.q + ((int64_t)p * prm.Hq + g * G + h) * D
                             : prm.k_new + ((int64_t)p * prm.Hkv + g) * D;
     const float x = __bfloat162float(src[j]), y = __bfloat162float(src[j + HALF]);
     float s, c;
-    sincosf(pos * prm.inv_freq[j], &s, &c);
+    sincosf(rope_reduce(pos, prm.theta[j]), &s, &c);
     const float sc = h < G ? prm.scale_log2 : 1.f;
     float* dst = h < G ? q_s + h * D : kn_s;
     dst[j] = (x * c - y * s) * sc;
@@ -249,7 +249,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.G = pb.G;
   prm.C = pb.C;
   prm.scale_log2 = pb.scale_log2;
-  for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  for (int j = 0; j < 64; ++j) prm.theta[j] = pb.inv_freq_d[j];
   if (bytes > 48 * 1024 &&
       cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)bytes) != cudaSuccess)

@@ -61,7 +61,7 @@ struct LongParams {
   int32_t* status;
   int Hq, Hkv, C;
   float scale_log2;
-  float inv_freq[64];
+  double theta[64];  // RoPE frequencies (angles reduced in double)
 };
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -127,14 +127,14 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
     fence_mbar_init();
   }
   // rotated query (pre-scaled to log2 units), rotated new key, new value
-  const float pos = (float)(prm.pos_offset ? prm.pos_offset[p] : C);
+  const long long pos = prm.pos_offset ? prm.pos_offset[p] : C;
   for (int idx = tid; idx < 2 * HALF; idx += kThreads) {
     const int which = idx / HALF, j = idx - which * HALF;  // 0: q, 1: k_new
     const bf16* src = which == 0 ? prm.q + ((int64_t)p * prm.Hq + g) * D
                                  : prm.k_new + ((int64_t)p * prm.Hkv + g) * D;
     const float x = __bfloat162float(src[j]), y = __bfloat162float(src[j + HALF]);
     float s, c;
-    sincosf(pos * prm.inv_freq[j], &s, &c);
+    sincosf(rope_reduce(pos, prm.theta[j]), &s, &c);
     const float sc = which == 0 ? prm.scale_log2 : 1.f;
     float* dst = which == 0 ? qs : kn;
     dst[j] = (x * c - y * s) * sc;
@@ -457,7 +457,7 @@ int launch_d(const Problem& pb, const float* kv_scale, float* block_mass, cudaSt
   prm.Hkv = pb.Hkv;
   prm.C = pb.C;
   prm.scale_log2 = pb.scale_log2;
-  for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  for (int j = 0; j < 64; ++j) prm.theta[j] = pb.inv_freq_d[j];
   const int64_t grid = (int64_t)pb.P * pb.Hkv;
   if (grid > 0x7fffffff) return GIST_ATTN_ERR_UNSUPPORTED;
   decode_long_kernel<D, FP8, STATS><<<(unsigned)grid, kThreads, 0, stream>>>(prm);

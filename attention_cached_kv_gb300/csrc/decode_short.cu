@@ -47,7 +47,7 @@ struct ShortParams {
   uint32_t region;  // bytes of one warp's shared memory
   int units;        // P * Hkv (below 2^31)
   float scale_log2;
-  float inv_freq[64];
+  double theta[64];  // RoPE frequencies (angles reduced in double)
 };
 
 // One warp's shared memory: two buffers, each with the K panels then the V
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
 #pragma unroll
     for (int e = 0; e < HALF / 32; ++e) {
       const int j = lane + 32 * e;
-      sincosf((float)pos * prm.inv_freq[j], &ksin[e], &kcos[e]);
+      sincosf(rope_reduce(pos, prm.theta[j]), &ksin[e], &kcos[e]);
       tab[j] = make_float2(kcos[e] * prm.scale_log2, ksin[e] * prm.scale_log2);
     }
     __syncwarp();
@@ -465,7 +465,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.region = Region<D>::bytes(prm.kvr);
   prm.units = pb.P * pb.Hkv;
   prm.scale_log2 = pb.scale_log2;
-  for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  for (int j = 0; j < 64; ++j) prm.theta[j] = pb.inv_freq_d[j];
   alignas(64) CUtensorMap tm_pool{}, tm_kn{}, tm_vn{};
   if (TMA) {
     int rc = encode_rows(&tm_pool, pb.kv_pool, (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len,

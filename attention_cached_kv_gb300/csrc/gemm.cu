@@ -67,7 +67,7 @@ struct GemmParams {
   int slots;     // pairs one 128-row tile can touch: (127 / l) + 2, at most kMaxSlots
   int tab_rows;  // 8 + ceil(l / 8): the two levels of the token-angle table
   uint32_t off_out, off_tab, tab_stride, off_base, off_bar;
-  float inv_freq[64];
+  double theta[64];  // RoPE frequencies (angles reduced in double)
 };
 
 struct GBars {
@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = idx / (HALF / 2), jp = idx - row * (HALF / 2);
       const int t = row < 8 ? row : 8 * (row - 8);
       float s0, c0, s1, c1;
-      sincosf((float)t * prm.inv_freq[2 * jp], &s0, &c0);
-      sincosf((float)t * prm.inv_freq[2 * jp + 1], &s1, &c1);
+      sincosf(rope_reduce(t, prm.theta[2 * jp]), &s0, &c0);
+      sincosf(rope_reduce(t, prm.theta[2 * jp + 1]), &s1, &c1);
       *reinterpret_cast<float4*>(smem + prm.off_tab + row * prm.tab_stride + jp * 16) =
           make_float4(c0, c1, s0, s1);
     }
@@ -230,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p * prm.l < prm.M) {
             const int pos = prm.pos_offset ? prm.pos_offset[p] : prm.C;
             float s0, c0, s1, c1;
-            sincosf((float)pos * prm.inv_freq[2 * jp], &s0, &c0);
-            sincosf((float)pos * prm.inv_freq[2 * jp + 1], &s1, &c1);
+            sincosf(rope_reduce(pos, prm.theta[2 * jp]), &s0, &c0);
+            sincosf(rope_reduce(pos, prm.theta[2 * jp + 1]), &s1, &c1);
             *reinterpret_cast<float4*>(base + idx * 16) = make_float4(c0, c1, s0, s1);
           }
         }
@@ -477,7 +477,7 @@ int launch_qkv_rope(const Problem& pb, const void* x, const void* w, int d_model
   prm.C = pb.C;
   prm.pos_offset = pb.pos_offset;
   prm.status = pb.status;
-  for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  for (int j = 0; j < 64; ++j) prm.theta[j] = pb.inv_freq_d[j];
   return launch_common(prm, x, w, pb.d, q, kn, vn, stream);
 }
 

@@ -23,13 +23,17 @@
 // rounded once to f16: 11 significant bits, so the rounding of rotated q stays
 // small against the bf16 output), S = q K^T (f16 x f16) and O += P V (bf16 x
 // bf16) on mma.sync m16n8k16 with fp32 accumulation, and a running max / sum
-// softmax across key tiles.  A value past the f16 range makes its rows' sums
-// non-finite, which the status word reports.
+// softmax across key tiles.  A key chunk with a value past the f16 range is
+// written as NaN and a q value past it becomes inf, so the rows that meet one
+// end with a non-finite sum; they are recomputed in fp32 from the inputs
+// (exact.cuh).  Base angles of a group or key tile are reduced modulo 2 pi in
+// double (rope_reduce), so every int32 position keeps its accuracy.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
 #include <math.h>
 
 #include "common.cuh"
+#include "exact.cuh"
 #include "kernels.h"
 
 namespace gattn {
@@ -54,6 +58,7 @@ struct StreamParams {
   uint32_t off_ring, ring_buf, off_rt, off_bq, off_bk, off_ids, off_bar, q_panel;
   float scale_log2;
   float inv_freq[64];
+  ExactInputs ex;  // the inputs again, for rows recomputed in fp32
 };
 
 struct Layout {
@@ -96,6 +101,16 @@ __device__ __forceinline__ uint32_t f16pair(float lo, float hi) {
 // bf16 pair -> f16 pair (exact for magnitudes in [2^-17, 65504])
 __device__ __forceinline__ uint32_t bf16x2_to_f16pair(uint32_t v) {
   return f16pair(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+// An f16 chunk, or all NaN if one element is not finite (past the f16 range):
+// the rows whose logits read it then end with a non-finite sum.
+__device__ __forceinline__ uint4 f16_chunk_or_nan(uint4 h) {
+  const bool bad = (h.x & 0x7c00u) == 0x7c00u || (h.x & 0x7c000000u) == 0x7c000000u ||
+                   (h.y & 0x7c00u) == 0x7c00u || (h.y & 0x7c000000u) == 0x7c000000u ||
+                   (h.z & 0x7c00u) == 0x7c00u || (h.z & 0x7c000000u) == 0x7c000000u ||
+                   (h.w & 0x7c00u) == 0x7c00u || (h.w & 0x7c000000u) == 0x7c000000u;
+  const uint32_t nan2 = 0x7e007e00u;
+  return bad ? make_uint4(nan2, nan2, nan2, nan2) : h;
 }
 // D(16x8) += A(16x16, f16, row) * B(16x8, f16, col)
 __device__ __forceinline__ void mma_16816_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -171,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
   }
   for (int j = tid; j < HALF; j += kThreads) {
     float s, c;
-    sincosf((float)(pos0 + t0) * prm.inv_freq[j], &s, &c);
+    sincosf(rope_reduce((long long)pos0 + t0, prm.ex.theta[j]), &s, &c);
     bq[j] = make_float2(c, s);
   }
   bad = __syncthreads_or(bad);
@@ -184,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     float2* base = bk + (kt & 1) * HALF;
     for (int j = tid; j < HALF; j += kThreads) {
       float s, c;
-      sincosf((float)(pos0 + inew0) * prm.inv_freq[j], &s, &c);
+      sincosf(rope_reduce((long long)pos0 + inew0, prm.ex.theta[j]), &s, &c);
       base[j] = make_float2(c, s);
     }
     __syncthreads();
@@ -217,9 +232,10 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
             ol[e] = f16pair(x.x * c0.x - y.x * c0.y, x.y * c1.x - y.y * c1.y);
             oh[e] = f16pair(y.x * c0.x + x.x * c0.y, y.y * c1.x + x.y * c1.y);
           }
-          sts16(kb + ko, make_uint4(ol[0], ol[1], ol[2], ol[3]));
+          sts16(kb + ko, f16_chunk_or_nan(make_uint4(ol[0], ol[1], ol[2], ol[3])));
           const int ch = c + CPR / 2;
-          sts16(kb + (ch >> 3) * kv_panel + swz128(r, ch & 7), make_uint4(oh[0], oh[1], oh[2], oh[3]));
+          sts16(kb + (ch >> 3) * kv_panel + swz128(r, ch & 7),
+                f16_chunk_or_nan(make_uint4(oh[0], oh[1], oh[2], oh[3])));
         }
       }
     }
@@ -237,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       if (k0 + r < C && k0 + r < kmax) {
         const uint32_t a = kb + (c >> 3) * kv_panel + swz128(r, c & 7);
         const uint4 v = lds16(a);
-        sts16(a, make_uint4(bf16x2_to_f16pair(v.x), bf16x2_to_f16pair(v.y), bf16x2_to_f16pair(v.z),
-                            bf16x2_to_f16pair(v.w)));
+        sts16(a, f16_chunk_or_nan(make_uint4(bf16x2_to_f16pair(v.x), bf16x2_to_f16pair(v.y),
+                                             bf16x2_to_f16pair(v.z), bf16x2_to_f16pair(v.w))));
       }
     }
     return true;
@@ -385,10 +401,25 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
       l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
       l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-      // a non-finite sum: a query or key value past the f16 range
-      if ((ra < rows && !(l_a <= 3.0e38f)) || (rb < rows && !(l_b <= 3.0e38f)))
-        report(prm.status, GIST_ATTN_STATUS_RANGE);
-      const float inv_a = 1.f / l_a, inv_b = 1.f / l_b;
+      float inv_a = 1.f / l_a, inv_b = 1.f / l_b;
+      // a non-finite sum: a query or key value past the f16 range reached the
+      // row; this lane's columns of it are recomputed in fp32
+      for (int w = 0; w < 2; ++w) {
+        const int rr = w ? rb : ra;
+        if (rr < rows && !((w ? l_b : l_a) <= 3.0e38f)) {
+          float ex[D / 4];
+          const int tt = w ? ttb : tta;
+          if (!exact_row<D, D / 4>(prm.ex, p, t0 + tt, g * G + (rr - tt * G), w ? lo_b : lo_a,
+                                   w ? lim_b : lim_a, 2 * (lane & 3), 8, ex))
+            report(prm.status, GIST_ATTN_STATUS_RANGE);
+#pragma unroll
+          for (int dn = 0; dn < D / 8; ++dn) {
+            o[dn][2 * w] = ex[2 * dn];
+            o[dn][2 * w + 1] = ex[2 * dn + 1];
+          }
+          if (w) inv_b = 1.f; else inv_a = 1.f;
+        }
+      }
 #pragma unroll
       for (int dn = 0; dn < D / 8; ++dn) {
         const uint32_t panel = sQ + (dn >> 3) * prm.q_panel + (lane & 3) * 4;
@@ -458,6 +489,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.q_panel = L.q_panel;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  exact_inputs_from(prm.ex, pb);
   alignas(64) CUtensorMap tm_q, tm_o;
   int rc = encode_map(&tm_q, pb.q, pb, L.Tg);
   if (rc != GIST_ATTN_OK) return rc;

@@ -34,6 +34,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "exact.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -56,6 +57,12 @@ struct LongParams {
   const float2* q_base;
   const float2* q_rel;
   float scale_log2;
+  // The call's own inputs: a row whose softmax sum comes out non-finite (an f16
+  // key chunk the staged pre-pass wrote as NaN, or a q value past the f16
+  // range) is stored as NaN and, once the CTA's stores have landed, recomputed
+  // from them in fp32 (exact.cuh).
+  ExactInputs ex;
+  bf16* out;
 };
 
 // A CTA's tiles are blockIdx.x, blockIdx.x + gridDim.x, ... of the row-major
@@ -125,6 +132,7 @@ struct LBars {
   uint64_t s_done, p_done, o_done, o_stored[2];
   uint64_t q_ready[2];  // q rotated in its stage (when it arrives unrotated)
   uint32_t tmem_slot;
+  int flagged;  // a row of this CTA came out non-finite (repaired at the end)
 };
 
 // 4-D tiled load into shared memory, completing bytes on `bar`.
@@ -220,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&bars->s_done, 1);
     mbar_init(&bars->p_done, kCompute);
     mbar_init(&bars->o_done, 1);
+    bars->flagged = 0;
     fence_mbar_init();
   }
   for (int idx = tid; idx < 17 * 16; idx += kThreads) bias[idx] = (idx & 15) < (idx >> 4) ? 0.f : kNegInf;
@@ -380,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (lane == 0) {
       bulk_wait_all();
+      fence_proxy_async_global();  // the stores are visible to the repair step
       if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     }
     __syncwarp();
@@ -490,32 +500,35 @@ __global__ void __launch_bounds__(kThreads, 2)
           slot[h * 128 + r] = mx;
           named_bar_sync(pair_bar, 64);
           const float mb = fmaxf(slot[r], slot[128 + r]);
-          // (S - m) scale is in log2 units; the first block always moves m
-          if ((mb - m) * sc > kSlack) {  // the first block, or a jump: move m, scale O and the sum down
-            if (m != kNegInf) {
-              const float f = ex2_approx((m - mb) * sc);
-              const uint64_t f2 = f2_make(f, f);
-              acc[0] = f2_mul(acc[0], f2);
-              acc[1] = f2_mul(acc[1], f2);
+          // (S - m) scale is in log2 units; the first block always moves m.  A
+          // row whose maximum jumps scales its O and sum down first.  The TMEM
+          // load and store are warp-collective, so the whole warp takes that
+          // branch when any of its rows needs it; the other rows scale by 1.
+          const bool move = (mb - m) * sc > kSlack;
+          const bool rescale = move && m != kNegInf;
+          if (__any_sync(0xffffffffu, rescale)) {
+            const float f = rescale ? ex2_approx((m - mb) * sc) : 1.f;
+            const uint64_t f2 = f2_make(f, f);
+            acc[0] = f2_mul(acc[0], f2);
+            acc[1] = f2_mul(acc[1], f2);
 #pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                uint32_t ov[16];
-                const uint32_t oa = tmem + lane_base + kOCol + (h * 2 + c) * 16;
-                tc::ld16(oa, ov);
-                tc::wait_ld();
-                uint32_t w[16];
+            for (int c = 0; c < 2; ++c) {
+              uint32_t ov[16];
+              const uint32_t oa = tmem + lane_base + kOCol + (h * 2 + c) * 16;
+              tc::ld16(oa, ov);
+              tc::wait_ld();
+              uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  float x, y;
-                  f2_split(f2_mul(f2_make(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), f2), x, y);
-                  w[2 * e] = __float_as_uint(x);
-                  w[2 * e + 1] = __float_as_uint(y);
-                }
-                tmem_st16(oa, w);
+              for (int e = 0; e < 8; ++e) {
+                float x, y;
+                f2_split(f2_mul(f2_make(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), f2), x, y);
+                w[2 * e] = __float_as_uint(x);
+                w[2 * e + 1] = __float_as_uint(y);
               }
+              tmem_st16(oa, w);
             }
-            m = mb;
           }
+          if (move) m = mb;
           // P = exp2((S - m) scale) into TMEM as bf16 pairs (group q -> P
           // columns [16 q, 16 q + 16)), summed
           const uint64_t nmc2 = f2_make(-m * sc, -m * sc);
@@ -579,8 +592,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         red_sum[h * 128 + r] = (a0 + a1) + (b0 + b1);
         named_bar_sync(pair_bar, 64);
         const float sum = red_sum[r] + red_sum[128 + r];
-        if (valid && !(sum <= 3.0e38f)) report(prm.status, GIST_ATTN_STATUS_RANGE);
-        const float inv = rcp_approx(sum);
+        const bool fin = sum <= 3.0e38f;
+        const float inv = fin ? rcp_approx(sum) : __int_as_float(0x7fc00000);  // NaN row
+        if (valid && !fin) bars->flagged = 1;
         const uint32_t stage = sbase + kOffQ + (i & 1) * kTile;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -611,6 +625,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 8) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  // rows stored as NaN (a value past the f16 range reached them): recompute in fp32
+  if (bars->flagged) {
+    TileWalk tw;
+    tw.init(prm);
+    for (int i = 0; i < my_tiles; ++i, tw.next(prm))
+      exact_repair_rows<64>(prm.ex, prm.out, tw.p, tw.g, tw.mt * Tm, min(l, (tw.mt + 1) * Tm), tid,
+                            kThreads, prm.status);
   }
 }
 
@@ -680,6 +702,8 @@ int launch_prefill_long_on(const Problem& pb, const void* q, const void* k, cons
   prm.q_base = q_base;
   prm.q_rel = q_rel;
   prm.scale_log2 = pb.scale_log2;
+  exact_inputs_from(prm.ex, pb);
+  prm.out = static_cast<bf16*>(pb.out);
   alignas(64) CUtensorMap tm_q, tm_o, tm_k, tm_v;
   int rc = encode_qo(&tm_q, q, pb, prm.Tm);
   if (rc == GIST_ATTN_OK) rc = encode_qo(&tm_o, pb.out, pb, prm.Tm);

@@ -20,11 +20,19 @@
 //     back into TMEM as bf16), and normalise O into the stage for the store.
 //   S = q K^T takes q and K in f16: rotated q and the rotated new keys are
 //   rounded once to f16 (11 significant bits, where bf16 has 8), and the cached
-//   bf16 keys convert to f16 exactly (magnitudes in [2^-17, 65504]).  A value
-//   past the f16 range makes its rows' softmax sums non-finite, which the
-//   status word reports.  P V stays bf16 x bf16.  Inputs that arrive rotated
-//   (the QKV projection's epilogue rotated and rounded them once) skip the
-//   rotation and the conversion: S = q K^T runs on the bf16 values as stored.
+//   bf16 keys convert to f16 exactly (magnitudes in [2^-17, 65504]).  A key
+//   chunk with a value past the f16 range is written as NaN and a rotated q
+//   value past it becomes inf, so every row that meets one ends with a
+//   non-finite softmax sum and is stored as NaN; the CTA notes that, and once
+//   its last store has landed it recomputes those rows in fp32 from the inputs
+//   (exact.cuh), so the result holds on the whole bf16 range while the hot
+//   loop carries no extra code.  P V stays
+//   bf16 x bf16.  Inputs that arrive rotated (the QKV projection's epilogue
+//   rotated and rounded them once) skip the rotation and the conversion:
+//   S = q K^T runs on the bf16 values as stored.
+//   Rotation angles: the base angle pos theta_j of a unit's first token is
+//   reduced modulo 2 pi in double (rope_reduce), and token t adds t theta_j in
+//   fp32, so positions anywhere in int32 keep their accuracy.
 // Hand-offs use mbarriers; the compute warps are software-pipelined so that the
 // rotation of tile i+1 runs while O(i) = P V is on the tensor core and the
 // normalisation of tile i runs while S(i+1) is.  One pass covers a tile's
@@ -34,6 +42,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "exact.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -60,16 +69,19 @@ struct TcParams {
   int num_units;  // P * Hkv
   int kv_rows;    // rows of one K (or V) panel
   int rotated;    // q and k_new arrive rotated: no RoPE, S = q K^T in bf16 as stored
-  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_bar;
+  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_base,
+      off_bar;
   uint32_t p_col, o_col, tmem_cols;  // TMEM plan: S at column 0
   float scale_log2;
   float inv_freq[64];
+  ExactInputs ex;  // the inputs again, for rows recomputed in fp32
+  bf16* out;
 };
 
 struct Layout {
   int Tm, n_mt, kv_rows, stages;
-  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_bar,
-      bytes;
+  uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_base,
+      off_bar, bytes;
   uint32_t p_col, o_col, tmem_cols;
 };
 
@@ -94,6 +106,8 @@ Layout plan_stages(const Problem& pb, int stages) {
   off += 2u * 2 * 128 * 4;  // partial row max and row sum of each half
   L.off_bias = off;
   off += 17u * 16 * 4;  // mask rows: bias[v][e] = 0 for e < v, else -inf
+  L.off_base = off;
+  off += (uint32_t)(pb.d / 2) * 4;  // base angles of the table's first token
   L.off_bar = off;
   off += 128;
   L.bytes = off + 1024;
@@ -156,6 +170,18 @@ __device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t v) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return f2_to_f16x2(bf16x2_to_f2(v));
 }
+// An f16 chunk of eight keys' elements, or all NaN if one of them is not
+// finite (past the f16 range): every logit that reads the chunk becomes NaN,
+// which sends those rows to the fp32 recomputation.
+__device__ __forceinline__ uint4 f16_chunk_or_nan(uint4 h) {
+  const uint32_t e = 0x7c007c00u;
+  const bool bad = (h.x & 0x7c00u) == 0x7c00u || (h.x & 0x7c000000u) == 0x7c000000u ||
+                   (h.y & 0x7c00u) == 0x7c00u || (h.y & 0x7c000000u) == 0x7c000000u ||
+                   (h.z & 0x7c00u) == 0x7c00u || (h.z & 0x7c000000u) == 0x7c000000u ||
+                   (h.w & 0x7c00u) == 0x7c00u || (h.w & 0x7c000000u) == 0x7c000000u;
+  const uint32_t nan2 = e | 0x02000200u;
+  return bad ? make_uint4(nan2, nan2, nan2, nan2) : h;
+}
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -187,6 +213,7 @@ struct Bars {
                          // (two, alternating: the compute warps can finish tile i+1
                          // before the TMA warp has waited on tile i)
   uint32_t tmem_slot;
+  int flagged;  // a row of this CTA came out non-finite (repaired at the end)
 };
 
 // NCH: S chunks of 16 columns per thread (the tile's keys / 32, rounded up).
@@ -212,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
   float* red_sum = red_max + 256;                                  // [2][128]
   const uint8_t* tab = smem + prm.off_tab;
   float* bias = reinterpret_cast<float*>(smem + prm.off_bias);  // [17][16]
+  float* base_ang = reinterpret_cast<float*>(smem + prm.off_base);  // [d/2]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = prm.G, C = prm.C, l = prm.l, Tm = prm.Tm, n_mt = prm.n_mt;
@@ -238,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_stored[0], kCompute);
     mbar_init(&bars->o_stored[1], kCompute);
+    bars->flagged = 0;
     fence_mbar_init();
   }
   {
@@ -256,17 +285,26 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       sts16(sbase + (sp / NP) * prm.stage_bytes + (sp % NP) * kPanel + swz128(Tm * G + rr, c), z);
     }
   }
-  auto build_table = [&](int pos_base, int nthreads) {
+  // (cos, sin) of (pos_base + t) theta_j for every new token t < l: the base
+  // angle reduced in double by threads j < d/2 (then a barrier), t theta_j in fp32
+  auto build_base = [&](int pos_base) {
+    if (tid < HALF) base_ang[tid] = rope_reduce(pos_base, prm.ex.theta[tid]);
+  };
+  auto build_table = [&](int nthreads) {
     for (int idx = tid; idx < l * (HALF / 2); idx += nthreads) {
       const int t = idx / (HALF / 2), jp = idx - t * (HALF / 2);
       float s0, c0, s1, c1;
-      sincosf((float)(pos_base + t) * prm.inv_freq[2 * jp], &s0, &c0);
-      sincosf((float)(pos_base + t) * prm.inv_freq[2 * jp + 1], &s1, &c1);
+      sincosf(fmaf((float)t, prm.inv_freq[2 * jp], base_ang[2 * jp]), &s0, &c0);
+      sincosf(fmaf((float)t, prm.inv_freq[2 * jp + 1], base_ang[2 * jp + 1]), &s1, &c1);
       *reinterpret_cast<float4*>(smem + prm.off_tab + t * prm.tab_stride + jp * 16) =
           make_float4(c0, c1, s0, s1);
     }
   };
-  if (!prm.pos_offset) build_table(C, kThreads);
+  if (!prm.pos_offset) {
+    build_base(C);
+    __syncthreads();
+    build_table(kThreads);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -365,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     }
     if (lane == 0) {
       bulk_wait_all();
+      fence_proxy_async_global();  // the stores are visible to the repair step
       if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     }
     __syncwarp();
@@ -427,7 +466,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     auto prepare_unit = [&](int k, bool bad) {
       if (prm.pos_offset && !prm.rotated) {
         named_bar_sync(kBarCompute, kCompute);  // nobody still reads the previous table
-        build_table(prm.pos_offset[unit_of(k) / prm.Hkv], kCompute);
+        build_base(prm.pos_offset[unit_of(k) / prm.Hkv]);
+        named_bar_sync(kBarCompute, kCompute);
+        build_table(kCompute);
         named_bar_sync(kBarCompute, kCompute);
       }
       if (!bad && !prm.rotated) {
@@ -438,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
             const int t = w / CPR, c = w % CPR;
             const uint32_t a = chunk_addr(kb, kv_panel, bi * bl + t, c);
             const uint4 v = lds16(a);
-            sts16(a, make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                                bf16x2_to_f16x2(v.w)));
+            sts16(a, f16_chunk_or_nan(make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                                 bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w))));
           }
         }
         for (int w = tid; w < l * (CPR / 2); w += kCompute) {
@@ -448,10 +489,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           const uint32_t a1 = chunk_addr(kb, kv_panel, C + t, J + CPR / 2);
           uint64_t xr[4], yr[4];
           rope_chunk(lds16(a0), lds16(a1), tab + t * prm.tab_stride, 8 * J, xr, yr);
-          sts16(a0, make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]), f2_to_f16x2(xr[2]),
-                               f2_to_f16x2(xr[3])));
-          sts16(a1, make_uint4(f2_to_f16x2(yr[0]), f2_to_f16x2(yr[1]), f2_to_f16x2(yr[2]),
-                               f2_to_f16x2(yr[3])));
+          sts16(a0, f16_chunk_or_nan(make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]),
+                                                f2_to_f16x2(xr[2]), f2_to_f16x2(xr[3]))));
+          sts16(a1, f16_chunk_or_nan(make_uint4(f2_to_f16x2(yr[0]), f2_to_f16x2(yr[1]),
+                                                f2_to_f16x2(yr[2]), f2_to_f16x2(yr[3]))));
         }
       }
       fence_proxy_async_smem();  // before the rope_done arrival that hands K to the MMA
@@ -665,8 +706,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           }
         } else {
           const float sum = red_sum[r] + red_sum[128 + r];
-          if (valid && !(sum <= 3.0e38f)) report(prm.status, GIST_ATTN_STATUS_RANGE);
-          const float inv = rcp_approx(sum);
+          const bool fin = sum <= 3.0e38f;
+          const float inv = fin ? rcp_approx(sum) : __int_as_float(0x7fc00000);  // NaN row
+          if (valid && !fin) bars->flagged = 1;
           const uint64_t inv2 = f2_make(inv, inv);
 #pragma unroll
           for (int c = 0; c < OC; ++c) {
@@ -705,6 +747,13 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
   if (warp == 8) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, prm.tmem_cols);
+  }
+  // rows stored as NaN (a value past the f16 range reached them): recompute in fp32
+  if (bars->flagged) {
+    for (int k = 0; k < my_units; ++k) {
+      const int u = unit_of(k), p = u / prm.Hkv;
+      exact_repair_rows<D>(prm.ex, prm.out, p, u - p * prm.Hkv, 0, l, tid, kThreads, prm.status);
+    }
   }
 }
 
@@ -751,12 +800,15 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.tab_stride = L.tab_stride;
   prm.off_red = L.off_red;
   prm.off_bias = L.off_bias;
+  prm.off_base = L.off_base;
   prm.off_bar = L.off_bar;
   prm.p_col = L.p_col;
   prm.o_col = L.o_col;
   prm.tmem_cols = L.tmem_cols;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  exact_inputs_from(prm.ex, pb);
+  prm.out = static_cast<bf16*>(pb.out);
 
   alignas(64) CUtensorMap tm_q, tm_o;
   int rc = encode_map(&tm_q, pb.q, pb, L.Tm);

@@ -18,9 +18,13 @@
 // zero values, so its output rows come out exactly 0, and the status word says
 // so.
 //
-// One CTA per pair.  Angles: fp32 sincos of (position x frequency); those of
-// the new keys for up to 128 tokens at a time in shared memory, (cos_j,
-// cos_j+1, sin_j, sin_j+1) per frequency pair.
+// One CTA per pair.  Angles: base angles (position x frequency) reduced modulo
+// 2 pi in double (rope_reduce), so every int32 position keeps its accuracy;
+// those of the new keys for up to 128 tokens at a time in shared memory, the
+// chunk's base plus t theta_j in fp32, (cos_j, cos_j+1, sin_j, sin_j+1) per
+// frequency pair.  A key chunk with a value past the f16 range is written as
+// NaN, so the rows that read it come out with a non-finite softmax sum and the
+// attention kernel recomputes them in fp32 from the inputs.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
 #include <math.h>
@@ -48,6 +52,7 @@ struct StageParams {
   bf16* vw;
   int l, Hkv, C;
   float inv_freq[32];
+  double theta[32];  // the same frequencies in double
 };
 
 __device__ __forceinline__ uint32_t to_f16x2(float lo, float hi) {
@@ -58,10 +63,14 @@ __device__ __forceinline__ uint32_t to_f16x2(float lo, float hi) {
 __device__ __forceinline__ float2 bf16x2_f2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
-__device__ __forceinline__ void stg16(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
+// An f16 chunk, or all NaN if one element is not finite (past the f16 range).
+__device__ __forceinline__ uint4 f16_chunk_or_nan(uint4 h) {
+  const bool bad = (h.x & 0x7c00u) == 0x7c00u || (h.x & 0x7c000000u) == 0x7c000000u ||
+                   (h.y & 0x7c00u) == 0x7c00u || (h.y & 0x7c000000u) == 0x7c000000u ||
+                   (h.z & 0x7c00u) == 0x7c00u || (h.z & 0x7c000000u) == 0x7c000000u ||
+                   (h.w & 0x7c00u) == 0x7c00u || (h.w & 0x7c000000u) == 0x7c000000u;
+  const uint32_t nan2 = 0x7e007e00u;
+  return bad ? make_uint4(nan2, nan2, nan2, nan2) : h;
 }
 
 // Rotates the 8-element chunk pair (x: elements 8 c.., y: elements 32 + 8 c..)
@@ -78,12 +87,13 @@ __device__ __forceinline__ void rotate_store(const bf16* src, uint16_t* dst, con
     ox[e] = to_f16x2(a.x * cs.x - b.x * cs.z, a.y * cs.y - b.y * cs.w);
     oy[e] = to_f16x2(b.x * cs.x + a.x * cs.z, b.y * cs.y + a.y * cs.w);
   }
-  stg16(dst + 8 * c, make_uint4(ox[0], ox[1], ox[2], ox[3]));
-  stg16(dst + 32 + 8 * c, make_uint4(oy[0], oy[1], oy[2], oy[3]));
+  stg16(dst + 8 * c, f16_chunk_or_nan(make_uint4(ox[0], ox[1], ox[2], ox[3])));
+  stg16(dst + 32 + 8 * c, f16_chunk_or_nan(make_uint4(oy[0], oy[1], oy[2], oy[3])));
 }
 
 __global__ void __launch_bounds__(kThreads) stage_kernel(const __grid_constant__ StageParams prm) {
   __shared__ float4 tab[kTabRows * 16];
+  __shared__ float base_ang[32];
   __shared__ int32_t ids[kMaxStageBlocks];
   const int tid = threadIdx.x, p = blockIdx.x;
   const int l = prm.l, Hkv = prm.Hkv, C = prm.C, rows = C + l;
@@ -118,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(const __grid_constant__
       const float2 f = bf16x2_f2(kk[e]);
       h[e] = to_f16x2(f.x, f.y);
     }
-    stg16(prm.kw + o, make_uint4(h[0], h[1], h[2], h[3]));
+    stg16(prm.kw + o, f16_chunk_or_nan(make_uint4(h[0], h[1], h[2], h[3])));
     stg16(prm.vw + o, v);
   }
 
@@ -127,13 +137,13 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(const __grid_constant__
   const int pos0 = prm.pos_offset ? prm.pos_offset[p] : C;
   if (tid < 32) {
     float s, c;
-    sincosf((float)pos0 * prm.inv_freq[tid], &s, &c);
+    sincosf(rope_reduce(pos0, prm.theta[tid]), &s, &c);
     prm.base[(size_t)p * 32 + tid] = make_float2(c, s);
   }
   if (tid < 32) {
     for (int t = (int)blockIdx.x; t < l; t += (int)gridDim.x) {
       float s, c;
-      sincosf((float)t * prm.inv_freq[tid], &s, &c);
+      sincosf(rope_reduce(t, prm.theta[tid]), &s, &c);
       prm.rel[(size_t)t * 32 + tid] = make_float2(c, s);
     }
   }
@@ -142,11 +152,13 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(const __grid_constant__
   for (int t0 = 0; t0 < l; t0 += kTabRows) {
     const int nt = min(kTabRows, l - t0);
     __syncthreads();  // the previous table is no longer read
+    if (tid < 32) base_ang[tid] = rope_reduce((long long)pos0 + t0, prm.theta[tid]);
+    __syncthreads();
     for (int idx = tid; idx < nt * 16; idx += kThreads) {
       const int t = idx >> 4, jp = idx & 15;
       float s0, c0, s1, c1;
-      sincosf((float)(pos0 + t0 + t) * prm.inv_freq[2 * jp], &s0, &c0);
-      sincosf((float)(pos0 + t0 + t) * prm.inv_freq[2 * jp + 1], &s1, &c1);
+      sincosf(fmaf((float)t, prm.inv_freq[2 * jp], base_ang[2 * jp]), &s0, &c0);
+      sincosf(fmaf((float)t, prm.inv_freq[2 * jp + 1], base_ang[2 * jp + 1]), &s1, &c1);
       tab[idx] = make_float4(c0, c1, s0, s1);
     }
     __syncthreads();
@@ -206,7 +218,10 @@ int launch_staged(const Problem& pb, void* workspace, cudaStream_t stream) {
   prm.l = pb.l;
   prm.Hkv = pb.Hkv;
   prm.C = pb.C;
-  for (int j = 0; j < 32; ++j) prm.inv_freq[j] = pb.inv_freq[j];
+  for (int j = 0; j < 32; ++j) {
+    prm.inv_freq[j] = pb.inv_freq[j];
+    prm.theta[j] = pb.inv_freq_d[j];
+  }
   stage_kernel<<<pb.P, kThreads, 0, stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return GIST_ATTN_ERR_LAUNCH;
   return launch_prefill_long_on(pb, pb.q, ws + L.k_off, ws + L.v_off, pb.C, true,

@@ -62,10 +62,12 @@ extern "C" {
                                         pair's output rows were written as zeros     */
 #define GIST_ATTN_STATUS_TIMEOUT 2   /* a bounded wait on an asynchronous copy gave up;
                                         the affected outputs are unspecified          */
-#define GIST_ATTN_STATUS_RANGE 4     /* a row's softmax sum was not finite: a query or
-                                        key value beyond the f16 range (|x| >= 65520)
-                                        in a kernel that forms q.K in f16; that row's
-                                        outputs are NaN                               */
+#define GIST_ATTN_STATUS_RANGE 4     /* a row's softmax sum was not finite even in
+                                        fp32: a NaN input, or logits or values near the
+                                        fp32 limit; that row's outputs are not finite.
+                                        (Values past the f16 range alone do not set it:
+                                        the kernels that form q.K in f16 recompute the
+                                        rows they reach in fp32.)                      */
 
 typedef struct {
   int32_t num_pairs;       /* P >= 0: pairs (or decode sequences) in this call          */

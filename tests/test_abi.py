@@ -115,7 +115,7 @@ def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, 1, 2, 3):
         assert binding.status_string(code)
     assert "block" in binding.status_string(binding.STATUS_BAD_BLOCK)
-    assert "f16" in binding.status_string(binding.STATUS_RANGE)
+    assert "fp32" in binding.status_string(binding.STATUS_RANGE)
 
 
 def test_gather_debug_rejects_bad_arguments(fake_ptrs):
