@@ -209,6 +209,7 @@ extern "C" int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void*
   pb.pos_offset = pos_offset;
   pb.out = out;
   if (pb.C > 0 && gattn::decode_long_fits(pb)) return gattn::launch_decode_long_fp8(pb, kv_scale, stream);
+  if (gattn::decode_short_fits(pb)) return gattn::launch_decode_short_fp8(pb, kv_scale, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 

@@ -21,8 +21,11 @@
 // 1-byte KV elements), one fp32 scale per (block, layer, K|V, KV head): the
 // chunks are half as many bytes, widened in registers only to f16 pairs
 // (cvt e4m3x2 -> f16x2) and multiplied against the f16 query slice and the
-// f16 value weight with fp32 accumulation (mixed-precision FMA); the K scale
-// multiplies the logit and the V scale the value weight.
+// f16 value weight with fp32 accumulation (mixed-precision FMA).  The query is
+// brought into the f16 range by a power of two (folded back into the logit);
+// the K scale multiplies the fp32 logit, and the V scale multiplies each
+// chunk's fp32 partial P V sum, so a small scale never pushes a weight into
+// f16's subnormal range.
 //
 // With STATS it also writes, per (sequence, head, cached block), the block's
 // attention mass -- the sum of the softmax weights of its rows -- the statistic
@@ -180,10 +183,20 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
   // FP8: the query slice as f16 (low half of each register), for the mixed
   // f16 x f16 + fp32 products against keys widened only to f16
   uint32_t qh[FP8 ? QE : 1];
+  float qfac = 1.f;  // FP8: the power of two the f16 query slice was divided by
   if constexpr (FP8) {
+    float mx = 0.f;
+#pragma unroll
+    for (int e = 0; e < QE; ++e) mx = fmaxf(mx, fabsf(qr[e]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    const int ex = mx >= 16384.f ? ilogbf(mx) - 13 : 0;
+    qfac = ldexpf(1.f, ex);
+    const float inv = ldexpf(1.f, -ex);
 #pragma unroll
     for (int e = 0; e < QE; ++e) {
-      const __half hq = __float2half_rn(qr[e]);
+      const __half hq = __float2half_rn(qr[e] * inv);
       qh[e] = *reinterpret_cast<const unsigned short*>(&hq);
     }
   }
@@ -269,24 +282,29 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
     };
     auto vacc = [&](const uint8_t* stage, float pk, float vsc) {
       const uint8_t* vrows = stage + kChunk * kRow + warp * 4 * kRow;
+      float t[VE];
+#pragma unroll
+      for (int e = 0; e < VE; ++e) t[e] = 0.f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __half ph = __float2half_rn(__shfl_sync(0xffffffffu, pk, j * 8) * vsc);
+        const __half ph = __float2half_rn(__shfl_sync(0xffffffffu, pk, j * 8));
         const uint32_t p16 = *reinterpret_cast<const unsigned short*>(&ph);
         const uint8_t* vr = vrows + j * kRow + lane * VE;
         if constexpr (VE == 4) {
           const uint32_t raw = *reinterpret_cast<const uint32_t*>(vr);
           const uint32_t a = e4m3x2_to_f16x2(raw & 0xffffu), b2 = e4m3x2_to_f16x2(raw >> 16);
-          o[0] = fma_f16f32(p16, a, o[0]);
-          o[1] = fma_f16f32(p16, a >> 16, o[1]);
-          o[2] = fma_f16f32(p16, b2, o[2]);
-          o[3] = fma_f16f32(p16, b2 >> 16, o[3]);
+          t[0] = fma_f16f32(p16, a, t[0]);
+          t[1] = fma_f16f32(p16, a >> 16, t[1]);
+          t[2] = fma_f16f32(p16, b2, t[2]);
+          t[3] = fma_f16f32(p16, b2 >> 16, t[3]);
         } else {
           const uint32_t a = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(vr));
-          o[0] = fma_f16f32(p16, a, o[0]);
-          o[1] = fma_f16f32(p16, a >> 16, o[1]);
+          t[0] = fma_f16f32(p16, a, t[0]);
+          t[1] = fma_f16f32(p16, a >> 16, t[1]);
         }
       }
+#pragma unroll
+      for (int e = 0; e < VE; ++e) o[e] = fmaf(vsc, t[e], o[e]);
     };
     for (int ci = 0; ci < n_chunks; ci += 2) {
       const bool two = ci + 1 < n_chunks;  // uniform
@@ -296,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
       const uint8_t* st0 = ring + s0 * kStageBytes;
       const uint8_t* st1 = ring + s1 * kStageBytes;
       const int b0 = (ci * kChunk) / bl, b1 = ((ci + 1) * kChunk) / bl;
-      const float x0 = kdot(st0) * kscale[b0];
-      const float x1 = two ? kdot(st1) * kscale[b1] : kNegInf;
+      const float x0 = kdot(st0) * (kscale[b0] * qfac);
+      const float x1 = two ? kdot(st1) * (kscale[b1] * qfac) : kNegInf;
       float cm = fmaxf(x0, x1);
       cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
       cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));

@@ -6,20 +6,40 @@
 // read-only blocks) and to its own key, and its K/V are never stored.
 // [KV page, "Reusable-state"]: o_t = softmax(q_t K_{<=t}^T / sqrt(d_k)) V_{<=t}.
 //
-// Persistent warps, one (pair, KV head) unit at a time, two units in flight per
-// warp: while a warp computes unit n from one shared-memory buffer, the 16-byte
-// cp.async copies of unit n+1 (its cached K/V rows through the pool gather, its
-// new key and value rows) fill the other buffer, its query rows travel straight
-// into registers in the mma fragment layout, and the block ids of unit n+2 are
-// on their way.  A unit is (G <= 16) x (C + 1 <= 32) x d: the query fragments
-// are rotated in registers and split into bf16 hi + lo (two MMA passes, so the
-// rounding of rotated q stays out of the logits), S = q K^T and O = P V run on
-// mma.sync (m16n8k16, and m16n8k8 for a last 8-key step) with fp32
-// accumulation, the softmax on the S fragments with quad shuffles; rows are
-// written straight from the accumulator fragments.  (The problem is 7 x 17 x 64
-// here; the 5th-generation MMA needs at least 64 rows.)
+// A unit is (pair, KV head): G <= 16 query heads against C <= 32 cached keys and
+// the new key.  The cached part runs transposed, S^T = K q^T on mma.sync
+// m16n8k16: the keys are the 16 rows of an MMA tile and the query heads its
+// 8-wide N (one tile of heads for G <= 8, two for G <= 16), so the 7 heads of a
+// 14/2 model leave one column idle instead of nine rows.  The softmax runs down
+// the key rows of the accumulator (shuffles across the 8 lanes of a column);
+// movmatrix.trans turns P^T into the A layout of O = P V.  The new key and value
+// (the 17th key of the query-gisted workload) are taken in fp32 on the CUDA
+// cores: each lane holds 16 elements of one head's rotated query and the same
+// elements of the rotated new key, and reduces over its head's four lanes.  The
+// query's B fragments come from its rows in shared memory by ldmatrix, are
+// rotated in fp32, pre-scaled to log2 units and split into bf16 hi + lo (two MMA
+// passes), so the rounding of rotated q stays out of the logits; keys, values
+// and P V stay bf16 with fp32 accumulation, so every bf16 input is in range.
+//
+// Persistent warps, two units in flight per warp: while a warp computes unit n
+// from one of its two shared-memory buffers, one lane's tensor copies of unit
+// n + 1 (its cached K and V blocks as whole {64, block_len} boxes of the pool,
+// its q rows, its new key and value) fill the other buffer and complete on that
+// buffer's mbarrier; the block ids of unit n + 2 are on their way.  A wait that
+// runs out (1 s) reports GIST_ATTN_STATUS_TIMEOUT, waits once more for the copy
+// still in flight and ends the warp.
+//
+// FP8 pool ([Suffix page, §2 and the end of §5]: 1-byte KV elements, one fp32
+// scale per (block, layer, K|V, KV head)): the E4M3 boxes land in a staging area
+// and are widened to f16 in the swizzled tiles (cvt e4m3x2 -> f16x2, exact); the
+// query is scaled into the f16 range by a power of two per head and split into
+// f16 hi + lo; the K scale multiplies the fp32 logits; each block's V scale
+// over the unit's largest multiplies the fp32 weights before they are rounded
+// to f16 (so no weight drops into f16's subnormal range because of a small
+// scale), and the unit's largest V scale multiplies the output.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上";
+//        [Suffix page] icman.com.cn news 64898;
 //        [KV page] "为什么自回归推理缓存 KV，而不缓存历史 Q？".
 #include <math.h>
 
@@ -31,428 +51,606 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxKeys = 32;  // C + 1
-constexpr int kMaxBlocks = 32;
+constexpr int kMaxCached = 32;  // two 16-key tiles
+constexpr int kMaxBlocks = 32;  // a unit's block ids are held one per lane
 
 struct ShortParams {
   const bf16* q;
   const bf16* k_new;
   const bf16* v_new;
   bf16* out;
-  PoolView pv;
+  const float* kv_scale;  // FP8: [num_blocks][L][2][Hkv]
+  PoolView pv;            // the pool (bf16, or E4M3 bytes at the same element offsets)
   const int32_t* pos_offset;
   int32_t* status;
   int Hq, Hkv, G, C;
-  int kvr;          // key rows per buffer: C + 1 rounded up to 8
+  int units;        // P * Hkv (at most 2^30)
   uint32_t region;  // bytes of one warp's shared memory
-  int units;        // P * Hkv (below 2^31)
   float scale_log2;
   double theta[64];  // RoPE frequencies (angles reduced in double)
 };
 
-// One warp's shared memory: two buffers, each with the K panels then the V
-// panels (kvr rows of 128 bytes, 128-byte swizzle), then the (cos, sin) table of
-// the new token's position.
-template <int D>
+// One warp's shared memory: the swizzled tiles of two buffers, then the small
+// parts of both buffers, the (cos, sin) table of the query's position and the
+// buffers' mbarriers.  A buffer's tiles are the K tile and the V tile (MT x 16
+// rows of 128 bytes per 64-column panel, 128-byte swizzle, 1 KiB-aligned) and
+// the q tile (GN x 8 rows per panel, same swizzle; it also holds the output rows
+// before their store), and for an FP8 pool the E4M3 rows of K and V as they
+// arrive; its small parts are the new key and value rows.  Offsets of buffer
+// b's parts are the buffer-0 offsets plus b x buf (tiles) or b x small (new
+// rows).  Keeping the small parts out of the 1 KiB-aligned tiles lets five CTAs
+// of four warps share an SM on the query-gisted shape.
+template <int D, int GN, int MT, bool FP8>
 struct Region {
   static constexpr int NP = D / 64;
-  __host__ __device__ static uint32_t panel(int kvr) { return (uint32_t)kvr * 128; }
-  __host__ __device__ static uint32_t buf(int kvr) { return 2u * NP * panel(kvr); }
-  __host__ __device__ static uint32_t tab(int kvr) { return 2 * buf(kvr); }
-  __host__ __device__ static uint32_t bars(int kvr) { return tab(kvr) + (D / 2) * 8; }  // 2 mbarriers
-  // rounded to 1 KiB so that every buffer of every warp starts on a swizzle atom
-  __host__ __device__ static uint32_t bytes(int kvr) { return (bars(kvr) + 16 + 1023) & ~1023u; }
+  static constexpr uint32_t kv_panel = MT * 16 * 128;
+  static constexpr uint32_t q_panel = GN * 8 * 128;
+  static constexpr uint32_t k_off = 0;
+  static constexpr uint32_t v_off = k_off + NP * kv_panel;
+  static constexpr uint32_t q_off = v_off + NP * kv_panel;
+  static constexpr uint32_t k8_off = q_off + NP * q_panel;
+  static constexpr uint32_t v8_off = k8_off + (FP8 ? MT * 16 * D : 0);
+  static constexpr uint32_t buf = (v8_off + (FP8 ? MT * 16 * D : 0) + 1023) / 1024 * 1024;
+  static constexpr uint32_t small = 2 * D * 2;  // the new key row, then the new value row
+  static constexpr uint32_t kn_off = 2 * buf;   // buffer b: + b x small
+  static constexpr uint32_t vn_off = kn_off + D * 2;
+  static constexpr uint32_t tab_off = kn_off + 2 * small;  // float2 [D / 2]
+  static constexpr uint32_t bar_off = tab_off + D * 4;
+  static constexpr uint32_t bytes = (bar_off + 16 + 1023) / 1024 * 1024;
 };
 
-// D(16x8) += A(16x8, bf16, row) * B(8x8, bf16, col)
-__device__ __forceinline__ void mma_1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6},"
-      " {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(b0));
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
-
-__device__ __forceinline__ uint32_t ldg32(const bf16* p) {
+// Transposes an 8x8 matrix of 16-bit elements held as one row pair per lane
+// (row lane/4, columns 2(lane%4) and +1) into the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)v16));
+  return h;
+}
+// fp32 pair -> f16 pair, round to nearest even (first element in the low half)
+__device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t v) {
+  float a, b;
+  f2_split(v, a, b);
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+__device__ __forceinline__ uint64_t f16x2_to_f2(uint32_t h) {
+  float a, b;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(a), "=f"(b)
+      : "r"(h));
+  return f2_make(a, b);
+}
+// Splits an fp32 pair into f16 hi + lo: hi = f16(x), lo = f16(x - hi).
+__device__ __forceinline__ void f2_split_f16(uint64_t x, uint32_t& hi, uint32_t& lo) {
+  hi = f2_to_f16x2(x);
+  lo = f2_to_f16x2(f2_sub(x, f16x2_to_f2(hi)));
+}
+// A pair of weights as the 16-bit operand type of P V.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_p(float a, float b) {
+  if constexpr (F16) return f2_to_f16x2(f2_make(a, b));
+  return float2_to_bf16x2(a, b);
+}
 
-// G8: the group has at most 8 query heads, so rows 8..15 of every 16-row
-// fragment are zero and their work is left out at compile time.
-// TMA: a unit's rows arrive by tensor copies issued by one lane (cached blocks of
-// a multiple of 8 rows, each (block, K|V) a {64, block_len} box, the new key and
-// value {64, 1} boxes), completing on the buffer's mbarrier; otherwise every lane
-// issues 16-byte cp.async copies.
-template <int D, bool G8, bool TMA>
+// 2-D tiled store from shared memory (rows outside the tensor are dropped).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// D: head dim.  GN: 8-head tiles of the N dimension.  MT: 16-key tiles.
+template <int D, int GN, int MT, bool FP8>
 __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_constant__ ShortParams prm,
                                                                 const __grid_constant__ CUtensorMap tm_pool,
+                                                                const __grid_constant__ CUtensorMap tm_q,
                                                                 const __grid_constant__ CUtensorMap tm_kn,
-                                                                const __grid_constant__ CUtensorMap tm_vn) {
-  using R = Region<D>;
+                                                                const __grid_constant__ CUtensorMap tm_vn,
+                                                                const __grid_constant__ CUtensorMap tm_o) {
+  using R = Region<D, GN, MT, FP8>;
   constexpr int NP = D / 64;
-  constexpr int CPR = D / 8;
-  constexpr int HALF = D / 2;
-  constexpr int KS = D / 16;  // k-steps of the q fragments
+  constexpr int CPR = D / 8;  // 16-byte chunks per bf16 row
+  constexpr int KS = D / 16;  // k-steps over d
+  constexpr int HK = KS / 2;  // k-steps holding the first half of d
+  constexpr int NQ = HK * 2;  // (x, y) fp32 pairs per lane and head tile
   constexpr float kNegInf = -INFINITY;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int G = prm.G, C = prm.C;
+  const int bpp = prm.pv.blocks_per_pair, bl = prm.pv.block_len;
+  const int NG = prm.Hkv;  // units per pair
   const int W = gridDim.x * kWarps;
   int u = blockIdx.x * kWarps + warp;
   if (u >= prm.units) return;  // warp-uniform; nothing below synchronises the CTA
-  const int G = prm.G, C = prm.C, NK = C + 1, kvr = prm.kvr;
-  const int bpp = prm.pv.blocks_per_pair, bl = prm.pv.block_len;
   uint8_t* reg = smem + warp * prm.region;
   const uint32_t base = smem_u32(reg);
-  const uint32_t pnl = R::panel(kvr), bufb = R::buf(kvr);
-  float2* tab = reinterpret_cast<float2*>(reg + R::tab(kvr));
-  uint64_t* kvbar = reinterpret_cast<uint64_t*>(reg + R::bars(kvr));  // one per buffer (TMA)
-  if (TMA) {
-    if ((base & 1023u) != 0) {  // the swizzle atoms need 1 KiB alignment: never expected
-      if (lane == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
-      return;
-    }
-    if (lane == 0) {
-      mbar_init(&kvbar[0], 1);
-      mbar_init(&kvbar[1], 1);
-      fence_mbar_init();
-    }
-    __syncwarp();
+  // (c_j, s_j, c_j+1, s_j+1) x softmax scale at index j / 2 for even j
+  const float4* tab = reinterpret_cast<const float4*>(reg + R::tab_off);
+  float2* tabw = reinterpret_cast<float2*>(reg + R::tab_off);
+  uint64_t* kvbar = reinterpret_cast<uint64_t*>(reg + R::bar_off);
+  if ((base & 1023u) != 0) {  // the swizzle atoms need 1 KiB alignment: never expected
+    if (lane == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    return;
   }
-  auto kaddr = [&](int b, int row, int c) {
-    return base + b * bufb + (c >> 3) * pnl + swz128(row, c & 7);
-  };
-  auto vaddr = [&](int b, int row, int c) {
-    return base + b * bufb + (NP + (c >> 3)) * pnl + swz128(row, c & 7);
-  };
+  if (lane == 0) {
+    mbar_init(&kvbar[0], 1);
+    mbar_init(&kvbar[1], 1);
+    fence_mbar_init();
+  }
+  // rows no copy writes stay zero in both buffers: key rows C.. of the K and V
+  // tiles, head rows G.. of the q tile
+  const int krows = C;
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t bb = base + b * R::buf;
+    const int kpad = MT * 16 - krows;
+    for (int idx = lane; idx < NP * kpad * 8; idx += 32) {
+      const int c = idx & 7, rest = idx >> 3, row = krows + rest % kpad, pn = rest / kpad;
+      sts16(bb + R::k_off + pn * R::kv_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
+      sts16(bb + R::v_off + pn * R::kv_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
+    }
+    for (int idx = lane; idx < NP * GN * 8 * 8; idx += 32) {
+      const int c = idx & 7, row = (idx >> 3) % (GN * 8), pn = (idx >> 3) / (GN * 8);
+      if (row >= G) sts16(bb + R::q_off + pn * R::q_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
 
-  // rows past the keys stay zero in both buffers (no copy writes them)
-  if (kvr > NK) {
-    const int pad = kvr - NK;
-    for (int idx = lane; idx < 2 * 2 * pad * CPR; idx += 32) {
-      const int c = idx % CPR, rest = idx / CPR;
-      const int row = NK + rest % pad, kv = (rest / pad) & 1, b = rest / (2 * pad);
-      sts16(kv ? vaddr(b, row, c) : kaddr(b, row, c), make_uint4(0, 0, 0, 0));
-    }
-  }
-  // (cos, sin) of the new token's position: lane j keeps frequencies j (and
-  // j + 32) in registers for the key; the table holds them times the softmax
-  // scale for the query fragments
-  float kcos[HALF / 32], ksin[HALF / 32];
-  auto build_tab = [&](int pos) {
+  // This lane's key rows 16 mt + g8 + 8 hh: live (a cached key) and, FP8, the
+  // block whose scales they take -- fixed for the launch.
+  bool live[MT][2];
+  int kblk[MT][2];
 #pragma unroll
-    for (int e = 0; e < HALF / 32; ++e) {
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int row = mt * 16 + g8 + 8 * hh;
+      live[mt][hh] = row < krows;
+      kblk[mt][hh] = min(row, krows - 1) / bl;
+    }
+
+  // (cos, sin) x scale of the query's position, frequency j = lane (and lane +
+  // 32): the angle reduced in double
+  auto build_tab = [&](int pos) {
+    __syncwarp();  // the previous unit's reads are done
+#pragma unroll
+    for (int e = 0; e < D / 64; ++e) {
       const int j = lane + 32 * e;
-      sincosf(rope_reduce(pos, prm.theta[j]), &ksin[e], &kcos[e]);
-      tab[j] = make_float2(kcos[e] * prm.scale_log2, ksin[e] * prm.scale_log2);
+      float s, c;
+      sincosf(rope_reduce(pos, prm.theta[j]), &s, &c);
+      tabw[j] = make_float2(c * prm.scale_log2, s * prm.scale_log2);
     }
     __syncwarp();
   };
   const bool fixed_pos = prm.pos_offset == nullptr;
   if (fixed_pos) build_tab(C);
 
-  // block id of the unit's lane-th block (lanes < blocks_per_pair)
-  auto load_id = [&](int v) -> int32_t {
-    return (v < prm.units && lane < bpp) ? pool_block_id(prm.pv, v / prm.Hkv, lane) : 0;
+  // Per unit, lane b < bpp holds the b-th block id (and, FP8, its K and V scales).
+  struct Ids {
+    int32_t id;
+    float ks, vs;
   };
-  // cp.async of unit v's rows into buffer b; true (warp-uniform) if one of its
-  // block ids is out of range (its cached rows are then not copied)
-  auto issue = [&](int p, int g, int b, int32_t id) -> bool {
+  auto load_ids = [&](int v, int pv_, int gv) -> Ids {
+    Ids r{0, 1.f, 1.f};
+    if (v < prm.units && lane < bpp) {
+      r.id = pool_block_id(prm.pv, pv_, lane);
+      if constexpr (FP8) {
+        if (pool_block_ok(prm.pv, r.id)) {
+          const int64_t si = (((int64_t)r.id * prm.pv.num_layers + prm.pv.layer) * 2) * prm.Hkv + gv;
+          r.ks = prm.kv_scale[si];
+          r.vs = prm.kv_scale[si + prm.Hkv];
+        }
+      }
+    }
+    return r;
+  };
+  // Tensor copies of unit (p, KV head g0) into buffer b, issued by lane 0;
+  // returns (warp-uniform) whether one of its block ids is out of range, in
+  // which case its cached rows are not copied.
+  auto issue = [&](int p, int g0, int b, int32_t id) -> bool {
     const bool bad = __any_sync(0xffffffffu, lane < bpp && !pool_block_ok(prm.pv, id));
-    if (TMA) {
-      const uint32_t buf = base + b * bufb;
-      if (lane == 0)
-        mbar_arrive_expect_tx(&kvbar[b], (bad ? 0u : (uint32_t)bpp * 2 * bl * 128 * NP) + 2u * 128 * NP);
-      for (int bi = 0; bi < bpp; ++bi) {  // uniform loop: the shuffle is safe
-        const int32_t blk = __shfl_sync(0xffffffffu, id, bi);
-        if (lane == 0 && !bad) {
-          const int row_k = (int)((((int64_t)blk * prm.pv.num_layers + prm.pv.layer) * 2 * prm.Hkv + g) * bl);
-          const int row_v = row_k + prm.Hkv * bl;
+    const uint32_t bb = base + b * R::buf;
+    constexpr uint32_t kv_row_bytes = FP8 ? D : D * 2;
+    if (lane == 0) {
+      bulk_wait_read_all();  // the output store of two units ago has read the q tile
+      mbar_arrive_expect_tx(&kvbar[b], (bad ? 0u : (uint32_t)(bpp * 2 * bl) * kv_row_bytes) +
+                                           (uint32_t)G * D * 2 + 2u * D * 2);
+    }
+    for (int bi = 0; bi < bpp; ++bi) {  // uniform loop: the shuffle is safe
+      const int32_t blk = __shfl_sync(0xffffffffu, id, bi);
+      if (lane == 0 && !bad) {
+        const int row_k =
+            (int)((((int64_t)blk * prm.pv.num_layers + prm.pv.layer) * 2 * prm.Hkv + g0) * bl);
+        const int row_v = row_k + prm.Hkv * bl;
+        if constexpr (FP8) {
+          tma_load_2d(bb + R::k8_off + bi * bl * D, &tm_pool, &kvbar[b], 0, row_k);
+          tma_load_2d(bb + R::v8_off + bi * bl * D, &tm_pool, &kvbar[b], 0, row_v);
+        } else {
 #pragma unroll
           for (int x = 0; x < NP; ++x) {
-            tma_load_2d(buf + x * pnl + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x, row_k);
-            tma_load_2d(buf + (NP + x) * pnl + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x, row_v);
+            tma_load_2d(bb + R::k_off + x * R::kv_panel + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x, row_k);
+            tma_load_2d(bb + R::v_off + x * R::kv_panel + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x, row_v);
           }
         }
       }
-      if (lane == 0) {
+    }
+    if (lane == 0) {
 #pragma unroll
-        for (int x = 0; x < NP; ++x) {
-          tma_load_2d(buf + x * pnl + C * 128, &tm_kn, &kvbar[b], 64 * x, p * prm.Hkv + g);
-          tma_load_2d(buf + (NP + x) * pnl + C * 128, &tm_vn, &kvbar[b], 64 * x, p * prm.Hkv + g);
-        }
-      }
-      return bad;
+      for (int x = 0; x < NP; ++x)
+        tma_load_2d(bb + R::q_off + x * R::q_panel, &tm_q, &kvbar[b], 64 * x, p * prm.Hq + g0 * G);
+      tma_load_2d(base + R::kn_off + b * R::small, &tm_kn, &kvbar[b], 0, p * prm.Hkv + g0);
+      tma_load_2d(base + R::vn_off + b * R::small, &tm_vn, &kvbar[b], 0, p * prm.Hkv + g0);
     }
-    constexpr int kStep = 32 / CPR;  // rows per pass of the warp
-    const int c = lane % CPR, r0 = lane / CPR;
-    if (!bad) {
-      // this lane's chunk column c of rows r0, r0 + kStep, ... of every block;
-      // a block's V rows sit Hkv * block_len rows after its K rows
-      const uint32_t col = base + b * bufb + (c >> 3) * pnl;
-      const uint32_t v_off = NP * pnl;
-      const int64_t v_gap = (int64_t)prm.Hkv * bl * D;
-      for (int bi = 0; bi < bpp; ++bi) {  // uniform loop: the shuffle is safe
-        const int32_t blk = __shfl_sync(0xffffffffu, id, bi);
-        const bf16* src = pool_row(prm.pv, blk, g, 0, r0) + c * 8;
-        for (int row = bi * bl + r0; row < (bi + 1) * bl; row += kStep, src += kStep * D) {
-          const uint32_t dst = col + swz128(row, c & 7);
-          cp_async16(dst, src);
-          cp_async16(dst + v_off, src + v_gap);
-        }
-      }
-    }
-    // the new token's raw key (rotated later) and its value: row C
-    const size_t nrow = ((size_t)p * prm.Hkv + g) * D;
-    for (int c2 = lane; c2 < 2 * CPR; c2 += 32) {
-      if (c2 < CPR)
-        cp_async16(kaddr(b, C, c2), prm.k_new + nrow + c2 * 8);
-      else
-        cp_async16(vaddr(b, C, c2 - CPR), prm.v_new + nrow + (c2 - CPR) * 8);
-    }
-    cp_async_commit();
     return bad;
   };
-  // unit v's query rows (heads) lane/4 and lane/4 + 8 of its group in the mma
-  // A-fragment layout: columns ks*16 + 2(lane%4) + {0, 1} and + 8
-  auto load_q = [&](int p, int g, uint32_t (&a)[KS][4]) {
-    const bf16* q0 = prm.q + ((size_t)p * prm.Hq + (size_t)g * G) * D + 2 * (lane & 3);
-    const int ra = lane >> 2, rb = ra + 8;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      a[ks][0] = ra < G ? ldg32(q0 + (size_t)ra * D + ks * 16) : 0u;
-      a[ks][2] = ra < G ? ldg32(q0 + (size_t)ra * D + ks * 16 + 8) : 0u;
-      a[ks][1] = (!G8 && rb < G) ? ldg32(q0 + (size_t)rb * D + ks * 16) : 0u;
-      a[ks][3] = (!G8 && rb < G) ? ldg32(q0 + (size_t)rb * D + ks * 16 + 8) : 0u;
+
+  // ---- the walk over units u, u + W, ...: (pair, unit-in-pair) by carries
+  const int dp = W / NG, dg = W - dp * NG;
+  int p = u / NG, gg = u - p * NG;
+  auto step = [&](int& pp, int& gq) {
+    gq += dg;
+    pp += dp;
+    if (gq >= NG) {
+      gq -= NG;
+      ++pp;
     }
   };
-
-  // ---- prologue: unit u's copies and query; the next unit's block ids
-  uint32_t qcur[KS][4];
-  int p = u / prm.Hkv, g = u - p * prm.Hkv;
-  bool bad_cur = issue(p, g, 0, load_id(u));
-  load_q(p, g, qcur);
-  int un = u + W;
-  int pn = un / prm.Hkv, gn = un - pn * prm.Hkv;
-  int32_t id_next = load_id(un);
+  Ids ids_cur = load_ids(u, p, gg);
+  bool bad_cur = issue(p, gg, 0, ids_cur.id);
+  int un = u + W, pn = p, gn = gg;
+  step(pn, gn);
+  Ids ids_next = load_ids(un, pn, gn);
 
   for (int n = 0;; ++n) {
     const int b = n & 1;
+    const uint32_t bb = base + b * R::buf;
     // ---- unit un's copies into the other buffer (free since the last unit),
-    // its query into registers, and the block ids of the unit after it
-    uint32_t qnext[KS][4];
-    bool bad_next = false;
+    // and the block ids of the unit after it
     const bool more = un < prm.units;
+    int pa2 = pn, ga2 = gn;
+    step(pa2, ga2);
+    bool bad_next = false;
+    Ids ids_after = ids_next;
     if (more) {
-      bad_next = issue(pn, gn, b ^ 1, id_next);
-      load_q(pn, gn, qnext);
-      id_next = load_id(un + W);
-      if (!TMA) cp_async_wait_group<1>();
-    } else if (!TMA) {
-      cp_async_wait_group<0>();
+      bad_next = issue(pn, gn, b ^ 1, ids_next.id);
+      ids_after = load_ids(un + W, pa2, ga2);
     }
-    if (TMA) {  // unit u's copies are the ((n / 2) + 1)-th phase of its buffer's barrier
-      if (!mbar_wait(&kvbar[b], (uint32_t)(n >> 1) & 1u) && lane == 0)
-        report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    // unit u's copies are the ((n / 2) + 1)-th phase of its buffer's barrier
+    if (__any_sync(0xffffffffu, !mbar_wait(&kvbar[b], (uint32_t)(n >> 1) & 1u))) {
+      // give up: report, wait (bounded) for the copy still in flight, stop
+      if (lane == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+      if (more) mbar_wait(&kvbar[b ^ 1], (uint32_t)((n + 1) >> 1) & 1u);
+      if (lane == 0) bulk_wait_all();
+      return;
     }
-    __syncwarp();  // every lane's copies of unit u have landed
 
-    // ---- unit u = (pair p, KV head g)
-    bf16* out = prm.out + ((size_t)p * prm.Hq + (size_t)g * G) * D;
+    const int g0 = gg;
     if (bad_cur) {
+      bf16* out = prm.out + ((size_t)p * prm.Hq + (size_t)g0 * G) * D;
       for (int idx = lane; idx < G * CPR; idx += 32)
         *reinterpret_cast<uint4*>(out + idx * 8) = make_uint4(0, 0, 0, 0);
       if (lane == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
     } else {
       if (!fixed_pos) build_tab(prm.pos_offset[p]);
-      // the new key (row C), rotated in place: lane j takes frequencies j, j + 32
+      float vmax = 1.f, vinv = 1.f;  // FP8: the unit's largest V scale and its inverse
+      if constexpr (FP8) {
+        // widen the E4M3 rows of K and V to f16 in the swizzled tiles
+        constexpr int PER = 32 / CPR;  // rows per pass of the warp
+        const int c = lane % CPR;
+        for (int row = lane / CPR; row < krows; row += PER) {
 #pragma unroll
-      for (int e = 0; e < HALF / 32; ++e) {
-        const int j = lane + 32 * e;
-        const float2 cs = make_float2(kcos[e], ksin[e]);
-        const uint32_t ax = kaddr(b, C, j >> 3) + (j & 7) * 2;
-        const uint32_t ay = kaddr(b, C, (j + HALF) >> 3) + (j & 7) * 2;
-        uint16_t xb, yb;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(xb) : "r"(ax));
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(yb) : "r"(ay));
-        const float x = __uint_as_float((uint32_t)xb << 16), y = __uint_as_float((uint32_t)yb << 16);
-        const bf16 xr = __float2bfloat16_rn(x * cs.x - y * cs.y);
-        const bf16 yr = __float2bfloat16_rn(y * cs.x + x * cs.y);
-        asm volatile("st.shared.u16 [%0], %1;" ::"r"(ax), "h"(*reinterpret_cast<const uint16_t*>(&xr)));
-        asm volatile("st.shared.u16 [%0], %1;" ::"r"(ay), "h"(*reinterpret_cast<const uint16_t*>(&yr)));
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint2 raw = lds64(bb + (kv ? R::v8_off : R::k8_off) + row * D + c * 8);
+            sts16(bb + (kv ? R::v_off : R::k_off) + (c >> 3) * R::kv_panel + swz128(row, c & 7),
+                  make_uint4(e4m3x2_to_f16x2(raw.x & 0xffffu), e4m3x2_to_f16x2(raw.x >> 16),
+                             e4m3x2_to_f16x2(raw.y & 0xffffu), e4m3x2_to_f16x2(raw.y >> 16)));
+          }
+        }
+        vmax = lane < bpp ? ids_cur.vs : 0.f;
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, s));
+        vinv = vmax > 0.f ? 1.f / vmax : 0.f;
+        __syncwarp();
       }
-      __syncwarp();
 
-      // ---- q fragments: rotated, scaled, split into hi + lo
-      uint32_t qh[KS][4], ql[KS][4];
+      // ---- q: B fragments of head slot 8 hn + g8, elements d = 16 ks + 8 r +
+      // 2 t4 and + 1, rotated in fp32 (scale folded into the table), split
+      // into hi + lo; the new key's logit from the unrotated values (the same
+      // rotation of q and of the new key cancels in their dot product)
+      uint32_t qh[GN][KS][2], ql[GN][KS][2];
+      float qf[GN];    // FP8: 2^e, the factor the head's f16 query was divided by
+      float snew[GN];  // logit of the new key, head slot 8 hn + g8 (log2 units)
 #pragma unroll
-      for (int ks = 0; ks < KS / 2; ++ks) {
+      for (int hn = 0; hn < GN; ++hn) {
+        uint32_t qb[KS][2];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          if (G8 && (r & 1)) {  // rows 8..15
-            qh[ks][r] = ql[ks][r] = qh[ks + KS / 2][r] = ql[ks + KS / 2][r] = 0u;
-            continue;
-          }
-          const int j = ks * 16 + 2 * (lane & 3) + ((r & 2) ? 8 : 0);
-          const float4 cs = *reinterpret_cast<const float4*>(&tab[j]);  // (c_j, s_j, c_j+1, s_j+1)
-          const uint64_t c = f2_make(cs.x, cs.z), sn = f2_make(cs.y, cs.w);
-          const uint64_t x = bf16x2_to_f2(qcur[ks][r]), y = bf16x2_to_f2(qcur[ks + KS / 2][r]);
-          f2_split_bf16(f2_sub(f2_mul(x, c), f2_mul(y, sn)), qh[ks][r], ql[ks][r]);
-          f2_split_bf16(f2_fma(y, c, f2_mul(x, sn)), qh[ks + KS / 2][r], ql[ks + KS / 2][r]);
+        for (int ks = 0; ks < KS; ks += 2) {
+          // matrices (k-step ks: d 0-7, 8-15), (ks + 1: d 0-7, 8-15)
+          const int c8 = 2 * ks + (lane >> 3);
+          uint32_t r4[4];
+          ldsm_x4(bb + R::q_off + (c8 >> 3) * R::q_panel + swz128(hn * 8 + (lane & 7), c8 & 7), r4);
+          qb[ks][0] = r4[0];
+          qb[ks][1] = r4[1];
+          qb[ks + 1][0] = r4[2];
+          qb[ks + 1][1] = r4[3];
         }
-      }
-      // ---- S = q K^T over kvr keys (n-tiles of 8)
-      float s[4][4];
+        const uint32_t kn = base + R::kn_off + b * R::small;  // the new key
+        uint64_t dot = f2_make(0.f, 0.f);
+        uint64_t qx[NQ], qy[NQ];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-        if (nt * 8 < kvr) {
-          const int krow = nt * 8 + (lane & 7);
+        for (int ks = 0; ks < HK; ++ks) {
 #pragma unroll
-          for (int k2 = 0; k2 < D / 32; ++k2) {
-            uint32_t bb[4];
-            ldsm_x4(kaddr(b, krow, k2 * 4 + (lane >> 3)), bb);
-            mma_16816(s[nt], qh[2 * k2], bb[0], bb[1]);
-            mma_16816(s[nt], qh[2 * k2 + 1], bb[2], bb[3]);
-            mma_16816(s[nt], ql[2 * k2], bb[0], bb[1]);
-            mma_16816(s[nt], ql[2 * k2 + 1], bb[2], bb[3]);
-          }
-        }
-      }
-      // ---- softmax over the NK valid keys (rows: lane/4 and lane/4 + 8)
-      float ma = kNegInf, mb = kNegInf;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        if (nt * 8 + 8 > NK) {  // the n-tile holding the last key, or past it (uniform)
-          const int key = nt * 8 + 2 * (lane & 3);
-          s[nt][0] = key < NK ? s[nt][0] : kNegInf;
-          s[nt][1] = key + 1 < NK ? s[nt][1] : kNegInf;
-          s[nt][2] = key < NK ? s[nt][2] : kNegInf;
-          s[nt][3] = key + 1 < NK ? s[nt][3] : kNegInf;
-        }
-        ma = max3f(ma, s[nt][0], s[nt][1]);
-        mb = max3f(mb, s[nt][2], s[nt][3]);
-      }
-      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
-      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-      float la = 0.f, lb = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        if (nt * 8 < kvr) {
-          s[nt][0] = ex2_approx(s[nt][0] - ma);
-          s[nt][1] = ex2_approx(s[nt][1] - ma);
-          la += s[nt][0] + s[nt][1];
-          if (G8) {
-            s[nt][2] = s[nt][3] = 0.f;
-          } else {
-            s[nt][2] = ex2_approx(s[nt][2] - mb);
-            s[nt][3] = ex2_approx(s[nt][3] - mb);
-            lb += s[nt][2] + s[nt][3];
+          for (int r = 0; r < 2; ++r) {
+            const int d0 = 16 * ks + 8 * r + 2 * t4;
+            const float4 cs = tab[d0 >> 1];
+            const uint64_t c = f2_make(cs.x, cs.z), sn = f2_make(cs.y, cs.w);
+            const uint64_t x = bf16x2_to_f2(qb[ks][r]), y = bf16x2_to_f2(qb[ks + HK][r]);
+            dot = f2_fma(x, bf16x2_to_f2(lds32(kn + d0 * 2)), dot);
+            dot = f2_fma(y, bf16x2_to_f2(lds32(kn + (d0 + D / 2) * 2)), dot);
+            qx[2 * ks + r] = f2_sub(f2_mul(x, c), f2_mul(y, sn));
+            qy[2 * ks + r] = f2_fma(y, c, f2_mul(x, sn));
           }
         }
+        {
+          float a, bq;
+          f2_split(dot, a, bq);
+          float sd = a + bq;
+          sd += __shfl_xor_sync(0xffffffffu, sd, 1);
+          sd += __shfl_xor_sync(0xffffffffu, sd, 2);
+          snew[hn] = sd * prm.scale_log2;
+        }
+        if constexpr (FP8) {
+          // a power of two per head brings the query into the f16 range
+          float mx = 0.f;
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) {
+            float a0, a1, b0, b1;
+            f2_split(qx[i], a0, a1);
+            f2_split(qy[i], b0, b1);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))));
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          // e = floor(log2 mx) - 13 for mx >= 2^14 (mx is finite and normal there)
+          const int e = mx >= 16384.f ? (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127 - 13 : 0;
+          qf[hn] = __uint_as_float((uint32_t)(127 + e) << 23);
+          const float f = __uint_as_float((uint32_t)(127 - e) << 23);
+          const uint64_t f2 = f2_make(f, f);
+#pragma unroll
+          for (int ks = 0; ks < HK; ++ks)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              f2_split_f16(f2_mul(qx[2 * ks + r], f2), qh[hn][ks][r], ql[hn][ks][r]);
+              f2_split_f16(f2_mul(qy[2 * ks + r], f2), qh[hn][ks + HK][r], ql[hn][ks + HK][r]);
+            }
+        } else {
+          qf[hn] = 1.f;
+#pragma unroll
+          for (int ks = 0; ks < HK; ++ks)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              f2_split_bf16(qx[2 * ks + r], qh[hn][ks][r], ql[hn][ks][r]);
+              f2_split_bf16(qy[2 * ks + r], qh[hn][ks + HK][r], ql[hn][ks + HK][r]);
+            }
+        }
       }
-      la += __shfl_xor_sync(0xffffffffu, la, 1);
-      la += __shfl_xor_sync(0xffffffffu, la, 2);
-      lb += __shfl_xor_sync(0xffffffffu, lb, 1);
-      lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-      // ---- O = P V: key steps of 16, then one of 8 when kvr is an odd multiple of 8
+
+      // ---- S^T = K q^T: rows = keys 16 mt + g8 (+ 8), columns = head slots 8 hn + 2 t4 (+ 1)
+      float s[MT][GN][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int hn = 0; hn < GN; ++hn) s[mt][hn][0] = s[mt][hn][1] = s[mt][hn][2] = s[mt][hn][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a[4];
+          const int c8 = 2 * ks + (lane >> 4);
+          ldsm_x4(bb + R::k_off + (c8 >> 3) * R::kv_panel +
+                      swz128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, c8 & 7),
+                  a);
+#pragma unroll
+          for (int hn = 0; hn < GN; ++hn) {
+            mma16816<FP8>(s[mt][hn], a[0], a[1], a[2], a[3], qh[hn][ks][0], qh[hn][ks][1]);
+            mma16816<FP8>(s[mt][hn], a[0], a[1], a[2], a[3], ql[hn][ks][0], ql[hn][ks][1]);
+          }
+        }
+      }
+
+      // ---- softmax of every head over its cached keys and the new key
+      float pn_[GN][2], il[GN][2];  // weight of the new key and 1 / sum, head slots 8 hn + 2 t4 (+ 1)
+      uint32_t pa[MT][4];           // A fragments of P for P V, one per 16-key step
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) pa[mt][0] = pa[mt][1] = pa[mt][2] = pa[mt][3] = 0u;
+#pragma unroll
+      for (int hn = 0; hn < GN; ++hn) {
+        float f0 = 1.f, f1 = 1.f;  // FP8: 2^e of head slots 2 t4, 2 t4 + 1
+        if constexpr (FP8) {
+          f0 = __shfl_sync(0xffffffffu, qf[hn], 8 * t4);
+          f1 = __shfl_sync(0xffffffffu, qf[hn], 8 * t4 + 4);
+        }
+        float m0 = kNegInf, m1 = kNegInf;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float kf = 1.f;
+            if constexpr (FP8) kf = __shfl_sync(0xffffffffu, ids_cur.ks, kblk[mt][hh]);
+            float& x0 = s[mt][hn][2 * hh];
+            float& x1 = s[mt][hn][2 * hh + 1];
+            x0 = live[mt][hh] ? x0 * (kf * f0) : kNegInf;
+            x1 = live[mt][hh] ? x1 * (kf * f1) : kNegInf;
+            m0 = fmaxf(m0, x0);
+            m1 = fmaxf(m1, x1);
+          }
+        }
+#pragma unroll
+        for (int sft = 4; sft < 32; sft <<= 1) {
+          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, sft));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, sft));
+        }
+        const float sn0 = __shfl_sync(0xffffffffu, snew[hn], 8 * t4);
+        const float sn1 = __shfl_sync(0xffffffffu, snew[hn], 8 * t4 + 4);
+        m0 = fmaxf(m0, sn0);
+        m1 = fmaxf(m1, sn1);
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float e0 = ex2_approx(s[mt][hn][2 * hh] - m0);
+            const float e1 = ex2_approx(s[mt][hn][2 * hh + 1] - m1);
+            l0 += e0;
+            l1 += e1;
+            float vf = 1.f;
+            if constexpr (FP8) {
+              const float vs = __shfl_sync(0xffffffffu, ids_cur.vs, kblk[mt][hh]);
+              vf = vs * vinv;
+            }
+            // P^T rows (keys) -> P rows (head slots): this lane gets head slot
+            // 8 hn + g8, keys 16 mt + 8 hh + 2 t4 (+ 1)
+            pa[mt][hn + 2 * hh] = movmatrix_trans(pack_p<FP8>(e0 * vf, e1 * vf));
+          }
+        }
+#pragma unroll
+        for (int sft = 4; sft < 32; sft <<= 1) {
+          l0 += __shfl_xor_sync(0xffffffffu, l0, sft);
+          l1 += __shfl_xor_sync(0xffffffffu, l1, sft);
+        }
+        pn_[hn][0] = ex2_approx(sn0 - m0);
+        pn_[hn][1] = ex2_approx(sn1 - m1);
+        il[hn][0] = rcp_approx(l0 + pn_[hn][0]);
+        il[hn][1] = rcp_approx(l1 + pn_[hn][1]);
+      }
+
+      // ---- O = P V: rows = head slots g8 (+ 8), columns 8 dn + 2 t4 (+ 1)
       float o[D / 8][4];
 #pragma unroll
       for (int dn = 0; dn < D / 8; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        if (kk * 16 + 16 <= kvr) {
-          uint32_t pa[4];
-          pa[0] = float2_to_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-          pa[1] = float2_to_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-          pa[2] = float2_to_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-          pa[3] = float2_to_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-          const int vrow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-          for (int dq = 0; dq < D / 16; ++dq) {
-            uint32_t bb[4];
-            ldsm_x4_trans(vaddr(b, vrow, dq * 2 + (lane >> 4)), bb);
-            mma_16816(o[2 * dq], pa, bb[0], bb[1]);
-            mma_16816(o[2 * dq + 1], pa, bb[2], bb[3]);
-          }
-        } else if (kk * 16 + 8 == kvr) {
-          const uint32_t a0 = float2_to_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-          const uint32_t a1 = float2_to_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-          const int vrow = kk * 16 + (lane & 7);
-#pragma unroll
-          for (int cq = 0; cq < D / 32; ++cq) {  // four 8-column n-tiles per load
-            uint32_t bb[4];
-            ldsm_x4_trans(vaddr(b, vrow, cq * 4 + (lane >> 3)), bb);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) mma_1688(o[4 * cq + m], a0, a1, bb[m]);
-          }
+        for (int dq = 0; dq < D / 16; ++dq) {
+          uint32_t bv[4];
+          const int c8 = 2 * dq + (lane >> 4);
+          ldsm_x4_trans(bb + R::v_off + (c8 >> 3) * R::kv_panel +
+                            swz128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, c8 & 7),
+                        bv);
+          mma16816<FP8>(o[2 * dq], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], bv[0], bv[1]);
+          mma16816<FP8>(o[2 * dq + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], bv[2], bv[3]);
         }
       }
-      // ---- rows 0..G-1 straight to global (row lane/4; rows lane/4 + 8 when G > 8)
-      const int ra = lane >> 2, rb = ra + 8;
-      const float ia = rcp_approx(la), ib = rcp_approx(lb);
+
+      // ---- the new value, normalisation, into the q tile's rows: this lane's
+      // rows are head slots 8 hn + g8, whose softmax terms sit in lane g8 / 2
+      // (slot g8 % 2); then one tensor store per panel
 #pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        const int col = dn * 8 + 2 * (lane & 3);
-        if (ra < G)
-          *reinterpret_cast<uint32_t*>(out + (int64_t)ra * D + col) = float2_to_bf16x2(o[dn][0] * ia, o[dn][1] * ia);
-        if (!G8 && rb < G)
-          *reinterpret_cast<uint32_t*>(out + (int64_t)rb * D + col) = float2_to_bf16x2(o[dn][2] * ib, o[dn][3] * ib);
+      for (int hn = 0; hn < GN; ++hn) {
+        const int src = g8 >> 1;
+        const float pa0 = __shfl_sync(0xffffffffu, pn_[hn][0], src);
+        const float pa1 = __shfl_sync(0xffffffffu, pn_[hn][1], src);
+        const float ia0 = __shfl_sync(0xffffffffu, il[hn][0], src);
+        const float ia1 = __shfl_sync(0xffffffffu, il[hn][1], src);
+        const float pnew = (g8 & 1) ? pa1 : pa0, inv = (g8 & 1) ? ia1 : ia0;
+        const uint64_t oc = f2_make(vmax * inv, vmax * inv), on = f2_make(pnew * inv, pnew * inv);
+        const uint32_t vn = base + R::vn_off + b * R::small;
+        const int slot = hn * 8 + g8;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+          const int col = dn * 8 + 2 * t4;
+          const uint64_t r2 = f2_fma(bf16x2_to_f2(lds32(vn + col * 2)), on,
+                                     f2_mul(f2_make(o[dn][2 * hn], o[dn][2 * hn + 1]), oc));
+          sts32(bb + R::q_off + (dn >> 3) * R::q_panel + swz128(slot, dn & 7) + 4 * t4, f2_to_bf16x2(r2));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int x = 0; x < NP; ++x)
+          tma_store_2d(&tm_o, bb + R::q_off + x * R::q_panel, 64 * x, p * prm.Hq + g0 * G);
+        bulk_commit();
       }
     }
-    // buffer b is free for the unit after next; its shared-memory reads and the
-    // key rotation's writes come before the tensor copies that refill it
+    // buffer b is free for the unit after next; its shared-memory reads and
+    // writes come before the tensor copies that refill it
     fence_proxy_async_smem();
     __syncwarp();
     if (!more) break;
     u = un;
     p = pn;
-    g = gn;
+    gg = gn;
     un += W;
-    pn = un / prm.Hkv;
-    gn = un - pn * prm.Hkv;
+    pn = pa2;
+    gn = ga2;
     bad_cur = bad_next;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) qcur[ks][r] = qnext[ks][r];
+    ids_cur = ids_next;
+    ids_next = ids_after;
   }
+  if (lane == 0) bulk_wait_all();
 }
 
-// [rows][d] bf16 viewed as 64-column boxes of box_rows rows, 128-byte swizzle.
-int encode_rows(CUtensorMap* m, const void* base, int64_t rows, int d, int box_rows) {
+// [rows][cols] 2-D view of a row-major array, boxes of {box_cols, box_rows},
+// 128-byte swizzle (bf16, 64 columns) or none.
+int encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType type, int elem_bytes,
+              int64_t rows, int cols, int box_cols, int box_rows, bool swizzle) {
   const EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return GIST_ATTN_ERR_LAUNCH;
-  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
 }
 
-// Tensor copies need whole swizzle atoms per cached block (a multiple of 8 rows),
-// boxes of at most 256 rows and row coordinates below 2^31.
-bool tma_path(const Problem& pb) {
-  const int64_t pool_rows = (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len;
-  return pb.blocks_per_pair > 0 && pb.block_len % 8 == 0 && pb.block_len <= 256 &&
-         pool_rows < 0x7fffffff && (int64_t)pb.P * pb.Hkv < 0x7fffffff;
-}
-
-template <int D, bool G8, bool TMA>
-int launch_d(const Problem& pb, cudaStream_t stream) {
+template <int D, int GN, int MT, bool FP8>
+int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
+  using R = Region<D, GN, MT, FP8>;
   ShortParams prm{};
   prm.q = static_cast<const bf16*>(pb.q);
   prm.k_new = static_cast<const bf16*>(pb.k_new);
   prm.v_new = static_cast<const bf16*>(pb.v_new);
   prm.out = static_cast<bf16*>(pb.out);
+  prm.kv_scale = kv_scale;
   prm.pv = PoolView{static_cast<const bf16*>(pb.kv_pool), pb.item_ids, pb.block_table,
                     pb.blocks_per_pair, pb.block_len, pb.num_blocks, pb.L, pb.layer, pb.Hkv, pb.d};
   prm.pos_offset = pb.pos_offset;
@@ -461,53 +659,76 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.Hkv = pb.Hkv;
   prm.G = pb.G;
   prm.C = pb.C;
-  prm.kvr = (pb.C + 1 + 7) / 8 * 8;
-  prm.region = Region<D>::bytes(prm.kvr);
   prm.units = pb.P * pb.Hkv;
+  prm.region = R::bytes;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.theta[j] = pb.inv_freq_d[j];
-  alignas(64) CUtensorMap tm_pool{}, tm_kn{}, tm_vn{};
-  if (TMA) {
-    int rc = encode_rows(&tm_pool, pb.kv_pool, (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len,
-                         D, pb.block_len);
-    if (rc == GIST_ATTN_OK) rc = encode_rows(&tm_kn, pb.k_new, (int64_t)pb.P * pb.Hkv, D, 1);
-    if (rc == GIST_ATTN_OK) rc = encode_rows(&tm_vn, pb.v_new, (int64_t)pb.P * pb.Hkv, D, 1);
-    if (rc != GIST_ATTN_OK) return rc;
-  }
-  const uint32_t bytes = kWarps * prm.region;
-  if (cudaFuncSetAttribute(decode_short_kernel<D, G8, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)bytes) != cudaSuccess)
+  alignas(64) CUtensorMap tm_pool{}, tm_q{}, tm_kn{}, tm_vn{}, tm_o{};
+  const int64_t pool_rows = (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len;
+  const int box_rows = pb.block_len;  // a block's rows of one KV head
+  int rc = FP8 ? encode_2d(&tm_pool, pb.kv_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pool_rows, D, D,
+                           box_rows, false)
+               : encode_2d(&tm_pool, pb.kv_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool_rows, D,
+                           64, box_rows, true);
+  if (rc == GIST_ATTN_OK)
+    rc = encode_2d(&tm_q, pb.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hq, D, 64,
+                   pb.G, true);
+  if (rc == GIST_ATTN_OK)
+    rc = encode_2d(&tm_o, pb.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hq, D, 64,
+                   pb.G, true);
+  if (rc == GIST_ATTN_OK)
+    rc = encode_2d(&tm_kn, pb.k_new, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hkv, D,
+                   D, 1, false);
+  if (rc == GIST_ATTN_OK)
+    rc = encode_2d(&tm_vn, pb.v_new, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hkv, D,
+                   D, 1, false);
+  if (rc != GIST_ATTN_OK) return rc;
+  const uint32_t bytes = kWarps * R::bytes;
+  auto kern = decode_short_kernel<D, GN, MT, FP8>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_short_kernel<D, G8, TMA>, kThreads,
-                                                    bytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, bytes) != cudaSuccess ||
       per_sm < 1)
     return GIST_ATTN_ERR_LAUNCH;
   // persistent: one wave of resident CTAs walks all units
   const int64_t need = (prm.units + kWarps - 1) / kWarps;
   const int64_t grid = need < (int64_t)sms * per_sm ? need : (int64_t)sms * per_sm;
-  decode_short_kernel<D, G8, TMA><<<(unsigned)grid, kThreads, bytes, stream>>>(prm, tm_pool, tm_kn, tm_vn);
+  kern<<<(unsigned)grid, kThreads, bytes, stream>>>(prm, tm_pool, tm_q, tm_kn, tm_vn, tm_o);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
-template <int D, bool G8>
-int launch_path(const Problem& pb, cudaStream_t stream) {
-  return tma_path(pb) ? launch_d<D, G8, true>(pb, stream) : launch_d<D, G8, false>(pb, stream);
+template <int D, bool FP8>
+int launch_shape(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
+  const bool g2 = pb.G > 8, m2 = pb.C > 16;
+  if (g2)
+    return m2 ? launch_d<D, 2, 2, FP8>(pb, kv_scale, stream) : launch_d<D, 2, 1, FP8>(pb, kv_scale, stream);
+  return m2 ? launch_d<D, 1, 2, FP8>(pb, kv_scale, stream) : launch_d<D, 1, 1, FP8>(pb, kv_scale, stream);
 }
 
 }  // namespace
 
+// l = 1, 1 <= C <= 32 cached keys in blocks of a multiple of 8 rows (whole
+// swizzle atoms per tensor copy), at most 16 query heads per KV head.
 bool decode_short_fits(const Problem& pb) {
-  return pb.l == 1 && pb.G <= 16 && pb.C + 1 <= kMaxKeys && pb.blocks_per_pair <= kMaxBlocks &&
-         (pb.d == 64 || pb.d == 128) && (int64_t)pb.P * pb.Hkv <= (1 << 30);  // int unit indices
+  const int64_t pool_rows = (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len;
+  return pb.l == 1 && pb.G <= 16 && pb.C >= 1 && pb.C <= kMaxCached &&
+         pb.blocks_per_pair <= kMaxBlocks && pb.block_len % 8 == 0 && pb.block_len <= 256 &&
+         (pb.d == 64 || pb.d == 128) && pool_rows < 0x7fffffff &&
+         (int64_t)pb.P * pb.Hq < 0x7fffffff && (int64_t)pb.P * pb.Hkv <= (1 << 30);
 }
 
 int launch_decode_short(const Problem& pb, cudaStream_t stream) {
-  const bool g8 = pb.G <= 8;
-  if (pb.d == 64) return g8 ? launch_path<64, true>(pb, stream) : launch_path<64, false>(pb, stream);
-  if (pb.d == 128) return g8 ? launch_path<128, true>(pb, stream) : launch_path<128, false>(pb, stream);
+  if (pb.d == 64) return launch_shape<64, false>(pb, nullptr, stream);
+  if (pb.d == 128) return launch_shape<128, false>(pb, nullptr, stream);
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+int launch_decode_short_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
+  if (pb.d == 64) return launch_shape<64, true>(pb, kv_scale, stream);
+  if (pb.d == 128) return launch_shape<128, true>(pb, kv_scale, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 

@@ -54,6 +54,7 @@ int launch_decode(const Problem& pb, cudaStream_t stream);
 int launch_decode_long(const Problem& pb, cudaStream_t stream);
 int launch_decode_long_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
 int launch_decode_short(const Problem& pb, cudaStream_t stream);
+int launch_decode_short_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
 int launch_gather(const Problem& pb, void* dst, cudaStream_t stream);
 int launch_decode_long_stats(const Problem& pb, float* block_mass, cudaStream_t stream);
 int launch_append(const Problem& pb, void* pool, const int32_t* slot, cudaStream_t stream);

@@ -197,10 +197,12 @@ int gist_attn_fwd_noalloc(const void* q, const void* k_new, const void* v_new,
  *   kv_pool_e4m3 uint8 [num_blocks][L][2][Hkv][block_len][d] (same layout as the
  *                bf16 pool, one byte per element), 16-byte aligned
  *   kv_scale     float [num_blocks][L][2][Hkv], 4-byte aligned
- * Other arguments as gist_attn_fwd.  This build runs the decode step (l = 1) with
- * equal query and KV head counts, a cache of at least 64 rows and blocks of a
- * multiple of 16 rows (the paged layout); other shapes return
- * GIST_ATTN_ERR_UNSUPPORTED.
+ * Other arguments as gist_attn_fwd.  This build runs the decode step (l = 1):
+ * equal query and KV head counts with a cache of at least 64 rows in blocks of
+ * a multiple of 16 rows (the paged layout), or groups of at most 16 query heads
+ * with at most 32 cached rows in blocks of a multiple of 8 rows (the
+ * query-gisted layout of [Gist page, "能不能再进一步"]); other shapes return
+ * GIST_ATTN_ERR_UNSUPPORTED.  Scales must be finite and non-negative.
  */
 int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void* v_new,
                         const void* kv_pool_e4m3, const float* kv_scale,

@@ -36,6 +36,70 @@ def test_fp8_decode_every_sequence(d, bl, bpp, random_pos):
     compare(got, oracle_ref_fp8(wl, pool8, scale, layer=2), f"fp8 d={d} bl={bl}")
 
 
+@pytest.mark.parametrize("P,Hq,Hkv,d,bl,bpp,rpos", [
+    (9, 14, 2, 64, 8, 2, False),    # the query-gisted shape: 7 heads, 16 cached keys
+    (5, 32, 2, 64, 8, 4, True),     # 16 heads, 32 cached keys
+    (6, 16, 4, 128, 8, 3, True),    # d = 128, 24 cached keys
+    (7, 14, 2, 64, 16, 1, False),   # item ids, one 16-row block
+])
+def test_fp8_short_decode_every_pair(P, Hq, Hkv, d, bl, bpp, rpos):
+    """E4M3 pools behind the short decode (GQA groups, caches of at most 32 keys)."""
+    wl = workloads.make_custom(P, 1, Hq, Hkv, d, bl, bpp, 11, num_layers=2, layer=1, device=DEV,
+                               seed=P + bl, random_pos=rpos)
+    pool8, scale = workloads.make_fp8_pool(wl, seed=P)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, wl.item_ids,
+                                      wl.block_table, wl.pos_offset, dims=dict(wl.dims, layer=1),
+                                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(got, oracle_ref_fp8(wl, pool8, scale, layer=1), f"fp8 short G={Hq // Hkv} d={d}")
+
+
+@pytest.mark.parametrize("shape", ["short", "paged"])
+@pytest.mark.parametrize("magnitude", [1e-2, 1e-4])
+def test_fp8_small_scales(shape, magnitude):
+    """Scales near amax / 448 of real activations (1e-2, 1e-4), spread over two
+    decades per block: the weights must not lose precision to them."""
+    if shape == "short":
+        wl = workloads.make_custom(6, 1, 14, 2, 64, 8, 2, 9, device=DEV, seed=4)
+    else:
+        wl = workloads.make_custom(4, 1, 8, 8, 128, 32, 3, 9, device=DEV, seed=4, use_table=True)
+    pool8, scale = workloads.make_fp8_pool(wl, seed=3)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    scale = scale * magnitude * torch.pow(10.0, -2.0 * torch.rand(scale.shape, generator=g, device=DEV))
+    # values large enough that the result is not just the new token's own value
+    wl.q.mul_(1.0 / magnitude ** 0.5)
+    wl.k_new.mul_(magnitude ** 0.5)
+    wl.v_new.mul_(magnitude)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, None, wl.block_table,
+                                      None, dims=wl.dims, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle_ref_fp8(wl, pool8, scale)
+    # the tolerance is relative to the output's scale: compare in units of it
+    s = float(np.abs(ref).max())
+    compare(got / s, ref / s, f"fp8 {shape} scales ~{magnitude}")
+
+
+def test_fp8_qgist_workload_sampled():
+    """The query-gisted workload (25,000 pairs, l = 1 against 8 + 8 cached keys)
+    read from an E4M3 pool, as the benchmark's --kv fp8 row times it."""
+    wl = workloads.make("qgist", device=DEV, num_layers=2)
+    pool8, scale = workloads.make_fp8_pool(wl)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, None, wl.block_table,
+                                      None, dims=dict(wl.dims, layer=1), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel = np.sort(np.random.default_rng(1).choice(wl.dims["num_pairs"], 400, replace=False))
+    compare(got[torch.from_numpy(sel).to(DEV)], oracle_ref_fp8(wl, pool8, scale, layer=1, pairs=sel),
+            "fp8 qgist")
+    del wl, pool8, got
+    torch.cuda.empty_cache()
+
+
 def test_fp8_paged_workload_sampled():
     wl = workloads.make("paged", device=DEV, num_layers=4)
     pool8, scale = workloads.make_fp8_pool(wl)

@@ -73,6 +73,32 @@ def test_edge_shapes_every_pair(shape, random_pos):
     compare(got, oracle_ref(wl, layer=1), str(shape))
 
 
+# l = 1 shapes of the short decode (at most 32 cached keys in blocks of 8-row
+# multiples): one or two 8-head tiles, one or two 16-key tiles
+SHORT = [
+    (7, 14, 2, 64, 8, 2),     # the query-gisted shape: 7 heads, 16 keys
+    (6, 14, 2, 64, 8, 1),     # 8 cached keys
+    (5, 16, 2, 128, 8, 2),    # G = 8: a full head tile, d = 128
+    (4, 32, 2, 64, 8, 4),     # G = 16, 32 cached keys
+    (5, 24, 2, 64, 16, 2),    # G = 12, 16-row blocks
+    (6, 9, 3, 64, 8, 3),      # odd KV heads, 24 keys
+    (4, 16, 4, 128, 16, 1),   # item ids, d = 128
+    (3, 8, 8, 64, 24, 1),     # MHA, one 24-row block
+]
+
+
+@pytest.mark.parametrize("P,Hq,Hkv,d,bl,bpp", SHORT, ids=lambda v: str(v))
+@pytest.mark.parametrize("random_pos", [False, True])
+def test_short_decode_shapes(P, Hq, Hkv, d, bl, bpp, random_pos):
+    wl = workloads.make_custom(P, 1, Hq, Hkv, d, bl, bpp, 9, num_layers=2, layer=1, device=DEV,
+                               seed=P * bl + bpp, random_pos=random_pos)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = run_gpu(wl, layer=1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(got, oracle_ref(wl, layer=1), f"short decode G={Hq // Hkv} C={bl * bpp}")
+
+
 @pytest.mark.parametrize("k", [1, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("l", [16, 64, 256])
 def test_sweep_shapes(k, l):
