@@ -21,7 +21,8 @@ OBJ_DIR = os.path.join(CSRC, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libgistattn.so")
 SOURCES = ["api.cu", "prefill.cu", "prefill_tc.cu", "prefill_long.cu", "decode.cu", "decode_long.cu",
-           "decode_short.cu", "gather.cu", "append.cu", "gemm.cu", "stage.cu", "noalloc.cu"]
+           "decode_short.cu", "gather.cu", "append.cu", "gemm.cu", "stage.cu", "noalloc.cu",
+           "decode_gqa.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -139,6 +139,7 @@ int dispatch_fwd(const Problem& pb, cudaStream_t stream) {
   if (pb.l == 1) {
     if (decode_long_fits(pb)) return launch_decode_long(pb, stream);
     if (decode_short_fits(pb)) return launch_decode_short(pb, stream);
+    if (decode_gqa_fits(pb)) return launch_decode_gqa(pb, stream);
     if (decode_fits(pb)) return launch_decode(pb, stream);
   }
   if (prefill_tc_fits(pb)) return launch_prefill_tc(pb, stream);
@@ -210,6 +211,7 @@ extern "C" int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void*
   pb.out = out;
   if (pb.C > 0 && gattn::decode_long_fits(pb)) return gattn::launch_decode_long_fp8(pb, kv_scale, stream);
   if (gattn::decode_short_fits(pb)) return gattn::launch_decode_short_fp8(pb, kv_scale, stream);
+  if (gattn::decode_gqa_fits(pb)) return gattn::launch_decode_gqa_fp8(pb, kv_scale, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 
@@ -238,6 +240,8 @@ extern "C" int gist_attn_fwd_block_mass(const void* q, const void* k_new, const 
   pb.out = out;
   if (pb.C > 0 && gattn::decode_long_stats_fits(pb))
     return gattn::launch_decode_long_stats(pb, block_mass, stream);
+  if (pb.C > 0 && gattn::decode_gqa_stats_fits(pb))
+    return gattn::launch_decode_gqa_stats(pb, block_mass, stream);
   return GIST_ATTN_ERR_UNSUPPORTED;
 }
 

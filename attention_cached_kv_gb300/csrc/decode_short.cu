@@ -44,6 +44,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "frag.cuh"
 #include "kernels.h"
 
 namespace gattn {
@@ -99,80 +100,6 @@ struct Region {
   static constexpr uint32_t bytes = (bar_off + 16 + 1023) / 1024 * 1024;
 };
 
-template <bool F16>
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  if constexpr (F16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-        " {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-        " {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
-}
-// Transposes an 8x8 matrix of 16-bit elements held as one row pair per lane
-// (row lane/4, columns 2(lane%4) and +1) into the same layout.
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
-  uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-  return d;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
-  uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)v16));
-  return h;
-}
-// fp32 pair -> f16 pair, round to nearest even (first element in the low half)
-__device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t v) {
-  float a, b;
-  f2_split(v, a, b);
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
-  return r;
-}
-__device__ __forceinline__ uint64_t f16x2_to_f2(uint32_t h) {
-  float a, b;
-  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
-      : "=f"(a), "=f"(b)
-      : "r"(h));
-  return f2_make(a, b);
-}
-// Splits an fp32 pair into f16 hi + lo: hi = f16(x), lo = f16(x - hi).
-__device__ __forceinline__ void f2_split_f16(uint64_t x, uint32_t& hi, uint32_t& lo) {
-  hi = f2_to_f16x2(x);
-  lo = f2_to_f16x2(f2_sub(x, f16x2_to_f2(hi)));
-}
-// A pair of weights as the 16-bit operand type of P V.
-template <bool F16>
-__device__ __forceinline__ uint32_t pack_p(float a, float b) {
-  if constexpr (F16) return f2_to_f16x2(f2_make(a, b));
-  return float2_to_bf16x2(a, b);
-}
-
-// 2-D tiled store from shared memory (rows outside the tensor are dropped).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(src), "r"(c0), "r"(c1)
-               : "memory");
-}
-
 // D: head dim.  GN: 8-head tiles of the N dimension.  MT: 16-key tiles.
 template <int D, int GN, int MT, bool FP8>
 __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_constant__ ShortParams prm,
@@ -186,7 +113,6 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   constexpr int CPR = D / 8;  // 16-byte chunks per bf16 row
   constexpr int KS = D / 16;  // k-steps over d
   constexpr int HK = KS / 2;  // k-steps holding the first half of d
-  constexpr int NQ = HK * 2;  // (x, y) fp32 pairs per lane and head tile
   constexpr float kNegInf = -INFINITY;
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -389,86 +315,33 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         __syncwarp();
       }
 
-      // ---- q: B fragments of head slot 8 hn + g8, elements d = 16 ks + 8 r +
-      // 2 t4 and + 1, rotated in fp32 (scale folded into the table), split
-      // into hi + lo; the new key's logit from the unrotated values (the same
+      // ---- q: B fragments of head slot 8 hn + g8 (rotated, scaled, split into
+      // hi + lo); the new key's logit from the unrotated values (the same
       // rotation of q and of the new key cancels in their dot product)
       uint32_t qh[GN][KS][2], ql[GN][KS][2];
       float qf[GN];    // FP8: 2^e, the factor the head's f16 query was divided by
       float snew[GN];  // logit of the new key, head slot 8 hn + g8 (log2 units)
+      const uint32_t kn = base + R::kn_off + b * R::small;  // the new key
 #pragma unroll
       for (int hn = 0; hn < GN; ++hn) {
-        uint32_t qb[KS][2];
-#pragma unroll
-        for (int ks = 0; ks < KS; ks += 2) {
-          // matrices (k-step ks: d 0-7, 8-15), (ks + 1: d 0-7, 8-15)
-          const int c8 = 2 * ks + (lane >> 3);
-          uint32_t r4[4];
-          ldsm_x4(bb + R::q_off + (c8 >> 3) * R::q_panel + swz128(hn * 8 + (lane & 7), c8 & 7), r4);
-          qb[ks][0] = r4[0];
-          qb[ks][1] = r4[1];
-          qb[ks + 1][0] = r4[2];
-          qb[ks + 1][1] = r4[3];
-        }
-        const uint32_t kn = base + R::kn_off + b * R::small;  // the new key
+        uint64_t rx[KS], ry[KS];
+        q_fragments<D, FP8>(bb + R::q_off, R::q_panel, hn, tab, qh[hn], ql[hn], rx, ry, qf[hn]);
         uint64_t dot = f2_make(0.f, 0.f);
-        uint64_t qx[NQ], qy[NQ];
 #pragma unroll
         for (int ks = 0; ks < HK; ++ks) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int d0 = 16 * ks + 8 * r + 2 * t4;
-            const float4 cs = tab[d0 >> 1];
-            const uint64_t c = f2_make(cs.x, cs.z), sn = f2_make(cs.y, cs.w);
-            const uint64_t x = bf16x2_to_f2(qb[ks][r]), y = bf16x2_to_f2(qb[ks + HK][r]);
-            dot = f2_fma(x, bf16x2_to_f2(lds32(kn + d0 * 2)), dot);
-            dot = f2_fma(y, bf16x2_to_f2(lds32(kn + (d0 + D / 2) * 2)), dot);
-            qx[2 * ks + r] = f2_sub(f2_mul(x, c), f2_mul(y, sn));
-            qy[2 * ks + r] = f2_fma(y, c, f2_mul(x, sn));
+            dot = f2_fma(rx[2 * ks + r], bf16x2_to_f2(lds32(kn + d0 * 2)), dot);
+            dot = f2_fma(ry[2 * ks + r], bf16x2_to_f2(lds32(kn + (d0 + D / 2) * 2)), dot);
           }
         }
-        {
-          float a, bq;
-          f2_split(dot, a, bq);
-          float sd = a + bq;
-          sd += __shfl_xor_sync(0xffffffffu, sd, 1);
-          sd += __shfl_xor_sync(0xffffffffu, sd, 2);
-          snew[hn] = sd * prm.scale_log2;
-        }
-        if constexpr (FP8) {
-          // a power of two per head brings the query into the f16 range
-          float mx = 0.f;
-#pragma unroll
-          for (int i = 0; i < NQ; ++i) {
-            float a0, a1, b0, b1;
-            f2_split(qx[i], a0, a1);
-            f2_split(qy[i], b0, b1);
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))));
-          }
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          // e = floor(log2 mx) - 13 for mx >= 2^14 (mx is finite and normal there)
-          const int e = mx >= 16384.f ? (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127 - 13 : 0;
-          qf[hn] = __uint_as_float((uint32_t)(127 + e) << 23);
-          const float f = __uint_as_float((uint32_t)(127 - e) << 23);
-          const uint64_t f2 = f2_make(f, f);
-#pragma unroll
-          for (int ks = 0; ks < HK; ++ks)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              f2_split_f16(f2_mul(qx[2 * ks + r], f2), qh[hn][ks][r], ql[hn][ks][r]);
-              f2_split_f16(f2_mul(qy[2 * ks + r], f2), qh[hn][ks + HK][r], ql[hn][ks + HK][r]);
-            }
-        } else {
-          qf[hn] = 1.f;
-#pragma unroll
-          for (int ks = 0; ks < HK; ++ks)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              f2_split_bf16(qx[2 * ks + r], qh[hn][ks][r], ql[hn][ks][r]);
-              f2_split_bf16(qy[2 * ks + r], qh[hn][ks + HK][r], ql[hn][ks + HK][r]);
-            }
-        }
+        float a, bq;
+        f2_split(dot, a, bq);
+        float sd = a + bq;
+        sd += __shfl_xor_sync(0xffffffffu, sd, 1);
+        sd += __shfl_xor_sync(0xffffffffu, sd, 2);
+        snew[hn] = sd * prm.scale_log2;
       }
 
       // ---- S^T = K q^T: rows = keys 16 mt + g8 (+ 8), columns = head slots 8 hn + 2 t4 (+ 1)
@@ -623,23 +496,6 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     ids_next = ids_after;
   }
   if (lane == 0) bulk_wait_all();
-}
-
-// [rows][cols] 2-D view of a row-major array, boxes of {box_cols, box_rows},
-// 128-byte swizzle (bf16, 64 columns) or none.
-int encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType type, int elem_bytes,
-              int64_t rows, int cols, int box_cols, int box_rows, bool swizzle) {
-  const EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return GIST_ATTN_ERR_LAUNCH;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
-  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
 }
 
 template <int D, int GN, int MT, bool FP8>

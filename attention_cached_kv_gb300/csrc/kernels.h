@@ -57,6 +57,9 @@ int launch_decode_short(const Problem& pb, cudaStream_t stream);
 int launch_decode_short_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
 int launch_gather(const Problem& pb, void* dst, cudaStream_t stream);
 int launch_decode_long_stats(const Problem& pb, float* block_mass, cudaStream_t stream);
+int launch_decode_gqa(const Problem& pb, cudaStream_t stream);
+int launch_decode_gqa_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
+int launch_decode_gqa_stats(const Problem& pb, float* block_mass, cudaStream_t stream);
 int launch_append(const Problem& pb, void* pool, const int32_t* slot, cudaStream_t stream);
 int launch_store(const Problem& pb, void* pool, const int32_t* first_row, const int32_t* store_pos,
                  cudaStream_t stream);
@@ -76,5 +79,7 @@ bool decode_fits(const Problem& pb);
 bool decode_long_fits(const Problem& pb);
 bool decode_short_fits(const Problem& pb);
 bool decode_long_stats_fits(const Problem& pb);
+bool decode_gqa_fits(const Problem& pb);
+bool decode_gqa_stats_fits(const Problem& pb);
 
 }  // namespace gattn

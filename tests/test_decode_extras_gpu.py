@@ -24,14 +24,17 @@ def _lib():
     torch.cuda.empty_cache()
 
 
-def _paged(P, H, d, bl, bpp, nb, seed, L=2, layer=1, random_pos=False):
-    return workloads.make_custom(P, 1, H, H, d, bl, bpp, nb, num_layers=L, layer=layer, device=DEV,
+def _paged(P, H, d, bl, bpp, nb, seed, L=2, layer=1, random_pos=False, G=1):
+    return workloads.make_custom(P, 1, H * G, H, d, bl, bpp, nb, num_layers=L, layer=layer, device=DEV,
                                  seed=seed, random_pos=random_pos, use_table=True)
 
 
+@pytest.mark.parametrize("G", [1, 7, 16])
 @pytest.mark.parametrize("d,bl,bpp,random_pos", [(128, 256, 4, False), (64, 16, 9, True), (128, 32, 7, True)])
-def test_block_mass(d, bl, bpp, random_pos):
-    wl = _paged(5, 4, d, bl, bpp, 11, seed=bl + bpp, random_pos=random_pos)
+def test_block_mass(d, bl, bpp, random_pos, G):
+    """One mass per query head and block, for MHA (G = 1) and GQA groups of 7
+    and 16 query heads per KV head."""
+    wl = _paged(5, 4 if G == 1 else 2, d, bl, bpp, 11, seed=bl + bpp + G, random_pos=random_pos, G=G)
     dims = dict(wl.dims, layer=1)
     out, mass = binding.gist_attn_fwd_block_mass(wl.q, wl.k_new, wl.v_new, wl.kv_pool, wl.block_table,
                                                  wl.pos_offset, dims=dims)

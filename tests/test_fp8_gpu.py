@@ -56,13 +56,15 @@ def test_fp8_short_decode_every_pair(P, Hq, Hkv, d, bl, bpp, rpos):
     compare(got, oracle_ref_fp8(wl, pool8, scale, layer=1), f"fp8 short G={Hq // Hkv} d={d}")
 
 
-@pytest.mark.parametrize("shape", ["short", "paged"])
+@pytest.mark.parametrize("shape", ["short", "paged", "gqa"])
 @pytest.mark.parametrize("magnitude", [1e-2, 1e-4])
 def test_fp8_small_scales(shape, magnitude):
     """Scales near amax / 448 of real activations (1e-2, 1e-4), spread over two
     decades per block: the weights must not lose precision to them."""
     if shape == "short":
         wl = workloads.make_custom(6, 1, 14, 2, 64, 8, 2, 9, device=DEV, seed=4)
+    elif shape == "gqa":
+        wl = workloads.make_custom(4, 1, 16, 4, 128, 32, 3, 9, device=DEV, seed=4, use_table=True)
     else:
         wl = workloads.make_custom(4, 1, 8, 8, 128, 32, 3, 9, device=DEV, seed=4, use_table=True)
     pool8, scale = workloads.make_fp8_pool(wl, seed=3)
@@ -98,6 +100,25 @@ def test_fp8_qgist_workload_sampled():
             "fp8 qgist")
     del wl, pool8, got
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("P,Hq,Hkv,d,bl,bpp,rpos", [
+    (4, 32, 8, 128, 256, 2, False),   # GQA 4:1 over two 256-token blocks
+    (3, 14, 2, 64, 32, 3, True),      # the gist model's 7:1 groups, 96 keys
+    (2, 32, 2, 128, 16, 5, True),     # 16 heads per KV head
+])
+def test_fp8_gqa_paged_decode(P, Hq, Hkv, d, bl, bpp, rpos):
+    """E4M3 pools behind the long GQA decode (more than 32 cached keys, groups
+    of 2..16 query heads)."""
+    wl = workloads.make_custom(P, 1, Hq, Hkv, d, bl, bpp, 9, num_layers=2, layer=1, device=DEV,
+                               seed=bl + bpp, random_pos=rpos, use_table=True)
+    pool8, scale = workloads.make_fp8_pool(wl, seed=bl)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, None, wl.block_table,
+                                      wl.pos_offset, dims=dict(wl.dims, layer=1), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(got, oracle_ref_fp8(wl, pool8, scale, layer=1), f"fp8 gqa G={Hq // Hkv} d={d}")
 
 
 def test_fp8_paged_workload_sampled():

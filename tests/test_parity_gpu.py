@@ -99,6 +99,29 @@ def test_short_decode_shapes(P, Hq, Hkv, d, bl, bpp, random_pos):
     compare(got, oracle_ref(wl, layer=1), f"short decode G={Hq // Hkv} C={bl * bpp}")
 
 
+# l = 1 with groups of 2..16 query heads and caches past 32 keys in blocks of
+# 16-row multiples: the long GQA decode
+GQA = [
+    (3, 32, 8, 128, 256, 2),   # paged, 4 heads per KV head
+    (2, 14, 2, 64, 16, 5),     # the gist model's groups, 80 keys
+    (2, 32, 2, 64, 32, 3),     # 16 heads per KV head
+    (3, 16, 4, 128, 64, 3),    # 4 heads, 192 keys
+    (2, 6, 3, 64, 48, 1),      # item ids, 2 heads, one 48-row block
+]
+
+
+@pytest.mark.parametrize("P,Hq,Hkv,d,bl,bpp", GQA, ids=lambda v: str(v))
+@pytest.mark.parametrize("random_pos", [False, True])
+def test_gqa_decode_shapes(P, Hq, Hkv, d, bl, bpp, random_pos):
+    wl = workloads.make_custom(P, 1, Hq, Hkv, d, bl, bpp, 9, num_layers=2, layer=1, device=DEV,
+                               seed=P * bl + bpp, random_pos=random_pos)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = run_gpu(wl, layer=1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(got, oracle_ref(wl, layer=1), f"gqa decode G={Hq // Hkv} C={bl * bpp}")
+
+
 @pytest.mark.parametrize("k", [1, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("l", [16, 64, 256])
 def test_sweep_shapes(k, l):

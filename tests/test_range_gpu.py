@@ -40,9 +40,10 @@ SHAPES = {
     "prefill_stream": (3, 40, 14, 2, 64, 100, 2, 7, False),
     "staged": (3, 150, 14, 2, 64, 16, 2, 7, True),
     "decode_short": (5, 1, 14, 2, 64, 8, 2, 9, False),
-    "decode_short_cp": (4, 1, 14, 2, 64, 5, 3, 9, False),
+    "decode_5row_blocks": (4, 1, 14, 2, 64, 5, 3, 9, False),
     "decode_long": (3, 1, 8, 8, 128, 64, 2, 7, False),
-    "decode": (3, 1, 16, 2, 64, 32, 4, 9, False),
+    "decode_gqa": (3, 1, 16, 2, 64, 32, 4, 9, False),
+    "decode": (3, 1, 16, 2, 64, 20, 4, 9, False),
 }
 
 
