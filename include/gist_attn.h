@@ -199,10 +199,12 @@ int gist_attn_fwd_noalloc(const void* q, const void* k_new, const void* v_new,
  *   kv_scale     float [num_blocks][L][2][Hkv], 4-byte aligned
  * Other arguments as gist_attn_fwd.  This build runs the decode step (l = 1):
  * equal query and KV head counts with a cache of at least 64 rows in blocks of
- * a multiple of 16 rows (the paged layout), or groups of at most 16 query heads
- * with at most 32 cached rows in blocks of a multiple of 8 rows (the
- * query-gisted layout of [Gist page, "能不能再进一步"]); other shapes return
- * GIST_ATTN_ERR_UNSUPPORTED.  Scales must be finite and non-negative.
+ * a multiple of 16 rows (the paged layout); groups of 2..16 query heads with
+ * more than 32 cached rows in at most 512 blocks of a multiple of 16 rows (GQA
+ * paged); or groups of at most 16 query heads with at most 32 cached rows in
+ * blocks of a multiple of 8 rows (the query-gisted layout of [Gist page,
+ * "能不能再进一步"]).  Other shapes return GIST_ATTN_ERR_UNSUPPORTED.  Scales
+ * must be finite and non-negative.
  */
 int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void* v_new,
                         const void* kv_pool_e4m3, const float* kv_scale,
@@ -220,8 +222,10 @@ int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void* v_new,
  *               weights over the rows of the b-th block of p's table.  The new
  *               token's own weight is 1 - sum_b block_mass[p][h][b].
  * Other arguments as gist_attn_fwd (block_table required).  This build runs
- * equal query and KV head counts, at least 64 cached rows, at most 8192, in
- * blocks of a multiple of 16 rows; other shapes return GIST_ATTN_ERR_UNSUPPORTED.
+ * groups of 1..16 query heads per KV head over blocks of a multiple of 16 rows:
+ * equal head counts with 64..8192 cached rows, or 2..16 heads per KV head with
+ * 33..8192 cached rows in at most 512 blocks; other shapes return
+ * GIST_ATTN_ERR_UNSUPPORTED.
  */
 int gist_attn_fwd_block_mass(const void* q, const void* k_new, const void* v_new,
                              const void* kv_pool, const int32_t* block_table,
