@@ -580,57 +580,30 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       tc::fence_after_sync();
       const int lim = C + t0 + tt + 1;  // keys row r sees
       const int lim_all = C + t0 + 1;   // keys every row of the tile sees
-      // Chunks c < cd lie below the causal diagonal for every row of the tile;
-      // chunks from cd on reach it and take an additive 0 / -inf row from the
-      // bias table.  Those run in a separate (not unrolled) loop, so the mask
-      // code is not predicated onto the other chunks.
+      // In the exponential pass, chunks c < cd lie below the causal diagonal
+      // for every row of the tile; chunks from cd on reach it and take an
+      // additive 0 / -inf row from the bias table.  Those run in a separate
+      // (not unrolled) loop, so the mask code is not predicated onto the others.
       const int cd = lim_all >> 4;
       const int c_diag = cd + ((cd ^ h) & 1);  // this half's first chunk at the diagonal
       // the row of the bias table for chunk c: 0 for the keys row r sees, -inf after
       auto bias_row = [&](int c) {
         return reinterpret_cast<const float4*>(bias + min(max(lim - c * 16, 0), 16) * 16);
       };
-      auto mask16 = [&](int c, uint32_t (&sv)[16]) {
-        const float4* bt = bias_row(c);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 bq = bt[q4];
-          float a, b;
-          f2_split(f2_add(f2_make(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1])),
-                          f2_make(bq.x, bq.y)), a, b);
-          sv[4 * q4] = __float_as_uint(a);
-          sv[4 * q4 + 1] = __float_as_uint(b);
-          f2_split(f2_add(f2_make(__uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3])),
-                          f2_make(bq.z, bq.w)), a, b);
-          sv[4 * q4 + 2] = __float_as_uint(a);
-          sv[4 * q4 + 3] = __float_as_uint(b);
-        }
-      };
-      auto max16 = [&](const uint32_t (&v)[16], float& mx0, float& mx1) {
-        const float a = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-        const float b = max3f(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
-        const float d = max3f(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
-        const float e = max3f(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
-        const float f = max3f(__uint_as_float(v[12]), __uint_as_float(v[13]), __uint_as_float(v[14]));
-        mx0 = max3f(mx0, a, b);
-        mx1 = max3f(mx1, max3f(d, e, f), __uint_as_float(v[15]));
-      };
       if (wlive) {
-        float mx0 = kNegInf, mx1 = kNegInf;
+        // The row maximum runs over all N columns, the causally masked ones
+        // (later tokens of the tile, zero padding) included: m is at least the
+        // maximum over the keys the row sees, so its weights are at most 1 and
+        // the result is the same softmax.  Only a masked logit ~100 (log2
+        // units) above every visible one could underflow the weights; the sum
+        // check below sends such a row to the fp32 recomputation.
+        float mx0 = kNegInf;
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
           const int c = 2 * cc + h;
-          if (c < cd && c * 16 < N) mx0 = fmaxf(mx0, ld16_max(tmem + lane_base + c * 16));
+          if (c * 16 < N) mx0 = fmaxf(mx0, ld16_max(tmem + lane_base + c * 16));
         }
-#pragma unroll 1
-        for (int c = c_diag; c * 16 < N; c += 2) {
-          uint32_t v[16];
-          tc::ld16(tmem + lane_base + c * 16, v);
-          tc::wait_ld();
-          mask16(c, v);
-          max16(v, mx0, mx1);
-        }
-        red_max[h * 128 + r] = fmaxf(mx0, mx1);
+        red_max[h * 128 + r] = mx0;
         named_bar_sync(pair_bar, 64);
         const float m = fmaxf(red_max[r], red_max[128 + r]);
         {
@@ -706,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           }
         } else {
           const float sum = red_sum[r] + red_sum[128 + r];
-          const bool fin = sum <= 3.0e38f;
+          const bool fin = sum <= 3.0e38f && sum >= 1.0e-30f;
           const float inv = fin ? rcp_approx(sum) : __int_as_float(0x7fc00000);  // NaN row
           if (valid && !fin) bars->flagged = 1;
           const uint64_t inv2 = f2_make(inv, inv);

@@ -123,6 +123,16 @@ def test_positions_far_from_zero(kernel):
     check(wl, staged, f"{kernel} far positions")
 
 
+def test_masked_key_far_above_the_visible_ones():
+    """A later token's key of magnitude 1e4: rows of earlier tokens must not see
+    it, although its logit there is tens of thousands of log2 units above every
+    key they do see (the tensor-core prefill takes the row maximum over the
+    whole tile and recomputes rows whose weights underflow)."""
+    wl, staged = make("prefill_tc", seed=13)
+    wl.k_new[:, 6] = 1.0e4 * torch.sign(wl.k_new[:, 6].float()).to(torch.bfloat16)
+    check(wl, staged, "prefill_tc masked key 1e4")
+
+
 @pytest.mark.parametrize("scale", [0.3, 0.5])
 def test_gist_layer_full_size_explicit_scale(scale):
     """The full-size gist layer (12,800 Zipf pairs, the benchmark's launch) at an
