@@ -13,10 +13,14 @@
 //   * warp 8 (MMA): tcgen05.mma issue (S = Q K^T, O = P V);
 //   * warp 9 (TMA): TMA loads of 128-row Q tiles into a 3-stage ring and TMA
 //     stores of O, so that waiting for a store never delays the tensor core;
+//   * warp 10 (K/V): stages each unit's K/V into one of two buffers one unit
+//     ahead (cached rows through the pool gather, new rows raw, by 16-byte
+//     cp.async), converts the cached keys to f16 and rotates the new keys in
+//     place, and hands the buffer over by an mbarrier; the tensor core's commit
+//     after the unit's last P V hands it back.  This keeps the staging off the
+//     compute warps, whose per-row work sets the pace;
 //   * warps 0-7 (compute): two threads per tile row (TMEM lane = row; the
-//     halves split the columns).  They stage each unit's K/V (cached rows
-//     through the pool gather, new rows raw, by 16-byte cp.async two units
-//     ahead), rotate the new keys, rotate q, run the softmax out of TMEM (P
+//     halves split the columns).  They rotate q, run the softmax out of TMEM (P
 //     back into TMEM as bf16), and normalise O into the stage for the store.
 //   S = q K^T takes q and K in f16: rotated q and the rotated new keys are
 //   rounded once to f16 (11 significant bits, where bf16 has 8), and the cached
@@ -50,12 +54,17 @@ namespace gattn {
 namespace {
 
 constexpr int kCompute = 256;            // 8 compute warps
-constexpr int kThreads = kCompute + 64;  // + the MMA warp and the TMA warp
+// K/V warps: one where two CTAs share an SM (d = 64), four for d = 128, whose
+// units carry twice the rows per byte of staging and whose one CTA per SM
+// leaves registers for them
+__host__ __device__ constexpr int kv_warps(int D) { return D == 64 ? 1 : 4; }
+// + the MMA warp, the TMA warp and the K/V warps
+__host__ __device__ constexpr int threads_of(int D) { return kCompute + 64 + 32 * kv_warps(D); }
+constexpr uint32_t kBarKV = 1;  // named barrier of the K/V warps
 constexpr int kMaxStages = 3;  // q/O stages: 3, or 2 where that lets two CTAs share an SM
 constexpr int kMaxKeys = 128;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxBlocksPerPair = 64;
-constexpr uint32_t kBarCompute = 1;  // named barrier of the compute warps
 
 struct TcParams {
   const bf16* k_new;
@@ -64,6 +73,7 @@ struct TcParams {
   const int32_t* pos_offset;
   int32_t* status;
   int l, Hkv, G, C;
+  int tab_bufs;   // angle tables: 1 (one position layout for every pair), 2 (per unit)
   int Tm;         // tokens per M-tile
   int n_mt;       // M-tiles per unit
   int num_units;  // P * Hkv
@@ -101,13 +111,16 @@ Layout plan_stages(const Problem& pb, int stages) {
   // per token: (cos, cos, sin, sin) of frequency pairs, 16 B each, +16 B so that
   // consecutive tokens start on different banks
   L.tab_stride = (uint32_t)(pb.d / 4) * 16 + 16;
-  off += (uint32_t)pb.l * L.tab_stride;
+  // one table when every pair's new tokens sit at the same positions, else
+  // one per K/V buffer (the K/V warp fills the next unit's while the compute
+  // warps read the current one's)
+  off += (pb.pos_offset ? 2u : 1u) * (uint32_t)pb.l * L.tab_stride;
   L.off_red = off;
   off += 2u * 2 * 128 * 4;  // partial row max and row sum of each half
   L.off_bias = off;
   off += 17u * 16 * 4;  // mask rows: bias[v][e] = 0 for e < v, else -inf
   L.off_base = off;
-  off += (uint32_t)(pb.d / 2) * 4;  // base angles of the table's first token
+  off += (uint32_t)pb.d * 4;  // base angles of a table's first token (set-up; K/V warp)
   L.off_bar = off;
   off += 128;
   L.bytes = off + 1024;
@@ -212,6 +225,9 @@ struct Bars {
   uint64_t o_stored[2];  // compute -> TMA warp: O of tile i written into its stage
                          // (two, alternating: the compute warps can finish tile i+1
                          // before the TMA warp has waited on tile i)
+  uint64_t kv_ready[2];  // K/V warp -> compute warps: buffer b holds its unit, prepared
+  uint64_t kv_free[2];   // tensor core (commit after the unit's last P V) -> K/V warp
+  int unit_bad[2];       // buffer b's unit has a block id out of range
   uint32_t tmem_slot;
   int flagged;  // a row of this CTA came out non-finite (repaired at the end)
 };
@@ -220,12 +236,14 @@ struct Bars {
 // Registers: each of the 4 SM sub-partitions holds 16 K; two CTAs of 9 warps
 // put 5 warps on one of them (96 registers a thread), one CTA puts 3 (168).
 template <int D, int NCH, int NS>
-__global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
+__global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_o,
                       const __grid_constant__ TcParams prm) {
   constexpr int NP = D / 64;   // 64-column panels
   constexpr int CPR = D / 8;   // 16-byte chunks per row
+  constexpr int kThreads = threads_of(D);
+  constexpr int KVT = 32 * kv_warps(D);  // K/V threads
   constexpr int HALF = D / 2;
   constexpr float kNegInf = -INFINITY;
   constexpr uint32_t kPanel = 128 * 128;  // one 128-row Q panel
@@ -237,7 +255,6 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + prm.off_bar);
   float* red_max = reinterpret_cast<float*>(smem + prm.off_red);  // [2][128]
   float* red_sum = red_max + 256;                                  // [2][128]
-  const uint8_t* tab = smem + prm.off_tab;
   float* bias = reinterpret_cast<float*>(smem + prm.off_bias);  // [17][16]
   float* base_ang = reinterpret_cast<float*>(smem + prm.off_base);  // [d/2]
 
@@ -266,6 +283,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_stored[0], kCompute);
     mbar_init(&bars->o_stored[1], kCompute);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->kv_ready[b], 1);
+      mbar_init(&bars->kv_free[b], 1);
+    }
     bars->flagged = 0;
     fence_mbar_init();
   }
@@ -290,20 +311,23 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
   auto build_base = [&](int pos_base) {
     if (tid < HALF) base_ang[tid] = rope_reduce(pos_base, prm.ex.theta[tid]);
   };
-  auto build_table = [&](int nthreads) {
-    for (int idx = tid; idx < l * (HALF / 2); idx += nthreads) {
+  auto build_table = [&](uint8_t* table, int first, int nthreads) {
+    for (int idx = first; idx < l * (HALF / 2); idx += nthreads) {
       const int t = idx / (HALF / 2), jp = idx - t * (HALF / 2);
       float s0, c0, s1, c1;
       sincosf(fmaf((float)t, prm.inv_freq[2 * jp], base_ang[2 * jp]), &s0, &c0);
       sincosf(fmaf((float)t, prm.inv_freq[2 * jp + 1], base_ang[2 * jp + 1]), &s1, &c1);
-      *reinterpret_cast<float4*>(smem + prm.off_tab + t * prm.tab_stride + jp * 16) =
-          make_float4(c0, c1, s0, s1);
+      *reinterpret_cast<float4*>(table + t * prm.tab_stride + jp * 16) = make_float4(c0, c1, s0, s1);
     }
+  };
+  // the angle table of K/V buffer b's unit
+  auto table_of = [&](int b) -> uint8_t* {
+    return smem + prm.off_tab + (prm.tab_bufs == 2 ? b : 0) * (uint32_t)l * prm.tab_stride;
   };
   if (!prm.pos_offset) {
     build_base(C);
     __syncthreads();
-    build_table(kThreads);
+    build_table(table_of(0), tid, kThreads);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -349,6 +373,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           tc::mma_ts(tmem + prm.o_col, tmem + prm.p_col + ks * 8, bd, idesc, ks > 0);
         }
         tc::commit(smem_u32(&bars->o_done));
+        // the unit's last P V: its K/V buffer is free once this completes
+        if (mt == n_mt - 1) tc::commit(smem_u32(&bars->kv_free[k & 1]));
       }
       __syncwarp();
     }
@@ -407,75 +433,77 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     }
     __syncwarp();
-  } else {
-    // ================================================================ compute
-    const int h = warp >> 2;               // which half of the row's columns
-    const int r = (warp & 3) * 32 + lane;  // tile row == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  } else if (warp >= 10) {
+    // ================================================================ K/V
+    // Unit k goes to buffer k & 1 once the tensor core has finished unit k - 2
+    // there: cp.async of its rows (cached through the pool gather, new ones
+    // raw), then the cached keys converted to f16 and the new keys rotated at
+    // the unit's positions and rounded once to f16, in place (a chunk past the
+    // f16 range becomes NaN, which sends the rows that read it to the fp32
+    // recomputation).  Inputs that arrive rotated are only copied.
     auto chunk_addr = [](uint32_t base, uint32_t pstride, int row, int J) {
       return base + (J >> 3) * pstride + swz128(row, J & 7);
     };
-    // cp.async of unit u's K/V rows (cached, then new ones raw) into buffer b.
-    auto stage_kv = [&](int u, int b) -> bool {
-      // Each thread copies fixed 16-byte chunks of the unit's rows, and later
-      // converts or rotates exactly the chunks it copied, so waiting for its
-      // own copies is enough (no barrier): a new key row's chunk pair (J,
-      // J + d/16) goes to one thread.  Block ids are read by every thread (a
-      // broadcast load), so `bad` comes out the same in all of them.  Returns
-      // true if one of this unit's block ids is out of range (its rows are then
-      // not copied).
-      const int p = u / prm.Hkv, g = u % prm.Hkv;
+    const int bl = prm.pv.block_len, bpp = prm.pv.blocks_per_pair;
+    const size_t row_stride = (size_t)prm.Hkv * D;  // between consecutive new tokens
+    const int kt = tid - (kCompute + 64);           // K/V thread index
+    auto kv_sync = [&]() {
+      if (KVT == 32) __syncwarp(); else named_bar_sync(kBarKV, KVT);
+    };
+    bool failed = false;
+    for (int k = 0; k < my_units && !failed; ++k) {
+      const int b = k & 1, u = unit_of(k), p = u / prm.Hkv, g = u - p * prm.Hkv;
+      if (k >= 2 && !mbar_wait(&bars->kv_free[b], (uint32_t)((k >> 1) - 1) & 1u)) failed = true;
+      if (KVT == 32 ? __any_sync(0xffffffffu, failed) : named_bar_or(kBarKV, KVT, failed)) {
+        failed = true;
+        break;
+      }
       const uint32_t kb = sbase + prm.off_kv + b * prm.kv_buf_bytes;
       const uint32_t vb = kb + NP * kv_panel;
-      const int bl = prm.pv.block_len;
       bool bad = false;
-      for (int bi = 0; bi < prm.pv.blocks_per_pair; ++bi) {
-        const int32_t blk = pool_block_id(prm.pv, p, bi);
+      for (int bi = 0; bi < bpp; ++bi) {
+        const int32_t blk = pool_block_id(prm.pv, p, bi);  // the same in every lane
         if (!pool_block_ok(prm.pv, blk)) {
           bad = true;
           continue;
         }
         const bf16* ks = pool_row(prm.pv, blk, g, 0, 0);
         const bf16* vs = pool_row(prm.pv, blk, g, 1, 0);
-        for (int w = tid; w < bl * CPR; w += kCompute) {
+        for (int w = kt; w < bl * CPR; w += KVT) {
           const int t = w / CPR, c = w % CPR;
           const uint32_t o = (c >> 3) * kv_panel + swz128(bi * bl + t, c & 7);
           cp_async16(kb + o, ks + t * D + c * 8);
           cp_async16(vb + o, vs + t * D + c * 8);
         }
       }
-      const size_t row_stride = (size_t)prm.Hkv * D;  // between consecutive new tokens
       const bf16* kn = prm.k_new + ((size_t)p * l * prm.Hkv + g) * D;
       const bf16* vn = prm.v_new + ((size_t)p * l * prm.Hkv + g) * D;
-      for (int w = tid; w < l * (CPR / 2); w += kCompute) {
-        const int t = w / (CPR / 2), J = w % (CPR / 2);
-        const bf16* src = kn + t * row_stride + J * 8;
-        cp_async16(chunk_addr(kb, kv_panel, C + t, J), src);
-        cp_async16(chunk_addr(kb, kv_panel, C + t, J + CPR / 2), src + HALF);
-      }
-      for (int w = tid; w < l * CPR; w += kCompute) {
+      for (int w = kt; w < l * CPR; w += KVT) {
         const int t = w / CPR, c = w % CPR;
+        cp_async16(chunk_addr(kb, kv_panel, C + t, c), kn + t * row_stride + c * 8);
         cp_async16(chunk_addr(vb, kv_panel, C + t, c), vn + t * row_stride + c * 8);
       }
       cp_async_commit();
-      return bad;
-    };
-    // Unit k's K/V have landed (each thread waited for its own copies): convert
-    // this thread's cached key chunks to f16 and rotate its new key chunk
-    // pairs with the table of the unit's positions, in place.
-    auto prepare_unit = [&](int k, bool bad) {
+      uint8_t* table = table_of(b);
       if (prm.pos_offset && !prm.rotated) {
-        named_bar_sync(kBarCompute, kCompute);  // nobody still reads the previous table
-        build_base(prm.pos_offset[unit_of(k) / prm.Hkv]);
-        named_bar_sync(kBarCompute, kCompute);
-        build_table(kCompute);
-        named_bar_sync(kBarCompute, kCompute);
+        // this unit's angle table (the compute warps read it for q as well)
+        if (kt < HALF) base_ang[HALF + kt] = rope_reduce(prm.pos_offset[p], prm.ex.theta[kt]);
+        if (KVT < HALF && kt + KVT < HALF)
+          base_ang[HALF + kt + KVT] = rope_reduce(prm.pos_offset[p], prm.ex.theta[kt + KVT]);
+        kv_sync();
+        for (int idx = kt; idx < l * (HALF / 2); idx += KVT) {
+          const int t = idx / (HALF / 2), jp = idx - t * (HALF / 2);
+          float s0, c0, s1, c1;
+          sincosf(fmaf((float)t, prm.inv_freq[2 * jp], base_ang[HALF + 2 * jp]), &s0, &c0);
+          sincosf(fmaf((float)t, prm.inv_freq[2 * jp + 1], base_ang[HALF + 2 * jp + 1]), &s1, &c1);
+          *reinterpret_cast<float4*>(table + t * prm.tab_stride + jp * 16) = make_float4(c0, c1, s0, s1);
+        }
       }
+      cp_async_wait_all();
+      kv_sync();  // every K/V thread's copies (and table rows) have landed
       if (!bad && !prm.rotated) {
-        const uint32_t kb = sbase + prm.off_kv + (k & 1) * prm.kv_buf_bytes;
-        const int bl = prm.pv.block_len;
-        for (int bi = 0; bi < prm.pv.blocks_per_pair; ++bi) {
-          for (int w = tid; w < bl * CPR; w += kCompute) {
+        for (int bi = 0; bi < bpp; ++bi) {
+          for (int w = kt; w < bl * CPR; w += KVT) {
             const int t = w / CPR, c = w % CPR;
             const uint32_t a = chunk_addr(kb, kv_panel, bi * bl + t, c);
             const uint4 v = lds16(a);
@@ -483,19 +511,35 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
                                                  bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w))));
           }
         }
-        for (int w = tid; w < l * (CPR / 2); w += kCompute) {
+        for (int w = kt; w < l * (CPR / 2); w += KVT) {
           const int t = w / (CPR / 2), J = w % (CPR / 2);
           const uint32_t a0 = chunk_addr(kb, kv_panel, C + t, J);
           const uint32_t a1 = chunk_addr(kb, kv_panel, C + t, J + CPR / 2);
           uint64_t xr[4], yr[4];
-          rope_chunk(lds16(a0), lds16(a1), tab + t * prm.tab_stride, 8 * J, xr, yr);
+          rope_chunk(lds16(a0), lds16(a1), table + t * prm.tab_stride, 8 * J, xr, yr);
           sts16(a0, f16_chunk_or_nan(make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]),
                                                 f2_to_f16x2(xr[2]), f2_to_f16x2(xr[3]))));
           sts16(a1, f16_chunk_or_nan(make_uint4(f2_to_f16x2(yr[0]), f2_to_f16x2(yr[1]),
                                                 f2_to_f16x2(yr[2]), f2_to_f16x2(yr[3]))));
         }
       }
-      fence_proxy_async_smem();  // before the rope_done arrival that hands K to the MMA
+      if (kt == 0) {
+        bars->unit_bad[b] = bad ? 1 : 0;
+        if (bad) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
+      }
+      fence_proxy_async_smem();  // the tensor core reads K/V next
+      kv_sync();
+      if (kt == 0) mbar_arrive(&bars->kv_ready[b]);
+    }
+    if (failed && kt == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    cp_async_wait_all();
+  } else {
+    // ================================================================ compute
+    const int h = warp >> 2;               // which half of the row's columns
+    const int r = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    auto chunk_addr = [](uint32_t base, uint32_t pstride, int row, int J) {
+      return base + (J >> 3) * pstride + swz128(row, J & 7);
     };
     // A wait that has timed out once turns every later wait of this thread
     // into a no-op, so a stuck pipeline ends in bounded time (the status word
@@ -509,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
     // Rotate row r of tile i's q (this half's chunk pairs) into the stage as f16.
     // Rows past the tile's tokens hold zeros (TMA fill, or set-up for rows no
     // box reaches), so they come out zero without a select.
-    auto rope_tile = [&](int i, int mt) {
+    auto rope_tile = [&](int i, int mt, const uint8_t* tab) {
       const int s = stage_of(i);
       const uint32_t stage = sbase + s * prm.stage_bytes;
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
@@ -551,23 +595,21 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       mbar_arrive(&bars->rope_done);
     };
 
-    // out-of-range block id in the unit of K/V buffer 0 / 1 (this thread's view
-    // until prepare_unit makes it the unit's)
-    bool bad0 = false, bad1 = false;
+    // unit k's K/V buffer is ready: k-th use of buffer k & 1
+    bool bad_unit = false;  // the current unit has a block id out of range
+    auto unit_ready = [&](int k) -> bool {
+      wait(&bars->kv_ready[k & 1], (uint32_t)(k >> 1) & 1u);
+      return bars->unit_bad[k & 1] != 0;
+    };
+    bool bad_next = false;
     if (my_units > 0) {
-      bad0 = stage_kv(unit_of(0), 0);
-      if (my_units > 1) {
-        bad1 = stage_kv(unit_of(1), 1);
-        cp_async_wait_group<1>();
-      } else {
-        cp_async_wait_group<0>();
-      }
-      prepare_unit(0, bad0);
-      rope_tile(0, 0);
+      bad_unit = unit_ready(0);
+      rope_tile(0, 0, table_of(0));
     }
     for (int i = 0, k = 0, mt = 0; i < my_tiles; ++i, mt = (mt + 1 == n_mt) ? (++k, 0) : mt + 1) {
       const uint32_t par = (uint32_t)i & 1u;
-      const bool bad = (k & 1) ? bad1 : bad0;
+      if (mt == 0 && i > 0) bad_unit = bad_next;
+      const bool bad = bad_unit;
       const int t0 = mt * Tm, toks = min(Tm, l - t0);
       const bool valid = row_tok < toks;
       const bool wlive = (warp & 3) * 32 < toks * G;  // warp-uniform, same for the row's partner
@@ -658,11 +700,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
       mbar_arrive(&bars->p_done);
       // ---- next tile's K/V and q rotation (overlaps O = P V on the tensor core)
       if (i + 1 < my_tiles) {
-        if (mt + 1 == n_mt) {  // the next tile opens unit k+1
-          cp_async_wait_group<0>();
-          prepare_unit(k + 1, ((k + 1) & 1) ? bad1 : bad0);
-        }
-        rope_tile(i + 1, mt + 1 == n_mt ? 0 : mt + 1);
+        const bool opens = mt + 1 == n_mt;  // the next tile opens unit k+1
+        if (opens) bad_next = unit_ready(k + 1);
+        rope_tile(i + 1, opens ? 0 : mt + 1, table_of(opens ? (k + 1) & 1 : k & 1));
       }
       // ---- O of row r, this half's columns, normalised into the stage
       wait(&bars->o_done, par);
@@ -701,18 +741,11 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && NCH <= 3) ? 2 : 1)
           }
         }
       }
-      if (bad && mt == 0 && tid == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
       fence_proxy_async_smem();
       tc::fence_before_sync();
       mbar_arrive(&bars->o_stored[i & 1]);
-      // ---- the last tile of unit k: its K/V buffer is free for unit k+2
-      if (mt == n_mt - 1 && k + 2 < my_units) {
-        const bool bk = stage_kv(unit_of(k + 2), k & 1);
-        if (k & 1) bad1 = bk; else bad0 = bk;
-      }
     }
     if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
-    cp_async_wait_all();
   }
 
   tc::fence_before_sync();
@@ -761,6 +794,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.Hkv = pb.Hkv;
   prm.G = pb.G;
   prm.C = pb.C;
+  prm.tab_bufs = pb.pos_offset ? 2 : 1;
   prm.Tm = L.Tm;
   prm.n_mt = L.n_mt;
   prm.num_units = pb.P * pb.Hkv;
@@ -800,7 +834,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   const int per_sm = (D == 64 && L.tmem_cols == 256 && L.bytes <= kTwoPerSmBytes) ? 2 : 1;
   const int64_t units = (int64_t)pb.P * pb.Hkv;
   const int grid = (int)(units < (int64_t)sms * per_sm ? units : (int64_t)sms * per_sm);
-  prefill_tc_kernel<D, NCH, NS><<<grid, kThreads, L.bytes, stream>>>(tm_q, tm_o, prm);
+  prefill_tc_kernel<D, NCH, NS><<<grid, threads_of(D), L.bytes, stream>>>(tm_q, tm_o, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
