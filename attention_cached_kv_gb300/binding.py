@@ -20,6 +20,7 @@ OK, ERR_NULL, ERR_DIMS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_LAUNCH, ERR_SCRATCH = 0,
 NOALLOC_SCRATCH_BYTES = 64 << 20  # GIST_ATTN_NOALLOC_SCRATCH_BYTES
 STATUS_BAD_BLOCK, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4
 FLAG_PREROTATED = 1
+FLAG_TEST_WITHHOLD = 2  # tests of the timeout path only (see the header)
 
 EXPORTS = ("gist_attn_fwd", "gist_attn_workspace_bytes", "gist_attn_fwd_ws", "gist_attn_fwd_noalloc", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
            "gist_attn_fwd_gist_mask", "gist_kv_store", "gist_qkv_rope", "gist_out_proj",

@@ -70,7 +70,7 @@ int check_dims(const gist_attn_dims* dm, Problem* pb) {
   pb->C = (int)C;
   const double scale = d.softmax_scale > 0.f ? (double)d.softmax_scale : 1.0 / sqrt((double)d.head_dim);
   pb->scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
-  if (d.flags & ~GIST_ATTN_FLAG_PREROTATED) return GIST_ATTN_ERR_DIMS;
+  if (d.flags & ~(GIST_ATTN_FLAG_PREROTATED | GIST_ATTN_FLAG_TEST_WITHHOLD)) return GIST_ATTN_ERR_DIMS;
   // pre-rotated inputs: every rotation angle is 0 (cos 1, sin 0), the identity
   const bool rotate = !(d.flags & GIST_ATTN_FLAG_PREROTATED);
   for (int j = 0; j < 64; ++j) {

@@ -33,6 +33,12 @@
 // Each warp records log2 of its share of every chunk against its running max;
 // the shares are brought to the final max and normaliser at the end.
 //
+// A wait on a chunk that runs out (after wait_ns) ends the walk for the whole
+// CTA: no further copies are issued, every copy already issued is waited for
+// once more (bounded), and GIST_ATTN_STATUS_TIMEOUT is reported; the outputs
+// are then unspecified.  (GIST_ATTN_FLAG_TEST_WITHHOLD withholds the first
+// chunk's copy and shortens wait_ns, so a test can walk this path.)
+//
 // Pages: [Suffix page] icman.com.cn news 64898;
 //        [KV page] "为什么自回归推理缓存 KV，而不缓存历史 Q？".
 #include <math.h>
@@ -63,6 +69,8 @@ struct LongParams {
   const int32_t* pos_offset;
   int32_t* status;
   int Hq, Hkv, C;
+  int withhold;       // test hook: do not issue chunk 0's copy
+  uint64_t wait_ns;   // limit of every wait on a copy
   float scale_log2;
   double theta[64];  // RoPE frequencies (angles reduced in double)
 };
@@ -172,8 +180,12 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
     bulk_g2s(ring0 + s * kStageBytes, krow, kChunk * kRow, &full[s]);
     bulk_g2s(ring0 + s * kStageBytes + kChunk * kRow, vrow, kChunk * kRow, &full[s]);
   };
-  if (tid == 0)
-    for (int ci = 0; ci < kStages && ci < n_chunks; ++ci) issue(ci);
+  int issued = 0;  // thread 0: chunks whose copies were issued (0 .. issued - 1)
+  if (tid == 0) {
+    for (int ci = 0; ci < kStages && ci < n_chunks; ++ci)
+      if (!(prm.withhold && ci == 0)) issue(ci);
+    issued = min(kStages, n_chunks);
+  }
 
   // this lane's slice of the query: elements (lane % 8) * QE ..
   const int kg = lane >> 3, sl = lane & 7;
@@ -252,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
     }
   };
 
-  bool ok = true;
+  bool failed = false;
+  int consumed = 0;  // chunks whose stages this CTA has finished with
   if constexpr (FP8) {
     // Two 16-key chunks per step (an fp8 chunk is half the bytes of a bf16 one):
     // one online-softmax update and one barrier per 8 keys of a warp.
@@ -309,8 +322,13 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
     for (int ci = 0; ci < n_chunks; ci += 2) {
       const bool two = ci + 1 < n_chunks;  // uniform
       const int s0 = ci % kStages, s1 = (ci + 1) % kStages;
-      ok = mbar_wait(&full[s0], (uint32_t)(ci / kStages) & 1u) && ok;
-      if (two) ok = mbar_wait(&full[s1], (uint32_t)((ci + 1) / kStages) & 1u) && ok;
+      if (!mbar_wait(&full[s0], (uint32_t)(ci / kStages) & 1u, prm.wait_ns)) failed = true;
+      if (two && !failed && !mbar_wait(&full[s1], (uint32_t)((ci + 1) / kStages) & 1u, prm.wait_ns))
+        failed = true;
+      if (__syncthreads_or(failed)) {
+        failed = true;
+        break;
+      }
       const uint8_t* st0 = ring + s0 * kStageBytes;
       const uint8_t* st1 = ring + s1 * kStageBytes;
       const int b0 = (ci * kChunk) / bl, b1 = ((ci + 1) * kChunk) / bl;
@@ -339,15 +357,20 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
         }
       }
       __syncthreads();  // every warp is done with both stages
+      consumed = ci + (two ? 2 : 1);
       if (tid == 0) {
         if (ci + kStages < n_chunks) issue(ci + kStages);
         if (ci + 1 + kStages < n_chunks) issue(ci + 1 + kStages);
+        issued = min(n_chunks, consumed + kStages);
       }
     }
   } else {
     for (int ci = 0; ci < n_chunks; ++ci) {
       const int s = ci % kStages;
-      ok = mbar_wait(&full[s], (uint32_t)(ci / kStages) & 1u) && ok;
+      if (__syncthreads_or(!mbar_wait(&full[s], (uint32_t)(ci / kStages) & 1u, prm.wait_ns))) {
+        failed = true;
+        break;
+      }
       const uint8_t* stage = ring + s * kStageBytes;
       float acc = 0.f;
       if constexpr (FP8) {
@@ -396,7 +419,11 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
         if (lane == 0) chunk_lg[ci][warp] = last_share;
       }
       __syncthreads();  // every warp is done with stage s
-      if (tid == 0 && ci + kStages < n_chunks) issue(ci + kStages);
+      consumed = ci + 1;
+      if (tid == 0) {
+        if (ci + kStages < n_chunks) issue(ci + kStages);
+        issued = min(n_chunks, consumed + kStages);
+      }
     }
   }
   // the new token's own key and value (warp 0, group 0)
@@ -455,7 +482,13 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
       mass[b] = acc * invL;
     }
   }
-  if (!ok && tid == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+  if (failed && tid == 0) {
+    report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+    // every copy issued and not consumed lands in its stage before the CTA
+    // leaves (a withheld one is skipped): one more bounded wait each
+    for (int ci = consumed; ci < issued; ++ci)
+      if (!(prm.withhold && ci == 0)) mbar_wait(&full[ci % kStages], (uint32_t)(ci / kStages) & 1u, prm.wait_ns);
+  }
 }
 
 template <int D, bool FP8, bool STATS>
@@ -476,6 +509,8 @@ int launch_d(const Problem& pb, const float* kv_scale, float* block_mass, cudaSt
   prm.C = pb.C;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.theta[j] = pb.inv_freq_d[j];
+  prm.withhold = (pb.flags & GIST_ATTN_FLAG_TEST_WITHHOLD) ? 1 : 0;
+  prm.wait_ns = prm.withhold ? 20000000ull : kWaitLimitNs;
   const int64_t grid = (int64_t)pb.P * pb.Hkv;
   if (grid > 0x7fffffff) return GIST_ATTN_ERR_UNSUPPORTED;
   decode_long_kernel<D, FP8, STATS><<<(unsigned)grid, kThreads, 0, stream>>>(prm);

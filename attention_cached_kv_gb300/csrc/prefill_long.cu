@@ -131,6 +131,7 @@ struct LBars {
   uint64_t qfull[2], kfull[2], kfree[2], vfull[2], vfree[2];
   uint64_t s_done, p_done, o_done, o_stored[2];
   uint64_t q_ready[2];  // q rotated in its stage (when it arrives unrotated)
+  uint64_t drain;  // the MMA warp's last commit: no MMA in flight at teardown
   uint32_t tmem_slot;
   int flagged;  // a row of this CTA came out non-finite (repaired at the end)
 };
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&bars->s_done, 1);
     mbar_init(&bars->p_done, kCompute);
     mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
     bars->flagged = 0;
     fence_mbar_init();
   }
@@ -348,6 +350,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       load_k();
       load_v();
     }
+    // every MMA this warp issued completes before the CTA tears TMEM down
+    // (after a timed-out wait too): one commit, one bounded wait
+    if (lane == 0) tc::commit(smem_u32(&bars->drain));
+    __syncwarp();
+    if (!mbar_wait(&bars->drain, 0)) failed = true;
+    if (failed && lane == 0) {
+      // K and V loads issued and not consumed land before the CTA leaves
+      for (int j = sx; j < kc; ++j) mbar_wait(&bars->kfull[j & 1], (uint32_t)(j >> 1) & 1u);
+      for (int j = px; j < vc; ++j) mbar_wait(&bars->vfull[j & 1], (uint32_t)(j >> 1) & 1u);
+    }
     if (lane == 0 && failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     __syncwarp();
   } else if (warp == 9) {
@@ -373,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     load_q();
     load_q();
-    for (int i = 0; i < my_tiles; ++i) {
+    int i = 0;  // tiles stored
+    for (; i < my_tiles; ++i) {
       if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored[i & 1], (uint32_t)(i >> 1) & 1u))) {
         failed = true;
         break;
@@ -390,7 +403,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       bulk_wait_all();
       fence_proxy_async_global();  // the stores are visible to the repair step
-      if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+      if (failed) {
+        report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+        // q loads issued for tiles i .. qi - 1 land before the CTA leaves
+        for (int t = i; t < qi; ++t) mbar_wait(&bars->qfull[t & 1], (uint32_t)(t >> 1) & 1u);
+      }
     }
     __syncwarp();
   } else {

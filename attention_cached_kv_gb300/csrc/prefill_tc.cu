@@ -228,6 +228,7 @@ struct Bars {
   uint64_t kv_ready[2];  // K/V warp -> compute warps: buffer b holds its unit, prepared
   uint64_t kv_free[2];   // tensor core (commit after the unit's last P V) -> K/V warp
   int unit_bad[2];       // buffer b's unit has a block id out of range
+  uint64_t drain;  // the MMA warp's last commit: no MMA in flight at teardown
   uint32_t tmem_slot;
   int flagged;  // a row of this CTA came out non-finite (repaired at the end)
 };
@@ -281,6 +282,7 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
     mbar_init(&bars->s_done, 1);
     mbar_init(&bars->p_done, kCompute);
     mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
     mbar_init(&bars->o_stored[0], kCompute);
     mbar_init(&bars->o_stored[1], kCompute);
     for (int b = 0; b < 2; ++b) {
@@ -378,6 +380,11 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
       }
       __syncwarp();
     }
+    // every MMA this warp issued completes before the CTA tears TMEM down
+    // (after a timed-out wait too): one commit, one bounded wait
+    if (lane == 0) tc::commit(smem_u32(&bars->drain));
+    __syncwarp();
+    if (!mbar_wait(&bars->drain, 0)) failed = true;
     if (lane == 0 && failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
     __syncwarp();
   } else if (warp == 9) {
@@ -406,7 +413,8 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
       tma_prefetch_map(&tm_o);
       for (int i = 0; i < NS; ++i) load_tile(i);
     }
-    for (int i = 0; i < my_tiles; ++i) {
+    int i = 0;  // tiles stored
+    for (; i < my_tiles; ++i) {
       if (__any_sync(0xffffffffu, !mbar_wait(&bars->o_stored[i & 1], (uint32_t)(i >> 1) & 1u))) {
         failed = true;
         break;
@@ -430,7 +438,11 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
     if (lane == 0) {
       bulk_wait_all();
       fence_proxy_async_global();  // the stores are visible to the repair step
-      if (failed) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+      if (failed) {
+        report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
+        // q loads issued for tiles i .. i + NS - 1 land before the CTA leaves
+        for (int t = i; t < i + NS && t < my_tiles; ++t) mbar_wait(&bars->qfull[stage_of(t)], stage_round(t));
+      }
     }
     __syncwarp();
   } else if (warp >= 10) {

@@ -91,6 +91,13 @@ typedef struct {
 /* dims->flags: q and k_new arrive already rotated at their positions (for example
  * by gist_qkv_rope), so the attention and the pool writers apply no RoPE. */
 #define GIST_ATTN_FLAG_PREROTATED 1
+/* dims->flags, for tests of the error path only: the paged MHA decode step
+ * (gist_attn_fwd with l = 1, equal head counts, 64+ cached rows in 16-row
+ * blocks) withholds the copy of its first cached chunk and shortens its
+ * bounded waits to 20 ms, so every CTA gives up, waits for the copies it did
+ * issue, and reports GIST_ATTN_STATUS_TIMEOUT; the outputs are then
+ * unspecified.  Other kernels ignore the flag.  Nothing faults or hangs. */
+#define GIST_ATTN_FLAG_TEST_WITHHOLD 2
 
 /*
  * gist_attn_fwd -- one layer of attention for all pairs, one launch on `stream`.

@@ -100,3 +100,32 @@ def test_append_rejects_bad_slot():
     changed_blocks = torch.nonzero((wl.kv_pool != before).flatten(1).any(1)).flatten().tolist()
     allowed = {int(wl.block_table[0, 0]), int(wl.block_table[2, 0])}
     assert set(changed_blocks) <= allowed
+
+
+def test_a_wait_that_runs_out_reports_timeout_and_leaves_the_context_usable():
+    """GIST_ATTN_FLAG_TEST_WITHHOLD makes the paged decode withhold its first
+    chunk's copy (nothing faults: a flag that nothing sets): every CTA's bounded
+    wait runs out after 20 ms, it waits for the copies it did issue and reports
+    GIST_ATTN_STATUS_TIMEOUT.  The call ends in bounded time and the next call on
+    the same context is correct."""
+    import time
+    wl = _paged(4, 4, 128, 64, 3, 9, seed=21)
+    dims = dict(wl.dims, layer=1)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    binding.gist_attn_fwd(wl.q, wl.k_new, wl.v_new, wl.kv_pool, None, wl.block_table, None,
+                          dims=dict(dims, flags=binding.FLAG_TEST_WITHHOLD), status=status)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert int(status.item()) & binding.STATUS_TIMEOUT
+    assert elapsed < 5.0, elapsed
+    status.zero_()
+    out = binding.gist_attn_fwd(wl.q, wl.k_new, wl.v_new, wl.kv_pool, None, wl.block_table, None,
+                                dims=dims, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    pool1 = wl.kv_pool[:, 1:2].contiguous()
+    ref = oracle.gist_attn(wl.q, wl.k_new, wl.v_new, pool1, block_table=wl.block_table,
+                           dims=dict(dims, num_layers=1, layer=0))
+    compare(out, ref, "after the timeout")
