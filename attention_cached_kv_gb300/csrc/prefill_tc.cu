@@ -54,15 +54,17 @@ namespace gattn {
 namespace {
 
 constexpr int kCompute = 256;            // 8 compute warps
-// K/V warps: one where two CTAs share an SM (d = 64), four for d = 128, whose
-// units carry twice the rows per byte of staging and whose one CTA per SM
-// leaves registers for them
-__host__ __device__ constexpr int kv_warps(int D) { return D == 64 ? 1 : 4; }
+// Two CTAs share an SM for d = 64 with at most 96 keys (three 16-column chunks
+// per thread); wider tiles and d = 128 run one CTA per SM.
+__host__ __device__ constexpr bool two_per_sm(int D, int NCH) { return D == 64 && NCH <= 3; }
+// K/V warps: one where two CTAs share an SM; four where one CTA per SM leaves
+// registers for them (d = 128 units carry twice the bytes, wide key sets more rows)
+__host__ __device__ constexpr int kv_warps(int D, int NCH) { return two_per_sm(D, NCH) ? 1 : 4; }
 // + the MMA warp, the TMA warp and the K/V warps
-__host__ __device__ constexpr int threads_of(int D) { return kCompute + 64 + 32 * kv_warps(D); }
+__host__ __device__ constexpr int threads_of(int D, int NCH) { return kCompute + 64 + 32 * kv_warps(D, NCH); }
 constexpr uint32_t kBarKV = 1;  // named barrier of the K/V warps
 constexpr int kMaxStages = 3;  // q/O stages: 3, or 2 where that lets two CTAs share an SM
-constexpr int kMaxKeys = 128;
+constexpr int kMaxKeys = 288;  // S, P and O of a 128-row tile within 512 TMEM columns
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxBlocksPerPair = 64;
 
@@ -74,6 +76,7 @@ struct TcParams {
   int32_t* status;
   int l, Hkv, G, C;
   int tab_bufs;   // angle tables: 1 (one position layout for every pair), 2 (per unit)
+  int tab_rows;   // rows of a table: l, or 16 + ceil(l / 16) for a two-level one
   int Tm;         // tokens per M-tile
   int n_mt;       // M-tiles per unit
   int num_units;  // P * Hkv
@@ -89,7 +92,7 @@ struct TcParams {
 };
 
 struct Layout {
-  int Tm, n_mt, kv_rows, stages;
+  int Tm, n_mt, kv_rows, stages, tab_rows;
   uint32_t stage_bytes, off_kv, kv_buf_bytes, off_tab, tab_stride, off_red, off_bias, off_base,
       off_bar, bytes;
   uint32_t p_col, o_col, tmem_cols;
@@ -113,8 +116,12 @@ Layout plan_stages(const Problem& pb, int stages) {
   L.tab_stride = (uint32_t)(pb.d / 4) * 16 + 16;
   // one table when every pair's new tokens sit at the same positions, else
   // one per K/V buffer (the K/V warp fills the next unit's while the compute
-  // warps read the current one's)
-  off += (pb.pos_offset ? 2u : 1u) * (uint32_t)pb.l * L.tab_stride;
+  // warps read the current one's).  Tiles of more than 128 keys (long new
+  // blocks) take a two-level table: rows t < 16 hold the angles of tokens
+  // 0..15, rows 16 + a those of the offsets 16 a, and a token's angle is the
+  // sum of its two (angle addition in the rotation).
+  L.tab_rows = L.kv_rows > 128 ? 16 + (pb.l + 15) / 16 : pb.l;
+  off += (pb.pos_offset ? 2u : 1u) * (uint32_t)L.tab_rows * L.tab_stride;
   L.off_red = off;
   off += 2u * 2 * 128 * 4;  // partial row max and row sum of each half
   L.off_bias = off;
@@ -138,6 +145,7 @@ Layout plan_stages(const Problem& pb, int stages) {
 constexpr uint32_t kTwoPerSmBytes = 113 * 1024;
 Layout plan(const Problem& pb) {
   const Layout L3 = plan_stages(pb, kMaxStages);
+  if (L3.bytes > (uint32_t)kMaxSmem) return plan_stages(pb, 2);  // wide key sets
   // (wider key sets than 96 run one CTA per SM for their registers anyway)
   if (pb.d == 64 && L3.kv_rows <= 96 && L3.tmem_cols == 256 && L3.bytes > kTwoPerSmBytes) {
     const Layout L2 = plan_stages(pb, 2);
@@ -148,15 +156,25 @@ Layout plan(const Problem& pb) {
 
 // Rotate one 16-byte chunk of x (elements j0..j0+7) against its partner chunk y
 // (elements j0+d/2..): (x, y) <- (x cos - y sin, y cos + x sin), fp32 pairs.
-// The table row holds (cos_j, cos_j+1, sin_j, sin_j+1) per frequency pair.
+// The table row holds (cos_j, cos_j+1, sin_j, sin_j+1) per frequency pair; a
+// second row (two-level tables, else null) adds its angles to the first's.
 __device__ __forceinline__ void rope_chunk(const uint4& x, const uint4& y, const uint8_t* trow,
-                                           int j0, uint64_t (&xr)[4], uint64_t (&yr)[4]) {
+                                           const uint8_t* trow_hi, int j0, uint64_t (&xr)[4],
+                                           uint64_t (&yr)[4]) {
   const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const uint4 cs = *reinterpret_cast<const uint4*>(trow + ((j0 >> 1) + e) * 16);
-    const uint64_t c = f2_make(__uint_as_float(cs.x), __uint_as_float(cs.y));
-    const uint64_t sn = f2_make(__uint_as_float(cs.z), __uint_as_float(cs.w));
+    uint64_t c = f2_make(__uint_as_float(cs.x), __uint_as_float(cs.y));
+    uint64_t sn = f2_make(__uint_as_float(cs.z), __uint_as_float(cs.w));
+    if (trow_hi) {
+      const uint4 hs = *reinterpret_cast<const uint4*>(trow_hi + ((j0 >> 1) + e) * 16);
+      const uint64_t hc = f2_make(__uint_as_float(hs.x), __uint_as_float(hs.y));
+      const uint64_t hsn = f2_make(__uint_as_float(hs.z), __uint_as_float(hs.w));
+      const uint64_t c2 = f2_sub(f2_mul(c, hc), f2_mul(sn, hsn));
+      sn = f2_fma(sn, hc, f2_mul(c, hsn));
+      c = c2;
+    }
     const uint64_t xf = bf16x2_to_f2(xw[e]), yf = bf16x2_to_f2(yw[e]);
     xr[e] = f2_sub(f2_mul(xf, c), f2_mul(yf, sn));
     yr[e] = f2_fma(yf, c, f2_mul(xf, sn));
@@ -237,14 +255,15 @@ struct Bars {
 // Registers: each of the 4 SM sub-partitions holds 16 K; two CTAs of 9 warps
 // put 5 warps on one of them (96 registers a thread), one CTA puts 3 (168).
 template <int D, int NCH, int NS>
-__global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
+__global__ void __launch_bounds__(threads_of(D, NCH), two_per_sm(D, NCH) ? 2 : 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_o,
                       const __grid_constant__ TcParams prm) {
   constexpr int NP = D / 64;   // 64-column panels
   constexpr int CPR = D / 8;   // 16-byte chunks per row
-  constexpr int kThreads = threads_of(D);
-  constexpr int KVT = 32 * kv_warps(D);  // K/V threads
+  constexpr int kThreads = threads_of(D, NCH);
+  constexpr bool TAB2 = NCH > 4;  // two-level angle tables (tiles of more than 128 keys)
+  constexpr int KVT = 32 * kv_warps(D, NCH);  // K/V threads
   constexpr int HALF = D / 2;
   constexpr float kNegInf = -INFINITY;
   constexpr uint32_t kPanel = 128 * 128;  // one 128-row Q panel
@@ -313,23 +332,43 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
   auto build_base = [&](int pos_base) {
     if (tid < HALF) base_ang[tid] = rope_reduce(pos_base, prm.ex.theta[tid]);
   };
-  auto build_table = [&](uint8_t* table, int first, int nthreads) {
-    for (int idx = first; idx < l * (HALF / 2); idx += nthreads) {
-      const int t = idx / (HALF / 2), jp = idx - t * (HALF / 2);
+  // Rows [r0, r1) of a table: a token row t holds (cos, sin) of its base angle
+  // ba (reduced in double) plus t theta_j; a two-level table's rows 16 + a
+  // hold the angles of 16 a theta_j alone (reduced in double).
+  auto fill_rows = [&](uint8_t* table, const float* ba, int r0, int r1, int first, int nthreads) {
+    for (int idx = first; idx < (r1 - r0) * (HALF / 2); idx += nthreads) {
+      const int row = r0 + idx / (HALF / 2), jp = idx % (HALF / 2);
+      float a0, a1;
+      if (TAB2 && row >= 16) {
+        a0 = rope_reduce(16 * (row - 16), prm.ex.theta[2 * jp]);
+        a1 = rope_reduce(16 * (row - 16), prm.ex.theta[2 * jp + 1]);
+      } else {
+        a0 = fmaf((float)row, prm.inv_freq[2 * jp], ba[2 * jp]);
+        a1 = fmaf((float)row, prm.inv_freq[2 * jp + 1], ba[2 * jp + 1]);
+      }
       float s0, c0, s1, c1;
-      sincosf(fmaf((float)t, prm.inv_freq[2 * jp], base_ang[2 * jp]), &s0, &c0);
-      sincosf(fmaf((float)t, prm.inv_freq[2 * jp + 1], base_ang[2 * jp + 1]), &s1, &c1);
-      *reinterpret_cast<float4*>(table + t * prm.tab_stride + jp * 16) = make_float4(c0, c1, s0, s1);
+      sincosf(a0, &s0, &c0);
+      sincosf(a1, &s1, &c1);
+      *reinterpret_cast<float4*>(table + row * prm.tab_stride + jp * 16) = make_float4(c0, c1, s0, s1);
     }
   };
   // the angle table of K/V buffer b's unit
   auto table_of = [&](int b) -> uint8_t* {
-    return smem + prm.off_tab + (prm.tab_bufs == 2 ? b : 0) * (uint32_t)l * prm.tab_stride;
+    return smem + prm.off_tab + (prm.tab_bufs == 2 ? b : 0) * (uint32_t)prm.tab_rows * prm.tab_stride;
+  };
+  // the table rows of new token t: the token's own (or its offset t mod 16)
+  // and, for two-level tables, that of 16 floor(t / 16)
+  auto trow_lo = [&](const uint8_t* table, int t) { return table + (TAB2 ? (t & 15) : t) * prm.tab_stride; };
+  auto trow_hi = [&](const uint8_t* table, int t) -> const uint8_t* {
+    return TAB2 ? table + (16 + (t >> 4)) * prm.tab_stride : nullptr;
   };
   if (!prm.pos_offset) {
     build_base(C);
     __syncthreads();
-    build_table(table_of(0), tid, kThreads);
+    fill_rows(table_of(0), base_ang, 0, prm.tab_rows, tid, kThreads);
+  } else if (TAB2) {
+    // the offset rows of both tables do not depend on the unit's position
+    for (int b = 0; b < 2; ++b) fill_rows(table_of(b), base_ang, 16, prm.tab_rows, tid, kThreads);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -352,14 +391,23 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
       if (__any_sync(0xffffffffu, !mbar_wait(&bars->rope_done, par))) { failed = true; break; }
       tc::fence_after_sync();
       if (lane == 0) {
-        const uint32_t idesc =
-            prm.rotated ? tc::idesc_bf16_f32(128, N, 0) : tc::idesc_f16_f32(128, N, 0);
+        // one MMA covers at most 256 keys: wider tiles take a second one for
+        // keys 256.. (K rows 256.. start 32 swizzle atoms further on)
+        const int N1 = min(N, 256);
+        const uint32_t id1 =
+            prm.rotated ? tc::idesc_bf16_f32(128, N1, 0) : tc::idesc_f16_f32(128, N1, 0);
+        const uint32_t id2 = prm.rotated ? tc::idesc_bf16_f32(128, N > 256 ? N - 256 : 16, 0)
+                                         : tc::idesc_f16_f32(128, N > 256 ? N - 256 : 16, 0);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = (uint32_t)(ks & 3) * 32;  // 16 columns = 32 bytes
           const uint64_t a = tc::smem_desc_sw128(stage + (ks >> 2) * kPanel + koff, 16, 1024);
           const uint64_t bd = tc::smem_desc_sw128(kb + (ks >> 2) * kv_panel + koff, 16, 1024);
-          tc::mma_ss(tmem, a, bd, idesc, ks > 0);
+          tc::mma_ss(tmem, a, bd, id1, ks > 0);
+          if (N > 256) {
+            const uint64_t bd2 = tc::smem_desc_sw128(kb + (ks >> 2) * kv_panel + 256 * 128 + koff, 16, 1024);
+            tc::mma_ss(tmem + 256, a, bd2, id2, ks > 0);
+          }
         }
         tc::commit(smem_u32(&bars->s_done));
       }
@@ -503,13 +551,7 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
         if (KVT < HALF && kt + KVT < HALF)
           base_ang[HALF + kt + KVT] = rope_reduce(prm.pos_offset[p], prm.ex.theta[kt + KVT]);
         kv_sync();
-        for (int idx = kt; idx < l * (HALF / 2); idx += KVT) {
-          const int t = idx / (HALF / 2), jp = idx - t * (HALF / 2);
-          float s0, c0, s1, c1;
-          sincosf(fmaf((float)t, prm.inv_freq[2 * jp], base_ang[HALF + 2 * jp]), &s0, &c0);
-          sincosf(fmaf((float)t, prm.inv_freq[2 * jp + 1], base_ang[HALF + 2 * jp + 1]), &s1, &c1);
-          *reinterpret_cast<float4*>(table + t * prm.tab_stride + jp * 16) = make_float4(c0, c1, s0, s1);
-        }
+        fill_rows(table, base_ang + HALF, 0, TAB2 ? 16 : l, kt, KVT);
       }
       cp_async_wait_all();
       kv_sync();  // every K/V thread's copies (and table rows) have landed
@@ -528,7 +570,7 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
           const uint32_t a0 = chunk_addr(kb, kv_panel, C + t, J);
           const uint32_t a1 = chunk_addr(kb, kv_panel, C + t, J + CPR / 2);
           uint64_t xr[4], yr[4];
-          rope_chunk(lds16(a0), lds16(a1), table + t * prm.tab_stride, 8 * J, xr, yr);
+          rope_chunk(lds16(a0), lds16(a1), trow_lo(table, t), trow_hi(table, t), 8 * J, xr, yr);
           sts16(a0, f16_chunk_or_nan(make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]),
                                                 f2_to_f16x2(xr[2]), f2_to_f16x2(xr[3]))));
           sts16(a1, f16_chunk_or_nan(make_uint4(f2_to_f16x2(yr[0]), f2_to_f16x2(yr[1]),
@@ -580,7 +622,8 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
         return;
       }
       constexpr int JH = CPR / 4;  // chunk pairs per half
-      const uint8_t* trow = tab + (t0 + tt) * prm.tab_stride;
+      const uint8_t* trow = trow_lo(tab, t0 + tt);
+      const uint8_t* trh = trow_hi(tab, t0 + tt);
       // All of this thread's chunks are read before the first store, and the
       // stores leave the table reads free to move, so one shared-memory round
       // trip covers the whole row half.
@@ -594,7 +637,7 @@ __global__ void __launch_bounds__(threads_of(D), (D == 64 && NCH <= 3) ? 2 : 1)
       for (int jj = 0; jj < JH; ++jj) {
         const int J = h * JH + jj;
         uint64_t xr[4], yr[4];
-        rope_chunk(xs[jj], ys[jj], trow, 8 * J, xr, yr);
+        rope_chunk(xs[jj], ys[jj], trow, trh, 8 * J, xr, yr);
         sts16_ordered(chunk_addr(stage, kPanel, r, J),
                       make_uint4(f2_to_f16x2(xr[0]), f2_to_f16x2(xr[1]), f2_to_f16x2(xr[2]),
                                  f2_to_f16x2(xr[3])));
@@ -807,6 +850,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.G = pb.G;
   prm.C = pb.C;
   prm.tab_bufs = pb.pos_offset ? 2 : 1;
+  prm.tab_rows = L.tab_rows;
   prm.Tm = L.Tm;
   prm.n_mt = L.n_mt;
   prm.num_units = pb.P * pb.Hkv;
@@ -843,10 +887,10 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
     return GIST_ATTN_ERR_LAUNCH;
   // Two CTAs per SM only when both fit: two 256-column TMEM allocations and
   // shared memory for two.  A larger TMEM plan or shared memory means one.
-  const int per_sm = (D == 64 && L.tmem_cols == 256 && L.bytes <= kTwoPerSmBytes) ? 2 : 1;
+  const int per_sm = (two_per_sm(D, NCH) && L.tmem_cols == 256 && L.bytes <= kTwoPerSmBytes) ? 2 : 1;
   const int64_t units = (int64_t)pb.P * pb.Hkv;
   const int grid = (int)(units < (int64_t)sms * per_sm ? units : (int64_t)sms * per_sm);
-  prefill_tc_kernel<D, NCH, NS><<<grid, threads_of(D), L.bytes, stream>>>(tm_q, tm_o, prm);
+  prefill_tc_kernel<D, NCH, NS><<<grid, threads_of(D, NCH), L.bytes, stream>>>(tm_q, tm_o, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
@@ -857,21 +901,26 @@ bool prefill_tc_fits(const Problem& pb) {
   if (pb.blocks_per_pair > kMaxBlocksPerPair) return false;
   if (pb.d != 64 && pb.d != 128) return false;
   if ((int64_t)pb.P * pb.Hkv > 0x7fffffff) return false;
-  return plan(pb).bytes <= (uint32_t)kMaxSmem;
+  const Layout L = plan(pb);
+  if (L.o_col + pb.d > 512) return false;  // S, P and O within the SM's TMEM
+  if (pb.d == 128 && L.kv_rows > 128) return false;  // (built for at most 4 chunks per thread)
+  return L.bytes <= (uint32_t)kMaxSmem;
 }
 
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream) {
-  const int chunks = (plan(pb).kv_rows / 16 + 1) / 2;  // per thread: chunks h, h+2, ...
+  const Layout L = plan(pb);
+  const int chunks = (L.kv_rows / 16 + 1) / 2;  // per thread: chunks h, h+2, ...
   if (pb.d == 64) {
     if (chunks <= 2) return launch_d<64, 2, 3>(pb, stream);
-    if (chunks <= 3)
-      return plan(pb).stages == 2 ? launch_d<64, 3, 2>(pb, stream) : launch_d<64, 3, 3>(pb, stream);
-    return launch_d<64, 4, 3>(pb, stream);
+    if (chunks <= 3) return L.stages == 2 ? launch_d<64, 3, 2>(pb, stream) : launch_d<64, 3, 3>(pb, stream);
+    if (chunks <= 4) return launch_d<64, 4, 3>(pb, stream);
+    if (chunks <= 6) return L.stages == 2 ? launch_d<64, 6, 2>(pb, stream) : launch_d<64, 6, 3>(pb, stream);
+    return L.stages == 2 ? launch_d<64, 9, 2>(pb, stream) : launch_d<64, 9, 3>(pb, stream);
   }
-  if (pb.d == 128) {
-    if (chunks <= 2) return launch_d<128, 2, 3>(pb, stream);
-    if (chunks <= 3) return launch_d<128, 3, 3>(pb, stream);
-    return launch_d<128, 4, 3>(pb, stream);
+  if (pb.d == 128) {  // (two q stages where a per-unit angle table takes the room of a third)
+    if (chunks <= 2) return L.stages == 2 ? launch_d<128, 2, 2>(pb, stream) : launch_d<128, 2, 3>(pb, stream);
+    if (chunks <= 3) return L.stages == 2 ? launch_d<128, 3, 2>(pb, stream) : launch_d<128, 3, 3>(pb, stream);
+    return L.stages == 2 ? launch_d<128, 4, 2>(pb, stream) : launch_d<128, 4, 3>(pb, stream);
   }
   return GIST_ATTN_ERR_UNSUPPORTED;
 }

@@ -35,12 +35,12 @@ UNIT = "pairs/s"
 FALLBACK_HBM_GBS = 6800.0
 # the dominant kernel of each workload and the sources it is built from
 KERNEL_OF = {
-    "gist": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh"]),
-    "wide": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh"]),
-    "tiny": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh"]),
-    "qgist": ("decode_short_kernel", ["decode_short.cu", "common.cuh"]),
+    "gist": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh", "exact.cuh"]),
+    "wide": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh", "exact.cuh"]),
+    "tiny": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh", "exact.cuh"]),
+    "qgist": ("decode_short_kernel", ["decode_short.cu", "frag.cuh", "common.cuh"]),
     "paged": ("decode_long_kernel", ["decode_long.cu", "common.cuh"]),
-    "offline": ("prefill_long_kernel", ["prefill_long.cu", "tcgen05.cuh", "common.cuh"]),
+    "offline": ("prefill_long_kernel", ["prefill_long.cu", "tcgen05.cuh", "common.cuh", "exact.cuh"]),
 }
 
 DESCR = {
@@ -652,9 +652,10 @@ def run_sweep(args, dev, stream, status, ws, rank, peak, peak_src):
             nbytes = algorithmic_bytes_per_launch(wl)["total"]
             flops = 4.0 * hd * Hq * (l_new * k + l_new * (l_new + 1) / 2) * P  # useful: scores + PV
             gbs = nbytes / (t_attn * 1e-3) / 1e9
-            # the library's dispatch: the single-pass tensor-core kernel while the
-            # keys fit 128, else the staged path (pre-pass + long-sequence kernel)
-            kernel = "prefill_tc_kernel" if k + l_new <= 128 else "stage_kernel + prefill_long_kernel"
+            # the library's dispatch: the single-pass tensor-core kernel while a
+            # tile's keys fit its TMEM (288), else the staged path (pre-pass +
+            # long-sequence kernel), which is when the call wants a workspace
+            kernel = "stage_kernel + prefill_long_kernel" if nws else "prefill_tc_kernel"
             if rank == 0:
                 print(json.dumps({
                     "metric": "(item,query) pairs/s per layer-attention", "row": "sweep", "k": k, "l": l_new,

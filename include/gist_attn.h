@@ -134,10 +134,11 @@ int gist_attn_fwd(const void* q, const void* k_new, const void* v_new, const voi
 /*
  * gist_attn_workspace_bytes -- device bytes of the workspace gist_attn_fwd_ws
  * uses for these dimensions, or 0 when they run without one.  Host only.
- * Non-zero for d = 64, n_new >= 2, cached + new keys above 128 and groups of
- * at most 128 heads (cached blocks per pair <= 64), where the staged path
- * applies: 256 * P + 256 * n_new + 2 * (2 * P * (cached + n_new) * Hkv * 64)
- * bytes, each of the four parts rounded up to 256.  Invalid dims return 0.
+ * Non-zero for d = 64, n_new >= 2, cached + new keys above the 288 that the
+ * single-pass tensor-core kernel holds, and groups of at most 128 heads (cached
+ * blocks per pair <= 64), where the staged path applies: 256 * P + 256 * n_new +
+ * 2 * (2 * P * (cached + n_new) * Hkv * 64) bytes, each of the four parts
+ * rounded up to 256.  Invalid dims return 0.
  */
 size_t gist_attn_workspace_bytes(const gist_attn_dims* dims);
 

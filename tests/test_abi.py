@@ -199,14 +199,15 @@ def test_workspace_bytes(lib):
     def up(x):
         return (x + 255) // 256 * 256
 
-    for P, l, Hq, Hkv, C in [(12800, 256, 14, 2, 8), (3, 129, 7, 1, 64), (5, 200, 16, 2, 1)]:
+    for P, l, Hq, Hkv, C in [(12800, 300, 14, 2, 8), (3, 250, 7, 1, 64), (5, 300, 16, 2, 1)]:
         d = _dims(num_pairs=P, n_new=l, num_q_heads=Hq, num_kv_heads=Hkv, block_len=C)
         want = up(P * 32 * 8) + up(l * 32 * 8) + 2 * up(P * (C + l) * Hkv * 64 * 2)
         assert binding.workspace_bytes(d) == want, (P, l, C)
     assert binding.workspace_bytes(_dims(n_new=64)) == 0            # 72 keys: single-pass kernel
+    assert binding.workspace_bytes(_dims()) == 0                    # 264 keys: single pass, 512 TMEM columns
     assert binding.workspace_bytes(_dims(n_new=1)) == 0             # decode
     assert binding.workspace_bytes(_dims(head_dim=128)) == 0        # d = 128: streaming kernel
     assert binding.workspace_bytes(_dims(num_pairs=0)) == 0
     assert binding.workspace_bytes(_dims(num_kv_heads=3)) == 0      # invalid: 14 % 3
     assert binding.workspace_bytes(_dims(block_len=0, blocks_per_pair=0, flags=1)) == 0  # pre-rotated, no cache
-    assert binding.workspace_bytes(_dims(block_len=0, blocks_per_pair=0)) > 0  # raw inputs, no cache
+    assert binding.workspace_bytes(_dims(n_new=300, block_len=0, blocks_per_pair=0)) > 0  # raw inputs, no cache

@@ -149,7 +149,7 @@ def test_full_size_workloads_sampled(name, n_sample, layer):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("k,l", [(32, 64), (64, 16)])
+@pytest.mark.parametrize("k,l", [(32, 64), (64, 16), (8, 256), (32, 256)])
 def test_sweep_points_full_size_sampled(k, l):
     """Sweep points of the gist workload at full size (12,800 Zipf pairs): k = 32
     runs with two q stages so that two CTAs share an SM; k = 64, l = 16 is the

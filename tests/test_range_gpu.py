@@ -38,7 +38,8 @@ SHAPES = {
     "prefill_tc": (4, 12, 14, 2, 64, 8, 1, 6, False),
     "prefill_tc_d128": (3, 20, 32, 8, 128, 8, 1, 5, False),
     "prefill_stream": (3, 40, 14, 2, 64, 100, 2, 7, False),
-    "staged": (3, 150, 14, 2, 64, 16, 2, 7, True),
+    "staged": (3, 290, 14, 2, 64, 16, 2, 7, True),
+    "prefill_tc_wide_keys": (3, 200, 14, 2, 64, 16, 2, 7, False),
     "decode_short": (5, 1, 14, 2, 64, 8, 2, 9, False),
     "decode_5row_blocks": (4, 1, 14, 2, 64, 5, 3, 9, False),
     "decode_long": (3, 1, 8, 8, 128, 64, 2, 7, False),

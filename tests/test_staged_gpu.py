@@ -39,14 +39,14 @@ def run_ws(wl, layer=0, status=None):
 
 SHAPES = [
     # P, l, Hq, Hkv, block_len, blocks_per_pair, num_blocks, random_pos
-    (4, 256, 14, 2, 8, 1, 20, False),    # a sweep point: gist k = 8, l = 256
+    (4, 300, 14, 2, 8, 1, 20, False),    # gist k = 8, 308 keys
     (3, 256, 14, 2, 64, 1, 9, True),     # the widest gist of the sweep
-    (5, 200, 14, 2, 1, 1, 7, True),      # one cached position, ragged tiles
-    (3, 150, 16, 2, 16, 2, 11, True),    # two cached blocks through a table, G = 8
+    (5, 300, 14, 2, 1, 1, 7, True),      # one cached position, ragged tiles
+    (3, 290, 16, 2, 16, 2, 11, True),    # two cached blocks through a table, G = 8
     (2, 300, 4, 4, 32, 1, 5, False),     # MHA: 128 tokens per tile
-    (2, 140, 128, 1, 8, 1, 4, False),    # G = 128: one token per tile
+    (2, 290, 128, 1, 8, 1, 4, False),    # G = 128: one token per tile
     (3, 300, 14, 2, 0, 0, 0, True),      # no cache: the offline pass on pre-RoPE inputs
-    (64, 200, 14, 2, 16, 1, 40, True),   # 1,536 tiles: several per persistent CTA
+    (64, 290, 14, 2, 16, 1, 40, True),   # 2,176 tiles: several per persistent CTA
 ]
 
 
@@ -77,7 +77,7 @@ def test_without_workspace_the_call_is_gist_attn_fwd():
 
 
 def test_staged_bad_block_zeroes_that_pair_and_sets_status():
-    wl = workloads.make_custom(4, 180, 14, 2, 64, 8, 1, 6, device=DEV, seed=8)
+    wl = workloads.make_custom(4, 290, 14, 2, 64, 8, 1, 6, device=DEV, seed=8)
     wl.item_ids[2] = 6  # one past the pool
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     got = run_ws(wl, status=status)
@@ -92,7 +92,7 @@ def test_staged_value_past_f16_range_matches_oracle():
     """A query element past the f16 range (the staged path forms q.K in f16):
     the rows that meet it are recomputed in fp32 and every pair matches the
     oracle."""
-    wl = workloads.make_custom(2, 160, 14, 2, 64, 8, 1, 4, device=DEV, seed=9)
+    wl = workloads.make_custom(2, 290, 14, 2, 64, 8, 1, 4, device=DEV, seed=9)
     wl.q[1, 5, 3, 7] = 1.0e5
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     got = run_ws(wl, status=status)
@@ -102,22 +102,22 @@ def test_staged_value_past_f16_range_matches_oracle():
 
 
 def test_staged_is_deterministic():
-    wl = workloads.make_custom(3, 220, 14, 2, 64, 16, 1, 5, device=DEV, seed=10)
+    wl = workloads.make_custom(3, 290, 14, 2, 64, 16, 1, 5, device=DEV, seed=10)
     a, b = run_ws(wl), run_ws(wl)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
 
 
-def test_sweep_point_l256_full_size_sampled():
-    """The sweep point k = 8, l = 256 at its full size (12,800 Zipf pairs), as the
-    benchmark times it; the oracle checks a sample of pairs."""
-    wl = workloads.make(workloads.sweep_spec(8, 256), device=DEV, num_layers=2)
+def test_sweep_point_k64_l256_full_size_sampled():
+    """The widest sweep point, k = 64, l = 256 (320 keys), at its full size
+    (12,800 Zipf pairs), as the benchmark times it; the oracle checks a sample."""
+    wl = workloads.make(workloads.sweep_spec(64, 256), device=DEV, num_layers=2)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     got = run_ws(wl, layer=1, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     sel = np.sort(np.random.default_rng(7).choice(wl.dims["num_pairs"], size=40, replace=False))
-    compare(got[torch.from_numpy(sel).to(DEV)], oracle_ref(wl, layer=1, pairs=sel), "k=8 l=256")
+    compare(got[torch.from_numpy(sel).to(DEV)], oracle_ref(wl, layer=1, pairs=sel), "k=64 l=256")
     assert torch.isfinite(got.float()).all()
     del wl, got
     torch.cuda.empty_cache()
@@ -127,7 +127,7 @@ def test_staged_prerotated_inputs_with_a_cache():
     """Pre-rotated q and k_new (GIST_ATTN_FLAG_PREROTATED) behind a cache: the
     pre-pass only converts (every angle is 0) and the result is the oracle's
     prerotated attention."""
-    wl = workloads.make_custom(3, 210, 14, 2, 64, 16, 1, 5, device=DEV, seed=12, random_pos=True)
+    wl = workloads.make_custom(3, 290, 14, 2, 64, 16, 1, 5, device=DEV, seed=12, random_pos=True)
     dims = dict(wl.dims, flags=binding.FLAG_PREROTATED)
     n = binding.workspace_bytes(dims)
     assert n > 0

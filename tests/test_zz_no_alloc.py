@@ -19,8 +19,8 @@ from parity_utils import compare
 DEV = "cuda"
 
 # (P, l, Hq, Hkv, block_len, blocks_per_pair, num_blocks, random_pos): both take
-# the staged path (d = 64, more than 128 keys), the second through a block table
-CASES = [(4, 256, 14, 2, 8, 1, 20, False), (3, 150, 16, 2, 16, 2, 11, True)]
+# the staged path (d = 64, more than 288 keys), the second through a block table
+CASES = [(4, 300, 14, 2, 8, 1, 20, False), (3, 290, 16, 2, 16, 2, 11, True)]
 
 
 def _with_workspace(wl):
@@ -59,7 +59,7 @@ def test_too_much_scratch_is_rejected_on_the_host():
     if torch.cuda.is_available():
         pytest.skip("fake device addresses: host-only test")
     lib = binding.load_library()
-    dims = dict(num_pairs=1024, n_new=256, num_q_heads=14, num_kv_heads=2, head_dim=64,
+    dims = dict(num_pairs=1024, n_new=300, num_q_heads=14, num_kv_heads=2, head_dim=64,
                 block_len=8, blocks_per_pair=1, num_blocks=16, num_layers=1, layer=0,
                 rope_theta=1e4, softmax_scale=0.0)
     assert binding.workspace_bytes(dims) > binding.NOALLOC_SCRATCH_BYTES
