@@ -71,34 +71,45 @@ struct ShortParams {
   double theta[64];  // RoPE frequencies (angles reduced in double)
 };
 
-// One warp's shared memory: the swizzled tiles of two buffers, then the small
-// parts of both buffers, the (cos, sin) table of the query's position and the
-// buffers' mbarriers.  A buffer's tiles are the K tile and the V tile (MT x 16
-// rows of 128 bytes per 64-column panel, 128-byte swizzle, 1 KiB-aligned) and
-// the q tile (GN x 8 rows per panel, same swizzle; it also holds the output rows
-// before their store), and for an FP8 pool the E4M3 rows of K and V as they
-// arrive; its small parts are the new key and value rows.  Offsets of buffer
-// b's parts are the buffer-0 offsets plus b x buf (tiles) or b x small (new
-// rows).  Keeping the small parts out of the 1 KiB-aligned tiles lets five CTAs
-// of four warps share an SM on the query-gisted shape.
+// One warp's shared memory: the swizzled K and V tiles (MT x 16 rows of 128
+// bytes per 64-column panel, 128-byte swizzle, 1 KiB-aligned) and the parts of
+// two buffers, then the small parts of both buffers, the (cos, sin) table of
+// the query's position and the buffers' mbarriers.  With a bf16 pool each
+// buffer has its own K and V tiles, which the tensor copies fill; with an FP8
+// pool the two buffers share one pair, into which the unit being computed
+// widens the E4M3 rows its buffer staged (the copies of the next unit land in
+// the other buffer's staging rows meanwhile).  A buffer's own part is the q
+// tile (GN x 8 rows per panel, same swizzle) and, FP8, the staged E4M3 rows of
+// K and V; its small parts are the new key and value rows.  Keeping the small
+// parts out of the 1 KiB-aligned tiles, and the FP8 pool's widened tiles
+// single, lets five CTAs of four warps share an SM on the query-gisted shape
+// with either pool.
 template <int D, int GN, int MT, bool FP8>
 struct Region {
   static constexpr int NP = D / 64;
   static constexpr uint32_t kv_panel = MT * 16 * 128;
   static constexpr uint32_t q_panel = GN * 8 * 128;
-  static constexpr uint32_t k_off = 0;
-  static constexpr uint32_t v_off = k_off + NP * kv_panel;
-  static constexpr uint32_t q_off = v_off + NP * kv_panel;
-  static constexpr uint32_t k8_off = q_off + NP * q_panel;
-  static constexpr uint32_t v8_off = k8_off + (FP8 ? MT * 16 * D : 0);
-  static constexpr uint32_t buf = (v8_off + (FP8 ? MT * 16 * D : 0) + 1023) / 1024 * 1024;
+  static constexpr uint32_t kv_tiles = 2 * NP * kv_panel;          // a K and a V tile
+  static constexpr uint32_t own = (FP8 ? 0 : kv_tiles) + NP * q_panel + (FP8 ? 2 * MT * 16 * D : 0);
+  static constexpr uint32_t buf = (own + 1023) / 1024 * 1024;      // one buffer's own part
+  static constexpr uint32_t buf0 = FP8 ? kv_tiles : 0;              // where buffer 0's part starts
+  static constexpr uint32_t kv_step = FP8 ? 0 : buf;                // K/V tiles of buffer 1 - buffer 0
+  static constexpr uint32_t q_in = FP8 ? 0 : kv_tiles;              // q tile within a buffer's part
   static constexpr uint32_t small = 2 * D * 2;  // the new key row, then the new value row
-  static constexpr uint32_t kn_off = 2 * buf;   // buffer b: + b x small
+  static constexpr uint32_t kn_off = buf0 + 2 * buf;  // buffer b: + b x small
   static constexpr uint32_t vn_off = kn_off + D * 2;
   static constexpr uint32_t tab_off = kn_off + 2 * small;  // float2 [D / 2]
   static constexpr uint32_t bar_off = tab_off + D * 4;
   static constexpr uint32_t bytes = (bar_off + 16 + 1023) / 1024 * 1024;
+  // offsets of buffer b's K tile, V tile, q tile and staged E4M3 K and V rows
+  static constexpr uint32_t k_at(int b) { return b * kv_step; }
+  static constexpr uint32_t v_at(int b) { return b * kv_step + NP * kv_panel; }
+  static constexpr uint32_t q_at(int b) { return buf0 + b * buf + q_in; }
+  static constexpr uint32_t k8_at(int b) { return q_at(b) + NP * q_panel; }
+  static constexpr uint32_t v8_at(int b) { return k8_at(b) + MT * 16 * D; }
 };
+static_assert(Region<64, 1, 1, false>::bytes == 11 * 1024 && Region<64, 1, 1, true>::bytes == 11 * 1024,
+              "the query-gisted shape fits five CTAs of four warps per SM with either pool");
 
 // D: head dim.  GN: 8-head tiles of the N dimension.  MT: 16-key tiles.
 template <int D, int GN, int MT, bool FP8>
@@ -106,8 +117,7 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
                                                                 const __grid_constant__ CUtensorMap tm_pool,
                                                                 const __grid_constant__ CUtensorMap tm_q,
                                                                 const __grid_constant__ CUtensorMap tm_kn,
-                                                                const __grid_constant__ CUtensorMap tm_vn,
-                                                                const __grid_constant__ CUtensorMap tm_o) {
+                                                                const __grid_constant__ CUtensorMap tm_vn) {
   using R = Region<D, GN, MT, FP8>;
   constexpr int NP = D / 64;
   constexpr int CPR = D / 8;  // 16-byte chunks per bf16 row
@@ -143,16 +153,15 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   // tiles, head rows G.. of the q tile
   const int krows = C;
   for (int b = 0; b < 2; ++b) {
-    const uint32_t bb = base + b * R::buf;
     const int kpad = MT * 16 - krows;
     for (int idx = lane; idx < NP * kpad * 8; idx += 32) {
       const int c = idx & 7, rest = idx >> 3, row = krows + rest % kpad, pn = rest / kpad;
-      sts16(bb + R::k_off + pn * R::kv_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
-      sts16(bb + R::v_off + pn * R::kv_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
+      sts16(base + R::k_at(b) + pn * R::kv_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
+      sts16(base + R::v_at(b) + pn * R::kv_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
     }
     for (int idx = lane; idx < NP * GN * 8 * 8; idx += 32) {
       const int c = idx & 7, row = (idx >> 3) % (GN * 8), pn = (idx >> 3) / (GN * 8);
-      if (row >= G) sts16(bb + R::q_off + pn * R::q_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
+      if (row >= G) sts16(base + R::q_at(b) + pn * R::q_panel + swz128(row, c), make_uint4(0, 0, 0, 0));
     }
   }
   fence_proxy_async_smem();
@@ -211,10 +220,8 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   // which case its cached rows are not copied.
   auto issue = [&](int p, int g0, int b, int32_t id) -> bool {
     const bool bad = __any_sync(0xffffffffu, lane < bpp && !pool_block_ok(prm.pv, id));
-    const uint32_t bb = base + b * R::buf;
     constexpr uint32_t kv_row_bytes = FP8 ? D : D * 2;
     if (lane == 0) {
-      bulk_wait_read_all();  // the output store of two units ago has read the q tile
       mbar_arrive_expect_tx(&kvbar[b], (bad ? 0u : (uint32_t)(bpp * 2 * bl) * kv_row_bytes) +
                                            (uint32_t)G * D * 2 + 2u * D * 2);
     }
@@ -225,13 +232,15 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
             (int)((((int64_t)blk * prm.pv.num_layers + prm.pv.layer) * 2 * prm.Hkv + g0) * bl);
         const int row_v = row_k + prm.Hkv * bl;
         if constexpr (FP8) {
-          tma_load_2d(bb + R::k8_off + bi * bl * D, &tm_pool, &kvbar[b], 0, row_k);
-          tma_load_2d(bb + R::v8_off + bi * bl * D, &tm_pool, &kvbar[b], 0, row_v);
+          tma_load_2d(base + R::k8_at(b) + bi * bl * D, &tm_pool, &kvbar[b], 0, row_k);
+          tma_load_2d(base + R::v8_at(b) + bi * bl * D, &tm_pool, &kvbar[b], 0, row_v);
         } else {
 #pragma unroll
           for (int x = 0; x < NP; ++x) {
-            tma_load_2d(bb + R::k_off + x * R::kv_panel + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x, row_k);
-            tma_load_2d(bb + R::v_off + x * R::kv_panel + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x, row_v);
+            tma_load_2d(base + R::k_at(b) + x * R::kv_panel + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x,
+                        row_k);
+            tma_load_2d(base + R::v_at(b) + x * R::kv_panel + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x,
+                        row_v);
           }
         }
       }
@@ -239,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     if (lane == 0) {
 #pragma unroll
       for (int x = 0; x < NP; ++x)
-        tma_load_2d(bb + R::q_off + x * R::q_panel, &tm_q, &kvbar[b], 64 * x, p * prm.Hq + g0 * G);
+        tma_load_2d(base + R::q_at(b) + x * R::q_panel, &tm_q, &kvbar[b], 64 * x, p * prm.Hq + g0 * G);
       tma_load_2d(base + R::kn_off + b * R::small, &tm_kn, &kvbar[b], 0, p * prm.Hkv + g0);
       tma_load_2d(base + R::vn_off + b * R::small, &tm_vn, &kvbar[b], 0, p * prm.Hkv + g0);
     }
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
 
   for (int n = 0;; ++n) {
     const int b = n & 1;
-    const uint32_t bb = base + b * R::buf;
+    const uint32_t kt = base + R::k_at(b), vt = base + R::v_at(b), qt = base + R::q_at(b);
     // ---- unit un's copies into the other buffer (free since the last unit),
     // and the block ids of the unit after it
     const bool more = un < prm.units;
@@ -282,7 +291,6 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       // give up: report, wait (bounded) for the copy still in flight, stop
       if (lane == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
       if (more) mbar_wait(&kvbar[b ^ 1], (uint32_t)((n + 1) >> 1) & 1u);
-      if (lane == 0) bulk_wait_all();
       return;
     }
 
@@ -302,8 +310,8 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         for (int row = lane / CPR; row < krows; row += PER) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
-            const uint2 raw = lds64(bb + (kv ? R::v8_off : R::k8_off) + row * D + c * 8);
-            sts16(bb + (kv ? R::v_off : R::k_off) + (c >> 3) * R::kv_panel + swz128(row, c & 7),
+            const uint2 raw = lds64(base + (kv ? R::v8_at(b) : R::k8_at(b)) + row * D + c * 8);
+            sts16((kv ? vt : kt) + (c >> 3) * R::kv_panel + swz128(row, c & 7),
                   make_uint4(e4m3x2_to_f16x2(raw.x & 0xffffu), e4m3x2_to_f16x2(raw.x >> 16),
                              e4m3x2_to_f16x2(raw.y & 0xffffu), e4m3x2_to_f16x2(raw.y >> 16)));
           }
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
 #pragma unroll
       for (int hn = 0; hn < GN; ++hn) {
         uint64_t rx[KS], ry[KS];
-        q_fragments<D, FP8>(bb + R::q_off, R::q_panel, hn, tab, qh[hn], ql[hn], rx, ry, qf[hn]);
+        q_fragments<D, FP8>(qt, R::q_panel, hn, tab, qh[hn], ql[hn], rx, ry, qf[hn]);
         uint64_t dot = f2_make(0.f, 0.f);
 #pragma unroll
         for (int ks = 0; ks < HK; ++ks) {
@@ -345,24 +353,30 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       }
 
       // ---- S^T = K q^T: rows = keys 16 mt + g8 (+ 8), columns = head slots 8 hn + 2 t4 (+ 1)
-      float s[MT][GN][4];
+      float s[MT][GN][4], s2[MT][GN][4];  // hi and lo passes in separate chains
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-        for (int hn = 0; hn < GN; ++hn) s[mt][hn][0] = s[mt][hn][1] = s[mt][hn][2] = s[mt][hn][3] = 0.f;
+        for (int hn = 0; hn < GN; ++hn)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[mt][hn][e] = s2[mt][hn][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t a[4];
           const int c8 = 2 * ks + (lane >> 4);
-          ldsm_x4(bb + R::k_off + (c8 >> 3) * R::kv_panel +
+          ldsm_x4(kt + (c8 >> 3) * R::kv_panel +
                       swz128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, c8 & 7),
                   a);
 #pragma unroll
           for (int hn = 0; hn < GN; ++hn) {
             mma16816<FP8>(s[mt][hn], a[0], a[1], a[2], a[3], qh[hn][ks][0], qh[hn][ks][1]);
-            mma16816<FP8>(s[mt][hn], a[0], a[1], a[2], a[3], ql[hn][ks][0], ql[hn][ks][1]);
+            mma16816<FP8>(s2[mt][hn], a[0], a[1], a[2], a[3], ql[hn][ks][0], ql[hn][ks][1]);
           }
         }
+#pragma unroll
+        for (int hn = 0; hn < GN; ++hn)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[mt][hn][e] += s2[mt][hn][e];
       }
 
       // ---- softmax of every head over its cached keys and the new key
@@ -441,7 +455,7 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         for (int dq = 0; dq < D / 16; ++dq) {
           uint32_t bv[4];
           const int c8 = 2 * dq + (lane >> 4);
-          ldsm_x4_trans(bb + R::v_off + (c8 >> 3) * R::kv_panel +
+          ldsm_x4_trans(vt + (c8 >> 3) * R::kv_panel +
                             swz128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, c8 & 7),
                         bv);
           mma16816<FP8>(o[2 * dq], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], bv[0], bv[1]);
@@ -449,9 +463,10 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         }
       }
 
-      // ---- the new value, normalisation, into the q tile's rows: this lane's
-      // rows are head slots 8 hn + g8, whose softmax terms sit in lane g8 / 2
-      // (slot g8 % 2); then one tensor store per panel
+      // ---- the new value and the normalisation: this lane's rows are head
+      // slots 8 hn + g8, whose softmax terms sit in lane g8 / 2 (slot g8 % 2).
+      // The rows go straight to global memory (the four lanes of a row write 16
+      // contiguous bytes per 8-column step), so no store ever holds a buffer.
 #pragma unroll
       for (int hn = 0; hn < GN; ++hn) {
         const int src = g8 >> 1;
@@ -463,21 +478,14 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         const uint64_t oc = f2_make(vmax * inv, vmax * inv), on = f2_make(pnew * inv, pnew * inv);
         const uint32_t vn = base + R::vn_off + b * R::small;
         const int slot = hn * 8 + g8;
+        bf16* orow = prm.out + ((size_t)p * prm.Hq + (size_t)g0 * G + slot) * D;
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn) {
           const int col = dn * 8 + 2 * t4;
           const uint64_t r2 = f2_fma(bf16x2_to_f2(lds32(vn + col * 2)), on,
                                      f2_mul(f2_make(o[dn][2 * hn], o[dn][2 * hn + 1]), oc));
-          sts32(bb + R::q_off + (dn >> 3) * R::q_panel + swz128(slot, dn & 7) + 4 * t4, f2_to_bf16x2(r2));
+          if (slot < G) *reinterpret_cast<uint32_t*>(orow + col) = f2_to_bf16x2(r2);
         }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-#pragma unroll
-        for (int x = 0; x < NP; ++x)
-          tma_store_2d(&tm_o, bb + R::q_off + x * R::q_panel, 64 * x, p * prm.Hq + g0 * G);
-        bulk_commit();
       }
     }
     // buffer b is free for the unit after next; its shared-memory reads and
@@ -495,7 +503,6 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     ids_cur = ids_next;
     ids_next = ids_after;
   }
-  if (lane == 0) bulk_wait_all();
 }
 
 template <int D, int GN, int MT, bool FP8>
@@ -519,7 +526,7 @@ int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
   prm.region = R::bytes;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.theta[j] = pb.inv_freq_d[j];
-  alignas(64) CUtensorMap tm_pool{}, tm_q{}, tm_kn{}, tm_vn{}, tm_o{};
+  alignas(64) CUtensorMap tm_pool{}, tm_q{}, tm_kn{}, tm_vn{};
   const int64_t pool_rows = (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len;
   const int box_rows = pb.block_len;  // a block's rows of one KV head
   int rc = FP8 ? encode_2d(&tm_pool, pb.kv_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pool_rows, D, D,
@@ -528,9 +535,6 @@ int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
                            64, box_rows, true);
   if (rc == GIST_ATTN_OK)
     rc = encode_2d(&tm_q, pb.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hq, D, 64,
-                   pb.G, true);
-  if (rc == GIST_ATTN_OK)
-    rc = encode_2d(&tm_o, pb.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hq, D, 64,
                    pb.G, true);
   if (rc == GIST_ATTN_OK)
     rc = encode_2d(&tm_kn, pb.k_new, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hkv, D,
@@ -552,7 +556,7 @@ int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
   // persistent: one wave of resident CTAs walks all units
   const int64_t need = (prm.units + kWarps - 1) / kWarps;
   const int64_t grid = need < (int64_t)sms * per_sm ? need : (int64_t)sms * per_sm;
-  kern<<<(unsigned)grid, kThreads, bytes, stream>>>(prm, tm_pool, tm_q, tm_kn, tm_vn, tm_o);
+  kern<<<(unsigned)grid, kThreads, bytes, stream>>>(prm, tm_pool, tm_q, tm_kn, tm_vn);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
