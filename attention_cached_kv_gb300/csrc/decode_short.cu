@@ -215,9 +215,12 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     }
     return r;
   };
-  // Tensor copies of unit (p, KV head g0) into buffer b, issued by lane 0;
-  // returns (warp-uniform) whether one of its block ids is out of range, in
-  // which case its cached rows are not copied.
+  // Tensor copies of unit (p, KV head g0) into buffer b, issued by the lanes
+  // side by side: lane t < bpp copies block t's K and V rows, lanes 29, 30 and
+  // 31 the q rows, the new key and the new value.  Lane 0 first sets the
+  // barrier's byte count with its one arrival, so copies landing before that
+  // cannot complete the phase.  Returns (warp-uniform) whether one of the
+  // unit's block ids is out of range, in which case no cached rows are copied.
   auto issue = [&](int p, int g0, int b, int32_t id) -> bool {
     const bool bad = __any_sync(0xffffffffu, lane < bpp && !pool_block_ok(prm.pv, id));
     constexpr uint32_t kv_row_bytes = FP8 ? D : D * 2;
@@ -225,32 +228,32 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       mbar_arrive_expect_tx(&kvbar[b], (bad ? 0u : (uint32_t)(bpp * 2 * bl) * kv_row_bytes) +
                                            (uint32_t)G * D * 2 + 2u * D * 2);
     }
-    for (int bi = 0; bi < bpp; ++bi) {  // uniform loop: the shuffle is safe
-      const int32_t blk = __shfl_sync(0xffffffffu, id, bi);
-      if (lane == 0 && !bad) {
-        const int row_k =
-            (int)((((int64_t)blk * prm.pv.num_layers + prm.pv.layer) * 2 * prm.Hkv + g0) * bl);
-        const int row_v = row_k + prm.Hkv * bl;
-        if constexpr (FP8) {
-          tma_load_2d(base + R::k8_at(b) + bi * bl * D, &tm_pool, &kvbar[b], 0, row_k);
-          tma_load_2d(base + R::v8_at(b) + bi * bl * D, &tm_pool, &kvbar[b], 0, row_v);
-        } else {
+    if (lane < bpp && !bad) {
+      const int row_k = (int)((((int64_t)id * prm.pv.num_layers + prm.pv.layer) * 2 * prm.Hkv + g0) * bl);
+      const int row_v = row_k + prm.Hkv * bl;
+      if constexpr (FP8) {
+        tma_load_2d(base + R::k8_at(b) + lane * bl * D, &tm_pool, &kvbar[b], 0, row_k);
+        tma_load_2d(base + R::v8_at(b) + lane * bl * D, &tm_pool, &kvbar[b], 0, row_v);
+      } else {
 #pragma unroll
-          for (int x = 0; x < NP; ++x) {
-            tma_load_2d(base + R::k_at(b) + x * R::kv_panel + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x,
-                        row_k);
-            tma_load_2d(base + R::v_at(b) + x * R::kv_panel + bi * bl * 128, &tm_pool, &kvbar[b], 64 * x,
-                        row_v);
-          }
+        for (int x = 0; x < NP; ++x) {
+          tma_load_2d(base + R::k_at(b) + x * R::kv_panel + lane * bl * 128, &tm_pool, &kvbar[b], 64 * x,
+                      row_k);
+          tma_load_2d(base + R::v_at(b) + x * R::kv_panel + lane * bl * 128, &tm_pool, &kvbar[b], 64 * x,
+                      row_v);
         }
       }
     }
-    if (lane == 0) {
+    if (lane >= 29) {
+      if (lane == 29) {
 #pragma unroll
-      for (int x = 0; x < NP; ++x)
-        tma_load_2d(base + R::q_at(b) + x * R::q_panel, &tm_q, &kvbar[b], 64 * x, p * prm.Hq + g0 * G);
-      tma_load_2d(base + R::kn_off + b * R::small, &tm_kn, &kvbar[b], 0, p * prm.Hkv + g0);
-      tma_load_2d(base + R::vn_off + b * R::small, &tm_vn, &kvbar[b], 0, p * prm.Hkv + g0);
+        for (int x = 0; x < NP; ++x)
+          tma_load_2d(base + R::q_at(b) + x * R::q_panel, &tm_q, &kvbar[b], 64 * x, p * prm.Hq + g0 * G);
+      } else {
+        const bool k = lane == 30;
+        tma_load_2d(base + (k ? R::kn_off : R::vn_off) + b * R::small, k ? &tm_kn : &tm_vn, &kvbar[b], 0,
+                    p * prm.Hkv + g0);
+      }
     }
     return bad;
   };
