@@ -204,7 +204,8 @@ __global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_const
 #pragma unroll
   for (int hn = 0; hn < GN; ++hn) {
     uint64_t rx[KS], ry[KS];
-    q_fragments<D, FP8>(base + L::q_off, L::q_panel, hn, tab, qh[hn], ql[hn], rx, ry, qf[hn]);
+    uint32_t qr[KS][2];
+    q_fragments<D, FP8>(base + L::q_off, L::q_panel, hn, tab, qh[hn], ql[hn], qr, rx, ry, qf[hn]);
     snew[hn] = 0.f;
     if (warp == 0) {
       // q . k_new of the unrotated rows (the same rotation of both cancels)

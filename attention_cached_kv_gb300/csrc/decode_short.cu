@@ -122,7 +122,6 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   constexpr int NP = D / 64;
   constexpr int CPR = D / 8;  // 16-byte chunks per bf16 row
   constexpr int KS = D / 16;  // k-steps over d
-  constexpr int HK = KS / 2;  // k-steps holding the first half of d
   constexpr float kNegInf = -INFINITY;
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -327,32 +326,38 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       }
 
       // ---- q: B fragments of head slot 8 hn + g8 (rotated, scaled, split into
-      // hi + lo); the new key's logit from the unrotated values (the same
-      // rotation of q and of the new key cancels in their dot product)
+      // hi + lo), and the new key's logits from the unrotated values (the same
+      // rotation of q and of the new key cancels in their dot product), on the
+      // tensor core: A = the new key in all 16 rows, B = the raw bf16 query, so
+      // every row of the result holds the same logits and each lane finds those
+      // of its own columns, head slots 8 hn + 2 t4 (+ 1), in sn[hn][0 .. 1].
+      // bf16 x bf16 products are exact; the sum is fp32.
       uint32_t qh[GN][KS][2], ql[GN][KS][2];
-      float qf[GN];    // FP8: 2^e, the factor the head's f16 query was divided by
-      float snew[GN];  // logit of the new key, head slot 8 hn + g8 (log2 units)
-      const uint32_t kn = base + R::kn_off + b * R::small;  // the new key
+      float qf[GN];        // FP8: 2^e, the factor the head's f16 query was divided by
+      float sn[GN][4];     // logits of the new key (log2 units once scaled)
+      uint32_t ka[KS][2];  // A registers a0 (= a1) and a2 (= a3) of k-step ks
+      {
+        const uint32_t kn = base + R::kn_off + b * R::small;  // the new key
+        const int mat = lane >> 3;  // ldmatrix: matrix mat's eight rows all read one chunk
+#pragma unroll
+        for (int ks = 0; ks < KS; ks += 2) {
+          uint32_t r4[4];
+          ldsm_x4(kn + (16 * (ks + (mat >> 1)) + 8 * (mat & 1)) * 2, r4);
+          ka[ks][0] = r4[0];
+          ka[ks][1] = r4[1];
+          ka[ks + 1][0] = r4[2];
+          ka[ks + 1][1] = r4[3];
+        }
+      }
 #pragma unroll
       for (int hn = 0; hn < GN; ++hn) {
         uint64_t rx[KS], ry[KS];
-        q_fragments<D, FP8>(qt, R::q_panel, hn, tab, qh[hn], ql[hn], rx, ry, qf[hn]);
-        uint64_t dot = f2_make(0.f, 0.f);
+        uint32_t qr[KS][2];
+        q_fragments<D, FP8>(qt, R::q_panel, hn, tab, qh[hn], ql[hn], qr, rx, ry, qf[hn]);
+        sn[hn][0] = sn[hn][1] = sn[hn][2] = sn[hn][3] = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < HK; ++ks) {
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int d0 = 16 * ks + 8 * r + 2 * t4;
-            dot = f2_fma(rx[2 * ks + r], bf16x2_to_f2(lds32(kn + d0 * 2)), dot);
-            dot = f2_fma(ry[2 * ks + r], bf16x2_to_f2(lds32(kn + (d0 + D / 2) * 2)), dot);
-          }
-        }
-        float a, bq;
-        f2_split(dot, a, bq);
-        float sd = a + bq;
-        sd += __shfl_xor_sync(0xffffffffu, sd, 1);
-        sd += __shfl_xor_sync(0xffffffffu, sd, 2);
-        snew[hn] = sd * prm.scale_log2;
+        for (int ks = 0; ks < KS; ++ks)
+          mma16816<false>(sn[hn], ka[ks][0], ka[ks][0], ka[ks][1], ka[ks][1], qr[ks][0], qr[ks][1]);
       }
 
       // ---- S^T = K q^T: rows = keys 16 mt + g8 (+ 8), columns = head slots 8 hn + 2 t4 (+ 1)
@@ -414,8 +419,8 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
           m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, sft));
           m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, sft));
         }
-        const float sn0 = __shfl_sync(0xffffffffu, snew[hn], 8 * t4);
-        const float sn1 = __shfl_sync(0xffffffffu, snew[hn], 8 * t4 + 4);
+        const float sn0 = sn[hn][0] * prm.scale_log2;
+        const float sn1 = sn[hn][1] * prm.scale_log2;
         m0 = fmaxf(m0, sn0);
         m1 = fmaxf(m1, sn1);
         float l0 = 0.f, l1 = 0.f;

@@ -94,12 +94,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src,
 // register [ks][r].  Each element pair (d, d + D/2) is rotated in fp32 by the
 // angles of `tab` ((c_j, s_j, c_j+1, s_j+1) x scale at index j/2, even j),
 // then split into hi + lo (bf16, or f16 after dividing by the power of two
-// *qf so the tile's heads fit f16).  The raw pairs (x, y) = (d, d + D/2) are
-// returned for the new key's dot product.
+// *qf so the tile's heads fit f16).  The unrotated query is returned too, for
+// the new key's logit: as the raw bf16 B fragments qr, and as the fp32 pairs
+// (x, y) = (d, d + D/2).
 template <int D, bool F16>
 __device__ __forceinline__ void q_fragments(uint32_t qtile, uint32_t q_panel, int hn, const float4* tab,
                                             uint32_t (&qh)[D / 16][2], uint32_t (&ql)[D / 16][2],
-                                            uint64_t (&rx)[D / 16], uint64_t (&ry)[D / 16], float& qf) {
+                                            uint32_t (&qr)[D / 16][2], uint64_t (&rx)[D / 16],
+                                            uint64_t (&ry)[D / 16], float& qf) {
   constexpr int KS = D / 16, HK = KS / 2;
   const int lane = threadIdx.x & 31, t4 = lane & 3;
   uint32_t qb[KS][2];
@@ -113,6 +115,11 @@ __device__ __forceinline__ void q_fragments(uint32_t qtile, uint32_t q_panel, in
     qb[ks][1] = r4[1];
     qb[ks + 1][0] = r4[2];
     qb[ks + 1][1] = r4[3];
+  }
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    qr[ks][0] = qb[ks][0];
+    qr[ks][1] = qb[ks][1];
   }
   uint64_t qx[KS], qy[KS];
 #pragma unroll
