@@ -12,26 +12,30 @@
 // 8-wide N (one tile of heads for G <= 8, two for G <= 16), so the 7 heads of a
 // 14/2 model leave one column idle instead of nine rows.  The softmax runs down
 // the key rows of the accumulator (shuffles across the 8 lanes of a column);
-// movmatrix.trans turns P^T into the A layout of O = P V.  The new key and value
-// (the 17th key of the query-gisted workload) are taken in fp32 on the CUDA
-// cores: each lane holds 16 elements of one head's rotated query and the same
-// elements of the rotated new key, and reduces over its head's four lanes.  The
-// query's B fragments come from its rows in shared memory by ldmatrix, are
-// rotated in fp32, pre-scaled to log2 units and split into bf16 hi + lo (two MMA
-// passes), so the rounding of rotated q stays out of the logits; keys, values
-// and P V stay bf16 with fp32 accumulation, so every bf16 input is in range.
+// movmatrix.trans turns P^T into the A layout of O = P V.  The new key (the
+// 17th key of the query-gisted workload) meets the unrotated query: the same
+// rotation of both cancels in their dot product, so its logits come from one
+// more tensor-core pass over the raw bf16 fragments (exact products, fp32
+// sum), and the new value joins in fp32 in the epilogue.  The query's B
+// fragments come from its rows in shared memory by ldmatrix, are rotated in
+// fp32, pre-scaled to log2 units and split into bf16 hi + lo (two MMA passes),
+// so the rounding of rotated q stays out of the logits; keys, values and P V
+// stay bf16 with fp32 accumulation, so every bf16 input is in range.  The
+// output rows go from the accumulators straight to global memory.
 //
 // Persistent warps, two units in flight per warp: while a warp computes unit n
-// from one of its two shared-memory buffers, one lane's tensor copies of unit
-// n + 1 (its cached K and V blocks as whole {64, block_len} boxes of the pool,
-// its q rows, its new key and value) fill the other buffer and complete on that
+// from one of its two shared-memory buffers, the tensor copies of unit n + 1
+// (its cached K and V blocks as whole {64, block_len} boxes of the pool, one
+// lane per block, and its q rows, new key and new value from three more lanes,
+// all issued side by side) fill the other buffer and complete on that
 // buffer's mbarrier; the block ids of unit n + 2 are on their way.  A wait that
 // runs out (1 s) reports GIST_ATTN_STATUS_TIMEOUT, waits once more for the copy
 // still in flight and ends the warp.
 //
 // FP8 pool ([Suffix page, §2 and the end of §5]: 1-byte KV elements, one fp32
-// scale per (block, layer, K|V, KV head)): the E4M3 boxes land in a staging area
-// and are widened to f16 in the swizzled tiles (cvt e4m3x2 -> f16x2, exact); the
+// scale per (block, layer, K|V, KV head)): the E4M3 boxes land in the buffer's
+// staging rows and are widened to f16 in one pair of swizzled tiles that both
+// buffers share (cvt e4m3x2 -> f16x2, exact); the
 // query is scaled into the f16 range by a power of two per head and split into
 // f16 hi + lo; the K scale multiplies the fp32 logits; each block's V scale
 // over the unit's largest multiplies the fp32 weights before they are rounded
