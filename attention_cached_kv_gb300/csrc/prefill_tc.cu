@@ -57,11 +57,14 @@ constexpr int kCompute = 256;            // 8 compute warps
 // Two CTAs share an SM for d = 64 with at most 96 keys (three 16-column chunks
 // per thread); wider tiles and d = 128 run one CTA per SM.
 __host__ __device__ constexpr bool two_per_sm(int D, int NCH) { return D == 64 && NCH <= 3; }
-// K/V warps: one where two CTAs share an SM; four where one CTA per SM leaves
+// K/V warps: where two CTAs share an SM, one when a unit spans several tiles
+// and three when it is one tile (ℓ ≤ ⌊128/G⌋: the unit's copies and key
+// conversion then recur every tile); four where one CTA per SM leaves
 // registers for them (d = 128 units carry twice the bytes, wide key sets more rows)
 __host__ __device__ constexpr int kv_warps(int D, int NCH) { return two_per_sm(D, NCH) ? 1 : 4; }
+constexpr int kKvWarpsOneTile = 3;
 // + the MMA warp, the TMA warp and the K/V warps
-__host__ __device__ constexpr int threads_of(int D, int NCH) { return kCompute + 64 + 32 * kv_warps(D, NCH); }
+__host__ __device__ constexpr int threads_of(int KVW) { return kCompute + 64 + 32 * KVW; }
 constexpr uint32_t kBarKV = 1;  // named barrier of the K/V warps
 constexpr int kMaxStages = 3;  // q/O stages: 3, or 2 where that lets two CTAs share an SM
 constexpr int kMaxKeys = 288;  // S, P and O of a 128-row tile within 512 TMEM columns
@@ -252,18 +255,19 @@ struct Bars {
 };
 
 // NCH: S chunks of 16 columns per thread (the tile's keys / 32, rounded up).
-// Registers: each of the 4 SM sub-partitions holds 16 K; two CTAs of 9 warps
-// put 5 warps on one of them (96 registers a thread), one CTA puts 3 (168).
-template <int D, int NCH, int NS>
-__global__ void __launch_bounds__(threads_of(D, NCH), two_per_sm(D, NCH) ? 2 : 1)
+// KVW: K/V warps.  Registers: each of the 4 SM sub-partitions holds 16 K; two
+// CTAs of 11 warps (one K/V warp) put 6 warps on one of them (85 registers a
+// thread), of 13 warps (three) 7 (73); one CTA of 14 warps puts 4 (128).
+template <int D, int NCH, int NS, int KVW>
+__global__ void __launch_bounds__(threads_of(KVW), two_per_sm(D, NCH) ? 2 : 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_o,
                       const __grid_constant__ TcParams prm) {
   constexpr int NP = D / 64;   // 64-column panels
   constexpr int CPR = D / 8;   // 16-byte chunks per row
-  constexpr int kThreads = threads_of(D, NCH);
+  constexpr int kThreads = threads_of(KVW);
   constexpr bool TAB2 = NCH > 4;  // two-level angle tables (tiles of more than 128 keys)
-  constexpr int KVT = 32 * kv_warps(D, NCH);  // K/V threads
+  constexpr int KVT = 32 * KVW;  // K/V threads
   constexpr int HALF = D / 2;
   constexpr float kNegInf = -INFINITY;
   constexpr uint32_t kPanel = 128 * 128;  // one 128-row Q panel
@@ -834,7 +838,7 @@ int encode_map(CUtensorMap* m, const void* base, const Problem& pb, int Tm) {
   return r == CUDA_SUCCESS ? GIST_ATTN_OK : GIST_ATTN_ERR_UNSUPPORTED;
 }
 
-template <int D, int NCH, int NS>
+template <int D, int NCH, int NS, int KVW = kv_warps(D, NCH)>
 int launch_d(const Problem& pb, cudaStream_t stream) {
   const Layout L = plan(pb);
   if (L.stages != NS) return GIST_ATTN_ERR_UNSUPPORTED;  // shared memory is sized for L.stages
@@ -878,7 +882,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   if (rc != GIST_ATTN_OK) return rc;
   rc = encode_map(&tm_o, pb.out, pb, L.Tm);
   if (rc != GIST_ATTN_OK) return rc;
-  if (cudaFuncSetAttribute(prefill_tc_kernel<D, NCH, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(prefill_tc_kernel<D, NCH, NS, KVW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)L.bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   int dev = 0, sms = 0;
@@ -890,7 +894,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   const int per_sm = (two_per_sm(D, NCH) && L.tmem_cols == 256 && L.bytes <= kTwoPerSmBytes) ? 2 : 1;
   const int64_t units = (int64_t)pb.P * pb.Hkv;
   const int grid = (int)(units < (int64_t)sms * per_sm ? units : (int64_t)sms * per_sm);
-  prefill_tc_kernel<D, NCH, NS><<<grid, threads_of(D, NCH), L.bytes, stream>>>(tm_q, tm_o, prm);
+  prefill_tc_kernel<D, NCH, NS, KVW><<<grid, threads_of(KVW), L.bytes, stream>>>(tm_q, tm_o, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
@@ -911,8 +915,13 @@ int launch_prefill_tc(const Problem& pb, cudaStream_t stream) {
   const Layout L = plan(pb);
   const int chunks = (L.kv_rows / 16 + 1) / 2;  // per thread: chunks h, h+2, ...
   if (pb.d == 64) {
-    if (chunks <= 2) return launch_d<64, 2, 3>(pb, stream);
-    if (chunks <= 3) return L.stages == 2 ? launch_d<64, 3, 2>(pb, stream) : launch_d<64, 3, 3>(pb, stream);
+    constexpr int K3 = kKvWarpsOneTile;
+    const bool one_tile = L.n_mt == 1;
+    if (chunks <= 2) return one_tile ? launch_d<64, 2, 3, K3>(pb, stream) : launch_d<64, 2, 3>(pb, stream);
+    if (chunks <= 3) {
+      if (L.stages == 2) return one_tile ? launch_d<64, 3, 2, K3>(pb, stream) : launch_d<64, 3, 2>(pb, stream);
+      return one_tile ? launch_d<64, 3, 3, K3>(pb, stream) : launch_d<64, 3, 3>(pb, stream);
+    }
     if (chunks <= 4) return launch_d<64, 4, 3>(pb, stream);
     if (chunks <= 6) return L.stages == 2 ? launch_d<64, 6, 2>(pb, stream) : launch_d<64, 6, 3>(pb, stream);
     return L.stages == 2 ? launch_d<64, 9, 2>(pb, stream) : launch_d<64, 9, 3>(pb, stream);
