@@ -205,7 +205,9 @@ __global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_const
   for (int hn = 0; hn < GN; ++hn) {
     uint64_t rx[KS], ry[KS];
     uint32_t qr[KS][2];
-    q_fragments<D, FP8>(base + L::q_off, L::q_panel, hn, tab, qh[hn], ql[hn], qr, rx, ry, qf[hn]);
+    q_fragments<D, FP8>(base + L::q_off, L::q_panel, hn,
+                        [&](int ks, int r) { return tab[(16 * ks + 8 * r + 2 * (lane & 3)) >> 1]; }, qh[hn],
+                        ql[hn], qr, rx, ry, qf[hn]);
     snew[hn] = 0.f;
     if (warp == 0) {
       // q . k_new of the unrotated rows (the same rotation of both cancels)

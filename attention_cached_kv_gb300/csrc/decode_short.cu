@@ -196,8 +196,20 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     }
     __syncwarp();
   };
+  // this lane's angles, frequencies 16 ks + 8 r + 2 t4 (+ 1) at [2 ks + r]: read
+  // once per launch where every query sits at the same position
+  float4 cs[KS];
+  auto load_cs = [&]() {
+#pragma unroll
+    for (int ks = 0; ks < KS / 2; ++ks)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) cs[2 * ks + r] = tab[(16 * ks + 8 * r + 2 * t4) >> 1];
+  };
   const bool fixed_pos = prm.pos_offset == nullptr;
-  if (fixed_pos) build_tab(C);
+  if (fixed_pos) {
+    build_tab(C);
+    load_cs();
+  }
 
   // Per unit, lane b < bpp holds the b-th block id (and, FP8, its K and V scales).
   struct Ids {
@@ -307,7 +319,10 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         *reinterpret_cast<uint4*>(out + idx * 8) = make_uint4(0, 0, 0, 0);
       if (lane == 0) report(prm.status, GIST_ATTN_STATUS_BAD_BLOCK);
     } else {
-      if (!fixed_pos) build_tab(prm.pos_offset[p]);
+      if (!fixed_pos) {
+        build_tab(prm.pos_offset[p]);
+        load_cs();
+      }
       float vmax = 1.f, vinv = 1.f;  // FP8: the unit's largest V scale and its inverse
       if constexpr (FP8) {
         // widen the E4M3 rows of K and V to f16 in the swizzled tiles
@@ -357,7 +372,8 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       for (int hn = 0; hn < GN; ++hn) {
         uint64_t rx[KS], ry[KS];
         uint32_t qr[KS][2];
-        q_fragments<D, FP8>(qt, R::q_panel, hn, tab, qh[hn], ql[hn], qr, rx, ry, qf[hn]);
+        q_fragments<D, FP8>(qt, R::q_panel, hn, [&](int ks, int r) { return cs[2 * ks + r]; }, qh[hn],
+                            ql[hn], qr, rx, ry, qf[hn]);
         sn[hn][0] = sn[hn][1] = sn[hn][2] = sn[hn][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks)

@@ -92,18 +92,19 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src,
 // (128-byte swizzle, q_panel bytes per 64-column panel, tile rows hn*8..+7):
 // lane gets head row hn*8 + g8, elements d = 16 ks + 8 r + 2 t4 (+1) in
 // register [ks][r].  Each element pair (d, d + D/2) is rotated in fp32 by the
-// angles of `tab` ((c_j, s_j, c_j+1, s_j+1) x scale at index j/2, even j),
+// angles cs_of(ks, r) returns for this lane's frequencies j = 16 ks + 8 r + 2 t4
+// and j + 1: (c_j, s_j, c_j+1, s_j+1) x scale,
 // then split into hi + lo (bf16, or f16 after dividing by the power of two
 // *qf so the tile's heads fit f16).  The unrotated query is returned too, for
 // the new key's logit: as the raw bf16 B fragments qr, and as the fp32 pairs
 // (x, y) = (d, d + D/2).
-template <int D, bool F16>
-__device__ __forceinline__ void q_fragments(uint32_t qtile, uint32_t q_panel, int hn, const float4* tab,
+template <int D, bool F16, class CS>
+__device__ __forceinline__ void q_fragments(uint32_t qtile, uint32_t q_panel, int hn, CS cs_of,
                                             uint32_t (&qh)[D / 16][2], uint32_t (&ql)[D / 16][2],
                                             uint32_t (&qr)[D / 16][2], uint64_t (&rx)[D / 16],
                                             uint64_t (&ry)[D / 16], float& qf) {
   constexpr int KS = D / 16, HK = KS / 2;
-  const int lane = threadIdx.x & 31, t4 = lane & 3;
+  const int lane = threadIdx.x & 31;
   uint32_t qb[KS][2];
 #pragma unroll
   for (int ks = 0; ks < KS; ks += 2) {
@@ -126,7 +127,7 @@ __device__ __forceinline__ void q_fragments(uint32_t qtile, uint32_t q_panel, in
   for (int ks = 0; ks < HK; ++ks) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const float4 cs = tab[(16 * ks + 8 * r + 2 * t4) >> 1];
+      const float4 cs = cs_of(ks, r);
       const uint64_t c = f2_make(cs.x, cs.z), sn = f2_make(cs.y, cs.w);
       const uint64_t x = bf16x2_to_f2(qb[ks][r]), y = bf16x2_to_f2(qb[ks + HK][r]);
       rx[2 * ks + r] = x;
