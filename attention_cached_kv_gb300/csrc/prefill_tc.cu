@@ -56,7 +56,7 @@ namespace {
 constexpr int kCompute = 256;            // 8 compute warps
 // Two CTAs share an SM for d = 64 with at most 96 keys (three 16-column chunks
 // per thread); wider tiles and d = 128 run one CTA per SM.
-__host__ __device__ constexpr bool two_per_sm(int D, int NCH) { return D == 64 && NCH <= 3; }
+__host__ __device__ constexpr bool two_per_sm(int D, int NCH) { return D == 64 && NCH <= 4; }
 // K/V warps: where two CTAs share an SM, one when a unit spans several tiles
 // and three when it is one tile (ℓ ≤ ⌊128/G⌋: the unit's copies and key
 // conversion then recur every tile); four where one CTA per SM leaves
@@ -123,7 +123,7 @@ Layout plan_stages(const Problem& pb, int stages) {
   // blocks) take a two-level table: rows t < 16 hold the angles of tokens
   // 0..15, rows 16 + a those of the offsets 16 a, and a token's angle is the
   // sum of its two (angle addition in the rotation).
-  L.tab_rows = L.kv_rows > 128 ? 16 + (pb.l + 15) / 16 : pb.l;
+  L.tab_rows = L.kv_rows > 96 ? 16 + (pb.l + 15) / 16 : pb.l;
   off += (pb.pos_offset ? 2u : 1u) * (uint32_t)L.tab_rows * L.tab_stride;
   L.off_red = off;
   off += 2u * 2 * 128 * 4;  // partial row max and row sum of each half
@@ -150,7 +150,7 @@ Layout plan(const Problem& pb) {
   const Layout L3 = plan_stages(pb, kMaxStages);
   if (L3.bytes > (uint32_t)kMaxSmem) return plan_stages(pb, 2);  // wide key sets
   // (wider key sets than 96 run one CTA per SM for their registers anyway)
-  if (pb.d == 64 && L3.kv_rows <= 96 && L3.tmem_cols == 256 && L3.bytes > kTwoPerSmBytes) {
+  if (pb.d == 64 && L3.kv_rows <= 128 && L3.tmem_cols == 256 && L3.bytes > kTwoPerSmBytes) {
     const Layout L2 = plan_stages(pb, 2);
     if (L2.bytes <= kTwoPerSmBytes) return L2;
   }
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(threads_of(KVW), two_per_sm(D, NCH) ? 2 : 1)
   constexpr int NP = D / 64;   // 64-column panels
   constexpr int CPR = D / 8;   // 16-byte chunks per row
   constexpr int kThreads = threads_of(KVW);
-  constexpr bool TAB2 = NCH > 4;  // two-level angle tables (tiles of more than 128 keys)
+  constexpr bool TAB2 = NCH > 3;  // two-level angle tables (tiles of more than 96 keys)
   constexpr int KVT = 32 * KVW;  // K/V threads
   constexpr int HALF = D / 2;
   constexpr float kNegInf = -INFINITY;
@@ -922,7 +922,7 @@ int launch_prefill_tc(const Problem& pb, cudaStream_t stream) {
       if (L.stages == 2) return one_tile ? launch_d<64, 3, 2, K3>(pb, stream) : launch_d<64, 3, 2>(pb, stream);
       return one_tile ? launch_d<64, 3, 3, K3>(pb, stream) : launch_d<64, 3, 3>(pb, stream);
     }
-    if (chunks <= 4) return launch_d<64, 4, 3>(pb, stream);
+    if (chunks <= 4) return L.stages == 2 ? launch_d<64, 4, 2>(pb, stream) : launch_d<64, 4, 3>(pb, stream);
     if (chunks <= 6) return L.stages == 2 ? launch_d<64, 6, 2>(pb, stream) : launch_d<64, 6, 3>(pb, stream);
     return L.stages == 2 ? launch_d<64, 9, 2>(pb, stream) : launch_d<64, 9, 3>(pb, stream);
   }
