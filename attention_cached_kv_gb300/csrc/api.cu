@@ -209,6 +209,7 @@ extern "C" int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void*
   pb.block_table = block_table;
   pb.pos_offset = pos_offset;
   pb.out = out;
+  if (gattn::prefill_tc_fits(pb)) return gattn::launch_prefill_tc_fp8(pb, kv_scale, stream);
   if (pb.C > 0 && gattn::decode_long_fits(pb)) return gattn::launch_decode_long_fp8(pb, kv_scale, stream);
   if (gattn::decode_short_fits(pb)) return gattn::launch_decode_short_fp8(pb, kv_scale, stream);
   if (gattn::decode_gqa_fits(pb)) return gattn::launch_decode_gqa_fp8(pb, kv_scale, stream);

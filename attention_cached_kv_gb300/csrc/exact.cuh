@@ -32,7 +32,29 @@ struct ExactInputs {
   int rotate;        // 0: q and k_new arrive rotated
   float scale_log2;  // softmax scale x log2(e)
   double theta[64];  // RoPE frequencies rope_theta^(-2j/d), j < d/2
+  // FP8 pool: one fp32 scale per (block, layer, K|V, KV head), the pool's rows
+  // E4M3 bytes at the same element offsets; null for a bf16 pool
+  const float* kv_scale;
 };
+
+// Two E4M3 bytes (the low 16 bits) -> an f16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3_pair_to_f16x2(uint32_t v16) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)v16));
+  return r;
+}
+// An f16 pair -> fp32 (low half first).
+__device__ __forceinline__ void f16x2_to_floats(uint32_t h, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+}
+// One E4M3 byte -> fp32, exactly.
+__device__ __forceinline__ float e4m3_to_float(uint8_t b) {
+  float lo, hi;
+  f16x2_to_floats(e4m3_pair_to_f16x2(b), lo, hi);
+  return lo;
+}
 
 // Rotates v at position `pos`: each pair (v[j], v[j + d/2]) by pos * theta_j.
 template <int D>
@@ -51,6 +73,12 @@ template <int D>
 __device__ __forceinline__ void exact_load_row(float (&v)[D], const bf16* src) {
 #pragma unroll 1
   for (int j = 0; j < D; ++j) v[j] = __bfloat162float(src[j]);
+}
+// A cached row of an FP8 pool (E4M3 bytes), dequantised by its scale.
+template <int D>
+__device__ __forceinline__ void exact_load_row8(float (&v)[D], const uint8_t* src, float scale) {
+#pragma unroll 1
+  for (int j = 0; j < D; ++j) v[j] = e4m3_to_float(src[j]) * scale;
 }
 
 // Output columns col(i) = c0 + (i / 2) * cstep + (i % 2), i < NC, of row
@@ -73,12 +101,22 @@ __device__ __forceinline__ bool exact_row(const ExactInputs& in, int p, int t, i
 #pragma unroll 1
   for (int kappa = lo; kappa < hi; ++kappa) {
     const bf16 *krow, *vrow;
+    const uint8_t* vrow8 = nullptr;  // FP8 pool: the cached value row's bytes
+    float vsc = 1.f;
     if (kappa < in.C) {
       const int b = kappa / in.pv.block_len, r = kappa - b * in.pv.block_len;
       const int32_t blk = pool_block_id(in.pv, p, b);
       krow = pool_row(in.pv, blk, g, 0, r);
       vrow = pool_row(in.pv, blk, g, 1, r);
-      exact_load_row<D>(kr, krow);
+      if (in.kv_scale) {
+        const uint8_t* base8 = reinterpret_cast<const uint8_t*>(in.pv.pool);
+        const int64_t si = (((int64_t)blk * in.pv.num_layers + in.pv.layer) * 2) * in.Hkv + g;
+        exact_load_row8<D>(kr, base8 + (krow - in.pv.pool), in.kv_scale[si]);
+        vrow8 = base8 + (vrow - in.pv.pool);
+        vsc = in.kv_scale[si + in.Hkv];
+      } else {
+        exact_load_row<D>(kr, krow);
+      }
     } else {
       const int i = kappa - in.C;
       const size_t o_new = (((size_t)p * in.l + i) * in.Hkv + g) * D;
@@ -96,8 +134,11 @@ __device__ __forceinline__ bool exact_row(const ExactInputs& in, int p, int t, i
     const float pk = exp2f(s - mn);
     lsum = lsum * al + pk;
 #pragma unroll 1
-    for (int i = 0; i < NC; ++i)
-      o[i] = o[i] * al + pk * __bfloat162float(vrow[c0 + (i >> 1) * cstep + (i & 1)]);
+    for (int i = 0; i < NC; ++i) {
+      const int col = c0 + (i >> 1) * cstep + (i & 1);
+      const float v = vrow8 ? e4m3_to_float(vrow8[col]) * vsc : __bfloat162float(vrow[col]);
+      o[i] = o[i] * al + pk * v;
+    }
     m = mn;
   }
   const float inv = 1.f / lsum;
@@ -167,6 +208,7 @@ inline void exact_inputs_from(ExactInputs& e, const Pb& pb) {
   e.rotate = (pb.flags & GIST_ATTN_FLAG_PREROTATED) ? 0 : 1;
   e.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) e.theta[j] = pb.inv_freq_d[j];
+  e.kv_scale = nullptr;
 }
 
 }  // namespace gattn

@@ -41,6 +41,7 @@ EncodeTiledFn encode_tiled_fn();
 // Each returns GIST_ATTN_OK or a negative GIST_ATTN_ERR_* code.
 int launch_prefill(const Problem& pb, cudaStream_t stream);
 int launch_prefill_tc(const Problem& pb, cudaStream_t stream);
+int launch_prefill_tc_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream);
 int launch_prefill_long(const Problem& pb, cudaStream_t stream);
 int launch_prefill_long_on(const Problem& pb, const void* q, const void* k, const void* v, int C,
                            bool f16, const float2* q_base, const float2* q_rel, cudaStream_t stream);

@@ -92,6 +92,9 @@ struct TcParams {
   float inv_freq[64];
   ExactInputs ex;  // the inputs again, for rows recomputed in fp32
   bf16* out;
+  // FP8 pool: one fp32 scale per (block, layer, K|V, KV head), the pool's rows
+  // E4M3 bytes at the same element offsets; null for a bf16 pool
+  const float* kv_scale;
 };
 
 struct Layout {
@@ -207,6 +210,20 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
 // An f16 chunk of eight keys' elements, or all NaN if one of them is not
 // finite (past the f16 range): every logit that reads the chunk becomes NaN,
 // which sends those rows to the fp32 recomputation.
+// Eight E4M3 values (bytes of a, then of b) times `scale`, rounded once to
+// f16 (F16) or bf16: one 16-byte chunk of a tile row.
+template <bool F16>
+__device__ __forceinline__ uint4 e4m3x8_scaled(uint32_t a, uint32_t b, float scale) {
+  const uint32_t pr[4] = {a & 0xffffu, a >> 16, b & 0xffffu, b >> 16};
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float lo, hi;
+    f16x2_to_floats(e4m3_pair_to_f16x2(pr[e]), lo, hi);
+    w[e] = F16 ? f2_to_f16x2(f2_make(lo * scale, hi * scale)) : float2_to_bf16x2(lo * scale, hi * scale);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 __device__ __forceinline__ uint4 f16_chunk_or_nan(uint4 h) {
   const uint32_t e = 0x7c007c00u;
   const bool bad = (h.x & 0x7c00u) == 0x7c00u || (h.x & 0x7c000000u) == 0x7c000000u ||
@@ -255,10 +272,10 @@ struct Bars {
 };
 
 // NCH: S chunks of 16 columns per thread (the tile's keys / 32, rounded up).
-// KVW: K/V warps.  Registers: each of the 4 SM sub-partitions holds 16 K; two
+// KVW: K/V warps.  FP8: the pool holds E4M3 bytes and scales.  Registers: each of the 4 SM sub-partitions holds 16 K; two
 // CTAs of 11 warps (one K/V warp) put 6 warps on one of them (85 registers a
 // thread), of 13 warps (three) 7 (73); one CTA of 14 warps puts 4 (128).
-template <int D, int NCH, int NS, int KVW>
+template <int D, int NCH, int NS, int KVW, bool FP8>
 __global__ void __launch_bounds__(threads_of(KVW), two_per_sm(D, NCH) ? 2 : 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_o,
@@ -533,11 +550,39 @@ __global__ void __launch_bounds__(threads_of(KVW), two_per_sm(D, NCH) ? 2 : 1)
         }
         const bf16* ks = pool_row(prm.pv, blk, g, 0, 0);
         const bf16* vs = pool_row(prm.pv, blk, g, 1, 0);
-        for (int w = kt; w < bl * CPR; w += KVT) {
-          const int t = w / CPR, c = w % CPR;
-          const uint32_t o = (c >> 3) * kv_panel + swz128(bi * bl + t, c & 7);
-          cp_async16(kb + o, ks + t * D + c * 8);
-          cp_async16(vb + o, vs + t * D + c * 8);
+        if constexpr (FP8) {
+          // FP8 pool: 16 E4M3 bytes of a row at a time, dequantised by the
+          // block's scales straight into the tiles (keys to f16 with chunks past
+          // its range NaN, or bf16 for inputs that arrive rotated; values to
+          // bf16), with their own loads: the block is a few rows
+          const uint8_t* base8 = reinterpret_cast<const uint8_t*>(prm.pv.pool);
+          const uint8_t* k8 = base8 + (ks - prm.pv.pool);
+          const uint8_t* v8 = base8 + (vs - prm.pv.pool);
+          const int64_t si = (((int64_t)blk * prm.pv.num_layers + prm.pv.layer) * 2) * prm.Hkv + g;
+          const float ksc = prm.kv_scale[si], vsc = prm.kv_scale[si + prm.Hkv];
+          for (int w = kt; w < bl * (D / 16); w += KVT) {
+            const int t = w / (D / 16), c = 2 * (w % (D / 16));  // f16 chunks c, c + 1
+            const uint4 kr = __ldg(reinterpret_cast<const uint4*>(k8 + t * D + c * 8));
+            const uint4 vr = __ldg(reinterpret_cast<const uint4*>(v8 + t * D + c * 8));
+            const int row = bi * bl + t;
+            if (prm.rotated) {
+              sts16(chunk_addr(kb, kv_panel, row, c), e4m3x8_scaled<false>(kr.x, kr.y, ksc));
+              sts16(chunk_addr(kb, kv_panel, row, c + 1), e4m3x8_scaled<false>(kr.z, kr.w, ksc));
+            } else {
+              sts16(chunk_addr(kb, kv_panel, row, c), f16_chunk_or_nan(e4m3x8_scaled<true>(kr.x, kr.y, ksc)));
+              sts16(chunk_addr(kb, kv_panel, row, c + 1),
+                    f16_chunk_or_nan(e4m3x8_scaled<true>(kr.z, kr.w, ksc)));
+            }
+            sts16(chunk_addr(vb, kv_panel, row, c), e4m3x8_scaled<false>(vr.x, vr.y, vsc));
+            sts16(chunk_addr(vb, kv_panel, row, c + 1), e4m3x8_scaled<false>(vr.z, vr.w, vsc));
+          }
+        } else {
+          for (int w = kt; w < bl * CPR; w += KVT) {
+            const int t = w / CPR, c = w % CPR;
+            const uint32_t o = (c >> 3) * kv_panel + swz128(bi * bl + t, c & 7);
+            cp_async16(kb + o, ks + t * D + c * 8);
+            cp_async16(vb + o, vs + t * D + c * 8);
+          }
         }
       }
       const bf16* kn = prm.k_new + ((size_t)p * l * prm.Hkv + g) * D;
@@ -560,7 +605,7 @@ __global__ void __launch_bounds__(threads_of(KVW), two_per_sm(D, NCH) ? 2 : 1)
       cp_async_wait_all();
       kv_sync();  // every K/V thread's copies (and table rows) have landed
       if (!bad && !prm.rotated) {
-        for (int bi = 0; bi < bpp; ++bi) {
+        for (int bi = 0; bi < (FP8 ? 0 : bpp); ++bi) {  // (an FP8 pool's keys are f16 already)
           for (int w = kt; w < bl * CPR; w += KVT) {
             const int t = w / CPR, c = w % CPR;
             const uint32_t a = chunk_addr(kb, kv_panel, bi * bl + t, c);
@@ -839,7 +884,8 @@ int encode_map(CUtensorMap* m, const void* base, const Problem& pb, int Tm) {
 }
 
 template <int D, int NCH, int NS, int KVW = kv_warps(D, NCH)>
-int launch_d(const Problem& pb, cudaStream_t stream) {
+int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
+  constexpr bool F = false;
   const Layout L = plan(pb);
   if (L.stages != NS) return GIST_ATTN_ERR_UNSUPPORTED;  // shared memory is sized for L.stages
   TcParams prm{};
@@ -875,15 +921,17 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.inv_freq[j] = pb.inv_freq[j];
   exact_inputs_from(prm.ex, pb);
+  prm.ex.kv_scale = kv_scale;
   prm.out = static_cast<bf16*>(pb.out);
+  prm.kv_scale = kv_scale;
 
   alignas(64) CUtensorMap tm_q, tm_o;
   int rc = encode_map(&tm_q, pb.q, pb, L.Tm);
   if (rc != GIST_ATTN_OK) return rc;
   rc = encode_map(&tm_o, pb.out, pb, L.Tm);
   if (rc != GIST_ATTN_OK) return rc;
-  if (cudaFuncSetAttribute(prefill_tc_kernel<D, NCH, NS, KVW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)L.bytes) != cudaSuccess)
+  auto kern = kv_scale ? prefill_tc_kernel<D, NCH, NS, KVW, true> : prefill_tc_kernel<D, NCH, NS, KVW, F>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -894,7 +942,7 @@ int launch_d(const Problem& pb, cudaStream_t stream) {
   const int per_sm = (two_per_sm(D, NCH) && L.tmem_cols == 256 && L.bytes <= kTwoPerSmBytes) ? 2 : 1;
   const int64_t units = (int64_t)pb.P * pb.Hkv;
   const int grid = (int)(units < (int64_t)sms * per_sm ? units : (int64_t)sms * per_sm);
-  prefill_tc_kernel<D, NCH, NS, KVW><<<grid, threads_of(KVW), L.bytes, stream>>>(tm_q, tm_o, prm);
+  kern<<<grid, threads_of(KVW), L.bytes, stream>>>(tm_q, tm_o, prm);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
@@ -911,27 +959,39 @@ bool prefill_tc_fits(const Problem& pb) {
   return L.bytes <= (uint32_t)kMaxSmem;
 }
 
-int launch_prefill_tc(const Problem& pb, cudaStream_t stream) {
+namespace {
+int launch_any(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
   const Layout L = plan(pb);
   const int chunks = (L.kv_rows / 16 + 1) / 2;  // per thread: chunks h, h+2, ...
+  const bool s2 = L.stages == 2;
+  const float* ks = kv_scale;
   if (pb.d == 64) {
     constexpr int K3 = kKvWarpsOneTile;
-    const bool one_tile = L.n_mt == 1;
-    if (chunks <= 2) return one_tile ? launch_d<64, 2, 3, K3>(pb, stream) : launch_d<64, 2, 3>(pb, stream);
+    const bool one = L.n_mt == 1;
+    if (chunks <= 2) return one ? launch_d<64, 2, 3, K3>(pb, ks, stream) : launch_d<64, 2, 3>(pb, ks, stream);
     if (chunks <= 3) {
-      if (L.stages == 2) return one_tile ? launch_d<64, 3, 2, K3>(pb, stream) : launch_d<64, 3, 2>(pb, stream);
-      return one_tile ? launch_d<64, 3, 3, K3>(pb, stream) : launch_d<64, 3, 3>(pb, stream);
+      if (s2) return one ? launch_d<64, 3, 2, K3>(pb, ks, stream) : launch_d<64, 3, 2>(pb, ks, stream);
+      return one ? launch_d<64, 3, 3, K3>(pb, ks, stream) : launch_d<64, 3, 3>(pb, ks, stream);
     }
-    if (chunks <= 4) return L.stages == 2 ? launch_d<64, 4, 2>(pb, stream) : launch_d<64, 4, 3>(pb, stream);
-    if (chunks <= 6) return L.stages == 2 ? launch_d<64, 6, 2>(pb, stream) : launch_d<64, 6, 3>(pb, stream);
-    return L.stages == 2 ? launch_d<64, 9, 2>(pb, stream) : launch_d<64, 9, 3>(pb, stream);
+    if (chunks <= 4) return s2 ? launch_d<64, 4, 2>(pb, ks, stream) : launch_d<64, 4, 3>(pb, ks, stream);
+    if (chunks <= 6) return s2 ? launch_d<64, 6, 2>(pb, ks, stream) : launch_d<64, 6, 3>(pb, ks, stream);
+    return s2 ? launch_d<64, 9, 2>(pb, ks, stream) : launch_d<64, 9, 3>(pb, ks, stream);
   }
   if (pb.d == 128) {  // (two q stages where a per-unit angle table takes the room of a third)
-    if (chunks <= 2) return L.stages == 2 ? launch_d<128, 2, 2>(pb, stream) : launch_d<128, 2, 3>(pb, stream);
-    if (chunks <= 3) return L.stages == 2 ? launch_d<128, 3, 2>(pb, stream) : launch_d<128, 3, 3>(pb, stream);
-    return L.stages == 2 ? launch_d<128, 4, 2>(pb, stream) : launch_d<128, 4, 3>(pb, stream);
+    if (chunks <= 2) return s2 ? launch_d<128, 2, 2>(pb, ks, stream) : launch_d<128, 2, 3>(pb, ks, stream);
+    if (chunks <= 3) return s2 ? launch_d<128, 3, 2>(pb, ks, stream) : launch_d<128, 3, 3>(pb, ks, stream);
+    return s2 ? launch_d<128, 4, 2>(pb, ks, stream) : launch_d<128, 4, 3>(pb, ks, stream);
   }
   return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+int launch_prefill_tc(const Problem& pb, cudaStream_t stream) { return launch_any(pb, nullptr, stream); }
+
+// The E4M3 pool: the K/V warps dequantise the cached rows by their scales.
+int launch_prefill_tc_fp8(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
+  return launch_any(pb, kv_scale, stream);
 }
 
 }  // namespace gattn

@@ -205,12 +205,15 @@ int gist_attn_fwd_noalloc(const void* q, const void* k_new, const void* v_new,
  *   kv_pool_e4m3 uint8 [num_blocks][L][2][Hkv][block_len][d] (same layout as the
  *                bf16 pool, one byte per element), 16-byte aligned
  *   kv_scale     float [num_blocks][L][2][Hkv], 4-byte aligned
- * Other arguments as gist_attn_fwd.  This build runs the decode step (l = 1):
- * equal query and KV head counts with a cache of at least 64 rows in blocks of
- * a multiple of 16 rows (the paged layout); groups of 2..16 query heads with
- * more than 32 cached rows in at most 512 blocks of a multiple of 16 rows (GQA
- * paged); or groups of at most 16 query heads with at most 32 cached rows in
- * blocks of a multiple of 8 rows (the query-gisted layout of [Gist page,
+ * Other arguments as gist_attn_fwd.  This build runs blocks of l >= 2 new
+ * tokens whose cached rows and new tokens together are at most 288 keys for
+ * d = 64 and 128 for d = 128, with at most 128 query heads per KV head (the
+ * shapes of gist_attn_fwd's tensor-core prefill), and the decode step (l = 1):
+ * equal query and KV head counts with a cache of at least 64 rows in blocks
+ * of a multiple of 16 rows (the paged layout); groups of 2..16 query heads
+ * with more than 32 cached rows in at most 512 blocks of a multiple of 16 rows
+ * (GQA paged); or groups of at most 16 query heads with at most 32 cached rows
+ * in blocks of a multiple of 8 rows (the query-gisted layout of [Gist page,
  * "能不能再进一步"]).  Other shapes return GIST_ATTN_ERR_UNSUPPORTED.  Scales
  * must be finite and non-negative.
  */

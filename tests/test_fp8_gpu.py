@@ -56,7 +56,7 @@ def test_fp8_short_decode_every_pair(P, Hq, Hkv, d, bl, bpp, rpos):
     compare(got, oracle_ref_fp8(wl, pool8, scale, layer=1), f"fp8 short G={Hq // Hkv} d={d}")
 
 
-@pytest.mark.parametrize("shape", ["short", "paged", "gqa"])
+@pytest.mark.parametrize("shape", ["short", "paged", "gqa", "prefill"])
 @pytest.mark.parametrize("magnitude", [1e-2, 1e-4])
 def test_fp8_small_scales(shape, magnitude):
     """Scales near amax / 448 of real activations (1e-2, 1e-4), spread over two
@@ -65,6 +65,8 @@ def test_fp8_small_scales(shape, magnitude):
         wl = workloads.make_custom(6, 1, 14, 2, 64, 8, 2, 9, device=DEV, seed=4)
     elif shape == "gqa":
         wl = workloads.make_custom(4, 1, 16, 4, 128, 32, 3, 9, device=DEV, seed=4, use_table=True)
+    elif shape == "prefill":
+        wl = workloads.make_custom(4, 12, 14, 2, 64, 8, 2, 9, device=DEV, seed=4, use_table=True)
     else:
         wl = workloads.make_custom(4, 1, 8, 8, 128, 32, 3, 9, device=DEV, seed=4, use_table=True)
     pool8, scale = workloads.make_fp8_pool(wl, seed=3)
@@ -132,12 +134,73 @@ def test_fp8_paged_workload_sampled():
 
 
 def test_fp8_unsupported_shapes_are_refused():
-    wl = workloads.make_custom(2, 4, 8, 2, 64, 8, 1, 3, device=DEV)
+    """Four new tokens behind 320 cached keys: more keys than a tensor-core tile
+    holds, and not a decode step."""
+    wl = workloads.make_custom(2, 4, 8, 2, 64, 160, 2, 3, device=DEV)
     pool8, scale = workloads.make_fp8_pool(wl)
     with pytest.raises(binding.GistAttnError) as e:
-        binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, wl.item_ids, None, None,
-                                    dims=wl.dims)
+        binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, wl.item_ids,
+                                    wl.block_table, None, dims=wl.dims)
     assert e.value.code == binding.ERR_UNSUPPORTED
+
+
+# l >= 2: the tensor-core prefill dequantises the cached rows in its K/V warps
+PREFILL = [
+    (4, 12, 14, 2, 64, 8, 1, True),     # the gist model: 8 item-gist keys, 12 new tokens
+    (3, 20, 32, 8, 128, 8, 1, False),   # the wide model's heads
+    (3, 40, 14, 2, 64, 16, 3, True),    # three 16-row blocks, several tiles per unit
+    (3, 16, 14, 2, 64, 32, 2, False),   # one tile per unit (three K/V warps), 80 keys
+    (2, 64, 14, 2, 64, 32, 2, True),    # 128 keys: the two-level angle table
+    (2, 256, 14, 2, 64, 8, 4, False),   # 288 keys per tile
+]
+
+
+@pytest.mark.parametrize("P,l,Hq,Hkv,d,bl,bpp,rpos", PREFILL, ids=lambda v: str(v))
+def test_fp8_prefill_every_pair(P, l, Hq, Hkv, d, bl, bpp, rpos):
+    wl = workloads.make_custom(P, l, Hq, Hkv, d, bl, bpp, 9, num_layers=2, layer=1, device=DEV,
+                               seed=l + bl, random_pos=rpos)
+    pool8, scale = workloads.make_fp8_pool(wl, seed=l)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, wl.item_ids,
+                                      wl.block_table, wl.pos_offset, dims=dict(wl.dims, layer=1),
+                                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(got, oracle_ref_fp8(wl, pool8, scale, layer=1), f"fp8 prefill l={l} C={bl * bpp} d={d}")
+
+
+def test_fp8_prefill_keys_past_the_f16_range():
+    """A block whose K scale (1e5) dequantises keys past the f16 range: the rows
+    that read them are recomputed in fp32 from the E4M3 bytes and match the
+    oracle; the status word stays clear."""
+    wl = workloads.make_custom(4, 12, 14, 2, 64, 8, 1, 6, num_layers=2, layer=1, device=DEV, seed=9)
+    pool8, scale = workloads.make_fp8_pool(wl, seed=9)
+    blk = int(wl.item_ids[1].item())
+    scale[blk, 1, 0, 0] = 1.0e5
+    wl.q.mul_(1.0e-5)  # logits against that block stay of order one
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, wl.item_ids, None, None,
+                                      dims=dict(wl.dims, layer=1), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(got, oracle_ref_fp8(wl, pool8, scale, layer=1), "fp8 prefill keys past f16")
+
+
+def test_fp8_gist_workload_sampled():
+    """The gist workload (12,800 pairs, l = 64 against 8 cached keys) read from
+    an E4M3 pool, as the benchmark's --workload gist --kv fp8 row times it."""
+    wl = workloads.make("gist", device=DEV, num_layers=2)
+    pool8, scale = workloads.make_fp8_pool(wl)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, wl.item_ids, None, None,
+                                      dims=dict(wl.dims, layer=1), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel = np.sort(np.random.default_rng(2).choice(wl.dims["num_pairs"], 60, replace=False))
+    compare(got[torch.from_numpy(sel).to(DEV)], oracle_ref_fp8(wl, pool8, scale, layer=1, pairs=sel),
+            "fp8 gist")
+    del wl, pool8, got
+    torch.cuda.empty_cache()
 
 
 def test_fp8_bad_block_zeroes_and_flags():
