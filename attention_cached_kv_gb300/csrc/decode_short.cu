@@ -21,15 +21,13 @@
 // fp32, pre-scaled to log2 units and split into bf16 hi + lo (two MMA passes),
 // so the rounding of rotated q stays out of the logits; keys, values and P V
 // stay bf16 with fp32 accumulation, so every bf16 input is in range.  The
-// output rows go from the accumulators into the unit's q tile (read by then)
-// and out by one tensor store.
+// output rows go from the accumulators straight to global memory.
 //
 // Persistent warps, two units in flight per warp: while a warp computes unit n
 // from one of its two shared-memory buffers, the tensor copies of unit n + 1
 // (its cached K and V blocks as whole {64, block_len} boxes of the pool, one
-// lane per block, and its new key and value from two more lanes, all issued
-// side by side; its q rows part-way through unit n, once the store of unit
-// n - 1 has read that q tile) fill the other buffer and complete on that
+// lane per block, and its q rows, new key and new value from three more lanes,
+// all issued side by side) fill the other buffer and complete on that
 // buffer's mbarrier; the block ids of unit n + 2 are on their way.  A wait that
 // runs out (1 s) reports GIST_ATTN_STATUS_TIMEOUT, waits once more for the copy
 // still in flight and ends the warp.
@@ -85,8 +83,7 @@ struct ShortParams {
 // pool the two buffers share one pair, into which the unit being computed
 // widens the E4M3 rows its buffer staged (the copies of the next unit land in
 // the other buffer's staging rows meanwhile).  A buffer's own part is the q
-// tile (GN x 8 rows per panel, same swizzle; it holds the unit's output rows
-// before their store) and, FP8, the staged E4M3 rows of
+// tile (GN x 8 rows per panel, same swizzle) and, FP8, the staged E4M3 rows of
 // K and V; its small parts are the new key and value rows.  Keeping the small
 // parts out of the 1 KiB-aligned tiles, and the FP8 pool's widened tiles
 // single, lets five CTAs of four warps share an SM on the query-gisted shape
@@ -124,8 +121,7 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
                                                                 const __grid_constant__ CUtensorMap tm_pool,
                                                                 const __grid_constant__ CUtensorMap tm_q,
                                                                 const __grid_constant__ CUtensorMap tm_kn,
-                                                                const __grid_constant__ CUtensorMap tm_vn,
-                                                                const __grid_constant__ CUtensorMap tm_o) {
+                                                                const __grid_constant__ CUtensorMap tm_vn) {
   using R = Region<D, GN, MT, FP8>;
   constexpr int NP = D / 64;
   constexpr int CPR = D / 8;  // 16-byte chunks per bf16 row
@@ -263,25 +259,18 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         }
       }
     }
-    if (lane >= 30) {
-      const bool k = lane == 30;
-      tma_load_2d(base + (k ? R::kn_off : R::vn_off) + b * R::small, k ? &tm_kn : &tm_vn, &kvbar[b], 0,
-                  p * prm.Hkv + g0);
+    if (lane >= 29) {
+      if (lane == 29) {
+#pragma unroll
+        for (int x = 0; x < NP; ++x)
+          tma_load_2d(base + R::q_at(b) + x * R::q_panel, &tm_q, &kvbar[b], 64 * x, p * prm.Hq + g0 * G);
+      } else {
+        const bool k = lane == 30;
+        tma_load_2d(base + (k ? R::kn_off : R::vn_off) + b * R::small, k ? &tm_kn : &tm_vn, &kvbar[b], 0,
+                    p * prm.Hkv + g0);
+      }
     }
     return bad;
-  };
-  // The q rows of unit (p, KV head g0) into buffer b, by lane 29 once the output
-  // store that last read the buffer's q tile (lane 29's, a unit earlier) has
-  // read it.  They count towards the same barrier phase as the unit's other
-  // copies; issued part-way through the previous unit, so the store has long
-  // finished reading by then.
-  auto issue_q = [&](int p, int g0, int b) {
-    if (lane == 29) {
-      bulk_wait_read_all();
-#pragma unroll
-      for (int x = 0; x < NP; ++x)
-        tma_load_2d(base + R::q_at(b) + x * R::q_panel, &tm_q, &kvbar[b], 64 * x, p * prm.Hq + g0 * G);
-    }
   };
 
   // ---- the walk over units u, u + W, ...: (pair, unit-in-pair) by carries
@@ -297,7 +286,6 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
   };
   Ids ids_cur = load_ids(u, p, gg);
   bool bad_cur = issue(p, gg, 0, ids_cur.id);
-  issue_q(p, gg, 0);
   int un = u + W, pn = p, gn = gg;
   step(pn, gn);
   Ids ids_next = load_ids(un, pn, gn);
@@ -321,13 +309,11 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
       // give up: report, wait (bounded) for the copy still in flight, stop
       if (lane == 0) report(prm.status, GIST_ATTN_STATUS_TIMEOUT);
       if (more) mbar_wait(&kvbar[b ^ 1], (uint32_t)((n + 1) >> 1) & 1u);
-      if (lane == 29) bulk_wait_all();
       return;
     }
 
     const int g0 = gg;
     if (bad_cur) {
-      if (more) issue_q(pn, gn, b ^ 1);
       bf16* out = prm.out + ((size_t)p * prm.Hq + (size_t)g0 * G) * D;
       for (int idx = lane; idx < G * CPR; idx += 32)
         *reinterpret_cast<uint4*>(out + idx * 8) = make_uint4(0, 0, 0, 0);
@@ -420,7 +406,6 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
 #pragma unroll
           for (int e = 0; e < 4; ++e) s[mt][hn][e] += s2[mt][hn][e];
       }
-      if (more) issue_q(pn, gn, b ^ 1);  // the next unit's q rows
 
       // ---- softmax of every head over its cached keys and the new key
       float pn_[GN][2], il[GN][2];  // weight of the new key and 1 / sum, head slots 8 hn + 2 t4 (+ 1)
@@ -508,8 +493,8 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
 
       // ---- the new value and the normalisation: this lane's rows are head
       // slots 8 hn + g8, whose softmax terms sit in lane g8 / 2 (slot g8 % 2).
-      // The rows go into the q tile (its fragments were read before S), then out
-      // by one tensor store per panel from lane 29.
+      // The rows go straight to global memory (the four lanes of a row write 16
+      // contiguous bytes per 8-column step), so no store ever holds a buffer.
 #pragma unroll
       for (int hn = 0; hn < GN; ++hn) {
         const int src = g8 >> 1;
@@ -521,20 +506,14 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
         const uint64_t oc = f2_make(vmax * inv, vmax * inv), on = f2_make(pnew * inv, pnew * inv);
         const uint32_t vn = base + R::vn_off + b * R::small;
         const int slot = hn * 8 + g8;
+        bf16* orow = prm.out + ((size_t)p * prm.Hq + (size_t)g0 * G + slot) * D;
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn) {
           const int col = dn * 8 + 2 * t4;
           const uint64_t r2 = f2_fma(bf16x2_to_f2(lds32(vn + col * 2)), on,
                                      f2_mul(f2_make(o[dn][2 * hn], o[dn][2 * hn + 1]), oc));
-          sts32(qt + (dn >> 3) * R::q_panel + swz128(slot, dn & 7) + 4 * t4, f2_to_bf16x2(r2));
+          if (slot < G) *reinterpret_cast<uint32_t*>(orow + col) = f2_to_bf16x2(r2);
         }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 29) {
-#pragma unroll
-        for (int x = 0; x < NP; ++x) tma_store_2d(&tm_o, qt + x * R::q_panel, 64 * x, p * prm.Hq + g0 * G);
-        bulk_commit();
       }
     }
     // buffer b is free for the unit after next; its shared-memory reads and
@@ -552,7 +531,6 @@ __global__ void __launch_bounds__(kThreads) decode_short_kernel(const __grid_con
     ids_cur = ids_next;
     ids_next = ids_after;
   }
-  if (lane == 29) bulk_wait_all();
 }
 
 template <int D, int GN, int MT, bool FP8>
@@ -576,7 +554,7 @@ int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
   prm.region = R::bytes;
   prm.scale_log2 = pb.scale_log2;
   for (int j = 0; j < 64; ++j) prm.theta[j] = pb.inv_freq_d[j];
-  alignas(64) CUtensorMap tm_pool{}, tm_q{}, tm_kn{}, tm_vn{}, tm_o{};
+  alignas(64) CUtensorMap tm_pool{}, tm_q{}, tm_kn{}, tm_vn{};
   const int64_t pool_rows = (int64_t)pb.num_blocks * pb.L * 2 * pb.Hkv * pb.block_len;
   const int box_rows = pb.block_len;  // a block's rows of one KV head
   int rc = FP8 ? encode_2d(&tm_pool, pb.kv_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pool_rows, D, D,
@@ -585,9 +563,6 @@ int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
                            64, box_rows, true);
   if (rc == GIST_ATTN_OK)
     rc = encode_2d(&tm_q, pb.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hq, D, 64,
-                   pb.G, true);
-  if (rc == GIST_ATTN_OK)
-    rc = encode_2d(&tm_o, pb.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hq, D, 64,
                    pb.G, true);
   if (rc == GIST_ATTN_OK)
     rc = encode_2d(&tm_kn, pb.k_new, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (int64_t)pb.P * pb.Hkv, D,
@@ -609,7 +584,7 @@ int launch_d(const Problem& pb, const float* kv_scale, cudaStream_t stream) {
   // persistent: one wave of resident CTAs walks all units
   const int64_t need = (prm.units + kWarps - 1) / kWarps;
   const int64_t grid = need < (int64_t)sms * per_sm ? need : (int64_t)sms * per_sm;
-  kern<<<(unsigned)grid, kThreads, bytes, stream>>>(prm, tm_pool, tm_q, tm_kn, tm_vn, tm_o);
+  kern<<<(unsigned)grid, kThreads, bytes, stream>>>(prm, tm_pool, tm_q, tm_kn, tm_vn);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
