@@ -268,9 +268,12 @@ def oracle_rate(wl, layer: int, target_s: float) -> dict:
     t0 = run(n0)
     want = n0 * target_s / max(t0, 1e-6)  # pairs that take about target_s
     n = int(min(P, max(n0, want)))
-    # a layer that takes well under target_s is timed over several passes
-    reps = max(1, int(round(want / P))) if n == P else 1
-    t = sum(run(n) for _ in range(reps))
+    # a layer that takes well under target_s is timed over as many passes as
+    # that takes
+    t, reps = run(n), 1
+    while n == P and t < target_s:
+        t += run(n)
+        reps += 1
     passes = f", {reps} passes" if reps > 1 else ""
     return {"value": n * reps / t, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} of {P} pairs of layer {layer}, all heads and tokens{passes} ({t:.1f} s)"}
