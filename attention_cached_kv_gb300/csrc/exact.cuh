@@ -21,6 +21,13 @@
 
 namespace gattn {
 
+// Rows whose largest logit (log2 units, scale applied) exceeds this are also
+// recomputed here by the kernels that round q and the keys to f16 for q.K: the
+// rounding puts an error of about 2^-12 |q| |k| scale on every logit, and large
+// logits come with large norms, so past ~20 (about 14 nats) that error nears
+// the parity bound of the outputs.  Ordinary rows sit far below it.
+constexpr float kExactLogit = 20.f;
+
 // The call's inputs as the C ABI received them.
 struct ExactInputs {
   const bf16* q;      // [P][l][Hq][d]

@@ -402,11 +402,12 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
       l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
       float inv_a = 1.f / l_a, inv_b = 1.f / l_b;
-      // a non-finite sum: a query or key value past the f16 range reached the
-      // row; this lane's columns of it are recomputed in fp32
+      // a non-finite sum (a query or key value past the f16 range reached the
+      // row) or a largest logit past kExactLogit: this lane's columns of the row
+      // are recomputed in fp32
       for (int w = 0; w < 2; ++w) {
         const int rr = w ? rb : ra;
-        if (rr < rows && !((w ? l_b : l_a) <= 3.0e38f)) {
+        if (rr < rows && !((w ? l_b : l_a) <= 3.0e38f && (w ? m_b : m_a) <= kExactLogit)) {
           float ex[D / 4];
           const int tt = w ? ttb : tta;
           if (!exact_row<D, D / 4>(prm.ex, p, t0 + tt, g * G + (rr - tt * G), w ? lo_b : lo_a,

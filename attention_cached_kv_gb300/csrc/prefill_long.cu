@@ -609,7 +609,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         red_sum[h * 128 + r] = (a0 + a1) + (b0 + b1);
         named_bar_sync(pair_bar, 64);
         const float sum = red_sum[r] + red_sum[128 + r];
-        const bool fin = sum <= 3.0e38f;
+        // (f16 scores: a row whose largest logit passes kExactLogit goes to fp32 too)
+        const bool fin = sum <= 3.0e38f && !(prm.f16 && m * sc > kExactLogit);
         const float inv = fin ? rcp_approx(sum) : __int_as_float(0x7fc00000);  // NaN row
         if (valid && !fin) bars->flagged = 1;
         const uint32_t stage = sbase + kOffQ + (i & 1) * kTile;

@@ -749,6 +749,10 @@ __global__ void __launch_bounds__(threads_of(KVW), two_per_sm(D, NCH) ? 2 : 1)
           const int c = 2 * cc + h;
           if (c * 16 < N) mx0 = fmaxf(mx0, ld16_max(tmem + lane_base + c * 16));
         }
+        // A row whose largest logit passes kExactLogit (q.K in f16 too coarse
+        // there) takes m = +inf: every weight is 0, the sum too, and the row
+        // goes to the fp32 recomputation.
+        if (mx0 * prm.scale_log2 > kExactLogit && !prm.rotated) mx0 = INFINITY;
         red_max[h * 128 + r] = mx0;
         named_bar_sync(pair_bar, 64);
         const float m = fmaxf(red_max[r], red_max[128 + r]);

@@ -9,7 +9,8 @@ on:
     cached key -- the kernels that form q.K in f16 recompute the rows that meet
     one in fp32 -- and in a value;
   * positions far from 0 (6.5e4, 1e6, 2^30 and the largest that fits), where an
-    angle formed as an fp32 product would be off by whole radians.
+    angle formed as an fp32 product would be off by whole radians;
+  * q and keys scaled up together, so that logits spread over tens of nats.
 Every case names the kernel its shape selects (the dispatch of gist_attn_fwd)."""
 from __future__ import annotations
 
@@ -37,7 +38,7 @@ def _lib():
 SHAPES = {
     "prefill_tc": (4, 12, 14, 2, 64, 8, 1, 6, False),
     "prefill_tc_d128": (3, 20, 32, 8, 128, 8, 1, 5, False),
-    "prefill_stream": (3, 40, 14, 2, 64, 100, 2, 7, False),
+    "prefill_stream": (3, 40, 14, 2, 64, 128, 2, 7, False),  # 296 keys: past prefill_tc
     "staged": (3, 290, 14, 2, 64, 16, 2, 7, True),
     "prefill_tc_wide_keys": (3, 200, 14, 2, 64, 16, 2, 7, False),
     "decode_short": (5, 1, 14, 2, 64, 8, 2, 9, False),
@@ -122,6 +123,20 @@ def test_positions_far_from_zero(kernel):
     wl.pos_offset = torch.tensor([far[i % len(far)] for i in range(P)], dtype=torch.int32,
                                  device=DEV)
     check(wl, staged, f"{kernel} far positions")
+
+
+@pytest.mark.parametrize("kernel", sorted(SHAPES))
+@pytest.mark.parametrize("factor", [2.0, 4.0])
+def test_large_logits(kernel, factor):
+    """q and every key scaled by `factor` (logits by factor^2: a spread of 4 and
+    16 times the workloads', up to tens of nats): the kernels that round q and
+    the keys to f16 send rows whose largest logit is that large to the fp32
+    recomputation, so the output still matches the oracle everywhere."""
+    wl, staged = make(kernel, seed=17, random_pos=True)
+    wl.q.mul_(factor)
+    wl.k_new.mul_(factor)
+    wl.kv_pool[:, :, 0].mul_(factor)
+    check(wl, staged, f"{kernel} logits x{factor * factor:g}")
 
 
 def test_masked_key_far_above_the_visible_ones():
