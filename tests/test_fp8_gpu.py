@@ -169,6 +169,21 @@ def test_fp8_prefill_every_pair(P, l, Hq, Hkv, d, bl, bpp, rpos):
     compare(got, oracle_ref_fp8(wl, pool8, scale, layer=1), f"fp8 prefill l={l} C={bl * bpp} d={d}")
 
 
+def test_fp8_prefill_prerotated():
+    """q and k_new that arrive rotated (GIST_ATTN_FLAG_PREROTATED, the fused
+    projection's output): S runs in bf16, so the cached keys dequantise to bf16."""
+    wl = workloads.make_custom(3, 20, 14, 2, 64, 16, 2, 7, num_layers=2, layer=1, device=DEV, seed=23,
+                               random_pos=True)
+    pool8, scale = workloads.make_fp8_pool(wl, seed=23)
+    wl.dims = dict(wl.dims, layer=1, flags=binding.FLAG_PREROTATED)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, wl.item_ids,
+                                      wl.block_table, wl.pos_offset, dims=wl.dims, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(got, oracle_ref_fp8(wl, pool8, scale, layer=1), "fp8 prefill pre-rotated")
+
+
 def test_fp8_prefill_keys_past_the_f16_range():
     """A block whose K scale (1e5) dequantises keys past the f16 range: the rows
     that read them are recomputed in fp32 from the E4M3 bytes and match the
