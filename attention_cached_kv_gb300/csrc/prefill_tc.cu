@@ -13,12 +13,14 @@
 //   * warp 8 (MMA): tcgen05.mma issue (S = Q K^T, O = P V);
 //   * warp 9 (TMA): TMA loads of 128-row Q tiles into a 3-stage ring and TMA
 //     stores of O, so that waiting for a store never delays the tensor core;
-//   * warp 10 (K/V): stages each unit's K/V into one of two buffers one unit
-//     ahead (cached rows through the pool gather, new rows raw, by 16-byte
-//     cp.async), converts the cached keys to f16 and rotates the new keys in
-//     place, and hands the buffer over by an mbarrier; the tensor core's commit
-//     after the unit's last P V hands it back.  This keeps the staging off the
-//     compute warps, whose per-row work sets the pace;
+//   * warps 10.. (K/V: one, or three where a unit is a single tile, or four
+//     with one CTA per SM): stage each unit's K/V into one of two buffers one
+//     unit ahead (cached rows through the pool gather, new rows raw, by 16-byte
+//     cp.async; an E4M3 pool's cached rows are dequantised by their block
+//     scales on the way in), convert the cached keys to f16 and rotate the new
+//     keys in place, and hand the buffer over by an mbarrier; the tensor core's
+//     commit after the unit's last P V hands it back.  This keeps the staging
+//     off the compute warps, whose per-row work sets the pace;
 //   * warps 0-7 (compute): two threads per tile row (TMEM lane = row; the
 //     halves split the columns).  They rotate q, run the softmax out of TMEM (P
 //     back into TMEM as bf16), and normalise O into the stage for the store.
@@ -30,7 +32,9 @@
 //   non-finite softmax sum and is stored as NaN; the CTA notes that, and once
 //   its last store has landed it recomputes those rows in fp32 from the inputs
 //   (exact.cuh), so the result holds on the whole bf16 range while the hot
-//   loop carries no extra code.  P V stays
+//   loop carries no extra code.  A row whose largest logit passes kExactLogit
+//   (where the f16 rounding of q nears the parity bound) is sent there too, by
+//   taking +inf for its maximum.  P V stays
 //   bf16 x bf16.  Inputs that arrive rotated (the QKV projection's epilogue
 //   rotated and rounded them once) skip the rotation and the conversion:
 //   S = q K^T runs on the bf16 values as stored.
@@ -40,7 +44,8 @@
 // Hand-offs use mbarriers; the compute warps are software-pipelined so that the
 // rotation of tile i+1 runs while O(i) = P V is on the tensor core and the
 // normalisation of tile i runs while S(i+1) is.  One pass covers a tile's
-// whole key range (keys <= 128), so the softmax needs no running rescale.
+// whole key range (up to 288 keys: S in two MMAs past 256 columns), so the
+// softmax needs no running rescale.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".
 #include <math.h>
