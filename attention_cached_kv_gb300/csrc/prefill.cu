@@ -25,8 +25,8 @@
 // bf16) on mma.sync m16n8k16 with fp32 accumulation, and a running max / sum
 // softmax across key tiles.  A key chunk with a value past the f16 range is
 // written as NaN and a q value past it becomes inf, so the rows that meet one
-// end with a non-finite sum; they are recomputed in fp32 from the inputs
-// (exact.cuh).  Base angles of a group or key tile are reduced modulo 2 pi in
+// end with a non-finite sum; they, and the rows whose largest logit passes
+// kExactLogit, are recomputed in fp32 from the inputs (exact.cuh).  Base angles of a group or key tile are reduced modulo 2 pi in
 // double (rope_reduce), so every int32 position keeps its accuracy.
 //
 // Pages: [Gist page] "把 item 压成 KV：gist 能不能用在相关性任务上".

@@ -59,8 +59,9 @@ struct LongParams {
   float scale_log2;
   // The call's own inputs: a row whose softmax sum comes out non-finite (an f16
   // key chunk the staged pre-pass wrote as NaN, or a q value past the f16
-  // range) is stored as NaN and, once the CTA's stores have landed, recomputed
-  // from them in fp32 (exact.cuh).
+  // range; with f16 scores also a largest logit past kExactLogit) is stored as
+  // NaN and, once the CTA's stores have landed, recomputed from them in fp32
+  // (exact.cuh).
   ExactInputs ex;
   bf16* out;
 };
