@@ -80,6 +80,8 @@ SPECS = {
     "wide": Spec("wide", 28, 32, 8, 128, 64, 8, 1, queries=128, candidates=50,
                  pool_items=20_000, ids="uniform"),
     "paged": Spec("paged", 32, 32, 32, 128, 1, 256, 16, paged_seqs=32, paged_pool_blocks=512),
+    # the same paged decode with the wide model's GQA heads (28 layers, 32 / 8, d 128)
+    "paged_gqa": Spec("paged_gqa", 28, 32, 8, 128, 1, 256, 16, paged_seqs=32, paged_pool_blocks=512),
 }
 
 

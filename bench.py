@@ -40,6 +40,7 @@ KERNEL_OF = {
     "tiny": ("prefill_tc_kernel", ["prefill_tc.cu", "tcgen05.cuh", "common.cuh", "exact.cuh"]),
     "qgist": ("decode_short_kernel", ["decode_short.cu", "frag.cuh", "common.cuh"]),
     "paged": ("decode_long_kernel", ["decode_long.cu", "common.cuh"]),
+    "paged_gqa": ("decode_gqa_kernel", ["decode_gqa.cu", "frag.cuh", "common.cuh"]),
     "offline": ("prefill_long_kernel", ["prefill_long.cu", "tcgen05.cuh", "common.cuh", "exact.cuh"]),
 }
 
@@ -52,6 +53,8 @@ DESCR = {
             "candidates (6,400 pairs); pool 20k items",
     "paged": "paged decode: 32 layers, Hq=Hkv=32, d=128, l=1, 4096 cached tokens in 16 blocks "
              "of 256 behind permuted block tables; batch 32",
+    "paged_gqa": "paged GQA decode: 28 layers, Hq=32, Hkv=8, d=128, l=1, 4096 cached tokens in 16 "
+                 "blocks of 256 behind permuted block tables; batch 32",
     "tiny": "tiny: 1 layer, Hq=14, Hkv=2, d=64, k=8, l=64, 32 pairs, pool 16 items",
 }
 

@@ -133,7 +133,7 @@ def test_sweep_shapes(k, l):
 
 
 @pytest.mark.parametrize("name,n_sample,layer", [
-    ("gist", 160, 17), ("qgist", 600, 9), ("wide", 96, 27), ("paged", 32, 31)])
+    ("gist", 160, 17), ("qgist", 600, 9), ("wide", 96, 27), ("paged", 32, 31), ("paged_gqa", 32, 27)])
 def test_full_size_workloads_sampled(name, n_sample, layer):
     """The benchmark's workloads at full size; the oracle checks a sample."""
     wl = workloads.make(name, device=DEV)
