@@ -64,19 +64,24 @@ struct GqaParams {
   double theta[64];  // RoPE frequencies (angles reduced in double)
 };
 
-// Shared memory: the warps' rings (per stage the K tile and the V tile, 16
-// rows of 128 bytes per 64-column panel, 128-byte swizzle, and for FP8 the
-// E4M3 rows as they arrive), the q tile (GN x 8 rows per panel), the (cos, sin)
-// table, the block ids (and FP8 scales), the STATS log-sums and the
-// mbarriers.  After the chunk loop the ring holds the warps' partial results.
+// Shared memory: the warps' rings, the q tile (GN x 8 rows per panel), the
+// (cos, sin) table, the block ids (and FP8 scales), the STATS log-sums and the
+// mbarriers.  A bf16 ring stage holds a chunk's K tile and V tile (16 rows of
+// 128 bytes per 64-column panel, 128-byte swizzle) as the tensor copies write
+// them; an FP8 ring stage holds only the chunk's E4M3 rows, and each warp widens
+// the chunk it computes into one K/V tile pair of its own, so the same bytes
+// keep four chunks in flight instead of two.  After the chunk loop the ring
+// holds the warps' partial results.
 template <int D, int GN, bool FP8, bool STATS>
 struct GLayout {
   static constexpr int NP = D / 64;
-  static constexpr int S = FP8 ? 2 : 3;  // ring stages per warp
+  static constexpr int S = FP8 ? 4 : 3;  // ring stages per warp
   static constexpr uint32_t tile = kChunk * 128;
-  static constexpr uint32_t k_off = 0, v_off = NP * tile, k8_off = 2 * NP * tile;
-  static constexpr uint32_t stage = (k8_off + (FP8 ? 2 * kChunk * D : 0) + 1023) / 1024 * 1024;
-  static constexpr uint32_t ring = kWarps * S * stage;
+  static constexpr uint32_t k_off = 0, v_off = NP * tile;    // within a bf16 stage, or FP8 wide
+  static constexpr uint32_t wide = FP8 ? 2 * NP * tile : 0;  // FP8: the warp's widened pair
+  static constexpr uint32_t stage = FP8 ? 2 * kChunk * D : 2 * NP * tile;
+  static constexpr uint32_t warp_bytes = wide + S * stage;
+  static constexpr uint32_t ring = kWarps * warp_bytes;
   static constexpr uint32_t q_panel = GN * 8 * 128;
   static constexpr uint32_t q_off = ring;
   static constexpr uint32_t tab_off = q_off + NP * q_panel;
@@ -172,18 +177,19 @@ __global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_const
     for (int x = 0; x < NP; ++x)
       tma_load_2d(base + L::q_off + x * L::q_panel, &tm_q, qbar, 64 * x, p * prm.Hq + g * G);
   }
-  const uint32_t ring_w = base + warp * S * L::stage;
+  const uint32_t ring_w = base + warp * L::warp_bytes;
+  const uint32_t stages_w = ring_w + L::wide;  // stage s at + s * stage
   auto issue = [&](int c, int s) {  // chunk c into stage s of this warp (lane 0)
     const int key = c * kChunk, b = key / bl, t = key - b * bl;
     const int row_k =
         (int)((((int64_t)ids[b] * prm.pv.num_layers + prm.pv.layer) * 2 * prm.Hkv + g) * bl + t);
     const int row_v = row_k + prm.Hkv * bl;
-    const uint32_t st = ring_w + s * L::stage;
+    const uint32_t st = stages_w + s * L::stage;
     uint64_t* bar = &full[warp * S + s];
     if constexpr (FP8) {
       mbar_arrive_expect_tx(bar, 2u * kChunk * D);
-      tma_load_2d(st + L::k8_off, &tm_pool, bar, 0, row_k);
-      tma_load_2d(st + L::k8_off + kChunk * D, &tm_pool, bar, 0, row_v);
+      tma_load_2d(st, &tm_pool, bar, 0, row_k);
+      tma_load_2d(st + kChunk * D, &tm_pool, bar, 0, row_v);
     } else {
       mbar_arrive_expect_tx(bar, 2u * kChunk * D * 2);
 #pragma unroll
@@ -248,18 +254,20 @@ __global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_const
     const int c = warp + k * kWarps;
     if (c >= nchunks || __any_sync(0xffffffffu, failed)) break;
     const int s = k % S;
-    const uint32_t st = ring_w + s * L::stage;
+    const uint32_t st = stages_w + s * L::stage;
+    const uint32_t kv = FP8 ? ring_w : st;  // the chunk's K and V tiles
     if (!mbar_wait(&full[warp * S + s], (uint32_t)(k / S) & 1u)) failed = true;
     if (__any_sync(0xffffffffu, failed)) break;
     const int blk = (c * kChunk) / bl;
     if constexpr (FP8) {
-      // widen the chunk's E4M3 rows to f16 in the swizzled tiles
+      // widen the chunk's E4M3 rows to f16 in the warp's swizzled tiles (the
+      // previous chunk's reads of them are done: same warp, in order)
       constexpr int CPR = D / 8, PER = 32 / CPR;
       const int cc = lane % CPR;
       for (int row = lane / CPR; row < 2 * kChunk; row += PER) {
-        const uint2 raw = lds64(st + L::k8_off + row * D + cc * 8);
-        const int kv = row >= kChunk, r = row - kv * kChunk;
-        sts16(st + (kv ? L::v_off : L::k_off) + (cc >> 3) * L::tile + swz128(r, cc & 7),
+        const uint2 raw = lds64(st + row * D + cc * 8);
+        const int isv = row >= kChunk, r = row - isv * kChunk;
+        sts16(kv + (isv ? L::v_off : L::k_off) + (cc >> 3) * L::tile + swz128(r, cc & 7),
               make_uint4(e4m3x2_to_f16x2(raw.x & 0xffffu), e4m3x2_to_f16x2(raw.x >> 16),
                          e4m3x2_to_f16x2(raw.y & 0xffffu), e4m3x2_to_f16x2(raw.y >> 16)));
       }
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_const
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
       const int c8 = 2 * ks + (lane >> 4);
-      ldsm_x4(st + L::k_off + (c8 >> 3) * L::tile + swz128((lane & 7) + ((lane >> 3) & 1) * 8, c8 & 7), a);
+      ldsm_x4(kv + L::k_off + (c8 >> 3) * L::tile + swz128((lane & 7) + ((lane >> 3) & 1) * 8, c8 & 7), a);
 #pragma unroll
       for (int hn = 0; hn < GN; ++hn) {
         mma16816<FP8>(sc[hn], a[0], a[1], a[2], a[3], qh[hn][ks][0], qh[hn][ks][1]);
@@ -334,7 +342,7 @@ __global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_const
     for (int dq = 0; dq < D / 16; ++dq) {
       uint32_t bv[4];
       const int c8 = 2 * dq + (lane >> 4);
-      ldsm_x4_trans(st + L::v_off + (c8 >> 3) * L::tile + swz128((lane & 7) + ((lane >> 3) & 1) * 8, c8 & 7), bv);
+      ldsm_x4_trans(kv + L::v_off + (c8 >> 3) * L::tile + swz128((lane & 7) + ((lane >> 3) & 1) * 8, c8 & 7), bv);
       mma16816<FP8>(o[2 * dq], pa[0], pa[1], pa[2], pa[3], bv[0], bv[1]);
       mma16816<FP8>(o[2 * dq + 1], pa[0], pa[1], pa[2], pa[3], bv[2], bv[3]);
     }
