@@ -43,8 +43,6 @@
 namespace gattn {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
 constexpr int kChunk = 16;           // keys per chunk
 constexpr int kMaxBlocks = 512;      // cached blocks per sequence
 constexpr int kMaxStatChunks = 512;  // STATS: C / 16
@@ -71,17 +69,21 @@ struct GqaParams {
 // them; an FP8 ring stage holds only the chunk's E4M3 rows, and each warp widens
 // the chunk it computes into one K/V tile pair of its own, so the same bytes
 // keep four chunks in flight instead of two.  After the chunk loop the ring
-// holds the warps' partial results.
+// holds the warps' partial results.  With an E4M3 pool and one 8-head tile the
+// kernel runs eight warps with one or two staging stages each (the widening
+// doubles the instructions per chunk, so more warps hide it); otherwise four
+// warps, with three bf16 stages or four E4M3 ones.
 template <int D, int GN, bool FP8, bool STATS>
 struct GLayout {
   static constexpr int NP = D / 64;
-  static constexpr int S = FP8 ? 4 : 3;  // ring stages per warp
+  static constexpr int W = FP8 && GN == 1 ? 8 : 4;  // warps
+  static constexpr int S = !FP8 ? 3 : W == 8 ? (D == 128 ? 1 : 2) : 4;  // ring stages per warp
   static constexpr uint32_t tile = kChunk * 128;
   static constexpr uint32_t k_off = 0, v_off = NP * tile;    // within a bf16 stage, or FP8 wide
   static constexpr uint32_t wide = FP8 ? 2 * NP * tile : 0;  // FP8: the warp's widened pair
   static constexpr uint32_t stage = FP8 ? 2 * kChunk * D : 2 * NP * tile;
   static constexpr uint32_t warp_bytes = wide + S * stage;
-  static constexpr uint32_t ring = kWarps * warp_bytes;
+  static constexpr uint32_t ring = W * warp_bytes;
   static constexpr uint32_t q_panel = GN * 8 * 128;
   static constexpr uint32_t q_off = ring;
   static constexpr uint32_t tab_off = q_off + NP * q_panel;
@@ -89,21 +91,22 @@ struct GLayout {
   static constexpr uint32_t sc_off = ids_off + kMaxBlocks * 4;
   static constexpr uint32_t lg_off = sc_off + (FP8 ? 2 * kMaxBlocks * 4 : 0);
   static constexpr uint32_t bar_off = lg_off + (STATS ? kMaxStatChunks * 16 * 4 : 0);
-  static constexpr uint32_t bytes = bar_off + (kWarps * S + 1) * 8 + 16;
-  // the merge area inside the ring: per source (4 warps, the new token) and
+  static constexpr uint32_t bytes = bar_off + (W * S + 1) * 8 + 16;
+  // the merge area inside the ring: per source (the W warps, the new token) and
   // head slot the maximum, the sum and O
-  static constexpr uint32_t mm_off = 0, ml_off = 5 * 16 * 4, mo_off = 2 * 5 * 16 * 4;
-  static_assert(mo_off + 5 * 16 * D * 4 <= ring, "merge area");
+  static constexpr uint32_t mm_off = 0, ml_off = (W + 1) * 16 * 4, mo_off = 2 * (W + 1) * 16 * 4;
+  static_assert(mo_off + (W + 1) * 16 * D * 4 <= ring, "merge area");
 };
 
 template <int D, int GN, bool FP8, bool STATS>
-__global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_constant__ GqaParams prm,
+__global__ void __launch_bounds__(GLayout<D, GN, FP8, STATS>::W * 32, FP8 ? 2 : 0) decode_gqa_kernel(const __grid_constant__ GqaParams prm,
                                                               const __grid_constant__ CUtensorMap tm_pool,
                                                               const __grid_constant__ CUtensorMap tm_q) {
   using L = GLayout<D, GN, FP8, STATS>;
   constexpr int NP = D / 64;
   constexpr int KS = D / 16, HK = KS / 2;
   constexpr int S = L::S;
+  constexpr int kWarps = L::W, kThreads = kWarps * 32;
   constexpr float kNegInf = -INFINITY;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -271,7 +274,10 @@ __global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_const
               make_uint4(e4m3x2_to_f16x2(raw.x & 0xffffu), e4m3x2_to_f16x2(raw.x >> 16),
                          e4m3x2_to_f16x2(raw.y & 0xffffu), e4m3x2_to_f16x2(raw.y >> 16)));
       }
+      // the staged bytes are read: refill the stage now, while this chunk is computed
+      fence_proxy_async_smem();
       __syncwarp();
+      if (lane == 0 && c + S * kWarps < nchunks) issue(c + S * kWarps, s);
     }
     // S^T = K q^T: rows keys g8, g8 + 8 of the chunk; columns head slots
     float sc[GN][4];
@@ -346,10 +352,14 @@ __global__ void __launch_bounds__(kThreads) decode_gqa_kernel(const __grid_const
       mma16816<FP8>(o[2 * dq], pa[0], pa[1], pa[2], pa[3], bv[0], bv[1]);
       mma16816<FP8>(o[2 * dq + 1], pa[0], pa[1], pa[2], pa[3], bv[2], bv[3]);
     }
-    // stage s is free: its reads (and the widening's writes) come before the refill
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && c + S * kWarps < nchunks) issue(c + S * kWarps, s);
+    // (bf16) stage s is free: its reads come before the refill
+    if constexpr (!FP8) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && c + S * kWarps < nchunks) issue(c + S * kWarps, s);
+    } else {
+      __syncwarp();  // every lane is done with the widened tiles before the next widening
+    }
   }
   if (__any_sync(0xffffffffu, failed)) {
     if (lane == 0) {
@@ -463,7 +473,7 @@ int launch_d(const Problem& pb, const float* kv_scale, float* block_mass, cudaSt
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
     return GIST_ATTN_ERR_LAUNCH;
   const int64_t grid = (int64_t)pb.P * pb.Hkv;
-  kern<<<(unsigned)grid, kThreads, bytes, stream>>>(prm, tm_pool, tm_q);
+  kern<<<(unsigned)grid, L::W * 32, bytes, stream>>>(prm, tm_pool, tm_q);
   return cudaGetLastError() == cudaSuccess ? GIST_ATTN_OK : GIST_ATTN_ERR_LAUNCH;
 }
 
