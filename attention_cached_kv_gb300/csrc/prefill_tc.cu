@@ -245,7 +245,9 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 }
 
 // TMEM load of 16 columns of this thread's lane that also returns their maximum.
-__device__ __forceinline__ float ld16_max(uint32_t taddr) {
+// It does not wait: the maximum is valid after tcgen05.wait::ld, which the
+// caller issues once for several such loads (ld_red_wait).
+__device__ __forceinline__ float ld16_max_async(uint32_t taddr) {
   uint32_t r[16];
   float m;
   asm volatile(
@@ -255,8 +257,14 @@ __device__ __forceinline__ float ld16_max(uint32_t taddr) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15]), "=f"(m)
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+f"(m)::"memory");
   return m;
+}
+// Waits for this thread's TMEM loads; the maxima of the loads pass through it.
+template <int N>
+__device__ __forceinline__ void ld_red_wait(float (&m)[N]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(m[i]));
 }
 
 struct Bars {
@@ -748,12 +756,17 @@ __global__ void __launch_bounds__(threads_of(KVW), two_per_sm(D, NCH) ? 2 : 1)
         // the result is the same softmax.  Only a masked logit ~100 (log2
         // units) above every visible one could underflow the weights; the sum
         // check below sends such a row to the fp32 recomputation.
-        float mx0 = kNegInf;
+        // (the half's loads issued together, one wait for all of them)
+        float mxs[NCH];
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
           const int c = 2 * cc + h;
-          if (c * 16 < N) mx0 = fmaxf(mx0, ld16_max(tmem + lane_base + c * 16));
+          mxs[cc] = c * 16 < N ? ld16_max_async(tmem + lane_base + c * 16) : kNegInf;
         }
+        ld_red_wait(mxs);
+        float mx0 = mxs[0];
+#pragma unroll
+        for (int cc = 1; cc < NCH; ++cc) mx0 = fmaxf(mx0, mxs[cc]);
         // A row whose largest logit passes kExactLogit (q.K in f16 too coarse
         // there) takes m = +inf: every weight is 0, the sum too, and the row
         // goes to the fp32 recomputation.
