@@ -6,23 +6,25 @@
 // K_{<=t} = [K_{<t}; k_t]; [Suffix page, §5 第一步 and §6 问题四]: the context
 // lives in fixed-size blocks of a pool reached through a block table.  Every
 // query head of a group reads the same K/V rows, so each row is read once per
-// KV head: one CTA per (sequence, KV head), four warps, warp w taking the
-// 16-key chunks w, w + 4, ... of the context.
+// KV head: one CTA per (sequence, KV head) of W warps, warp w taking the
+// 16-key chunks w, w + W, ... of the context (W = 4; 8 for an E4M3 pool with
+// one 8-head tile, where the widening doubles the work per chunk).
 //
 // A chunk's K and V rows (16 rows of one block and head, contiguous in the pool)
-// arrive by tensor copies with 128-byte swizzle into a per-warp ring of three
-// stages, issued by the warp's lane 0.  Per chunk the warp forms S^T = K q^T on
+// arrive by tensor copies with 128-byte swizzle into a per-warp ring, issued by
+// the warp's lane 0.  Per chunk the warp forms S^T = K q^T on
 // mma.sync m16n8k16 with the keys as the 16 rows and the group's heads as the
 // N (one or two 8-head tiles), q rotated in fp32 and split into bf16 hi + lo;
 // keeps a running maximum and sum per head (shuffles down the key rows), moves
 // P^T into the A layout by movmatrix.trans and accumulates O = P V on the same
-// MMA.  At the end the four warps' (maximum, sum, O) and the new token's own key
+// MMA.  At the end the W warps' (maximum, sum, O) and the new token's own key
 // and value (an fp32 dot of the unrotated q and k_new: the same rotation of both
 // cancels) merge in shared memory.
 //
 // FP8 pool ([Suffix page, §2 and the end of §5], one fp32 scale per (block,
-// layer, K|V, KV head)): the E4M3 rows land in a staging area of the stage and
-// are widened to f16 (exact); q is divided by a power of two per head into the
+// layer, K|V, KV head)): a ring stage holds a chunk's E4M3 rows, which the
+// warp widens to f16 (exact) into one tile pair of its own and then refills
+// the stage at once; q is divided by a power of two per head into the
 // f16 range and split into f16 hi + lo; the K scale multiplies the fp32 logits,
 // each block's V scale over the context's largest the fp32 weights, and that
 // largest scale the merged output.
@@ -66,9 +68,9 @@ struct GqaParams {
 // (cos, sin) table, the block ids (and FP8 scales), the STATS log-sums and the
 // mbarriers.  A bf16 ring stage holds a chunk's K tile and V tile (16 rows of
 // 128 bytes per 64-column panel, 128-byte swizzle) as the tensor copies write
-// them; an FP8 ring stage holds only the chunk's E4M3 rows, and each warp widens
-// the chunk it computes into one K/V tile pair of its own, so the same bytes
-// keep four chunks in flight instead of two.  After the chunk loop the ring
+// them; an FP8 ring stage holds only the chunk's E4M3 rows (half a bf16
+// stage), and each warp widens the chunk it computes into one K/V tile pair of
+// its own.  After the chunk loop the ring
 // holds the warps' partial results.  With an E4M3 pool and one 8-head tile the
 // kernel runs eight warps with one or two staging stages each (the widening
 // doubles the instructions per chunk, so more warps hide it); otherwise four
@@ -99,9 +101,10 @@ struct GLayout {
 };
 
 template <int D, int GN, bool FP8, bool STATS>
-__global__ void __launch_bounds__(GLayout<D, GN, FP8, STATS>::W * 32, FP8 ? 2 : 0) decode_gqa_kernel(const __grid_constant__ GqaParams prm,
-                                                              const __grid_constant__ CUtensorMap tm_pool,
-                                                              const __grid_constant__ CUtensorMap tm_q) {
+__global__ void __launch_bounds__(GLayout<D, GN, FP8, STATS>::W * 32, FP8 ? 2 : 0)
+    decode_gqa_kernel(const __grid_constant__ GqaParams prm,
+                      const __grid_constant__ CUtensorMap tm_pool,
+                      const __grid_constant__ CUtensorMap tm_q) {
   using L = GLayout<D, GN, FP8, STATS>;
   constexpr int NP = D / 64;
   constexpr int KS = D / 16, HK = KS / 2;

@@ -108,6 +108,8 @@ def test_fp8_qgist_workload_sampled():
     (4, 32, 8, 128, 256, 2, False),   # GQA 4:1 over two 256-token blocks
     (3, 14, 2, 64, 32, 3, True),      # the gist model's 7:1 groups, 96 keys
     (2, 32, 2, 128, 16, 5, True),     # 16 heads per KV head
+    (3, 32, 8, 128, 16, 21, True),    # 21 chunks over eight warps: a ragged last round
+    (2, 16, 4, 64, 16, 13, False),    # d = 64, two stages per warp, 13 chunks
 ])
 def test_fp8_gqa_paged_decode(P, Hq, Hkv, d, bl, bpp, rpos):
     """E4M3 pools behind the long GQA decode (more than 32 cached keys, groups
@@ -131,6 +133,25 @@ def test_fp8_paged_workload_sampled():
     sel = np.arange(0, 32, 3)
     compare(got[torch.from_numpy(sel).to(DEV)], oracle_ref_fp8(wl, pool8, scale, layer=3, pairs=sel),
             "fp8 paged")
+
+
+def test_fp8_paged_gqa_workload_sampled():
+    """The paged GQA workload (32 sequences x 4096 cached tokens, 32 / 8 heads,
+    d = 128) from an E4M3 pool, in the launch configuration the benchmark's
+    --kv fp8 row times; the oracle checks every fourth sequence."""
+    wl = workloads.make("paged_gqa", device=DEV, num_layers=2)
+    pool8, scale = workloads.make_fp8_pool(wl)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.gist_attn_fwd_fp8kv(wl.q, wl.k_new, wl.v_new, pool8, scale, None, wl.block_table,
+                                      None, dims=dict(wl.dims, layer=1), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel = np.arange(1, 32, 4)
+    compare(got[torch.from_numpy(sel).to(DEV)], oracle_ref_fp8(wl, pool8, scale, layer=1, pairs=sel),
+            "fp8 paged gqa")
+    assert torch.isfinite(got.float()).all()
+    del wl, pool8, got
+    torch.cuda.empty_cache()
 
 
 def test_fp8_unsupported_shapes_are_refused():
