@@ -21,11 +21,15 @@ NOALLOC_SCRATCH_BYTES = 64 << 20  # GIST_ATTN_NOALLOC_SCRATCH_BYTES
 STATUS_BAD_BLOCK, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4
 FLAG_PREROTATED = 1
 FLAG_TEST_WITHHOLD = 2  # tests of the timeout path only (see the header)
+# gist_attn_route: entry points and the kernels they run (GIST_ATTN_ENTRY_* / _ROUTE_*)
+ENTRY_FWD, ENTRY_FWD_WS, ENTRY_FP8KV, ENTRY_BLOCK_MASS, ENTRY_GIST_MASK = 0, 1, 2, 3, 4
+ROUTES = {0: "none", 1: "prefill_tc", 2: "prefill_long", 3: "prefill_stream", 4: "staged",
+          5: "decode_long", 6: "decode_short", 7: "decode_gqa", 8: "decode"}
 
 EXPORTS = ("gist_attn_fwd", "gist_attn_workspace_bytes", "gist_attn_fwd_ws", "gist_attn_fwd_noalloc", "gist_attn_fwd_fp8kv", "gist_attn_fwd_block_mass", "gist_kv_append",
            "gist_attn_fwd_gist_mask", "gist_kv_store", "gist_qkv_rope", "gist_out_proj",
            "gist_attn_gather_debug", "gist_kv_bytes_per_position", "gist_kv_bytes_per_item",
-           "gist_kv_bytes_batch", "gist_attn_status_string")
+           "gist_kv_bytes_batch", "gist_attn_status_string", "gist_attn_route")
 
 
 class GistAttnError(RuntimeError):
@@ -103,6 +107,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.gist_kv_bytes_batch.argtypes = [ctypes.c_int] * 6
             lib.gist_attn_status_string.restype = ctypes.c_char_p
             lib.gist_attn_status_string.argtypes = [ctypes.c_int]
+            lib.gist_attn_route.restype = ctypes.c_int
+            lib.gist_attn_route.argtypes = [ctypes.c_int, ctypes.POINTER(Dims)]
             _lib = lib
     return _lib
 
@@ -167,6 +173,17 @@ def gist_attn_fwd(q, k_new, v_new, kv_pool, item_ids=None, block_table=None, pos
                            ctypes.byref(D), _stream(stream))
     _raise(rc)
     return out
+
+
+def route(dims: dict, entry: int = ENTRY_FWD) -> str:
+    """The kernel an entry point runs for these dimensions (a name from ROUTES),
+    asked of the library on the host; raises GistAttnError where the entry
+    point would refuse the shape."""
+    D = make_dims(dims)
+    rc = int(load_library().gist_attn_route(int(entry), ctypes.byref(D)))
+    if rc < 0:
+        _raise(rc)
+    return ROUTES[rc]
 
 
 def workspace_bytes(dims: dict) -> int:

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/gist_attn.h: argument checks on the
-// host, kernel selection, and the cache byte-count helpers.
+// host, kernel selection (one route function per entry point, also reported by
+// gist_attn_route), and the cache byte-count helpers.
 //
 // Nothing here allocates device memory or keeps state between calls; the only
 // process-wide value is the driver's tensor-map encoder, looked up once.
@@ -135,17 +136,64 @@ bool wants_stage(const Problem& pb) {
   return pb.l >= 2 && !prefill_tc_fits(pb) && !prefill_long_fits(pb) && staged_fits(pb);
 }
 
-int dispatch_fwd(const Problem& pb, cudaStream_t stream) {
+// Kernel selection, one function per entry point: the entry points launch what
+// these return, and gist_attn_route reports it.  Each returns a
+// GIST_ATTN_ROUTE_* value, or GIST_ATTN_ERR_UNSUPPORTED.
+
+// gist_attn_fwd: the decode kernels for l = 1, then the tensor-core prefill
+// (every key of a tile in one pass), the long prefill (pre-rotated, no cache),
+// and the streaming prefill for everything else.
+int route_fwd(const Problem& pb) {
   if (pb.l == 1) {
-    if (decode_long_fits(pb)) return launch_decode_long(pb, stream);
-    if (decode_short_fits(pb)) return launch_decode_short(pb, stream);
-    if (decode_gqa_fits(pb)) return launch_decode_gqa(pb, stream);
-    if (decode_fits(pb)) return launch_decode(pb, stream);
+    if (decode_long_fits(pb)) return GIST_ATTN_ROUTE_DECODE_LONG;
+    if (decode_short_fits(pb)) return GIST_ATTN_ROUTE_DECODE_SHORT;
+    if (decode_gqa_fits(pb)) return GIST_ATTN_ROUTE_DECODE_GQA;
+    if (decode_fits(pb)) return GIST_ATTN_ROUTE_DECODE;
   }
-  if (prefill_tc_fits(pb)) return launch_prefill_tc(pb, stream);
-  if (prefill_long_fits(pb)) return launch_prefill_long(pb, stream);
-  if (prefill_fits(pb)) return launch_prefill(pb, stream);
+  if (prefill_tc_fits(pb)) return GIST_ATTN_ROUTE_PREFILL_TC;
+  if (prefill_long_fits(pb)) return GIST_ATTN_ROUTE_PREFILL_LONG;
+  if (prefill_fits(pb)) return GIST_ATTN_ROUTE_PREFILL_STREAM;
   return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+// gist_attn_fwd_ws with a large enough workspace: the staged path where it
+// applies, else as gist_attn_fwd.
+int route_fwd_ws(const Problem& pb) {
+  return wants_stage(pb) ? GIST_ATTN_ROUTE_STAGED : route_fwd(pb);
+}
+
+// gist_attn_fwd_fp8kv: the kernels with an E4M3 variant.
+int route_fp8(const Problem& pb) {
+  if (prefill_tc_fits(pb)) return GIST_ATTN_ROUTE_PREFILL_TC;
+  if (pb.C > 0 && decode_long_fits(pb)) return GIST_ATTN_ROUTE_DECODE_LONG;
+  if (decode_short_fits(pb)) return GIST_ATTN_ROUTE_DECODE_SHORT;
+  if (decode_gqa_fits(pb)) return GIST_ATTN_ROUTE_DECODE_GQA;
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+// gist_attn_fwd_block_mass: the decode kernels with a STATS variant.
+int route_block_mass(const Problem& pb) {
+  if (pb.C > 0 && decode_long_stats_fits(pb)) return GIST_ATTN_ROUTE_DECODE_LONG;
+  if (pb.C > 0 && decode_gqa_stats_fits(pb)) return GIST_ATTN_ROUTE_DECODE_GQA;
+  return GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+// gist_attn_fwd_gist_mask: the streaming prefill, the one kernel with the mask.
+int route_gist_mask(const Problem& pb) {
+  return prefill_fits(pb) ? GIST_ATTN_ROUTE_PREFILL_STREAM : GIST_ATTN_ERR_UNSUPPORTED;
+}
+
+int dispatch_fwd(const Problem& pb, cudaStream_t stream) {
+  switch (route_fwd(pb)) {
+    case GIST_ATTN_ROUTE_DECODE_LONG: return launch_decode_long(pb, stream);
+    case GIST_ATTN_ROUTE_DECODE_SHORT: return launch_decode_short(pb, stream);
+    case GIST_ATTN_ROUTE_DECODE_GQA: return launch_decode_gqa(pb, stream);
+    case GIST_ATTN_ROUTE_DECODE: return launch_decode(pb, stream);
+    case GIST_ATTN_ROUTE_PREFILL_TC: return launch_prefill_tc(pb, stream);
+    case GIST_ATTN_ROUTE_PREFILL_LONG: return launch_prefill_long(pb, stream);
+    case GIST_ATTN_ROUTE_PREFILL_STREAM: return launch_prefill(pb, stream);
+    default: return GIST_ATTN_ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace
@@ -178,7 +226,8 @@ extern "C" int gist_attn_fwd_ws(const void* q, const void* k_new, const void* v_
   const int rc = gattn::prepare_fwd(q, k_new, v_new, kv_pool, item_ids, block_table, pos_offset, out,
                                     dims, &pb);
   if (rc != GIST_ATTN_OK || pb.P == 0) return rc;
-  if (workspace && gattn::aligned(workspace, 256) && gattn::wants_stage(pb) &&
+  if (workspace && gattn::aligned(workspace, 256) &&
+      gattn::route_fwd_ws(pb) == GIST_ATTN_ROUTE_STAGED &&
       workspace_bytes >= gattn::stage_layout(pb).bytes)
     return gattn::launch_staged(pb, workspace, stream);
   return gattn::dispatch_fwd(pb, stream);
@@ -209,11 +258,13 @@ extern "C" int gist_attn_fwd_fp8kv(const void* q, const void* k_new, const void*
   pb.block_table = block_table;
   pb.pos_offset = pos_offset;
   pb.out = out;
-  if (gattn::prefill_tc_fits(pb)) return gattn::launch_prefill_tc_fp8(pb, kv_scale, stream);
-  if (pb.C > 0 && gattn::decode_long_fits(pb)) return gattn::launch_decode_long_fp8(pb, kv_scale, stream);
-  if (gattn::decode_short_fits(pb)) return gattn::launch_decode_short_fp8(pb, kv_scale, stream);
-  if (gattn::decode_gqa_fits(pb)) return gattn::launch_decode_gqa_fp8(pb, kv_scale, stream);
-  return GIST_ATTN_ERR_UNSUPPORTED;
+  switch (gattn::route_fp8(pb)) {
+    case GIST_ATTN_ROUTE_PREFILL_TC: return gattn::launch_prefill_tc_fp8(pb, kv_scale, stream);
+    case GIST_ATTN_ROUTE_DECODE_LONG: return gattn::launch_decode_long_fp8(pb, kv_scale, stream);
+    case GIST_ATTN_ROUTE_DECODE_SHORT: return gattn::launch_decode_short_fp8(pb, kv_scale, stream);
+    case GIST_ATTN_ROUTE_DECODE_GQA: return gattn::launch_decode_gqa_fp8(pb, kv_scale, stream);
+    default: return GIST_ATTN_ERR_UNSUPPORTED;
+  }
 }
 
 extern "C" int gist_attn_fwd_block_mass(const void* q, const void* k_new, const void* v_new,
@@ -239,11 +290,11 @@ extern "C" int gist_attn_fwd_block_mass(const void* q, const void* k_new, const 
   pb.block_table = block_table;
   pb.pos_offset = pos_offset;
   pb.out = out;
-  if (pb.C > 0 && gattn::decode_long_stats_fits(pb))
-    return gattn::launch_decode_long_stats(pb, block_mass, stream);
-  if (pb.C > 0 && gattn::decode_gqa_stats_fits(pb))
-    return gattn::launch_decode_gqa_stats(pb, block_mass, stream);
-  return GIST_ATTN_ERR_UNSUPPORTED;
+  switch (gattn::route_block_mass(pb)) {
+    case GIST_ATTN_ROUTE_DECODE_LONG: return gattn::launch_decode_long_stats(pb, block_mass, stream);
+    case GIST_ATTN_ROUTE_DECODE_GQA: return gattn::launch_decode_gqa_stats(pb, block_mass, stream);
+    default: return GIST_ATTN_ERR_UNSUPPORTED;
+  }
 }
 
 extern "C" int gist_kv_append(const void* k_new, const void* v_new, void* kv_pool,
@@ -295,7 +346,7 @@ extern "C" int gist_attn_fwd_gist_mask(const void* q, const void* k_new, const v
   pb.gist_start = gist_start;
   pb.gist_len = gist_len;
   if (pb.C == 0) pb.blocks_per_pair = 0;
-  if (!gattn::prefill_fits(pb)) return GIST_ATTN_ERR_UNSUPPORTED;
+  if (gattn::route_gist_mask(pb) != GIST_ATTN_ROUTE_PREFILL_STREAM) return GIST_ATTN_ERR_UNSUPPORTED;
   return gattn::launch_prefill(pb, stream);
 }
 
@@ -382,6 +433,25 @@ extern "C" size_t gist_kv_bytes_per_item(int L, int Hkv, int d, int k, int elem_
 extern "C" size_t gist_kv_bytes_batch(int B, int L, int T, int Hkv, int d, int elem_bytes) {
   if (B < 0 || T < 0) return 0;
   return (size_t)B * T * gist_kv_bytes_per_position(L, Hkv, d, elem_bytes);
+}
+
+extern "C" int gist_attn_route(int entry, const gist_attn_dims* dims) {
+  Problem pb{};
+  const int rc = gattn::check_dims(dims, &pb);
+  if (rc != GIST_ATTN_OK) return rc;
+  if (pb.P == 0) return GIST_ATTN_ROUTE_NONE;
+  switch (entry) {
+    case GIST_ATTN_ENTRY_FWD:
+    case GIST_ATTN_ENTRY_FWD_WS:
+      if (pb.C == 0) pb.blocks_per_pair = 0;  // as prepare_fwd leaves it
+      return entry == GIST_ATTN_ENTRY_FWD ? gattn::route_fwd(pb) : gattn::route_fwd_ws(pb);
+    case GIST_ATTN_ENTRY_FP8KV: return gattn::route_fp8(pb);
+    case GIST_ATTN_ENTRY_BLOCK_MASS: return gattn::route_block_mass(pb);
+    case GIST_ATTN_ENTRY_GIST_MASK:
+      if (pb.C == 0) pb.blocks_per_pair = 0;
+      return gattn::route_gist_mask(pb);
+    default: return GIST_ATTN_ERR_UNSUPPORTED;
+  }
 }
 
 extern "C" const char* gist_attn_status_string(int status) {

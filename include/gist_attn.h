@@ -364,6 +364,41 @@ size_t gist_kv_bytes_batch(int B, int L, int T, int Hkv, int d, int elem_bytes);
  */
 const char* gist_attn_status_string(int status);
 
+/*
+ * gist_attn_route -- which kernel an entry point runs for these dimensions, as
+ * a host-only query: nothing is read from device memory and nothing is
+ * launched.  The answer comes from the same function the entry point's own
+ * dispatch uses, so a caller (or a test) can see which path a shape takes
+ * before it provides any buffer.  The pages define no such call; it exposes
+ * how this library splits the attention of [Gist page, "在线的一次 attention"]
+ * and the decode step of [KV page, "Reusable-state"] across its kernels.
+ *   entry  one of GIST_ATTN_ENTRY_*; GIST_ATTN_ENTRY_FWD_WS answers for
+ *          gist_attn_fwd_ws (and gist_attn_fwd_noalloc) given a workspace of
+ *          at least gist_attn_workspace_bytes(dims) bytes
+ *   dims   as for that entry point (the gist-mask entry with gist_len 0)
+ * Returns one of GIST_ATTN_ROUTE_* (>= 0; GIST_ATTN_ROUTE_NONE when num_pairs
+ * is 0), the GIST_ATTN_ERR_* code the entry point's dimension checks return,
+ * or GIST_ATTN_ERR_UNSUPPORTED when no kernel takes the shape (or `entry` is
+ * not one of the values below).
+ */
+#define GIST_ATTN_ENTRY_FWD 0        /* gist_attn_fwd                               */
+#define GIST_ATTN_ENTRY_FWD_WS 1     /* gist_attn_fwd_ws / _noalloc with workspace  */
+#define GIST_ATTN_ENTRY_FP8KV 2      /* gist_attn_fwd_fp8kv                         */
+#define GIST_ATTN_ENTRY_BLOCK_MASS 3 /* gist_attn_fwd_block_mass                    */
+#define GIST_ATTN_ENTRY_GIST_MASK 4  /* gist_attn_fwd_gist_mask                     */
+
+#define GIST_ATTN_ROUTE_NONE 0           /* nothing to launch (num_pairs == 0)          */
+#define GIST_ATTN_ROUTE_PREFILL_TC 1     /* tcgen05 prefill, a tile's keys in one pass  */
+#define GIST_ATTN_ROUTE_PREFILL_LONG 2   /* tcgen05 prefill over 128-key blocks         */
+#define GIST_ATTN_ROUTE_PREFILL_STREAM 3 /* streaming mma.sync prefill, any length      */
+#define GIST_ATTN_ROUTE_STAGED 4         /* staging pre-pass, then the 128-key blocks   */
+#define GIST_ATTN_ROUTE_DECODE_LONG 5    /* l = 1, one head per KV head, long cache     */
+#define GIST_ATTN_ROUTE_DECODE_SHORT 6   /* l = 1, cache of at most 32 keys             */
+#define GIST_ATTN_ROUTE_DECODE_GQA 7     /* l = 1, 2..16 heads per KV head, longer cache */
+#define GIST_ATTN_ROUTE_DECODE 8         /* l = 1, the other shapes (CUDA cores)        */
+
+int gist_attn_route(int entry, const gist_attn_dims* dims);
+
 #ifdef __cplusplus
 }
 #endif
