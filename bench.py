@@ -11,6 +11,14 @@ workload), so each launch streams from DRAM.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gist]
   python bench.py --impl reference ...   # the fp64 oracle on the host cores
 
+Other rows: --workload {tiny,gist,qgist,wide,paged,paged_gqa}; --kv fp8 (the
+same workload from an E4M3 pool, the roofline counting fp8 bytes); --fused
+(QKV projection with RoPE, attention on its pre-rotated output, output
+projection); --row offline | block-mass | sweep [--sweep-point K:L] (the
+offline gist pass, the decode step with per-block attention mass and the
+append, the k x l sweep).  --queries / --pool-items / --layers shrink a
+workload for profiling captures; --no-e2e / --no-cpu-baseline skip those legs.
+
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload on its own GPU (weak scaling, no collective on the data path); the
 reported time is the maximum over ranks.
