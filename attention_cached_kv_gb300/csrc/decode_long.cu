@@ -216,8 +216,9 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
 #pragma unroll
   for (int e = 0; e < VE; ++e) o[e] = 0.f;
 
-  // one key per 8-lane group: logit s (all 8 lanes), then the warp's online update
-  auto consume = [&](float s_key, bool valid, const uint8_t* vrows, float vsc) {
+  // bf16 pool: one key per 8-lane group: logit s (all 8 lanes), then the warp's
+  // online update
+  auto consume = [&](float s_key, bool valid, const uint8_t* vrows) {
     float sv = valid ? s_key : kNegInf;
     float cm = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, 8));
     cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
@@ -233,33 +234,15 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
     for (int e = 0; e < VE; ++e) o[e] *= al;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float pj = __shfl_sync(0xffffffffu, pk, j * 8) * vsc;
-      if constexpr (FP8) {
-        const uint8_t* vr = vrows + j * kRow + lane * VE;
-        const __half ph = __float2half_rn(pj);
-        const uint32_t p16 = *reinterpret_cast<const unsigned short*>(&ph);
-        if constexpr (VE == 4) {
-          const uint32_t raw = *reinterpret_cast<const uint32_t*>(vr);
-          const uint32_t a = e4m3x2_to_f16x2(raw & 0xffffu), b2 = e4m3x2_to_f16x2(raw >> 16);
-          o[0] = fma_f16f32(p16, a, o[0]);
-          o[1] = fma_f16f32(p16, a >> 16, o[1]);
-          o[2] = fma_f16f32(p16, b2, o[2]);
-          o[3] = fma_f16f32(p16, b2 >> 16, o[3]);
-        } else {
-          const uint32_t a = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(vr));
-          o[0] = fma_f16f32(p16, a, o[0]);
-          o[1] = fma_f16f32(p16, a >> 16, o[1]);
-        }
+      const float pj = __shfl_sync(0xffffffffu, pk, j * 8);
+      const uint8_t* vr = vrows + j * kRow + lane * VE * 2;
+      if constexpr (VE == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(vr);
+        const float2 a = bf16x2_to_float2(raw.x), b2 = bf16x2_to_float2(raw.y);
+        o[0] += pj * a.x; o[1] += pj * a.y; o[2] += pj * b2.x; o[3] += pj * b2.y;
       } else {
-        const uint8_t* vr = vrows + j * kRow + lane * VE * 2;
-        if constexpr (VE == 4) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(vr);
-          const float2 a = bf16x2_to_float2(raw.x), b2 = bf16x2_to_float2(raw.y);
-          o[0] += pj * a.x; o[1] += pj * a.y; o[2] += pj * b2.x; o[3] += pj * b2.y;
-        } else {
-          const float2 a = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(vr));
-          o[0] += pj * a.x; o[1] += pj * a.y;
-        }
+        const float2 a = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(vr));
+        o[0] += pj * a.x; o[1] += pj * a.y;
       }
     }
   };
@@ -373,48 +356,22 @@ __global__ void __launch_bounds__(kThreads, STATS ? 6 : 7)
       }
       const uint8_t* stage = ring + s * kStageBytes;
       float acc = 0.f;
-      if constexpr (FP8) {
-        const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE;
-        uint32_t w[QE / 4];
-        if constexpr (QE == 16) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(krow);
-          w[0] = raw.x; w[1] = raw.y; w[2] = raw.z; w[3] = raw.w;
-        } else {
-          const uint2 raw = *reinterpret_cast<const uint2*>(krow);
-          w[0] = raw.x; w[1] = raw.y;
-        }
-  #pragma unroll
-        for (int e = 0; e < QE / 4; ++e) {
-          const uint32_t k0 = e4m3x2_to_f16x2(w[e] & 0xffffu), k1 = e4m3x2_to_f16x2(w[e] >> 16);
-          acc = fma_f16f32(qh[4 * e], k0, acc);
-          acc = fma_f16f32(qh[4 * e + 1], k0 >> 16, acc);
-          acc = fma_f16f32(qh[4 * e + 2], k1, acc);
-          acc = fma_f16f32(qh[4 * e + 3], k1 >> 16, acc);
-        }
-      } else {
-        const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE * 2;
-  #pragma unroll
-        for (int v = 0; v < QE / 8; ++v) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(krow + v * 16);
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 kf = bf16x2_to_float2(w[e]);
-            acc = fmaf(qr[v * 8 + 2 * e], kf.x, acc);
-            acc = fmaf(qr[v * 8 + 2 * e + 1], kf.y, acc);
-          }
+      const uint8_t* krow = stage + (warp * 4 + kg) * kRow + sl * QE * 2;
+#pragma unroll
+      for (int v = 0; v < QE / 8; ++v) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(krow + v * 16);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 kf = bf16x2_to_float2(w[e]);
+          acc = fmaf(qr[v * 8 + 2 * e], kf.x, acc);
+          acc = fmaf(qr[v * 8 + 2 * e + 1], kf.y, acc);
         }
       }
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      float vsc = 1.f;
-      if constexpr (FP8) {
-        const int b = (ci * kChunk) / bl;
-        acc *= kscale[b];
-        vsc = vscale[b];
-      }
-      consume(acc, true, stage + kChunk * kRow + warp * 4 * kRow, vsc);
+      consume(acc, true, stage + kChunk * kRow + warp * 4 * kRow);
       if constexpr (STATS) {
         if (lane == 0) chunk_lg[ci][warp] = last_share;
       }
