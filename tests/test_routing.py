@@ -132,3 +132,20 @@ def test_workspace_is_asked_for_exactly_where_the_staged_path_runs():
                workloads.dims_of(workloads.sweep_spec(32, 256)), dims(4, 256, 32, 8, 128, 8, 1, 4)):
         staged = binding.route(dm, WS) == "staged"
         assert (binding.workspace_bytes(dm) > 0) == staged
+
+
+def test_gpu_parity_shapes_reach_every_single_launch_kernel():
+    """The GPU parity tests' edge shapes, short-cache decodes and GQA decodes,
+    routed on the host: between them they run every kernel gist_attn_fwd can
+    launch (the long prefill and the staged path have test files of their
+    own), so a change of the selection rules cannot leave a kernel untested."""
+    import test_parity_gpu as par
+
+    def d(P, l, Hq, Hkv, hd, bl, bpp, nb):
+        return dict(dims(P, l, Hq, Hkv, hd, bl, bpp, nb), num_layers=2, layer=1)
+
+    seen = {binding.route(d(*s)) for s in par.EDGE}
+    seen |= {binding.route(d(P, 1, Hq, Hkv, hd, bl, bpp, 9)) for P, Hq, Hkv, hd, bl, bpp in par.SHORT}
+    seen |= {binding.route(d(P, 1, Hq, Hkv, hd, bl, bpp, 9)) for P, Hq, Hkv, hd, bl, bpp in par.GQA}
+    assert seen >= {"prefill_tc", "prefill_stream", "decode_long", "decode_short", "decode_gqa",
+                    "decode"}, seen
