@@ -22,6 +22,10 @@ workload for profiling captures; --no-e2e / --no-cpu-baseline skip those legs.
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload on its own GPU (weak scaling, no collective on the data path); the
 reported time is the maximum over ranks.
+
+The plain default single-GPU run (no profiling options) also times the other
+workloads and the E4M3 pools after the headline measurement, a few steps
+each, and reports them under "rows" in the same JSON line.
 """
 from __future__ import annotations
 
@@ -92,7 +96,17 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--no-extra-rows", action="store_true",
+                    help="skip the other workloads' rows of the default single-GPU run")
     return ap.parse_args(argv)
+
+
+# The default single-GPU run also times these (workload, KV element type) rows
+# after the headline one, a few steps each, and reports them under "rows".
+EXTRA_ROWS = [("wide", "bf16"), ("qgist", "bf16"), ("paged", "bf16"), ("paged_gqa", "bf16"),
+              ("gist", "fp8"), ("wide", "fp8"), ("qgist", "fp8"), ("paged", "fp8"),
+              ("paged_gqa", "fp8")]
+EXTRA_ROWS_SECONDS = 60.0  # no further row starts after this much wall time
 
 
 # ----------------------------------------------------------------- helpers ---
@@ -852,6 +866,55 @@ def run_row(args) -> dict:
             "gpu_launches": 2 * L * args.steps, "impl": "ours"}
 
 
+def wants_extra_rows(args, ws: int) -> bool:
+    """Only the plain default run adds the other rows: one GPU, the headline
+    workload, none of the options the profiling commands use."""
+    return (args.impl == "ours" and ws == 1 and not args.no_extra_rows and not args.row
+            and args.workload == "gist" and args.kv == "bf16" and not args.fused
+            and not (args.no_e2e or args.no_cpu_baseline or args.queries or args.pool_items
+                     or args.layers))
+
+
+def run_extra_rows(args, run=None) -> list:
+    """Each row of EXTRA_ROWS through the same measurement as the headline
+    (fewer steps, no e2e or CPU leg); a row that fails is reported with its
+    error instead of its numbers, and the headline line is still printed."""
+    run = run or run_ours
+    rows, t0 = [], time.time()
+    for name, kv in EXTRA_ROWS:
+        if time.time() - t0 > EXTRA_ROWS_SECONDS:
+            rows.append({"workload": name, "kv": kv, "skipped": "time budget of the extra rows"})
+            continue
+        sub = argparse.Namespace(**vars(args))
+        sub.workload, sub.kv, sub.fused = name, kv, False
+        sub.steps, sub.warmup = max(1, min(args.steps, 10)), max(3, min(args.warmup, 5))
+        sub.no_e2e = sub.no_cpu_baseline = True
+        sub.queries = sub.pool_items = sub.layers = 0
+        try:
+            r = run(sub)
+            roof = r["roofline"]
+            rows.append({"workload": name, "kv": kv, "config": r["config"]["workload"],
+                         "value": r["value"], "unit": r["unit"], "steps": sub.steps,
+                         "warmup": sub.warmup, "ms_per_step": r["ms_per_step"],
+                         "kernel": roof["kernel"], "avg_launch_ms": roof["avg_launch_ms"],
+                         "achieved_gbs": roof["achieved"], "frac": roof["frac"],
+                         "algorithmic_bytes_per_launch": roof["algorithmic_bytes_per_launch"],
+                         "traffic": roof["traffic"], "gpu_launches": r["gpu_launches"],
+                         "clocks": r["clocks"]})
+        except Exception as e:  # keep the headline line: report the row's failure
+            rows.append({"workload": name, "kv": kv, "error": f"{type(e).__name__}: {e}"[:300]})
+        finally:
+            try:
+                import gc
+
+                import torch
+                gc.collect()
+                torch.cuda.empty_cache()
+            except Exception:
+                pass
+    return rows
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.row and args.impl == "ours":
@@ -859,6 +922,8 @@ def main(argv=None):
     else:
         res = run_reference(args) if args.impl == "reference" else run_ours(args)
     ws, rank, _ = dist_env()
+    if res is not None and wants_extra_rows(args, ws):
+        res["rows"] = run_extra_rows(args)
     if res is not None and rank == 0:
         line = json.dumps(res)
         print(line, flush=True)
